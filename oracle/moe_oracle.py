@@ -1,0 +1,343 @@
+"""Plain CPU oracle for the single-GPU MoE layer forward.
+
+TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import or run this module; the library never does.  It
+shares no code with the CUDA path: it is the method's definition written out
+in float64 numpy, step by step, in the order and notation of the pages.
+
+Sources (page title, section):
+  [FFN]  "MoE 与专家并行" (hs-black.github.io/posts/scaling-moe), 从稠密 FFN 到 MoE:
+         SwiGLU FFN(u) = W_down (SiLU(W_gate u) ⊙ W_up u);
+         layer output h'_t = u_t + sum_i g_{i,t} FFN_i(u_t), g = 0 off the top-k.
+  [RTR]  same page, 路由器：打分、top-k、加权求和: H = U W_r; score s = softmax or
+         sigmoid of H; top-k set T_t; gates from the selected scores; the
+         noisy top-k logits H_i = (x W_g)_i + N(0,1) * Softplus((x W_noise)_i);
+         the single-GPU shapes listing (permute by expert, grouped FFN,
+         index_add back into token order).
+  [SCR]  same page, softmax 门控还是 sigmoid 门控: the scoring table (softmax
+         then top-k without renormalisation; softmax then renormalise over the
+         selected; top-k then softmax; sigmoid then renormalise) and the
+         identity top-k-then-softmax == softmax-then-renormalise.
+  [CAP]  same page, 专家容量与丢 token: C = ceil(CF * T * k / E); slots are
+         filled in token order, overflow is dropped and takes the residual
+         only; for top-k every token's first choice is placed before any
+         second choice.
+  [AUX]  same page, 负载均衡辅助损失：推导与梯度: f_i = fraction of assignments to
+         expert i, P_i = (1/T) sum_t s_{i,t}, L_aux = alpha * E * sum_i f_i P_i
+         (this oracle reports E * sum f_i P_i, i.e. alpha = 1); for sigmoid
+         scores P_i uses s'_{i,t} = s_{i,t} / sum_j s_{j,t}.
+  [VIO]  same page, 无辅助损失的负载均衡: MaxVio = (max_i Load_i - mean) / mean.
+
+Readings where the pages are silent (the same readings the library follows):
+  * selection is made on the float32 logits (softmax and sigmoid are strictly
+    increasing, so this is the top-k of the scores without exp-rounding ties);
+    ties go to the lower expert id, both for membership and for rank order;
+  * the logits are rounded to float32 before selection and scoring (the
+    library's logits are float32);
+  * "no capacity limit" means C = T (an expert can receive each token once);
+  * f_i counts the router's assignments before drops and is normalised by T*k;
+  * a dropped assignment contributes nothing and the kept gates are not
+    renormalised; rows inside an expert segment are in slot (priority) order.
+
+Every function here is pinned by the `-m "not gpu"` tests (worked examples of
+the pages, closed forms, invariants, brute force and textbook special cases).
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+
+SOFTMAX = 0
+SIGMOID = 1
+CHOICE_MAJOR = 0
+TOKEN_MAJOR = 1
+
+
+def f64(a) -> np.ndarray:
+    """Exact float64 copy of a numpy array or (CPU/GPU) torch tensor of any float type."""
+    if hasattr(a, "detach"):
+        import torch
+        a = a.detach().to("cpu")
+        if a.dtype in (torch.bfloat16, torch.float16):
+            a = a.to(torch.float32)
+        a = a.numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Router  [RTR]
+# --------------------------------------------------------------------------
+
+def softplus(x: np.ndarray) -> np.ndarray:
+    """Softplus(x) = ln(1 + e^x), written in the overflow-free form."""
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def router_logits(U, W_r, b_r=None, W_noise=None, eps=None) -> np.ndarray:
+    """Router logits H = U W_r (+ per-expert bias) (+ noisy-top-k noise), float64.
+
+    [RTR]: H = U W_r with W_r in R^{h x E}; the noisy router adds
+    N(0,1) * Softplus(U W_noise), with the standard-normal draws eps [T, E]
+    passed in.  The bias b_r [E] is an additive per-expert logit offset.
+    """
+    U = f64(U)
+    H = U @ f64(W_r)
+    if b_r is not None:
+        H = H + f64(b_r)[None, :]
+    if W_noise is not None:
+        H = H + f64(eps) * softplus(U @ f64(W_noise))
+    return H
+
+
+def round_f32(H: np.ndarray) -> np.ndarray:
+    """Round to float32 (returned as float64 holding float32 values)."""
+    return np.asarray(H, dtype=np.float32).astype(np.float64)
+
+
+def topk_select(H32: np.ndarray, k: int) -> np.ndarray:
+    """Top-k expert ids per token, highest first, ties to the lower expert id.
+
+    [RTR] step 2 (select the k highest); the stable sort keeps equal values in
+    increasing expert order.
+    """
+    order = np.argsort(-np.asarray(H32, dtype=np.float64), axis=1, kind="stable")
+    return order[:, :k].astype(np.int32)
+
+
+def scores(H: np.ndarray, score_fn: int) -> np.ndarray:
+    """Affinities s_{i,t}: softmax over the E experts or independent sigmoids.  [RTR] step 1, [SCR]."""
+    H = np.asarray(H, dtype=np.float64)
+    if score_fn == SOFTMAX:
+        z = np.exp(H - H.max(axis=1, keepdims=True))
+        return z / z.sum(axis=1, keepdims=True)
+    if score_fn == SIGMOID:
+        return 1.0 / (1.0 + np.exp(-H))
+    raise ValueError("score_fn")
+
+
+def gates(s: np.ndarray, idx: np.ndarray, renorm: bool) -> np.ndarray:
+    """Gate values of the selected experts, [T, k].
+
+    [SCR]: g_i = s_i / sum_{j in T_t} s_j when renormalised, g_i = s_i otherwise.
+    """
+    sel = np.take_along_axis(s, np.asarray(idx, dtype=np.int64), axis=1)
+    if renorm:
+        return sel / sel.sum(axis=1, keepdims=True)
+    return sel
+
+
+# --------------------------------------------------------------------------
+# Capacity and dispatch  [CAP]
+# --------------------------------------------------------------------------
+
+def capacity(T: int, E: int, k: int, capacity_factor: float, override: int = 0) -> int:
+    """C = ceil(CF * T * k / E), exact on the float32 value of CF; CF <= 0: C = T."""
+    if override > 0:
+        return int(override)
+    if capacity_factor <= 0:
+        return int(T)
+    cf = Fraction(float(np.float32(capacity_factor)))
+    return int(math.ceil(cf * T * k / E))
+
+
+def priority_order(T: int, k: int, priority: int):
+    """The (token, choice) pairs in the order their slots are filled.
+
+    [CAP]: every token's first choice before any second choice (choice-major,
+    tokens in order within a choice); token-major takes a token's choices
+    together.
+    """
+    if priority == CHOICE_MAJOR:
+        j, t = np.meshgrid(np.arange(k), np.arange(T), indexing="ij")
+    elif priority == TOKEN_MAJOR:
+        t, j = np.meshgrid(np.arange(T), np.arange(k), indexing="ij")
+    else:
+        raise ValueError("priority")
+    return t.reshape(-1), j.reshape(-1)
+
+
+def dispatch(idx: np.ndarray, E: int, C: int, priority: int = CHOICE_MAJOR) -> dict:
+    """Capacity-limited assignment of (token, choice) pairs to expert slots.
+
+    [CAP] + the permute of [RTR]'s shapes listing: walking the pairs in
+    priority order, the n-th pair that chose expert e takes slot n of e; it is
+    kept iff n < C.  Kept rows are packed expert by expert (offsets = the
+    exclusive prefix sum of the kept counts) in slot order, so the row of a
+    kept pair is offsets[e] + slot and row_token[row] is its token.
+    Returns counts_routed [E], counts_kept [E], offsets [E+1], slot [T*k]
+    (slot of pair t*k+j), slot_row [T*k] (-1 when dropped), row_token [A],
+    n_dropped.
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    T, k = idx.shape
+    t_seq, j_seq = priority_order(T, k, priority)
+    e_seq = idx[t_seq, j_seq]
+    counts_routed = np.bincount(e_seq, minlength=E).astype(np.int64)
+    # rank of each pair among the earlier pairs of the same expert (stable sort keeps priority order)
+    grouped = np.argsort(e_seq, kind="stable")
+    first = np.concatenate([[0], np.cumsum(counts_routed)[:-1]])
+    rank = np.empty(T * k, dtype=np.int64)
+    rank[grouped] = np.arange(T * k) - first[e_seq[grouped]]
+    counts_kept = np.minimum(counts_routed, C)
+    offsets = np.concatenate([[0], np.cumsum(counts_kept)]).astype(np.int64)
+    pair = t_seq * k + j_seq
+    slot = np.empty(T * k, dtype=np.int64)
+    slot[pair] = rank
+    kept = rank < C
+    slot_row = np.full(T * k, -1, dtype=np.int64)
+    slot_row[pair[kept]] = offsets[e_seq[kept]] + rank[kept]
+    A = int(offsets[E])
+    row_token = np.full(A, -1, dtype=np.int64)
+    row_token[slot_row[pair[kept]]] = t_seq[kept]
+    return dict(counts_routed=counts_routed, counts_kept=counts_kept, offsets=offsets,
+                slot=slot, slot_row=slot_row, row_token=row_token,
+                n_dropped=int(T * k - A), C=int(C))
+
+
+def permute(U, row_token: np.ndarray) -> np.ndarray:
+    """X = U[row_token]: the expert inputs, contiguous per expert.  [RTR] shapes listing."""
+    return f64(U)[np.asarray(row_token, dtype=np.int64)]
+
+
+# --------------------------------------------------------------------------
+# Experts and combine  [FFN]
+# --------------------------------------------------------------------------
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """SiLU(x) = x * sigmoid(x)."""
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def swiglu(x, W_gate_e, W_up_e, W_down_e):
+    """One expert on rows x [n, h]: returns (FFN(x) [n, h], the SiLU(gate)*up activation [n, d_e]).
+
+    [FFN]: FFN(u) = W_down (SiLU(W_gate u) ⊙ W_up u), W_gate, W_up in R^{d_e x h},
+    W_down in R^{h x d_e}.
+    """
+    x = f64(x)
+    a = silu(x @ f64(W_gate_e).T) * (x @ f64(W_up_e).T)
+    return a @ f64(W_down_e).T, a
+
+
+def expert_ffn(X, offsets, W_gate, W_up, W_down, d_e: int):
+    """Y = the grouped FFN over the expert segments of X (rows offsets[e]..offsets[e+1]).
+
+    [RTR] shapes listing (grouped_ffn) with [FFN]'s expert.
+    """
+    X = f64(X)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E = len(offsets) - 1
+    Y = np.zeros((X.shape[0], X.shape[1]))
+    act = np.zeros((X.shape[0], d_e))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            Y[lo:hi], act[lo:hi] = swiglu(X[lo:hi], W_gate[e], W_up[e], W_down[e])
+    return Y, act
+
+
+def combine(U, Y, slot_row, gate, k: int) -> np.ndarray:
+    """out_t = u_t + sum_j g_{j,t} Y[row of (t, j)], kept pairs only, j ascending.
+
+    [FFN] layer output with [RTR]'s index_add back into token order; a dropped
+    pair adds nothing (its token keeps the residual only, [CAP]).
+    """
+    out = f64(U).copy()
+    T = out.shape[0]
+    sr = np.asarray(slot_row, dtype=np.int64).reshape(T, k)
+    g = f64(gate).reshape(T, k)
+    Y = f64(Y)
+    for j in range(k):
+        m = sr[:, j] >= 0
+        out[m] += g[m, j][:, None] * Y[sr[m, j]]
+    return out
+
+
+# --------------------------------------------------------------------------
+# Load statistics  [AUX], [VIO]
+# --------------------------------------------------------------------------
+
+def load_stats(counts_routed, s: np.ndarray, T: int, k: int, score_fn: int) -> dict:
+    """f_i, P_i, E * sum_i f_i P_i and MaxVio.  [AUX], [VIO]."""
+    counts_routed = np.asarray(counts_routed, dtype=np.float64)
+    E = counts_routed.shape[0]
+    f = counts_routed / (T * k)
+    sp = s / s.sum(axis=1, keepdims=True) if score_fn == SIGMOID else s
+    P = sp.sum(axis=0) / T
+    aux = E * float((f * P).sum())
+    mean = counts_routed.mean()
+    maxvio = float((counts_routed.max() - mean) / mean) if mean > 0 else 0.0
+    return dict(f=f, P=P, aux=aux, maxvio=maxvio)
+
+
+# --------------------------------------------------------------------------
+# The whole layer
+# --------------------------------------------------------------------------
+
+def route(H, k: int, score_fn: int, renorm: bool) -> dict:
+    """From logits to (idx, gates, scores): rounding to fp32, selection, scoring, gates."""
+    H32 = round_f32(H)
+    idx = topk_select(H32, k)
+    s = scores(H32, score_fn)
+    return dict(logits=H32, idx=idx, s=s, gate=gates(s, idx, renorm))
+
+
+def layer_forward(inp, *, T, h, E, k, d_e, score_fn, renorm, capacity_factor,
+                  capacity_override=0, priority=CHOICE_MAJOR, logits=None) -> dict:
+    """The full single-GPU MoE layer forward, stage by stage, in float64.
+
+    `inp` carries U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down (numpy or
+    torch).  If `logits` is given the router GEMM is skipped and those logits
+    are used as they are.
+    """
+    H = router_logits(inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps) if logits is None else f64(logits)
+    r = route(H, k, score_fn, renorm)
+    C = capacity(T, E, k, capacity_factor, capacity_override)
+    d = dispatch(r["idx"], E, C, priority)
+    X = permute(inp.U, d["row_token"])
+    Y, act = expert_ffn(X, d["offsets"], inp.W_gate, inp.W_up, inp.W_down, d_e)
+    out = combine(inp.U, Y, d["slot_row"], r["gate"], k)
+    st = load_stats(d["counts_routed"], r["s"], T, k, score_fn)
+    return dict(r, **d, X=X, act=act, Y=Y, out=out, **st)
+
+
+def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int) -> dict:
+    """out rows (and the Y rows they use) for a sample of tokens, computed one by one.
+
+    For full-size checks: X[row] = U[t] for a kept pair, so each needed Y row
+    is one expert applied to one token row ([FFN]); out follows [FFN]'s layer
+    output.  Returns {"out": [n, h], "Y": {row: [h]}}.
+    """
+    tokens = np.asarray(tokens, dtype=np.int64)
+    idx = np.asarray(idx, dtype=np.int64)
+    gate = f64(gate)
+    sr = np.asarray(slot_row, dtype=np.int64).reshape(-1, k)
+    outs, Yrows = [], {}
+    for t in tokens:
+        u = f64(inp.U[int(t)]).reshape(1, -1)
+        acc = u.copy()
+        for j in range(k):
+            row = int(sr[t, j])
+            if row < 0:
+                continue
+            e = int(idx[t, j])
+            y, _ = swiglu(u, inp.W_gate[e], inp.W_up[e], inp.W_down[e])
+            Yrows[row] = y[0]
+            acc = acc + gate[t, j] * y
+        outs.append(acc[0])
+    return dict(out=np.stack(outs) if outs else np.zeros((0, 0)), Y=Yrows)
+
+
+def topk_margins(H32: np.ndarray, k: int) -> np.ndarray:
+    """Smallest gap between adjacent values among each row's k+1 largest logits.
+
+    Used by the tests to keep end-to-end routing decisions away from ties:
+    a token whose margin is below the threshold is redrawn.
+    """
+    s = -np.sort(-np.asarray(H32, dtype=np.float64), axis=1)[:, :k + 1]
+    if s.shape[1] < 2:
+        return np.full(s.shape[0], np.inf)
+    return np.min(s[:, :-1] - s[:, 1:], axis=1)

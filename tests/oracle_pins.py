@@ -1,0 +1,391 @@
+"""Pins that tie the oracle to what the pages and the mathematics fix.
+
+Each pin takes the oracle module and raises AssertionError when the oracle
+disagrees with a printed worked example, a closed form, an invariant, a brute
+force on tiny inputs or a textbook special case.  test_oracle_pins runs them on
+the oracle; test_oracle_sensitivity plants one plausible mistake at a time in
+the oracle and checks that some pin fails.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+import types
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name)) as fh:
+        return json.load(fh)
+
+
+def _inputs(**kw):
+    return types.SimpleNamespace(**kw)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- gates
+
+def pin_gate_worked_example(O):
+    """Top-2 scores 0.80 and 0.49 normalise to 0.62 and 0.38 (sigmoid router, E=8)."""
+    g = golden("gate_worked_example.json")
+    s_top = np.array(g["top_scores"])
+    others = np.array([0.30, 0.22, 0.15, 0.10, 0.05, 0.02])
+    s = np.concatenate([others[:3], [s_top[1]], others[3:], [s_top[0]]])  # shuffled positions
+    H = np.log(s / (1 - s))[None, :]                                      # sigmoid^-1
+    r = O.route(H, g["k"], O.SIGMOID, True)
+    assert list(r["idx"][0]) == [len(s) - 1, 3], r["idx"]
+    assert np.allclose(np.round(r["gate"][0], 2), g["gates_2dp"]), r["gate"]
+    exact = s_top / s_top.sum()
+    assert np.allclose(r["gate"][0], exact, atol=1e-6), (r["gate"], exact)
+
+
+def pin_topk_then_softmax_identity(O):
+    """Softmax then renormalise over the selected == softmax over the selected logits only."""
+    rng = _rng(1)
+    H = rng.normal(size=(64, 16)) * 2
+    k = 4
+    r = O.route(H, k, O.SOFTMAX, True)
+    sel = np.take_along_axis(r["logits"], r["idx"].astype(np.int64), 1)
+    direct = np.exp(sel - sel.max(1, keepdims=True))
+    direct /= direct.sum(1, keepdims=True)
+    assert np.allclose(r["gate"], direct, rtol=1e-12, atol=1e-14)
+
+
+def pin_gate_sums(O):
+    """Renormalised gates sum to 1; unrenormalised softmax gates sum below 1 and equal the scores."""
+    rng = _rng(2)
+    H = rng.normal(size=(50, 12))
+    for fn in (O.SOFTMAX, O.SIGMOID):
+        r = O.route(H, 3, fn, True)
+        assert np.allclose(r["gate"].sum(1), 1.0, atol=1e-12)
+    r = O.route(H, 3, O.SOFTMAX, False)
+    assert np.all(r["gate"].sum(1) < 1.0)
+    # with no renormalisation the gate is the softmax probability itself
+    p = np.exp(r["logits"]) / np.exp(r["logits"]).sum(1, keepdims=True)
+    assert np.allclose(r["gate"], np.take_along_axis(p, r["idx"].astype(np.int64), 1), atol=1e-12)
+
+
+def pin_sigmoid_scores(O):
+    """Sigmoid scores are independent per expert: s = 1/(1+e^-x); s(0) = 1/2; s(ln 3) = 3/4."""
+    H = np.array([[0.0, math.log(3.0), -math.log(3.0)]])
+    s = O.scores(H, O.SIGMOID)
+    assert np.allclose(s, [[0.5, 0.75, 0.25]], atol=1e-15)
+    s2 = O.scores(np.array([[0.0, math.log(3.0), 5.0]]), O.SIGMOID)
+    assert np.allclose(s2[0, :2], s[0, :2], atol=1e-15)
+
+
+def pin_softmax_bf16_example(O):
+    """Ten logits of 128 and one of 128.5: 0.142; after bf16 rounding 128.5 -> 128: 1/11 = 0.091."""
+    import torch
+    g = golden("softmax_bf16_example.json")
+    H = np.array([g["logits"]], dtype=np.float64)
+    s = O.scores(H, O.SOFTMAX)
+    assert round(float(s[0, -1]), g["printed_decimals"]) == g["softmax_of_last"]
+    Hb = torch.tensor(H, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    sb = O.scores(Hb, O.SOFTMAX)
+    assert round(float(sb[0, -1]), g["printed_decimals"]) == g["softmax_of_last_after_bf16"]
+    assert abs(sb[0, -1] - 1 / 11) < 1e-15
+
+
+# ---------------------------------------------------------------- router
+
+def pin_router_logits_small(O):
+    """H = U W_r on hand-computed integers, plus bias; the noisy term is eps*ln2 when U W_noise = 0."""
+    U = np.array([[1.0, 2.0], [3.0, 4.0]])
+    W = np.array([[1.0, 0.0, 2.0], [0.0, 1.0, 3.0]])
+    H = O.router_logits(U, W)
+    assert np.array_equal(H, [[1, 2, 8], [3, 4, 18]])
+    b = np.array([0.5, -1.0, 0.0])
+    assert np.array_equal(O.router_logits(U, W, b), [[1.5, 1, 8], [3.5, 3, 18]])
+    eps = np.array([[1.0, -2.0, 0.5], [0.0, 1.0, 1.0]])
+    Hn = O.router_logits(U, W, None, np.zeros((2, 3)), eps)
+    assert np.allclose(Hn - H, eps * math.log(2.0), atol=1e-15)
+
+
+def pin_softplus(O):
+    """Softplus closed forms: ln 2 at 0, x + ln(1+e^-x) for x > 0, e^x-ish far left, no overflow."""
+    x = np.array([0.0, 1.0, -1.0, 50.0, -50.0, 800.0])
+    sp = O.softplus(x)
+    assert abs(sp[0] - math.log(2)) < 1e-15
+    assert abs(sp[1] - math.log(1 + math.e)) < 1e-14
+    assert abs(sp[2] - math.log(1 + 1 / math.e)) < 1e-15
+    assert abs(sp[3] - 50.0) < 1e-14 and abs(sp[4] - math.exp(-50)) < 1e-30
+    assert sp[5] == 800.0
+
+
+def pin_topk_bruteforce(O):
+    """Top-k against sorting every row by (-value, expert id), on small integers with many ties."""
+    rng = _rng(3)
+    for E, k in ((5, 2), (8, 3), (16, 16), (1, 1), (12, 1)):
+        H = rng.integers(-3, 4, size=(40, E)).astype(np.float64)
+        idx = O.topk_select(H, k)
+        for t in range(H.shape[0]):
+            ref = sorted(range(E), key=lambda e: (-H[t, e], e))[:k]
+            assert list(idx[t]) == ref, (E, k, t, H[t], idx[t], ref)
+
+
+def pin_topk_ties(O):
+    """Exact ties go to the lower expert id, for membership and for rank order."""
+    H = np.array([[1.0, 3.0, 3.0, 2.0, 3.0],
+                  [0.0, 0.0, 0.0, 0.0, 0.0],
+                  [-1.0, 5.0, -1.0, -1.0, 5.0]])
+    idx = O.topk_select(H, 3)
+    assert idx.tolist() == [[1, 2, 4], [0, 1, 2], [1, 4, 0]]
+
+
+# ---------------------------------------------------------------- capacity / dispatch
+
+def pin_capacity_examples(O):
+    g = golden("capacity_examples.json")
+    s, l = g["small"], g["large"]
+    assert O.capacity(s["T"], s["E"], s["k"], s["CF"]) == s["C"]
+    assert O.capacity(l["T"], l["E"], l["k"], l["CF"]) == l["C"]
+    assert l["T"] * l["k"] // l["E"] == l["balanced_load"]
+    # ceil of a non-integer load: 10 tokens, 4 experts, top-1, CF 1 -> 2.5 -> 3; CF 1.1 -> 2.75 -> 3
+    assert O.capacity(10, 4, 1, 1.0) == 3
+    assert O.capacity(10, 4, 1, 1.1) == 3
+    assert O.capacity(700, 8, 2, 1.25) == 219      # 218.75
+    assert O.capacity(16, 4, 2, 0.0) == 16         # no limit: C = T
+    assert O.capacity(16, 4, 2, 1.0, override=5) == 5
+
+
+def pin_dispatch_small_example(O):
+    """T=12, E=4, k=1, CF=1: C=3; the expert with 5 tokens drops its last 2 (token order)."""
+    g = golden("capacity_examples.json")["small"]
+    # expert 0 ("expert 1" of the example) gets 5 tokens, experts 1, 2 get 3, expert 3 gets 1
+    idx = np.array([[0], [1], [0], [2], [0], [1], [2], [0], [1], [3], [2], [0]])
+    C = O.capacity(g["T"], g["E"], g["k"], g["CF"])
+    d = O.dispatch(idx, g["E"], C)
+    assert d["counts_routed"].tolist() == [5, 3, 3, 1]
+    assert d["counts_routed"][0] - d["counts_kept"][0] == g["hot_expert_dropped"]
+    assert C - d["counts_kept"][3] == g["cold_expert_idle_slots"]
+    dropped = [t for t in range(12) if d["slot_row"][t] < 0]
+    assert dropped == [7, 11]                        # the last two of expert 0, in token order
+    assert d["n_dropped"] == 2
+    assert d["offsets"].tolist() == [0, 3, 6, 9, 10]
+    assert d["row_token"].tolist() == [0, 2, 4, 1, 5, 8, 3, 6, 10, 9]
+
+
+def pin_dispatch_large_example(O):
+    """T=4096, E=64, k=8, CF=1.25: C=640; 900 assignments drop 260, 300 leave 340 slots idle."""
+    g = golden("capacity_examples.json")["large"]
+    T, E, k = g["T"], g["E"], g["k"]
+    rng = _rng(4)
+    idx = np.zeros((T, k), dtype=np.int64)
+    for t in range(T):
+        fixed = []
+        if t < g["hot_expert_assignments"]:
+            fixed.append(0)
+        if t < g["cold_expert_assignments"]:
+            fixed.append(1)
+        rest = rng.choice(np.arange(2, E), size=k - len(fixed), replace=False)
+        row = np.concatenate([fixed, rest])
+        rng.shuffle(row)
+        idx[t] = row
+    C = O.capacity(T, E, k, g["CF"])
+    d = O.dispatch(idx, E, C)
+    assert d["counts_routed"][0] == 900 and d["counts_routed"][1] == 300
+    assert d["counts_routed"][0] - d["counts_kept"][0] == g["hot_expert_dropped"]
+    assert C - d["counts_kept"][1] == g["cold_expert_idle_slots"]
+
+
+def _dispatch_loop(idx, E, C, priority):
+    """Pure-Python slot filling, one pair at a time (brute force for tiny inputs)."""
+    T, k = idx.shape
+    pairs = ([(t, j) for j in range(k) for t in range(T)] if priority == 0
+             else [(t, j) for t in range(T) for j in range(k)])
+    fill = [0] * E
+    slot = {}
+    for (t, j) in pairs:
+        e = int(idx[t, j])
+        slot[(t, j)] = fill[e]
+        fill[e] += 1
+    kept = [min(c, C) for c in fill]
+    off = [0]
+    for c in kept:
+        off.append(off[-1] + c)
+    slot_row = [-1] * (T * k)
+    row_token = [None] * off[-1]
+    for (t, j), s in slot.items():
+        if s < C:
+            r = off[int(idx[t, j])] + s
+            slot_row[t * k + j] = r
+            row_token[r] = t
+    return fill, kept, off, slot_row, row_token
+
+
+def pin_dispatch_bruteforce(O):
+    rng = _rng(5)
+    for (T, E, k, C) in ((9, 3, 2, 2), (20, 5, 3, 4), (16, 4, 4, 16), (1, 1, 1, 1), (30, 6, 1, 3), (7, 8, 8, 1)):
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+        for pr in (0, 1):
+            d = O.dispatch(idx, E, C, pr)
+            fill, kept, off, slot_row, row_token = _dispatch_loop(idx, E, C, pr)
+            assert d["counts_routed"].tolist() == fill
+            assert d["counts_kept"].tolist() == kept
+            assert d["offsets"].tolist() == off
+            assert d["slot_row"].tolist() == slot_row, (T, E, k, C, pr)
+            assert d["row_token"].tolist() == row_token
+
+
+def pin_dispatch_invariants(O):
+    """Counts add up, slot_row is a bijection onto [0, A), rows point back at their token,
+    and under choice-major priority the kept pairs of every expert precede its dropped ones."""
+    rng = _rng(6)
+    T, E, k = 300, 10, 3
+    p = np.arange(1, E + 1, dtype=float) ** -1.2
+    p /= p.sum()
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)])
+    C = O.capacity(T, E, k, 1.0)
+    d = O.dispatch(idx, E, C, 0)
+    A = int(d["offsets"][-1])
+    assert d["counts_kept"].sum() == T * k - d["n_dropped"] == A
+    assert d["counts_routed"].sum() == T * k
+    kept = d["slot_row"][d["slot_row"] >= 0]
+    assert sorted(kept.tolist()) == list(range(A))
+    for pair in range(T * k):
+        r = d["slot_row"][pair]
+        if r >= 0:
+            t, j = divmod(pair, k)
+            assert d["row_token"][r] == t
+            e = idx[t, j]
+            assert d["offsets"][e] <= r < d["offsets"][e + 1]
+    assert np.all(np.diff(d["offsets"]) >= 0)
+    for e in range(E):
+        ks = [(j, t) for t in range(T) for j in range(k) if idx[t, j] == e and d["slot_row"][t * k + j] >= 0]
+        ds = [(j, t) for t in range(T) for j in range(k) if idx[t, j] == e and d["slot_row"][t * k + j] < 0]
+        if ks and ds:
+            assert max(ks) < min(ds)
+    assert d["n_dropped"] > 0      # the skewed draw must overflow somebody for this to test anything
+
+
+# ---------------------------------------------------------------- experts / combine
+
+def _small_layer(rng, T, h, E, k, d_e, std=0.3):
+    return _inputs(U=rng.normal(size=(T, h)), W_r=rng.normal(size=(h, E)) * std, b_r=None,
+                   W_noise=None, eps=None,
+                   W_gate=rng.normal(size=(E, d_e, h)) * std, W_up=rng.normal(size=(E, d_e, h)) * std,
+                   W_down=rng.normal(size=(E, h, d_e)) * std)
+
+
+def pin_textbook_dense_swiglu(O):
+    """E=1, k=1 reduces to a dense SwiGLU FFN plus the residual (torch's silu and matmul)."""
+    import torch
+    rng = _rng(7)
+    T, h, d_e = 13, 6, 10
+    inp = _small_layer(rng, T, h, 1, 1, d_e)
+    res = O.layer_forward(inp, T=T, h=h, E=1, k=1, d_e=d_e, score_fn=O.SOFTMAX, renorm=True,
+                          capacity_factor=0.0)
+    U = torch.tensor(inp.U)
+    Wg, Wu, Wd = (torch.tensor(x[0]) for x in (inp.W_gate, inp.W_up, inp.W_down))
+    ref = U + torch.nn.functional.linear(torch.nn.functional.silu(torch.nn.functional.linear(U, Wg))
+                                         * torch.nn.functional.linear(U, Wu), Wd)
+    assert np.allclose(res["out"], ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(res["gate"], 1.0)
+
+
+def pin_dense_bruteforce(O):
+    """Unbounded capacity: every expert on every token, masked by the gates, equals the routed path."""
+    import torch
+    rng = _rng(8)
+    for (T, h, E, k, d_e, fn, rn) in ((17, 8, 5, 2, 12, 0, True), (11, 6, 4, 3, 7, 1, True),
+                                      (9, 5, 6, 1, 4, 0, False)):
+        inp = _small_layer(rng, T, h, E, k, d_e)
+        res = O.layer_forward(inp, T=T, h=h, E=E, k=k, d_e=d_e, score_fn=fn, renorm=rn,
+                              capacity_factor=0.0)
+        assert res["n_dropped"] == 0
+        G = np.zeros((T, E))
+        for t in range(T):
+            for j in range(k):
+                G[t, res["idx"][t, j]] = res["gate"][t, j]
+        U = torch.tensor(inp.U)
+        out = U.clone()
+        for e in range(E):
+            Wg, Wu, Wd = (torch.tensor(x[e]) for x in (inp.W_gate, inp.W_up, inp.W_down))
+            y = torch.nn.functional.linear(torch.nn.functional.silu(U @ Wg.T) * (U @ Wu.T), Wd)
+            out += torch.tensor(G[:, e])[:, None] * y
+        assert np.allclose(res["out"], out.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_zero_experts_and_drops(O):
+    """Zero down-projection gives out == U exactly; a token whose pairs all drop keeps U exactly."""
+    rng = _rng(9)
+    T, h, E, k, d_e = 40, 8, 4, 2, 6
+    inp = _small_layer(rng, T, h, E, k, d_e)
+    inp.W_down = np.zeros_like(inp.W_down)
+    res = O.layer_forward(inp, T=T, h=h, E=E, k=k, d_e=d_e, score_fn=0, renorm=True, capacity_factor=1.0)
+    assert np.array_equal(res["out"], inp.U)
+    inp = _small_layer(rng, T, h, E, k, d_e)
+    res = O.layer_forward(inp, T=T, h=h, E=E, k=k, d_e=d_e, score_fn=0, renorm=True,
+                          capacity_factor=0.0, capacity_override=2)
+    sr = res["slot_row"].reshape(T, k)
+    all_dropped = np.all(sr < 0, axis=1)
+    assert all_dropped.sum() > 0
+    assert np.array_equal(res["out"][all_dropped], inp.U[all_dropped])
+    assert not np.allclose(res["out"][~all_dropped], inp.U[~all_dropped])
+
+
+def pin_sampled_matches_full(O):
+    rng = _rng(10)
+    T, h, E, k, d_e = 50, 8, 6, 2, 12
+    inp = _small_layer(rng, T, h, E, k, d_e)
+    res = O.layer_forward(inp, T=T, h=h, E=E, k=k, d_e=d_e, score_fn=0, renorm=True, capacity_factor=1.0)
+    toks = [0, 7, 21, 49]
+    smp = O.sampled_outputs(inp, toks, res["idx"], res["gate"], res["slot_row"], k)
+    assert np.allclose(smp["out"], res["out"][toks], rtol=1e-12, atol=1e-12)
+    for row, y in smp["Y"].items():
+        assert np.allclose(y, res["Y"][row], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- statistics
+
+def pin_aux_balance(O):
+    """E * sum f P == 1 at perfect balance; == E when all load and all probability sit on one expert."""
+    g = golden("aux_balance.json")
+    for E, k in ((4, 1), (8, 2), (64, 6)):
+        T = E * 10
+        counts = np.full(E, T * k // E)
+        s = np.full((T, E), 1.0 / E)
+        st = O.load_stats(counts, s, T, k, O.SOFTMAX)
+        assert abs(st["aux"] - g["value_at_balance"]) < 1e-12
+        assert abs(st["maxvio"]) < 1e-12
+    E, T = 8, 20
+    counts = np.zeros(E)
+    counts[3] = T
+    s = np.zeros((T, E))
+    s[:, 3] = 1.0
+    assert abs(O.load_stats(counts, s, T, 1, O.SOFTMAX)["aux"] - E) < 1e-12
+
+
+def pin_stats_sums(O):
+    """sum f = 1; sum P = 1 for softmax and for normalised sigmoid scores; MaxVio of (2,1,1,0) is 1."""
+    rng = _rng(11)
+    T, E, k = 30, 7, 2
+    H = rng.normal(size=(T, E))
+    for fn in (O.SOFTMAX, O.SIGMOID):
+        r = O.route(H, k, fn, True)
+        d = O.dispatch(r["idx"], E, T)
+        st = O.load_stats(d["counts_routed"], r["s"], T, k, fn)
+        assert abs(st["f"].sum() - 1) < 1e-12
+        assert abs(st["P"].sum() - 1) < 1e-12
+    st = O.load_stats(np.array([2, 1, 1, 0]), np.full((4, 4), 0.25), 4, 1, O.SOFTMAX)
+    assert abs(st["maxvio"] - 1.0) < 1e-15
+
+
+def pin_sigmoid_P_normalised(O):
+    """Sigmoid P_i averages s_i / sum_j s_j: two tokens, sigmoid scores (1/2, 1/2) and (3/4, 1/4)."""
+    H = np.array([[0.0, 0.0], [math.log(3.0), -math.log(3.0)]])
+    s = O.scores(H, O.SIGMOID)
+    st = O.load_stats(np.array([1, 1]), s, 2, 1, O.SIGMOID)
+    assert np.allclose(st["P"], [(0.5 + 0.75) / 2, (0.5 + 0.25) / 2], atol=1e-15)
+
+
+ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -1,0 +1,123 @@
+"""Each plausible oracle mistake must be caught by at least one pin (CPU).
+
+A mistake is planted in the oracle module (never in the library), all pins are
+run against the planted oracle, and at least one must fail.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins
+
+O = oracle.moe_oracle
+_orig = {name: getattr(O, name) for name in dir(O) if callable(getattr(O, name))}
+
+
+def _gates_no_renorm(s, idx, renorm):
+    return _orig["gates"](s, idx, False)
+
+
+def _topk_ties_high(H32, k):
+    E = H32.shape[1]
+    rev = np.asarray(H32)[:, ::-1]
+    order = np.argsort(-rev, axis=1, kind="stable")
+    return (E - 1 - order[:, :k]).astype(np.int32)
+
+
+def _capacity_floor(T, E, k, cf, override=0):
+    if override > 0:
+        return override
+    if cf <= 0:
+        return T
+    return int(math.floor(Fraction(float(np.float32(cf))) * T * k / E))
+
+
+def _capacity_without_k(T, E, k, cf, override=0):
+    return _orig["capacity"](T, E, 1, cf, override)
+
+
+def _silu_sign(x):
+    return x / (1.0 + np.exp(x))
+
+
+def _swiglu_swapped(x, Wg, Wu, Wd):
+    return _orig["swiglu"](x, Wu, Wg, Wd)
+
+
+def _combine_no_gate(U, Y, slot_row, gate, k):
+    return _orig["combine"](U, Y, slot_row, np.ones_like(np.asarray(gate, dtype=float)), k)
+
+
+def _dispatch_token_major(idx, E, C, priority=0):
+    return _orig["dispatch"](idx, E, C, 1)
+
+
+def _stats_unnormalised_sigmoid(counts, s, T, k, fn):
+    return _orig["load_stats"](counts, s, T, k, O.SOFTMAX)
+
+
+def _stats_f_over_T(counts, s, T, k, fn):
+    return _orig["load_stats"](counts, s, T, 1, fn)
+
+
+def _logits_no_bias(U, W_r, b_r=None, W_noise=None, eps=None):
+    return _orig["router_logits"](U, W_r, None, W_noise, eps)
+
+
+def _softplus_exp(x):
+    return np.exp(x)
+
+
+def _dispatch_offsets_routed(idx, E, C, priority=0):
+    d = _orig["dispatch"](idx, E, C, priority)
+    d["offsets"] = np.concatenate([[0], np.cumsum(d["counts_routed"])])
+    return d
+
+
+def _scores_softmax_no_shift_wrong_axis(H, fn):
+    if fn == O.SOFTMAX:
+        z = np.exp(H)
+        return z / z.sum(axis=0, keepdims=True)
+    return _orig["scores"](H, fn)
+
+
+def _sigmoid_wrong_sign(H, fn):
+    if fn == O.SIGMOID:
+        return 1.0 / (1.0 + np.exp(H))
+    return _orig["scores"](H, fn)
+
+
+MUTANTS = {
+    "gates_not_renormalised": ("gates", _gates_no_renorm),
+    "ties_to_higher_id": ("topk_select", _topk_ties_high),
+    "capacity_floor": ("capacity", _capacity_floor),
+    "capacity_without_k": ("capacity", _capacity_without_k),
+    "silu_sign": ("silu", _silu_sign),
+    "gate_up_swapped": ("swiglu", _swiglu_swapped),
+    "combine_ignores_gates": ("combine", _combine_no_gate),
+    "token_major_priority": ("dispatch", _dispatch_token_major),
+    "sigmoid_P_unnormalised": ("load_stats", _stats_unnormalised_sigmoid),
+    "f_normalised_by_T": ("load_stats", _stats_f_over_T),
+    "bias_dropped": ("router_logits", _logits_no_bias),
+    "noise_exp_not_softplus": ("softplus", _softplus_exp),
+    "offsets_from_routed_counts": ("dispatch", _dispatch_offsets_routed),
+    "softmax_over_tokens": ("scores", _scores_softmax_no_shift_wrong_axis),
+    "sigmoid_sign": ("scores", _sigmoid_wrong_sign),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(O, attr, fn)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(O)
+        except Exception:  # an assertion, or a shape error the mistake causes
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake {name!r} passed every pin"
