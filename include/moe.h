@@ -1,0 +1,216 @@
+/*
+ * moe.h -- C ABI of libmoe.so, a B300 (sm_103a) single-GPU Mixture-of-Experts
+ * layer forward.
+ *
+ * The operations and their notation come from "MoE 与专家并行"
+ * (hs-black.github.io/posts/scaling-moe):
+ *   - 从稠密 FFN 到 MoE: SwiGLU expert FFN(u) = W_down (SiLU(W_gate u) ⊙ W_up u)
+ *     and the layer output h'_t = u_t + sum_i g_{i,t} FFN_i(u_t);
+ *   - 路由器：打分、top-k、加权求和: H = U W_r, scores, top-k, gates, the noisy
+ *     top-k router, and the single-GPU shapes listing (permute by expert,
+ *     grouped FFN, index_add back into token order);
+ *   - softmax 门控还是 sigmoid 门控: softmax / sigmoid scoring, with or without
+ *     renormalisation over the selected experts;
+ *   - 专家容量与丢 token: capacity C = ceil(CF * T * k / E), slots filled in
+ *     token order with every token's first choice before any second choice,
+ *     overflow dropped (the token keeps its residual only);
+ *   - 负载均衡辅助损失：推导与梯度: f_i, P_i and E * sum_i f_i P_i (sigmoid P_i
+ *     from s_i / sum_j s_j);
+ *   - 专家计算：padding、block-sparse 与 grouped GEMM: one grouped GEMM over the
+ *     variable-length expert segments, gate and up fused into one [h, 2 d_e]
+ *     product, then SiLU * up, then down.
+ * The capacity formula also appears, for top-1, in the router / expert-
+ * parallel tutorial at aissn.com/133.html (section 工程难点 2).
+ *
+ * Conventions shared by every entry point
+ *   Notation: T tokens, h hidden size, E experts, k experts per token, d_e
+ *   expert intermediate size, A = number of kept (token, expert) pairs.
+ *   Layouts are row-major and dense.  "act dtype" is the config's dtype
+ *   (MOE_F32: float, MOE_BF16: bfloat16) for activations and weights; router
+ *   logits, gates, scores and statistics are float32.
+ *   Memory: every array argument is a DEVICE pointer, 16-byte aligned, owned
+ *   by the caller, unless stated otherwise.  The library never allocates,
+ *   frees or synchronises (moe_get_device_status excepted) and keeps no
+ *   global state; all work is enqueued on the caller's stream in order.
+ *   Workspace: `ws` is caller-owned device scratch of moe_workspace_size()
+ *   bytes, 256-byte aligned, zero-filled once after allocation.  It carries
+ *   the device status word and the per-block partial sums one stage hands to
+ *   the next, so the stage calls of one layer must use the same `ws`, and
+ *   calls that share a `ws` must not overlap on the GPU.
+ *   Errors: argument and shape errors return MOE_ERR_INVALID_ARG or
+ *   MOE_ERR_UNSUPPORTED before anything is enqueued; a failed launch returns
+ *   MOE_ERR_CUDA; errors only the device can see (an expert id out of range,
+ *   inconsistent expert offsets, a pipeline wait that timed out) set the
+ *   status word in `ws` and the offending element is skipped -- read it with
+ *   moe_get_device_status().  moe_last_error() gives a one-line message for
+ *   the last non-OK return of the calling host thread.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad shape, k > E, ... */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid MoE config outside the supported ranges */
+  MOE_ERR_CUDA = 3,          /* a CUDA call or launch failed */
+  MOE_ERR_DEVICE = 4         /* the device status word is set (moe_get_device_status) */
+} moe_status;
+
+typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum moe_priority {
+  MOE_PRIORITY_CHOICE_MAJOR = 0, /* all first choices (tokens in order), then all second choices, ... */
+  MOE_PRIORITY_TOKEN_MAJOR = 1   /* token by token, a token's choices in rank order */
+} moe_priority;
+
+/* Device status codes written into the workspace status word. */
+enum {
+  MOE_DEV_OK = 0,
+  MOE_DEV_BAD_EXPERT_ID = 1,  /* moe_dispatch saw idx outside [0, E); that pair was dropped */
+  MOE_DEV_TIMEOUT = 2,        /* a pipeline wait in the grouped GEMM gave up; outputs are invalid */
+  MOE_DEV_BAD_ROW = 3,        /* moe_combine saw slot_row outside [-1, T*k); that pair was skipped */
+  MOE_DEV_BAD_OFFSETS = 4     /* moe_expert_ffn saw non-monotone or out-of-range offsets; nothing written */
+};
+
+typedef struct moe_config {
+  int64_t T;              /* tokens, >= 0; T * k < 2^31 */
+  int32_t h;              /* hidden size, >= 1, multiple of 8 */
+  int32_t E;              /* experts, 1..1024 */
+  int32_t k;              /* experts per token, 1..min(E, 16) */
+  int32_t d_e;            /* expert intermediate size, >= 1, multiple of 8 */
+  float capacity_factor;  /* CF; <= 0 means no capacity limit (C = T) */
+  int32_t capacity;       /* > 0 overrides the formula with this C */
+  int32_t score_fn;       /* moe_score_fn */
+  int32_t renorm;         /* nonzero: g_j = s_j / sum of the k selected s; zero: g_j = s_j */
+  int32_t noisy;          /* nonzero: noisy top-k router (W_noise, eps required) */
+  int32_t priority;       /* moe_priority: order in which capacity slots are filled */
+  int32_t dtype;          /* moe_dtype of activations and weights */
+} moe_config;
+
+/* Library version string, e.g. "moe-b300 0.1 sm_103a". */
+const char* moe_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status status);
+
+/* One-line message for the last non-OK return on the calling host thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Expert capacity C (host only, no CUDA call).  C = ceil(CF * T * k / E)
+ * evaluated exactly on the float32 value of CF; CF <= 0: C = T; cfg->capacity
+ * > 0: C = cfg->capacity.  Section 专家容量与丢 token. */
+moe_status moe_capacity(const moe_config* cfg, int64_t* C);
+
+/* Bytes of device workspace the calls below need for this config (host only). */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Router: logits, scores, top-k and gates for every token.
+ * Section 路由器：打分、top-k、加权求和 and section softmax 门控还是 sigmoid 门控.
+ *   U        [T, h] act dtype         token hidden states
+ *   W_r      [h, E] act dtype         router weight (column i = expert i's centroid)
+ *   b_r      [E] float32 or NULL      per-expert additive logit bias
+ *   W_noise  [h, E] act dtype         noisy router only (cfg->noisy), else ignored
+ *   eps      [T, E] float32           noisy router only: the N(0,1) draws
+ *   logits_in [T, E] float32 or NULL  stage mode: use these final logits as they
+ *                                     are (U, W_r, b_r, W_noise, eps ignored)
+ *   logits_out [T, E] float32 or NULL receives the final logits
+ *                                     H = U W_r + b_r + eps * softplus(U W_noise)
+ *   idx      [T, k] int32 out         selected experts, highest logit first, ties
+ *                                     to the lower expert id
+ *   gate     [T, k] float32 out       g_j (renormalised over the k or not, cfg->renorm)
+ * Logits accumulate in float32 from the act-dtype inputs; selection compares
+ * the float32 logits.  Also leaves per-block sums of the scores (sigmoid:
+ * s_i / sum_j s_j) in `ws` for moe_combine's P_i. */
+moe_status moe_route(const moe_config* cfg, const void* U, const void* W_r, const float* b_r,
+                     const void* W_noise, const float* eps, const float* logits_in,
+                     float* logits_out, int32_t* idx, float* gate, void* ws, moe_stream_t stream);
+
+/* Capacity-limited dispatch: per-expert histogram, prefix sums, slots, drop
+ * mask, offsets, and the row copy X[row] = U[token].
+ * Section 专家容量与丢 token and the permute of the shapes listing.
+ *   U        [T, h] act dtype
+ *   idx      [T, k] int32             from moe_route (any values; ids outside
+ *                                     [0, E) set MOE_DEV_BAD_EXPERT_ID and drop)
+ *   counts_routed [E] int32 out       pairs that chose expert e (before drops)
+ *   counts_kept   [E] int32 out       min(counts_routed[e], C)
+ *   offsets  [E+1] int32 out          exclusive prefix sum of counts_kept; A = offsets[E]
+ *   slot_row [T*k] int32 out          row of pair (t, j) = t*k + j in X, or -1 if dropped
+ *   row_token [T*k] int32 out         token of each row; only the first A are written
+ *   X        [T*k, h] act dtype out   expert inputs, segment e = rows offsets[e]..offsets[e+1],
+ *                                     in slot (priority) order; only the first A rows written
+ *   n_dropped [1] int64 out           T*k - A
+ * All of it is integer work and bit-exact: the n-th pair (in cfg->priority
+ * order) that chose expert e takes slot n and is kept iff n < C. */
+moe_status moe_dispatch(const moe_config* cfg, const void* U, const int32_t* idx,
+                        int32_t* counts_routed, int32_t* counts_kept, int32_t* offsets,
+                        int32_t* slot_row, int32_t* row_token, void* X, int64_t* n_dropped,
+                        void* ws, moe_stream_t stream);
+
+/* Grouped SwiGLU expert FFN over the expert segments of X.
+ * Section 从稠密 FFN 到 MoE (the expert) and section 专家计算：padding、block-sparse
+ * 与 grouped GEMM (one grouped GEMM for gate|up, SiLU * up, one for down).
+ *   X        [T*k, h] act dtype       rows 0..A-1 valid (from moe_dispatch)
+ *   offsets  [E+1] int32              expert segments (device-resident; no host read)
+ *   W_gate   [E, d_e, h] act dtype    W_gate[e] in R^{d_e x h}
+ *   W_up     [E, d_e, h] act dtype
+ *   W_down   [E, h, d_e] act dtype    W_down[e] in R^{h x d_e}
+ *   act      [T*k, d_e] act dtype out SiLU(X W_gate^T) * (X W_up^T), rounded to act dtype
+ *   Y        [T*k, h] act dtype out   act W_down^T, rounded to act dtype
+ * Accumulation is float32.  bf16 runs on the tcgen05 tensor cores (operands
+ * staged by TMA, accumulators in tensor memory); float32 on the CUDA cores.
+ * Rows >= A of act and Y are not written. */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const int32_t* offsets,
+                          const void* W_gate, const void* W_up, const void* W_down,
+                          void* act, void* Y, void* ws, moe_stream_t stream);
+
+/* Combine and load statistics.
+ * Section 从稠密 FFN 到 MoE (h'_t = u_t + sum g FFN), the index_add of the
+ * shapes listing, and section 负载均衡辅助损失：推导与梯度 (f, P, aux).
+ *   U        [T, h] act dtype
+ *   Y        [T*k, h] act dtype       from moe_expert_ffn
+ *   slot_row [T*k] int32, gate [T, k] float32, counts_routed [E] int32
+ *   out      [T, h] act dtype out     u_t + sum over kept j (ascending) of gate[t,j] * Y[row],
+ *                                     float32 accumulation, one rounding
+ *   f        [E] float32 out          counts_routed[i] / (T*k)
+ *   P        [E] float32 out          (1/T) sum_t s_{i,t}, from the partial sums moe_route
+ *                                     left in this `ws`
+ *   aux      [1] float32 out          E * sum_i f_i P_i (the balance loss with alpha = 1) */
+moe_status moe_combine(const moe_config* cfg, const void* U, const void* Y, const int32_t* slot_row,
+                       const float* gate, const int32_t* counts_routed, void* out, float* f,
+                       float* P, float* aux, void* ws, moe_stream_t stream);
+
+/* Every input and output of one layer forward (pointer meanings as above). */
+typedef struct moe_layer_args {
+  const void* U; const void* W_r; const float* b_r; const void* W_noise; const float* eps;
+  const void* W_gate; const void* W_up; const void* W_down;
+  float* logits_out;                          /* NULL: logits are not written */
+  int32_t* idx; float* gate;
+  int32_t* counts_routed; int32_t* counts_kept; int32_t* offsets;
+  int32_t* slot_row; int32_t* row_token; int64_t* n_dropped;
+  void* X; void* act; void* Y;
+  void* out; float* f; float* P; float* aux;
+} moe_layer_args;
+
+/* The whole layer: moe_route, moe_dispatch, moe_expert_ffn, moe_combine in
+ * order on `stream`, with no host synchronisation in between. */
+moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args* args, void* ws,
+                             moe_stream_t stream);
+
+/* Synchronises `stream`, returns the device status word of `ws` in *code
+ * (MOE_DEV_*) and clears it.  Returns MOE_ERR_DEVICE if the word was set. */
+moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

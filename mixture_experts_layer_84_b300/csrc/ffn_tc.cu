@@ -1,0 +1,375 @@
+// Grouped bf16 SwiGLU expert FFN on the 5th-generation tensor cores.
+//
+// "MoE 与专家并行" (hs-black.github.io/posts/scaling-moe), section 从稠密 FFN 到 MoE:
+// FFN(u) = W_down (SiLU(W_gate u) ⊙ W_up u); section 专家计算：padding、
+// block-sparse 与 grouped GEMM: one launch runs the GEMMs of every expert over
+// its own variable-length segment, scheduled tile by tile inside the kernel
+// from the per-expert offsets; gate and up form one [h, 2 d_e] product,
+// followed by the elementwise SiLU * up, then the down GEMM.
+//
+// Kernel (one persistent CTA per SM, 192 threads):
+//   warp 0    TMA producer: 4-stage ring of {X tile 128x64, W tile 256x64}
+//             (bf16, 128-byte swizzle), completion counted on mbarriers;
+//   warp 1    allocates 512 tensor-memory columns (two 128x256 f32
+//             accumulators) and one lane issues tcgen05.mma 128x256x16,
+//             releasing smem stages and finished accumulators with
+//             tcgen05.commit;
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (TMEM lane = tile row),
+//             SiLU(gate) * up (first GEMM) or plain (second), bf16 rounding,
+//             masked stores of the rows inside the expert segment.
+// Gate|up fusion: a B stage holds 128 rows of W_gate[e] followed by the same
+// 128 rows of W_up[e], so accumulator columns c and 128+c are the gate and up
+// values of output column c; no repacking of the weights is needed.
+// Tile order: expert, then output-column tile, then row tile, so the CTAs that
+// run together share the weight tile (read once from HBM, then from L2), and
+// an expert's rows stay in L2 while its column tiles go by.
+// Every mbarrier wait is bounded (2 s); a wait that gives up makes every role
+// leave its loop, in-flight copies and MMAs are drained (again bounded), the
+// tensor memory is freed and MOE_DEV_TIMEOUT is recorded in the status word.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;                       // tile rows = TMEM lanes
+constexpr int BN = 256;                       // MMA N = B rows per stage
+constexpr int BK = 64;                        // K per stage (one 128-byte swizzle row of bf16)
+constexpr int UK = 16;                        // K per tcgen05.mma kind::f16
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;     // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;     // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t ACC_COLS = 256;            // f32 columns of one 128 x 256 accumulator
+constexpr uint32_t TMEM_COLS = 512;           // two accumulators
+constexpr int THREADS = 192;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr int MAX_E = 1024;
+constexpr size_t BAR_BYTES = 128;             // 13 mbarriers + tmem address + flags
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + sizeof(int) * (MAX_E + 1);
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+__device__ __forceinline__ void decode_tile(const int* tab, int E, int NT, int tile, int* e, int* nt, int* mt) {
+  int lo = 0, hi = E;  // tab[lo]*NT <= tile < tab[hi]*NT
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tab[mid] * NT <= tile)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int m_e = tab[lo + 1] - tab[lo];
+  const int local = tile - tab[lo] * NT;
+  *e = lo;
+  *nt = local / m_e;
+  *mt = local - (*nt) * m_e;
+}
+
+// Wait without regard to the abort flag (drains in-flight work before exit).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+__device__ __forceinline__ void store_32(bf16* orow, int col0, int n_out, const uint32_t* packed) {
+  if (col0 + 32 <= n_out) {
+    uint4* d = reinterpret_cast<uint4*>(orow + col0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+  } else {
+    const bf16* src = reinterpret_cast<const bf16*>(packed);
+    for (int i = 0; i < 32 && col0 + i < n_out; ++i) orow[col0 + i] = src[i];
+  }
+}
+
+// SWIGLU: out[row, c] = SiLU(A W0^T)[row, c] * (A W1^T)[row, c], c < n_out (= d_e), W0/W1 rows per expert = d_e.
+// plain:  out[row, c] = (A W0^T)[row, c],                         c < n_out (= h),   W0 rows per expert = h.
+template <bool SWIGLU>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets, int E, int K,
+                    int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status) {
+  constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* bad_flag = reinterpret_cast<int*>(tmem_holder + 2);
+  int* tab = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + BAR_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NT = (n_out + TILE_N - 1) / TILE_N;
+  const int KB = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    *bad_flag = 0;
+  }
+  __syncthreads();
+  // every CTA checks every segment before anything is written
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int lo = offsets[e], hi = offsets[e + 1];
+    int m = 0;
+    if (lo < 0 || hi < lo || static_cast<int64_t>(hi) > rows_cap)
+      *bad_flag = 1;
+    else
+      m = (hi - lo + BM - 1) / BM;
+    tab[e + 1] = m;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tab[0] = 0;
+    for (int e = 0; e < E; ++e) tab[e + 1] += tab[e];
+    if (*bad_flag && blockIdx.x == 0) set_status(status, MOE_DEV_BAD_OFFSETS);
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 4);
+    }
+    ptx::mbar_init(drain, 1);
+    ptx::fence_mbarrier_init();
+    ptx::fence_proxy_async_smem();
+  }
+  __syncthreads();
+  if (*bad_flag) return;
+  const int total = tab[E] * NT;
+  if (static_cast<int>(blockIdx.x) >= total) return;
+
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB0);
+      if (SWIGLU) ptx::prefetch_tmap(&tmB1);
+      const uint64_t pol_a = ptx::policy_evict_last();
+      const uint64_t pol_b = ptx::policy_evict_normal();
+      uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int e, nt, mt;
+        decode_tile(tab, E, NT, tile, &e, &nt, &mt);
+        const int a_row = offsets[e] + mt * BM;
+        const int b_row = e * b_rows_per_expert + nt * TILE_N;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + stage * STAGE_BYTES;
+          ptx::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          ptx::tma_load_2d(sa, &tmA, kb * BK, a_row, &full[stage], pol_a);
+          if (SWIGLU) {
+            ptx::tma_load_2d(sa + A_BYTES, &tmB0, kb * BK, b_row, &full[stage], pol_b);
+            ptx::tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB1, kb * BK, b_row, &full[stage], pol_b);
+          } else {
+            ptx::tma_load_2d(sa + A_BYTES, &tmB0, kb * BK, b_row, &full[stage], pol_b);
+          }
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy this thread started has landed before the block may exit
+      for (int s = 0; s < STAGES; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_phase >> s) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        if (!ptx::mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(stages + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            ptx::mma_bf16_ss(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * UK * 2), ptx::sdesc_kmajor_sw128(sb + kk * UK * 2),
+                             IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty[stage]);  // stage is free once these MMAs have read it
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&tfull[acc]);  // accumulator complete
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      ptx::mma_commit(drain);  // every MMA issued above has completed once this arrives
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    const int r_local = q * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, nt, mt;
+      decode_tile(tab, E, NT, tile, &e, &nt, &mt);
+      const int seg = offsets[e];
+      const int n_e = offsets[e + 1] - seg;
+      const bool row_ok = mt * BM + r_local < n_e;
+      const int64_t row = static_cast<int64_t>(seg) + mt * BM + r_local;
+      // the tcgen05.ld below is warp-collective: the warp leaves together or not at all
+      const bool ready = ptx::mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, WAIT_LIMIT_NS);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
+      bf16* orow = out + row * n_out;
+      if (SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t gv[32], uv[32], packed[16];
+          ptx::tmem_ld_32x32b_x32(tb + c, gv);
+          ptx::tmem_ld_32x32b_x32(tb + BN / 2 + c, uv);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i]));
+            const float a1 = silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1]));
+            packed[i] = Vec16<bf16>::pack2(a0, a1);
+          }
+          if (row_ok) store_32(orow, nt * TILE_N + c, n_out, packed);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32], packed[16];
+          ptx::tmem_ld_32x32b_x32(tb + c, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = Vec16<bf16>::pack2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if (row_ok) store_32(orow, nt * TILE_N + c, n_out, packed);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  if (threadIdx.x == 0 && *abort_flag) set_status(status, MOE_DEV_TIMEOUT);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of box_rows x 64 with the 128-byte swizzle.
+static bool make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
+                          const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
+                          cudaStream_t s) {
+  using namespace tc;
+  if (p.Tk == 0) return cudaSuccess;
+  CUtensorMap tmX, tmG, tmU, tmAct, tmD;
+  const uint64_t Tk = static_cast<uint64_t>(p.Tk);
+  if (!make_tmap(&tmX, X, Tk, p.h, BM) ||
+      !make_tmap(&tmG, W_gate, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2) ||
+      !make_tmap(&tmU, W_up, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2) ||
+      !make_tmap(&tmAct, act, Tk, p.d_e, BM) ||
+      !make_tmap(&tmD, W_down, static_cast<uint64_t>(p.E) * p.h, p.d_e, BN))
+    return cudaErrorNotSupported;
+  const int nsm = current_sm_count();
+  const int64_t mtiles_max = (p.Tk + BM - 1) / BM + p.E;
+  const int64_t tiles1 = mtiles_max * ((p.d_e + BN / 2 - 1) / (BN / 2));
+  const int64_t tiles2 = mtiles_max * ((p.h + BN - 1) / BN);
+  if (tiles1 >= (int64_t(1) << 31) || tiles2 >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  const int grid1 = static_cast<int>(std::min<int64_t>(nsm, tiles1));
+  const int grid2 = static_cast<int>(std::min<int64_t>(nsm, tiles2));
+
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(grouped_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  grouped_gemm_tc<true><<<grid1, THREADS, SMEM_BYTES, s>>>(tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
+                                                           static_cast<bf16*>(act), status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  grouped_gemm_tc<false><<<grid2, THREADS, SMEM_BYTES, s>>>(tmAct, tmD, tmD, offsets, p.E, p.d_e, p.h, p.h, p.Tk,
+                                                            static_cast<bf16*>(Y), status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

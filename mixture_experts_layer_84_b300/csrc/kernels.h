@@ -1,0 +1,83 @@
+// Internal launch interface of libmoe (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Tile constants shared by the launch plan and the kernels.
+constexpr int route_bt_for(int ep) { return ep <= 256 ? 32 : 8192 / ep; }  // tokens per partial-logits block
+constexpr int route_kc_for(int ep) { return ep <= 128 ? 64 : 8192 / ep; }  // h chunk per pipeline stage
+constexpr int kSelTokens = 32;        // tokens per select block (8 warps x 4)
+constexpr int kDispatchChunk = 4096;  // priority positions per dispatch chunk
+
+// Sizes derived from one moe_config, and the carve-up of the workspace.
+struct Plan {
+  int64_t T = 0;
+  int h = 0, E = 0, k = 0, d_e = 0;
+  int64_t C = 0;           // expert capacity
+  int64_t Tk = 0;          // T * k = rows of the capacity buffers X, act, Y
+  bool bf16 = false;
+  bool noisy = false;
+  int score_fn = 0, renorm = 0, priority = 0;
+
+  // router
+  int route_ep = 0;        // E rounded up to the router's compile-time width
+  int route_bt = 0;        // tokens per partial-logits block
+  int route_kc = 0;        // K chunk of the partial-logits block
+  int route_rowblocks = 0; // ceil(T / route_bt)
+  int route_splits = 0;    // split of h across blocks (summed in fixed order by the select kernel)
+  int sel_tokens = 0;      // tokens per select block
+  int sel_blocks = 0;      // ceil(T / sel_tokens): number of P partial rows
+
+  // dispatch
+  int chunk = 0;           // priority positions per histogram chunk
+  int n_chunks = 0;
+
+  // workspace byte offsets
+  size_t ws_status = 0, ws_part = 0, ws_npart = 0, ws_ppart = 0, ws_hist = 0, ws_total = 0;
+};
+
+// Validates the config and fills `plan`; on failure returns the status and a message.
+moe_status make_plan(const moe_config* cfg, Plan* plan, const char** msg);
+
+cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const void* W_noise,
+                         const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                         uint8_t* ws, cudaStream_t s);
+
+cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, int32_t* counts_routed,
+                            int32_t* counts_kept, int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* X,
+                            int64_t* n_dropped, uint8_t* ws, cudaStream_t s);
+
+cudaError_t launch_expert_ffn(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
+                              const void* W_up, const void* W_down, void* act, void* Y, uint8_t* ws, cudaStream_t s);
+
+cudaError_t launch_combine(const Plan& p, const void* U, const void* Y, const int32_t* slot_row, const float* gate,
+                           const int32_t* counts_routed, void* out, float* f, float* P, float* aux, uint8_t* ws,
+                           cudaStream_t s);
+
+// Grouped bf16 GEMMs on tcgen05 (both FFN halves); returns cudaErrorNotSupported when the
+// tensor maps cannot be built.
+cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
+                          const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
+                          cudaStream_t s);
+cudaError_t launch_ffn_simt_f32(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
+                                const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
+                                cudaStream_t s);
+
+inline int32_t* ws_status(const Plan& p, uint8_t* ws) { return reinterpret_cast<int32_t*>(ws + p.ws_status); }
+
+// Streaming multiprocessors of the current device (148 on B300 if the query fails).
+inline int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0)
+    return 148;
+  return n;
+}
+
+}  // namespace moe

@@ -1,0 +1,369 @@
+// C ABI of libmoe: argument validation, the launch plan and workspace
+// carve-up, and the launch sequence of each entry point (include/moe.h).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+moe_status cuda_fail(const char* where, cudaError_t e) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// ceil(cf * Tk / E), exact on the float32 value of cf (cf = m * 2^ex with an integer m).
+int64_t capacity_exact(int64_t Tk, int E, float cf) {
+  if (Tk == 0) return 0;
+  int ex = 0;
+  const float fr = frexpf(cf, &ex);  // cf = fr * 2^ex, fr in [0.5, 1)
+  const uint64_t m = static_cast<uint64_t>(ldexpf(fr, 24));
+  ex -= 24;  // cf = m * 2^ex exactly
+  typedef unsigned __int128 u128;
+  u128 num = static_cast<u128>(m) * static_cast<u128>(Tk);
+  u128 den = static_cast<u128>(E);
+  if (ex >= 0) {
+    if (ex > 60) return INT64_MAX;
+    num <<= ex;
+  } else {
+    if (-ex > 100) return 1;  // 0 < cf*Tk/E < 1
+    den <<= -ex;
+  }
+  const u128 q = (num + den - 1) / den;
+  return q > static_cast<u128>(INT64_MAX) ? INT64_MAX : static_cast<int64_t>(q);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A device array argument: required unless it holds no bytes; aligned as given.
+moe_status check_ptr(const char* fn, const char* name, const void* p, size_t bytes, size_t align) {
+  if (bytes > 0 && p == nullptr) return fail(MOE_ERR_INVALID_ARG, "%s: %s is NULL", fn, name);
+  if (p != nullptr && !aligned(p, align))
+    return fail(MOE_ERR_INVALID_ARG, "%s: %s is not %zu-byte aligned", fn, name, align);
+  return MOE_OK;
+}
+
+#define CHECK(expr)                   \
+  do {                                \
+    moe_status st_ = (expr);          \
+    if (st_ != MOE_OK) return st_;    \
+  } while (0)
+
+}  // namespace
+
+moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
+  static thread_local char buf[256];
+  auto bad = [&](moe_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    *msg = buf;
+    return st;
+  };
+  if (!cfg) return bad(MOE_ERR_INVALID_ARG, "cfg is NULL");
+  if (cfg->T < 0) return bad(MOE_ERR_INVALID_ARG, "T = %lld < 0", static_cast<long long>(cfg->T));
+  if (cfg->h < 1 || cfg->E < 1 || cfg->k < 1 || cfg->d_e < 1)
+    return bad(MOE_ERR_INVALID_ARG, "h, E, k, d_e must be >= 1 (got %d, %d, %d, %d)", cfg->h, cfg->E, cfg->k,
+               cfg->d_e);
+  if (cfg->k > cfg->E) return bad(MOE_ERR_INVALID_ARG, "k = %d > E = %d", cfg->k, cfg->E);
+  if (cfg->dtype != MOE_F32 && cfg->dtype != MOE_BF16) return bad(MOE_ERR_INVALID_ARG, "dtype %d", cfg->dtype);
+  if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID)
+    return bad(MOE_ERR_INVALID_ARG, "score_fn %d", cfg->score_fn);
+  if (cfg->priority != MOE_PRIORITY_CHOICE_MAJOR && cfg->priority != MOE_PRIORITY_TOKEN_MAJOR)
+    return bad(MOE_ERR_INVALID_ARG, "priority %d", cfg->priority);
+  if (cfg->capacity < 0) return bad(MOE_ERR_INVALID_ARG, "capacity = %d < 0", cfg->capacity);
+  if (!isfinite(cfg->capacity_factor)) return bad(MOE_ERR_INVALID_ARG, "capacity_factor is not finite");
+  if (cfg->E > 1024) return bad(MOE_ERR_UNSUPPORTED, "E = %d > 1024", cfg->E);
+  if (cfg->k > 16) return bad(MOE_ERR_UNSUPPORTED, "k = %d > 16", cfg->k);
+  if (cfg->h % 8 != 0 || cfg->d_e % 8 != 0)
+    return bad(MOE_ERR_UNSUPPORTED, "h = %d and d_e = %d must be multiples of 8", cfg->h, cfg->d_e);
+  const int64_t Tk = cfg->T * cfg->k;
+  if (Tk >= (int64_t(1) << 31)) return bad(MOE_ERR_UNSUPPORTED, "T * k = %lld >= 2^31", static_cast<long long>(Tk));
+  if (cfg->dtype == MOE_BF16 && static_cast<int64_t>(cfg->E) * std::max(cfg->h, cfg->d_e) >= (int64_t(1) << 31))
+    return bad(MOE_ERR_UNSUPPORTED, "E * max(h, d_e) >= 2^31");
+
+  Plan q;
+  q.T = cfg->T;
+  q.h = cfg->h;
+  q.E = cfg->E;
+  q.k = cfg->k;
+  q.d_e = cfg->d_e;
+  q.Tk = Tk;
+  q.bf16 = cfg->dtype == MOE_BF16;
+  q.noisy = cfg->noisy != 0;
+  q.score_fn = cfg->score_fn;
+  q.renorm = cfg->renorm != 0;
+  q.priority = cfg->priority;
+  if (cfg->capacity > 0)
+    q.C = cfg->capacity;
+  else if (cfg->capacity_factor <= 0.f)
+    q.C = cfg->T;
+  else
+    q.C = capacity_exact(Tk, cfg->E, cfg->capacity_factor);
+
+  int ep = 8;
+  while (ep < q.E) ep <<= 1;
+  q.route_ep = ep;
+  q.route_bt = route_bt_for(ep);
+  q.route_kc = route_kc_for(ep);
+  q.route_rowblocks = static_cast<int>((q.T + q.route_bt - 1) / q.route_bt);
+  const int nkc = (q.h + q.route_kc - 1) / q.route_kc;
+  int splits = q.route_rowblocks > 0 ? (512 + q.route_rowblocks - 1) / q.route_rowblocks : 1;
+  splits = std::max(1, std::min(splits, std::min(16, nkc)));
+  q.route_splits = splits;
+  q.sel_tokens = kSelTokens;
+  q.sel_blocks = static_cast<int>((q.T + kSelTokens - 1) / kSelTokens);
+  q.chunk = kDispatchChunk;
+  q.n_chunks = static_cast<int>((Tk + kDispatchChunk - 1) / kDispatchChunk);
+
+  size_t off = 0;
+  q.ws_status = off;
+  off += 256;
+  const size_t logits_bytes = sizeof(float) * static_cast<size_t>(splits) * q.T * q.E;
+  q.ws_part = off;
+  off += align256(logits_bytes);
+  q.ws_npart = off;
+  if (q.noisy) off += align256(logits_bytes);
+  q.ws_ppart = off;
+  off += align256(sizeof(float) * static_cast<size_t>(q.sel_blocks) * q.E);
+  q.ws_hist = off;
+  off += align256(sizeof(int32_t) * static_cast<size_t>(q.n_chunks) * q.E);
+  q.ws_total = off;
+  *p = q;
+  return MOE_OK;
+}
+
+namespace {
+
+moe_status plan_or_fail(const char* fn, const moe_config* cfg, Plan* p) {
+  const char* msg = "";
+  const moe_status st = make_plan(cfg, p, &msg);
+  if (st != MOE_OK) return fail(st, "%s: %s", fn, msg);
+  return MOE_OK;
+}
+
+moe_status check_route_args(const char* fn, const Plan& p, const void* U, const void* W_r, const void* W_noise,
+                            const float* eps, const float* logits_in, const float* logits_out, const int32_t* idx,
+                            const float* gate, const void* ws) {
+  const size_t es = p.bf16 ? 2 : 4;
+  const size_t TE = static_cast<size_t>(p.T) * p.E;
+  if (!logits_in) {
+    CHECK(check_ptr(fn, "U", U, static_cast<size_t>(p.T) * p.h * es, 16));
+    CHECK(check_ptr(fn, "W_r", W_r, p.T > 0 ? static_cast<size_t>(p.h) * p.E * es : 0, es));
+    if (p.noisy) {
+      CHECK(check_ptr(fn, "W_noise", W_noise, p.T > 0 ? static_cast<size_t>(p.h) * p.E * es : 0, es));
+      CHECK(check_ptr(fn, "eps", eps, TE * 4, 4));
+    }
+  } else {
+    CHECK(check_ptr(fn, "logits_in", logits_in, TE * 4, 4));
+  }
+  CHECK(check_ptr(fn, "logits_out", logits_out, 0, 4));
+  CHECK(check_ptr(fn, "idx", idx, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(check_ptr(fn, "gate", gate, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(check_ptr(fn, "ws", ws, p.ws_total, 256));
+  return MOE_OK;
+}
+
+moe_status check_dispatch_args(const char* fn, const Plan& p, const void* U, const int32_t* idx,
+                               const int32_t* counts_routed, const int32_t* counts_kept, const int32_t* offsets,
+                               const int32_t* slot_row, const int32_t* row_token, const void* X,
+                               const int64_t* n_dropped, const void* ws) {
+  const size_t es = p.bf16 ? 2 : 4;
+  CHECK(check_ptr(fn, "U", U, static_cast<size_t>(p.T) * p.h * es, 16));
+  CHECK(check_ptr(fn, "idx", idx, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(check_ptr(fn, "counts_routed", counts_routed, static_cast<size_t>(p.E) * 4, 4));
+  CHECK(check_ptr(fn, "counts_kept", counts_kept, static_cast<size_t>(p.E) * 4, 4));
+  CHECK(check_ptr(fn, "offsets", offsets, static_cast<size_t>(p.E + 1) * 4, 4));
+  CHECK(check_ptr(fn, "slot_row", slot_row, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(check_ptr(fn, "row_token", row_token, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(check_ptr(fn, "X", X, static_cast<size_t>(p.Tk) * p.h * es, 16));
+  CHECK(check_ptr(fn, "n_dropped", n_dropped, 8, 8));
+  CHECK(check_ptr(fn, "ws", ws, p.ws_total, 256));
+  return MOE_OK;
+}
+
+moe_status check_ffn_args(const char* fn, const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
+                          const void* W_up, const void* W_down, const void* act, const void* Y, const void* ws) {
+  const size_t es = p.bf16 ? 2 : 4;
+  const size_t wbytes = p.Tk > 0 ? static_cast<size_t>(p.E) * p.d_e * p.h * es : 0;
+  CHECK(check_ptr(fn, "X", X, static_cast<size_t>(p.Tk) * p.h * es, 16));
+  CHECK(check_ptr(fn, "offsets", offsets, static_cast<size_t>(p.E + 1) * 4, 4));
+  CHECK(check_ptr(fn, "W_gate", W_gate, wbytes, 16));
+  CHECK(check_ptr(fn, "W_up", W_up, wbytes, 16));
+  CHECK(check_ptr(fn, "W_down", W_down, wbytes, 16));
+  CHECK(check_ptr(fn, "act", act, static_cast<size_t>(p.Tk) * p.d_e * es, 16));
+  CHECK(check_ptr(fn, "Y", Y, static_cast<size_t>(p.Tk) * p.h * es, 16));
+  CHECK(check_ptr(fn, "ws", ws, p.ws_total, 256));
+  return MOE_OK;
+}
+
+moe_status check_combine_args(const char* fn, const Plan& p, const void* U, const void* Y, const int32_t* slot_row,
+                              const float* gate, const int32_t* counts_routed, const void* out, const float* f,
+                              const float* P, const float* aux, const void* ws) {
+  const size_t es = p.bf16 ? 2 : 4;
+  CHECK(check_ptr(fn, "U", U, static_cast<size_t>(p.T) * p.h * es, 16));
+  CHECK(check_ptr(fn, "Y", Y, static_cast<size_t>(p.Tk) * p.h * es, 16));
+  CHECK(check_ptr(fn, "slot_row", slot_row, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(check_ptr(fn, "gate", gate, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(check_ptr(fn, "counts_routed", counts_routed, static_cast<size_t>(p.E) * 4, 4));
+  CHECK(check_ptr(fn, "out", out, static_cast<size_t>(p.T) * p.h * es, 16));
+  CHECK(check_ptr(fn, "f", f, static_cast<size_t>(p.E) * 4, 4));
+  CHECK(check_ptr(fn, "P", P, static_cast<size_t>(p.E) * 4, 4));
+  CHECK(check_ptr(fn, "aux", aux, 4, 4));
+  CHECK(check_ptr(fn, "ws", ws, p.ws_total, 256));
+  return MOE_OK;
+}
+
+}  // namespace
+
+cudaError_t launch_expert_ffn(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
+                              const void* W_up, const void* W_down, void* act, void* Y, uint8_t* ws, cudaStream_t s) {
+  if (p.bf16) return launch_ffn_tc(p, X, offsets, W_gate, W_up, W_down, act, Y, ws_status(p, ws), s);
+  return launch_ffn_simt_f32(p, X, offsets, W_gate, W_up, W_down, act, Y, ws_status(p, ws), s);
+}
+
+}  // namespace moe
+
+using moe::Plan;
+
+MOE_API const char* moe_version(void) { return "moe-b300 0.1 sm_103a"; }
+
+MOE_API const char* moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+MOE_API const char* moe_last_error(void) { return moe::g_last_error; }
+
+MOE_API moe_status moe_capacity(const moe_config* cfg, int64_t* C) {
+  Plan p;
+  CHECK(moe::plan_or_fail("moe_capacity", cfg, &p));
+  if (!C) return moe::fail(MOE_ERR_INVALID_ARG, "moe_capacity: C is NULL");
+  *C = p.C;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  Plan p;
+  CHECK(moe::plan_or_fail("moe_workspace_size", cfg, &p));
+  if (!bytes) return moe::fail(MOE_ERR_INVALID_ARG, "moe_workspace_size: bytes is NULL");
+  *bytes = p.ws_total;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_route(const moe_config* cfg, const void* U, const void* W_r, const float* b_r,
+                             const void* W_noise, const float* eps, const float* logits_in, float* logits_out,
+                             int32_t* idx, float* gate, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_route";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  CHECK(moe::check_route_args(fn, p, U, W_r, W_noise, eps, logits_in, logits_out, idx, gate, ws));
+  CHECK(moe::check_ptr(fn, "b_r", b_r, 0, 4));
+  const cudaError_t e = moe::launch_route(p, U, W_r, b_r, W_noise, eps, logits_in, logits_out, idx, gate,
+                                          static_cast<uint8_t*>(ws), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* U, const int32_t* idx, int32_t* counts_routed,
+                                int32_t* counts_kept, int32_t* offsets, int32_t* slot_row, int32_t* row_token,
+                                void* X, int64_t* n_dropped, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_dispatch";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  CHECK(moe::check_dispatch_args(fn, p, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, X,
+                                 n_dropped, ws));
+  const cudaError_t e = moe::launch_dispatch(p, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, X,
+                                             n_dropped, static_cast<uint8_t*>(ws), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const int32_t* offsets, const void* W_gate,
+                                  const void* W_up, const void* W_down, void* act, void* Y, void* ws,
+                                  moe_stream_t stream) {
+  static const char* fn = "moe_expert_ffn";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  CHECK(moe::check_ffn_args(fn, p, X, offsets, W_gate, W_up, W_down, act, Y, ws));
+  const cudaError_t e = moe::launch_expert_ffn(p, X, offsets, W_gate, W_up, W_down, act, Y,
+                                               static_cast<uint8_t*>(ws), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_combine(const moe_config* cfg, const void* U, const void* Y, const int32_t* slot_row,
+                               const float* gate, const int32_t* counts_routed, void* out, float* f, float* P,
+                               float* aux, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_combine";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  CHECK(moe::check_combine_args(fn, p, U, Y, slot_row, gate, counts_routed, out, f, P, aux, ws));
+  const cudaError_t e = moe::launch_combine(p, U, Y, slot_row, gate, counts_routed, out, f, P, aux,
+                                            static_cast<uint8_t*>(ws), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args* a, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_layer_forward";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (!a) return moe::fail(MOE_ERR_INVALID_ARG, "%s: args is NULL", fn);
+  CHECK(moe::check_route_args(fn, p, a->U, a->W_r, a->W_noise, a->eps, nullptr, a->logits_out, a->idx, a->gate, ws));
+  CHECK(moe::check_ptr(fn, "b_r", a->b_r, 0, 4));
+  CHECK(moe::check_dispatch_args(fn, p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row,
+                                 a->row_token, a->X, a->n_dropped, ws));
+  CHECK(moe::check_ffn_args(fn, p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, ws));
+  CHECK(moe::check_combine_args(fn, p, a->U, a->Y, a->slot_row, a->gate, a->counts_routed, a->out, a->f, a->P,
+                                a->aux, ws));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  cudaError_t e = moe::launch_route(p, a->U, a->W_r, a->b_r, a->W_noise, a->eps, nullptr, a->logits_out, a->idx,
+                                    a->gate, w, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/route", e);
+  e = moe::launch_dispatch(p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row, a->row_token,
+                           a->X, a->n_dropped, w, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/dispatch", e);
+  e = moe::launch_expert_ffn(p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, w, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/expert_ffn", e);
+  e = moe::launch_combine(p, a->U, a->Y, a->slot_row, a->gate, a->counts_routed, a->out, a->f, a->P, a->aux, w,
+                          stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/combine", e);
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* code) {
+  static const char* fn = "moe_get_device_status";
+  if (!ws || !moe::aligned(ws, 256)) return moe::fail(MOE_ERR_INVALID_ARG, "%s: ws is NULL or misaligned", fn);
+  if (!code) return moe::fail(MOE_ERR_INVALID_ARG, "%s: code is NULL", fn);
+  int32_t h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess && h != 0) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return moe::cuda_fail(fn, e);
+  *code = h;
+  if (h != 0) return moe::fail(MOE_ERR_DEVICE, "%s: device status %d", fn, h);
+  return MOE_OK;
+}
