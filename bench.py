@@ -1,0 +1,521 @@
+#!/usr/bin/env python
+"""Throughput of the single-GPU MoE layer forward (libmoe on B300, sm_103a).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl b300|reference]
+
+One step = one pass of the whole layer (router, dispatch, grouped SwiGLU
+experts, combine + statistics) over one batch of T tokens whose inputs are
+already resident in HBM.  Each step takes the next of several token batches
+so the working set of consecutive steps exceeds L2 (126 MB); the expert
+weights alone are larger than L2 on every workload but the tiny one.
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica (independent batches, no collective on the data path): weak scaling.
+
+--impl reference times the plain float64 CPU oracle (oracle/) on the host
+cores on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_84_b300 import synth  # noqa: E402
+from mixture_experts_layer_84_b300 import workloads as W  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 B300; dispatch/combine %HBM BW; expert GEMM %TC peak"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+GEMM_SOURCES = ["mixture_experts_layer_84_b300/csrc/ffn_tc.cu", "mixture_experts_layer_84_b300/csrc/ptx.cuh"]
+
+
+# ----------------------------------------------------------------------------- ranks
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend: str):
+    ws, rank, local = dist_env()
+    if ws > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(device=None):
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        if device is not None and device.type == "cuda":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+    if device is not None and device.type == "cuda":
+        torch.cuda.synchronize(device)
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (x itself when not distributed)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank_step: int, steps: int, n_ranks: int, max_seconds: float) -> float:
+    """Whole-job tokens/s: every rank processed its own batches in the slowest rank's time."""
+    return tokens_per_rank_step * steps * n_ranks / max_seconds
+
+
+# ----------------------------------------------------------------------------- peaks, clocks
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples of one GPU while a region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+            if not self.uuid.startswith("GPU-"):
+                self.uuid = "GPU-" + self.uuid
+        except Exception:
+            self.uuid = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd[1:1] = ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "power_w_max": max(power) if power else None, "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def stage_work(w: W.Workload, A: float, n_active: float):
+    """Algorithmic bytes and FLOPs of each stage for one step (A kept pairs, n_active experts with rows)."""
+    b = w.elem_bytes
+    T, h, E, k, d = w.T, w.h, w.E, w.k, w.d_e
+    route_bytes = T * h * b + h * E * b + T * k * 8 + (h * E * b + T * E * 4 if w.noisy else 0)
+    route_flops = 2 * T * h * E * (2 if w.noisy else 1)
+    dispatch_bytes = T * h * b + A * h * b + T * k * 12
+    ffn_flops = 6 * A * h * d
+    ffn_bytes = 3 * h * d * b * n_active + 2 * A * h * b + 2 * A * d * b
+    combine_bytes = A * h * b + 2 * T * h * b + T * k * 8
+    return {"route": {"bytes": route_bytes, "flops": route_flops},
+            "dispatch": {"bytes": dispatch_bytes, "flops": 0},
+            "ffn": {"bytes": ffn_bytes, "flops": ffn_flops},
+            "combine": {"bytes": combine_bytes, "flops": 0}}
+
+
+def launches_per_step(w: W.Workload) -> int:
+    """Kernels libmoe launches for one moe_layer_forward of this workload."""
+    if w.T == 0:
+        return 2  # dispatch scan + statistics
+    route, dispatch, ffn, combine = 2, 4, 2, 2
+    return route + dispatch + ffn + combine
+
+
+def kernel_source_sha(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profile_traffic(workload_name):
+    """DRAM bytes per step of the grouped GEMM (both launches) from the committed ncu summary,
+    if the kernel source it was taken on is the current one (else None)."""
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    m_tr = re.search(r"traffic_bytes_per_step:\s*([0-9.eE+]+)", txt)
+    if not (m_sha and m_tr) or m_sha.group(1) != kernel_source_sha(GEMM_SOURCES):
+        return None
+    return float(m_tr.group(1))
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+class _Inp:
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+class ExpertsF64:
+    """One kind of expert weight, widened to float64 expert by expert on first use (then cached)."""
+
+    def __init__(self, W_all, preload=()):
+        self.W = W_all
+        self.cache = {}
+        for e in preload:
+            self[e]
+
+    def __getitem__(self, e):
+        import oracle
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = oracle.f64(self.W[e])
+        return self.cache[e]
+
+
+def oracle_inputs_host(inp: "synth.LayerInputs", U_host, experts=()):
+    """Host copies for the oracle: token rows as given, router weights and the listed experts'
+    weights widened to float64 beforehand (input preparation, outside any timed region)."""
+    import oracle
+    f = oracle.f64
+    return _Inp(U=U_host, W_r=f(inp.W_r), b_r=None if inp.b_r is None else f(inp.b_r),
+                W_noise=None if inp.W_noise is None else f(inp.W_noise),
+                eps=None if inp.eps is None else f(inp.eps),
+                W_gate=ExpertsF64(inp.W_gate, experts), W_up=ExpertsF64(inp.W_up, experts),
+                W_down=ExpertsF64(inp.W_down, experts))
+
+
+def touched_experts(w: W.Workload, host, tokens):
+    import numpy as np
+    import oracle
+    H = oracle.router_logits(host.U[tokens], host.W_r, host.b_r, host.W_noise,
+                             None if host.eps is None else host.eps[tokens])
+    return sorted(set(np.unique(oracle.route(H, w.k, w.score_fn, w.renorm)["idx"]).tolist()))
+
+
+def oracle_step(w: W.Workload, host, tokens):
+    """The oracle's whole layer forward on a sample of the batch's tokens."""
+    import oracle
+    sub = _Inp(U=host.U[tokens], W_r=host.W_r, b_r=host.b_r, W_noise=host.W_noise,
+               eps=None if host.eps is None else host.eps[tokens],
+               W_gate=host.W_gate, W_up=host.W_up, W_down=host.W_down)
+    return oracle.layer_forward(sub, T=len(tokens), h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn,
+                                renorm=w.renorm, capacity_factor=w.capacity_factor, capacity_override=w.capacity,
+                                priority=w.priority)
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(w: W.Workload, inp, n_tokens: int):
+    import numpy as np
+    import oracle
+    n_tokens = max(1, min(n_tokens, w.T))
+    sub_inp = synth.LayerInputs(U=inp.U[:n_tokens], W_r=inp.W_r, b_r=inp.b_r, W_noise=inp.W_noise,
+                                eps=None if inp.eps is None else inp.eps[:n_tokens],
+                                W_gate=inp.W_gate, W_up=inp.W_up, W_down=inp.W_down)
+    host = oracle_inputs_host(sub_inp, oracle.f64(sub_inp.U))
+    toks = np.arange(n_tokens)
+    for e in touched_experts(w, host, toks):
+        host.W_gate[e], host.W_up[e], host.W_down[e]
+    t0 = time.perf_counter()
+    oracle_step(w, host, toks)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"oracle layer forward (float64 numpy) on the first {n_tokens} of the batch's {w.T} "
+                      f"tokens with the same weights (widened to float64 beforehand), one call, "
+                      f"{dt:.1f} s; capacity from those {n_tokens} tokens"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def workload_config(w: W.Workload, n_rot: int = 0):
+    c = {"workload": w.name, "T": w.T, "h": w.h, "E": w.E, "k": w.k, "d_e": w.d_e,
+         "score": "softmax" if w.score_fn == W.SOFTMAX else "sigmoid", "renorm": w.renorm, "noisy": w.noisy,
+         "capacity_factor": w.capacity_factor, "logit_bias": w.bias, "parallelism": "replicas"}
+    if n_rot:
+        c["l2"] = (f"inputs larger than L2: {n_rot} rotating token batches plus "
+                   f"{3 * w.E * w.h * w.d_e * w.elem_bytes / 1e9:.2f} GB of expert weights per step")
+    return c
+
+
+def run_reference(args, w: W.Workload):
+    import numpy as np
+    import oracle
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = synth.generate(w, seed=0, device="cpu")
+    f64_bytes = 3 * w.E * w.h * w.d_e * 8
+    host = oracle_inputs_host(inp, oracle.f64(inp.U), range(w.E) if f64_bytes <= 24e9 else ())
+    budget = float(args.reference_budget_s)
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(w.T, size=min(4, w.T), replace=False))
+    t0 = time.perf_counter()
+    oracle_step(w, host, probe)
+    per_tok = (time.perf_counter() - t0) / len(probe)
+    n = int(max(1, min(w.T, budget / max(1, args.steps + args.warmup) / max(per_tok, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_step(w, host, np.sort(rng.choice(w.T, size=n, replace=False)))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, host, np.sort(rng.choice(w.T, size=n, replace=False)))
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    sample = (f"each step: the oracle layer forward (float64 numpy) on {n} tokens drawn from the "
+              f"{w.T}-token batch; expert weights widened to float64 "
+              + ("beforehand" if f64_bytes <= 24e9 else "on first use (inside the timed steps)"))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- B300 arm
+
+def run_b300(args, w: W.Workload):
+    ws_n, rank, local = init_dist("nccl")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from mixture_experts_layer_84_b300 import _lib as L
+
+    inp = synth.generate(w, seed=0, device=device)
+    ubytes = w.T * w.h * w.elem_bytes
+    n_rot = max(2, min(64, math.ceil(2 * L2_BYTES / max(ubytes, 1))))
+    pool = [inp.U] + [synth.normal((w.T, w.h), 1.0, 100 + r, "U", device, w.torch_dtype) for r in range(n_rot - 1)]
+    cfg = L.config_of(w)
+    bufs = L.LayerBuffers.allocate(cfg, device=device)
+
+    def stage_calls(U, ev=None):
+        # the four stage calls of moe_layer_forward, with events between them
+        L.moe_route(cfg, U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, None, None, bufs.idx, bufs.gate, bufs.ws)
+        if ev is not None:
+            ev[0].record()
+        L.moe_dispatch(cfg, U, bufs.idx, bufs.counts_routed, bufs.counts_kept, bufs.offsets, bufs.slot_row,
+                       bufs.row_token, bufs.X, bufs.n_dropped, bufs.ws)
+        if ev is not None:
+            ev[1].record()
+        L.moe_expert_ffn(cfg, bufs.X, bufs.offsets, inp.W_gate, inp.W_up, inp.W_down, bufs.act, bufs.Y, bufs.ws)
+        if ev is not None:
+            ev[2].record()
+        L.moe_combine(cfg, U, bufs.Y, bufs.slot_row, bufs.gate, bufs.counts_routed, bufs.out, bufs.f, bufs.P,
+                      bufs.aux, bufs.ws)
+
+    # kept pairs and active experts of each batch (outside any timed region)
+    A_of, act_of = [], []
+    for U in pool:
+        stage_calls(U)
+        off = bufs.offsets.cpu()
+        A_of.append(int(off[-1]))
+        act_of.append(int(((off[1:] - off[:-1]) > 0).sum()))
+    code = L.moe_get_device_status(bufs.ws)
+    if code != 0:
+        raise SystemExit(f"bench.py: device status {code} during warm-up")
+
+    for i in range(args.warmup):
+        stage_calls(pool[i % n_rot])
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(device) if rank == 0 else None
+    barrier(device)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(device)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        starts[i].record()
+        stage_calls(pool[i % n_rot], evs[i])
+        ends[i].record()
+    t_end.record()
+    barrier(device)
+    total_ms = t_start.elapsed_time(t_end)
+
+    # end to end through the public call: pinned host tokens in, out (and aux) back, every step
+    U_host = [torch.empty((w.T, w.h), dtype=w.torch_dtype, pin_memory=True) for _ in range(2)]
+    for j in range(2):
+        U_host[j].copy_(pool[j])
+    out_host = torch.empty((w.T, w.h), dtype=w.torch_dtype, pin_memory=True)
+    aux_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    U_dev = torch.empty_like(inp.U)
+
+    def e2e_step(j):
+        U_dev.copy_(U_host[j % 2], non_blocking=True)
+        L.moe_layer_forward(cfg, U_dev, inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up, inp.W_down,
+                            bufs)
+        out_host.copy_(bufs.out, non_blocking=True)
+        aux_host.copy_(bufs.aux, non_blocking=True)
+
+    for j in range(3):
+        e2e_step(j)
+    barrier(device)
+    t0 = time.perf_counter()
+    for j in range(K):
+        e2e_step(j)
+    torch.cuda.synchronize(device)
+    e2e_s = time.perf_counter() - t0
+    barrier(device)
+    clk = clocks.stop() if clocks else None
+    code = L.moe_get_device_status(bufs.ws)
+    if code != 0:
+        raise SystemExit(f"bench.py: device status {code} after the timed region")
+
+    max_ms = max_over_ranks(total_ms, device)
+    max_e2e = max_over_ranks(e2e_s, device)
+    if rank != 0:
+        return 0
+
+    stage_ms = {"route": [], "dispatch": [], "ffn": [], "combine": []}
+    for i in range(K):
+        e = evs[i]
+        stage_ms["route"].append(starts[i].elapsed_time(e[0]))
+        stage_ms["dispatch"].append(e[0].elapsed_time(e[1]))
+        stage_ms["ffn"].append(e[1].elapsed_time(e[2]))
+        stage_ms["combine"].append(e[2].elapsed_time(ends[i]))
+    A_mean = sum(A_of[i % n_rot] for i in range(K)) / K
+    act_mean = sum(act_of[i % n_rot] for i in range(K)) / K
+    work = stage_work(w, A_mean, act_mean)
+    peaks, peak_src = measured_peaks()
+    stages = {}
+    for name, ms in stage_ms.items():
+        m = sum(ms) / len(ms)
+        wk = work[name]
+        gbs = wk["bytes"] / (m * 1e-3) / 1e9
+        d = {"ms": round(m, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        if wk["flops"]:
+            tf = wk["flops"] / (m * 1e-3) / 1e12
+            d["TFLOP/s"] = round(tf, 2)
+            d["frac_tensor"] = round(tf / peaks["bf16_tflops"], 4)
+        stages[name] = d
+
+    ffn_ms = sum(stage_ms["ffn"]) / K
+    ffn = work["ffn"]
+    intensity = ffn["flops"] / max(ffn["bytes"], 1)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if w.dtype == W.F32:
+        # float32 CUDA-core FMA peak: 148 SMs x 128 lanes x 2 FLOP x 2.032 GHz
+        roof = {"bound": "alu", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12,
+                "peak": 148 * 128 * 2 * 2.032e9 / 1e12, "unit": "TFLOP/s"}
+    elif intensity >= ridge:
+        roof = {"bound": "tensor", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": ffn["bytes"] / (ffn_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["achieved"] = round(roof["achieved"], 2)
+    roof["traffic"] = profile_traffic(w.name)
+    roof["kernel"] = "grouped SwiGLU expert GEMM: grouped_gemm_tc gate|up + down, both launches of one step"
+    roof["peak_source"] = f"{peak_src}, {'bf16 burst' if roof['bound'] == 'tensor' else roof['bound']}"
+
+    value = weak_scaling_value(w.T, K, ws_n, max_ms * 1e-3)
+    e2e_value = weak_scaling_value(w.T, K, ws_n, max_e2e)
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_n, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(max_ms / K, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
+            "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, device-resident)",
+            "config": workload_config(w, n_rot),
+            "roofline": roof, "stages": stages,
+            "kept_pairs_A": A_mean, "active_experts": act_mean,
+            "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": w.T * w.h * w.elem_bytes,
+                    "d2h_bytes_per_step": w.T * w.h * w.elem_bytes + 4},
+            "gpu_launches": launches_per_step(w) * K,
+            "clocks": clk}
+    if ws_n == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample_tokens or default_cpu_sample(w))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def default_cpu_sample(w: W.Workload) -> int:
+    return {"tiny_fp32": 256, "mixtral_bf16": 96, "switch_noisy_bf16": 2048, "dsv3_bf16": 48,
+            "stress_bf16": 512}.get(w.name, 128)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=W.MIXTRAL.name, choices=sorted(W.BY_NAME))
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("bench.py: --warmup must be >= 3")
+    w = W.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_b300(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

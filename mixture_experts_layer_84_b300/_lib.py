@@ -1,0 +1,269 @@
+"""Thin ctypes binding of libmoe.so (include/moe.h).
+
+Argument marshalling only: torch tensors are checked for device, dtype,
+contiguity and size, and passed to the C ABI as raw pointers on the current
+CUDA stream.  Every step of the MoE layer runs in the library's kernels; if
+the library is missing this module raises at import, there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+from . import workloads as W
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(5)
+MOE_DEV_OK, MOE_DEV_BAD_EXPERT_ID, MOE_DEV_TIMEOUT, MOE_DEV_BAD_ROW, MOE_DEV_BAD_OFFSETS = range(5)
+
+EXPORTS = ("moe_version", "moe_status_string", "moe_last_error", "moe_capacity", "moe_workspace_size",
+           "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer_forward",
+           "moe_get_device_status")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_name(status)}: {message}")
+        self.status = status
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("h", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("d_e", ctypes.c_int32), ("capacity_factor", ctypes.c_float), ("capacity", ctypes.c_int32),
+                ("score_fn", ctypes.c_int32), ("renorm", ctypes.c_int32), ("noisy", ctypes.c_int32),
+                ("priority", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+
+
+class moe_layer_args(ctypes.Structure):
+    _fields_ = [(n, _P) for n in (
+        "U", "W_r", "b_r", "W_noise", "eps", "W_gate", "W_up", "W_down", "logits_out", "idx", "gate",
+        "counts_routed", "counts_kept", "offsets", "slot_row", "row_token", "n_dropped", "X", "act", "Y",
+        "out", "f", "P", "aux")]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run "
+                          "`python -m mixture_experts_layer_84_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    S, I64, SZ = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    cfgp = ctypes.POINTER(moe_config)
+    lib.moe_version.restype = ctypes.c_char_p
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_status_string.argtypes = [S]
+    lib.moe_last_error.restype = ctypes.c_char_p
+    lib.moe_capacity.restype = S
+    lib.moe_capacity.argtypes = [cfgp, ctypes.POINTER(I64)]
+    lib.moe_workspace_size.restype = S
+    lib.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(SZ)]
+    lib.moe_route.restype = S
+    lib.moe_route.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
+    lib.moe_dispatch.restype = S
+    lib.moe_dispatch.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
+    lib.moe_expert_ffn.restype = S
+    lib.moe_expert_ffn.argtypes = [cfgp] + [_P] * 7 + [_P, _P]
+    lib.moe_combine.restype = S
+    lib.moe_combine.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
+    lib.moe_layer_forward.restype = S
+    lib.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), _P, _P]
+    lib.moe_get_device_status.restype = S
+    lib.moe_get_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
+    return lib
+
+
+lib = _load()
+
+
+def status_name(status: int) -> str:
+    return lib.moe_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib.moe_version().decode()
+
+
+def _check(status: int) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, lib.moe_last_error().decode())
+
+
+def config(T, h, E, k, d_e, *, capacity_factor=0.0, capacity=0, score_fn=W.SOFTMAX, renorm=True, noisy=False,
+           priority=W.PRIORITY_CHOICE_MAJOR, dtype=W.BF16) -> moe_config:
+    return moe_config(int(T), int(h), int(E), int(k), int(d_e), float(capacity_factor), int(capacity),
+                      int(score_fn), int(bool(renorm)), int(bool(noisy)), int(priority), int(dtype))
+
+
+def config_of(w: W.Workload, **override) -> moe_config:
+    kw = dict(capacity_factor=w.capacity_factor, capacity=w.capacity, score_fn=w.score_fn, renorm=w.renorm,
+              noisy=w.noisy, priority=w.priority, dtype=w.dtype)
+    kw.update(override)
+    T = kw.pop("T", w.T)
+    return config(T, w.h, w.E, w.k, w.d_e, **kw)
+
+
+def capacity(cfg: moe_config) -> int:
+    c = ctypes.c_int64()
+    _check(lib.moe_capacity(ctypes.byref(cfg), ctypes.byref(c)))
+    return c.value
+
+
+def workspace_size(cfg: moe_config) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def _act_dtype(cfg: moe_config):
+    return torch.bfloat16 if cfg.dtype == W.BF16 else torch.float32
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, numel: Optional[int] = None) -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, need {numel}")
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(stream) -> Optional[int]:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream if s.cuda_stream else None
+
+
+def new_workspace(cfg: moe_config, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of moe_workspace_size() bytes (256-byte aligned by the allocator)."""
+    return torch.zeros(max(workspace_size(cfg), 256), dtype=torch.uint8, device=device)
+
+
+def moe_route(cfg, U, W_r, b_r, W_noise, eps, logits_in, logits_out, idx, gate, ws, stream=None):
+    dt = _act_dtype(cfg)
+    T, E, k, h = cfg.T, cfg.E, cfg.k, cfg.h
+    _check(lib.moe_route(ctypes.byref(cfg), _ptr(U, "U", dt, T * h) if logits_in is None else None,
+                         _ptr(W_r, "W_r", dt, h * E) if logits_in is None else None,
+                         _ptr(b_r, "b_r", torch.float32, E), _ptr(W_noise, "W_noise", dt, h * E),
+                         _ptr(eps, "eps", torch.float32, T * E), _ptr(logits_in, "logits_in", torch.float32, T * E),
+                         _ptr(logits_out, "logits_out", torch.float32, T * E), _ptr(idx, "idx", torch.int32, T * k),
+                         _ptr(gate, "gate", torch.float32, T * k), _ptr(ws, "ws"), _stream(stream)))
+
+
+def moe_dispatch(cfg, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, X, n_dropped, ws,
+                 stream=None):
+    dt = _act_dtype(cfg)
+    T, E, k, h = cfg.T, cfg.E, cfg.k, cfg.h
+    _check(lib.moe_dispatch(ctypes.byref(cfg), _ptr(U, "U", dt, T * h), _ptr(idx, "idx", torch.int32, T * k),
+                            _ptr(counts_routed, "counts_routed", torch.int32, E),
+                            _ptr(counts_kept, "counts_kept", torch.int32, E),
+                            _ptr(offsets, "offsets", torch.int32, E + 1),
+                            _ptr(slot_row, "slot_row", torch.int32, T * k),
+                            _ptr(row_token, "row_token", torch.int32, T * k), _ptr(X, "X", dt, T * k * h),
+                            _ptr(n_dropped, "n_dropped", torch.int64, 1), _ptr(ws, "ws"), _stream(stream)))
+
+
+def moe_expert_ffn(cfg, X, offsets, W_gate, W_up, W_down, act, Y, ws, stream=None):
+    dt = _act_dtype(cfg)
+    T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
+    _check(lib.moe_expert_ffn(ctypes.byref(cfg), _ptr(X, "X", dt, T * k * h),
+                              _ptr(offsets, "offsets", torch.int32, E + 1), _ptr(W_gate, "W_gate", dt, E * d * h),
+                              _ptr(W_up, "W_up", dt, E * d * h), _ptr(W_down, "W_down", dt, E * h * d),
+                              _ptr(act, "act", dt, T * k * d), _ptr(Y, "Y", dt, T * k * h), _ptr(ws, "ws"),
+                              _stream(stream)))
+
+
+def moe_combine(cfg, U, Y, slot_row, gate, counts_routed, out, f, P, aux, ws, stream=None):
+    dt = _act_dtype(cfg)
+    T, E, k, h = cfg.T, cfg.E, cfg.k, cfg.h
+    _check(lib.moe_combine(ctypes.byref(cfg), _ptr(U, "U", dt, T * h), _ptr(Y, "Y", dt, T * k * h),
+                           _ptr(slot_row, "slot_row", torch.int32, T * k), _ptr(gate, "gate", torch.float32, T * k),
+                           _ptr(counts_routed, "counts_routed", torch.int32, E), _ptr(out, "out", dt, T * h),
+                           _ptr(f, "f", torch.float32, E), _ptr(P, "P", torch.float32, E),
+                           _ptr(aux, "aux", torch.float32, 1), _ptr(ws, "ws"), _stream(stream)))
+
+
+@dataclasses.dataclass
+class LayerBuffers:
+    """Device buffers for every output of one layer forward (capacity-sized X, act, Y)."""
+    idx: torch.Tensor
+    gate: torch.Tensor
+    logits: Optional[torch.Tensor]
+    counts_routed: torch.Tensor
+    counts_kept: torch.Tensor
+    offsets: torch.Tensor
+    slot_row: torch.Tensor
+    row_token: torch.Tensor
+    n_dropped: torch.Tensor
+    X: torch.Tensor
+    act: torch.Tensor
+    Y: torch.Tensor
+    out: torch.Tensor
+    f: torch.Tensor
+    P: torch.Tensor
+    aux: torch.Tensor
+    ws: torch.Tensor
+
+    @staticmethod
+    def allocate(cfg: moe_config, device="cuda", with_logits: bool = False) -> "LayerBuffers":
+        dt = _act_dtype(cfg)
+        T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
+        i32, f32 = torch.int32, torch.float32
+        return LayerBuffers(
+            idx=torch.empty((T, k), dtype=i32, device=device), gate=torch.empty((T, k), dtype=f32, device=device),
+            logits=torch.empty((T, E), dtype=f32, device=device) if with_logits else None,
+            counts_routed=torch.empty(E, dtype=i32, device=device),
+            counts_kept=torch.empty(E, dtype=i32, device=device),
+            offsets=torch.empty(E + 1, dtype=i32, device=device),
+            slot_row=torch.empty(T * k, dtype=i32, device=device),
+            row_token=torch.empty(T * k, dtype=i32, device=device),
+            n_dropped=torch.empty(1, dtype=torch.int64, device=device),
+            X=torch.empty((T * k, h), dtype=dt, device=device), act=torch.empty((T * k, d), dtype=dt, device=device),
+            Y=torch.empty((T * k, h), dtype=dt, device=device), out=torch.empty((T, h), dtype=dt, device=device),
+            f=torch.empty(E, dtype=f32, device=device), P=torch.empty(E, dtype=f32, device=device),
+            aux=torch.empty(1, dtype=f32, device=device), ws=new_workspace(cfg, device))
+
+
+def moe_layer_forward(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: LayerBuffers, stream=None):
+    dt = _act_dtype(cfg)
+    T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
+    a = moe_layer_args(
+        U=_ptr(U, "U", dt, T * h), W_r=_ptr(W_r, "W_r", dt, h * E), b_r=_ptr(b_r, "b_r", torch.float32, E),
+        W_noise=_ptr(W_noise, "W_noise", dt, h * E), eps=_ptr(eps, "eps", torch.float32, T * E),
+        W_gate=_ptr(W_gate, "W_gate", dt, E * d * h), W_up=_ptr(W_up, "W_up", dt, E * d * h),
+        W_down=_ptr(W_down, "W_down", dt, E * h * d),
+        logits_out=_ptr(bufs.logits, "logits", torch.float32, T * E),
+        idx=_ptr(bufs.idx, "idx", torch.int32, T * k), gate=_ptr(bufs.gate, "gate", torch.float32, T * k),
+        counts_routed=_ptr(bufs.counts_routed, "counts_routed", torch.int32, E),
+        counts_kept=_ptr(bufs.counts_kept, "counts_kept", torch.int32, E),
+        offsets=_ptr(bufs.offsets, "offsets", torch.int32, E + 1),
+        slot_row=_ptr(bufs.slot_row, "slot_row", torch.int32, T * k),
+        row_token=_ptr(bufs.row_token, "row_token", torch.int32, T * k),
+        n_dropped=_ptr(bufs.n_dropped, "n_dropped", torch.int64, 1),
+        X=_ptr(bufs.X, "X", dt, T * k * h), act=_ptr(bufs.act, "act", dt, T * k * d),
+        Y=_ptr(bufs.Y, "Y", dt, T * k * h), out=_ptr(bufs.out, "out", dt, T * h),
+        f=_ptr(bufs.f, "f", torch.float32, E), P=_ptr(bufs.P, "P", torch.float32, E),
+        aux=_ptr(bufs.aux, "aux", torch.float32, 1))
+    _check(lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(a), _ptr(bufs.ws, "ws"), _stream(stream)))
+
+
+def moe_get_device_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the workspace's device status code."""
+    code = ctypes.c_int32()
+    st = lib.moe_get_device_status(_ptr(ws, "ws"), _stream(stream), ctypes.byref(code))
+    if st not in (MOE_OK, MOE_ERR_DEVICE):
+        _check(st)
+    return code.value

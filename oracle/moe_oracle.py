@@ -305,29 +305,38 @@ def layer_forward(inp, *, T, h, E, k, d_e, score_fn, renorm, capacity_factor,
 
 
 def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int) -> dict:
-    """out rows (and the Y rows they use) for a sample of tokens, computed one by one.
+    """out rows (and the Y rows they use) for a sample of tokens.
 
     For full-size checks: X[row] = U[t] for a kept pair, so each needed Y row
     is one expert applied to one token row ([FFN]); out follows [FFN]'s layer
-    output.  Returns {"out": [n, h], "Y": {row: [h]}}.
+    output.  The sampled rows are grouped by expert so that each expert's
+    weights are read (and widened to float64) once.
+    Returns {"out": [n, h], "Y": {row: [h]}}.
     """
-    tokens = np.asarray(tokens, dtype=np.int64)
+    tokens = [int(t) for t in tokens]
     idx = np.asarray(idx, dtype=np.int64)
     gate = f64(gate)
     sr = np.asarray(slot_row, dtype=np.int64).reshape(-1, k)
+    U = {t: f64(inp.U[t]) for t in tokens}
+    by_expert = {}
+    for t in tokens:
+        for j in range(k):
+            if sr[t, j] >= 0:
+                by_expert.setdefault(int(idx[t, j]), []).append((t, j))
+    y_of = {}
+    for e, pairs in sorted(by_expert.items()):
+        x = np.stack([U[t] for t, _ in pairs])
+        y, _ = swiglu(x, inp.W_gate[e], inp.W_up[e], inp.W_down[e])
+        for (t, j), row in zip(pairs, y):
+            y_of[(t, j)] = row
     outs, Yrows = [], {}
     for t in tokens:
-        u = f64(inp.U[int(t)]).reshape(1, -1)
-        acc = u.copy()
+        acc = U[t].copy()
         for j in range(k):
-            row = int(sr[t, j])
-            if row < 0:
-                continue
-            e = int(idx[t, j])
-            y, _ = swiglu(u, inp.W_gate[e], inp.W_up[e], inp.W_down[e])
-            Yrows[row] = y[0]
-            acc = acc + gate[t, j] * y
-        outs.append(acc[0])
+            if sr[t, j] >= 0:
+                Yrows[int(sr[t, j])] = y_of[(t, j)]
+                acc = acc + gate[t, j] * y_of[(t, j)]
+        outs.append(acc)
     return dict(out=np.stack(outs) if outs else np.zeros((0, 0)), Y=Yrows)
 
 

@@ -1,0 +1,74 @@
+"""Shared pieces of the GPU parity tests: margin-safe inputs, error measures.
+
+The oracle decides every expected value; the library's outputs are only ever
+compared against it (or against properties that hold at any size).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from mixture_experts_layer_84_b300 import synth
+from mixture_experts_layer_84_b300 import workloads as W
+
+# Output tolerances: normwise max relative error max|a-b| / max|b|.
+TOL = {W.F32: 1e-5, W.BF16: 2e-2}
+LOGIT_TOL = 1e-5     # float32 logits, gates and statistics on both dtypes
+MARGIN = 1e-3        # every adjacent gap among the top-(k+1) logits of a token
+ULP_BITS = {W.F32: 23, W.BF16: 7}
+
+
+def f64(x):
+    return oracle.f64(x)
+
+
+def normwise(a, b) -> float:
+    a, b = f64(a), f64(b)
+    if a.size == 0:
+        return 0.0
+    den = float(np.max(np.abs(b)))
+    num = float(np.max(np.abs(a - b)))
+    return num / den if den > 0 else num
+
+
+def delta_error(out, U, out_ref, dtype) -> float:
+    """Normwise error of the expert contribution out - U against the oracle's.
+
+    The layer output is rounded once to its dtype at the scale of |out| (the
+    residual dominates it), so one unit in the last place of out is allowed
+    per element before the error is measured against max |out_ref - U|.
+    """
+    o, u, ref = f64(out), f64(U), f64(out_ref)
+    d, dref = o - u, ref - u
+    mag = np.maximum(np.abs(ref), np.finfo(np.float64).tiny)
+    ulp = 2.0 ** (np.floor(np.log2(mag)) - ULP_BITS[dtype])
+    excess = np.maximum(np.abs(d - dref) - ulp, 0.0)
+    if excess.size == 0:
+        return 0.0
+    den = float(np.max(np.abs(dref)))
+    return float(np.max(excess)) / den if den > 0 else float(np.max(excess))
+
+
+def logits_of(w: W.Workload, inp, rows=None) -> np.ndarray:
+    if rows is None:
+        return oracle.router_logits(inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps)
+    r = torch.as_tensor(rows, device=inp.U.device)
+    return oracle.router_logits(inp.U[r], inp.W_r, inp.b_r, inp.W_noise,
+                                None if inp.eps is None else inp.eps[r])
+
+
+def margin_inputs(w: W.Workload, seed: int = 0, device="cuda", experts: bool = True, max_rounds: int = 30):
+    """Layer inputs whose tokens all keep a top-(k+1) logit margin >= MARGIN (in float64).
+
+    Tokens that violate it get fresh U (and eps) rows; returns (inputs, float64 logits).
+    """
+    inp = synth.generate(w, seed, device, experts=experts)
+    H = logits_of(w, inp)
+    for attempt in range(max_rounds):
+        bad = np.nonzero(oracle.topk_margins(H, w.k) < MARGIN)[0]
+        if bad.size == 0:
+            return inp, H
+        synth.redraw_rows(inp, torch.as_tensor(bad, dtype=torch.int64), seed, attempt)
+        H[bad] = logits_of(w, inp, bad)
+    raise RuntimeError(f"could not reach the top-k margin for {w.name}")

@@ -1,0 +1,77 @@
+"""moe_expert_ffn against the oracle: the grouped SwiGLU over ragged expert segments
+(tcgen05 for bf16, CUDA cores for float32)."""
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import TOL, normwise
+from mixture_experts_layer_84_b300 import _lib as L
+from mixture_experts_layer_84_b300 import synth
+from mixture_experts_layer_84_b300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+EDGE = [
+    # h and d_e off the 64/128 grid: K tails and an output-column tail
+    W.Workload("ffn_tails_bf16", T=333, h=136, E=6, k=2, d_e=200, dtype=W.BF16, score_fn=W.SOFTMAX, renorm=True,
+               noisy=False, capacity_factor=0.0),
+    W.Workload("ffn_one_expert_bf16", T=300, h=256, E=1, k=1, d_e=128, dtype=W.BF16, score_fn=W.SOFTMAX,
+               renorm=True, noisy=False, capacity_factor=0.0),
+    W.Workload("ffn_many_small_bf16", T=700, h=320, E=96, k=3, d_e=384, dtype=W.BF16, score_fn=W.SIGMOID,
+               renorm=True, noisy=False, capacity_factor=0.0),
+    W.Workload("ffn_tails_f32", T=123, h=72, E=5, k=2, d_e=40, dtype=W.F32, score_fn=W.SOFTMAX, renorm=True,
+               noisy=False, capacity_factor=0.0),
+]
+
+
+def segments(w, seed, zipf):
+    idx = synth.random_routing(w.T, w.E, w.k, seed=seed, zipf_s=zipf).numpy()
+    C = oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.capacity)
+    return oracle.dispatch(idx, w.E, C, w.priority)
+
+
+@pytest.mark.parametrize("w", W.SMALL + EDGE, ids=lambda w: w.name)
+@pytest.mark.parametrize("zipf", [0.0, 1.2])
+def test_expert_ffn(w, zipf):
+    inp = synth.generate(w, seed=2, device="cuda")
+    d = segments(w, seed=9, zipf=zipf)
+    A = int(d["offsets"][-1])
+    Tk = w.T * w.k
+    X = torch.zeros((Tk, w.h), dtype=w.torch_dtype, device="cuda")
+    X[:A] = inp.U[torch.as_tensor(d["row_token"], device="cuda")]
+    offsets = torch.as_tensor(d["offsets"], dtype=torch.int32, device="cuda")
+    act = torch.full((Tk, w.d_e), 7.0, dtype=w.torch_dtype, device="cuda")
+    Y = torch.full((Tk, w.h), 7.0, dtype=w.torch_dtype, device="cuda")
+    cfg = L.config_of(w)
+    ws = L.new_workspace(cfg)
+    L.moe_expert_ffn(cfg, X, offsets, inp.W_gate, inp.W_up, inp.W_down, act, Y, ws)
+    assert L.moe_get_device_status(ws) == 0
+    Y_ref, act_ref = oracle.expert_ffn(X[:A], d["offsets"], inp.W_gate, inp.W_up, inp.W_down, w.d_e)
+    tol = TOL[w.dtype]
+    assert normwise(act[:A], act_ref) <= tol
+    assert normwise(Y[:A], Y_ref) <= tol
+    # per expert as well, so a small expert cannot hide behind a large one
+    for e in range(w.E):
+        lo, hi = int(d["offsets"][e]), int(d["offsets"][e + 1])
+        if hi > lo:
+            assert normwise(Y[lo:hi], Y_ref[lo:hi]) <= tol, e
+    # rows >= A are not written
+    assert torch.all(Y[A:] == 7.0) and torch.all(act[A:] == 7.0)
+
+
+@pytest.mark.parametrize("dtype", [W.BF16, W.F32])
+def test_expert_ffn_rejects_inconsistent_offsets(dtype):
+    w = W.Workload("bad", T=64, h=64, E=4, k=2, d_e=64, dtype=dtype, score_fn=0, renorm=True, noisy=False,
+                   capacity_factor=0.0)
+    inp = synth.generate(w, seed=2, device="cuda")
+    Tk = w.T * w.k
+    X = torch.zeros((Tk, w.h), dtype=w.torch_dtype, device="cuda")
+    act = torch.full((Tk, w.d_e), 7.0, dtype=w.torch_dtype, device="cuda")
+    Y = torch.full((Tk, w.h), 7.0, dtype=w.torch_dtype, device="cuda")
+    cfg = L.config_of(w)
+    ws = L.new_workspace(cfg)
+    for bad in ([0, 10, 5, 20, 30], [0, 10, 20, 30, Tk + 1], [-4, 10, 20, 30, 40]):
+        offsets = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        L.moe_expert_ffn(cfg, X, offsets, inp.W_gate, inp.W_up, inp.W_down, act, Y, ws)
+        assert L.moe_get_device_status(ws) == L.MOE_DEV_BAD_OFFSETS
+        assert torch.all(Y == 7.0) and torch.all(act == 7.0)
