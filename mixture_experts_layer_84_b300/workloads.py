@@ -80,5 +80,9 @@ STRESS_SMALL = STRESS.replace(name="stress_small", T=3000, h=256, d_e=192)
 
 SMALL = [TINY_FP32, MIXTRAL_SMALL, SWITCH_SMALL, DSV3_SMALL, STRESS_SMALL]
 
-BY_NAME = {w.name: w for w in FULL + SMALL}
+# Mixtral-shaped with a quarter of d_e: the same kernels and tiles with about
+# 1 GB on the device, for detailed hardware-counter captures.
+MIXTRAL_NARROW = MIXTRAL.replace(name="mixtral_narrow_bf16", d_e=3584)
+
+BY_NAME = {w.name: w for w in FULL + SMALL + [MIXTRAL_NARROW]}
 
