@@ -31,7 +31,8 @@
  *   Memory: every array argument is a DEVICE pointer, 16-byte aligned, owned
  *   by the caller, unless stated otherwise.  The library never allocates,
  *   frees or synchronises (moe_get_device_status excepted) and keeps no
- *   global state; all work is enqueued on the caller's stream in order.
+ *   global state apart from the static histogram of moe_dispatch_noalloc;
+ *   all work is enqueued on the caller's stream in order.
  *   Workspace: `ws` is caller-owned device scratch of moe_workspace_size()
  *   bytes, 256-byte aligned, zero-filled once after allocation.  It carries
  *   the device status word and the per-block partial sums one stage hands to
@@ -154,6 +155,42 @@ moe_status moe_dispatch(const moe_config* cfg, const void* U, const int32_t* idx
                         int32_t* counts_routed, int32_t* counts_kept, int32_t* offsets,
                         int32_t* slot_row, int32_t* row_token, void* X, int64_t* n_dropped,
                         void* ws, moe_stream_t stream);
+
+/* moe_dispatch for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it is a deployment variant of
+ * moe_dispatch.  Some callers are not allowed to allocate device memory at
+ * all: an engine that reserves its whole device memory up front and forbids
+ * allocation once it is serving, a plugin whose host framework hands it tensors
+ * but offers no scratch allocator, or code that must not pay for an allocation
+ * (nor risk one failing) on the hot path.  This entry point needs no `ws`: the
+ * only scratch dispatch uses, the per-chunk expert histogram, sits in a
+ * file-scope device array inside libmoe of MOE_NOALLOC_HIST_MAX int32 (4 MiB).
+ * Every GPU that loads the library keeps that array until the process exits.
+ * The call makes no cudaMalloc or cudaFree and calls no allocating routine.
+ *
+ *   Arguments and results are those of moe_dispatch, bit for bit, except:
+ *   status   [1] int32 device out or NULL: zeroed by the call, then set to a
+ *            MOE_DEV_* code (an expert id outside [0, E) -> MOE_DEV_BAD_EXPERT_ID,
+ *            that pair dropped).  NULL: device-side errors are not reported.
+ *   Size limit: ceil(T*k / 4096) * E <= MOE_NOALLOC_HIST_MAX, else
+ *            MOE_ERR_UNSUPPORTED before anything is enqueued (for E = 1024 that
+ *            is T*k <= 4 Mi pairs).
+ *   Shared scratch: every call on a device uses the same array and leaves its
+ *            contents behind; each call rewrites all it reads, so no clearing is
+ *            needed between calls.  Calls whose work overlaps on the GPU (on
+ *            streams with no ordering between them) race on the array and give
+ *            wrong results: order them on one stream or with events.
+ *   First call per device: it looks up the array's device address on the
+ *            current device (cudaGetSymbolAddress) and caches it.  Make that
+ *            first call before any stream capture begins.
+ *   The current device must be the device that `stream` and every pointer
+ *   belong to. */
+#define MOE_NOALLOC_HIST_MAX (1 << 20)
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* U, const int32_t* idx,
+                                int32_t* counts_routed, int32_t* counts_kept, int32_t* offsets,
+                                int32_t* slot_row, int32_t* row_token, void* X, int64_t* n_dropped,
+                                int32_t* status, moe_stream_t stream);
 
 /* Grouped SwiGLU expert FFN over the expert segments of X.
  * Section 从稠密 FFN 到 MoE (the expert) and section 专家计算：padding、block-sparse

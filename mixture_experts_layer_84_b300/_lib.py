@@ -23,8 +23,8 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE =
 MOE_DEV_OK, MOE_DEV_BAD_EXPERT_ID, MOE_DEV_TIMEOUT, MOE_DEV_BAD_ROW, MOE_DEV_BAD_OFFSETS = range(5)
 
 EXPORTS = ("moe_version", "moe_status_string", "moe_last_error", "moe_capacity", "moe_workspace_size",
-           "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_layer_forward",
-           "moe_get_device_status")
+           "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine",
+           "moe_layer_forward", "moe_get_device_status")
 
 
 class MoeError(RuntimeError):
@@ -69,6 +69,8 @@ def _load() -> ctypes.CDLL:
     lib.moe_route.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
     lib.moe_dispatch.restype = S
     lib.moe_dispatch.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
+    lib.moe_dispatch_noalloc.restype = S
+    lib.moe_dispatch_noalloc.argtypes = [cfgp] + [_P] * 10 + [_P]
     lib.moe_expert_ffn.restype = S
     lib.moe_expert_ffn.argtypes = [cfgp] + [_P] * 7 + [_P, _P]
     lib.moe_combine.restype = S
@@ -174,6 +176,22 @@ def moe_dispatch(cfg, U, idx, counts_routed, counts_kept, offsets, slot_row, row
                             _ptr(slot_row, "slot_row", torch.int32, T * k),
                             _ptr(row_token, "row_token", torch.int32, T * k), _ptr(X, "X", dt, T * k * h),
                             _ptr(n_dropped, "n_dropped", torch.int64, 1), _ptr(ws, "ws"), _stream(stream)))
+
+
+def moe_dispatch_noalloc(cfg, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, X, n_dropped,
+                         status=None, stream=None):
+    """moe_dispatch without a workspace: the histogram scratch is the library's static device array."""
+    dt = _act_dtype(cfg)
+    T, E, k, h = cfg.T, cfg.E, cfg.k, cfg.h
+    _check(lib.moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(U, "U", dt, T * h),
+                                    _ptr(idx, "idx", torch.int32, T * k),
+                                    _ptr(counts_routed, "counts_routed", torch.int32, E),
+                                    _ptr(counts_kept, "counts_kept", torch.int32, E),
+                                    _ptr(offsets, "offsets", torch.int32, E + 1),
+                                    _ptr(slot_row, "slot_row", torch.int32, T * k),
+                                    _ptr(row_token, "row_token", torch.int32, T * k), _ptr(X, "X", dt, T * k * h),
+                                    _ptr(n_dropped, "n_dropped", torch.int64, 1),
+                                    _ptr(status, "status", torch.int32, 1), _stream(stream)))
 
 
 def moe_expert_ffn(cfg, X, offsets, W_gate, W_up, W_down, act, Y, ws, stream=None):

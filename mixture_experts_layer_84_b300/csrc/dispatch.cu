@@ -23,6 +23,7 @@
 //   dispatch_scatter one warp per token, 16-byte copies: each U row is read
 //                    once and written to the (up to k) rows it was kept in.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -268,6 +269,84 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
   if (e != cudaSuccess) return e;
   const int elem = p.bf16 ? 2 : 4;
   const int vpr = p.h * elem / 16;
+  const int64_t want = (p.T + 7) / 8;
+  const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(current_sm_count()) * 8));
+  dispatch_scatter<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), slot_row, static_cast<uint4*>(X), p.T, p.k,
+                                          vpr);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Dispatch without a caller-provided workspace (moe_dispatch_noalloc).
+//
+// The only scratch dispatch needs is the per-chunk histogram, [n_chunks, E]
+// int32.  Here it lives in one file-scope device array instead of the
+// workspace, so the caller allocates nothing beyond its inputs and outputs.
+// The array exists once per device for as long as the library is loaded, and
+// every call on a device shares it.  dispatch_count rewrites every entry a call
+// reads before the scan reads it, so nothing in it has to start at zero.  Calls
+// that overlap on the GPU (different streams, no ordering between them) race on
+// it.
+static __device__ __align__(256) int32_t g_noalloc_hist[MOE_NOALLOC_HIST_MAX];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_hist on the current device, looked up once per
+// device.  In host code the array's name is only a host-side stand-in, so the
+// kernels get this address, never the name.
+cudaError_t noalloc_hist_ptr(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_hist);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_noalloc(const Plan& p, const void* U, const int32_t* idx, int32_t* counts_routed,
+                                    int32_t* counts_kept, int32_t* offsets, int32_t* slot_row, int32_t* row_token,
+                                    void* X, int64_t* n_dropped, int32_t* status, cudaStream_t s) {
+  if (static_cast<int64_t>(p.n_chunks) * p.E > MOE_NOALLOC_HIST_MAX) return cudaErrorInvalidValue;
+  int32_t* hist = nullptr;
+  cudaError_t e = noalloc_hist_ptr(&hist);
+  if (e != cudaSuccess) return e;
+  if (status) {
+    e = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
+  }
+  if (p.n_chunks > 0) {
+    dispatch_count<<<p.n_chunks, DISPATCH_THREADS, sizeof(int32_t) * p.E, s>>>(idx, p.T, p.k, p.E, p.priority,
+                                                                               p.chunk, hist, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  int epow = 1;
+  while (epow < p.E) epow <<= 1;
+  int G = SCAN_THREADS / epow;
+  if (G > p.n_chunks) G = p.n_chunks > 0 ? p.n_chunks : 1;
+  if (G < 1) G = 1;
+  dispatch_scan<<<1, SCAN_THREADS, 0, s>>>(hist, p.n_chunks, p.E, G, p.C, p.Tk, counts_routed, counts_kept, offsets,
+                                           n_dropped);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_chunks == 0) return e;
+  dispatch_assign<<<p.n_chunks, DISPATCH_THREADS, sizeof(int32_t) * DISPATCH_WARPS * p.E, s>>>(
+      idx, p.T, p.k, p.E, p.priority, p.chunk, hist, offsets, p.C, slot_row, row_token);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int vpr = p.h * (p.bf16 ? 2 : 4) / 16;
   const int64_t want = (p.T + 7) / 8;
   const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(current_sm_count()) * 8));
   dispatch_scatter<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), slot_row, static_cast<uint4*>(X), p.T, p.k,

@@ -53,6 +53,12 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
                             int32_t* counts_kept, int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* X,
                             int64_t* n_dropped, uint8_t* ws, cudaStream_t s);
 
+// moe_dispatch with the histogram in the library's static device array (no workspace);
+// status (nullable) is zeroed, then receives MOE_DEV_* codes.
+cudaError_t launch_dispatch_noalloc(const Plan& p, const void* U, const int32_t* idx, int32_t* counts_routed,
+                                    int32_t* counts_kept, int32_t* offsets, int32_t* slot_row, int32_t* row_token,
+                                    void* X, int64_t* n_dropped, int32_t* status, cudaStream_t s);
+
 cudaError_t launch_expert_ffn(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                               const void* W_up, const void* W_down, void* act, void* Y, uint8_t* ws, cudaStream_t s);
 

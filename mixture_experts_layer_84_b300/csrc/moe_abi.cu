@@ -302,6 +302,34 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* U, const int3
   return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
 }
 
+MOE_API moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* U, const int32_t* idx,
+                                        int32_t* counts_routed, int32_t* counts_kept, int32_t* offsets,
+                                        int32_t* slot_row, int32_t* row_token, void* X, int64_t* n_dropped,
+                                        int32_t* status, moe_stream_t stream) {
+  static const char* fn = "moe_dispatch_noalloc";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  const int64_t hist = static_cast<int64_t>(p.n_chunks) * p.E;
+  if (hist > MOE_NOALLOC_HIST_MAX)
+    return moe::fail(MOE_ERR_UNSUPPORTED,
+                     "%s: ceil(T*k/%d) * E = %lld exceeds the static histogram of %d entries; use moe_dispatch", fn,
+                     p.chunk, static_cast<long long>(hist), MOE_NOALLOC_HIST_MAX);
+  const size_t es = p.bf16 ? 2 : 4;
+  CHECK(moe::check_ptr(fn, "U", U, static_cast<size_t>(p.T) * p.h * es, 16));
+  CHECK(moe::check_ptr(fn, "idx", idx, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "counts_routed", counts_routed, static_cast<size_t>(p.E) * 4, 4));
+  CHECK(moe::check_ptr(fn, "counts_kept", counts_kept, static_cast<size_t>(p.E) * 4, 4));
+  CHECK(moe::check_ptr(fn, "offsets", offsets, static_cast<size_t>(p.E + 1) * 4, 4));
+  CHECK(moe::check_ptr(fn, "slot_row", slot_row, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "row_token", row_token, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "X", X, static_cast<size_t>(p.Tk) * p.h * es, 16));
+  CHECK(moe::check_ptr(fn, "n_dropped", n_dropped, 8, 8));
+  CHECK(moe::check_ptr(fn, "status", status, 0, 4));
+  const cudaError_t e = moe::launch_dispatch_noalloc(p, U, idx, counts_routed, counts_kept, offsets, slot_row,
+                                                     row_token, X, n_dropped, status, stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
 MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const int32_t* offsets, const void* W_gate,
                                   const void* W_up, const void* W_down, void* act, void* Y, void* ws,
                                   moe_stream_t stream) {
