@@ -283,10 +283,22 @@ def cpu_baseline(w: W.Workload, inp, n_tokens: int):
 
 # ----------------------------------------------------------------------------- reference arm
 
+def ffn_tiles(w: W.Workload) -> str:
+    """The grouped-GEMM kernel libmoe picks: 256-row CTA-pair tiles when the mean expert segment is
+    at least 192 rows, else 128-row single-CTA tiles (MOE_FFN_TILES overrides)."""
+    env = os.environ.get("MOE_FFN_TILES", "")
+    if env in ("single", "pair"):
+        return env + " (MOE_FFN_TILES)"
+    if w.dtype == W.F32:
+        return "cuda-core float32"
+    return "pair" if w.T * w.k >= 1024 * w.E else "single"
+
+
 def workload_config(w: W.Workload, n_rot: int = 0):
     c = {"workload": w.name, "T": w.T, "h": w.h, "E": w.E, "k": w.k, "d_e": w.d_e,
          "score": "softmax" if w.score_fn == W.SOFTMAX else "sigmoid", "renorm": w.renorm, "noisy": w.noisy,
-         "capacity_factor": w.capacity_factor, "logit_bias": w.bias, "parallelism": "replicas"}
+         "capacity_factor": w.capacity_factor, "logit_bias": w.bias, "parallelism": "replicas",
+         "ffn_tiles": ffn_tiles(w)}
     if n_rot:
         c["l2"] = (f"inputs larger than L2: {n_rot} rotating token batches plus "
                    f"{3 * w.E * w.h * w.d_e * w.elem_bytes / 1e9:.2f} GB of expert weights per step")

@@ -28,6 +28,9 @@
 // tensor memory is freed and MOE_DEV_TIMEOUT is recorded in the status word.
 #include <cuda.h>
 
+#include <stdlib.h>
+#include <string.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -304,6 +307,266 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0 && *abort_flag) set_status(status, MOE_DEV_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// The same grouped GEMM on CTA pairs (cta_group::2): a cluster of two CTAs
+// computes a 256-row tile; each CTA stages its own 128 rows of A and one half
+// of the 256 B rows, so every stage is 32 KB per CTA instead of 48 KB, and the
+// shared-memory traffic per tensor-core cycle drops by a third.  The even CTA
+// issues the 256 x 256 x 16 MMAs for both; each CTA's tensor memory holds the
+// fp32 accumulator of its own 128 rows.  For the SwiGLU half the even CTA
+// stages the W_gate rows and the odd CTA the matching W_up rows, so
+// accumulator columns c and 128 + c are again gate and up of column c.
+//   full[s]   (even CTA) both CTAs' TMA bytes of stage s have landed
+//   empty[s]  (both)     the MMAs that read stage s are done (multicast commit)
+//   tfull[a]  (both)     accumulator a is complete (multicast commit)
+//   tempty[a] (even CTA) the 8 epilogue warps of the pair have read accumulator a
+constexpr int P_BM = 256;                        // rows per pair tile
+constexpr int P_STAGES = 6;
+constexpr uint32_t P_A_BYTES = 128 * BK * 2;     // 16 KB: this CTA's 128 rows
+constexpr uint32_t P_B_BYTES = 128 * BK * 2;     // 16 KB: this CTA's half of the 256 B rows
+constexpr uint32_t P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr size_t P_BAR_BYTES = 256;           // 17 mbarriers + tmem address + flags
+constexpr size_t P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + P_BAR_BYTES + sizeof(int) * (MAX_E + 1);
+static_assert(P_SMEM_BYTES <= 232448, "shared memory");
+static_assert((2 * P_STAGES + 2 + 2 + 1) * 8 + 12 <= P_BAR_BYTES, "barriers fit P_BAR_BYTES");
+
+__device__ __forceinline__ bool wait_cluster_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <bool SWIGLU>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    grouped_gemm_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                         const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets, int E, int K,
+                         int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out,
+                         int32_t* status) {
+  constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+  uint64_t* empty = full + P_STAGES;
+  uint64_t* tfull = empty + P_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* bad_flag = reinterpret_cast<int*>(tmem_holder + 2);
+  int* tab = reinterpret_cast<int*>(smem + P_STAGES * P_STAGE_BYTES + P_BAR_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool even = rank == 0;
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int ncl = static_cast<int>(gridDim.x >> 1);
+  const int NT = (n_out + TILE_N - 1) / TILE_N;
+  const int KB = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    *bad_flag = 0;
+  }
+  __syncthreads();
+  // both CTAs of a pair read the same offsets and reach the same decisions below
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int lo = offsets[e], hi = offsets[e + 1];
+    int m = 0;
+    if (lo < 0 || hi < lo || static_cast<int64_t>(hi) > rows_cap)
+      *bad_flag = 1;
+    else
+      m = (hi - lo + P_BM - 1) / P_BM;
+    tab[e + 1] = m;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tab[0] = 0;
+    for (int e = 0; e < E; ++e) tab[e + 1] += tab[e];
+    if (*bad_flag && blockIdx.x == 0) set_status(status, MOE_DEV_BAD_OFFSETS);
+    for (int s = 0; s < P_STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 8);
+    }
+    ptx::mbar_init(drain, 1);
+    ptx::fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (*bad_flag) return;
+  const int total = tab[E] * NT;
+  if (cid >= total) return;
+  // the peer's barriers must be initialised before anything can arrive on them
+  ptx::cluster_sync_all();
+
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB0);
+      if (SWIGLU) ptx::prefetch_tmap(&tmB1);
+      const CUtensorMap* tmB = (SWIGLU && !even) ? &tmB1 : &tmB0;
+      const uint64_t pol_a = ptx::policy_evict_last();
+      const uint64_t pol_b = ptx::policy_evict_normal();
+      uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < total; tile += ncl) {
+        int e, nt, mt;
+        decode_tile(tab, E, NT, tile, &e, &nt, &mt);
+        const int a_row = offsets[e] + mt * P_BM + static_cast<int>(rank) * 128;
+        const int b_row = SWIGLU ? e * b_rows_per_expert + nt * TILE_N
+                                 : e * b_rows_per_expert + nt * TILE_N + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + stage * P_STAGE_BYTES;
+          const uint32_t full_pair = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
+          if (even) ptx::mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
+          ptx::tma_load_2d_pair(sa, &tmA, kb * BK, a_row, full_pair, pol_a);
+          ptx::tma_load_2d_pair(sa + P_A_BYTES, tmB, kb * BK, b_row, full_pair, pol_b);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (even) {
+        // both CTAs' copies into every stage this CTA armed have landed before the pair may exit
+        for (int s = 0; s < P_STAGES; ++s)
+          if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_phase >> s) & 1u);
+      }
+      if (*abort_flag) {
+        // copies whose completion is counted in the other CTA cannot be awaited here: give them time
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (even && lane == 0) {
+      constexpr uint32_t IDESC = ptx::idesc_bf16_f32(P_BM, BN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < total; tile += ncl) {
+        if (!wait_cluster_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_cluster_bounded(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(stages + stage * P_STAGE_BYTES);
+          const uint32_t sb = sa + P_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            ptx::mma_bf16_ss_pair(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * UK * 2),
+                                  ptx::sdesc_kmajor_sw128(sb + kk * UK * 2), IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair(&empty[stage], 0x3);  // both CTAs' stage is free once these MMAs have read it
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair(&tfull[acc], 0x3);  // both halves of the accumulator are complete
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      ptx::mma_commit_pair(drain, 0x1);  // every MMA issued above has completed once this arrives
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    const int r_local = static_cast<int>(rank) * 128 + q * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = cid; tile < total; tile += ncl) {
+      int e, nt, mt;
+      decode_tile(tab, E, NT, tile, &e, &nt, &mt);
+      const int seg = offsets[e];
+      const int n_e = offsets[e + 1] - seg;
+      const bool row_ok = mt * P_BM + r_local < n_e;
+      const int64_t row = static_cast<int64_t>(seg) + mt * P_BM + r_local;
+      // the tcgen05.ld below is warp-collective: the warp leaves together or not at all
+      const bool ready = wait_cluster_bounded(&tfull[acc], acc_phase, abort_flag);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
+      bf16* orow = out + row * n_out;
+      if (SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t gv[32], uv[32], packed[16];
+          ptx::tmem_ld_32x32b_x32(tb + c, gv);
+          ptx::tmem_ld_32x32b_x32(tb + BN / 2 + c, uv);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i]));
+            const float a1 = silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1]));
+            packed[i] = Vec16<bf16>::pack2(a0, a1);
+          }
+          if (row_ok) store_32(orow, nt * TILE_N + c, n_out, packed);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32], packed[16];
+          ptx::tmem_ld_32x32b_x32(tb + c, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = Vec16<bf16>::pack2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if (row_ok) store_32(orow, nt * TILE_N + c, n_out, packed);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync_all();  // the even CTA's MMAs into this CTA's tensor memory are over
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  if (threadIdx.x == 0 && *abort_flag) set_status(status, MOE_DEV_TIMEOUT);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -336,40 +599,83 @@ static bool make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t
 
 }  // namespace tc
 
+// Which kernel runs the two grouped GEMMs.  CTA pairs cut the shared-memory
+// operand traffic per MMA by a third but compute 256-row tiles, so they pay
+// off when the expert segments are long (measured on B300: 0.80 vs 0.67 of
+// the bf16 peak with 6144-row segments, 0.61 vs 0.67 with 512-row ones);
+// shorter segments stay on single-CTA 128-row tiles.  MOE_FFN_TILES=single|pair overrides the
+// choice (for measurement and for testing both kernels).
+static bool use_pair_tiles(const Plan& p) {
+  const char* env = getenv("MOE_FFN_TILES");
+  if (env && strcmp(env, "single") == 0) return false;
+  if (env && strcmp(env, "pair") == 0) return true;
+  return p.Tk >= static_cast<int64_t>(1024) * p.E;  // mean rows per expert >= 1024
+}
+
+template <bool SWIGLU>
+static cudaError_t launch_gemm(bool pair, int grid, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                               const int32_t* offsets, int E, int K, int b_rows, int n_out, int64_t rows_cap, bf16* out,
+                               int32_t* status, cudaStream_t s) {
+  using namespace tc;
+  if (pair) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_pair<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(P_SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    // no more clusters than can be resident at once (SMs that cannot be paired stay idle)
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    lc.blockDim = dim3(THREADS);
+    lc.dynamicSmemBytes = P_SMEM_BYTES;
+    lc.stream = s;
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_tc_pair<SWIGLU>, &lc) == cudaSuccess &&
+        max_clusters > 0 && 2 * max_clusters < grid)
+      grid = 2 * max_clusters;
+    (void)cudaGetLastError();
+    grouped_gemm_tc_pair<SWIGLU><<<grid, THREADS, P_SMEM_BYTES, s>>>(a, b0, b1, offsets, E, K, b_rows, n_out, rows_cap,
+                                                                      out, status);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    grouped_gemm_tc<SWIGLU><<<grid, THREADS, SMEM_BYTES, s>>>(a, b0, b1, offsets, E, K, b_rows, n_out, rows_cap, out,
+                                                              status);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                           const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
                           cudaStream_t s) {
   using namespace tc;
   if (p.Tk == 0) return cudaSuccess;
+  const bool pair = use_pair_tiles(p);
+  const uint32_t a_box = pair ? 128 : BM;           // rows of A each CTA stages
+  const uint32_t down_box = pair ? BN / 2 : BN;     // rows of W_down each CTA stages
   CUtensorMap tmX, tmG, tmU, tmAct, tmD;
   const uint64_t Tk = static_cast<uint64_t>(p.Tk);
-  if (!make_tmap(&tmX, X, Tk, p.h, BM) ||
+  if (!make_tmap(&tmX, X, Tk, p.h, a_box) ||
       !make_tmap(&tmG, W_gate, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2) ||
       !make_tmap(&tmU, W_up, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2) ||
-      !make_tmap(&tmAct, act, Tk, p.d_e, BM) ||
-      !make_tmap(&tmD, W_down, static_cast<uint64_t>(p.E) * p.h, p.d_e, BN))
+      !make_tmap(&tmAct, act, Tk, p.d_e, a_box) ||
+      !make_tmap(&tmD, W_down, static_cast<uint64_t>(p.E) * p.h, p.d_e, down_box))
     return cudaErrorNotSupported;
   const int nsm = current_sm_count();
-  const int64_t mtiles_max = (p.Tk + BM - 1) / BM + p.E;
+  const int rows_per_tile = pair ? P_BM : BM;
+  const int64_t mtiles_max = (p.Tk + rows_per_tile - 1) / rows_per_tile + p.E;
   const int64_t tiles1 = mtiles_max * ((p.d_e + BN / 2 - 1) / (BN / 2));
   const int64_t tiles2 = mtiles_max * ((p.h + BN - 1) / BN);
   if (tiles1 >= (int64_t(1) << 31) || tiles2 >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
-  const int grid1 = static_cast<int>(std::min<int64_t>(nsm, tiles1));
-  const int grid2 = static_cast<int>(std::min<int64_t>(nsm, tiles2));
-
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_BYTES));
+  // persistent grids: one CTA per SM (pairs: one cluster per two SMs)
+  const int units = pair ? nsm / 2 : nsm;
+  const int per = pair ? 2 : 1;
+  const int grid1 = per * static_cast<int>(std::min<int64_t>(units, tiles1));
+  const int grid2 = per * static_cast<int>(std::min<int64_t>(units, tiles2));
+  cudaError_t e = launch_gemm<true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
+                                    static_cast<bf16*>(act), status, s);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(grouped_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(SMEM_BYTES));
-  if (e != cudaSuccess) return e;
-  grouped_gemm_tc<true><<<grid1, THREADS, SMEM_BYTES, s>>>(tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
-                                                           static_cast<bf16*>(act), status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  grouped_gemm_tc<false><<<grid2, THREADS, SMEM_BYTES, s>>>(tmAct, tmD, tmD, offsets, p.E, p.d_e, p.h, p.h, p.Tk,
-                                                            static_cast<bf16*>(Y), status);
-  return cudaGetLastError();
+  return launch_gemm<false>(pair, grid2, tmAct, tmD, tmD, offsets, p.E, p.d_e, p.h, p.h, p.Tk, static_cast<bf16*>(Y),
+                            status, s);
 }
 
 }  // namespace moe

@@ -13,7 +13,7 @@ namespace moe {
 constexpr int route_bt_for(int ep) { return ep <= 256 ? 32 : 8192 / ep; }  // tokens per partial-logits block
 constexpr int route_kc_for(int ep) { return ep <= 128 ? 64 : 8192 / ep; }  // h chunk per pipeline stage
 constexpr int kSelTokens = 32;        // tokens per select block (8 warps x 4)
-constexpr int kDispatchChunk = 4096;  // priority positions per dispatch chunk
+constexpr int kDispatchChunk = 4096;  // largest number of priority positions per dispatch chunk
 
 // Sizes derived from one moe_config, and the carve-up of the workspace.
 struct Plan {
@@ -31,6 +31,7 @@ struct Plan {
   int route_kc = 0;        // K chunk of the partial-logits block
   int route_rowblocks = 0; // ceil(T / route_bt)
   int route_splits = 0;    // split of h across blocks (summed in fixed order by the select kernel)
+  int route_tc_n = 0;      // > 0: bf16 logits on the tensor cores with this MMA width (E or 2E rounded up to 16)
   int sel_tokens = 0;      // tokens per select block
   int sel_blocks = 0;      // ceil(T / sel_tokens): number of P partial rows
 
@@ -39,7 +40,7 @@ struct Plan {
   int n_chunks = 0;
 
   // workspace byte offsets
-  size_t ws_status = 0, ws_part = 0, ws_npart = 0, ws_ppart = 0, ws_hist = 0, ws_total = 0;
+  size_t ws_status = 0, ws_part = 0, ws_npart = 0, ws_ppart = 0, ws_hist = 0, ws_wt = 0, ws_total = 0;
 };
 
 // Validates the config and fills `plan`; on failure returns the status and a message.
@@ -48,6 +49,10 @@ moe_status make_plan(const moe_config* cfg, Plan* plan, const char** msg);
 cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const void* W_noise,
                          const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                          uint8_t* ws, cudaStream_t s);
+
+// Router slice sums U W_r (and U W_noise) on the tensor cores (bf16, p.route_tc_n > 0).
+cudaError_t launch_route_logits_tc(const Plan& p, const void* U, const void* W_r, const void* W_noise, float* part,
+                                   float* npart, uint8_t* ws, cudaStream_t s);
 
 cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, int32_t* counts_routed,
                             int32_t* counts_kept, int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* X,

@@ -129,11 +129,28 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   const int nkc = (q.h + q.route_kc - 1) / q.route_kc;
   int splits = q.route_rowblocks > 0 ? (512 + q.route_rowblocks - 1) / q.route_rowblocks : 1;
   splits = std::max(1, std::min(splits, std::min(16, nkc)));
+  // bf16 with at most 256 logit columns per token (E, or 2E for the noisy router): tensor cores,
+  // 128-token tiles, h split so that the tiles x slices cover the GPU with >= 4 k-blocks a slice
+  const int n_cols = q.noisy ? 2 * q.E : q.E;
+  if (q.bf16 && n_cols <= 256) {
+    q.route_tc_n = (n_cols + 15) / 16 * 16;
+    const int64_t mtiles = (q.T + 127) / 128;
+    const int nkb = (q.h + 63) / 64;
+    int64_t want = mtiles > 0 ? (148 + mtiles - 1) / mtiles : 1;
+    want = std::min<int64_t>(want, std::max(1, nkb / 4));
+    splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 16)));
+  }
   q.route_splits = splits;
   q.sel_tokens = kSelTokens;
   q.sel_blocks = static_cast<int>((q.T + kSelTokens - 1) / kSelTokens);
-  q.chunk = kDispatchChunk;
-  q.n_chunks = static_cast<int>((Tk + kDispatchChunk - 1) / kDispatchChunk);
+  // dispatch chunks: about two per SM (multiples of 256 positions, 256 .. 4096), so small
+  // batches still spread over the GPU and large ones keep the histogram short
+  {
+    int64_t c = (Tk + 2 * 148 - 1) / (2 * 148);
+    c = (c + 255) / 256 * 256;
+    q.chunk = static_cast<int>(std::max<int64_t>(256, std::min<int64_t>(kDispatchChunk, c)));
+  }
+  q.n_chunks = static_cast<int>((Tk + q.chunk - 1) / q.chunk);
 
   size_t off = 0;
   q.ws_status = off;
@@ -147,6 +164,8 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   off += align256(sizeof(float) * static_cast<size_t>(q.sel_blocks) * q.E);
   q.ws_hist = off;
   off += align256(sizeof(int32_t) * static_cast<size_t>(q.n_chunks) * q.E);
+  q.ws_wt = off;
+  if (q.route_tc_n > 0) off += align256(sizeof(uint16_t) * static_cast<size_t>(q.route_tc_n) * q.h);
   q.ws_total = off;
   *p = q;
   return MOE_OK;

@@ -360,8 +360,9 @@ cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const fl
   float* ppart = reinterpret_cast<float*>(ws + p.ws_ppart);
   int splits = p.route_splits;
   if (!logits_in) {
-    cudaError_t e = p.bf16 ? launch_partial_t<bf16>(p, U, W_r, W_noise, part, npart, s)
-                           : launch_partial_t<float>(p, U, W_r, W_noise, part, npart, s);
+    cudaError_t e = p.route_tc_n > 0 ? launch_route_logits_tc(p, U, W_r, W_noise, part, npart, ws, s)
+                    : p.bf16         ? launch_partial_t<bf16>(p, U, W_r, W_noise, part, npart, s)
+                                     : launch_partial_t<float>(p, U, W_r, W_noise, part, npart, s);
     if (e != cudaSuccess) return e;
   } else {
     npart = nullptr;
