@@ -27,6 +27,8 @@ Sources (page title, section):
          (this oracle reports E * sum f_i P_i, i.e. alpha = 1); for sigmoid
          scores P_i uses s'_{i,t} = s_{i,t} / sum_j s_{j,t}.
   [VIO]  same page, 无辅助损失的负载均衡: MaxVio = (max_i Load_i - mean) / mean.
+  [ZL]   same page, Router z-loss 与数值稳定: L_z = (1/T) sum_t (log sum_j e^{H_{t,j}})^2,
+         the mean square of each token's log-sum-exp of its router logits.
 
 Readings where the pages are silent (the same readings the library follows):
   * selection is made on the float32 logits (softmax and sigmoid are strictly
@@ -273,6 +275,20 @@ def load_stats(counts_routed, s: np.ndarray, T: int, k: int, score_fn: int) -> d
     return dict(f=f, P=P, aux=aux, maxvio=maxvio)
 
 
+def router_z_loss(H) -> float:
+    """L_z = (1/T) sum_t LSE(H_t)^2 with LSE(x) = log sum_j e^{x_j}.  [ZL]
+
+    The log-sum-exp is taken in the max-shifted form m + log sum_j e^{x_j - m}.
+    """
+    H = np.asarray(H, dtype=np.float64)
+    T = H.shape[0]
+    if T == 0:
+        return 0.0
+    m = H.max(axis=1)
+    lse = m + np.log(np.exp(H - m[:, None]).sum(axis=1))
+    return float((lse ** 2).sum() / T)
+
+
 # --------------------------------------------------------------------------
 # The whole layer
 # --------------------------------------------------------------------------
@@ -301,7 +317,7 @@ def layer_forward(inp, *, T, h, E, k, d_e, score_fn, renorm, capacity_factor,
     Y, act = expert_ffn(X, d["offsets"], inp.W_gate, inp.W_up, inp.W_down, d_e)
     out = combine(inp.U, Y, d["slot_row"], r["gate"], k)
     st = load_stats(d["counts_routed"], r["s"], T, k, score_fn)
-    return dict(r, **d, X=X, act=act, Y=Y, out=out, **st)
+    return dict(r, **d, X=X, act=act, Y=Y, out=out, z_loss=router_z_loss(r["logits"]), **st)
 
 
 def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int) -> dict:

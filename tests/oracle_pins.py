@@ -388,4 +388,49 @@ def pin_sigmoid_P_normalised(O):
     assert np.allclose(st["P"], [(0.5 + 0.75) / 2, (0.5 + 0.25) / 2], atol=1e-15)
 
 
+# ---------------------------------------------------------------- router z-loss
+
+def pin_z_loss_closed_forms(O):
+    """Constant logits c over E experts: LSE = c + ln E, so L_z = (c + ln E)^2; the z-loss section's
+    rounding example row (ten logits of 128, one of 128.5) has LSE = 128 + ln(10 + e^0.5); a mean
+    over tokens, not a sum."""
+    for c, E in ((0.0, 8), (-3.0, 64), (2.5, 1)):
+        H = np.full((5, E), c)
+        assert abs(O.router_z_loss(H) - (c + math.log(E)) ** 2) < 1e-10
+    g = golden("softmax_bf16_example.json")
+    row = np.array([g["logits"]], dtype=np.float64)
+    lse = 128.0 + math.log(10.0 + math.exp(0.5))
+    assert abs(O.router_z_loss(row) - lse ** 2) < 1e-8
+    two = np.vstack([row, np.zeros((1, 11))])
+    assert abs(O.router_z_loss(two) - (lse ** 2 + math.log(11.0) ** 2) / 2) < 1e-8
+    assert O.router_z_loss(np.zeros((0, 4))) == 0.0
+
+
+def pin_z_loss_library_logsumexp(O):
+    """Against scipy's logsumexp on random logits of several scales (library routine)."""
+    from scipy.special import logsumexp
+    rng = _rng(23)
+    for scale in (0.1, 3.0, 40.0):
+        H = rng.normal(size=(50, 13)) * scale
+        want = float(np.mean(logsumexp(H, axis=1) ** 2))
+        assert abs(O.router_z_loss(H) - want) <= 1e-12 * max(1.0, want)
+
+
+def pin_z_loss_gradient_formula(O):
+    """The section's gradient, dL_z/dH_{t,k} = (2/T) LSE(H_t) softmax(H_t)_k, against central
+    differences of the oracle's L_z."""
+    rng = _rng(29)
+    H = rng.normal(size=(4, 6))
+    T = H.shape[0]
+    eps = 1e-6
+    lse = np.log(np.exp(H).sum(axis=1))
+    sm = np.exp(H) / np.exp(H).sum(axis=1, keepdims=True)
+    for t, j in ((0, 0), (2, 5), (3, 1)):
+        Hp, Hm = H.copy(), H.copy()
+        Hp[t, j] += eps
+        Hm[t, j] -= eps
+        fd = (O.router_z_loss(Hp) - O.router_z_loss(Hm)) / (2 * eps)
+        assert abs(fd - 2.0 / T * lse[t] * sm[t, j]) < 1e-7
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -90,6 +90,23 @@ def _sigmoid_wrong_sign(H, fn):
     return _orig["scores"](H, fn)
 
 
+def _z_loss_no_square(H):
+    H = np.asarray(H, dtype=np.float64)
+    if H.shape[0] == 0:
+        return 0.0
+    m = H.max(axis=1)
+    return float(np.mean(m + np.log(np.exp(H - m[:, None]).sum(axis=1))))
+
+
+def _z_loss_sum_over_tokens(H):
+    return _orig["router_z_loss"](H) * max(1, np.asarray(H).shape[0])
+
+
+def _z_loss_max_not_lse(H):
+    H = np.asarray(H, dtype=np.float64)
+    return float(np.mean(H.max(axis=1) ** 2)) if H.shape[0] else 0.0
+
+
 MUTANTS = {
     "gates_not_renormalised": ("gates", _gates_no_renorm),
     "ties_to_higher_id": ("topk_select", _topk_ties_high),
@@ -106,6 +123,9 @@ MUTANTS = {
     "offsets_from_routed_counts": ("dispatch", _dispatch_offsets_routed),
     "softmax_over_tokens": ("scores", _scores_softmax_no_shift_wrong_axis),
     "sigmoid_sign": ("scores", _sigmoid_wrong_sign),
+    "z_loss_not_squared": ("router_z_loss", _z_loss_no_square),
+    "z_loss_summed_not_averaged": ("router_z_loss", _z_loss_sum_over_tokens),
+    "z_loss_max_for_lse": ("router_z_loss", _z_loss_max_not_lse),
 }
 
 
