@@ -29,6 +29,12 @@ Sources (page title, section):
   [VIO]  same page, 无辅助损失的负载均衡: MaxVio = (max_i Load_i - mean) / mean.
   [ZL]   same page, Router z-loss 与数值稳定: L_z = (1/T) sum_t (log sum_j e^{H_{t,j}})^2,
          the mean square of each token's log-sum-exp of its router logits.
+  [SHR]  same page, 细粒度专家与共享专家 (shared expert isolation, the V3 form):
+         h'_t = u_t + sum_{i<=N_s} FFN^(s)_i(u_t) + sum_{i<=N_r} g_{i,t} FFN^(r)_i(u_t);
+         the shared experts take every token and bypass the router.
+  [LFB]  same page, 无辅助损失的负载均衡: a per-expert bias b_i used only to choose
+         the top-k (s_{i,t} + b_i), the gate stays s_{i,t}; after each batch
+         e_i = mean(c) - c_i and b_i <- b_i + u * sign(e_i).
 
 Readings where the pages are silent (the same readings the library follows):
   * selection is made on the float32 logits (softmax and sigmoid are strictly
@@ -241,13 +247,27 @@ def expert_ffn(X, offsets, W_gate, W_up, W_down, d_e: int):
     return Y, act
 
 
-def combine(U, Y, slot_row, gate, k: int) -> np.ndarray:
-    """out_t = u_t + sum_j g_{j,t} Y[row of (t, j)], kept pairs only, j ascending.
+def shared_ffn(U, W_gate_sh, W_up_sh, W_down_sh) -> np.ndarray:
+    """Y_sh [N_s, T, h]: each shared expert's SwiGLU FFN on every token.  [SHR], [FFN]"""
+    U = f64(U)
+    n_s = len(W_gate_sh)
+    Y = np.zeros((n_s,) + U.shape)
+    for i in range(n_s):
+        Y[i], _ = swiglu(U, W_gate_sh[i], W_up_sh[i], W_down_sh[i])
+    return Y
+
+
+def combine(U, Y, slot_row, gate, k: int, Y_shared=None) -> np.ndarray:
+    """out_t = u_t + sum_s Y_shared[s, t] + sum_j g_{j,t} Y[row of (t, j)], kept pairs only, j ascending.
 
     [FFN] layer output with [RTR]'s index_add back into token order; a dropped
-    pair adds nothing (its token keeps the residual only, [CAP]).
+    pair adds nothing (its token keeps the residual only, [CAP]); [SHR] the
+    shared experts' outputs enter with weight 1.
     """
     out = f64(U).copy()
+    if Y_shared is not None:
+        for ys in f64(Y_shared):
+            out += ys
     T = out.shape[0]
     sr = np.asarray(slot_row, dtype=np.int64).reshape(T, k)
     g = f64(gate).reshape(T, k)
@@ -293,40 +313,61 @@ def router_z_loss(H) -> float:
 # The whole layer
 # --------------------------------------------------------------------------
 
-def route(H, k: int, score_fn: int, renorm: bool) -> dict:
-    """From logits to (idx, gates, scores): rounding to fp32, selection, scoring, gates."""
+def balance_bias_update(b, counts_routed, u: float) -> np.ndarray:
+    """One step of the loss-free balancing bias: e_i = mean(c) - c_i, b_i <- b_i + u * sign(e_i).  [LFB]"""
+    c = np.asarray(counts_routed, dtype=np.float64)
+    e = c.mean() - c
+    return f64(b) + u * np.sign(e)
+
+
+def route(H, k: int, score_fn: int, renorm: bool, sel_bias=None) -> dict:
+    """From logits to (idx, gates, scores): rounding to fp32, selection, scoring, gates.
+
+    Without a selection bias the top-k is taken on the logits (the same order
+    as on the scores).  With one ([LFB]) it is taken on s + b, while the gates
+    still come from s; "sel_key" holds s + b.
+    """
     H32 = round_f32(H)
-    idx = topk_select(H32, k)
     s = scores(H32, score_fn)
-    return dict(logits=H32, idx=idx, s=s, gate=gates(s, idx, renorm))
+    if sel_bias is None:
+        idx = topk_select(H32, k)
+        key = H32
+    else:
+        key = s + f64(sel_bias)[None, :]
+        idx = topk_select(key, k)
+    return dict(logits=H32, idx=idx, s=s, gate=gates(s, idx, renorm), sel_key=key)
 
 
 def layer_forward(inp, *, T, h, E, k, d_e, score_fn, renorm, capacity_factor,
-                  capacity_override=0, priority=CHOICE_MAJOR, logits=None) -> dict:
+                  capacity_override=0, priority=CHOICE_MAJOR, logits=None, sel_bias=None, shared=None) -> dict:
     """The full single-GPU MoE layer forward, stage by stage, in float64.
 
     `inp` carries U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down (numpy or
     torch).  If `logits` is given the router GEMM is skipped and those logits
-    are used as they are.
+    are used as they are.  `sel_bias` [E] is the loss-free selection bias
+    ([LFB]); `shared` = (W_gate_sh, W_up_sh, W_down_sh) adds shared experts
+    ([SHR]).
     """
     H = router_logits(inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps) if logits is None else f64(logits)
-    r = route(H, k, score_fn, renorm)
+    r = route(H, k, score_fn, renorm, sel_bias)
     C = capacity(T, E, k, capacity_factor, capacity_override)
     d = dispatch(r["idx"], E, C, priority)
     X = permute(inp.U, d["row_token"])
     Y, act = expert_ffn(X, d["offsets"], inp.W_gate, inp.W_up, inp.W_down, d_e)
-    out = combine(inp.U, Y, d["slot_row"], r["gate"], k)
+    Y_sh = None if shared is None else shared_ffn(inp.U, *shared)
+    out = combine(inp.U, Y, d["slot_row"], r["gate"], k, Y_sh)
     st = load_stats(d["counts_routed"], r["s"], T, k, score_fn)
-    return dict(r, **d, X=X, act=act, Y=Y, out=out, z_loss=router_z_loss(r["logits"]), **st)
+    return dict(r, **d, X=X, act=act, Y=Y, Y_shared=Y_sh, out=out, z_loss=router_z_loss(r["logits"]), **st)
 
 
-def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int) -> dict:
+def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int, shared=None) -> dict:
     """out rows (and the Y rows they use) for a sample of tokens.
 
     For full-size checks: X[row] = U[t] for a kept pair, so each needed Y row
     is one expert applied to one token row ([FFN]); out follows [FFN]'s layer
     output.  The sampled rows are grouped by expert so that each expert's
     weights are read (and widened to float64) once.
+    With `shared` the shared experts' outputs ([SHR]) are added too.
     Returns {"out": [n, h], "Y": {row: [h]}}.
     """
     tokens = [int(t) for t in tokens]
@@ -346,8 +387,14 @@ def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int) -> dict:
         for (t, j), row in zip(pairs, y):
             y_of[(t, j)] = row
     outs, Yrows = [], {}
+    sh = {}
+    if shared is not None and tokens:
+        ysh = shared_ffn(np.stack([U[t] for t in tokens]), *shared).sum(axis=0)
+        sh = {t: ysh[i] for i, t in enumerate(tokens)}
     for t in tokens:
         acc = U[t].copy()
+        if shared is not None:
+            acc = acc + sh[t]
         for j in range(k):
             if sr[t, j] >= 0:
                 Yrows[int(sr[t, j])] = y_of[(t, j)]

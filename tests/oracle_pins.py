@@ -433,4 +433,98 @@ def pin_z_loss_gradient_formula(O):
         assert abs(fd - 2.0 / T * lse[t] * sm[t, j]) < 1e-7
 
 
+# ---------------------------------------------------------------- loss-free balancing bias
+
+def pin_loss_free_selection_example(O):
+    """Selection on s + b, gates from s: scores (.5, .4, .3) with b = (-.2, 0, .15) give keys
+    (.3, .4, .45); top-1 is expert 2 with gate s_2 = .3 (1 after renormalising); top-2 is (2, 1)
+    with renormalised gates (3/7, 4/7)."""
+    # softmax(log(s / sum s)) = s / sum s; the logits pass through float32, hence the 1e-7
+    s = np.array([[0.5, 0.4, 0.3]])
+    H = np.log(s / s.sum())
+    b = np.array([-0.2, 0.0, 0.15]) / s.sum()
+    r1 = O.route(H, 1, O.SOFTMAX, False, sel_bias=b)
+    assert r1["idx"].tolist() == [[2]]
+    assert abs(r1["gate"][0, 0] - 0.3 / s.sum()) < 1e-7
+    assert abs(O.route(H, 1, O.SOFTMAX, True, sel_bias=b)["gate"][0, 0] - 1.0) < 1e-12
+    r2 = O.route(H, 2, O.SOFTMAX, True, sel_bias=b)
+    assert r2["idx"].tolist() == [[2, 1]]
+    assert np.allclose(r2["gate"], [[3 / 7, 4 / 7]], atol=1e-7)
+    assert O.route(H, 1, O.SOFTMAX, False)["idx"].tolist() == [[0]]  # without the bias: expert 0
+
+
+def pin_loss_free_zero_bias_and_gates(O):
+    """A zero bias selects exactly what the logits select; any bias leaves the gate of a selected
+    expert equal to its (renormalised) score."""
+    rng = _rng(31)
+    H = rng.normal(size=(40, 12))
+    for fn in (O.SOFTMAX, O.SIGMOID):
+        plain = O.route(H, 3, fn, True)
+        zero = O.route(H, 3, fn, True, sel_bias=np.zeros(12))
+        assert np.array_equal(plain["idx"], zero["idx"])
+        b = rng.normal(size=12) * 0.3
+        biased = O.route(H, 3, fn, False, sel_bias=b)
+        sel = np.take_along_axis(biased["s"], biased["idx"].astype(np.int64), axis=1)
+        assert np.allclose(biased["gate"], sel, atol=0)
+        key = biased["s"] + b
+        brute = np.argsort(-key, axis=1, kind="stable")[:, :3]
+        assert np.array_equal(biased["idx"], brute)
+
+
+def pin_balance_bias_update(O):
+    """e_i = mean(c) - c_i; an overloaded expert's bias drops by u, an underloaded one rises by u,
+    one exactly at the mean keeps its bias."""
+    b = np.array([0.1, -0.2, 0.0, 0.3])
+    nb = O.balance_bias_update(b, [10, 5, 0, 5], 0.01)
+    assert np.allclose(nb, [0.09, -0.2, 0.01, 0.3], atol=1e-15)
+
+
+def pin_balance_bias_feedback(O):
+    """The section's illustration: 6 experts, 2400 random tokens a step, top-1, u = 0.01.  Experts
+    of unequal popularity start far from balance; the sign updates pull every load toward the
+    mean, so MaxVio falls by a large factor."""
+    rng = _rng(37)
+    E, T = 6, 2400
+    pop = np.linspace(-0.6, 0.6, E)
+    b = np.zeros(E)
+
+    def step(b):
+        s = O.scores(rng.normal(size=(T, E)) * 0.3 + pop, O.SIGMOID)
+        idx = O.topk_select(s + b, 1)
+        return np.bincount(idx[:, 0], minlength=E)
+
+    c0 = step(b)
+    vio0 = (c0.max() - c0.mean()) / c0.mean()
+    for _ in range(300):
+        b = O.balance_bias_update(b, step(b), 0.01)
+    vio = np.mean([(c.max() - c.mean()) / c.mean() for c in (step(b) for _ in range(20))])
+    assert vio0 > 1.0 and vio < vio0 / 5
+
+
+# ---------------------------------------------------------------- shared experts
+
+def pin_shared_experts(O):
+    """h' = u + sum_s FFN_s(u) + sum_i g_i FFN_i(u): zero shared weights change nothing; one
+    routed expert (k = 1, gate 1) identical to one shared expert doubles the FFN term; the shared
+    term equals torch's dense SwiGLU on every token."""
+    import torch
+    rng = _rng(41)
+    T, h, d = 9, 6, 5
+    U = rng.normal(size=(T, h))
+    Wg, Wu, Wd = rng.normal(size=(1, d, h)), rng.normal(size=(1, d, h)), rng.normal(size=(h, d))[None]
+    inp = _inputs(U=U, W_r=rng.normal(size=(h, 1)), b_r=None, W_noise=None, eps=None, W_gate=Wg, W_up=Wu,
+                  W_down=Wd)
+    kw = dict(T=T, h=h, E=1, k=1, d_e=d, score_fn=O.SOFTMAX, renorm=True, capacity_factor=0.0)
+    base = O.layer_forward(inp, **kw)
+    zero = O.layer_forward(inp, shared=(np.zeros_like(Wg), np.zeros_like(Wu), np.zeros_like(Wd)), **kw)
+    assert np.allclose(zero["out"], base["out"], atol=0)
+    same = O.layer_forward(inp, shared=(Wg, Wu, Wd), **kw)
+    assert np.allclose(same["out"] - U, 2 * (base["out"] - U), rtol=1e-12, atol=1e-12)
+    tU = torch.tensor(U)
+    dense = (torch.nn.functional.silu(tU @ torch.tensor(Wg[0]).T) * (tU @ torch.tensor(Wu[0]).T)) @ torch.tensor(Wd[0]).T
+    assert np.allclose(O.shared_ffn(U, Wg, Wu, Wd)[0], dense.numpy(), rtol=1e-12, atol=1e-12)
+    two = O.shared_ffn(U, np.concatenate([Wg, Wg]), np.concatenate([Wu, Wu]), np.concatenate([Wd, -Wd]))
+    assert np.allclose(two.sum(axis=0), 0, atol=1e-12)
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -107,6 +107,26 @@ def _z_loss_max_not_lse(H):
     return float(np.mean(H.max(axis=1) ** 2)) if H.shape[0] else 0.0
 
 
+def _bias_update_wrong_sign(b, counts, u):
+    c = np.asarray(counts, dtype=np.float64)
+    return np.asarray(b, dtype=np.float64) + u * np.sign(c - c.mean())
+
+
+def _route_gates_from_key(H, k, fn, renorm, sel_bias=None):
+    r = _orig["route"](H, k, fn, renorm, sel_bias)
+    if sel_bias is not None:
+        r["gate"] = _orig["gates"](r["s"] + np.asarray(sel_bias, dtype=np.float64)[None, :], r["idx"], renorm)
+    return r
+
+
+def _route_ignores_bias(H, k, fn, renorm, sel_bias=None):
+    return _orig["route"](H, k, fn, renorm, None)
+
+
+def _combine_ignores_shared(U, Y, slot_row, gate, k, Y_shared=None):
+    return _orig["combine"](U, Y, slot_row, gate, k, None)
+
+
 MUTANTS = {
     "gates_not_renormalised": ("gates", _gates_no_renorm),
     "ties_to_higher_id": ("topk_select", _topk_ties_high),
@@ -126,6 +146,10 @@ MUTANTS = {
     "z_loss_not_squared": ("router_z_loss", _z_loss_no_square),
     "z_loss_summed_not_averaged": ("router_z_loss", _z_loss_sum_over_tokens),
     "z_loss_max_for_lse": ("router_z_loss", _z_loss_max_not_lse),
+    "bias_update_wrong_sign": ("balance_bias_update", _bias_update_wrong_sign),
+    "loss_free_gates_from_key": ("route", _route_gates_from_key),
+    "loss_free_bias_ignored": ("route", _route_ignores_bias),
+    "shared_experts_not_added": ("combine", _combine_ignores_shared),
 }
 
 
