@@ -35,6 +35,13 @@ Sources (page title, section):
   [LFB]  same page, 无辅助损失的负载均衡: a per-expert bias b_i used only to choose
          the top-k (s_{i,t} + b_i), the gate stays s_{i,t}; after each batch
          e_i = mean(c) - c_i and b_i <- b_i + u * sign(e_i).
+  [GRD]  same page, 路由器：打分、top-k、加权求和 (how the router learns): with the
+         upstream gradient delta_t = dL/dh'_t, dL/dg_{i,t} = delta_t^T FFN_i(u_t) for
+         the selected experts, then through dg/dH to the logits; section
+         负载均衡辅助损失：推导与梯度 (梯度往哪推): f is a constant, and
+         d(sum_i f_i P_i)/dH_{t,k} = (1/T) s_k (f_k - sum_i f_i s_i) for softmax,
+         (1/T) s'_k (1 - s_k) (f_k - sum_i f_i s'_i) for sigmoid; section Router
+         z-loss: dL_z/dH_{t,k} = (2/T) LSE(H_t) softmax(H_t)_k.
 
 Readings where the pages are silent (the same readings the library follows):
   * selection is made on the float32 logits (softmax and sigmoid are strictly
@@ -401,6 +408,92 @@ def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int, shared=None) -> di
                 acc = acc + gate[t, j] * y_of[(t, j)]
         outs.append(acc)
     return dict(out=np.stack(outs) if outs else np.zeros((0, 0)), Y=Yrows)
+
+
+# --------------------------------------------------------------------------
+# Backward of the router side  [GRD]
+# --------------------------------------------------------------------------
+
+def combine_backward(dO, Y, slot_row, gate, k: int) -> dict:
+    """Backward of the combine for the upstream gradient dO [T, h].
+
+    out_t = u_t + sum_j g_{t,j} Y[row(t,j)] gives, per kept pair,
+    dL/dg_{t,j} = dO_t . Y[row] ([GRD]) and dL/dY[row] = g_{t,j} dO_t;
+    dropped pairs get d_gate = 0.  Returns d_gate [T, k] and dY [A, h] (rows of Y).
+    """
+    dO, Y, g = f64(dO), f64(Y), f64(gate)
+    T = dO.shape[0]
+    sr = np.asarray(slot_row, dtype=np.int64).reshape(T, k)
+    d_gate = np.zeros((T, k))
+    dY = np.zeros_like(Y)
+    for j in range(k):
+        m = sr[:, j] >= 0
+        rows = sr[m, j]
+        d_gate[m, j] = np.einsum("th,th->t", dO[m], Y[rows])
+        dY[rows] = g.reshape(T, k)[m, j][:, None] * dO[m]
+    return dict(d_gate=d_gate, dY=dY)
+
+
+def gate_backward(H32, idx, d_gate, score_fn: int, renorm: bool) -> np.ndarray:
+    """dL/dH [T, E] from dL/dg through the gate definition ([SCR], [GRD]).
+
+    softmax:  s = softmax(H); g_j = s_{i_j}, or s_{i_j} / sum_m s_{i_m} with renorm;
+    sigmoid:  s = sigmoid(H); the same two forms.  The selection itself is
+    not differentiated (the top-k set is held fixed).
+    """
+    H = np.asarray(H32, dtype=np.float64)
+    T, E = H.shape
+    idx = np.asarray(idx, dtype=np.int64)
+    k = idx.shape[1]
+    s = scores(H, score_fn)
+    sel = np.take_along_axis(s, idx, axis=1)
+    d_gate = f64(d_gate).reshape(T, k)
+    # dL/ds_{i_j} (for the selected experts; the other scores do not enter g)
+    if renorm:
+        S = sel.sum(axis=1, keepdims=True)
+        g = sel / S
+        # g_j = s_j / S: dg_j/ds_m = (delta_jm - g_j) / S
+        ds_sel = (d_gate - (d_gate * g).sum(axis=1, keepdims=True)) / S
+    else:
+        ds_sel = d_gate
+    ds = np.zeros((T, E))
+    np.add.at(ds, (np.repeat(np.arange(T), k), idx.reshape(-1)), ds_sel.reshape(-1))
+    if score_fn == SOFTMAX:
+        # ds_i/dH_k = s_i (delta_ik - s_k)
+        return s * (ds - (ds * s).sum(axis=1, keepdims=True))
+    return ds * s * (1.0 - s)
+
+
+def aux_loss_grad(H32, f, score_fn: int) -> np.ndarray:
+    """d(E * sum_i f_i P_i)/dH [T, E] with f held constant ([AUX], [GRD])."""
+    H = np.asarray(H32, dtype=np.float64)
+    T, E = H.shape
+    f = np.asarray(f, dtype=np.float64)
+    s = scores(H, score_fn)
+    if score_fn == SOFTMAX:
+        return E / T * s * (f[None, :] - (s * f[None, :]).sum(axis=1, keepdims=True))
+    sp = s / s.sum(axis=1, keepdims=True)
+    return E / T * sp * (1.0 - s) * (f[None, :] - (sp * f[None, :]).sum(axis=1, keepdims=True))
+
+
+def z_loss_grad(H32) -> np.ndarray:
+    """dL_z/dH [T, E] = (2/T) LSE(H_t) softmax(H_t) ([ZL])."""
+    H = np.asarray(H32, dtype=np.float64)
+    T = H.shape[0]
+    m = H.max(axis=1, keepdims=True)
+    lse = m + np.log(np.exp(H - m).sum(axis=1, keepdims=True))
+    return 2.0 / T * lse * scores(H, SOFTMAX)
+
+
+def router_backward(H32, idx, d_gate, f, score_fn: int, renorm: bool, w_aux: float = 0.0,
+                    w_z: float = 0.0) -> np.ndarray:
+    """dL/dH for L = (the loss through the gates) + w_aux * E sum f P + w_z * L_z."""
+    dH = gate_backward(H32, idx, d_gate, score_fn, renorm)
+    if w_aux:
+        dH = dH + w_aux * aux_loss_grad(H32, f, score_fn)
+    if w_z:
+        dH = dH + w_z * z_loss_grad(H32)
+    return dH
 
 
 def topk_margins(H32: np.ndarray, k: int) -> np.ndarray:

@@ -527,4 +527,84 @@ def pin_shared_experts(O):
     assert np.allclose(two.sum(axis=0), 0, atol=1e-12)
 
 
+# ---------------------------------------------------------------- router-side backward
+
+def pin_aux_grad_worked_example(O):
+    """The section's example: f = (.55, .25, .10, .10), s = (.4, .3, .2, .1): weighted mean load .325
+    and logit gradients (x T) .090, -.0225, -.045, -.0225 for sum f P (aux_loss_grad carries E/T)."""
+    g = golden("aux_grad_example.json")
+    s = np.array(g["s"])
+    f = np.array(g["f"])
+    assert abs(float((f * s).sum()) - g["weighted_mean_load"]) < 1e-12
+    H = np.log(s)[None, :]  # softmax(log s) = s, since s sums to 1
+    E, T = 4, 1
+    grad = O.aux_loss_grad(H, f, O.SOFTMAX) * T / E
+    assert np.allclose(grad[0], g["grad_times_T"], atol=5e-8)  # H passes through no rounding here
+
+
+def _fd(fun, X, i, j, eps=1e-6):
+    Xp, Xm = X.copy(), X.copy()
+    Xp[i, j] += eps
+    Xm[i, j] -= eps
+    return (fun(Xp) - fun(Xm)) / (2 * eps)
+
+
+def pin_aux_grad_finite_differences(O):
+    """aux_loss_grad against central differences of E * sum f P(H) with the load f held fixed, for
+    softmax and for sigmoid (P from s' = s / sum s), including the sigmoid saturation factor."""
+    rng = _rng(43)
+    T, E = 5, 6
+    H = rng.normal(size=(T, E)) * 1.5
+    counts = np.array([7, 1, 0, 3, 2, 2])
+    f = counts / counts.sum()
+    for fn in (O.SOFTMAX, O.SIGMOID):
+        def aux(Hx):
+            return O.load_stats(counts, O.scores(Hx, fn), T, counts.sum() / T, fn)["aux"]
+        G = O.aux_loss_grad(H, f, fn)
+        for (i, j) in ((0, 0), (2, 3), (4, 5), (1, 2)):
+            assert abs(_fd(aux, H, i, j) - G[i, j]) < 1e-7
+
+
+def pin_gate_backward_finite_differences(O):
+    """gate_backward against central differences of L(H) = sum_{t,j} w_{t,j} g_{t,j}(H) with the
+    top-k set fixed, for softmax/sigmoid, with and without renormalisation."""
+    rng = _rng(47)
+    T, E, k = 4, 7, 3
+    H = rng.normal(size=(T, E))
+    idx = O.topk_select(H, k)
+    w = rng.normal(size=(T, k))
+    for fn in (O.SOFTMAX, O.SIGMOID):
+        for renorm in (True, False):
+            def L(Hx):
+                return float((O.gates(O.scores(Hx, fn), idx, renorm) * w).sum())
+            G = O.gate_backward(H, idx, w, fn, renorm)
+            for (i, j) in ((0, int(idx[0, 0])), (1, int(idx[1, 2])), (3, 0), (2, 6), (2, int(idx[2, 1]))):
+                assert abs(_fd(L, H, i, j) - G[i, j]) < 1e-7, (fn, renorm, i, j)
+
+
+def pin_combine_and_z_backward(O):
+    """combine_backward: d_gate = dO . Y[row] and dY = g dO (the section's delta^T FFN_i), checked
+    by central differences of <dO, out>; a dropped pair gets zero.  z_loss_grad against differences
+    of the oracle's L_z."""
+    rng = _rng(53)
+    T, h, k = 3, 4, 2
+    U = rng.normal(size=(T, h))
+    Y = rng.normal(size=(T * k, h))
+    slot_row = np.array([0, 1, 2, -1, 4, 5])
+    gate = rng.random((T, k))
+    dO = rng.normal(size=(T, h))
+    b = O.combine_backward(dO, Y, slot_row, gate, k)
+    L_gate = lambda G: float((dO * O.combine(U, Y, slot_row, G, k)).sum())
+    for (i, j) in ((0, 0), (1, 0), (2, 1)):
+        assert abs(_fd(L_gate, gate, i, j) - b["d_gate"][i, j]) < 1e-7
+    assert b["d_gate"][1, 1] == 0.0
+    L_Y = lambda Yx: float((dO * O.combine(U, Yx, slot_row, gate, k)).sum())
+    for (r, c) in ((0, 1), (2, 3), (5, 0), (3, 2)):
+        assert abs(_fd(L_Y, Y, r, c) - b["dY"][r, c]) < 1e-7
+    H = rng.normal(size=(4, 5))
+    G = O.z_loss_grad(H)
+    for (i, j) in ((0, 0), (3, 4), (2, 1)):
+        assert abs(_fd(O.router_z_loss, H, i, j) - G[i, j]) < 1e-7
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

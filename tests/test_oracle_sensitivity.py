@@ -127,6 +127,24 @@ def _combine_ignores_shared(U, Y, slot_row, gate, k, Y_shared=None):
     return _orig["combine"](U, Y, slot_row, gate, k, None)
 
 
+def _aux_grad_no_mean_term(H, f, fn):
+    s = O.scores(np.asarray(H, dtype=np.float64), fn)
+    T, E = s.shape
+    return E / T * s * np.asarray(f, dtype=np.float64)[None, :]
+
+
+def _gate_backward_ignores_renorm(H, idx, d_gate, fn, renorm):
+    return _orig["gate_backward"](H, idx, d_gate, fn, False)
+
+
+def _z_grad_half(H):
+    return 0.5 * _orig["z_loss_grad"](H)
+
+
+def _combine_backward_no_gate(dO, Y, slot_row, gate, k):
+    return _orig["combine_backward"](dO, Y, slot_row, np.ones_like(np.asarray(gate, dtype=float)), k)
+
+
 MUTANTS = {
     "gates_not_renormalised": ("gates", _gates_no_renorm),
     "ties_to_higher_id": ("topk_select", _topk_ties_high),
@@ -150,6 +168,10 @@ MUTANTS = {
     "loss_free_gates_from_key": ("route", _route_gates_from_key),
     "loss_free_bias_ignored": ("route", _route_ignores_bias),
     "shared_experts_not_added": ("combine", _combine_ignores_shared),
+    "aux_grad_without_mean_load": ("aux_loss_grad", _aux_grad_no_mean_term),
+    "gate_backward_ignores_renorm": ("gate_backward", _gate_backward_ignores_renorm),
+    "z_grad_half": ("z_loss_grad", _z_grad_half),
+    "combine_backward_ignores_gate": ("combine_backward", _combine_backward_no_gate),
 }
 
 
