@@ -42,6 +42,9 @@ Sources (page title, section):
          d(sum_i f_i P_i)/dH_{t,k} = (1/T) s_k (f_k - sum_i f_i s_i) for softmax,
          (1/T) s'_k (1 - s_k) (f_k - sum_i f_i s'_i) for sigmoid; section Router
          z-loss: dL_z/dH_{t,k} = (2/T) LSE(H_t) softmax(H_t)_k.
+  [BWD]  same page, 专家计算：padding、block-sparse 与 grouped GEMM: the backward of
+         the SwiGLU experts is grouped GEMMs too, one group for the input
+         gradients and one for the weight gradients.
 
 Readings where the pages are silent (the same readings the library follows):
   * selection is made on the float32 logits (softmax and sigmoid are strictly
@@ -494,6 +497,63 @@ def router_backward(H32, idx, d_gate, f, score_fn: int, renorm: bool, w_aux: flo
     if w_z:
         dH = dH + w_z * z_loss_grad(H32)
     return dH
+
+
+# --------------------------------------------------------------------------
+# Backward of the experts and of the dispatch  [BWD], [FFN]
+# --------------------------------------------------------------------------
+
+def swiglu_backward(x, W_gate_e, W_up_e, W_down_e, dy) -> dict:
+    """Gradients of y = W_down (SiLU(W_gate x) * W_up x) for rows x [n, h] and dL/dy [n, h].
+
+    With G = x W_gate^T, Up = x W_up^T, s = sigmoid(G), a = G s Up:
+      d_act = dy W_down, dW_down = dy^T a,
+      dUp = d_act * G s, dG = d_act * Up * s (1 + G (1 - s)),
+      dx = dG W_gate + dUp W_up, dW_gate = dG^T x, dW_up = dUp^T x.
+    """
+    x, Wg, Wu, Wd, dy = f64(x), f64(W_gate_e), f64(W_up_e), f64(W_down_e), f64(dy)
+    G = x @ Wg.T
+    Up = x @ Wu.T
+    with np.errstate(over="ignore"):
+        sg = 1.0 / (1.0 + np.exp(-G))
+    silu_g = G * sg
+    act = silu_g * Up
+    d_act = dy @ Wd
+    dUp = d_act * silu_g
+    dG = d_act * Up * sg * (1.0 + G * (1.0 - sg))
+    return dict(d_act=d_act, dG=dG, dUp=dUp, dx=dG @ Wg + dUp @ Wu, dW_gate=dG.T @ x, dW_up=dUp.T @ x,
+                dW_down=dy.T @ act)
+
+
+def expert_ffn_backward(X, offsets, W_gate, W_up, W_down, dY, d_e: int) -> dict:
+    """The grouped backward over the expert segments: per row d_act, dG, dUp, dX; per expert
+    dW_gate [E, d_e, h], dW_up [E, d_e, h], dW_down [E, h, d_e] (zero for an expert with no rows)."""
+    X, dY = f64(X), f64(dY)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E = len(offsets) - 1
+    A, h = X.shape
+    out = dict(d_act=np.zeros((A, d_e)), dG=np.zeros((A, d_e)), dUp=np.zeros((A, d_e)), dX=np.zeros((A, h)),
+               dW_gate=np.zeros((E, d_e, h)), dW_up=np.zeros((E, d_e, h)), dW_down=np.zeros((E, h, d_e)))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            b = swiglu_backward(X[lo:hi], W_gate[e], W_up[e], W_down[e], dY[lo:hi])
+            out["d_act"][lo:hi], out["dG"][lo:hi], out["dUp"][lo:hi] = b["d_act"], b["dG"], b["dUp"]
+            out["dX"][lo:hi] = b["dx"]
+            out["dW_gate"][e], out["dW_up"][e], out["dW_down"][e] = b["dW_gate"], b["dW_up"], b["dW_down"]
+    return out
+
+
+def dispatch_backward(dO, dX, slot_row, k: int) -> np.ndarray:
+    """dL/dU from the residual and the permute: dU_t = dO_t + sum_{kept j} dX[row(t, j)] (X = U[perm])."""
+    dU = f64(dO).copy()
+    T = dU.shape[0]
+    sr = np.asarray(slot_row, dtype=np.int64).reshape(T, k)
+    dX = f64(dX)
+    for j in range(k):
+        m = sr[:, j] >= 0
+        dU[m] += dX[sr[m, j]]
+    return dU
 
 
 def topk_margins(H32: np.ndarray, k: int) -> np.ndarray:

@@ -607,4 +607,53 @@ def pin_combine_and_z_backward(O):
         assert abs(_fd(O.router_z_loss, H, i, j) - G[i, j]) < 1e-7
 
 
+# ---------------------------------------------------------------- expert and dispatch backward
+
+def pin_swiglu_backward_autograd(O):
+    """swiglu_backward against torch autograd through torch's silu and matmul (float64), and
+    SiLU'(0) = 1/2."""
+    import torch
+    rng = _rng(59)
+    n, h, d = 5, 7, 6
+    x, Wg, Wu, Wd, dy = (rng.normal(size=s) for s in ((n, h), (d, h), (d, h), (h, d), (n, h)))
+    t = {k_: torch.tensor(v, requires_grad=True) for k_, v in dict(x=x, Wg=Wg, Wu=Wu, Wd=Wd).items()}
+    y = (torch.nn.functional.silu(t["x"] @ t["Wg"].T) * (t["x"] @ t["Wu"].T)) @ t["Wd"].T
+    (y * torch.tensor(dy)).sum().backward()
+    b = O.swiglu_backward(x, Wg, Wu, Wd, dy)
+    for mine, ref in (("dx", "x"), ("dW_gate", "Wg"), ("dW_up", "Wu"), ("dW_down", "Wd")):
+        assert np.allclose(b[mine], t[ref].grad.numpy(), rtol=1e-10, atol=1e-12), mine
+    z = O.swiglu_backward(np.zeros((1, 1)), np.ones((1, 1)), np.ones((1, 1)), np.ones((1, 1)), np.ones((1, 1)))
+    assert z["dG"][0, 0] == 0.0  # Up = 0 at x = 0
+    one = O.swiglu_backward(np.ones((1, 1)), np.zeros((1, 1)), np.ones((1, 1)), np.ones((1, 1)), np.ones((1, 1)))
+    assert abs(one["dG"][0, 0] - 0.5) < 1e-15  # G = 0: SiLU'(0) = 1/2, Up = 1, d_act = 1
+
+
+def pin_expert_and_dispatch_backward_segments(O):
+    """The grouped backward equals the per-expert backward on each segment; an empty expert gets
+    zero weight gradients; dispatch_backward adds each kept row's dX to its token once."""
+    rng = _rng(61)
+    E, h, d, T, k = 3, 5, 4, 6, 2
+    idx = np.array([[0, 1], [1, 0], [0, 1], [1, 0], [0, 1], [1, 0]])
+    disp = O.dispatch(idx, E, T)
+    U = rng.normal(size=(T, h))
+    X = O.permute(U, disp["row_token"])
+    Wg, Wu, Wd = rng.normal(size=(E, d, h)), rng.normal(size=(E, d, h)), rng.normal(size=(E, h, d))
+    dY = rng.normal(size=X.shape)
+    g = O.expert_ffn_backward(X, disp["offsets"], Wg, Wu, Wd, dY, d)
+    for e in range(E):
+        lo, hi = disp["offsets"][e], disp["offsets"][e + 1]
+        if hi > lo:
+            b = O.swiglu_backward(X[lo:hi], Wg[e], Wu[e], Wd[e], dY[lo:hi])
+            assert np.allclose(g["dW_gate"][e], b["dW_gate"]) and np.allclose(g["dX"][lo:hi], b["dx"])
+        else:
+            assert not g["dW_down"][e].any() and not g["dW_gate"][e].any()
+    dO = rng.normal(size=(T, h))
+    dU = O.dispatch_backward(dO, g["dX"], disp["slot_row"], k)
+    want = dO.copy()
+    for t in range(T):
+        for j in range(k):
+            want[t] += g["dX"][disp["slot_row"][t * k + j]]
+    assert np.allclose(dU, want, atol=1e-12)
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -145,6 +145,22 @@ def _combine_backward_no_gate(dO, Y, slot_row, gate, k):
     return _orig["combine_backward"](dO, Y, slot_row, np.ones_like(np.asarray(gate, dtype=float)), k)
 
 
+def _swiglu_backward_sigmoid_only(x, Wg, Wu, Wd, dy):
+    b = _orig["swiglu_backward"](x, Wg, Wu, Wd, dy)
+    x64 = np.asarray(x, dtype=np.float64)
+    G = x64 @ np.asarray(Wg, dtype=np.float64).T
+    Up = x64 @ np.asarray(Wu, dtype=np.float64).T
+    sg = 1.0 / (1.0 + np.exp(-G))
+    b["dG"] = b["d_act"] * Up * sg  # drops the G (1 - s) term of SiLU'
+    b["dx"] = b["dG"] @ np.asarray(Wg, dtype=np.float64) + b["dUp"] @ np.asarray(Wu, dtype=np.float64)
+    b["dW_gate"] = b["dG"].T @ x64
+    return b
+
+
+def _dispatch_backward_no_residual(dO, dX, slot_row, k):
+    return _orig["dispatch_backward"](np.zeros_like(np.asarray(dO, dtype=np.float64)), dX, slot_row, k)
+
+
 MUTANTS = {
     "gates_not_renormalised": ("gates", _gates_no_renorm),
     "ties_to_higher_id": ("topk_select", _topk_ties_high),
@@ -172,6 +188,8 @@ MUTANTS = {
     "gate_backward_ignores_renorm": ("gate_backward", _gate_backward_ignores_renorm),
     "z_grad_half": ("z_loss_grad", _z_grad_half),
     "combine_backward_ignores_gate": ("combine_backward", _combine_backward_no_gate),
+    "silu_derivative_missing_term": ("swiglu_backward", _swiglu_backward_sigmoid_only),
+    "dispatch_backward_drops_residual": ("dispatch_backward", _dispatch_backward_no_residual),
 }
 
 
