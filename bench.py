@@ -158,11 +158,16 @@ def stage_work(w: W.Workload, A: float, n_active: float):
     dispatch_bytes = T * h * b + A * h * b + T * k * 12
     ffn_flops = 6 * A * h * d
     ffn_bytes = 3 * h * d * b * n_active + 2 * A * h * b + 2 * A * d * b
-    combine_bytes = A * h * b + 2 * T * h * b + T * k * 8
-    return {"route": {"bytes": route_bytes, "flops": route_flops},
+    combine_bytes = A * h * b + 2 * T * h * b + T * k * 8 + w.n_shared * T * h * b
+    work = {"route": {"bytes": route_bytes, "flops": route_flops},
             "dispatch": {"bytes": dispatch_bytes, "flops": 0},
             "ffn": {"bytes": ffn_bytes, "flops": ffn_flops},
             "combine": {"bytes": combine_bytes, "flops": 0}}
+    if w.n_shared:
+        ds = w.d_shared
+        work["shared_ffn"] = {"flops": 6 * T * h * ds * w.n_shared,
+                              "bytes": w.n_shared * (3 * h * ds * b + T * h * b + 2 * T * ds * b + T * h * b)}
+    return work
 
 
 def launches_per_step(w: W.Workload) -> int:
@@ -228,7 +233,9 @@ def oracle_inputs_host(inp: "synth.LayerInputs", U_host, experts=()):
                 W_noise=None if inp.W_noise is None else f(inp.W_noise),
                 eps=None if inp.eps is None else f(inp.eps),
                 W_gate=ExpertsF64(inp.W_gate, experts), W_up=ExpertsF64(inp.W_up, experts),
-                W_down=ExpertsF64(inp.W_down, experts))
+                W_down=ExpertsF64(inp.W_down, experts),
+                sel_bias=None if inp.sel_bias is None else f(inp.sel_bias),
+                shared=None if inp.shared is None else tuple(f(x) for x in inp.shared))
 
 
 def touched_experts(w: W.Workload, host, tokens):
@@ -236,7 +243,7 @@ def touched_experts(w: W.Workload, host, tokens):
     import oracle
     H = oracle.router_logits(host.U[tokens], host.W_r, host.b_r, host.W_noise,
                              None if host.eps is None else host.eps[tokens])
-    return sorted(set(np.unique(oracle.route(H, w.k, w.score_fn, w.renorm)["idx"]).tolist()))
+    return sorted(set(np.unique(oracle.route(H, w.k, w.score_fn, w.renorm, host.sel_bias)["idx"]).tolist()))
 
 
 def oracle_step(w: W.Workload, host, tokens):
@@ -247,7 +254,7 @@ def oracle_step(w: W.Workload, host, tokens):
                W_gate=host.W_gate, W_up=host.W_up, W_down=host.W_down)
     return oracle.layer_forward(sub, T=len(tokens), h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn,
                                 renorm=w.renorm, capacity_factor=w.capacity_factor, capacity_override=w.capacity,
-                                priority=w.priority)
+                                priority=w.priority, sel_bias=host.sel_bias, shared=host.shared)
 
 
 def blas_threads() -> int:
@@ -267,7 +274,8 @@ def cpu_baseline(w: W.Workload, inp, n_tokens: int):
     n_tokens = max(1, min(n_tokens, w.T))
     sub_inp = synth.LayerInputs(U=inp.U[:n_tokens], W_r=inp.W_r, b_r=inp.b_r, W_noise=inp.W_noise,
                                 eps=None if inp.eps is None else inp.eps[:n_tokens],
-                                W_gate=inp.W_gate, W_up=inp.W_up, W_down=inp.W_down)
+                                W_gate=inp.W_gate, W_up=inp.W_up, W_down=inp.W_down, sel_bias=inp.sel_bias,
+                                W_gate_sh=inp.W_gate_sh, W_up_sh=inp.W_up_sh, W_down_sh=inp.W_down_sh)
     host = oracle_inputs_host(sub_inp, oracle.f64(sub_inp.U))
     toks = np.arange(n_tokens)
     for e in touched_experts(w, host, toks):
@@ -285,7 +293,7 @@ def cpu_baseline(w: W.Workload, inp, n_tokens: int):
 
 def ffn_tiles(w: W.Workload) -> str:
     """The grouped-GEMM kernel libmoe picks: 256-row CTA-pair tiles when the mean expert segment is
-    at least 192 rows, else 128-row single-CTA tiles (MOE_FFN_TILES overrides)."""
+    at least 1024 rows, else 128-row single-CTA tiles (MOE_FFN_TILES overrides)."""
     env = os.environ.get("MOE_FFN_TILES", "")
     if env in ("single", "pair"):
         return env + " (MOE_FFN_TILES)"
@@ -299,6 +307,10 @@ def workload_config(w: W.Workload, n_rot: int = 0):
          "score": "softmax" if w.score_fn == W.SOFTMAX else "sigmoid", "renorm": w.renorm, "noisy": w.noisy,
          "capacity_factor": w.capacity_factor, "logit_bias": w.bias, "parallelism": "replicas",
          "ffn_tiles": ffn_tiles(w)}
+    if w.n_shared:
+        c.update(n_shared=w.n_shared, d_shared=w.d_shared)
+    if w.sel_bias != "none":
+        c["selection_bias"] = "loss-free balancing bias ~ N(0, 0.05) on the scores"
     if n_rot:
         c["l2"] = (f"inputs larger than L2: {n_rot} rotating token batches plus "
                    f"{3 * w.E * w.h * w.d_e * w.elem_bytes / 1e9:.2f} GB of expert weights per step")
@@ -360,8 +372,9 @@ def run_b300(args, w: W.Workload):
     bufs = L.LayerBuffers.allocate(cfg, device=device)
 
     def stage_calls(U, ev=None):
-        # the four stage calls of moe_layer_forward, with events between them
-        L.moe_route(cfg, U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, None, None, bufs.idx, bufs.gate, bufs.ws)
+        # the stage calls of moe_layer_forward, with events between them
+        L.moe_route(cfg, U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, None, None, bufs.idx, bufs.gate, bufs.ws,
+                    sel_bias=inp.sel_bias)
         if ev is not None:
             ev[0].record()
         L.moe_dispatch(cfg, U, bufs.idx, bufs.counts_routed, bufs.counts_kept, bufs.offsets, bufs.slot_row,
@@ -371,8 +384,13 @@ def run_b300(args, w: W.Workload):
         L.moe_expert_ffn(cfg, bufs.X, bufs.offsets, inp.W_gate, inp.W_up, inp.W_down, bufs.act, bufs.Y, bufs.ws)
         if ev is not None:
             ev[2].record()
+        if w.n_shared:
+            L.moe_shared_ffn(cfg, U, inp.W_gate_sh, inp.W_up_sh, inp.W_down_sh, bufs.act_shared, bufs.Y_shared,
+                             bufs.ws)
+        if ev is not None:
+            ev[3].record()
         L.moe_combine(cfg, U, bufs.Y, bufs.slot_row, bufs.gate, bufs.counts_routed, bufs.out, bufs.f, bufs.P,
-                      bufs.aux, bufs.ws)
+                      bufs.aux, bufs.ws, z_loss=bufs.z_loss, Y_shared=bufs.Y_shared)
 
     # kept pairs and active experts of each batch (outside any timed region)
     A_of, act_of = [], []
@@ -385,10 +403,8 @@ def run_b300(args, w: W.Workload):
     if code != 0:
         raise SystemExit(f"bench.py: device status {code} during warm-up")
 
-    for i in range(args.warmup):
-        stage_calls(pool[i % n_rot])
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     clocks = ClockSampler(device) if rank == 0 else None
@@ -396,6 +412,9 @@ def run_b300(args, w: W.Workload):
     if clocks:
         clocks.start()
         time.sleep(0.3)
+    # warm-up right before the timed region, so the clocks are at load when timing starts
+    for i in range(args.warmup):
+        stage_calls(pool[i % n_rot])
     barrier(device)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -408,23 +427,45 @@ def run_b300(args, w: W.Workload):
     barrier(device)
     total_ms = t_start.elapsed_time(t_end)
 
-    # end to end through the public call: pinned host tokens in, out (and aux) back, every step
+    # end to end through the public call: every step copies its tokens in from pinned host memory,
+    # runs moe_layer_forward and reads out (and aux) back.  Three streams pipeline the steps: the
+    # copy-in of step j+1 and the copy-out of step j-1 overlap the layer of step j.
+    import dataclasses
     U_host = [torch.empty((w.T, w.h), dtype=w.torch_dtype, pin_memory=True) for _ in range(2)]
     for j in range(2):
         U_host[j].copy_(pool[j])
-    out_host = torch.empty((w.T, w.h), dtype=w.torch_dtype, pin_memory=True)
-    aux_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
-    U_dev = torch.empty_like(inp.U)
+    out_host = [torch.empty((w.T, w.h), dtype=w.torch_dtype, pin_memory=True) for _ in range(2)]
+    aux_host = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    U_dev = [torch.empty_like(inp.U) for _ in range(2)]
+    bset = [bufs, dataclasses.replace(bufs, out=torch.empty_like(bufs.out), aux=torch.empty_like(bufs.aux))]
+    s_in, s_comp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_comp + ev_out:
+        e.record(torch.cuda.current_stream(device))
 
     def e2e_step(j):
-        U_dev.copy_(U_host[j % 2], non_blocking=True)
-        L.moe_layer_forward(cfg, U_dev, inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up, inp.W_down,
-                            bufs)
-        out_host.copy_(bufs.out, non_blocking=True)
-        aux_host.copy_(bufs.aux, non_blocking=True)
+        b = j % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_comp[b])            # the layer two steps back has read U_dev[b]
+            U_dev[b].copy_(U_host[b], non_blocking=True)
+            ev_in[b].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_in[b])
+            s_comp.wait_event(ev_out[b])           # out[b] of two steps back has been read
+            L.moe_layer_forward(cfg, U_dev[b], inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up,
+                                inp.W_down, bset[b], stream=s_comp, sel_bias=inp.sel_bias, shared=inp.shared)
+            ev_comp[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            out_host[b].copy_(bset[b].out, non_blocking=True)
+            aux_host[b].copy_(bset[b].aux, non_blocking=True)
+            ev_out[b].record(s_out)
 
     for j in range(3):
         e2e_step(j)
+    torch.cuda.synchronize(device)
     barrier(device)
     t0 = time.perf_counter()
     for j in range(K):
@@ -443,12 +484,16 @@ def run_b300(args, w: W.Workload):
         return 0
 
     stage_ms = {"route": [], "dispatch": [], "ffn": [], "combine": []}
+    if w.n_shared:
+        stage_ms["shared_ffn"] = []
     for i in range(K):
         e = evs[i]
         stage_ms["route"].append(starts[i].elapsed_time(e[0]))
         stage_ms["dispatch"].append(e[0].elapsed_time(e[1]))
         stage_ms["ffn"].append(e[1].elapsed_time(e[2]))
-        stage_ms["combine"].append(e[2].elapsed_time(ends[i]))
+        if w.n_shared:
+            stage_ms["shared_ffn"].append(e[2].elapsed_time(e[3]))
+        stage_ms["combine"].append(e[3].elapsed_time(ends[i]))
     A_mean = sum(A_of[i % n_rot] for i in range(K)) / K
     act_mean = sum(act_of[i % n_rot] for i in range(K)) / K
     work = stage_work(w, A_mean, act_mean)
@@ -480,6 +525,10 @@ def run_b300(args, w: W.Workload):
         roof = {"bound": "hbm", "achieved": ffn["bytes"] / (ffn_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    if roof["bound"] == "tensor":
+        # the same against the bf16 rate measured under the power cap in a seconds-long loop
+        roof["peak_sustained"] = peaks["bf16_tflops_sustained"]
+        roof["frac_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
     roof["achieved"] = round(roof["achieved"], 2)
     roof["traffic"] = profile_traffic(w.name)
     roof["kernel"] = "grouped SwiGLU expert GEMM: grouped_gemm_tc gate|up + down, both launches of one step"
@@ -496,7 +545,9 @@ def run_b300(args, w: W.Workload):
             "kept_pairs_A": A_mean, "active_experts": act_mean,
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.h * w.elem_bytes,
-                    "d2h_bytes_per_step": w.T * w.h * w.elem_bytes + 4},
+                    "d2h_bytes_per_step": w.T * w.h * w.elem_bytes + 4,
+                    "how": "moe_layer_forward per step with its U copied in from pinned host memory and out + aux "
+                           "copied back; copy-in, layer and copy-out of consecutive steps overlap on three streams"},
             "gpu_launches": launches_per_step(w) * K,
             "clocks": clk}
     if ws_n == 1 and not args.no_cpu_baseline:

@@ -95,6 +95,8 @@ typedef struct moe_config {
   int32_t noisy;          /* nonzero: noisy top-k router (W_noise, eps required) */
   int32_t priority;       /* moe_priority: order in which capacity slots are filled */
   int32_t dtype;          /* moe_dtype of activations and weights */
+  int32_t n_shared;       /* shared experts (every token, no router), 0..16; 0 = none */
+  int32_t d_shared;       /* their intermediate size (multiple of 8) when n_shared > 0 */
 } moe_config;
 
 /* Library version string, e.g. "moe-b300 0.1 sm_103a". */
@@ -115,10 +117,15 @@ moe_status moe_capacity(const moe_config* cfg, int64_t* C);
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Router: logits, scores, top-k and gates for every token.
- * Section 路由器：打分、top-k、加权求和 and section softmax 门控还是 sigmoid 门控.
+ * Section 路由器：打分、top-k、加权求和 and section softmax 门控还是 sigmoid 门控;
+ * the selection bias is section 无辅助损失的负载均衡 (loss-free balancing).
  *   U        [T, h] act dtype         token hidden states
  *   W_r      [h, E] act dtype         router weight (column i = expert i's centroid)
  *   b_r      [E] float32 or NULL      per-expert additive logit bias
+ *   sel_bias [E] float32 or NULL      loss-free balancing bias: when given, the top-k is
+ *                                     taken on score + sel_bias (score = softmax or sigmoid,
+ *                                     float32) while the gates stay the scores; NULL: the
+ *                                     top-k is taken on the logits
  *   W_noise  [h, E] act dtype         noisy router only (cfg->noisy), else ignored
  *   eps      [T, E] float32           noisy router only: the N(0,1) draws
  *   logits_in [T, E] float32 or NULL  stage mode: use these final logits as they
@@ -132,8 +139,16 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
  * the float32 logits.  Also leaves per-block sums of the scores (sigmoid:
  * s_i / sum_j s_j) in `ws` for moe_combine's P_i. */
 moe_status moe_route(const moe_config* cfg, const void* U, const void* W_r, const float* b_r,
-                     const void* W_noise, const float* eps, const float* logits_in,
-                     float* logits_out, int32_t* idx, float* gate, void* ws, moe_stream_t stream);
+                     const float* sel_bias, const void* W_noise, const float* eps,
+                     const float* logits_in, float* logits_out, int32_t* idx, float* gate, void* ws,
+                     moe_stream_t stream);
+
+/* One step of the loss-free balancing bias (section 无辅助损失的负载均衡):
+ *   bias[i] += u * sign(mean(counts_routed) - counts_routed[i]),
+ * the sign taken exactly on the integer counts.  counts_routed [E] int32 (e.g. from
+ * moe_dispatch), bias [E] float32 updated in place; one small kernel on `stream`. */
+moe_status moe_balance_bias_update(const moe_config* cfg, const int32_t* counts_routed, float u,
+                                   float* bias, moe_stream_t stream);
 
 /* Capacity-limited dispatch: per-expert histogram, prefix sums, slots, drop
  * mask, offsets, and the row copy X[row] = U[token].
@@ -209,21 +224,96 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const int32_t* o
                           const void* W_gate, const void* W_up, const void* W_down,
                           void* act, void* Y, void* ws, moe_stream_t stream);
 
+/* Shared experts (section 细粒度专家与共享专家, the shared-expert isolation of
+ * DeepSeekMoE / V3): cfg->n_shared SwiGLU experts that every token passes
+ * through, outside the router.
+ *   U            [T, h] act dtype
+ *   W_gate_shared, W_up_shared [n_shared, d_shared, h] act dtype
+ *   W_down_shared               [n_shared, h, d_shared] act dtype
+ *   act_shared   [T, d_shared] act dtype   scratch (reused for each shared expert)
+ *   Y_shared     [n_shared, T, h] act dtype out   FFN_s(u_t), rounded to act dtype
+ * The same grouped kernels as moe_expert_ffn, with one segment of all T rows. */
+moe_status moe_shared_ffn(const moe_config* cfg, const void* U, const void* W_gate_shared,
+                          const void* W_up_shared, const void* W_down_shared, void* act_shared,
+                          void* Y_shared, void* ws, moe_stream_t stream);
+
 /* Combine and load statistics.
  * Section 从稠密 FFN 到 MoE (h'_t = u_t + sum g FFN), the index_add of the
- * shapes listing, and section 负载均衡辅助损失：推导与梯度 (f, P, aux).
+ * shapes listing, section 负载均衡辅助损失：推导与梯度 (f, P, aux) and section
+ * Router z-loss 与数值稳定 (z_loss).
  *   U        [T, h] act dtype
  *   Y        [T*k, h] act dtype       from moe_expert_ffn
+ *   Y_shared [n_shared, T, h] or NULL from moe_shared_ffn (ignored when cfg->n_shared is 0)
  *   slot_row [T*k] int32, gate [T, k] float32, counts_routed [E] int32
- *   out      [T, h] act dtype out     u_t + sum over kept j (ascending) of gate[t,j] * Y[row],
- *                                     float32 accumulation, one rounding
+ *   out      [T, h] act dtype out     u_t + sum_s Y_shared[s, t] + sum over kept j (ascending)
+ *                                     of gate[t,j] * Y[row], float32 accumulation, one rounding
  *   f        [E] float32 out          counts_routed[i] / (T*k)
  *   P        [E] float32 out          (1/T) sum_t s_{i,t}, from the partial sums moe_route
  *                                     left in this `ws`
- *   aux      [1] float32 out          E * sum_i f_i P_i (the balance loss with alpha = 1) */
-moe_status moe_combine(const moe_config* cfg, const void* U, const void* Y, const int32_t* slot_row,
-                       const float* gate, const int32_t* counts_routed, void* out, float* f,
-                       float* P, float* aux, void* ws, moe_stream_t stream);
+ *   aux      [1] float32 out          E * sum_i f_i P_i (the balance loss with alpha = 1)
+ *   z_loss   [1] float32 out or NULL  (1/T) sum_t (log sum_j exp H_{t,j})^2 over the final
+ *                                     router logits (the router z-loss with c_z = 1), from the
+ *                                     per-block sums moe_route left in this `ws` */
+moe_status moe_combine(const moe_config* cfg, const void* U, const void* Y, const void* Y_shared,
+                       const int32_t* slot_row, const float* gate, const int32_t* counts_routed,
+                       void* out, float* f, float* P, float* aux, float* z_loss, void* ws,
+                       moe_stream_t stream);
+
+/* ---- Backward of the router side (section 路由器：打分、top-k、加权求和, how the
+ * router learns: dL/dg_{i,t} = delta_t^T FFN_i(u_t); section 负载均衡辅助损失：
+ * 推导与梯度, 梯度往哪推; section Router z-loss 与数值稳定). */
+
+/* Backward of moe_combine for the upstream gradient dO = dL/dout:
+ *   dO       [T, h] act dtype
+ *   Y, slot_row, gate                 as given to moe_combine
+ *   d_gate   [T, k] float32 out       dO_t . Y[row] for kept pairs (float32 sum), 0 if dropped
+ *   dY       [T*k, h] act dtype out   row r of a kept pair (t, j): gate[t,j] * dO_t, rounded
+ *                                     once; rows of dropped pairs and rows >= A untouched */
+moe_status moe_combine_backward(const moe_config* cfg, const void* dO, const void* Y,
+                                const int32_t* slot_row, const float* gate, float* d_gate, void* dY,
+                                void* ws, moe_stream_t stream);
+
+/* Gradient of the loss with respect to the router logits H (the top-k set held fixed):
+ *   dH = (dg/dH)^T d_gate + w_aux * d(E sum_i f_i P_i)/dH + w_z * dL_z/dH
+ *   logits   [T, E] float32           the final logits (moe_route's logits_out)
+ *   idx      [T, k] int32, d_gate [T, k] float32 (from moe_combine_backward)
+ *   counts_routed [E] int32           for f_i = counts / (T k); may be NULL when w_aux = 0
+ *   w_aux, w_z                        weights of the balance loss (alpha) and of the z-loss (c_z)
+ *   dH       [T, E] float32 out
+ * The gate part follows cfg->score_fn and cfg->renorm (gates from the scores, also under a
+ * loss-free selection bias); sigmoid P uses s / sum_j s_j. */
+moe_status moe_route_backward(const moe_config* cfg, const float* logits, const int32_t* idx,
+                              const float* d_gate, const int32_t* counts_routed, float w_aux,
+                              float w_z, float* dH, moe_stream_t stream);
+
+/* ---- Backward of the experts and of the permute (section 专家计算：padding、
+ * block-sparse 与 grouped GEMM: the experts' backward is grouped GEMMs too, one
+ * group for the input gradients and one for the weight gradients). */
+
+/* Backward of moe_expert_ffn for dY = dL/dY (bf16 configs; float32 returns MOE_ERR_UNSUPPORTED).
+ *   X, offsets, W_gate, W_up, W_down  as given to moe_expert_ffn
+ *   act      [T*k, d_e] bf16           moe_expert_ffn's act (for dW_down)
+ *   dY       [T*k, h] bf16             rows 0..A-1 read (e.g. from moe_combine_backward)
+ *   d_act    [T*k, d_e] bf16 out       dY W_down[e]
+ *   dG, dUp  [T*k, d_e] bf16 out       d_act * Up * SiLU'(G), d_act * SiLU(G), with G = X W_gate^T
+ *                                      and Up = X W_up^T recomputed
+ *   dX       [T*k, h] bf16 out         dG W_gate[e] + dUp W_up[e]
+ *   dW_gate, dW_up [E, d_e, h] float32 out   dG^T X, dUp^T X over each expert's rows
+ *   dW_down  [E, h, d_e] float32 out   dY^T act over each expert's rows (experts with no rows: 0)
+ * Rows >= A of the row outputs are not written.  All products run on the tensor cores
+ * (bf16 operands, float32 accumulation); the weights are read MN-major where the product
+ * contracts over their other dimension. */
+moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* X, const int32_t* offsets,
+                                   const void* W_gate, const void* W_up, const void* W_down,
+                                   const void* act, const void* dY, void* d_act, void* dG, void* dUp,
+                                   void* dX, float* dW_gate, float* dW_up, float* dW_down, void* ws,
+                                   moe_stream_t stream);
+
+/* Backward of the residual and the permute: dU_t = dO_t + sum over kept j (choice order) of
+ * dX[row(t, j)], float32 accumulation, one rounding.  dO [T, h], dX [T*k, h], slot_row [T*k],
+ * dU [T, h] out (act dtype).  The router's contribution dH W_r^T is not included. */
+moe_status moe_dispatch_backward(const moe_config* cfg, const void* dO, const void* dX,
+                                 const int32_t* slot_row, void* dU, void* ws, moe_stream_t stream);
 
 /* Every input and output of one layer forward (pointer meanings as above). */
 typedef struct moe_layer_args {
@@ -235,10 +325,14 @@ typedef struct moe_layer_args {
   int32_t* slot_row; int32_t* row_token; int64_t* n_dropped;
   void* X; void* act; void* Y;
   void* out; float* f; float* P; float* aux;
+  float* z_loss;                              /* NULL: the z-loss is not written */
+  const float* sel_bias;                      /* NULL: no loss-free selection bias */
+  const void* W_gate_shared; const void* W_up_shared; const void* W_down_shared;
+  void* act_shared; void* Y_shared;           /* used when cfg->n_shared > 0 */
 } moe_layer_args;
 
-/* The whole layer: moe_route, moe_dispatch, moe_expert_ffn, moe_combine in
- * order on `stream`, with no host synchronisation in between. */
+/* The whole layer: moe_route, moe_dispatch, moe_expert_ffn, (moe_shared_ffn,)
+ * moe_combine in order on `stream`, with no host synchronisation in between. */
 moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args* args, void* ws,
                              moe_stream_t stream);
 

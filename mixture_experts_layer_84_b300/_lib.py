@@ -23,8 +23,9 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE =
 MOE_DEV_OK, MOE_DEV_BAD_EXPERT_ID, MOE_DEV_TIMEOUT, MOE_DEV_BAD_ROW, MOE_DEV_BAD_OFFSETS = range(5)
 
 EXPORTS = ("moe_version", "moe_status_string", "moe_last_error", "moe_capacity", "moe_workspace_size",
-           "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine",
-           "moe_layer_forward", "moe_get_device_status")
+           "moe_route", "moe_balance_bias_update", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn",
+           "moe_shared_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status", "moe_combine_backward",
+           "moe_route_backward", "moe_expert_ffn_backward", "moe_dispatch_backward")
 
 
 class MoeError(RuntimeError):
@@ -37,7 +38,8 @@ class moe_config(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("h", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("d_e", ctypes.c_int32), ("capacity_factor", ctypes.c_float), ("capacity", ctypes.c_int32),
                 ("score_fn", ctypes.c_int32), ("renorm", ctypes.c_int32), ("noisy", ctypes.c_int32),
-                ("priority", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("priority", ctypes.c_int32), ("dtype", ctypes.c_int32), ("n_shared", ctypes.c_int32),
+                ("d_shared", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -47,7 +49,8 @@ class moe_layer_args(ctypes.Structure):
     _fields_ = [(n, _P) for n in (
         "U", "W_r", "b_r", "W_noise", "eps", "W_gate", "W_up", "W_down", "logits_out", "idx", "gate",
         "counts_routed", "counts_kept", "offsets", "slot_row", "row_token", "n_dropped", "X", "act", "Y",
-        "out", "f", "P", "aux")]
+        "out", "f", "P", "aux", "z_loss", "sel_bias", "W_gate_shared", "W_up_shared", "W_down_shared",
+        "act_shared", "Y_shared")]
 
 
 def _load() -> ctypes.CDLL:
@@ -66,7 +69,11 @@ def _load() -> ctypes.CDLL:
     lib.moe_workspace_size.restype = S
     lib.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(SZ)]
     lib.moe_route.restype = S
-    lib.moe_route.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
+    lib.moe_route.argtypes = [cfgp] + [_P] * 10 + [_P, _P]
+    lib.moe_balance_bias_update.restype = S
+    lib.moe_balance_bias_update.argtypes = [cfgp, _P, ctypes.c_float, _P, _P]
+    lib.moe_shared_ffn.restype = S
+    lib.moe_shared_ffn.argtypes = [cfgp] + [_P] * 6 + [_P, _P]
     lib.moe_dispatch.restype = S
     lib.moe_dispatch.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
     lib.moe_dispatch_noalloc.restype = S
@@ -74,7 +81,15 @@ def _load() -> ctypes.CDLL:
     lib.moe_expert_ffn.restype = S
     lib.moe_expert_ffn.argtypes = [cfgp] + [_P] * 7 + [_P, _P]
     lib.moe_combine.restype = S
-    lib.moe_combine.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
+    lib.moe_combine.argtypes = [cfgp] + [_P] * 11 + [_P, _P]
+    lib.moe_combine_backward.restype = S
+    lib.moe_combine_backward.argtypes = [cfgp] + [_P] * 6 + [_P, _P]
+    lib.moe_route_backward.restype = S
+    lib.moe_route_backward.argtypes = [cfgp, _P, _P, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P]
+    lib.moe_expert_ffn_backward.restype = S
+    lib.moe_expert_ffn_backward.argtypes = [cfgp] + [_P] * 14 + [_P, _P]
+    lib.moe_dispatch_backward.restype = S
+    lib.moe_dispatch_backward.argtypes = [cfgp] + [_P] * 4 + [_P, _P]
     lib.moe_layer_forward.restype = S
     lib.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), _P, _P]
     lib.moe_get_device_status.restype = S
@@ -99,14 +114,15 @@ def _check(status: int) -> None:
 
 
 def config(T, h, E, k, d_e, *, capacity_factor=0.0, capacity=0, score_fn=W.SOFTMAX, renorm=True, noisy=False,
-           priority=W.PRIORITY_CHOICE_MAJOR, dtype=W.BF16) -> moe_config:
+           priority=W.PRIORITY_CHOICE_MAJOR, dtype=W.BF16, n_shared=0, d_shared=0) -> moe_config:
     return moe_config(int(T), int(h), int(E), int(k), int(d_e), float(capacity_factor), int(capacity),
-                      int(score_fn), int(bool(renorm)), int(bool(noisy)), int(priority), int(dtype))
+                      int(score_fn), int(bool(renorm)), int(bool(noisy)), int(priority), int(dtype), int(n_shared),
+                      int(d_shared))
 
 
 def config_of(w: W.Workload, **override) -> moe_config:
     kw = dict(capacity_factor=w.capacity_factor, capacity=w.capacity, score_fn=w.score_fn, renorm=w.renorm,
-              noisy=w.noisy, priority=w.priority, dtype=w.dtype)
+              noisy=w.noisy, priority=w.priority, dtype=w.dtype, n_shared=w.n_shared, d_shared=w.d_shared)
     kw.update(override)
     T = kw.pop("T", w.T)
     return config(T, w.h, w.E, w.k, w.d_e, **kw)
@@ -154,12 +170,13 @@ def new_workspace(cfg: moe_config, device="cuda") -> torch.Tensor:
     return torch.zeros(max(workspace_size(cfg), 256), dtype=torch.uint8, device=device)
 
 
-def moe_route(cfg, U, W_r, b_r, W_noise, eps, logits_in, logits_out, idx, gate, ws, stream=None):
+def moe_route(cfg, U, W_r, b_r, W_noise, eps, logits_in, logits_out, idx, gate, ws, stream=None, sel_bias=None):
     dt = _act_dtype(cfg)
     T, E, k, h = cfg.T, cfg.E, cfg.k, cfg.h
     _check(lib.moe_route(ctypes.byref(cfg), _ptr(U, "U", dt, T * h) if logits_in is None else None,
                          _ptr(W_r, "W_r", dt, h * E) if logits_in is None else None,
-                         _ptr(b_r, "b_r", torch.float32, E), _ptr(W_noise, "W_noise", dt, h * E),
+                         _ptr(b_r, "b_r", torch.float32, E), _ptr(sel_bias, "sel_bias", torch.float32, E),
+                         _ptr(W_noise, "W_noise", dt, h * E),
                          _ptr(eps, "eps", torch.float32, T * E), _ptr(logits_in, "logits_in", torch.float32, T * E),
                          _ptr(logits_out, "logits_out", torch.float32, T * E), _ptr(idx, "idx", torch.int32, T * k),
                          _ptr(gate, "gate", torch.float32, T * k), _ptr(ws, "ws"), _stream(stream)))
@@ -194,6 +211,21 @@ def moe_dispatch_noalloc(cfg, U, idx, counts_routed, counts_kept, offsets, slot_
                                     _ptr(status, "status", torch.int32, 1), _stream(stream)))
 
 
+def moe_balance_bias_update(cfg, counts_routed, u, bias, stream=None):
+    """bias += u * sign(mean(counts) - counts), in place on the device."""
+    _check(lib.moe_balance_bias_update(ctypes.byref(cfg), _ptr(counts_routed, "counts_routed", torch.int32, cfg.E),
+                                       float(u), _ptr(bias, "bias", torch.float32, cfg.E), _stream(stream)))
+
+
+def moe_shared_ffn(cfg, U, W_gate_sh, W_up_sh, W_down_sh, act_sh, Y_sh, ws, stream=None):
+    dt = _act_dtype(cfg)
+    T, h, ns, ds = cfg.T, cfg.h, cfg.n_shared, cfg.d_shared
+    _check(lib.moe_shared_ffn(ctypes.byref(cfg), _ptr(U, "U", dt, T * h), _ptr(W_gate_sh, "W_gate_sh", dt, ns * ds * h),
+                              _ptr(W_up_sh, "W_up_sh", dt, ns * ds * h), _ptr(W_down_sh, "W_down_sh", dt, ns * h * ds),
+                              _ptr(act_sh, "act_sh", dt, T * ds), _ptr(Y_sh, "Y_sh", dt, ns * T * h), _ptr(ws, "ws"),
+                              _stream(stream)))
+
+
 def moe_expert_ffn(cfg, X, offsets, W_gate, W_up, W_down, act, Y, ws, stream=None):
     dt = _act_dtype(cfg)
     T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
@@ -204,14 +236,57 @@ def moe_expert_ffn(cfg, X, offsets, W_gate, W_up, W_down, act, Y, ws, stream=Non
                               _stream(stream)))
 
 
-def moe_combine(cfg, U, Y, slot_row, gate, counts_routed, out, f, P, aux, ws, stream=None):
+def moe_combine(cfg, U, Y, slot_row, gate, counts_routed, out, f, P, aux, ws, stream=None, z_loss=None,
+                Y_shared=None):
     dt = _act_dtype(cfg)
     T, E, k, h = cfg.T, cfg.E, cfg.k, cfg.h
     _check(lib.moe_combine(ctypes.byref(cfg), _ptr(U, "U", dt, T * h), _ptr(Y, "Y", dt, T * k * h),
+                           _ptr(Y_shared, "Y_shared", dt, cfg.n_shared * T * h),
                            _ptr(slot_row, "slot_row", torch.int32, T * k), _ptr(gate, "gate", torch.float32, T * k),
                            _ptr(counts_routed, "counts_routed", torch.int32, E), _ptr(out, "out", dt, T * h),
                            _ptr(f, "f", torch.float32, E), _ptr(P, "P", torch.float32, E),
-                           _ptr(aux, "aux", torch.float32, 1), _ptr(ws, "ws"), _stream(stream)))
+                           _ptr(aux, "aux", torch.float32, 1), _ptr(z_loss, "z_loss", torch.float32, 1),
+                           _ptr(ws, "ws"), _stream(stream)))
+
+
+def moe_combine_backward(cfg, dO, Y, slot_row, gate, d_gate, dY, ws, stream=None):
+    dt = _act_dtype(cfg)
+    T, k, h = cfg.T, cfg.k, cfg.h
+    _check(lib.moe_combine_backward(ctypes.byref(cfg), _ptr(dO, "dO", dt, T * h), _ptr(Y, "Y", dt, T * k * h),
+                                    _ptr(slot_row, "slot_row", torch.int32, T * k),
+                                    _ptr(gate, "gate", torch.float32, T * k),
+                                    _ptr(d_gate, "d_gate", torch.float32, T * k), _ptr(dY, "dY", dt, T * k * h),
+                                    _ptr(ws, "ws"), _stream(stream)))
+
+
+def moe_route_backward(cfg, logits, idx, d_gate, counts_routed, w_aux, w_z, dH, stream=None):
+    T, E, k = cfg.T, cfg.E, cfg.k
+    _check(lib.moe_route_backward(ctypes.byref(cfg), _ptr(logits, "logits", torch.float32, T * E),
+                                  _ptr(idx, "idx", torch.int32, T * k), _ptr(d_gate, "d_gate", torch.float32, T * k),
+                                  _ptr(counts_routed, "counts_routed", torch.int32, E), float(w_aux), float(w_z),
+                                  _ptr(dH, "dH", torch.float32, T * E), _stream(stream)))
+
+
+def moe_expert_ffn_backward(cfg, X, offsets, W_gate, W_up, W_down, act, dY, d_act, dG, dUp, dX, dW_gate, dW_up,
+                            dW_down, ws, stream=None):
+    dt = _act_dtype(cfg)
+    T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
+    f32 = torch.float32
+    _check(lib.moe_expert_ffn_backward(
+        ctypes.byref(cfg), _ptr(X, "X", dt, T * k * h), _ptr(offsets, "offsets", torch.int32, E + 1),
+        _ptr(W_gate, "W_gate", dt, E * d * h), _ptr(W_up, "W_up", dt, E * d * h), _ptr(W_down, "W_down", dt, E * h * d),
+        _ptr(act, "act", dt, T * k * d), _ptr(dY, "dY", dt, T * k * h), _ptr(d_act, "d_act", dt, T * k * d),
+        _ptr(dG, "dG", dt, T * k * d), _ptr(dUp, "dUp", dt, T * k * d), _ptr(dX, "dX", dt, T * k * h),
+        _ptr(dW_gate, "dW_gate", f32, E * d * h), _ptr(dW_up, "dW_up", f32, E * d * h),
+        _ptr(dW_down, "dW_down", f32, E * h * d), _ptr(ws, "ws"), _stream(stream)))
+
+
+def moe_dispatch_backward(cfg, dO, dX, slot_row, dU, ws, stream=None):
+    dt = _act_dtype(cfg)
+    T, k, h = cfg.T, cfg.k, cfg.h
+    _check(lib.moe_dispatch_backward(ctypes.byref(cfg), _ptr(dO, "dO", dt, T * h), _ptr(dX, "dX", dt, T * k * h),
+                                     _ptr(slot_row, "slot_row", torch.int32, T * k), _ptr(dU, "dU", dt, T * h),
+                                     _ptr(ws, "ws"), _stream(stream)))
 
 
 @dataclasses.dataclass
@@ -233,6 +308,9 @@ class LayerBuffers:
     f: torch.Tensor
     P: torch.Tensor
     aux: torch.Tensor
+    z_loss: torch.Tensor
+    act_shared: Optional[torch.Tensor]
+    Y_shared: Optional[torch.Tensor]
     ws: torch.Tensor
 
     @staticmethod
@@ -252,12 +330,21 @@ class LayerBuffers:
             X=torch.empty((T * k, h), dtype=dt, device=device), act=torch.empty((T * k, d), dtype=dt, device=device),
             Y=torch.empty((T * k, h), dtype=dt, device=device), out=torch.empty((T, h), dtype=dt, device=device),
             f=torch.empty(E, dtype=f32, device=device), P=torch.empty(E, dtype=f32, device=device),
-            aux=torch.empty(1, dtype=f32, device=device), ws=new_workspace(cfg, device))
+            aux=torch.empty(1, dtype=f32, device=device), z_loss=torch.empty(1, dtype=f32, device=device),
+            act_shared=torch.empty((T, cfg.d_shared), dtype=dt, device=device) if cfg.n_shared else None,
+            Y_shared=torch.empty((cfg.n_shared, T, h), dtype=dt, device=device) if cfg.n_shared else None,
+            ws=new_workspace(cfg, device))
 
 
-def moe_layer_forward(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: LayerBuffers, stream=None):
+def moe_layer_forward(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: LayerBuffers, stream=None,
+                      sel_bias=None, shared=None):
+    """The whole layer.  sel_bias: [E] loss-free selection bias; shared: (W_gate_sh, W_up_sh, W_down_sh)."""
     dt = _act_dtype(cfg)
     T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
+    ns, ds = cfg.n_shared, cfg.d_shared
+    if ns and shared is None:
+        raise ValueError("cfg.n_shared > 0 needs the shared experts' weights")
+    sg, su, sd = shared if ns else (None, None, None)
     a = moe_layer_args(
         U=_ptr(U, "U", dt, T * h), W_r=_ptr(W_r, "W_r", dt, h * E), b_r=_ptr(b_r, "b_r", torch.float32, E),
         W_noise=_ptr(W_noise, "W_noise", dt, h * E), eps=_ptr(eps, "eps", torch.float32, T * E),
@@ -274,7 +361,12 @@ def moe_layer_forward(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs
         X=_ptr(bufs.X, "X", dt, T * k * h), act=_ptr(bufs.act, "act", dt, T * k * d),
         Y=_ptr(bufs.Y, "Y", dt, T * k * h), out=_ptr(bufs.out, "out", dt, T * h),
         f=_ptr(bufs.f, "f", torch.float32, E), P=_ptr(bufs.P, "P", torch.float32, E),
-        aux=_ptr(bufs.aux, "aux", torch.float32, 1))
+        aux=_ptr(bufs.aux, "aux", torch.float32, 1), z_loss=_ptr(bufs.z_loss, "z_loss", torch.float32, 1),
+        sel_bias=_ptr(sel_bias, "sel_bias", torch.float32, E),
+        W_gate_shared=_ptr(sg, "W_gate_shared", dt, ns * ds * h), W_up_shared=_ptr(su, "W_up_shared", dt, ns * ds * h),
+        W_down_shared=_ptr(sd, "W_down_shared", dt, ns * h * ds),
+        act_shared=_ptr(bufs.act_shared, "act_shared", dt, T * ds) if ns else None,
+        Y_shared=_ptr(bufs.Y_shared, "Y_shared", dt, ns * T * h) if ns else None)
     _check(lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(a), _ptr(bufs.ws, "ws"), _stream(stream)))
 
 

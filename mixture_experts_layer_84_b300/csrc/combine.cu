@@ -8,9 +8,13 @@
 // E * sum_i f_i P_i.
 //
 // combine_rows: one warp per token, 16-byte vectors; float32 accumulation of
-// u_t + g_0 y_0 + g_1 y_1 + ... in choice order, rounded once.
-// load_stats: one block; P_i sums the router's per-block partials in a fixed
-// order (lane-strided then a butterfly), so it is identical from run to run.
+// u_t + (shared experts' rows) + g_0 y_0 + g_1 y_1 + ... in choice order,
+// rounded once (section 细粒度专家与共享专家: h'_t = u_t + sum_s FFN_s(u_t) +
+// sum_i g_{i,t} FFN_i(u_t)).
+// balance_bias_update: the loss-free balancing step of section 无辅助损失的负载均衡.
+// load_stats: one block per 32 experts (plus the z-loss column); P_i and L_z
+// sum the router's per-block partials in a fixed order, so they are
+// identical from run to run.
 #include <algorithm>
 
 #include "common.cuh"
@@ -22,6 +26,7 @@ constexpr int COMBINE_UNROLL = 2;
 
 template <typename T>
 __global__ void __launch_bounds__(256) combine_rows(const uint4* __restrict__ U, const uint4* __restrict__ Y,
+                                                    const uint4* __restrict__ Y_shared, int n_shared,
                                                     const int32_t* __restrict__ slot_row,
                                                     const float* __restrict__ gate, uint4* __restrict__ out, int64_t n_tok,
                                                     int k, int vpr, int64_t rows_cap, int32_t* status) {
@@ -46,6 +51,19 @@ __global__ void __launch_bounds__(256) combine_rows(const uint4* __restrict__ U,
       for (int u = 0; u < COMBINE_UNROLL; ++u) {
         const int v = base + lane + 32 * u;
         if (v < vpr) Vec16<T>::unpack(ldg_stream(U + t * vpr + v), acc[u]);
+      }
+      // shared experts (every token, weight 1), then the routed experts in choice order
+      for (int sh = 0; sh < n_shared; ++sh) {
+#pragma unroll
+        for (int u = 0; u < COMBINE_UNROLL; ++u) {
+          const int v = base + lane + 32 * u;
+          if (v < vpr) {
+            float y[N];
+            Vec16<T>::unpack(ldg_stream(Y_shared + (static_cast<int64_t>(sh) * n_tok + t) * vpr + v), y);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[u][i] += y[i];
+          }
+        }
       }
       for (int j = 0; j < k; ++j) {
         const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
@@ -73,53 +91,100 @@ __global__ void __launch_bounds__(256) combine_rows(const uint4* __restrict__ U,
 
 constexpr int STATS_THREADS = 1024;
 
-__global__ void __launch_bounds__(STATS_THREADS) load_stats(const float* __restrict__ ppart, int n_parts,
+// Block b owns experts 32b .. 32b+31 (lane = expert): warp w adds rows w, w+32, ... of the
+// router's per-block score sums, then warp 0 adds the 32 warp sums in order.  The block
+// that finishes last (an atomic count, no waiting) forms aux from f and P in expert order,
+// so every result is the same from run to run.
+__global__ void __launch_bounds__(STATS_THREADS) load_stats(const float* __restrict__ ppart,
+                                                            const int32_t* __restrict__ ppart_rows,
                                                             const int32_t* __restrict__ counts_routed, int64_t n_tok,
                                                             int k, int E, float* __restrict__ f,
-                                                            float* __restrict__ P, float* __restrict__ aux) {
-  __shared__ float fp[1024];
+                                                            float* __restrict__ P, float* __restrict__ aux,
+                                                            float* __restrict__ z_loss,
+                                                            int32_t* __restrict__ done_count) {
+  __shared__ float part_s[32][33];
+  __shared__ int last;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int nwarps = blockDim.x / 32;
-  for (int e = warp; e < E; e += nwarps) {
-    float s = 0.f;
-    for (int b = lane; b < n_parts; b += 32) s += ppart[static_cast<int64_t>(b) * E + e];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) {
-      const float Pi = n_tok > 0 ? s / static_cast<float>(n_tok) : 0.f;
-      const float fi = n_tok > 0 ? static_cast<float>(counts_routed[e]) / static_cast<float>(n_tok * k) : 0.f;
-      P[e] = Pi;
-      f[e] = fi;
-      fp[e] = fi * Pi;
+  const int e = blockIdx.x * 32 + lane;  // column E (the last block) holds the z-loss sums
+  const int n_parts = n_tok > 0 ? *ppart_rows : 0;
+  float s = 0.f;
+  if (e <= E)
+    for (int b = warp; b < n_parts; b += 32) s += ppart[static_cast<int64_t>(b) * (E + 1) + e];
+  part_s[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && e <= E) {
+    float tot = 0.f;
+    for (int w = 0; w < 32; ++w) tot += part_s[w][lane];
+    const float mean = n_tok > 0 ? tot / static_cast<float>(n_tok) : 0.f;
+    if (e < E) {
+      P[e] = mean;
+      f[e] = n_tok > 0 ? static_cast<float>(counts_routed[e]) / static_cast<float>(n_tok * k) : 0.f;
+    } else if (z_loss) {
+      *z_loss = mean;
     }
   }
+  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    last = atomicAdd(done_count, 1) == static_cast<int>(gridDim.x) - 1;
+    if (last) *done_count = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (last && threadIdx.x == 0) {
+    __threadfence();
     float a = 0.f;
-    for (int e = 0; e < E; ++e) a += fp[e];
+    for (int i = 0; i < E; ++i) a += __ldcg(f + i) * __ldcg(P + i);
     *aux = static_cast<float>(E) * a;
   }
 }
 
-cudaError_t launch_combine(const Plan& p, const void* U, const void* Y, const int32_t* slot_row, const float* gate,
-                           const int32_t* counts_routed, void* out, float* f, float* P, float* aux, uint8_t* ws,
-                           cudaStream_t s) {
+// b_i += u * sign(mean(c) - c_i), the sign taken exactly on integers: sign(sum_j c_j - E c_i).
+__global__ void __launch_bounds__(1024) balance_bias_update(int E, const int32_t* __restrict__ counts, float u,
+                                                            float* __restrict__ bias) {
+  __shared__ long long part[32];
+  long long s = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s += counts[e];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+  __syncthreads();
+  long long total = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += part[w];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const long long d = total - static_cast<long long>(E) * counts[e];
+    bias[e] += d > 0 ? u : d < 0 ? -u : 0.f;
+  }
+}
+
+cudaError_t launch_balance_bias_update(int E, const int32_t* counts_routed, float u, float* bias, cudaStream_t s) {
+  balance_bias_update<<<1, 1024, 0, s>>>(E, counts_routed, u, bias);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Plan& p, const void* U, const void* Y, const void* Y_shared, const int32_t* slot_row,
+                           const float* gate, const int32_t* counts_routed, void* out, float* f, float* P, float* aux,
+                           float* z_loss, uint8_t* ws, cudaStream_t s) {
   int32_t* status = ws_status(p, ws);
   if (p.T > 0) {
     const int vpr = p.h * (p.bf16 ? 2 : 4) / 16;
     const int64_t want = (p.T + 7) / 8;
     const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(current_sm_count()) * 8));
+    const int n_sh = Y_shared ? p.n_shared : 0;
+    const uint4* ysh = static_cast<const uint4*>(Y_shared);
     if (p.bf16)
-      combine_rows<bf16><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), static_cast<const uint4*>(Y), slot_row,
-                                                gate, static_cast<uint4*>(out), p.T, p.k, vpr, p.Tk, status);
+      combine_rows<bf16><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh,
+                                                slot_row, gate, static_cast<uint4*>(out), p.T, p.k, vpr, p.Tk, status);
     else
-      combine_rows<float><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), static_cast<const uint4*>(Y), slot_row,
-                                                 gate, static_cast<uint4*>(out), p.T, p.k, vpr, p.Tk, status);
+      combine_rows<float><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh,
+                                                 slot_row, gate, static_cast<uint4*>(out), p.T, p.k, vpr, p.Tk,
+                                                 status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const float* ppart = reinterpret_cast<const float*>(ws + p.ws_ppart);
-  load_stats<<<1, STATS_THREADS, 0, s>>>(ppart, p.T > 0 ? p.sel_blocks : 0, counts_routed, p.T, p.k, p.E, f, P, aux);
+  int32_t* done = reinterpret_cast<int32_t*>(ws + p.ws_status + 128);
+  load_stats<<<(p.E + 1 + 31) / 32, STATS_THREADS, 0, s>>>(ppart, ws_ppart_rows(p, ws), counts_routed, p.T, p.k, p.E,
+                                                           f, P, aux, z_loss, done);
   return cudaGetLastError();
 }
 

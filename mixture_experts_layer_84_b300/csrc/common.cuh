@@ -55,6 +55,13 @@ template <> struct Vec16<bf16> {
   }
 };
 
+// Bounds of expert segment e of a grouped FFN: rows offsets[e] .. offsets[e+1], or, with no
+// offsets (a shared expert, E = 1), every row 0 .. rows_cap.
+__device__ __forceinline__ int seg_lo(const int32_t* offsets, int e) { return offsets ? offsets[e] : 0; }
+__device__ __forceinline__ int seg_hi(const int32_t* offsets, int e, int64_t rows_cap) {
+  return offsets ? offsets[e + 1] : static_cast<int>(rows_cap);
+}
+
 // Streaming 16-byte global load that bypasses L1 allocation.
 __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   uint4 v;

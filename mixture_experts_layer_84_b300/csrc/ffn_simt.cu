@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(256) ffn_simt_f32(const float* __restrict__ A,
     int slot = blockIdx.x, found = -1, mt = 0;
     bool bad = false;
     for (int e = 0; e < E; ++e) {  // every segment is checked before any block writes
-      const int lo = offsets[e], hi = offsets[e + 1];
+      const int lo = seg_lo(offsets, e), hi = seg_hi(offsets, e, rows_cap);
       if (lo < 0 || hi < lo || static_cast<int64_t>(hi) > rows_cap) {
         bad = true;
         continue;
@@ -52,8 +52,8 @@ __global__ void __launch_bounds__(256) ffn_simt_f32(const float* __restrict__ A,
   __syncthreads();
   const int e = s_e;
   if (e < 0) return;
-  const int64_t row0 = static_cast<int64_t>(offsets[e]) + static_cast<int64_t>(s_mt) * SB;
-  const int nrows = min(SB, offsets[e + 1] - static_cast<int>(row0));
+  const int64_t row0 = static_cast<int64_t>(seg_lo(offsets, e)) + static_cast<int64_t>(s_mt) * SB;
+  const int nrows = min(SB, seg_hi(offsets, e, rows_cap) - static_cast<int>(row0));
   const int n0 = blockIdx.y * SB;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   float g[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, up[2][2] = {{0.f, 0.f}, {0.f, 0.f}};

@@ -83,7 +83,10 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+// SiLU(g) * u = g u / (1 + e^-g) with the fast exponential and division intrinsics: their
+// relative error (a few float32 ulps) is far below the bf16 rounding of the result, and the
+// epilogue must keep up with short (16 k-block) tiles; e^-g = inf gives 0, SiLU's limit.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g * u, 1.f + __expf(-g)); }
 
 __device__ __forceinline__ void store_32(bf16* orow, int col0, int n_out, const uint32_t* packed) {
   if (col0 + 32 <= n_out) {
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   // every CTA checks every segment before anything is written
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int lo = offsets[e], hi = offsets[e + 1];
+    const int lo = seg_lo(offsets, e), hi = seg_hi(offsets, e, rows_cap);
     int m = 0;
     if (lo < 0 || hi < lo || static_cast<int64_t>(hi) > rows_cap)
       *bad_flag = 1;
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, nt, mt;
         decode_tile(tab, E, NT, tile, &e, &nt, &mt);
-        const int a_row = offsets[e] + mt * BM;
+        const int a_row = seg_lo(offsets, e) + mt * BM;
         const int b_row = e * b_rows_per_expert + nt * TILE_N;
         for (int kb = 0; kb < KB; ++kb) {
           if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
@@ -255,8 +258,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, nt, mt;
       decode_tile(tab, E, NT, tile, &e, &nt, &mt);
-      const int seg = offsets[e];
-      const int n_e = offsets[e + 1] - seg;
+      const int seg = seg_lo(offsets, e);
+      const int n_e = seg_hi(offsets, e, rows_cap) - seg;
       const bool row_ok = mt * BM + r_local < n_e;
       const int64_t row = static_cast<int64_t>(seg) + mt * BM + r_local;
       // the tcgen05.ld below is warp-collective: the warp leaves together or not at all
@@ -380,7 +383,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   __syncthreads();
   // both CTAs of a pair read the same offsets and reach the same decisions below
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int lo = offsets[e], hi = offsets[e + 1];
+    const int lo = seg_lo(offsets, e), hi = seg_hi(offsets, e, rows_cap);
     int m = 0;
     if (lo < 0 || hi < lo || static_cast<int64_t>(hi) > rows_cap)
       *bad_flag = 1;
@@ -433,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int tile = cid; ok && tile < total; tile += ncl) {
         int e, nt, mt;
         decode_tile(tab, E, NT, tile, &e, &nt, &mt);
-        const int a_row = offsets[e] + mt * P_BM + static_cast<int>(rank) * 128;
+        const int a_row = seg_lo(offsets, e) + mt * P_BM + static_cast<int>(rank) * 128;
         const int b_row = SWIGLU ? e * b_rows_per_expert + nt * TILE_N
                                  : e * b_rows_per_expert + nt * TILE_N + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < KB; ++kb) {
@@ -514,8 +517,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int tile = cid; tile < total; tile += ncl) {
       int e, nt, mt;
       decode_tile(tab, E, NT, tile, &e, &nt, &mt);
-      const int seg = offsets[e];
-      const int n_e = offsets[e + 1] - seg;
+      const int seg = seg_lo(offsets, e);
+      const int n_e = seg_hi(offsets, e, rows_cap) - seg;
       const bool row_ok = mt * P_BM + r_local < n_e;
       const int64_t row = static_cast<int64_t>(seg) + mt * P_BM + r_local;
       // the tcgen05.ld below is warp-collective: the warp leaves together or not at all

@@ -12,7 +12,22 @@ namespace moe {
 // Tile constants shared by the launch plan and the kernels.
 constexpr int route_bt_for(int ep) { return ep <= 256 ? 32 : 8192 / ep; }  // tokens per partial-logits block
 constexpr int route_kc_for(int ep) { return ep <= 128 ? 64 : 8192 / ep; }  // h chunk per pipeline stage
-constexpr int kSelTokens = 32;        // tokens per select block (8 warps x 4)
+// The router's selection kernel: G lanes per token, each with a chunk of <= 32 experts
+// (G = E / 32 rounded up to a power of two), SELECT_THREADS / G tokens per block.
+constexpr int SELECT_THREADS = 256;
+constexpr int select_lanes_for(int E) {
+  return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : E <= 512 ? 16 : 32;
+}
+constexpr int select_tokens_for(int E) { return SELECT_THREADS / select_lanes_for(E); }
+// Shared memory of one select block: [tokens][G * CS] logits (CS = the odd chunk stride) + z.
+constexpr size_t select_smem_bytes(int E) {
+  return sizeof(float) *
+         static_cast<size_t>(select_tokens_for(E)) *
+         (select_lanes_for(E) * ((((E + select_lanes_for(E) - 1) / select_lanes_for(E)) & 1)
+                                     ? (E + select_lanes_for(E) - 1) / select_lanes_for(E) + 2
+                                     : (E + select_lanes_for(E) - 1) / select_lanes_for(E) + 1) +
+          1);
+}
 constexpr int kDispatchChunk = 4096;  // largest number of priority positions per dispatch chunk
 
 // Sizes derived from one moe_config, and the carve-up of the workspace.
@@ -24,6 +39,7 @@ struct Plan {
   bool bf16 = false;
   bool noisy = false;
   int score_fn = 0, renorm = 0, priority = 0;
+  int n_shared = 0, d_shared = 0;  // shared experts and their intermediate size
 
   // router
   int route_ep = 0;        // E rounded up to the router's compile-time width
@@ -46,9 +62,9 @@ struct Plan {
 // Validates the config and fills `plan`; on failure returns the status and a message.
 moe_status make_plan(const moe_config* cfg, Plan* plan, const char** msg);
 
-cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const void* W_noise,
-                         const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
-                         uint8_t* ws, cudaStream_t s);
+cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const float* sel_bias,
+                         const void* W_noise, const float* eps, const float* logits_in, float* logits_out,
+                         int32_t* idx, float* gate, uint8_t* ws, cudaStream_t s);
 
 // Router slice sums U W_r (and U W_noise) on the tensor cores (bf16, p.route_tc_n > 0).
 cudaError_t launch_route_logits_tc(const Plan& p, const void* U, const void* W_r, const void* W_noise, float* part,
@@ -67,9 +83,32 @@ cudaError_t launch_dispatch_noalloc(const Plan& p, const void* U, const int32_t*
 cudaError_t launch_expert_ffn(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                               const void* W_up, const void* W_down, void* act, void* Y, uint8_t* ws, cudaStream_t s);
 
-cudaError_t launch_combine(const Plan& p, const void* U, const void* Y, const int32_t* slot_row, const float* gate,
-                           const int32_t* counts_routed, void* out, float* f, float* P, float* aux, uint8_t* ws,
-                           cudaStream_t s);
+cudaError_t launch_combine(const Plan& p, const void* U, const void* Y, const void* Y_shared, const int32_t* slot_row,
+                           const float* gate, const int32_t* counts_routed, void* out, float* f, float* P, float* aux,
+                           float* z_loss, uint8_t* ws, cudaStream_t s);
+
+// Every shared expert's SwiGLU FFN on all T tokens: Y_sh[s] = FFN_s(U) (act_sh is scratch).
+cudaError_t launch_shared_ffn(const Plan& p, const void* U, const void* W_gate_sh, const void* W_up_sh,
+                              const void* W_down_sh, void* act_sh, void* Y_sh, uint8_t* ws, cudaStream_t s);
+
+// Backward of the combine: d_gate [T, k] = dO_t . Y[row], dY[row] = g dO_t.
+cudaError_t launch_combine_backward(const Plan& p, const void* dO, const void* Y, const int32_t* slot_row,
+                                    const float* gate, float* d_gate, void* dY, uint8_t* ws, cudaStream_t s);
+// Backward of the gates, the aux loss and the z-loss to the router logits: dH [T, E].
+cudaError_t launch_route_backward(const Plan& p, const float* logits, const int32_t* idx, const float* d_gate,
+                                  const int32_t* counts_routed, float w_aux, float w_z, float* dH, cudaStream_t s);
+
+// Backward of the grouped bf16 SwiGLU experts (tcgen05): d_act, dG, dUp, dX and float32 weight gradients.
+cudaError_t launch_ffn_backward_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
+                                   const void* W_up, const void* W_down, const void* act, const void* dY,
+                                   void* d_act, void* dG, void* dUp, void* dX, float* dW_gate, float* dW_up,
+                                   float* dW_down, int32_t* status, cudaStream_t s);
+// dU = dO + the dX rows of each token's kept pairs.
+cudaError_t launch_dispatch_backward(const Plan& p, const void* dO, const void* dX, const int32_t* slot_row, void* dU,
+                                     uint8_t* ws, cudaStream_t s);
+
+// b_i += u * sign(mean(counts) - counts_i) for the loss-free balancing bias.
+cudaError_t launch_balance_bias_update(int E, const int32_t* counts_routed, float u, float* bias, cudaStream_t s);
 
 // Grouped bf16 GEMMs on tcgen05 (both FFN halves); returns cudaErrorNotSupported when the
 // tensor maps cannot be built.
@@ -81,6 +120,10 @@ cudaError_t launch_ffn_simt_f32(const Plan& p, const void* X, const int32_t* off
                                 cudaStream_t s);
 
 inline int32_t* ws_status(const Plan& p, uint8_t* ws) { return reinterpret_cast<int32_t*>(ws + p.ws_status); }
+// Rows of per-block score sums the last router call left in the workspace (read by the statistics).
+inline int32_t* ws_ppart_rows(const Plan& p, uint8_t* ws) {
+  return reinterpret_cast<int32_t*>(ws + p.ws_status + 64);
+}
 
 // Streaming multiprocessors of the current device (148 on B300 if the query fails).
 inline int current_sm_count() {

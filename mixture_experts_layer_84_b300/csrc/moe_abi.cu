@@ -92,6 +92,13 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     return bad(MOE_ERR_INVALID_ARG, "priority %d", cfg->priority);
   if (cfg->capacity < 0) return bad(MOE_ERR_INVALID_ARG, "capacity = %d < 0", cfg->capacity);
   if (!isfinite(cfg->capacity_factor)) return bad(MOE_ERR_INVALID_ARG, "capacity_factor is not finite");
+  if (cfg->n_shared < 0 || cfg->n_shared > 16)
+    return bad(MOE_ERR_INVALID_ARG, "n_shared = %d outside 0..16", cfg->n_shared);
+  if (cfg->n_shared > 0 && (cfg->d_shared < 8 || cfg->d_shared % 8 != 0))
+    return bad(MOE_ERR_UNSUPPORTED, "d_shared = %d must be a positive multiple of 8", cfg->d_shared);
+  if (cfg->n_shared > 0 && cfg->dtype == MOE_BF16 &&
+      static_cast<int64_t>(cfg->n_shared) * std::max(cfg->h, cfg->d_shared) >= (int64_t(1) << 31))
+    return bad(MOE_ERR_UNSUPPORTED, "n_shared * max(h, d_shared) >= 2^31");
   if (cfg->E > 1024) return bad(MOE_ERR_UNSUPPORTED, "E = %d > 1024", cfg->E);
   if (cfg->k > 16) return bad(MOE_ERR_UNSUPPORTED, "k = %d > 16", cfg->k);
   if (cfg->h % 8 != 0 || cfg->d_e % 8 != 0)
@@ -113,6 +120,8 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   q.score_fn = cfg->score_fn;
   q.renorm = cfg->renorm != 0;
   q.priority = cfg->priority;
+  q.n_shared = cfg->n_shared;
+  q.d_shared = cfg->d_shared;
   if (cfg->capacity > 0)
     q.C = cfg->capacity;
   else if (cfg->capacity_factor <= 0.f)
@@ -141,8 +150,8 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 16)));
   }
   q.route_splits = splits;
-  q.sel_tokens = kSelTokens;
-  q.sel_blocks = static_cast<int>((q.T + kSelTokens - 1) / kSelTokens);
+  q.sel_tokens = select_tokens_for(q.E);
+  q.sel_blocks = static_cast<int>((q.T + q.sel_tokens - 1) / q.sel_tokens);
   // dispatch chunks: about two per SM (multiples of 256 positions, 256 .. 4096), so small
   // batches still spread over the GPU and large ones keep the histogram short
   {
@@ -161,7 +170,7 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   q.ws_npart = off;
   if (q.noisy) off += align256(logits_bytes);
   q.ws_ppart = off;
-  off += align256(sizeof(float) * static_cast<size_t>(q.sel_blocks) * q.E);
+  off += align256(sizeof(float) * static_cast<size_t>(q.sel_blocks) * (q.E + 1));
   q.ws_hist = off;
   off += align256(sizeof(int32_t) * static_cast<size_t>(q.n_chunks) * q.E);
   q.ws_wt = off;
@@ -260,6 +269,43 @@ cudaError_t launch_expert_ffn(const Plan& p, const void* X, const int32_t* offse
   return launch_ffn_simt_f32(p, X, offsets, W_gate, W_up, W_down, act, Y, ws_status(p, ws), s);
 }
 
+// Shared expert i is a grouped FFN with one segment of all T rows (no offsets): the same
+// kernels, planned with E = 1, T rows and d_shared.
+cudaError_t launch_shared_ffn(const Plan& p, const void* U, const void* W_gate_sh, const void* W_up_sh,
+                              const void* W_down_sh, void* act_sh, void* Y_sh, uint8_t* ws, cudaStream_t s) {
+  if (p.T == 0 || p.n_shared == 0) return cudaSuccess;
+  Plan q = p;
+  q.E = 1;
+  q.k = 1;
+  q.Tk = p.T;
+  q.d_e = p.d_shared;
+  const size_t es = p.bf16 ? 2 : 4;
+  const size_t w_in = static_cast<size_t>(p.d_shared) * p.h * es;  // one shared expert's W_gate / W_up / W_down
+  for (int i = 0; i < p.n_shared; ++i) {
+    const uint8_t* wg = static_cast<const uint8_t*>(W_gate_sh) + i * w_in;
+    const uint8_t* wu = static_cast<const uint8_t*>(W_up_sh) + i * w_in;
+    const uint8_t* wd = static_cast<const uint8_t*>(W_down_sh) + i * w_in;
+    uint8_t* y = static_cast<uint8_t*>(Y_sh) + static_cast<size_t>(i) * p.T * p.h * es;
+    const cudaError_t e = launch_expert_ffn(q, U, nullptr, wg, wu, wd, act_sh, y, ws, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+moe_status check_shared_args(const char* fn, const Plan& p, const void* U, const void* W_gate_sh, const void* W_up_sh,
+                             const void* W_down_sh, const void* act_sh, const void* Y_sh) {
+  if (p.n_shared == 0) return MOE_OK;
+  const size_t es = p.bf16 ? 2 : 4;
+  const size_t w = p.T > 0 ? static_cast<size_t>(p.n_shared) * p.d_shared * p.h * es : 0;
+  CHECK(check_ptr(fn, "U", U, static_cast<size_t>(p.T) * p.h * es, 16));
+  CHECK(check_ptr(fn, "W_gate_shared", W_gate_sh, w, 16));
+  CHECK(check_ptr(fn, "W_up_shared", W_up_sh, w, 16));
+  CHECK(check_ptr(fn, "W_down_shared", W_down_sh, w, 16));
+  CHECK(check_ptr(fn, "act_shared", act_sh, static_cast<size_t>(p.T) * p.d_shared * es, 16));
+  CHECK(check_ptr(fn, "Y_shared", Y_sh, static_cast<size_t>(p.n_shared) * p.T * p.h * es, 16));
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using moe::Plan;
@@ -296,14 +342,15 @@ MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
 }
 
 MOE_API moe_status moe_route(const moe_config* cfg, const void* U, const void* W_r, const float* b_r,
-                             const void* W_noise, const float* eps, const float* logits_in, float* logits_out,
-                             int32_t* idx, float* gate, void* ws, moe_stream_t stream) {
+                             const float* sel_bias, const void* W_noise, const float* eps, const float* logits_in,
+                             float* logits_out, int32_t* idx, float* gate, void* ws, moe_stream_t stream) {
   static const char* fn = "moe_route";
   Plan p;
   CHECK(moe::plan_or_fail(fn, cfg, &p));
   CHECK(moe::check_route_args(fn, p, U, W_r, W_noise, eps, logits_in, logits_out, idx, gate, ws));
   CHECK(moe::check_ptr(fn, "b_r", b_r, 0, 4));
-  const cudaError_t e = moe::launch_route(p, U, W_r, b_r, W_noise, eps, logits_in, logits_out, idx, gate,
+  CHECK(moe::check_ptr(fn, "sel_bias", sel_bias, 0, 4));
+  const cudaError_t e = moe::launch_route(p, U, W_r, b_r, sel_bias, W_noise, eps, logits_in, logits_out, idx, gate,
                                           static_cast<uint8_t*>(ws), stream);
   return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
 }
@@ -361,15 +408,120 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const in
   return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
 }
 
-MOE_API moe_status moe_combine(const moe_config* cfg, const void* U, const void* Y, const int32_t* slot_row,
-                               const float* gate, const int32_t* counts_routed, void* out, float* f, float* P,
-                               float* aux, void* ws, moe_stream_t stream) {
+MOE_API moe_status moe_combine(const moe_config* cfg, const void* U, const void* Y, const void* Y_shared,
+                               const int32_t* slot_row, const float* gate, const int32_t* counts_routed, void* out,
+                               float* f, float* P, float* aux, float* z_loss, void* ws, moe_stream_t stream) {
   static const char* fn = "moe_combine";
   Plan p;
   CHECK(moe::plan_or_fail(fn, cfg, &p));
   CHECK(moe::check_combine_args(fn, p, U, Y, slot_row, gate, counts_routed, out, f, P, aux, ws));
-  const cudaError_t e = moe::launch_combine(p, U, Y, slot_row, gate, counts_routed, out, f, P, aux,
+  CHECK(moe::check_ptr(fn, "z_loss", z_loss, 0, 4));
+  if (p.n_shared > 0)
+    CHECK(moe::check_ptr(fn, "Y_shared", Y_shared, static_cast<size_t>(p.n_shared) * p.T * p.h * (p.bf16 ? 2 : 4),
+                         16));
+  const cudaError_t e = moe::launch_combine(p, U, Y, p.n_shared > 0 ? Y_shared : nullptr, slot_row, gate,
+                                            counts_routed, out, f, P, aux, z_loss,
                                             static_cast<uint8_t*>(ws), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_shared_ffn(const moe_config* cfg, const void* U, const void* W_gate_shared,
+                                  const void* W_up_shared, const void* W_down_shared, void* act_shared,
+                                  void* Y_shared, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_shared_ffn";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (p.n_shared == 0) return moe::fail(MOE_ERR_INVALID_ARG, "%s: cfg->n_shared is 0", fn);
+  CHECK(moe::check_shared_args(fn, p, U, W_gate_shared, W_up_shared, W_down_shared, act_shared, Y_shared));
+  CHECK(moe::check_ptr(fn, "ws", ws, p.ws_total, 256));
+  const cudaError_t e = moe::launch_shared_ffn(p, U, W_gate_shared, W_up_shared, W_down_shared, act_shared, Y_shared,
+                                               static_cast<uint8_t*>(ws), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_balance_bias_update(const moe_config* cfg, const int32_t* counts_routed, float u, float* bias,
+                                           moe_stream_t stream) {
+  static const char* fn = "moe_balance_bias_update";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (!isfinite(u)) return moe::fail(MOE_ERR_INVALID_ARG, "%s: u is not finite", fn);
+  CHECK(moe::check_ptr(fn, "counts_routed", counts_routed, static_cast<size_t>(p.E) * 4, 4));
+  CHECK(moe::check_ptr(fn, "bias", bias, static_cast<size_t>(p.E) * 4, 4));
+  const cudaError_t e = moe::launch_balance_bias_update(p.E, counts_routed, u, bias, stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_combine_backward(const moe_config* cfg, const void* dO, const void* Y, const int32_t* slot_row,
+                                        const float* gate, float* d_gate, void* dY, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_combine_backward";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  const size_t es = p.bf16 ? 2 : 4;
+  CHECK(moe::check_ptr(fn, "dO", dO, static_cast<size_t>(p.T) * p.h * es, 16));
+  CHECK(moe::check_ptr(fn, "Y", Y, static_cast<size_t>(p.Tk) * p.h * es, 16));
+  CHECK(moe::check_ptr(fn, "slot_row", slot_row, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "gate", gate, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "d_gate", d_gate, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "dY", dY, static_cast<size_t>(p.Tk) * p.h * es, 16));
+  CHECK(moe::check_ptr(fn, "ws", ws, p.ws_total, 256));
+  const cudaError_t e = moe::launch_combine_backward(p, dO, Y, slot_row, gate, d_gate, dY, static_cast<uint8_t*>(ws),
+                                                     stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_route_backward(const moe_config* cfg, const float* logits, const int32_t* idx,
+                                      const float* d_gate, const int32_t* counts_routed, float w_aux, float w_z,
+                                      float* dH, moe_stream_t stream) {
+  static const char* fn = "moe_route_backward";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (!isfinite(w_aux) || !isfinite(w_z)) return moe::fail(MOE_ERR_INVALID_ARG, "%s: w_aux / w_z not finite", fn);
+  CHECK(moe::check_ptr(fn, "logits", logits, static_cast<size_t>(p.T) * p.E * 4, 4));
+  CHECK(moe::check_ptr(fn, "idx", idx, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "d_gate", d_gate, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "counts_routed", counts_routed, w_aux != 0.f ? static_cast<size_t>(p.E) * 4 : 0, 4));
+  CHECK(moe::check_ptr(fn, "dH", dH, static_cast<size_t>(p.T) * p.E * 4, 4));
+  const cudaError_t e = moe::launch_route_backward(p, logits, idx, d_gate, counts_routed, w_aux, w_z, dH, stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* X, const int32_t* offsets,
+                                           const void* W_gate, const void* W_up, const void* W_down, const void* act,
+                                           const void* dY, void* d_act, void* dG, void* dUp, void* dX,
+                                           float* dW_gate, float* dW_up, float* dW_down, void* ws,
+                                           moe_stream_t stream) {
+  static const char* fn = "moe_expert_ffn_backward";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (!p.bf16) return moe::fail(MOE_ERR_UNSUPPORTED, "%s: the expert backward runs on bf16 (tcgen05) only", fn);
+  CHECK(moe::check_ffn_args(fn, p, X, offsets, W_gate, W_up, W_down, act, dY, ws));
+  const size_t rows_d = static_cast<size_t>(p.Tk) * p.d_e * 2, rows_h = static_cast<size_t>(p.Tk) * p.h * 2;
+  const size_t wgrad = p.Tk > 0 ? static_cast<size_t>(p.E) * p.d_e * p.h * 4 : 0;
+  CHECK(moe::check_ptr(fn, "d_act", d_act, rows_d, 16));
+  CHECK(moe::check_ptr(fn, "dG", dG, rows_d, 16));
+  CHECK(moe::check_ptr(fn, "dUp", dUp, rows_d, 16));
+  CHECK(moe::check_ptr(fn, "dX", dX, rows_h, 16));
+  CHECK(moe::check_ptr(fn, "dW_gate", dW_gate, wgrad, 16));
+  CHECK(moe::check_ptr(fn, "dW_up", dW_up, wgrad, 16));
+  CHECK(moe::check_ptr(fn, "dW_down", dW_down, wgrad, 16));
+  const cudaError_t e = moe::launch_ffn_backward_tc(p, X, offsets, W_gate, W_up, W_down, act, dY, d_act, dG, dUp, dX,
+                                                    dW_gate, dW_up, dW_down,
+                                                    moe::ws_status(p, static_cast<uint8_t*>(ws)), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_dispatch_backward(const moe_config* cfg, const void* dO, const void* dX,
+                                         const int32_t* slot_row, void* dU, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_dispatch_backward";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  const size_t es = p.bf16 ? 2 : 4;
+  CHECK(moe::check_ptr(fn, "dO", dO, static_cast<size_t>(p.T) * p.h * es, 16));
+  CHECK(moe::check_ptr(fn, "dX", dX, static_cast<size_t>(p.Tk) * p.h * es, 16));
+  CHECK(moe::check_ptr(fn, "slot_row", slot_row, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "dU", dU, static_cast<size_t>(p.T) * p.h * es, 16));
+  CHECK(moe::check_ptr(fn, "ws", ws, p.ws_total, 256));
+  const cudaError_t e = moe::launch_dispatch_backward(p, dO, dX, slot_row, dU, static_cast<uint8_t*>(ws), stream);
   return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
 }
 
@@ -385,17 +537,26 @@ MOE_API moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args
   CHECK(moe::check_ffn_args(fn, p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, ws));
   CHECK(moe::check_combine_args(fn, p, a->U, a->Y, a->slot_row, a->gate, a->counts_routed, a->out, a->f, a->P,
                                 a->aux, ws));
+  CHECK(moe::check_ptr(fn, "z_loss", a->z_loss, 0, 4));
+  CHECK(moe::check_ptr(fn, "sel_bias", a->sel_bias, 0, 4));
+  CHECK(moe::check_shared_args(fn, p, a->U, a->W_gate_shared, a->W_up_shared, a->W_down_shared, a->act_shared,
+                               a->Y_shared));
   uint8_t* w = static_cast<uint8_t*>(ws);
-  cudaError_t e = moe::launch_route(p, a->U, a->W_r, a->b_r, a->W_noise, a->eps, nullptr, a->logits_out, a->idx,
-                                    a->gate, w, stream);
+  cudaError_t e = moe::launch_route(p, a->U, a->W_r, a->b_r, a->sel_bias, a->W_noise, a->eps, nullptr, a->logits_out,
+                                    a->idx, a->gate, w, stream);
   if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/route", e);
   e = moe::launch_dispatch(p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row, a->row_token,
                            a->X, a->n_dropped, w, stream);
   if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/dispatch", e);
   e = moe::launch_expert_ffn(p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, w, stream);
   if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/expert_ffn", e);
-  e = moe::launch_combine(p, a->U, a->Y, a->slot_row, a->gate, a->counts_routed, a->out, a->f, a->P, a->aux, w,
-                          stream);
+  if (p.n_shared > 0) {
+    e = moe::launch_shared_ffn(p, a->U, a->W_gate_shared, a->W_up_shared, a->W_down_shared, a->act_shared,
+                               a->Y_shared, w, stream);
+    if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/shared_ffn", e);
+  }
+  e = moe::launch_combine(p, a->U, a->Y, p.n_shared > 0 ? a->Y_shared : nullptr, a->slot_row, a->gate,
+                          a->counts_routed, a->out, a->f, a->P, a->aux, a->z_loss, w, stream);
   if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/combine", e);
   return MOE_OK;
 }

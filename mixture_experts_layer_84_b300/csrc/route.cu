@@ -163,139 +163,217 @@ __global__ void __launch_bounds__(256) route_partial_logits(const T* __restrict_
 
 __device__ __forceinline__ float softplus_f32(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
 constexpr int KMAX = 16;
-constexpr int SEL_WARPS = 8;
-constexpr int SEL_TPW = kSelTokens / SEL_WARPS;  // tokens per warp
 
-// One token per warp.  EV = logits held per lane (expert e = lane + 32 m).
-template <int EV>
-__global__ void __launch_bounds__(SEL_WARPS * 32) route_select(
+// (value, expert id) order of the selection: larger value first, equal values
+// by the lower expert id.
+__device__ __forceinline__ bool before(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// Selection over G lanes per token, TB = SELECT_THREADS / G tokens per block.
+//   1. the block stages the tile's final logits in shared memory with
+//      coalesced loads: slice sums added in slice order, + bias, + eps *
+//      softplus(noise slice sums) (or the given logits in stage mode); the
+//      logits also go to logits_out here.  Lane g of a token owns the
+//      expert chunk [g C, (g+1) C), C = ceil(E / G), stored with an odd
+//      stride CS so that the 32 lanes of a warp hit 32 different banks;
+//   2. the G lanes of a token combine their chunks' maxima and exp-sums with
+//      xor shuffles; each lane keeps a running top-KP list of its chunk
+//      (insertion) keyed by the logit, or, given a selection bias (the
+//      loss-free balancing of section 无辅助损失的负载均衡), by score + bias;
+//      the lanes merge their lists (a bitonic merge: the elementwise better
+//      of one list and the other reversed is bitonic and holds the top KP of
+//      both); the gates come from the selected experts' scores; then the
+//      normalised scores are written back;
+//   3. the block adds each expert's column over its tokens in order (the
+//      score sums for P_i), and in column E the tokens' squared log-sum-exp
+//      of the logits (the router z-loss of "MoE 与专家并行", section Router
+//      z-loss 与数值稳定: L_z = (1/T) sum_t LSE(H_t)^2).
+// KP = k rounded up to a power of two (the lists live in registers); ppart
+// rows are E + 1 floats wide.  Scores use the fast exponential (a few ulps;
+// the selection itself compares logits, or score + bias with a margin far
+// above that).
+template <int KP, int G>
+__global__ void __launch_bounds__(SELECT_THREADS) route_select(
     const float* __restrict__ part, const float* __restrict__ npart, int splits, const float* __restrict__ b_r,
-    const float* __restrict__ eps, const float* __restrict__ logits_in, float* __restrict__ logits_out,
-    int32_t* __restrict__ idx, float* __restrict__ gate, float* __restrict__ ppart, int64_t n_tok, int E, int k,
-    int score_fn, int renorm) {
-  __shared__ float red[SEL_WARPS][EV * 32];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  float pacc[EV];
-#pragma unroll
-  for (int m = 0; m < EV; ++m) pacc[m] = 0.f;
+    const float* __restrict__ sel_bias, const float* __restrict__ eps, const float* __restrict__ logits_in,
+    float* __restrict__ logits_out, int32_t* __restrict__ idx, float* __restrict__ gate, float* __restrict__ ppart,
+    int32_t* __restrict__ ppart_rows, int64_t n_tok, int E, int k, int score_fn, int renorm) {
+  constexpr int TB = SELECT_THREADS / G;
+  extern __shared__ float sx[];  // [TB][LD], then zsq[TB]
+  const int C = (E + G - 1) / G;
+  const int CS = (C & 1) ? C + 2 : C + 1;  // odd
+  const int LD = G * CS;
+  float* zsq = sx + TB * LD;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TB;
+  const int rows = static_cast<int>(n_tok - t0 < TB ? n_tok - t0 : TB);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NW = SELECT_THREADS / 32;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ppart_rows = static_cast<int32_t>(gridDim.x);
 
-  for (int tt = 0; tt < SEL_TPW; ++tt) {
-    const int64_t t = (static_cast<int64_t>(blockIdx.x) * SEL_WARPS + warp) * SEL_TPW + tt;
-    if (t >= n_tok) break;  // warp-uniform
-    float v[EV];
-#pragma unroll
-    for (int m = 0; m < EV; ++m) {
-      const int e = lane + 32 * m;
-      float x = -FLT_MAX;
-      if (e < E) {
-        if (logits_in) {
-          x = logits_in[t * E + e];
-        } else {
-          x = 0.f;
-          for (int s = 0; s < splits; ++s) x += part[(static_cast<int64_t>(s) * n_tok + t) * E + e];
-          if (b_r) x += b_r[e];
-          if (npart) {
-            float n = 0.f;
-            for (int s = 0; s < splits; ++s) n += npart[(static_cast<int64_t>(s) * n_tok + t) * E + e];
-            x = fmaf(eps[t * E + e], softplus_f32(n), x);
-          }
-        }
-        if (logits_out) logits_out[t * E + e] = x;
-      }
-      v[m] = x;
-    }
-
-    // scores of every expert (for P) -- softmax over E or independent sigmoids
-    float s[EV];
-    float mx = 0.f, denom_all = 0.f;
-    if (score_fn == MOE_SCORE_SOFTMAX) {
-      float lm = -FLT_MAX;
-#pragma unroll
-      for (int m = 0; m < EV; ++m)
-        if (lane + 32 * m < E) lm = fmaxf(lm, v[m]);
-      mx = warp_max(lm);
-      float ls = 0.f;
-#pragma unroll
-      for (int m = 0; m < EV; ++m) {
-        s[m] = (lane + 32 * m < E) ? expf(v[m] - mx) : 0.f;
-        ls += s[m];
-      }
-      denom_all = warp_sum(ls);
-#pragma unroll
-      for (int m = 0; m < EV; ++m) pacc[m] += s[m] / denom_all;
-    } else {
-      float ls = 0.f;
-#pragma unroll
-      for (int m = 0; m < EV; ++m) {
-        s[m] = (lane + 32 * m < E) ? 1.f / (1.f + expf(-v[m])) : 0.f;
-        ls += s[m];
-      }
-      const float tot = warp_sum(ls);
-#pragma unroll
-      for (int m = 0; m < EV; ++m) pacc[m] += s[m] / tot;
-    }
-
-    // k rounds of arg-max: highest logit, ties to the lower expert id
-    uint32_t taken = 0;
-    float sel_sum = 0.f, my_s = 0.f;
-    int my_e = 0;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      if (j >= k) break;
-      float bv = -FLT_MAX;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int m = 0; m < EV; ++m) {
-        const int e = lane + 32 * m;
-        if (e < E && !((taken >> m) & 1u) && (v[m] > bv || be == 0x7fffffff)) {
-          bv = v[m];
-          be = e;
+  // 1. final logits of the tile; rows t0 .. t0 + rows - 1 are contiguous in every input
+  for (int r = warp; r < rows; r += NW) {
+    const int64_t gr = (t0 + r) * E;
+    for (int e = lane; e < E; e += 32) {
+      const int64_t g = gr + e;
+      float x;
+      if (logits_in) {
+        x = logits_in[g];
+      } else {
+        x = part[g];
+        for (int sp = 1; sp < splits; ++sp) x += part[static_cast<int64_t>(sp) * n_tok * E + g];
+        if (b_r) x += b_r[e];
+        if (npart) {
+          float nz = npart[g];
+          for (int sp = 1; sp < splits; ++sp) nz += npart[static_cast<int64_t>(sp) * n_tok * E + g];
+          x = fmaf(eps[g], softplus_f32(nz), x);
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      const float sj = (score_fn == MOE_SCORE_SOFTMAX) ? expf(bv - mx) / denom_all : 1.f / (1.f + expf(-bv));
-      sel_sum += sj;
-      if (lane == j) {
-        my_e = be;
-        my_s = sj;
-      }
-    }
-    if (lane < k) {
-      idx[t * k + lane] = my_e;
-      gate[t * k + lane] = renorm ? my_s / sel_sum : my_s;
+      if (logits_out) logits_out[g] = x;
+      const int cg = e / C;
+      sx[r * LD + cg * CS + (e - cg * C)] = x;
     }
   }
-
-  // per-block score sums in a fixed order: warps 0..7
-#pragma unroll
-  for (int m = 0; m < EV; ++m) red[warp][lane + 32 * m] = pacc[m];
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float acc = 0.f;
+
+  // 2. G lanes per token: maximum, exp-sum and score denominator, then the top-k
+  const int r = threadIdx.x / G, g = threadIdx.x % G;
+  const bool tok = r < rows;
+  const int e0 = g * C;
+  const int e1 = min(E, e0 + C);
+  float* rowp = sx + r * LD;
+  float* chunk = rowp + g * CS;
+  const bool softmax = score_fn == MOE_SCORE_SOFTMAX;
+  float mx = -INFINITY;
+  if (tok)
+    for (int e = e0; e < e1; ++e) mx = fmaxf(mx, chunk[e - e0]);
 #pragma unroll
-    for (int w = 0; w < SEL_WARPS; ++w) acc += red[w][e];
-    ppart[static_cast<int64_t>(blockIdx.x) * E + e] = acc;
+  for (int o = 1; o < G; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum_exp = 0.f, denom = 0.f;
+  if (tok) {
+    for (int e = e0; e < e1; ++e) {
+      const float x = chunk[e - e0];
+      const float ex = __expf(x - mx);
+      sum_exp += ex;
+      denom += softmax ? ex : 1.f / (1.f + __expf(-x));
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) {
+    sum_exp += __shfl_xor_sync(0xffffffffu, sum_exp, o);
+    denom += __shfl_xor_sync(0xffffffffu, denom, o);
+  }
+  // selection key: the logit, or with a selection bias (loss-free balancing) the score + bias
+  float tv[KP];
+  int ti[KP];
+#pragma unroll
+  for (int j = 0; j < KP; ++j) {
+    tv[j] = -INFINITY;
+    ti[j] = 0x7fffffff;
+  }
+  if (tok) {
+    for (int e = e0; e < e1; ++e) {
+      const float x = chunk[e - e0];
+      const float key =
+          sel_bias ? (softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x))) + sel_bias[e] : x;
+      if (before(key, e, tv[KP - 1], ti[KP - 1])) {
+        float cv = key;
+        int ci = e;
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+          if (before(cv, ci, tv[j], ti[j])) {
+            const float tvj = tv[j];
+            const int tij = ti[j];
+            tv[j] = cv;
+            ti[j] = ci;
+            cv = tvj;
+            ci = tij;
+          }
+        }
+      }
+    }
+  }
+  // combine the G lanes' lists (consecutive lanes of one warp)
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) {
+    float bv[KP];
+    int bi[KP];
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+      bv[j] = __shfl_xor_sync(0xffffffffu, tv[KP - 1 - j], o);  // the partner's list, reversed
+      bi[j] = __shfl_xor_sync(0xffffffffu, ti[KP - 1 - j], o);
+    }
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+      if (before(bv[j], bi[j], tv[j], ti[j])) {
+        tv[j] = bv[j];
+        ti[j] = bi[j];
+      }
+    }
+#pragma unroll
+    for (int st = KP / 2; st > 0; st >>= 1) {
+#pragma unroll
+      for (int j = 0; j < KP; ++j) {
+        if ((j & st) == 0 && before(tv[j + st], ti[j + st], tv[j], ti[j])) {
+          const float tvj = tv[j];
+          const int tij = ti[j];
+          tv[j] = tv[j + st];
+          ti[j] = ti[j + st];
+          tv[j + st] = tvj;
+          ti[j + st] = tij;
+        }
+      }
+    }
+  }
+  if (tok) {
+    // gates from the scores of the selected experts (their logits are in the staged row)
+    float sel_s[KP], sel_sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+      sel_s[j] = 0.f;
+      if (j < k) {
+        const int e = ti[j];
+        const int cg = e / C;
+        const float x = rowp[cg * CS + (e - cg * C)];
+        sel_s[j] = softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x));
+        sel_sum += sel_s[j];
+      }
+    }
+    const int64_t t = t0 + r;
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+      if (j < k && j % G == g) {
+        idx[t * k + j] = ti[j];
+        gate[t * k + j] = renorm ? sel_s[j] / sel_sum : sel_s[j];
+      }
+    }
+  }
+  // every lane has read what it needs from the row before any lane overwrites its chunk
+  __syncwarp();
+  if (tok) {
+    for (int e = e0; e < e1; ++e) {
+      const float x = chunk[e - e0];
+      chunk[e - e0] = (softmax ? __expf(x - mx) : 1.f / (1.f + __expf(-x))) / denom;
+    }
+    if (g == 0) {
+      const float lse = mx + logf(sum_exp);
+      zsq[r] = lse * lse;
+    }
+  }
+  __syncthreads();
+
+  // 3. the tile's score sums and z-loss sum, tokens in order
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    float acc = 0.f;
+    if (e < E) {
+      const int cg = e / C;
+      const float* col = sx + cg * CS + (e - cg * C);
+      for (int i = 0; i < rows; ++i) acc += col[i * LD];
+    } else {
+      for (int i = 0; i < rows; ++i) acc += zsq[i];
+    }
+    ppart[static_cast<int64_t>(blockIdx.x) * (E + 1) + e] = acc;
   }
 }
 
@@ -340,19 +418,38 @@ cudaError_t launch_partial_t(const Plan& p, const void* U, const void* W_r, cons
   return cudaErrorInvalidValue;
 }
 
-template <int EV>
-cudaError_t launch_select_ev(const Plan& p, const float* part, const float* npart, int splits, const float* b_r,
-                             const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
-                             float* ppart, cudaStream_t s) {
-  route_select<EV><<<p.sel_blocks, SEL_WARPS * 32, 0, s>>>(part, npart, splits, b_r, eps, logits_in, logits_out,
-                                                           idx, gate, ppart, p.T, p.E, p.k, p.score_fn, p.renorm);
+template <int KP, int G>
+cudaError_t launch_select_g(const Plan& p, const float* part, const float* npart, int splits, const float* b_r,
+                            const float* sel_bias, const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                            float* ppart, int32_t* rows, cudaStream_t s) {
+  const size_t smem = select_smem_bytes(p.E);
+  auto kern = route_select<KP, G>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<p.sel_blocks, SELECT_THREADS, smem, s>>>(part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx,
+                                                  gate, ppart, rows, p.T, p.E, p.k, p.score_fn, p.renorm);
   return cudaGetLastError();
+}
+
+template <int KP>
+cudaError_t launch_select_kp(const Plan& p, const float* part, const float* npart, int splits, const float* b_r,
+                             const float* sel_bias, const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+                             float* ppart, int32_t* rows, cudaStream_t s) {
+  switch (select_lanes_for(p.E)) {
+#define MOE_SEL_G(gg) \
+  case gg: return launch_select_g<KP, gg>(p, part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx, gate, ppart, rows, s);
+    MOE_SEL_G(1) MOE_SEL_G(2) MOE_SEL_G(4) MOE_SEL_G(8) MOE_SEL_G(16) MOE_SEL_G(32)
+#undef MOE_SEL_G
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const void* W_noise,
-                         const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
+cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const float* sel_bias,
+                         const void* W_noise, const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                          uint8_t* ws, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
   float* part = reinterpret_cast<float*>(ws + p.ws_part);
@@ -368,14 +465,11 @@ cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const fl
     npart = nullptr;
     splits = 0;
   }
-  const int ev = (p.E + 31) / 32;
-  if (ev <= 1) return launch_select_ev<1>(p, part, npart, splits, b_r, eps, logits_in, logits_out, idx, gate, ppart, s);
-  if (ev <= 2) return launch_select_ev<2>(p, part, npart, splits, b_r, eps, logits_in, logits_out, idx, gate, ppart, s);
-  if (ev <= 4) return launch_select_ev<4>(p, part, npart, splits, b_r, eps, logits_in, logits_out, idx, gate, ppart, s);
-  if (ev <= 8) return launch_select_ev<8>(p, part, npart, splits, b_r, eps, logits_in, logits_out, idx, gate, ppart, s);
-  if (ev <= 16)
-    return launch_select_ev<16>(p, part, npart, splits, b_r, eps, logits_in, logits_out, idx, gate, ppart, s);
-  return launch_select_ev<32>(p, part, npart, splits, b_r, eps, logits_in, logits_out, idx, gate, ppart, s);
+  int32_t* rows = ws_ppart_rows(p, ws);
+  if (p.k <= 2) return launch_select_kp<2>(p, part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx, gate, ppart, rows, s);
+  if (p.k <= 4) return launch_select_kp<4>(p, part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx, gate, ppart, rows, s);
+  if (p.k <= 8) return launch_select_kp<8>(p, part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx, gate, ppart, rows, s);
+  return launch_select_kp<16>(p, part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx, gate, ppart, rows, s);
 }
 
 }  // namespace moe

@@ -13,6 +13,9 @@ Recipe (every tensor has its own generator stream, derived from the seed):
   b_r (per-expert logit bias)       [E]       fp32
       zipf:   b_e = 1.5 * ln p(e+1), p(r) = r^-1.1 / sum_{r'<=E} r'^-1.1
       normal: b_e ~ N(0, 0.5)
+  sel_bias (loss-free selection)    [E]       fp32, normal: N(0, 0.05)
+  W_gate_sh, W_up_sh ~ N(0, 0.02)   [n_shared, d_shared, h]  (shared experts)
+  W_down_sh ~ N(0, 0.02)            [n_shared, h, d_shared]
 Draws use torch's own generator on the device the tensors live on (Philox on
 CUDA, Mersenne twister on the CPU), so a given seed yields one fixed set of
 inputs per device type; a check always hands the oracle a copy of the exact
@@ -33,7 +36,8 @@ _MASK63 = (1 << 63) - 1
 _STREAM = {
     "U": 1, "W_r": 2, "W_noise": 3, "eps": 4, "b_r": 5,
     "W_gate": 10, "W_up": 11, "W_down": 12,
-    "redraw_U": 20, "redraw_eps": 21,
+    "redraw_U": 20, "redraw_eps": 21, "sel_bias": 6,
+    "W_gate_sh": 13, "W_up_sh": 14, "W_down_sh": 15,
     "logits": 30, "routing": 31, "gates": 32, "Y": 33, "X": 34,
 }
 
@@ -69,6 +73,15 @@ class LayerInputs:
     W_gate: Optional[torch.Tensor]
     W_up: Optional[torch.Tensor]
     W_down: Optional[torch.Tensor]
+    sel_bias: Optional[torch.Tensor] = None
+    W_gate_sh: Optional[torch.Tensor] = None
+    W_up_sh: Optional[torch.Tensor] = None
+    W_down_sh: Optional[torch.Tensor] = None
+
+    @property
+    def shared(self):
+        """(W_gate_sh, W_up_sh, W_down_sh), or None without shared experts."""
+        return None if self.W_gate_sh is None else (self.W_gate_sh, self.W_up_sh, self.W_down_sh)
 
     def to(self, device) -> "LayerInputs":
         return LayerInputs(**{f.name: (None if getattr(self, f.name) is None
@@ -108,7 +121,19 @@ def generate(w: Workload, seed: int = 0, device="cpu", experts: bool = True) -> 
             W_gate[e] = normal((w.d_e, w.h), std, seed, "W_gate", device, dt, sub=e)
             W_up[e] = normal((w.d_e, w.h), std, seed, "W_up", device, dt, sub=e)
             W_down[e] = normal((w.h, w.d_e), std, seed, "W_down", device, dt, sub=e)
-    return LayerInputs(U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down)
+    sel_bias = normal((w.E,), 0.05, seed, "sel_bias", device, torch.float32) if w.sel_bias == "normal" else None
+    if w.sel_bias not in ("none", "normal"):
+        raise ValueError(f"unknown selection bias kind {w.sel_bias!r}")
+    sh = [None, None, None]
+    if experts and w.n_shared > 0:
+        sh[0] = torch.empty((w.n_shared, w.d_shared, w.h), dtype=dt, device=device)
+        sh[1] = torch.empty((w.n_shared, w.d_shared, w.h), dtype=dt, device=device)
+        sh[2] = torch.empty((w.n_shared, w.h, w.d_shared), dtype=dt, device=device)
+        for i in range(w.n_shared):
+            sh[0][i] = normal((w.d_shared, w.h), std, seed, "W_gate_sh", device, dt, sub=i)
+            sh[1][i] = normal((w.d_shared, w.h), std, seed, "W_up_sh", device, dt, sub=i)
+            sh[2][i] = normal((w.h, w.d_shared), std, seed, "W_down_sh", device, dt, sub=i)
+    return LayerInputs(U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, sel_bias, *sh)
 
 
 def redraw_rows(inp: LayerInputs, rows: torch.Tensor, seed: int, attempt: int) -> None:

@@ -44,6 +44,9 @@ class Workload:
     capacity: int = 0     # > 0 overrides the capacity formula
     priority: int = PRIORITY_CHOICE_MAJOR
     weight_std: float = 0.02
+    n_shared: int = 0     # shared experts (every token, outside the router)
+    d_shared: int = 0     # their intermediate size
+    sel_bias: str = "none"  # loss-free selection bias: none | normal
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -72,6 +75,13 @@ STRESS = Workload("stress_bf16", T=65536, h=4096, E=64, k=6, d_e=1408, dtype=BF1
 
 FULL = [TINY_FP32, MIXTRAL, SWITCH, DSV3, STRESS]
 
+# DeepSeek-V3's full MoE block: the DS-V3 shape plus its one shared expert (d = 2048) and a
+# loss-free balancing bias on the selection ("MoE 与专家并行", sections 细粒度专家与共享专家 and
+# 无辅助损失的负载均衡).
+DSV3_SHARED = DSV3.replace(name="dsv3_shared_bf16", n_shared=1, d_shared=2048, sel_bias="normal")
+DSV3_SHARED_SMALL = DSV3_SHARED.replace(name="dsv3_shared_small", T=600, h=512, d_e=256, d_shared=384)
+EXTENDED = [DSV3_SHARED]
+
 # Reduced twins (same routing rule and precision, oracle-sized).
 MIXTRAL_SMALL = MIXTRAL.replace(name="mixtral_small", T=700, h=512, d_e=640)
 SWITCH_SMALL = SWITCH.replace(name="switch_small", T=3000, h=256, d_e=384)
@@ -84,5 +94,5 @@ SMALL = [TINY_FP32, MIXTRAL_SMALL, SWITCH_SMALL, DSV3_SMALL, STRESS_SMALL]
 # 1 GB on the device, for detailed hardware-counter captures.
 MIXTRAL_NARROW = MIXTRAL.replace(name="mixtral_narrow_bf16", d_e=3584)
 
-BY_NAME = {w.name: w for w in FULL + SMALL + [MIXTRAL_NARROW]}
+BY_NAME = {w.name: w for w in FULL + SMALL + EXTENDED + [MIXTRAL_NARROW, DSV3_SHARED_SMALL]}
 

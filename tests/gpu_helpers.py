@@ -58,15 +58,23 @@ def logits_of(w: W.Workload, inp, rows=None) -> np.ndarray:
                                 None if inp.eps is None else inp.eps[r])
 
 
+def selection_key(w: W.Workload, inp, H) -> np.ndarray:
+    """What the top-k is taken on: the logits, or score + selection bias (loss-free balancing)."""
+    if inp.sel_bias is None:
+        return H
+    return oracle.route(H, w.k, w.score_fn, w.renorm, inp.sel_bias)["sel_key"]
+
+
 def margin_inputs(w: W.Workload, seed: int = 0, device="cuda", experts: bool = True, max_rounds: int = 30):
-    """Layer inputs whose tokens all keep a top-(k+1) logit margin >= MARGIN (in float64).
+    """Layer inputs whose tokens all keep a top-(k+1) margin >= MARGIN (in float64) in the
+    selection key (the logits, or score + selection bias).
 
     Tokens that violate it get fresh U (and eps) rows; returns (inputs, float64 logits).
     """
     inp = synth.generate(w, seed, device, experts=experts)
     H = logits_of(w, inp)
     for attempt in range(max_rounds):
-        bad = np.nonzero(oracle.topk_margins(H, w.k) < MARGIN)[0]
+        bad = np.nonzero(oracle.topk_margins(selection_key(w, inp, H), w.k) < MARGIN)[0]
         if bad.size == 0:
             return inp, H
         synth.redraw_rows(inp, torch.as_tensor(bad, dtype=torch.int64), seed, attempt)

@@ -44,8 +44,8 @@ def test_version_and_status_strings():
 
 
 def test_config_struct_layout():
-    assert ctypes.sizeof(L.moe_config) == 8 + 4 * 11 + 4  # int64 T, 11 x 32-bit fields, tail padding
-    assert ctypes.sizeof(L.moe_layer_args) == 24 * 8
+    assert ctypes.sizeof(L.moe_config) == 8 + 4 * 13 + 4  # int64 T, 13 x 32-bit fields, tail padding
+    assert ctypes.sizeof(L.moe_layer_args) == 31 * 8
 
 
 @pytest.mark.parametrize("w", W.FULL + W.SMALL, ids=lambda w: w.name)
@@ -106,12 +106,12 @@ def test_bad_configs_rejected(kw, status):
 
 def test_null_pointers_rejected_before_any_launch():
     cfg = L.config(64, 64, 8, 2, 64, capacity_factor=1.0)
-    st = L.lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, None, None)
+    st = L.lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, None, None, None)
     assert st == L.MOE_ERR_INVALID_ARG
     assert "U is NULL" in L.lib.moe_last_error().decode()
     assert L.lib.moe_dispatch(ctypes.byref(cfg), *([None] * 11)) == L.MOE_ERR_INVALID_ARG
     assert L.lib.moe_expert_ffn(ctypes.byref(cfg), *([None] * 9)) == L.MOE_ERR_INVALID_ARG
-    assert L.lib.moe_combine(ctypes.byref(cfg), *([None] * 11)) == L.MOE_ERR_INVALID_ARG
+    assert L.lib.moe_combine(ctypes.byref(cfg), *([None] * 13)) == L.MOE_ERR_INVALID_ARG
     assert L.lib.moe_layer_forward(ctypes.byref(cfg), None, None, None) == L.MOE_ERR_INVALID_ARG
     assert L.lib.moe_get_device_status(None, None, None) == L.MOE_ERR_INVALID_ARG
 
@@ -120,6 +120,6 @@ def test_misaligned_pointer_rejected():
     cfg = L.config(64, 64, 8, 2, 64, capacity_factor=1.0, dtype=W.BF16)
     fake = ctypes.c_void_p(0x1000 + 2)  # never dereferenced: validation fails first
     ok = ctypes.c_void_p(0x100000)
-    st = L.lib.moe_route(ctypes.byref(cfg), fake, ok, None, None, None, None, None, ok, ok, ok, None)
+    st = L.lib.moe_route(ctypes.byref(cfg), fake, ok, None, None, None, None, None, None, ok, ok, ok, None)
     assert st == L.MOE_ERR_INVALID_ARG
     assert "aligned" in L.lib.moe_last_error().decode()

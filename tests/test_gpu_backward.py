@@ -1,0 +1,146 @@
+"""Backward of the router side against the oracle: the combine (gate gradients and the gradient
+into the expert outputs) and the router logits (gates, aux loss, z-loss)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import LOGIT_TOL, TOL, normwise
+from mixture_experts_layer_84_b300 import _lib as L
+from mixture_experts_layer_84_b300 import synth
+from mixture_experts_layer_84_b300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,h,E,k,C,dtype", [(700, 512, 8, 2, 200, W.BF16), (333, 136, 6, 3, 0, W.BF16),
+                                             (123, 72, 5, 2, 40, W.F32), (4096, 1024, 64, 6, 300, W.BF16)])
+def test_combine_backward(T, h, E, k, C, dtype):
+    tdt = torch.bfloat16 if dtype == W.BF16 else torch.float32
+    idx = synth.random_routing(T, E, k, seed=T, zipf_s=0.8).numpy()
+    d = oracle.dispatch(idx, E, C if C else T)
+    A = int(d["offsets"][-1])
+    dO = synth.random_rows(T, h, 1, "U", "cuda", tdt)
+    Y = synth.random_rows(T * k, h, 2, "Y", "cuda", tdt)
+    gate = synth.random_gates(T, k, seed=3, device="cuda")
+    slot_row = torch.as_tensor(d["slot_row"], dtype=torch.int32, device="cuda")
+    cfg = L.config(T, h, E, k, 8, capacity=C, dtype=dtype)
+    d_gate = torch.full((T, k), 9.0, dtype=torch.float32, device="cuda")
+    dY = torch.full((T * k, h), 7.0, dtype=tdt, device="cuda")
+    ws = L.new_workspace(cfg)
+    L.moe_combine_backward(cfg, dO, Y, slot_row, gate, d_gate, dY, ws)
+    assert L.moe_get_device_status(ws) == 0
+    ref = oracle.combine_backward(dO, Y, d["slot_row"], gate, k)
+    assert normwise(d_gate, ref["d_gate"]) <= LOGIT_TOL
+    assert np.all(d_gate.cpu().numpy()[d["slot_row"].reshape(T, k) < 0] == 0.0)
+    kept = np.sort(d["slot_row"][d["slot_row"] >= 0])
+    kt = torch.as_tensor(kept, device="cuda")
+    assert normwise(dY[kt], ref["dY"][kept]) <= TOL[dtype]
+    untouched = np.setdiff1d(np.arange(T * k), kept)
+    if untouched.size:
+        assert torch.all(dY[torch.as_tensor(untouched, device="cuda")] == 7.0)
+
+
+@pytest.mark.parametrize("E,k,score_fn,renorm", [(8, 2, W.SOFTMAX, True), (64, 6, W.SOFTMAX, True),
+                                                 (128, 1, W.SOFTMAX, False), (256, 8, W.SIGMOID, True),
+                                                 (32, 4, W.SIGMOID, False), (1000, 16, W.SOFTMAX, True)])
+@pytest.mark.parametrize("w_aux,w_z", [(0.0, 0.0), (0.01, 0.001), (1.0, 1.0)])
+def test_route_backward(E, k, score_fn, renorm, w_aux, w_z):
+    T = 300
+    H = synth.random_logits(T, E, seed=E + k, scale=2.0, tie_fraction=0.1)
+    r = oracle.route(oracle.f64(H), k, score_fn, renorm)
+    counts = np.bincount(r["idx"].reshape(-1), minlength=E)
+    d_gate = synth.normal((T, k), 1.0, seed=E, stream="gates", device="cpu", dtype=torch.float32)
+    cfg = L.config(T, 8, E, k, 8, score_fn=score_fn, renorm=renorm, dtype=W.F32)
+    dH = torch.full((T, E), 5.0, dtype=torch.float32, device="cuda")
+    L.moe_route_backward(cfg, H.cuda(), torch.as_tensor(r["idx"], dtype=torch.int32, device="cuda"), d_gate.cuda(),
+                         torch.as_tensor(counts, dtype=torch.int32, device="cuda"), w_aux, w_z, dH)
+    torch.cuda.synchronize()
+    f = counts / (T * k)
+    want = oracle.router_backward(oracle.f64(H), r["idx"], oracle.f64(d_gate), f, score_fn, renorm, w_aux, w_z)
+    assert normwise(dH, want) <= LOGIT_TOL
+
+
+def test_route_backward_under_selection_bias():
+    """With a loss-free selection bias the gates are still the scores, so the gate gradient is the
+    same function of the (biased) selection."""
+    T, E, k = 200, 64, 4
+    H = synth.random_logits(T, E, seed=5, scale=2.0, tie_fraction=0.0)
+    b = synth.normal((E,), 0.05, seed=5, stream="sel_bias", device="cpu", dtype=torch.float32)
+    r = oracle.route(oracle.f64(H), k, W.SIGMOID, True, oracle.f64(b))
+    d_gate = synth.normal((T, k), 1.0, seed=6, stream="gates", device="cpu", dtype=torch.float32)
+    cfg = L.config(T, 8, E, k, 8, score_fn=W.SIGMOID, renorm=True, dtype=W.F32)
+    dH = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    L.moe_route_backward(cfg, H.cuda(), torch.as_tensor(r["idx"], dtype=torch.int32, device="cuda"), d_gate.cuda(),
+                         None, 0.0, 0.0, dH)
+    torch.cuda.synchronize()
+    want = oracle.gate_backward(oracle.f64(H), r["idx"], oracle.f64(d_gate), W.SIGMOID, True)
+    assert normwise(dH, want) <= LOGIT_TOL
+
+
+EXPERT_BWD = [
+    # T, h, E, k, d_e, capacity (0: unbounded), routing skew
+    (700, 512, 8, 2, 640, 0, 0.0),      # several 128-row tiles per expert, 64-row K tails in the weight grads
+    (333, 136, 6, 2, 200, 0, 1.2),      # h and d_e off the 64/128 grid, skewed segments
+    (300, 256, 96, 3, 384, 0, 0.0),     # many small segments (a few rows each), some experts empty
+    (64, 128, 4, 1, 128, 10, 0.0),      # capacity-limited: every segment shorter than one k-block
+]
+
+
+@pytest.mark.parametrize("T,h,E,k,d_e,C,zipf", EXPERT_BWD)
+def test_expert_ffn_backward(T, h, E, k, d_e, C, zipf):
+    w = W.Workload("bwd", T=T, h=h, E=E, k=k, d_e=d_e, dtype=W.BF16, score_fn=W.SOFTMAX, renorm=True, noisy=False,
+                   capacity_factor=0.0, capacity=C)
+    inp = synth.generate(w, seed=7, device="cuda")
+    idx = synth.random_routing(T, E, k, seed=8, zipf_s=zipf).numpy()
+    d = oracle.dispatch(idx, E, C if C else T)
+    A = int(d["offsets"][-1])
+    Tk = T * k
+    X = torch.zeros((Tk, h), dtype=torch.bfloat16, device="cuda")
+    X[:A] = inp.U[torch.as_tensor(d["row_token"], device="cuda")]
+    offsets = torch.as_tensor(d["offsets"], dtype=torch.int32, device="cuda")
+    cfg = L.config_of(w)
+    ws = L.new_workspace(cfg)
+    act = torch.zeros((Tk, d_e), dtype=torch.bfloat16, device="cuda")
+    Y = torch.zeros((Tk, h), dtype=torch.bfloat16, device="cuda")
+    L.moe_expert_ffn(cfg, X, offsets, inp.W_gate, inp.W_up, inp.W_down, act, Y, ws)
+    dY = torch.full((Tk, h), float("nan"), dtype=torch.bfloat16, device="cuda")  # rows >= A must not be read
+    dY[:A] = synth.random_rows(A, h, 9, "Y", "cuda", torch.bfloat16)
+    bufs = {n: torch.full((Tk, d_e), 7.0, dtype=torch.bfloat16, device="cuda") for n in ("d_act", "dG", "dUp")}
+    dX = torch.full((Tk, h), 7.0, dtype=torch.bfloat16, device="cuda")
+    dW = {n: torch.full(s, 7.0, dtype=torch.float32, device="cuda")
+          for n, s in (("dW_gate", (E, d_e, h)), ("dW_up", (E, d_e, h)), ("dW_down", (E, h, d_e)))}
+    L.moe_expert_ffn_backward(cfg, X, offsets, inp.W_gate, inp.W_up, inp.W_down, act, dY, bufs["d_act"], bufs["dG"],
+                              bufs["dUp"], dX, dW["dW_gate"], dW["dW_up"], dW["dW_down"], ws)
+    assert L.moe_get_device_status(ws) == 0
+    ref = oracle.expert_ffn_backward(X[:A], d["offsets"], inp.W_gate, inp.W_up, inp.W_down, dY[:A], d_e)
+    tol = TOL[W.BF16]
+    for n in ("d_act", "dG", "dUp"):
+        assert normwise(bufs[n][:A], ref[n]) <= tol, n
+    assert normwise(dX[:A], ref["dX"]) <= tol
+    for n in ("dW_gate", "dW_up", "dW_down"):
+        assert normwise(dW[n], ref[n]) <= tol, n
+        # per expert too, so that a small expert cannot hide behind a large one
+        for e in range(E):
+            if d["offsets"][e + 1] > d["offsets"][e]:
+                assert normwise(dW[n][e], ref[n][e]) <= tol, (n, e)
+            else:
+                assert torch.all(dW[n][e] == 0.0), (n, e)
+    assert torch.all(dX[A:] == 7.0)
+
+
+@pytest.mark.parametrize("dtype", [W.BF16, W.F32])
+def test_dispatch_backward(dtype):
+    T, h, E, k = 500, 264, 16, 3
+    tdt = torch.bfloat16 if dtype == W.BF16 else torch.float32
+    idx = synth.random_routing(T, E, k, seed=3, zipf_s=1.0).numpy()
+    d = oracle.dispatch(idx, E, 60)
+    dO = synth.random_rows(T, h, 1, "U", "cuda", tdt)
+    dX = synth.random_rows(T * k, h, 2, "X", "cuda", tdt)
+    dU = torch.empty((T, h), dtype=tdt, device="cuda")
+    cfg = L.config(T, h, E, k, 8, capacity=60, dtype=dtype)
+    ws = L.new_workspace(cfg)
+    L.moe_dispatch_backward(cfg, dO, dX, torch.as_tensor(d["slot_row"], dtype=torch.int32, device="cuda"), dU, ws)
+    assert L.moe_get_device_status(ws) == 0
+    ref = oracle.dispatch_backward(dO, dX, d["slot_row"], k)
+    assert normwise(dU, ref) <= TOL[dtype]

@@ -32,7 +32,8 @@ def test_combine_and_stats(w):
     f = torch.empty(E, dtype=torch.float32, device="cuda")
     P = torch.empty(E, dtype=torch.float32, device="cuda")
     aux = torch.empty(1, dtype=torch.float32, device="cuda")
-    L.moe_combine(cfg, U, Y, slot_row, gate, counts, out, f, P, aux, ws)
+    z = torch.empty(1, dtype=torch.float32, device="cuda")
+    L.moe_combine(cfg, U, Y, slot_row, gate, counts, out, f, P, aux, ws, z_loss=z)
     assert L.moe_get_device_status(ws) == 0
     ref = oracle.combine(U, Y, d["slot_row"], r["gate"], k)
     tol = TOL[w.dtype]
@@ -42,6 +43,8 @@ def test_combine_and_stats(w):
     assert normwise(f, st["f"]) <= 1e-6
     assert normwise(P, st["P"]) <= LOGIT_TOL
     assert abs(float(aux.item()) - st["aux"]) <= LOGIT_TOL * max(1.0, abs(st["aux"]))
+    zl = oracle.router_z_loss(r["logits"])
+    assert abs(float(z.item()) - zl) <= LOGIT_TOL * max(1.0, abs(zl))
 
 
 def test_combine_bad_rows_flagged_and_skipped():

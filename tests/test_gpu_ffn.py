@@ -81,3 +81,25 @@ def test_expert_ffn_rejects_inconsistent_offsets(dtype, tiles, monkeypatch):
         L.moe_expert_ffn(cfg, X, offsets, inp.W_gate, inp.W_up, inp.W_down, act, Y, ws)
         assert L.moe_get_device_status(ws) == L.MOE_DEV_BAD_OFFSETS
         assert torch.all(Y == 7.0) and torch.all(act == 7.0)
+
+
+@pytest.mark.parametrize("tiles", ["single", "pair"])
+@pytest.mark.parametrize("T,h,n_shared,d_shared,dtype", [(600, 512, 1, 384, W.BF16), (1100, 256, 2, 200, W.BF16),
+                                                         (130, 64, 2, 40, W.F32), (1, 128, 1, 64, W.BF16)])
+def test_shared_ffn(T, h, n_shared, d_shared, dtype, tiles, monkeypatch):
+    """moe_shared_ffn: every shared expert's SwiGLU on every token, against the oracle."""
+    if dtype == W.F32 and tiles == "pair":
+        pytest.skip("float32 runs on the CUDA cores")
+    monkeypatch.setenv("MOE_FFN_TILES", tiles)
+    w = W.Workload("shared", T=T, h=h, E=4, k=1, d_e=64, dtype=dtype, score_fn=W.SOFTMAX, renorm=True, noisy=False,
+                   capacity_factor=0.0, n_shared=n_shared, d_shared=d_shared)
+    inp = synth.generate(w, seed=5, device="cuda")
+    cfg = L.config_of(w)
+    act = torch.empty((T, d_shared), dtype=w.torch_dtype, device="cuda")
+    Y = torch.full((n_shared, T, h), 7.0, dtype=w.torch_dtype, device="cuda")
+    ws = L.new_workspace(cfg)
+    L.moe_shared_ffn(cfg, inp.U, inp.W_gate_sh, inp.W_up_sh, inp.W_down_sh, act, Y, ws)
+    assert L.moe_get_device_status(ws) == 0
+    ref = oracle.shared_ffn(inp.U, *inp.shared)
+    for i in range(n_shared):
+        assert normwise(Y[i], ref[i]) <= TOL[dtype], i

@@ -22,14 +22,15 @@ pytestmark = pytest.mark.gpu
 def run_layer(w, inp, with_logits=True):
     cfg = L.config_of(w)
     bufs = L.LayerBuffers.allocate(cfg, with_logits=with_logits)
-    L.moe_layer_forward(cfg, inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up, inp.W_down, bufs)
+    L.moe_layer_forward(cfg, inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up, inp.W_down, bufs,
+                        sel_bias=inp.sel_bias, shared=inp.shared)
     code = L.moe_get_device_status(bufs.ws)
     assert code == 0, f"device status {code}"
     return cfg, bufs
 
 
-def check_routing_and_dispatch(w, bufs, H):
-    r = oracle.route(H, w.k, w.score_fn, w.renorm)
+def check_routing_and_dispatch(w, bufs, H, sel_bias=None):
+    r = oracle.route(H, w.k, w.score_fn, w.renorm, sel_bias)
     C = oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.capacity)
     d = oracle.dispatch(r["idx"], w.E, C, w.priority)
     A = int(d["offsets"][-1])
@@ -47,6 +48,8 @@ def check_routing_and_dispatch(w, bufs, H):
     assert normwise(bufs.f, st["f"]) <= 1e-6
     assert normwise(bufs.P, st["P"]) <= LOGIT_TOL
     assert abs(float(bufs.aux.item()) - st["aux"]) <= LOGIT_TOL * max(1.0, abs(st["aux"]))
+    zl = oracle.router_z_loss(r["logits"])
+    assert abs(float(bufs.z_loss.item()) - zl) <= LOGIT_TOL * max(1.0, abs(zl))
     return r, d, A
 
 
@@ -66,24 +69,36 @@ EDGE = [
 ]
 
 
+EDGE += [
+    W.DSV3_SHARED_SMALL,
+    # two shared experts, softmax router with a selection bias, float32
+    W.Workload("shared2_bias_f32", T=150, h=64, E=6, k=2, d_e=48, dtype=W.F32, score_fn=W.SOFTMAX, renorm=True,
+               noisy=False, capacity_factor=1.0, n_shared=2, d_shared=40, sel_bias="normal"),
+    W.Workload("shared2_bias_bf16", T=413, h=192, E=12, k=3, d_e=136, dtype=W.BF16, score_fn=W.SIGMOID,
+               renorm=False, noisy=True, capacity_factor=1.3, n_shared=2, d_shared=200, sel_bias="normal"),
+]
+
+
 @pytest.mark.parametrize("w", W.SMALL + EDGE, ids=lambda w: w.name)
 def test_layer_small(w):
     inp, H = margin_inputs(w, seed=0)
     cfg, bufs = run_layer(w, inp)
-    r, d, A = check_routing_and_dispatch(w, bufs, H)
+    r, d, A = check_routing_and_dispatch(w, bufs, H, inp.sel_bias)
     ref = oracle.layer_forward(inp, T=w.T, h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn, renorm=w.renorm,
                                capacity_factor=w.capacity_factor, capacity_override=w.capacity,
-                               priority=w.priority, logits=H)
+                               priority=w.priority, logits=H, sel_bias=inp.sel_bias, shared=inp.shared)
     tol = TOL[w.dtype]
     assert torch.equal(bufs.X[:A], inp.U[bufs.row_token[:A].long()])
     assert normwise(bufs.act[:A], ref["act"]) <= tol
     assert normwise(bufs.Y[:A], ref["Y"]) <= tol
     assert normwise(bufs.out, ref["out"]) <= tol
     assert delta_error(bufs.out, inp.U, ref["out"], w.dtype) <= tol
-    # tokens whose every pair was dropped keep exactly their residual
+    if w.n_shared:
+        assert normwise(bufs.Y_shared, ref["Y_shared"]) <= tol
+    # tokens whose every pair was dropped keep exactly their residual (plus the shared experts)
     sr = bufs.slot_row.view(w.T, w.k)
     gone = torch.all(sr < 0, dim=1)
-    if bool(gone.any()):
+    if bool(gone.any()) and not w.n_shared:
         assert torch.equal(bufs.out[gone], inp.U[gone])
 
 
@@ -96,6 +111,7 @@ def test_layer_empty_batch():
     assert int(bufs.n_dropped.item()) == 0
     assert bufs.f.tolist() == [0.0] * w.E and bufs.P.tolist() == [0.0] * w.E
     assert float(bufs.aux.item()) == 0.0
+    assert float(bufs.z_loss.item()) == 0.0
 
 
 def test_layer_deterministic():
@@ -107,14 +123,15 @@ def test_layer_deterministic():
         assert torch.equal(getattr(b1, name), getattr(b2, name)), name
 
 
-SAMPLE = {"mixtral_bf16": 64, "switch_noisy_bf16": 64, "dsv3_bf16": 16, "stress_bf16": 48, "tiny_fp32": 64}
+SAMPLE = {"mixtral_bf16": 64, "switch_noisy_bf16": 64, "dsv3_bf16": 16, "stress_bf16": 48, "tiny_fp32": 64,
+          "dsv3_shared_bf16": 16}
 
 
-@pytest.mark.parametrize("w", W.FULL, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", W.FULL + W.EXTENDED, ids=lambda w: w.name)
 def test_layer_full_size_sampled(w):
     inp, H = margin_inputs(w, seed=0)
     cfg, bufs = run_layer(w, inp, with_logits=True)
-    r, d, A = check_routing_and_dispatch(w, bufs, H)
+    r, d, A = check_routing_and_dispatch(w, bufs, H, inp.sel_bias)
     # permutation property on every kept row, on the device
     assert torch.equal(bufs.X[:A], inp.U[bufs.row_token[:A].long()])
     rng = np.random.default_rng(0)
@@ -124,7 +141,7 @@ def test_layer_full_size_sampled(w):
     dropped = np.nonzero(np.any(sr < 0, axis=1))[0]
     if dropped.size:
         toks = np.unique(np.concatenate([toks, dropped[:4]]))
-    smp = oracle.sampled_outputs(inp, toks, r["idx"], r["gate"], d["slot_row"], w.k)
+    smp = oracle.sampled_outputs(inp, toks, r["idx"], r["gate"], d["slot_row"], w.k, shared=inp.shared)
     tol = TOL[w.dtype]
     tt = torch.as_tensor(toks, device="cuda")
     assert normwise(bufs.out[tt], smp["out"]) <= tol

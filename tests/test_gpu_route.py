@@ -49,6 +49,27 @@ def test_route_stage_mode_all_equal_row():
     assert got[0] == [0, 1, 2, 3, 4] and got[1] == [7, 0, 1, 2, 3]
 
 
+@pytest.mark.parametrize("score_fn", [SM, SG])
+def test_route_stage_mode_masked_experts(score_fn):
+    """Logits of -inf (masked experts) are valid input: they rank last, ties to the lower id,
+    and get zero weight, as in the oracle."""
+    T, E, k = 70, 24, 6
+    logits = synth.random_logits(T, E, seed=11, scale=2.0, tie_fraction=0.0)
+    logits[:, 3::4] = -float("inf")
+    logits[5, :] = -float("inf")
+    logits[5, 7] = 0.25
+    cfg = L.config(T, 8, E, k, 8, score_fn=score_fn, renorm=True, dtype=W.F32)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = L.new_workspace(cfg)
+    L.moe_route(cfg, None, None, None, None, None, logits.cuda(), None, idx, gate, ws)
+    assert L.moe_get_device_status(ws) == 0
+    r = oracle.route(oracle.f64(logits), k, score_fn, True)
+    assert np.array_equal(idx.cpu().numpy(), r["idx"])
+    assert normwise(gate, r["gate"]) <= LOGIT_TOL
+    assert idx[5].tolist() == [7, 0, 1, 2, 3, 4]
+
+
 EXTRA = [
     W.Workload("route_e5_bf16", T=300, h=136, E=5, k=2, d_e=8, dtype=W.BF16, score_fn=SM, renorm=True,
                noisy=False, capacity_factor=1.0),
@@ -76,3 +97,84 @@ def test_route_end_to_end(w):
     assert normwise(logits, H) <= LOGIT_TOL
     assert np.array_equal(idx.cpu().numpy(), r["idx"])
     assert normwise(gate, r["gate"]) <= LOGIT_TOL
+
+
+@pytest.mark.parametrize("w", [W.MIXTRAL_SMALL, W.SWITCH_SMALL, W.DSV3_SMALL], ids=lambda w: w.name)
+def test_route_repeated_calls_on_one_workspace(w):
+    """The tensor-core router splits h over several CTAs per token tile; the CTA that finishes a
+    tile last adds the slices up, using per-tile counters kept in the workspace.  Repeated calls
+    on one workspace must give identical results (the counters return to zero), and the P sums
+    it leaves behind must match the oracle."""
+    inp, H = margin_inputs(w, seed=4, experts=False)
+    cfg = L.config_of(w)
+    T, E, k = w.T, w.E, w.k
+    ws = L.new_workspace(cfg)
+    outs = []
+    for _ in range(3):
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        L.moe_route(cfg, inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, None, None, idx, gate, ws)
+        assert L.moe_get_device_status(ws) == 0
+        outs.append((idx, gate))
+    for idx, gate in outs[1:]:
+        assert torch.equal(idx, outs[0][0]) and torch.equal(gate, outs[0][1])
+    r = oracle.route(H, k, w.score_fn, w.renorm)
+    assert np.array_equal(outs[0][0].cpu().numpy(), r["idx"])
+    # the statistics read the router's per-tile score sums from the same workspace
+    counts = torch.as_tensor(np.bincount(r["idx"].reshape(-1), minlength=E), dtype=torch.int32, device="cuda")
+    f, P, aux = (torch.empty(n, dtype=torch.float32, device="cuda") for n in (E, E, 1))
+    U0 = torch.zeros((T, w.h), dtype=w.torch_dtype, device="cuda")
+    Y0 = torch.zeros((T * k, w.h), dtype=w.torch_dtype, device="cuda")
+    sr = torch.full((T * k,), -1, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, w.h), dtype=w.torch_dtype, device="cuda")
+    z = torch.empty(1, dtype=torch.float32, device="cuda")
+    L.moe_combine(cfg, U0, Y0, sr, outs[0][1], counts, out, f, P, aux, ws, z_loss=z)
+    assert L.moe_get_device_status(ws) == 0
+    st = oracle.load_stats(np.bincount(r["idx"].reshape(-1), minlength=E), r["s"], T, k, w.score_fn)
+    assert normwise(P, st["P"]) <= LOGIT_TOL
+    assert abs(float(aux.item()) - st["aux"]) <= LOGIT_TOL * max(1.0, abs(st["aux"]))
+    zl = oracle.router_z_loss(H)
+    assert abs(float(z.item()) - zl) <= LOGIT_TOL * max(1.0, abs(zl))
+
+
+@pytest.mark.parametrize("T,E,k,score_fn,renorm", [(300, 8, 2, SG, True), (257, 256, 8, SG, True),
+                                                   (180, 64, 6, SM, True), (90, 128, 1, SM, False),
+                                                   (60, 1024, 16, SG, False)])
+def test_route_loss_free_selection_bias(T, E, k, score_fn, renorm):
+    """Loss-free balancing: top-k on score + bias, gates from the scores.  Both sides get the same
+    float32 logits; the rows whose selection keys keep a margin of 1e-4 (a few float32 ulps of a
+    score, well above the float32 score rounding) must select exactly what the oracle selects,
+    and every row's gates must be the scores of the experts it selected."""
+    logits = synth.random_logits(T, E, seed=T + E + 1, scale=2.0, tie_fraction=0.0)
+    bias = synth.normal((E,), 0.05, seed=E, stream="sel_bias", device="cpu", dtype=torch.float32)
+    cfg = L.config(T, 8, E, k, 8, score_fn=score_fn, renorm=renorm, dtype=W.F32)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = L.new_workspace(cfg)
+    L.moe_route(cfg, None, None, None, None, None, logits.cuda(), None, idx, gate, ws, sel_bias=bias.cuda())
+    assert L.moe_get_device_status(ws) == 0
+    r = oracle.route(oracle.f64(logits), k, score_fn, renorm, oracle.f64(bias))
+    ok = oracle.topk_margins(r["sel_key"], k) >= 1e-4
+    assert ok.mean() > 0.5
+    got = idx.cpu().numpy()
+    assert np.array_equal(got[ok], r["idx"][ok])
+    # gates: the (renormalised) scores of whatever was selected
+    sel = np.take_along_axis(r["s"], got.astype(np.int64), axis=1)
+    want = sel / sel.sum(axis=1, keepdims=True) if renorm else sel
+    assert normwise(gate, want) <= LOGIT_TOL
+
+
+@pytest.mark.parametrize("E", [8, 256, 1000])
+def test_balance_bias_update(E):
+    counts = torch.as_tensor(np.random.default_rng(E).integers(0, 50, size=E), dtype=torch.int32)
+    counts[0] = int(counts.sum() - counts[0]) // (E - 1) if E > 1 else counts[0]
+    bias = synth.normal((E,), 0.1, seed=E, stream="sel_bias", device="cpu", dtype=torch.float32)
+    cfg = L.config(64, 8, E, 1, 8, dtype=W.F32)
+    b = bias.cuda()
+    L.moe_balance_bias_update(cfg, counts.cuda(), 0.001, b)
+    torch.cuda.synchronize()
+    want = oracle.balance_bias_update(oracle.f64(bias), counts.numpy(), 0.001)
+    # float32 add of +-u: within one float32 rounding of the float64 update
+    assert np.max(np.abs(oracle.f64(b) - want)) <= 1e-7
+    step = np.sign(oracle.f64(b) - oracle.f64(bias))
+    assert np.array_equal(step, np.sign(want - oracle.f64(bias)))
