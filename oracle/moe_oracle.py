@@ -556,6 +556,49 @@ def dispatch_backward(dO, dX, slot_row, k: int) -> np.ndarray:
     return dU
 
 
+def router_input_backward(U, W_r, dH, W_noise=None, eps=None) -> dict:
+    """Backward of the router linear H = U W_r + b_r (+ eps * softplus(U W_noise)) ([RTR]).
+
+    dU = dH W_r^T (+ dN W_noise^T), dW_r = U^T dH, db_r = sum_t dH, dW_noise = U^T dN with
+    dN = dH * eps * sigmoid(U W_noise) (softplus' = sigmoid).
+    """
+    U, W_r, dH = f64(U), f64(W_r), f64(dH)
+    out = dict(dU=dH @ W_r.T, dW_r=U.T @ dH, db_r=dH.sum(axis=0), dW_noise=None)
+    if W_noise is not None:
+        with np.errstate(over="ignore"):
+            sg = 1.0 / (1.0 + np.exp(-(U @ f64(W_noise))))
+        dN = dH * f64(eps) * sg
+        out["dU"] = out["dU"] + dN @ f64(W_noise).T
+        out["dW_noise"] = U.T @ dN
+    return out
+
+
+def layer_backward(inp, fwd: dict, dO, *, k: int, d_e: int, score_fn: int, renorm: bool, w_aux: float = 0.0,
+                   w_z: float = 0.0) -> dict:
+    """Gradients of L = <dO, out> + w_aux E sum_i f_i P_i + w_z L_z through the whole layer, with
+    the routing decisions (top-k set, slots, drops) held fixed.  `fwd` is layer_forward's result.
+    [GRD], [BWD], [SHR], [RTR]
+    """
+    cb = combine_backward(dO, fwd["Y"], fwd["slot_row"], fwd["gate"], k)
+    dH = router_backward(fwd["logits"], fwd["idx"], cb["d_gate"], fwd["f"], score_fn, renorm, w_aux, w_z)
+    eb = expert_ffn_backward(fwd["X"], fwd["offsets"], inp.W_gate, inp.W_up, inp.W_down, cb["dY"], d_e)
+    rb = router_input_backward(inp.U, inp.W_r, dH, inp.W_noise, inp.eps)
+    dU = dispatch_backward(dO, eb["dX"], fwd["slot_row"], k) + rb["dU"]
+    out = dict(dU=dU, d_gate=cb["d_gate"], dY=cb["dY"], dH=dH, dW_r=rb["dW_r"], db_r=rb["db_r"],
+               dW_noise=rb["dW_noise"], **{n: eb[n] for n in ("d_act", "dG", "dUp", "dX", "dW_gate", "dW_up",
+                                                              "dW_down")})
+    shared = getattr(inp, "shared", None)
+    if shared is not None:
+        Wg, Wu, Wd = shared
+        sh = [swiglu_backward(inp.U, Wg[i], Wu[i], Wd[i], dO) for i in range(len(Wg))]
+        for b in sh:
+            out["dU"] = out["dU"] + b["dx"]
+        out["dW_gate_sh"] = np.stack([b["dW_gate"] for b in sh])
+        out["dW_up_sh"] = np.stack([b["dW_up"] for b in sh])
+        out["dW_down_sh"] = np.stack([b["dW_down"] for b in sh])
+    return out
+
+
 def topk_margins(H32: np.ndarray, k: int) -> np.ndarray:
     """Smallest gap between adjacent values among each row's k+1 largest logits.
 

@@ -656,4 +656,70 @@ def pin_expert_and_dispatch_backward_segments(O):
     assert np.allclose(dU, want, atol=1e-12)
 
 
+def _torch_layer_loss(t, fwd, dO, *, T, E, k, score_fn, renorm, w_aux, w_z, noisy):
+    """The layer written with torch ops for autograd, routing decisions (idx, slots) fixed."""
+    import torch
+    H = t["U"] @ t["W_r"] + t["b_r"]
+    if noisy:
+        H = H + torch.tensor(fwd["eps"]) * torch.nn.functional.softplus(t["U"] @ t["W_noise"])
+    s = torch.softmax(H, dim=1) if score_fn == 0 else torch.sigmoid(H)
+    idx = torch.tensor(fwd["idx"], dtype=torch.int64)
+    sel = torch.gather(s, 1, idx)
+    g = sel / sel.sum(dim=1, keepdim=True) if renorm else sel
+    out = t["U"].clone()
+    sr = fwd["slot_row"].reshape(T, k)
+    for tok in range(T):
+        for j in range(k):
+            if sr[tok, j] >= 0:
+                e = int(idx[tok, j])
+                u = t["U"][tok]
+                y = (torch.nn.functional.silu(t["W_gate"][e] @ u) * (t["W_up"][e] @ u)) @ t["W_down"][e].T
+                out[tok] = out[tok] + g[tok, j] * y
+    if "W_gate_sh" in t:
+        for i in range(t["W_gate_sh"].shape[0]):
+            out = out + (torch.nn.functional.silu(t["U"] @ t["W_gate_sh"][i].T) *
+                         (t["U"] @ t["W_up_sh"][i].T)) @ t["W_down_sh"][i].T
+    loss = (out * torch.tensor(dO)).sum()
+    f = torch.tensor(fwd["counts_routed"] / (T * k))
+    sp = s / s.sum(dim=1, keepdim=True) if score_fn == 1 else s
+    loss = loss + w_aux * E * (f * sp.mean(dim=0)).sum() + w_z * (torch.logsumexp(H, dim=1) ** 2).mean()
+    return loss
+
+
+def pin_layer_backward_autograd(O):
+    """layer_backward against torch autograd of the layer written with torch ops (softplus, softmax /
+    sigmoid, silu, matmul, logsumexp; float64), routing decisions held fixed: softmax+renorm with
+    drops and the noisy router, and sigmoid with a shared expert."""
+    import torch
+    rng = _rng(67)
+    T, h, E, k, d = 7, 5, 4, 2, 3
+    for score_fn, renorm, noisy, shared, C in ((0, True, True, False, 3), (1, True, False, True, 0), (0, False, False, False, 0)):
+        v = dict(U=rng.normal(size=(T, h)), W_r=rng.normal(size=(h, E)), b_r=rng.normal(size=E),
+                 W_noise=rng.normal(size=(h, E)) if noisy else None, eps=rng.normal(size=(T, E)) if noisy else None,
+                 W_gate=rng.normal(size=(E, d, h)), W_up=rng.normal(size=(E, d, h)), W_down=rng.normal(size=(E, h, d)))
+        inp = _inputs(**v)
+        if shared:
+            inp.shared = (rng.normal(size=(1, d, h)), rng.normal(size=(1, d, h)), rng.normal(size=(1, h, d)))
+        fwd = O.layer_forward(inp, T=T, h=h, E=E, k=k, d_e=d, score_fn=score_fn, renorm=renorm, capacity_factor=0.0,
+                              capacity_override=C, shared=getattr(inp, "shared", None))
+        fwd["eps"] = v["eps"]
+        dO = rng.normal(size=(T, h))
+        w_aux, w_z = 0.3, 0.2
+        g = O.layer_backward(inp, fwd, dO, k=k, d_e=d, score_fn=score_fn, renorm=renorm, w_aux=w_aux, w_z=w_z)
+        t = {n: torch.tensor(x, requires_grad=True) for n, x in v.items() if x is not None and n != "eps"}
+        if shared:
+            for n, x in zip(("W_gate_sh", "W_up_sh", "W_down_sh"), inp.shared):
+                t[n] = torch.tensor(x, requires_grad=True)
+        _torch_layer_loss(t, fwd, dO, T=T, E=E, k=k, score_fn=score_fn, renorm=renorm, w_aux=w_aux, w_z=w_z,
+                          noisy=noisy).backward()
+        pairs = [("dU", "U"), ("dW_r", "W_r"), ("db_r", "b_r"), ("dW_gate", "W_gate"), ("dW_up", "W_up"),
+                 ("dW_down", "W_down")]
+        if noisy:
+            pairs.append(("dW_noise", "W_noise"))
+        if shared:
+            pairs += [("dW_gate_sh", "W_gate_sh"), ("dW_up_sh", "W_up_sh"), ("dW_down_sh", "W_down_sh")]
+        for mine, ref in pairs:
+            assert np.allclose(g[mine], t[ref].grad.numpy(), rtol=1e-6, atol=1e-6), (score_fn, renorm, mine)
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -161,6 +161,15 @@ def _dispatch_backward_no_residual(dO, dX, slot_row, k):
     return _orig["dispatch_backward"](np.zeros_like(np.asarray(dO, dtype=np.float64)), dX, slot_row, k)
 
 
+def _router_input_backward_no_noise_factor(U, W_r, dH, W_noise=None, eps=None):
+    r = _orig["router_input_backward"](U, W_r, dH, None, None)
+    if W_noise is not None:
+        dN = np.asarray(dH, dtype=np.float64) * np.asarray(eps, dtype=np.float64)  # softplus' dropped
+        r["dU"] = r["dU"] + dN @ np.asarray(W_noise, dtype=np.float64).T
+        r["dW_noise"] = np.asarray(U, dtype=np.float64).T @ dN
+    return r
+
+
 MUTANTS = {
     "gates_not_renormalised": ("gates", _gates_no_renorm),
     "ties_to_higher_id": ("topk_select", _topk_ties_high),
@@ -190,6 +199,7 @@ MUTANTS = {
     "combine_backward_ignores_gate": ("combine_backward", _combine_backward_no_gate),
     "silu_derivative_missing_term": ("swiglu_backward", _swiglu_backward_sigmoid_only),
     "dispatch_backward_drops_residual": ("dispatch_backward", _dispatch_backward_no_residual),
+    "noise_branch_without_softplus_derivative": ("router_input_backward", _router_input_backward_no_noise_factor),
 }
 
 
