@@ -230,7 +230,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const int32_t* o
  *   U            [T, h] act dtype
  *   W_gate_shared, W_up_shared [n_shared, d_shared, h] act dtype
  *   W_down_shared               [n_shared, h, d_shared] act dtype
- *   act_shared   [T, d_shared] act dtype   scratch (reused for each shared expert)
+ *   act_shared   [n_shared, T, d_shared] act dtype out   SiLU(G) * Up of each shared expert
  *   Y_shared     [n_shared, T, h] act dtype out   FFN_s(u_t), rounded to act dtype
  * The same grouped kernels as moe_expert_ffn, with one segment of all T rows. */
 moe_status moe_shared_ffn(const moe_config* cfg, const void* U, const void* W_gate_shared,
@@ -315,6 +315,18 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* X, const i
 moe_status moe_dispatch_backward(const moe_config* cfg, const void* dO, const void* dX,
                                  const int32_t* slot_row, void* dU, void* ws, moe_stream_t stream);
 
+/* Backward of the router linear H = U W_r + b_r (+ eps * softplus(U W_noise)), bf16 configs:
+ *   dH       [T, E] float32           from moe_route_backward
+ *   dU_router [T, h] bf16 out         dH W_r^T (+ dN W_noise^T), dN = dH * eps * sigmoid(U W_noise)
+ *   dW_r     [h, E] float32 out       U^T dH;   dW_noise [h, E] float32 out (noisy): U^T dN
+ *   db_r     [E] float32 out or NULL  sum over tokens of dH
+ * The products run on the tensor cores with dH (and dN) rounded to bf16; the noise logits
+ * are recomputed. */
+moe_status moe_router_input_backward(const moe_config* cfg, const void* U, const void* W_r,
+                                     const void* W_noise, const float* eps, const float* dH,
+                                     void* dU_router, float* dW_r, float* dW_noise, float* db_r,
+                                     void* ws, moe_stream_t stream);
+
 /* Every input and output of one layer forward (pointer meanings as above). */
 typedef struct moe_layer_args {
   const void* U; const void* W_r; const float* b_r; const void* W_noise; const float* eps;
@@ -335,6 +347,33 @@ typedef struct moe_layer_args {
  * moe_combine in order on `stream`, with no host synchronisation in between. */
 moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args* args, void* ws,
                              moe_stream_t stream);
+
+/* Gradients and scratch of one layer backward (bf16 configs).  Scratch is caller-owned. */
+typedef struct moe_layer_grads {
+  const void* dO;        /* [T, h]   dL/dout */
+  float w_aux, w_z;      /* weights of E*sum f P and of the z-loss in the loss */
+  float* d_gate;         /* [T, k] scratch */
+  void* dY;              /* [T*k, h] scratch */
+  float* dH;             /* [T, E] out: dL/d(router logits) */
+  void* d_act; void* dG; void* dUp;   /* [T*k, d_e] scratch */
+  void* dX;              /* [T*k, h] scratch */
+  void* dU_router;       /* [T, h] scratch */
+  void* d_act_shared; void* dG_shared; void* dUp_shared;  /* [T, d_shared] scratch (n_shared > 0) */
+  void* dX_shared;       /* [n_shared, T, h] scratch */
+  void* dU;              /* [T, h] out: dL/dU */
+  float* dW_gate; float* dW_up; float* dW_down;          /* out, float32, shapes of the weights */
+  float* dW_r; float* db_r; float* dW_noise;             /* out [h, E], [E] or NULL, [h, E] (noisy) */
+  float* dW_gate_shared; float* dW_up_shared; float* dW_down_shared;  /* out (n_shared > 0) */
+} moe_layer_grads;
+
+/* The whole backward for L = <dO, out> + w_aux E sum_i f_i P_i + w_z L_z, the routing decisions
+ * of the forward held fixed: moe_combine_backward, moe_route_backward, moe_expert_ffn_backward,
+ * the shared experts' backward, moe_router_input_backward, moe_dispatch_backward, in order on
+ * `stream`.  `a` holds the forward's inputs and the tensors it saved (logits_out must have been
+ * requested; act, Y, X, act_shared, idx, gate, slot_row, offsets, counts_routed). */
+moe_status moe_layer_backward(const moe_config* cfg, const moe_layer_args* a, const moe_layer_grads* g,
+                              void* ws, moe_stream_t stream);
+
 
 /* Synchronises `stream`, returns the device status word of `ws` in *code
  * (MOE_DEV_*) and clears it.  Returns MOE_ERR_DEVICE if the word was set. */

@@ -25,7 +25,8 @@ MOE_DEV_OK, MOE_DEV_BAD_EXPERT_ID, MOE_DEV_TIMEOUT, MOE_DEV_BAD_ROW, MOE_DEV_BAD
 EXPORTS = ("moe_version", "moe_status_string", "moe_last_error", "moe_capacity", "moe_workspace_size",
            "moe_route", "moe_balance_bias_update", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn",
            "moe_shared_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status", "moe_combine_backward",
-           "moe_route_backward", "moe_expert_ffn_backward", "moe_dispatch_backward")
+           "moe_route_backward", "moe_expert_ffn_backward", "moe_dispatch_backward", "moe_router_input_backward",
+           "moe_layer_backward")
 
 
 class MoeError(RuntimeError):
@@ -51,6 +52,13 @@ class moe_layer_args(ctypes.Structure):
         "counts_routed", "counts_kept", "offsets", "slot_row", "row_token", "n_dropped", "X", "act", "Y",
         "out", "f", "P", "aux", "z_loss", "sel_bias", "W_gate_shared", "W_up_shared", "W_down_shared",
         "act_shared", "Y_shared")]
+
+
+class moe_layer_grads(ctypes.Structure):
+    _fields_ = ([("dO", _P), ("w_aux", ctypes.c_float), ("w_z", ctypes.c_float)] +
+                [(n, _P) for n in ("d_gate", "dY", "dH", "d_act", "dG", "dUp", "dX", "dU_router", "d_act_shared",
+                                   "dG_shared", "dUp_shared", "dX_shared", "dU", "dW_gate", "dW_up", "dW_down",
+                                   "dW_r", "db_r", "dW_noise", "dW_gate_shared", "dW_up_shared", "dW_down_shared")])
 
 
 def _load() -> ctypes.CDLL:
@@ -90,6 +98,10 @@ def _load() -> ctypes.CDLL:
     lib.moe_expert_ffn_backward.argtypes = [cfgp] + [_P] * 14 + [_P, _P]
     lib.moe_dispatch_backward.restype = S
     lib.moe_dispatch_backward.argtypes = [cfgp] + [_P] * 4 + [_P, _P]
+    lib.moe_router_input_backward.restype = S
+    lib.moe_router_input_backward.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
+    lib.moe_layer_backward.restype = S
+    lib.moe_layer_backward.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), ctypes.POINTER(moe_layer_grads), _P, _P]
     lib.moe_layer_forward.restype = S
     lib.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), _P, _P]
     lib.moe_get_device_status.restype = S
@@ -222,7 +234,7 @@ def moe_shared_ffn(cfg, U, W_gate_sh, W_up_sh, W_down_sh, act_sh, Y_sh, ws, stre
     T, h, ns, ds = cfg.T, cfg.h, cfg.n_shared, cfg.d_shared
     _check(lib.moe_shared_ffn(ctypes.byref(cfg), _ptr(U, "U", dt, T * h), _ptr(W_gate_sh, "W_gate_sh", dt, ns * ds * h),
                               _ptr(W_up_sh, "W_up_sh", dt, ns * ds * h), _ptr(W_down_sh, "W_down_sh", dt, ns * h * ds),
-                              _ptr(act_sh, "act_sh", dt, T * ds), _ptr(Y_sh, "Y_sh", dt, ns * T * h), _ptr(ws, "ws"),
+                              _ptr(act_sh, "act_sh", dt, ns * T * ds), _ptr(Y_sh, "Y_sh", dt, ns * T * h), _ptr(ws, "ws"),
                               _stream(stream)))
 
 
@@ -331,7 +343,7 @@ class LayerBuffers:
             Y=torch.empty((T * k, h), dtype=dt, device=device), out=torch.empty((T, h), dtype=dt, device=device),
             f=torch.empty(E, dtype=f32, device=device), P=torch.empty(E, dtype=f32, device=device),
             aux=torch.empty(1, dtype=f32, device=device), z_loss=torch.empty(1, dtype=f32, device=device),
-            act_shared=torch.empty((T, cfg.d_shared), dtype=dt, device=device) if cfg.n_shared else None,
+            act_shared=torch.empty((cfg.n_shared, T, cfg.d_shared), dtype=dt, device=device) if cfg.n_shared else None,
             Y_shared=torch.empty((cfg.n_shared, T, h), dtype=dt, device=device) if cfg.n_shared else None,
             ws=new_workspace(cfg, device))
 
@@ -339,6 +351,13 @@ class LayerBuffers:
 def moe_layer_forward(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: LayerBuffers, stream=None,
                       sel_bias=None, shared=None):
     """The whole layer.  sel_bias: [E] loss-free selection bias; shared: (W_gate_sh, W_up_sh, W_down_sh)."""
+    a = layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs, sel_bias, shared)
+    _check(lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(a), _ptr(bufs.ws, "ws"), _stream(stream)))
+
+
+def layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: LayerBuffers, sel_bias=None,
+               shared=None) -> moe_layer_args:
+    """The moe_layer_args of one layer (inputs, weights and every buffer of `bufs`)."""
     dt = _act_dtype(cfg)
     T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
     ns, ds = cfg.n_shared, cfg.d_shared
@@ -365,9 +384,68 @@ def moe_layer_forward(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs
         sel_bias=_ptr(sel_bias, "sel_bias", torch.float32, E),
         W_gate_shared=_ptr(sg, "W_gate_shared", dt, ns * ds * h), W_up_shared=_ptr(su, "W_up_shared", dt, ns * ds * h),
         W_down_shared=_ptr(sd, "W_down_shared", dt, ns * h * ds),
-        act_shared=_ptr(bufs.act_shared, "act_shared", dt, T * ds) if ns else None,
+        act_shared=_ptr(bufs.act_shared, "act_shared", dt, ns * T * ds) if ns else None,
         Y_shared=_ptr(bufs.Y_shared, "Y_shared", dt, ns * T * h) if ns else None)
-    _check(lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(a), _ptr(bufs.ws, "ws"), _stream(stream)))
+    return a
+
+
+@dataclasses.dataclass
+class GradBuffers:
+    """Scratch and outputs of one layer backward (bf16 configs)."""
+    d_gate: torch.Tensor
+    dY: torch.Tensor
+    dH: torch.Tensor
+    d_act: torch.Tensor
+    dG: torch.Tensor
+    dUp: torch.Tensor
+    dX: torch.Tensor
+    dU_router: torch.Tensor
+    dU: torch.Tensor
+    dW_gate: torch.Tensor
+    dW_up: torch.Tensor
+    dW_down: torch.Tensor
+    dW_r: torch.Tensor
+    db_r: torch.Tensor
+    dW_noise: Optional[torch.Tensor]
+    d_act_shared: Optional[torch.Tensor]
+    dG_shared: Optional[torch.Tensor]
+    dUp_shared: Optional[torch.Tensor]
+    dX_shared: Optional[torch.Tensor]
+    dW_gate_shared: Optional[torch.Tensor]
+    dW_up_shared: Optional[torch.Tensor]
+    dW_down_shared: Optional[torch.Tensor]
+
+    @staticmethod
+    def allocate(cfg: moe_config, device="cuda") -> "GradBuffers":
+        dt = _act_dtype(cfg)
+        T, E, k, h, d, ns, ds = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e, cfg.n_shared, cfg.d_shared
+        f32 = torch.float32
+
+        def z(*shape, dtype=dt):
+            return torch.empty(shape, dtype=dtype, device=device)
+        return GradBuffers(
+            d_gate=z(T, k, dtype=f32), dY=z(T * k, h), dH=z(T, E, dtype=f32), d_act=z(T * k, d), dG=z(T * k, d),
+            dUp=z(T * k, d), dX=z(T * k, h), dU_router=z(T, h), dU=z(T, h), dW_gate=z(E, d, h, dtype=f32),
+            dW_up=z(E, d, h, dtype=f32), dW_down=z(E, h, d, dtype=f32), dW_r=z(h, E, dtype=f32),
+            db_r=z(E, dtype=f32), dW_noise=z(h, E, dtype=f32) if cfg.noisy else None,
+            d_act_shared=z(T, ds) if ns else None, dG_shared=z(T, ds) if ns else None,
+            dUp_shared=z(T, ds) if ns else None, dX_shared=z(ns, T, h) if ns else None,
+            dW_gate_shared=z(ns, ds, h, dtype=f32) if ns else None, dW_up_shared=z(ns, ds, h, dtype=f32) if ns else None,
+            dW_down_shared=z(ns, h, ds, dtype=f32) if ns else None)
+
+
+def moe_layer_backward(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: LayerBuffers, dO,
+                       grads: GradBuffers, w_aux=0.0, w_z=0.0, stream=None, sel_bias=None, shared=None):
+    """The whole backward for <dO, out> + w_aux E sum f P + w_z L_z; `bufs` must hold the forward's
+    tensors (allocated with with_logits=True)."""
+    if bufs.logits is None:
+        raise ValueError("the backward needs the forward's logits (LayerBuffers.allocate(with_logits=True))")
+    a = layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs, sel_bias, shared)
+    dt = _act_dtype(cfg)
+    g = moe_layer_grads(dO=_ptr(dO, "dO", dt, cfg.T * cfg.h), w_aux=float(w_aux), w_z=float(w_z),
+                        **{f.name: _ptr(getattr(grads, f.name), f.name) for f in dataclasses.fields(grads)})
+    _check(lib.moe_layer_backward(ctypes.byref(cfg), ctypes.byref(a), ctypes.byref(g), _ptr(bufs.ws, "ws"),
+                                  _stream(stream)))
 
 
 def moe_get_device_status(ws: torch.Tensor, stream=None) -> int:

@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(RB_THREADS) route_backward(const float* __rest
 template <typename T>
 __global__ void __launch_bounds__(256) dispatch_backward(const uint4* __restrict__ dO, const uint4* __restrict__ dX,
                                                          const int32_t* __restrict__ slot_row,
+                                                         const uint4* __restrict__ extra,
+                                                         const uint4* __restrict__ more, int n_more,
                                                          uint4* __restrict__ dU, int64_t n_tok, int k, int vpr,
                                                          int64_t rows_cap, int32_t* status) {
   constexpr int N = Vec16<T>::N;
@@ -198,7 +200,18 @@ __global__ void __launch_bounds__(256) dispatch_backward(const uint4* __restrict
     for (int v0 = 0; v0 < vpr; v0 += 32) {
       const int v = v0 + lane;
       float acc[N];
-      if (v < vpr) Vec16<T>::unpack(ldg_stream(dO + t * vpr + v), acc);
+      if (v < vpr) {
+        Vec16<T>::unpack(ldg_stream(dO + t * vpr + v), acc);
+        // the router's and the shared experts' input gradients (each rounded once already)
+        for (int a = 0; a < 1 + n_more; ++a) {
+          const uint4* src = a == 0 ? extra : more + static_cast<int64_t>(a - 1) * n_tok * vpr;
+          if (!src) continue;
+          float x[N];
+          Vec16<T>::unpack(ldg_stream(src + t * vpr + v), x);
+#pragma unroll
+          for (int i = 0; i < N; ++i) acc[i] += x[i];
+        }
+      }
       for (int j = 0; j < k; ++j) {
         const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
         if (r < 0 || v >= vpr) continue;
@@ -213,7 +226,7 @@ __global__ void __launch_bounds__(256) dispatch_backward(const uint4* __restrict
 }
 
 cudaError_t launch_dispatch_backward(const Plan& p, const void* dO, const void* dX, const int32_t* slot_row, void* dU,
-                                     uint8_t* ws, cudaStream_t s) {
+                                     uint8_t* ws, cudaStream_t s, const void* extra, const void* more, int n_more) {
   if (p.T == 0) return cudaSuccess;
   const int vpr = p.h * (p.bf16 ? 2 : 4) / 16;
   const int64_t want = (p.T + 7) / 8;
@@ -221,10 +234,128 @@ cudaError_t launch_dispatch_backward(const Plan& p, const void* dO, const void* 
   int32_t* status = ws_status(p, ws);
   if (p.bf16)
     dispatch_backward<bf16><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(dO), static_cast<const uint4*>(dX),
-                                                   slot_row, static_cast<uint4*>(dU), p.T, p.k, vpr, p.Tk, status);
+                                                   slot_row, static_cast<const uint4*>(extra),
+                                                   static_cast<const uint4*>(more), more ? n_more : 0,
+                                                   static_cast<uint4*>(dU), p.T, p.k, vpr, p.Tk, status);
   else
     dispatch_backward<float><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(dO), static_cast<const uint4*>(dX),
-                                                    slot_row, static_cast<uint4*>(dU), p.T, p.k, vpr, p.Tk, status);
+                                                    slot_row, static_cast<const uint4*>(extra),
+                                                    static_cast<const uint4*>(more), more ? n_more : 0,
+                                                    static_cast<uint4*>(dU), p.T, p.k, vpr, p.Tk, status);
+  return cudaGetLastError();
+}
+
+// [dH | dN] in bf16, rows of rb_np columns (zero past the used ones): dN = dH * eps * sigmoid(U W_noise),
+// the noise logits summed from the router's h-slices in slice order.
+__global__ void router_grad_pack(const float* __restrict__ dH, const float* __restrict__ eps,
+                                 const float* __restrict__ npart, int splits, int64_t n_tok, int E, int np,
+                                 bf16* __restrict__ out) {
+  const int64_t n = n_tok * np;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / np;
+    const int c = static_cast<int>(i - t * np);
+    float v = 0.f;
+    if (c < E) {
+      v = dH[t * E + c];
+    } else if (npart && c < 2 * E) {
+      const int e = c - E;
+      float z = npart[t * E + e];
+      for (int sp = 1; sp < splits; ++sp) z += npart[(static_cast<int64_t>(sp) * n_tok + t) * E + e];
+      v = dH[t * E + e] * eps[t * E + e] / (1.f + __expf(-z));
+    }
+    out[i] = __float2bfloat16_rn(v);
+  }
+}
+
+// [W_r | W_noise] as a bf16 [h, np] matrix (zero past the used columns).
+template <typename T>
+__global__ void router_weight_pack(const T* __restrict__ W_r, const T* __restrict__ W_noise, int h, int E, int np,
+                                   bf16* __restrict__ out) {
+  const int64_t n = static_cast<int64_t>(h) * np;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / np;
+    const int c = static_cast<int>(i - r * np);
+    float v = 0.f;
+    if (c < E)
+      v = to_f32(W_r[r * E + c]);
+    else if (W_noise && c < 2 * E)
+      v = to_f32(W_noise[r * E + (c - E)]);
+    out[i] = __float2bfloat16_rn(v);
+  }
+}
+
+// dW [h, np] float32 -> dW_r [h, E] and dW_noise [h, E].
+__global__ void router_wgrad_split(const float* __restrict__ dW, int h, int E, int np, float* __restrict__ dW_r,
+                                   float* __restrict__ dW_noise) {
+  const int64_t n = static_cast<int64_t>(h) * E;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / E;
+    const int e = static_cast<int>(i - r * E);
+    dW_r[i] = dW[r * np + e];
+    if (dW_noise) dW_noise[i] = dW[r * np + E + e];
+  }
+}
+
+// db_r[e] = sum over tokens of dH[t, e]: block b owns 32 experts (lane = expert), warp w adds
+// rows w, w + 32, ..., then warp 0 adds the 32 warp sums in order.
+__global__ void __launch_bounds__(1024) column_sums(const float* __restrict__ dH, int64_t n_tok, int E,
+                                                    float* __restrict__ out) {
+  __shared__ float part[32][33];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int e = blockIdx.x * 32 + lane;
+  float s = 0.f;
+  if (e < E)
+    for (int64_t t = warp; t < n_tok; t += 32) s += dH[t * E + e];
+  part[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && e < E) {
+    float tot = 0.f;
+    for (int w = 0; w < 32; ++w) tot += part[w][lane];
+    out[e] = tot;
+  }
+}
+
+cudaError_t launch_router_input_backward(const Plan& p, const void* U, const void* W_r, const void* W_noise,
+                                         const float* eps, const float* dH, void* dU_r, float* dW_r, float* dW_noise,
+                                         float* db_r, uint8_t* ws, cudaStream_t s) {
+  if (p.T == 0) return cudaSuccess;
+  int32_t* status = ws_status(p, ws);
+  bf16* dHb = reinterpret_cast<bf16*>(ws + p.ws_rb_dh);
+  bf16* Wb = reinterpret_cast<bf16*>(ws + p.ws_rb_w);
+  float* dW = reinterpret_cast<float*>(ws + p.ws_rb_dw);
+  const float* npart = nullptr;
+  int splits = 1;
+  if (p.noisy) {
+    // the noise logits U W_noise again, as h-slice sums in the router's workspace
+    float* part = reinterpret_cast<float*>(ws + p.ws_part);
+    float* np_ = reinterpret_cast<float*>(ws + p.ws_npart);
+    const cudaError_t e = launch_route_logits_tc(p, U, W_r, W_noise, part, np_, ws, s);
+    if (e != cudaSuccess) return e;
+    npart = np_;
+    splits = p.route_splits;
+  }
+  const int blocks = current_sm_count() * 4;
+  router_grad_pack<<<blocks, 256, 0, s>>>(dH, p.noisy ? eps : nullptr, npart, splits, p.T, p.E, p.rb_np, dHb);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  router_weight_pack<bf16><<<blocks, 256, 0, s>>>(static_cast<const bf16*>(W_r),
+                                                  p.noisy ? static_cast<const bf16*>(W_noise) : nullptr, p.h, p.E,
+                                                  p.rb_np, Wb);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // dU_r = [dH | dN] [W_r | W_noise]^T: M = T, N = h, K = rb_np
+  e = launch_dense_gemm_tc(dHb, p.T, p.rb_np, Wb, p.h, dU_r, status, s);
+  if (e != cudaSuccess) return e;
+  // [dW_r | dW_noise] = U^T [dH | dN]: M = h, N = rb_np, K = T
+  e = launch_dense_wgrad_tc(U, dHb, p.T, p.h, p.rb_np, dW, status, s);
+  if (e != cudaSuccess) return e;
+  router_wgrad_split<<<blocks, 256, 0, s>>>(dW, p.h, p.E, p.rb_np, dW_r, p.noisy ? dW_noise : nullptr);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !db_r) return e;
+  column_sums<<<(p.E + 31) / 32, 1024, 0, s>>>(dH, p.T, p.E, db_r);
   return cudaGetLastError();
 }
 

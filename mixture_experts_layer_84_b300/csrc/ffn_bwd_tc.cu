@@ -617,6 +617,17 @@ static cudaError_t launch_wgrad(int nsm, const CUtensorMap& a, const CUtensorMap
 
 }  // namespace bwd
 
+// out[M, N] (float32) = A^T B over `rows` rows, A [rows, M] and B [rows, N] bf16 row-major.
+cudaError_t launch_dense_wgrad_tc(const void* A, const void* B, int64_t rows, int M, int N, float* out,
+                                  int32_t* status, cudaStream_t s) {
+  using namespace bwd;
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, A, static_cast<uint64_t>(rows), static_cast<uint64_t>(M), 64) ||
+      !make_tmap(&tb, B, static_cast<uint64_t>(rows), static_cast<uint64_t>(N), 64))
+    return cudaErrorNotSupported;
+  return launch_wgrad(current_sm_count(), ta, tb, nullptr, 1, M, N, rows, out, status, s);
+}
+
 cudaError_t launch_ffn_backward_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                                    const void* W_up, const void* W_down, const void* act, const void* dY,
                                    void* d_act, void* dG, void* dUp, void* dX, float* dW_gate, float* dW_up,

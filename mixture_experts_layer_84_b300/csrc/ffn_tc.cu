@@ -647,6 +647,21 @@ static cudaError_t launch_gemm(bool pair, int grid, const CUtensorMap& a, const 
   return cudaGetLastError();
 }
 
+// out[rows, N] = A[rows, K] B[N, K]^T (bf16, both K-major, float32 accumulation, bf16 out), one
+// segment of all rows on the single-CTA kernel.
+cudaError_t launch_dense_gemm_tc(const void* A, int64_t rows, int K, const void* B, int N, void* out, int32_t* status,
+                                 cudaStream_t s) {
+  using namespace tc;
+  if (rows == 0) return cudaSuccess;
+  CUtensorMap tmA, tmB;
+  if (!make_tmap(&tmA, A, static_cast<uint64_t>(rows), static_cast<uint64_t>(K), BM) ||
+      !make_tmap(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN))
+    return cudaErrorNotSupported;
+  const int64_t tiles = ((rows + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = static_cast<int>(std::min<int64_t>(current_sm_count(), tiles));
+  return launch_gemm<false>(false, grid, tmA, tmB, tmB, nullptr, 1, K, N, N, rows, static_cast<bf16*>(out), status, s);
+}
+
 cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                           const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
                           cudaStream_t s) {

@@ -13,21 +13,22 @@ namespace moe {
 constexpr int route_bt_for(int ep) { return ep <= 256 ? 32 : 8192 / ep; }  // tokens per partial-logits block
 constexpr int route_kc_for(int ep) { return ep <= 128 ? 64 : 8192 / ep; }  // h chunk per pipeline stage
 // The router's selection kernel: G lanes per token, each with a chunk of <= 32 experts
-// (G = E / 32 rounded up to a power of two), SELECT_THREADS / G tokens per block.
+// (G = E / 32 rounded up to a power of two); blocks of up to SELECT_THREADS threads.
 constexpr int SELECT_THREADS = 256;
 constexpr int select_lanes_for(int E) {
   return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : E <= 512 ? 16 : 32;
 }
-constexpr int select_tokens_for(int E) { return SELECT_THREADS / select_lanes_for(E); }
-// Shared memory of one select block: [tokens][G * CS] logits (CS = the odd chunk stride) + z.
-constexpr size_t select_smem_bytes(int E) {
-  return sizeof(float) *
-         static_cast<size_t>(select_tokens_for(E)) *
-         (select_lanes_for(E) * ((((E + select_lanes_for(E) - 1) / select_lanes_for(E)) & 1)
-                                     ? (E + select_lanes_for(E) - 1) / select_lanes_for(E) + 2
-                                     : (E + select_lanes_for(E) - 1) / select_lanes_for(E) + 1) +
-          1);
+// Odd stride of one lane's chunk of C = ceil(E / G) logits in the select block's shared memory.
+constexpr int select_chunk_stride(int E) {
+  return (((E + select_lanes_for(E) - 1) / select_lanes_for(E)) & 1)
+             ? (E + select_lanes_for(E) - 1) / select_lanes_for(E) + 2
+             : (E + select_lanes_for(E) - 1) / select_lanes_for(E) + 1;
 }
+// Shared memory of a select block of `tokens` tokens: [tokens][G * CS] logits + one z value each.
+constexpr size_t select_smem_bytes(int E, int tokens) {
+  return sizeof(float) * static_cast<size_t>(tokens) * (select_lanes_for(E) * select_chunk_stride(E) + 1);
+}
+
 constexpr int kDispatchChunk = 4096;  // largest number of priority positions per dispatch chunk
 
 // Sizes derived from one moe_config, and the carve-up of the workspace.
@@ -48,6 +49,7 @@ struct Plan {
   int route_rowblocks = 0; // ceil(T / route_bt)
   int route_splits = 0;    // split of h across blocks (summed in fixed order by the select kernel)
   int route_tc_n = 0;      // > 0: bf16 logits on the tensor cores with this MMA width (E or 2E rounded up to 16)
+  int sel_threads = 0;     // threads per select block (G lanes per token)
   int sel_tokens = 0;      // tokens per select block
   int sel_blocks = 0;      // ceil(T / sel_tokens): number of P partial rows
 
@@ -57,6 +59,9 @@ struct Plan {
 
   // workspace byte offsets
   size_t ws_status = 0, ws_part = 0, ws_npart = 0, ws_ppart = 0, ws_hist = 0, ws_wt = 0, ws_total = 0;
+  // router backward: [dH | dN] bf16 [T, rb_np], [W_r | W_noise] bf16 [h, rb_np], dW float32 [h, rb_np]
+  int rb_np = 0;
+  size_t ws_rb_dh = 0, ws_rb_w = 0, ws_rb_dw = 0;
 };
 
 // Validates the config and fills `plan`; on failure returns the status and a message.
@@ -103,9 +108,22 @@ cudaError_t launch_ffn_backward_tc(const Plan& p, const void* X, const int32_t* 
                                    const void* W_up, const void* W_down, const void* act, const void* dY,
                                    void* d_act, void* dG, void* dUp, void* dX, float* dW_gate, float* dW_up,
                                    float* dW_down, int32_t* status, cudaStream_t s);
+// out[rows, N] = A[rows, K] B[N, K]^T in bf16 on tcgen05 (one all-row segment).
+cudaError_t launch_dense_gemm_tc(const void* A, int64_t rows, int K, const void* B, int N, void* out, int32_t* status,
+                                 cudaStream_t s);
+// out[M, N] (float32) = A^T B over `rows` rows (A [rows, M], B [rows, N] bf16) on tcgen05.
+cudaError_t launch_dense_wgrad_tc(const void* A, const void* B, int64_t rows, int M, int N, float* out,
+                                  int32_t* status, cudaStream_t s);
+// Backward of the router linear (bf16): dU_r = [dH | dN] [W_r | W_noise]^T, dW_r, dW_noise, db_r.
+cudaError_t launch_router_input_backward(const Plan& p, const void* U, const void* W_r, const void* W_noise,
+                                         const float* eps, const float* dH, void* dU_r, float* dW_r, float* dW_noise,
+                                         float* db_r, uint8_t* ws, cudaStream_t s);
+
 // dU = dO + the dX rows of each token's kept pairs.
+// (+ extra [T, h] and n_more further [T, h] blocks at `more`, each nullable)
 cudaError_t launch_dispatch_backward(const Plan& p, const void* dO, const void* dX, const int32_t* slot_row, void* dU,
-                                     uint8_t* ws, cudaStream_t s);
+                                     uint8_t* ws, cudaStream_t s, const void* extra = nullptr,
+                                     const void* more = nullptr, int n_more = 0);
 
 // b_i += u * sign(mean(counts) - counts_i) for the loss-free balancing bias.
 cudaError_t launch_balance_bias_update(int E, const int32_t* counts_routed, float u, float* bias, cudaStream_t s);

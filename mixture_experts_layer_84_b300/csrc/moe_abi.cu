@@ -150,7 +150,15 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 16)));
   }
   q.route_splits = splits;
-  q.sel_tokens = select_tokens_for(q.E);
+  // selection blocks: 256 threads, fewer (down to a warp) when T is small, so that the
+  // blocks still spread over about twice the SMs
+  {
+    const int G = select_lanes_for(q.E);
+    int64_t threads = q.T > 0 ? G * ((q.T + 2 * 148 - 1) / (2 * 148)) : SELECT_THREADS;
+    threads = (threads + 31) / 32 * 32;
+    q.sel_threads = static_cast<int>(std::max<int64_t>(std::max(32, G), std::min<int64_t>(SELECT_THREADS, threads)));
+    q.sel_tokens = q.sel_threads / G;
+  }
   q.sel_blocks = static_cast<int>((q.T + q.sel_tokens - 1) / q.sel_tokens);
   // dispatch chunks: about two per SM (multiples of 256 positions, 256 .. 4096), so small
   // batches still spread over the GPU and large ones keep the histogram short
@@ -175,6 +183,13 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   off += align256(sizeof(int32_t) * static_cast<size_t>(q.n_chunks) * q.E);
   q.ws_wt = off;
   if (q.route_tc_n > 0) off += align256(sizeof(uint16_t) * static_cast<size_t>(q.route_tc_n) * q.h);
+  q.rb_np = ((q.noisy ? 2 * q.E : q.E) + 7) / 8 * 8;
+  q.ws_rb_dh = off;
+  off += align256(sizeof(uint16_t) * static_cast<size_t>(q.T) * q.rb_np);
+  q.ws_rb_w = off;
+  off += align256(sizeof(uint16_t) * static_cast<size_t>(q.h) * q.rb_np);
+  q.ws_rb_dw = off;
+  off += align256(sizeof(float) * static_cast<size_t>(q.h) * q.rb_np);
   q.ws_total = off;
   *p = q;
   return MOE_OK;
@@ -286,7 +301,8 @@ cudaError_t launch_shared_ffn(const Plan& p, const void* U, const void* W_gate_s
     const uint8_t* wu = static_cast<const uint8_t*>(W_up_sh) + i * w_in;
     const uint8_t* wd = static_cast<const uint8_t*>(W_down_sh) + i * w_in;
     uint8_t* y = static_cast<uint8_t*>(Y_sh) + static_cast<size_t>(i) * p.T * p.h * es;
-    const cudaError_t e = launch_expert_ffn(q, U, nullptr, wg, wu, wd, act_sh, y, ws, s);
+    uint8_t* a = static_cast<uint8_t*>(act_sh) + static_cast<size_t>(i) * p.T * p.d_shared * es;
+    const cudaError_t e = launch_expert_ffn(q, U, nullptr, wg, wu, wd, a, y, ws, s);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -301,7 +317,7 @@ moe_status check_shared_args(const char* fn, const Plan& p, const void* U, const
   CHECK(check_ptr(fn, "W_gate_shared", W_gate_sh, w, 16));
   CHECK(check_ptr(fn, "W_up_shared", W_up_sh, w, 16));
   CHECK(check_ptr(fn, "W_down_shared", W_down_sh, w, 16));
-  CHECK(check_ptr(fn, "act_shared", act_sh, static_cast<size_t>(p.T) * p.d_shared * es, 16));
+  CHECK(check_ptr(fn, "act_shared", act_sh, static_cast<size_t>(p.n_shared) * p.T * p.d_shared * es, 16));
   CHECK(check_ptr(fn, "Y_shared", Y_sh, static_cast<size_t>(p.n_shared) * p.T * p.h * es, 16));
   return MOE_OK;
 }
@@ -523,6 +539,129 @@ MOE_API moe_status moe_dispatch_backward(const moe_config* cfg, const void* dO, 
   CHECK(moe::check_ptr(fn, "ws", ws, p.ws_total, 256));
   const cudaError_t e = moe::launch_dispatch_backward(p, dO, dX, slot_row, dU, static_cast<uint8_t*>(ws), stream);
   return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_router_input_backward(const moe_config* cfg, const void* U, const void* W_r,
+                                             const void* W_noise, const float* eps, const float* dH, void* dU_router,
+                                             float* dW_r, float* dW_noise, float* db_r, void* ws,
+                                             moe_stream_t stream) {
+  static const char* fn = "moe_router_input_backward";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (!p.bf16) return moe::fail(MOE_ERR_UNSUPPORTED, "%s: the router backward runs on bf16 (tcgen05) only", fn);
+  if (p.noisy && p.route_tc_n == 0)
+    return moe::fail(MOE_ERR_UNSUPPORTED, "%s: the noisy router backward needs 2E <= 256", fn);
+  const size_t TE = static_cast<size_t>(p.T) * p.E, hE = static_cast<size_t>(p.h) * p.E;
+  CHECK(moe::check_ptr(fn, "U", U, static_cast<size_t>(p.T) * p.h * 2, 16));
+  CHECK(moe::check_ptr(fn, "W_r", W_r, p.T > 0 ? hE * 2 : 0, 16));
+  if (p.noisy) {
+    CHECK(moe::check_ptr(fn, "W_noise", W_noise, p.T > 0 ? hE * 2 : 0, 16));
+    CHECK(moe::check_ptr(fn, "eps", eps, TE * 4, 4));
+    CHECK(moe::check_ptr(fn, "dW_noise", dW_noise, p.T > 0 ? hE * 4 : 0, 16));
+  }
+  CHECK(moe::check_ptr(fn, "dH", dH, TE * 4, 4));
+  CHECK(moe::check_ptr(fn, "dU_router", dU_router, static_cast<size_t>(p.T) * p.h * 2, 16));
+  CHECK(moe::check_ptr(fn, "dW_r", dW_r, p.T > 0 ? hE * 4 : 0, 16));
+  CHECK(moe::check_ptr(fn, "db_r", db_r, 0, 4));
+  CHECK(moe::check_ptr(fn, "ws", ws, p.ws_total, 256));
+  const cudaError_t e = moe::launch_router_input_backward(p, U, W_r, W_noise, eps, dH, dU_router, dW_r, dW_noise,
+                                                          db_r, static_cast<uint8_t*>(ws), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_layer_backward(const moe_config* cfg, const moe_layer_args* a, const moe_layer_grads* g,
+                                      void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_layer_backward";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (!a || !g) return moe::fail(MOE_ERR_INVALID_ARG, "%s: args or grads is NULL", fn);
+  if (!p.bf16) return moe::fail(MOE_ERR_UNSUPPORTED, "%s: the backward runs on bf16 (tcgen05) only", fn);
+  if (p.noisy && p.route_tc_n == 0)
+    return moe::fail(MOE_ERR_UNSUPPORTED, "%s: the noisy router backward needs 2E <= 256", fn);
+  if (!isfinite(g->w_aux) || !isfinite(g->w_z)) return moe::fail(MOE_ERR_INVALID_ARG, "%s: w_aux / w_z", fn);
+  const size_t es = 2, Th = static_cast<size_t>(p.T) * p.h * es, Tkh = static_cast<size_t>(p.Tk) * p.h * es;
+  const size_t Tkd = static_cast<size_t>(p.Tk) * p.d_e * es, TE = static_cast<size_t>(p.T) * p.E * 4;
+  const size_t wg = p.Tk > 0 ? static_cast<size_t>(p.E) * p.d_e * p.h * 4 : 0;
+  const size_t hE = p.T > 0 ? static_cast<size_t>(p.h) * p.E * 4 : 0;
+  // what the forward saved
+  CHECK(moe::check_ffn_args(fn, p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, ws));
+  CHECK(moe::check_ptr(fn, "U", a->U, Th, 16));
+  CHECK(moe::check_ptr(fn, "W_r", a->W_r, p.T > 0 ? static_cast<size_t>(p.h) * p.E * 2 : 0, 16));
+  CHECK(moe::check_ptr(fn, "logits_out", a->logits_out, TE, 4));
+  CHECK(moe::check_ptr(fn, "idx", a->idx, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "gate", a->gate, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "slot_row", a->slot_row, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "counts_routed", a->counts_routed, g->w_aux != 0.f ? static_cast<size_t>(p.E) * 4 : 0, 4));
+  if (p.noisy) {
+    CHECK(moe::check_ptr(fn, "W_noise", a->W_noise, p.T > 0 ? static_cast<size_t>(p.h) * p.E * 2 : 0, 16));
+    CHECK(moe::check_ptr(fn, "eps", a->eps, TE, 4));
+    CHECK(moe::check_ptr(fn, "dW_noise", g->dW_noise, hE, 16));
+  }
+  CHECK(moe::check_shared_args(fn, p, a->U, a->W_gate_shared, a->W_up_shared, a->W_down_shared, a->act_shared,
+                               a->Y_shared));
+  // gradients and scratch
+  CHECK(moe::check_ptr(fn, "dO", g->dO, Th, 16));
+  CHECK(moe::check_ptr(fn, "d_gate", g->d_gate, static_cast<size_t>(p.Tk) * 4, 4));
+  CHECK(moe::check_ptr(fn, "dY", g->dY, Tkh, 16));
+  CHECK(moe::check_ptr(fn, "dH", g->dH, TE, 4));
+  CHECK(moe::check_ptr(fn, "d_act", g->d_act, Tkd, 16));
+  CHECK(moe::check_ptr(fn, "dG", g->dG, Tkd, 16));
+  CHECK(moe::check_ptr(fn, "dUp", g->dUp, Tkd, 16));
+  CHECK(moe::check_ptr(fn, "dX", g->dX, Tkh, 16));
+  CHECK(moe::check_ptr(fn, "dU_router", g->dU_router, Th, 16));
+  CHECK(moe::check_ptr(fn, "dU", g->dU, Th, 16));
+  CHECK(moe::check_ptr(fn, "dW_gate", g->dW_gate, wg, 16));
+  CHECK(moe::check_ptr(fn, "dW_up", g->dW_up, wg, 16));
+  CHECK(moe::check_ptr(fn, "dW_down", g->dW_down, wg, 16));
+  CHECK(moe::check_ptr(fn, "dW_r", g->dW_r, hE, 16));
+  CHECK(moe::check_ptr(fn, "db_r", g->db_r, 0, 4));
+  if (p.n_shared > 0) {
+    const size_t Td = static_cast<size_t>(p.T) * p.d_shared * es;
+    const size_t wsh = p.T > 0 ? static_cast<size_t>(p.n_shared) * p.d_shared * p.h * 4 : 0;
+    CHECK(moe::check_ptr(fn, "d_act_shared", g->d_act_shared, Td, 16));
+    CHECK(moe::check_ptr(fn, "dG_shared", g->dG_shared, Td, 16));
+    CHECK(moe::check_ptr(fn, "dUp_shared", g->dUp_shared, Td, 16));
+    CHECK(moe::check_ptr(fn, "dX_shared", g->dX_shared, static_cast<size_t>(p.n_shared) * Th, 16));
+    CHECK(moe::check_ptr(fn, "dW_gate_shared", g->dW_gate_shared, wsh, 16));
+    CHECK(moe::check_ptr(fn, "dW_up_shared", g->dW_up_shared, wsh, 16));
+    CHECK(moe::check_ptr(fn, "dW_down_shared", g->dW_down_shared, wsh, 16));
+  }
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = moe::ws_status(p, w);
+  cudaError_t e = moe::launch_combine_backward(p, g->dO, a->Y, a->slot_row, a->gate, g->d_gate, g->dY, w, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_backward/combine", e);
+  e = moe::launch_route_backward(p, a->logits_out, a->idx, g->d_gate, a->counts_routed, g->w_aux, g->w_z, g->dH,
+                                 stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_backward/route", e);
+  e = moe::launch_ffn_backward_tc(p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, g->dY, g->d_act, g->dG,
+                                  g->dUp, g->dX, g->dW_gate, g->dW_up, g->dW_down, status, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_backward/experts", e);
+  if (p.n_shared > 0 && p.T > 0) {
+    moe::Plan q = p;
+    q.E = 1;
+    q.k = 1;
+    q.Tk = p.T;
+    q.d_e = p.d_shared;
+    const size_t w_in = static_cast<size_t>(p.d_shared) * p.h;
+    for (int i = 0; i < p.n_shared; ++i) {
+      e = moe::launch_ffn_backward_tc(
+          q, a->U, nullptr, static_cast<const uint16_t*>(a->W_gate_shared) + i * w_in,
+          static_cast<const uint16_t*>(a->W_up_shared) + i * w_in,
+          static_cast<const uint16_t*>(a->W_down_shared) + i * w_in,
+          static_cast<const uint16_t*>(a->act_shared) + static_cast<size_t>(i) * p.T * p.d_shared, g->dO,
+          g->d_act_shared, g->dG_shared, g->dUp_shared,
+          static_cast<uint16_t*>(g->dX_shared) + static_cast<size_t>(i) * p.T * p.h, g->dW_gate_shared + i * w_in,
+          g->dW_up_shared + i * w_in, g->dW_down_shared + i * w_in, status, stream);
+      if (e != cudaSuccess) return moe::cuda_fail("moe_layer_backward/shared", e);
+    }
+  }
+  e = moe::launch_router_input_backward(p, a->U, a->W_r, a->W_noise, a->eps, g->dH, g->dU_router, g->dW_r,
+                                        g->dW_noise, g->db_r, w, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_backward/router", e);
+  e = moe::launch_dispatch_backward(p, g->dO, g->dX, a->slot_row, g->dU, w, stream, g->dU_router,
+                                    p.n_shared > 0 ? g->dX_shared : nullptr, p.n_shared);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_backward/dispatch", e);
+  return MOE_OK;
 }
 
 MOE_API moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args* a, void* ws, moe_stream_t stream) {

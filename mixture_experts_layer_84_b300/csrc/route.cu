@@ -171,7 +171,7 @@ __device__ __forceinline__ bool before(float av, int ai, float bv, int bi) {
   return av > bv || (av == bv && ai < bi);
 }
 
-// Selection over G lanes per token, TB = SELECT_THREADS / G tokens per block.
+// Selection over G lanes per token, TB = blockDim.x / G tokens per block.
 //   1. the block stages the tile's final logits in shared memory with
 //      coalesced loads: slice sums added in slice order, + bias, + eps *
 //      softplus(noise slice sums) (or the given logits in stage mode); the
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
     const float* __restrict__ sel_bias, const float* __restrict__ eps, const float* __restrict__ logits_in,
     float* __restrict__ logits_out, int32_t* __restrict__ idx, float* __restrict__ gate, float* __restrict__ ppart,
     int32_t* __restrict__ ppart_rows, int64_t n_tok, int E, int k, int score_fn, int renorm) {
-  constexpr int TB = SELECT_THREADS / G;
+  const int TB = static_cast<int>(blockDim.x) / G;
   extern __shared__ float sx[];  // [TB][LD], then zsq[TB]
   const int C = (E + G - 1) / G;
   const int CS = (C & 1) ? C + 2 : C + 1;  // odd
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TB;
   const int rows = static_cast<int>(n_tok - t0 < TB ? n_tok - t0 : TB);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int NW = SELECT_THREADS / 32;
+  const int NW = static_cast<int>(blockDim.x) / 32;
   if (blockIdx.x == 0 && threadIdx.x == 0) *ppart_rows = static_cast<int32_t>(gridDim.x);
 
   // 1. final logits of the tile; rows t0 .. t0 + rows - 1 are contiguous in every input
@@ -221,12 +221,24 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
       if (logits_in) {
         x = logits_in[g];
       } else {
-        x = part[g];
-        for (int sp = 1; sp < splits; ++sp) x += part[static_cast<int64_t>(sp) * n_tok * E + g];
+        // every slice's value is loaded before any is added (one memory latency, not `splits`),
+        // then added in slice order
+        const int64_t stride = n_tok * E;
+        float v[16];
+#pragma unroll
+        for (int sp = 0; sp < 16; ++sp) v[sp] = sp < splits ? part[sp * stride + g] : 0.f;
+        x = v[0];
+#pragma unroll
+        for (int sp = 1; sp < 16; ++sp)
+          if (sp < splits) x += v[sp];
         if (b_r) x += b_r[e];
         if (npart) {
-          float nz = npart[g];
-          for (int sp = 1; sp < splits; ++sp) nz += npart[static_cast<int64_t>(sp) * n_tok * E + g];
+#pragma unroll
+          for (int sp = 0; sp < 16; ++sp) v[sp] = sp < splits ? npart[sp * stride + g] : 0.f;
+          float nz = v[0];
+#pragma unroll
+          for (int sp = 1; sp < 16; ++sp)
+            if (sp < splits) nz += v[sp];
           x = fmaf(eps[g], softplus_f32(nz), x);
         }
       }
@@ -422,13 +434,13 @@ template <int KP, int G>
 cudaError_t launch_select_g(const Plan& p, const float* part, const float* npart, int splits, const float* b_r,
                             const float* sel_bias, const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                             float* ppart, int32_t* rows, cudaStream_t s) {
-  const size_t smem = select_smem_bytes(p.E);
+  const size_t smem = select_smem_bytes(p.E, p.sel_tokens);
   auto kern = route_select<KP, G>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  kern<<<p.sel_blocks, SELECT_THREADS, smem, s>>>(part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx,
+  kern<<<p.sel_blocks, p.sel_threads, smem, s>>>(part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx,
                                                   gate, ppart, rows, p.T, p.E, p.k, p.score_fn, p.renorm);
   return cudaGetLastError();
 }

@@ -144,3 +144,41 @@ def test_dispatch_backward(dtype):
     assert L.moe_get_device_status(ws) == 0
     ref = oracle.dispatch_backward(dO, dX, d["slot_row"], k)
     assert normwise(dU, ref) <= TOL[dtype]
+
+
+LAYER_BWD = [W.MIXTRAL_SMALL, W.SWITCH_SMALL, W.DSV3_SHARED_SMALL, W.STRESS_SMALL,
+             W.Workload("bwd_shared2_softmax_norenorm", T=333, h=192, E=12, k=3, d_e=136, dtype=W.BF16,
+                        score_fn=W.SOFTMAX, renorm=False, noisy=False, capacity_factor=1.2, bias="normal",
+                        n_shared=2, d_shared=200)]
+
+
+@pytest.mark.parametrize("w", LAYER_BWD, ids=lambda w: w.name)
+def test_layer_backward(w):
+    """moe_layer_backward against the oracle's layer_backward (itself pinned to torch autograd):
+    every input and weight gradient, with the balance loss and the z-loss in the objective."""
+    from gpu_helpers import margin_inputs
+    inp, H = margin_inputs(w, seed=2)
+    cfg = L.config_of(w)
+    bufs = L.LayerBuffers.allocate(cfg, with_logits=True)
+    L.moe_layer_forward(cfg, inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up, inp.W_down, bufs,
+                        sel_bias=inp.sel_bias, shared=inp.shared)
+    dO = synth.random_rows(w.T, w.h, 11, "Y", "cuda", torch.bfloat16)
+    grads = L.GradBuffers.allocate(cfg)
+    w_aux, w_z = 0.5, 0.05
+    L.moe_layer_backward(cfg, inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up, inp.W_down, bufs,
+                         dO, grads, w_aux=w_aux, w_z=w_z, sel_bias=inp.sel_bias, shared=inp.shared)
+    assert L.moe_get_device_status(bufs.ws) == 0
+    fwd = oracle.layer_forward(inp, T=w.T, h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn, renorm=w.renorm,
+                               capacity_factor=w.capacity_factor, capacity_override=w.capacity, priority=w.priority,
+                               logits=H, sel_bias=inp.sel_bias, shared=inp.shared)
+    ref = oracle.layer_backward(inp, fwd, dO, k=w.k, d_e=w.d_e, score_fn=w.score_fn, renorm=w.renorm, w_aux=w_aux,
+                                w_z=w_z)
+    tol = TOL[W.BF16]
+    names = ["dU", "dH", "dW_gate", "dW_up", "dW_down", "dW_r", "db_r"]
+    if w.noisy:
+        names.append("dW_noise")
+    if w.n_shared:
+        names += ["dW_gate_shared", "dW_up_shared", "dW_down_shared"]
+    for n in names:
+        refn = ref[n[:-len("_shared")] + "_sh" if n.endswith("_shared") else n]
+        assert normwise(getattr(grads, n), refn) <= tol, n

@@ -95,7 +95,7 @@ def test_shared_ffn(T, h, n_shared, d_shared, dtype, tiles, monkeypatch):
                    capacity_factor=0.0, n_shared=n_shared, d_shared=d_shared)
     inp = synth.generate(w, seed=5, device="cuda")
     cfg = L.config_of(w)
-    act = torch.empty((T, d_shared), dtype=w.torch_dtype, device="cuda")
+    act = torch.empty((n_shared, T, d_shared), dtype=w.torch_dtype, device="cuda")
     Y = torch.full((n_shared, T, h), 7.0, dtype=w.torch_dtype, device="cuda")
     ws = L.new_workspace(cfg)
     L.moe_shared_ffn(cfg, inp.U, inp.W_gate_sh, inp.W_up_sh, inp.W_down_sh, act, Y, ws)
