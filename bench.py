@@ -174,8 +174,10 @@ def launches_per_step(w: W.Workload) -> int:
     """Kernels libmoe launches for one moe_layer_forward of this workload."""
     if w.T == 0:
         return 2  # dispatch scan + statistics
-    route, dispatch, ffn, combine = 2, 4, 2, 2
-    return route + dispatch + ffn + combine
+    tc_router = w.dtype == W.BF16 and (2 * w.E if w.noisy else w.E) <= 256
+    route = 3 if tc_router else 2          # (weight pack +) logits + selection
+    dispatch, ffn, combine = 4, 2, 2       # count, scan, assign, scatter; two GEMMs; rows + statistics
+    return route + dispatch + ffn + 2 * w.n_shared + combine
 
 
 def kernel_source_sha(files) -> str:
@@ -208,32 +210,44 @@ class _Inp:
 
 
 class ExpertsF64:
-    """One kind of expert weight, widened to float64 expert by expert on first use (then cached)."""
+    """One kind of expert weight, widened to float64 expert by expert: once and kept (cache=True), or
+    on every use (the oracle's own conversion, for models whose float64 weights would not fit)."""
 
-    def __init__(self, W_all, preload=()):
+    def __init__(self, W_all, preload=(), cache=True):
         self.W = W_all
+        self.use_cache = cache
         self.cache = {}
         for e in preload:
             self[e]
 
+    def __len__(self):
+        return len(self.W)
+
     def __getitem__(self, e):
         import oracle
         e = int(e)
+        if not self.use_cache:
+            return oracle.f64(self.W[e])
         if e not in self.cache:
             self.cache[e] = oracle.f64(self.W[e])
         return self.cache[e]
 
 
-def oracle_inputs_host(inp: "synth.LayerInputs", U_host, experts=()):
-    """Host copies for the oracle: token rows as given, router weights and the listed experts'
-    weights widened to float64 beforehand (input preparation, outside any timed region)."""
+F64_CACHE_BYTES = 24e9  # expert weights are widened once when their float64 copy fits in this
+
+
+def oracle_inputs_host(inp: "synth.LayerInputs", U_host, experts=(), cache=True):
+    """Host copies for the oracle: token rows as given, router weights widened to float64, expert
+    weights widened beforehand (the listed experts) or by the oracle on every use (cache=False,
+    from host bf16 copies made here, outside any timed region)."""
     import oracle
     f = oracle.f64
+    Wg, Wu, Wd = (x if cache else x.cpu() for x in (inp.W_gate, inp.W_up, inp.W_down))
     return _Inp(U=U_host, W_r=f(inp.W_r), b_r=None if inp.b_r is None else f(inp.b_r),
                 W_noise=None if inp.W_noise is None else f(inp.W_noise),
                 eps=None if inp.eps is None else f(inp.eps),
-                W_gate=ExpertsF64(inp.W_gate, experts), W_up=ExpertsF64(inp.W_up, experts),
-                W_down=ExpertsF64(inp.W_down, experts),
+                W_gate=ExpertsF64(Wg, experts, cache), W_up=ExpertsF64(Wu, experts, cache),
+                W_down=ExpertsF64(Wd, experts, cache),
                 sel_bias=None if inp.sel_bias is None else f(inp.sel_bias),
                 shared=None if inp.shared is None else tuple(f(x) for x in inp.shared))
 
@@ -268,25 +282,41 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
-def cpu_baseline(w: W.Workload, inp, n_tokens: int):
+def cpu_baseline(w: W.Workload, inp, n_tokens: int = 0, target_s: float = 12.0):
+    """The oracle as it stands on the host cores, on a bounded sample of the batch: a probe on a
+    few tokens sets the sample size for about `target_s` seconds of CPU work (all T tokens, run
+    again until that time is reached, when the whole batch is faster)."""
     import numpy as np
     import oracle
-    n_tokens = max(1, min(n_tokens, w.T))
-    sub_inp = synth.LayerInputs(U=inp.U[:n_tokens], W_r=inp.W_r, b_r=inp.b_r, W_noise=inp.W_noise,
-                                eps=None if inp.eps is None else inp.eps[:n_tokens],
+    sub_inp = synth.LayerInputs(U=inp.U, W_r=inp.W_r, b_r=inp.b_r, W_noise=inp.W_noise, eps=inp.eps,
                                 W_gate=inp.W_gate, W_up=inp.W_up, W_down=inp.W_down, sel_bias=inp.sel_bias,
                                 W_gate_sh=inp.W_gate_sh, W_up_sh=inp.W_up_sh, W_down_sh=inp.W_down_sh)
-    host = oracle_inputs_host(sub_inp, oracle.f64(sub_inp.U))
-    toks = np.arange(n_tokens)
-    for e in touched_experts(w, host, toks):
-        host.W_gate[e], host.W_up[e], host.W_down[e]
-    t0 = time.perf_counter()
-    oracle_step(w, host, toks)
-    dt = time.perf_counter() - t0
-    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"oracle layer forward (float64 numpy) on the first {n_tokens} of the batch's {w.T} "
-                      f"tokens with the same weights (widened to float64 beforehand), one call, "
-                      f"{dt:.1f} s; capacity from those {n_tokens} tokens"}
+    cache = 3 * w.E * w.h * w.d_e * 8 <= F64_CACHE_BYTES
+    host = oracle_inputs_host(sub_inp, oracle.f64(sub_inp.U), cache=cache)
+    # grow the sample 4x at a time until one call takes a quarter of the target (or is the whole
+    # batch), then repeat that call until the target time is reached (30 s at most)
+    oracle_step(w, host, np.arange(min(w.T, 16)))  # untimed: first-call costs (BLAS threads, page faults)
+    n = min(w.T, 64)
+    while True:
+        t0 = time.perf_counter()
+        oracle_step(w, host, np.arange(n))
+        one = time.perf_counter() - t0
+        if n >= w.T or one >= target_s / 4 or (n_tokens and n >= n_tokens):
+            break
+        n = min(w.T, n * 4)
+    toks = np.arange(n)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(w, host, toks)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s or dt + dt / reps > 30.0:
+            break
+    return {"value": n * reps / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"oracle layer forward (float64 numpy) on the first {n} of the batch's {w.T} tokens, "
+                      f"{reps} call(s) in {dt:.1f} s, expert weights widened to float64 "
+                      + ("beforehand" if cache else "by the oracle on every use (their float64 copy is too large)")
+                      + f"; capacity from those {n} tokens"}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -324,8 +354,8 @@ def run_reference(args, w: W.Workload):
     if rank != 0:
         return 0
     inp = synth.generate(w, seed=0, device="cpu")
-    f64_bytes = 3 * w.E * w.h * w.d_e * 8
-    host = oracle_inputs_host(inp, oracle.f64(inp.U), range(w.E) if f64_bytes <= 24e9 else ())
+    cache = 3 * w.E * w.h * w.d_e * 8 <= F64_CACHE_BYTES
+    host = oracle_inputs_host(inp, oracle.f64(inp.U), range(w.E) if cache else (), cache=cache)
     budget = float(args.reference_budget_s)
     rng = np.random.default_rng(0)
     probe = np.sort(rng.choice(w.T, size=min(4, w.T), replace=False))
@@ -342,7 +372,7 @@ def run_reference(args, w: W.Workload):
     value = n * args.steps / dt
     sample = (f"each step: the oracle layer forward (float64 numpy) on {n} tokens drawn from the "
               f"{w.T}-token batch; expert weights widened to float64 "
-              + ("beforehand" if f64_bytes <= 24e9 else "on first use (inside the timed steps)"))
+              + ("beforehand" if cache else "by the oracle on every use (inside the timed steps)"))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -412,20 +442,53 @@ def run_b300(args, w: W.Workload):
     if clocks:
         clocks.start()
         time.sleep(0.3)
+    # one CUDA graph per rotating token batch: the whole moe_layer_forward (the stage calls in
+    # order), replayed as one launch per step
+    graphs, graph_error = [], None
+    if not args.no_graph:
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(cap):
+            stage_calls(pool[0])  # first calls on this stream outside the capture
+        torch.cuda.current_stream(device).wait_stream(cap)
+        torch.cuda.synchronize(device)
+        try:
+            for U in pool:
+                g = torch.cuda.CUDAGraph()
+                # relaxed: the library's host-side set-up calls (kernel attributes) are not stream work
+                with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                    stage_calls(U)
+                graphs.append(g)
+        except RuntimeError as exc:  # time eager launches instead, and say so
+            graphs, graph_error = [], str(exc).splitlines()[0][:200]
+            torch.cuda.synchronize(device)
+
+    def step(i):
+        if graphs:
+            graphs[i % n_rot].replay()
+        else:
+            stage_calls(pool[i % n_rot])
+
     # warm-up right before the timed region, so the clocks are at load when timing starts
     for i in range(args.warmup):
-        stage_calls(pool[i % n_rot])
+        step(i)
     barrier(device)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
     for i in range(K):
-        starts[i].record()
-        stage_calls(pool[i % n_rot], evs[i])
-        ends[i].record()
+        step(i)
     t_end.record()
     barrier(device)
     total_ms = t_start.elapsed_time(t_end)
+
+    # the stage breakdown: the same steps again, the stage calls issued one by one with events
+    # between them (not part of `value`)
+    for i in range(K):
+        starts[i].record()
+        stage_calls(pool[i % n_rot], evs[i])
+        ends[i].record()
+    torch.cuda.synchronize(device)
 
     # end to end through the public call: every step copies its tokens in from pinned host memory,
     # runs moe_layer_forward and reads out (and aux) back.  Three streams pipeline the steps: the
@@ -477,6 +540,44 @@ def run_b300(args, w: W.Workload):
     code = L.moe_get_device_status(bufs.ws)
     if code != 0:
         raise SystemExit(f"bench.py: device status {code} after the timed region")
+
+    # the layer backward (bf16): L = <dO, out> + 0.01 E sum f P + 0.001 L_z, on the forward of
+    # the first batch; timed over min(K, 50) steps after 3 warm-up steps (not part of `value`)
+    train = None
+    if w.dtype == W.BF16 and not args.no_backward:
+        fb = L.LayerBuffers.allocate(cfg, device=device, with_logits=True)
+        fwd_args = (cfg, pool[0], inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up, inp.W_down, fb)
+        L.moe_layer_forward(*fwd_args, sel_bias=inp.sel_bias, shared=inp.shared)
+        grads = L.GradBuffers.allocate(cfg, device=device)
+        dO = synth.normal((w.T, w.h), 1.0, 7, "Y", device, w.torch_dtype)
+
+        def bwd():
+            L.moe_layer_backward(*fwd_args, dO, grads, w_aux=0.01, w_z=0.001, sel_bias=inp.sel_bias,
+                                 shared=inp.shared)
+
+        for _ in range(3):
+            bwd()
+        KB = min(K, 50)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record()
+        for _ in range(KB):
+            bwd()
+        b1.record()
+        torch.cuda.synchronize(device)
+        bwd_ms = b0.elapsed_time(b1) / KB
+        code = L.moe_get_device_status(fb.ws)
+        if code != 0:
+            raise SystemExit(f"bench.py: device status {code} after the backward")
+        A0 = A_of[0]
+        bwd_flops = 12 * A0 * w.h * w.d_e + 2 * 6 * w.T * w.h * w.E  # experts (2x the forward) + router
+        if w.n_shared:
+            bwd_flops += 12 * w.T * w.h * w.d_shared * w.n_shared
+        train = {"backward_ms": round(bwd_ms, 4), "steps": KB,
+                 "forward_plus_backward_tokens_per_s": round(w.T / ((total_ms / K + bwd_ms) * 1e-3), 1),
+                 "backward_TFLOP/s": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 2),
+                 "what": "moe_layer_backward: combine, gate/aux/z, grouped expert backward (recomputed gate|up), "
+                         "router linear, permute; float32 weight gradients"}
+        del fb, grads
 
     max_ms = max_over_ranks(total_ms, device)
     max_e2e = max_over_ranks(e2e_s, device)
@@ -549,16 +650,15 @@ def run_b300(args, w: W.Workload):
                     "how": "moe_layer_forward per step with its U copied in from pinned host memory and out + aux "
                            "copied back; copy-in, layer and copy-out of consecutive steps overlap on three streams"},
             "gpu_launches": launches_per_step(w) * K,
+            "launch": "one CUDA graph replay per step (the whole layer)" if graphs else
+                      ("eager stage calls" + (f" (graph capture failed: {graph_error})" if graph_error else "")),
             "clocks": clk}
+    if train:
+        line["train_step"] = train
     if ws_n == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample_tokens or default_cpu_sample(w))
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample_tokens)
     print(json.dumps(line), flush=True)
     return 0
-
-
-def default_cpu_sample(w: W.Workload) -> int:
-    return {"tiny_fp32": 256, "mixtral_bf16": 96, "switch_noisy_bf16": 2048, "dsv3_bf16": 48,
-            "stress_bf16": 512}.get(w.name, 128)
 
 
 def main(argv=None):
@@ -570,6 +670,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA-graph replays")
+    ap.add_argument("--no-backward", action="store_true", help="skip timing the layer backward")
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
