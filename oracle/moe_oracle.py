@@ -42,6 +42,11 @@ Sources (page title, section):
          d(sum_i f_i P_i)/dH_{t,k} = (1/T) s_k (f_k - sum_i f_i s_i) for softmax,
          (1/T) s'_k (1 - s_k) (f_k - sum_i f_i s'_i) for sigmoid; section Router
          z-loss: dL_z/dH_{t,k} = (2/T) LSE(H_t) softmax(H_t)_k.
+  [GRP]  same page, 设备受限与节点受限路由 (node-limited routing, the V3 form): a token
+         may use the experts of at most M nodes, the nodes being ranked by the sum
+         of the K_r/M highest affinities among their experts; the top-k is then
+         taken over the experts of the chosen nodes only.  On one GPU the nodes
+         become n_group equal, contiguous groups of experts (reading below).
   [BWD]  same page, 专家计算：padding、block-sparse 与 grouped GEMM: the backward of
          the SwiGLU experts is grouped GEMMs too, one group for the input
          gradients and one for the weight gradients.
@@ -55,7 +60,13 @@ Readings where the pages are silent (the same readings the library follows):
   * "no capacity limit" means C = T (an expert can receive each token once);
   * f_i counts the router's assignments before drops and is normalised by T*k;
   * a dropped assignment contributes nothing and the kept gates are not
-    renormalised; rows inside an expert segment are in slot (priority) order.
+    renormalised; rows inside an expert segment are in slot (priority) order;
+  * group-limited routing ([GRP]) on one GPU: group q holds experts
+    [q*E/n_group, (q+1)*E/n_group); a group's score is the sum of its
+    r = k/topk_group highest affinities (the scores s, or s + b with a
+    loss-free selection bias); the topk_group best groups are kept, ties to
+    the lower group id; the top-k is then taken over the kept groups' experts
+    only (by the usual selection key).  Group selection adds no gradient path.
 
 Every function here is pinned by the `-m "not gpu"` tests (worked examples of
 the pages, closed forms, invariants, brute force and textbook special cases).
@@ -114,14 +125,41 @@ def round_f32(H: np.ndarray) -> np.ndarray:
     return np.asarray(H, dtype=np.float32).astype(np.float64)
 
 
-def topk_select(H32: np.ndarray, k: int) -> np.ndarray:
+def topk_select(H32: np.ndarray, k: int, allowed=None) -> np.ndarray:
     """Top-k expert ids per token, highest first, ties to the lower expert id.
 
     [RTR] step 2 (select the k highest); the stable sort keeps equal values in
-    increasing expert order.
+    increasing expert order.  `allowed` [T, E] (group-limited routing) puts
+    every allowed expert ahead of every other one, whatever the values.
     """
-    order = np.argsort(-np.asarray(H32, dtype=np.float64), axis=1, kind="stable")
+    key = -np.asarray(H32, dtype=np.float64)
+    if allowed is None:
+        order = np.argsort(key, axis=1, kind="stable")
+    else:
+        order = np.lexsort((key, ~np.asarray(allowed, dtype=bool)), axis=-1)  # lexsort is stable
     return order[:, :k].astype(np.int32)
+
+
+def group_scores(aff: np.ndarray, n_group: int, r: int) -> np.ndarray:
+    """[T, n_group]: each contiguous expert group's sum of its r highest affinities.  [GRP]"""
+    aff = np.asarray(aff, dtype=np.float64)
+    T, E = aff.shape
+    grouped = -np.sort(-aff.reshape(T, n_group, E // n_group), axis=2)
+    return grouped[:, :, :r].sum(axis=2)
+
+
+def group_limited_mask(aff: np.ndarray, n_group: int, topk_group: int, k: int) -> np.ndarray:
+    """[T, E] bool: the experts of each token's topk_group highest-scoring groups.
+
+    [GRP]: groups ranked by the sum of their k/topk_group highest affinities,
+    ties to the lower group id.
+    """
+    T, E = np.asarray(aff).shape
+    gs = group_scores(aff, n_group, k // topk_group)
+    best = np.argsort(-gs, axis=1, kind="stable")[:, :topk_group]
+    chosen = np.zeros(gs.shape, dtype=bool)
+    np.put_along_axis(chosen, best, True, axis=1)
+    return np.repeat(chosen, E // n_group, axis=1)
 
 
 def scores(H: np.ndarray, score_fn: int) -> np.ndarray:
@@ -330,36 +368,39 @@ def balance_bias_update(b, counts_routed, u: float) -> np.ndarray:
     return f64(b) + u * np.sign(e)
 
 
-def route(H, k: int, score_fn: int, renorm: bool, sel_bias=None) -> dict:
+def route(H, k: int, score_fn: int, renorm: bool, sel_bias=None, n_group: int = 1, topk_group: int = 1) -> dict:
     """From logits to (idx, gates, scores): rounding to fp32, selection, scoring, gates.
 
     Without a selection bias the top-k is taken on the logits (the same order
     as on the scores).  With one ([LFB]) it is taken on s + b, while the gates
-    still come from s; "sel_key" holds s + b.
+    still come from s; "sel_key" holds s + b.  With n_group > 1 the top-k is
+    limited to the experts of the topk_group best groups ([GRP]), the groups
+    being scored on the affinities s (s + b with a selection bias); "allowed"
+    holds that [T, E] mask (None without groups).
     """
     H32 = round_f32(H)
     s = scores(H32, score_fn)
-    if sel_bias is None:
-        idx = topk_select(H32, k)
-        key = H32
-    else:
-        key = s + f64(sel_bias)[None, :]
-        idx = topk_select(key, k)
-    return dict(logits=H32, idx=idx, s=s, gate=gates(s, idx, renorm), sel_key=key)
+    key = H32 if sel_bias is None else s + f64(sel_bias)[None, :]
+    allowed = None
+    if n_group > 1:
+        allowed = group_limited_mask(s if sel_bias is None else key, n_group, topk_group, k)
+    idx = topk_select(key, k, allowed)
+    return dict(logits=H32, idx=idx, s=s, gate=gates(s, idx, renorm), sel_key=key, allowed=allowed)
 
 
 def layer_forward(inp, *, T, h, E, k, d_e, score_fn, renorm, capacity_factor,
-                  capacity_override=0, priority=CHOICE_MAJOR, logits=None, sel_bias=None, shared=None) -> dict:
+                  capacity_override=0, priority=CHOICE_MAJOR, logits=None, sel_bias=None, shared=None,
+                  n_group=1, topk_group=1) -> dict:
     """The full single-GPU MoE layer forward, stage by stage, in float64.
 
     `inp` carries U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down (numpy or
     torch).  If `logits` is given the router GEMM is skipped and those logits
     are used as they are.  `sel_bias` [E] is the loss-free selection bias
     ([LFB]); `shared` = (W_gate_sh, W_up_sh, W_down_sh) adds shared experts
-    ([SHR]).
+    ([SHR]); n_group > 1 limits each token to topk_group expert groups ([GRP]).
     """
     H = router_logits(inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps) if logits is None else f64(logits)
-    r = route(H, k, score_fn, renorm, sel_bias)
+    r = route(H, k, score_fn, renorm, sel_bias, n_group, topk_group)
     C = capacity(T, E, k, capacity_factor, capacity_override)
     d = dispatch(r["idx"], E, C, priority)
     X = permute(inp.U, d["row_token"])
@@ -597,6 +638,15 @@ def layer_backward(inp, fwd: dict, dO, *, k: int, d_e: int, score_fn: int, renor
         out["dW_up_sh"] = np.stack([b["dW_up"] for b in sh])
         out["dW_down_sh"] = np.stack([b["dW_down"] for b in sh])
     return out
+
+
+def group_margins(aff: np.ndarray, n_group: int, topk_group: int, k: int) -> np.ndarray:
+    """Per token, the gap between the topk_group-th and the next group score (inf when every
+    group is kept).  Used by the tests to keep group decisions away from ties."""
+    if topk_group >= n_group:
+        return np.full(np.asarray(aff).shape[0], np.inf)
+    gs = -np.sort(-group_scores(aff, n_group, k // topk_group), axis=1)
+    return gs[:, topk_group - 1] - gs[:, topk_group]
 
 
 def topk_margins(H32: np.ndarray, k: int) -> np.ndarray:

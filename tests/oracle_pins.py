@@ -8,6 +8,7 @@ the oracle and checks that some pin fails.
 """
 from __future__ import annotations
 
+import itertools
 import json
 import math
 import os
@@ -469,6 +470,69 @@ def pin_loss_free_zero_bias_and_gates(O):
         key = biased["s"] + b
         brute = np.argsort(-key, axis=1, kind="stable")[:, :3]
         assert np.array_equal(biased["idx"], brute)
+
+
+def pin_group_limited_example(O):
+    """Group-limited routing worked by hand (sigmoid, 8 experts in 4 groups of 2, 2 groups kept,
+    k = 4 so each group is scored on its 2 best affinities): the group scores are
+    s(3)+s(-2) = 1.072, s(2.9)+s(2.8) = 1.891, 2 s(0) = 1.0 and s(1)+s(2.95) = 1.681, so groups
+    1 and 3 are kept and the top-4 is (7, 2, 3, 6), leaving out expert 0, the highest logit,
+    which plain top-4 ranks first."""
+    H = np.array([[3.0, -2.0, 2.9, 2.8, 0.0, 0.0, 1.0, 2.95]])
+    r = O.route(H, 4, O.SIGMOID, True, n_group=4, topk_group=2)
+    assert r["idx"].tolist() == [[7, 2, 3, 6]]
+    assert O.route(H, 4, O.SIGMOID, True)["idx"].tolist() == [[0, 7, 2, 3]]
+    sel = np.array([1.0 / (1.0 + math.exp(-v)) for v in (2.95, 2.9, 2.8, 1.0)])
+    assert np.allclose(r["gate"][0], sel / sel.sum(), rtol=0, atol=1e-7)
+
+
+def pin_group_limited_special_cases(O):
+    """Keeping every group, or a single group, or groups of one expert with topk_group = k, all
+    select exactly the plain top-k."""
+    rng = _rng(33)
+    H = rng.normal(size=(60, 16)) * 1.5
+    for fn in (O.SOFTMAX, O.SIGMOID):
+        plain = O.route(H, 4, fn, True)["idx"]
+        for n_group, topk_group in ((4, 4), (1, 1), (16, 4), (2, 2)):
+            r = O.route(H, 4, fn, True, n_group=n_group, topk_group=topk_group)
+            assert np.array_equal(r["idx"], plain), (fn, n_group, topk_group)
+
+
+def _group_limited_bruteforce(key, aff, n_group, topk_group, k):
+    """Per token: every topk_group-subset of groups scored by the sum of its groups' r best
+    affinities, the best subset kept; then every k-subset of the kept experts, the one with
+    the largest key sum selected, listed by decreasing key.  (Continuous random values: no ties.)"""
+    T, E = key.shape
+    S, r = E // n_group, k // topk_group
+    out = []
+    for t in range(T):
+        gscore = []
+        for q in range(n_group):
+            vals = sorted((aff[t, q * S + i] for i in range(S)), reverse=True)
+            gscore.append(sum(vals[:r]))
+        best = max(itertools.combinations(range(n_group), topk_group), key=lambda c: sum(gscore[q] for q in c))
+        experts = [e for e in range(E) if e // S in best]
+        sel = max(itertools.combinations(experts, k), key=lambda c: sum(key[t, e] for e in c))
+        out.append(sorted(sel, key=lambda e: -key[t, e]))
+    return np.array(out, dtype=np.int64)
+
+
+def pin_group_limited_bruteforce(O):
+    """Group-limited top-k against the subset brute force, with and without a selection bias."""
+    rng = _rng(34)
+    for E, n_group, topk_group, k, fn, bias in ((12, 4, 2, 4, O.SIGMOID, False), (8, 4, 2, 2, O.SOFTMAX, False),
+                                                (12, 3, 1, 2, O.SOFTMAX, True), (16, 4, 3, 3, O.SIGMOID, True),
+                                                (16, 8, 2, 4, O.SIGMOID, True)):
+        H = rng.normal(size=(40, E)) * 2.0
+        b = rng.normal(size=E) * 0.1 if bias else None
+        H32 = np.asarray(H, dtype=np.float32).astype(np.float64)
+        s = O.scores(H32, fn)
+        key = H32 if b is None else s + b
+        want = _group_limited_bruteforce(key, s if b is None else key, n_group, topk_group, k)
+        r = O.route(H, k, fn, True, b, n_group, topk_group)
+        assert np.array_equal(r["idx"], want), (E, n_group, topk_group, k)
+        groups = np.asarray(r["idx"]) // (E // n_group)
+        assert all(len(set(g)) <= topk_group for g in groups.tolist())
 
 
 def pin_balance_bias_update(O):

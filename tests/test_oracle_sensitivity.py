@@ -20,11 +20,39 @@ def _gates_no_renorm(s, idx, renorm):
     return _orig["gates"](s, idx, False)
 
 
-def _topk_ties_high(H32, k):
+def _topk_ties_high(H32, k, allowed=None):
     E = H32.shape[1]
     rev = np.asarray(H32)[:, ::-1]
-    order = np.argsort(-rev, axis=1, kind="stable")
+    if allowed is None:
+        order = np.argsort(-rev, axis=1, kind="stable")
+    else:
+        order = np.lexsort((-rev, ~np.asarray(allowed, dtype=bool)[:, ::-1]), axis=-1)
     return (E - 1 - order[:, :k]).astype(np.int32)
+
+
+def _topk_ignores_allowed(H32, k, allowed=None):
+    return _orig["topk_select"](H32, k, None)
+
+
+def _group_scores_best_only(aff, n_group, r):
+    return _orig["group_scores"](aff, n_group, 1)
+
+
+def _group_mask_strided(aff, n_group, topk_group, k):
+    T, E = np.asarray(aff).shape
+    perm = np.arange(E).reshape(E // n_group, n_group).T.reshape(-1)  # group q = experts q, q+n_group, ...
+    inv = np.argsort(perm)
+    m = _orig["group_limited_mask"](np.asarray(aff)[:, perm], n_group, topk_group, k)
+    return m[:, inv]
+
+
+def _route_groups_on_logits(H, k, fn, renorm, sel_bias=None, n_group=1, topk_group=1):
+    r = _orig["route"](H, k, fn, renorm, sel_bias, 1, 1)
+    if n_group > 1:
+        allowed = _orig["group_limited_mask"](r["logits"], n_group, topk_group, k)
+        r["idx"] = _orig["topk_select"](r["sel_key"], k, allowed)
+        r["gate"] = _orig["gates"](r["s"], r["idx"], renorm)
+    return r
 
 
 def _capacity_floor(T, E, k, cf, override=0):
@@ -112,15 +140,15 @@ def _bias_update_wrong_sign(b, counts, u):
     return np.asarray(b, dtype=np.float64) + u * np.sign(c - c.mean())
 
 
-def _route_gates_from_key(H, k, fn, renorm, sel_bias=None):
-    r = _orig["route"](H, k, fn, renorm, sel_bias)
+def _route_gates_from_key(H, k, fn, renorm, sel_bias=None, n_group=1, topk_group=1):
+    r = _orig["route"](H, k, fn, renorm, sel_bias, n_group, topk_group)
     if sel_bias is not None:
         r["gate"] = _orig["gates"](r["s"] + np.asarray(sel_bias, dtype=np.float64)[None, :], r["idx"], renorm)
     return r
 
 
-def _route_ignores_bias(H, k, fn, renorm, sel_bias=None):
-    return _orig["route"](H, k, fn, renorm, None)
+def _route_ignores_bias(H, k, fn, renorm, sel_bias=None, n_group=1, topk_group=1):
+    return _orig["route"](H, k, fn, renorm, None, n_group, topk_group)
 
 
 def _combine_ignores_shared(U, Y, slot_row, gate, k, Y_shared=None):
@@ -193,6 +221,10 @@ MUTANTS = {
     "loss_free_gates_from_key": ("route", _route_gates_from_key),
     "loss_free_bias_ignored": ("route", _route_ignores_bias),
     "shared_experts_not_added": ("combine", _combine_ignores_shared),
+    "group_mask_ignored": ("topk_select", _topk_ignores_allowed),
+    "group_scored_on_best_expert_only": ("group_scores", _group_scores_best_only),
+    "groups_strided_not_contiguous": ("group_limited_mask", _group_mask_strided),
+    "groups_scored_on_logits": ("route", _route_groups_on_logits),
     "aux_grad_without_mean_load": ("aux_loss_grad", _aux_grad_no_mean_term),
     "gate_backward_ignores_renorm": ("gate_backward", _gate_backward_ignores_renorm),
     "z_grad_half": ("z_loss_grad", _z_grad_half),
