@@ -257,7 +257,8 @@ def touched_experts(w: W.Workload, host, tokens):
     import oracle
     H = oracle.router_logits(host.U[tokens], host.W_r, host.b_r, host.W_noise,
                              None if host.eps is None else host.eps[tokens])
-    return sorted(set(np.unique(oracle.route(H, w.k, w.score_fn, w.renorm, host.sel_bias)["idx"]).tolist()))
+    r = oracle.route(H, w.k, w.score_fn, w.renorm, host.sel_bias, w.n_group, w.topk_group)
+    return sorted(set(np.unique(r["idx"]).tolist()))
 
 
 def oracle_step(w: W.Workload, host, tokens):
@@ -268,7 +269,8 @@ def oracle_step(w: W.Workload, host, tokens):
                W_gate=host.W_gate, W_up=host.W_up, W_down=host.W_down)
     return oracle.layer_forward(sub, T=len(tokens), h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn,
                                 renorm=w.renorm, capacity_factor=w.capacity_factor, capacity_override=w.capacity,
-                                priority=w.priority, sel_bias=host.sel_bias, shared=host.shared)
+                                priority=w.priority, sel_bias=host.sel_bias, shared=host.shared,
+                                n_group=w.n_group, topk_group=w.topk_group)
 
 
 def blas_threads() -> int:
@@ -341,6 +343,8 @@ def workload_config(w: W.Workload, n_rot: int = 0):
         c.update(n_shared=w.n_shared, d_shared=w.d_shared)
     if w.sel_bias != "none":
         c["selection_bias"] = "loss-free balancing bias ~ N(0, 0.05) on the scores"
+    if w.n_group > 1:
+        c.update(n_group=w.n_group, topk_group=w.topk_group)
     if n_rot:
         c["l2"] = (f"inputs larger than L2: {n_rot} rotating token batches plus "
                    f"{3 * w.E * w.h * w.d_e * w.elem_bytes / 1e9:.2f} GB of expert weights per step")

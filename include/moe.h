@@ -97,6 +97,10 @@ typedef struct moe_config {
   int32_t dtype;          /* moe_dtype of activations and weights */
   int32_t n_shared;       /* shared experts (every token, no router), 0..16; 0 = none */
   int32_t d_shared;       /* their intermediate size (multiple of 8) when n_shared > 0 */
+  int32_t n_group;        /* group-limited routing: 0 or 1 = off; else 2..32 equal, contiguous expert
+                           * groups (E % n_group == 0), see moe_route */
+  int32_t topk_group;     /* groups kept per token when n_group > 1: 1..n_group, k % topk_group == 0,
+                           * k <= topk_group * E / n_group */
 } moe_config;
 
 /* Library version string, e.g. "moe-b300 0.1 sm_103a". */
@@ -137,7 +141,13 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
  *   gate     [T, k] float32 out       g_j (renormalised over the k or not, cfg->renorm)
  * Logits accumulate in float32 from the act-dtype inputs; selection compares
  * the float32 logits.  Also leaves per-block sums of the scores (sigmoid:
- * s_i / sum_j s_j) in `ws` for moe_combine's P_i. */
+ * s_i / sum_j s_j) in `ws` for moe_combine's P_i.
+ * Group-limited routing (cfg->n_group > 1; section 设备受限与节点受限路由, node-limited
+ * routing with the nodes read as expert groups): group q holds experts
+ * [q*E/n_group, (q+1)*E/n_group); each group is scored by the float32 sum of its
+ * k/topk_group highest affinities (the score, or score + sel_bias when sel_bias is
+ * given); the topk_group best groups are kept (ties to the lower group id), and the
+ * top-k above is taken over their experts only. */
 moe_status moe_route(const moe_config* cfg, const void* U, const void* W_r, const float* b_r,
                      const float* sel_bias, const void* W_noise, const float* eps,
                      const float* logits_in, float* logits_out, int32_t* idx, float* gate, void* ws,

@@ -40,7 +40,7 @@ class moe_config(ctypes.Structure):
                 ("d_e", ctypes.c_int32), ("capacity_factor", ctypes.c_float), ("capacity", ctypes.c_int32),
                 ("score_fn", ctypes.c_int32), ("renorm", ctypes.c_int32), ("noisy", ctypes.c_int32),
                 ("priority", ctypes.c_int32), ("dtype", ctypes.c_int32), ("n_shared", ctypes.c_int32),
-                ("d_shared", ctypes.c_int32)]
+                ("d_shared", ctypes.c_int32), ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -126,15 +126,17 @@ def _check(status: int) -> None:
 
 
 def config(T, h, E, k, d_e, *, capacity_factor=0.0, capacity=0, score_fn=W.SOFTMAX, renorm=True, noisy=False,
-           priority=W.PRIORITY_CHOICE_MAJOR, dtype=W.BF16, n_shared=0, d_shared=0) -> moe_config:
+           priority=W.PRIORITY_CHOICE_MAJOR, dtype=W.BF16, n_shared=0, d_shared=0, n_group=0,
+           topk_group=0) -> moe_config:
     return moe_config(int(T), int(h), int(E), int(k), int(d_e), float(capacity_factor), int(capacity),
                       int(score_fn), int(bool(renorm)), int(bool(noisy)), int(priority), int(dtype), int(n_shared),
-                      int(d_shared))
+                      int(d_shared), int(n_group), int(topk_group))
 
 
 def config_of(w: W.Workload, **override) -> moe_config:
     kw = dict(capacity_factor=w.capacity_factor, capacity=w.capacity, score_fn=w.score_fn, renorm=w.renorm,
-              noisy=w.noisy, priority=w.priority, dtype=w.dtype, n_shared=w.n_shared, d_shared=w.d_shared)
+              noisy=w.noisy, priority=w.priority, dtype=w.dtype, n_shared=w.n_shared, d_shared=w.d_shared,
+              n_group=w.n_group, topk_group=w.topk_group)
     kw.update(override)
     T = kw.pop("T", w.T)
     return config(T, w.h, w.E, w.k, w.d_e, **kw)

@@ -24,10 +24,13 @@ constexpr int select_chunk_stride(int E) {
              ? (E + select_lanes_for(E) - 1) / select_lanes_for(E) + 2
              : (E + select_lanes_for(E) - 1) / select_lanes_for(E) + 1;
 }
-// Shared memory of a select block of `tokens` tokens: [tokens][G * CS] logits + one z value each.
-constexpr size_t select_smem_bytes(int E, int tokens) {
-  return sizeof(float) * static_cast<size_t>(tokens) * (select_lanes_for(E) * select_chunk_stride(E) + 1);
+// Shared memory of a select block of `tokens` tokens: [tokens][G * CS] logits, one z value each,
+// then (group-limited routing) [tokens][n_group] group scores.
+constexpr size_t select_smem_bytes(int E, int tokens, int n_group = 0) {
+  return sizeof(float) * static_cast<size_t>(tokens) *
+         (select_lanes_for(E) * select_chunk_stride(E) + 1 + (n_group > 1 ? n_group : 0));
 }
+constexpr int MAX_GROUPS = 32;  // group-limited routing: kept groups fit one 32-bit mask
 
 constexpr int kDispatchChunk = 4096;  // largest number of priority positions per dispatch chunk
 
@@ -41,6 +44,7 @@ struct Plan {
   bool noisy = false;
   int score_fn = 0, renorm = 0, priority = 0;
   int n_shared = 0, d_shared = 0;  // shared experts and their intermediate size
+  int n_group = 0, topk_group = 0; // group-limited routing (n_group > 1), else 0
 
   // router
   int route_ep = 0;        // E rounded up to the router's compile-time width

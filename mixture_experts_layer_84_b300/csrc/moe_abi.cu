@@ -99,6 +99,20 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   if (cfg->n_shared > 0 && cfg->dtype == MOE_BF16 &&
       static_cast<int64_t>(cfg->n_shared) * std::max(cfg->h, cfg->d_shared) >= (int64_t(1) << 31))
     return bad(MOE_ERR_UNSUPPORTED, "n_shared * max(h, d_shared) >= 2^31");
+  if (cfg->n_group > 1) {
+    if (cfg->n_group > MAX_GROUPS) return bad(MOE_ERR_UNSUPPORTED, "n_group = %d > %d", cfg->n_group, MAX_GROUPS);
+    if (cfg->E % cfg->n_group != 0)
+      return bad(MOE_ERR_INVALID_ARG, "E = %d is not a multiple of n_group = %d", cfg->E, cfg->n_group);
+    if (cfg->topk_group < 1 || cfg->topk_group > cfg->n_group)
+      return bad(MOE_ERR_INVALID_ARG, "topk_group = %d outside 1..n_group = %d", cfg->topk_group, cfg->n_group);
+    if (cfg->k % cfg->topk_group != 0)
+      return bad(MOE_ERR_INVALID_ARG, "k = %d is not a multiple of topk_group = %d", cfg->k, cfg->topk_group);
+    if (static_cast<int64_t>(cfg->topk_group) * (cfg->E / cfg->n_group) < cfg->k)
+      return bad(MOE_ERR_INVALID_ARG, "k = %d > topk_group * E / n_group = %d", cfg->k,
+                 cfg->topk_group * (cfg->E / cfg->n_group));
+  } else if (cfg->n_group < 0) {
+    return bad(MOE_ERR_INVALID_ARG, "n_group = %d < 0", cfg->n_group);
+  }
   if (cfg->E > 1024) return bad(MOE_ERR_UNSUPPORTED, "E = %d > 1024", cfg->E);
   if (cfg->k > 16) return bad(MOE_ERR_UNSUPPORTED, "k = %d > 16", cfg->k);
   if (cfg->h % 8 != 0 || cfg->d_e % 8 != 0)
@@ -122,6 +136,10 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   q.priority = cfg->priority;
   q.n_shared = cfg->n_shared;
   q.d_shared = cfg->d_shared;
+  if (cfg->n_group > 1) {
+    q.n_group = cfg->n_group;
+    q.topk_group = cfg->topk_group;
+  }
   if (cfg->capacity > 0)
     q.C = cfg->capacity;
   else if (cfg->capacity_factor <= 0.f)

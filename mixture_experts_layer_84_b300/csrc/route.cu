@@ -199,9 +199,10 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
     const float* __restrict__ part, const float* __restrict__ npart, int splits, const float* __restrict__ b_r,
     const float* __restrict__ sel_bias, const float* __restrict__ eps, const float* __restrict__ logits_in,
     float* __restrict__ logits_out, int32_t* __restrict__ idx, float* __restrict__ gate, float* __restrict__ ppart,
-    int32_t* __restrict__ ppart_rows, int64_t n_tok, int E, int k, int score_fn, int renorm) {
+    int32_t* __restrict__ ppart_rows, int64_t n_tok, int E, int k, int score_fn, int renorm, int n_group,
+    int topk_group) {
   const int TB = static_cast<int>(blockDim.x) / G;
-  extern __shared__ float sx[];  // [TB][LD], then zsq[TB]
+  extern __shared__ float sx[];  // [TB][LD], then zsq[TB], then (groups) gsc[TB][n_group]
   const int C = (E + G - 1) / G;
   const int CS = (C & 1) ? C + 2 : C + 1;  // odd
   const int LD = G * CS;
@@ -276,6 +277,52 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
     sum_exp += __shfl_xor_sync(0xffffffffu, sum_exp, o);
     denom += __shfl_xor_sync(0xffffffffu, denom, o);
   }
+  // group-limited routing: each group's score is the sum of its r = k / topk_group best
+  // affinities (score, + bias when selecting with one); a lane scores groups g, g + G, ...
+  // reading the token's staged row, then every lane of the token ranks all the groups
+  uint32_t keep = 0xffffffffu;
+  int gsz = E;  // experts per group
+  if (n_group > 1) {
+    gsz = E / n_group;
+    const int r_top = k / topk_group;
+    float* gs = zsq + TB + r * n_group;
+    if (tok) {
+      for (int q = g; q < n_group; q += G) {
+        float best[KP];
+#pragma unroll
+        for (int j = 0; j < KP; ++j) best[j] = -INFINITY;
+        for (int e = q * gsz; e < (q + 1) * gsz; ++e) {
+          const int cg = e / C;
+          const float x = rowp[cg * CS + (e - cg * C)];
+          float a = softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x));
+          if (sel_bias) a += sel_bias[e];
+#pragma unroll
+          for (int j = 0; j < KP; ++j) {
+            if (j < r_top && a > best[j]) {
+              const float t = best[j];
+              best[j] = a;
+              a = t;
+            }
+          }
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < KP; ++j)
+          if (j < r_top) sum += best[j];
+        gs[q] = sum;
+      }
+    }
+    __syncwarp();
+    keep = 0;
+    if (tok) {
+      for (int q = 0; q < n_group; ++q) {
+        const float v = gs[q];
+        int rank = 0;
+        for (int q2 = 0; q2 < n_group; ++q2) rank += (gs[q2] > v || (gs[q2] == v && q2 < q)) ? 1 : 0;
+        if (rank < topk_group) keep |= 1u << q;
+      }
+    }
+  }
   // selection key: the logit, or with a selection bias (loss-free balancing) the score + bias
   float tv[KP];
   int ti[KP];
@@ -285,7 +332,13 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
     ti[j] = 0x7fffffff;
   }
   if (tok) {
+    int grp = e0 / gsz, grp_end = (grp + 1) * gsz;  // the group of expert e, tracked as e advances
     for (int e = e0; e < e1; ++e) {
+      if (e == grp_end) {
+        ++grp;
+        grp_end += gsz;
+      }
+      if (!((keep >> grp) & 1u)) continue;  // outside the kept groups (never without groups: grp = 0)
       const float x = chunk[e - e0];
       const float key =
           sel_bias ? (softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x))) + sel_bias[e] : x;
@@ -434,14 +487,15 @@ template <int KP, int G>
 cudaError_t launch_select_g(const Plan& p, const float* part, const float* npart, int splits, const float* b_r,
                             const float* sel_bias, const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                             float* ppart, int32_t* rows, cudaStream_t s) {
-  const size_t smem = select_smem_bytes(p.E, p.sel_tokens);
+  const size_t smem = select_smem_bytes(p.E, p.sel_tokens, p.n_group);
   auto kern = route_select<KP, G>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
   kern<<<p.sel_blocks, p.sel_threads, smem, s>>>(part, npart, splits, b_r, sel_bias, eps, logits_in, logits_out, idx,
-                                                  gate, ppart, rows, p.T, p.E, p.k, p.score_fn, p.renorm);
+                                                  gate, ppart, rows, p.T, p.E, p.k, p.score_fn, p.renorm,
+                                                  p.n_group, p.topk_group);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,8 @@ class Workload:
     n_shared: int = 0     # shared experts (every token, outside the router)
     d_shared: int = 0     # their intermediate size
     sel_bias: str = "none"  # loss-free selection bias: none | normal
+    n_group: int = 0      # group-limited routing: experts in n_group contiguous groups (0 = off)
+    topk_group: int = 0   # groups a token may use
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -75,10 +77,12 @@ STRESS = Workload("stress_bf16", T=65536, h=4096, E=64, k=6, d_e=1408, dtype=BF1
 
 FULL = [TINY_FP32, MIXTRAL, SWITCH, DSV3, STRESS]
 
-# DeepSeek-V3's full MoE block: the DS-V3 shape plus its one shared expert (d = 2048) and a
-# loss-free balancing bias on the selection ("MoE 与专家并行", sections 细粒度专家与共享专家 and
-# 无辅助损失的负载均衡).
-DSV3_SHARED = DSV3.replace(name="dsv3_shared_bf16", n_shared=1, d_shared=2048, sel_bias="normal")
+# DeepSeek-V3's full MoE block: the DS-V3 shape plus its one shared expert (d = 2048), a
+# loss-free balancing bias on the selection, and group-limited routing with its 8 groups of 32
+# experts, 4 kept per token ("MoE 与专家并行", sections 细粒度专家与共享专家,
+# 无辅助损失的负载均衡 and 设备受限与节点受限路由, the node limit M = 4 read as expert groups).
+DSV3_SHARED = DSV3.replace(name="dsv3_shared_bf16", n_shared=1, d_shared=2048, sel_bias="normal",
+                           n_group=8, topk_group=4)
 DSV3_SHARED_SMALL = DSV3_SHARED.replace(name="dsv3_shared_small", T=600, h=512, d_e=256, d_shared=384)
 EXTENDED = [DSV3_SHARED]
 

@@ -58,23 +58,34 @@ def logits_of(w: W.Workload, inp, rows=None) -> np.ndarray:
                                 None if inp.eps is None else inp.eps[r])
 
 
-def selection_key(w: W.Workload, inp, H) -> np.ndarray:
-    """What the top-k is taken on: the logits, or score + selection bias (loss-free balancing)."""
-    if inp.sel_bias is None:
-        return H
-    return oracle.route(H, w.k, w.score_fn, w.renorm, inp.sel_bias)["sel_key"]
+def route_of(w: W.Workload, H, sel_bias=None) -> dict:
+    """The oracle's routing of logits H under workload w (selection bias, expert groups)."""
+    return oracle.route(H, w.k, w.score_fn, w.renorm, sel_bias, w.n_group, w.topk_group)
 
 
-def margin_inputs(w: W.Workload, seed: int = 0, device="cuda", experts: bool = True, max_rounds: int = 30):
-    """Layer inputs whose tokens all keep a top-(k+1) margin >= MARGIN (in float64) in the
-    selection key (the logits, or score + selection bias).
+def selection_margins(w: W.Workload, H, sel_bias=None) -> np.ndarray:
+    """Per token, the smallest gap that decides its routing: adjacent gaps among the top-(k+1)
+    selection keys (the logits, or score + selection bias) of the experts it may use, and with
+    expert groups the gap between the last kept and the first dropped group score."""
+    r = route_of(w, H, sel_bias)
+    key = r["sel_key"]
+    if r["allowed"] is None:
+        return oracle.topk_margins(key, w.k)
+    m = oracle.topk_margins(np.where(r["allowed"], key, -np.inf), w.k)
+    aff = r["s"] if sel_bias is None else key
+    return np.minimum(m, oracle.group_margins(aff, w.n_group, w.topk_group, w.k))
+
+
+def margin_inputs(w: W.Workload, seed: int = 0, device="cuda", experts: bool = True, max_rounds: int = 40):
+    """Layer inputs whose tokens all keep a routing margin >= MARGIN (in float64): see
+    selection_margins.
 
     Tokens that violate it get fresh U (and eps) rows; returns (inputs, float64 logits).
     """
     inp = synth.generate(w, seed, device, experts=experts)
     H = logits_of(w, inp)
     for attempt in range(max_rounds):
-        bad = np.nonzero(oracle.topk_margins(selection_key(w, inp, H), w.k) < MARGIN)[0]
+        bad = np.nonzero(selection_margins(w, H, inp.sel_bias) < MARGIN)[0]
         if bad.size == 0:
             return inp, H
         synth.redraw_rows(inp, torch.as_tensor(bad, dtype=torch.int64), seed, attempt)

@@ -44,7 +44,7 @@ def test_version_and_status_strings():
 
 
 def test_config_struct_layout():
-    assert ctypes.sizeof(L.moe_config) == 8 + 4 * 13 + 4  # int64 T, 13 x 32-bit fields, tail padding
+    assert ctypes.sizeof(L.moe_config) == 8 + 4 * 15 + 4  # int64 T, 15 x 32-bit fields, tail padding
     assert ctypes.sizeof(L.moe_layer_args) == 31 * 8
 
 
@@ -93,6 +93,13 @@ def test_workspace_size_grows_with_tokens():
     (dict(capacity=-3), L.MOE_ERR_INVALID_ARG),
     (dict(capacity_factor=float("nan")), L.MOE_ERR_INVALID_ARG),
     (dict(T=2 ** 30, k=2), L.MOE_ERR_UNSUPPORTED),
+    (dict(n_group=-1), L.MOE_ERR_INVALID_ARG),
+    (dict(n_group=3, topk_group=1), L.MOE_ERR_INVALID_ARG),           # E = 8 not a multiple of 3
+    (dict(n_group=4, topk_group=0), L.MOE_ERR_INVALID_ARG),
+    (dict(n_group=4, topk_group=5), L.MOE_ERR_INVALID_ARG),
+    (dict(E=16, k=3, n_group=4, topk_group=2), L.MOE_ERR_INVALID_ARG),  # k not a multiple of topk_group
+    (dict(E=16, k=4, n_group=8, topk_group=1), L.MOE_ERR_INVALID_ARG),  # 1 group of 2 cannot hold k = 4
+    (dict(E=128, n_group=64, topk_group=2), L.MOE_ERR_UNSUPPORTED),
 ])
 def test_bad_configs_rejected(kw, status):
     base = dict(T=64, h=64, E=8, k=2, d_e=64)
@@ -102,6 +109,13 @@ def test_bad_configs_rejected(kw, status):
     n = ctypes.c_size_t()
     assert L.lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
     assert L.lib.moe_last_error().decode()
+
+
+def test_group_limited_configs_accepted():
+    n = ctypes.c_size_t()
+    for kw in (dict(n_group=0), dict(n_group=1), dict(n_group=8, topk_group=4), dict(n_group=32, topk_group=8)):
+        cfg = L.config(4096, 7168, 256, 8, 2048, **kw)
+        assert L.lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == L.MOE_OK, kw
 
 
 def test_null_pointers_rejected_before_any_launch():

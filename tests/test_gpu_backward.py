@@ -170,7 +170,8 @@ def test_layer_backward(w):
     assert L.moe_get_device_status(bufs.ws) == 0
     fwd = oracle.layer_forward(inp, T=w.T, h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn, renorm=w.renorm,
                                capacity_factor=w.capacity_factor, capacity_override=w.capacity, priority=w.priority,
-                               logits=H, sel_bias=inp.sel_bias, shared=inp.shared)
+                               logits=H, sel_bias=inp.sel_bias, shared=inp.shared, n_group=w.n_group,
+                               topk_group=w.topk_group)
     ref = oracle.layer_backward(inp, fwd, dO, k=w.k, d_e=w.d_e, score_fn=w.score_fn, renorm=w.renorm, w_aux=w_aux,
                                 w_z=w_z)
     tol = TOL[W.BF16]

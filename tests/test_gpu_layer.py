@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import LOGIT_TOL, TOL, delta_error, margin_inputs, normwise
+from gpu_helpers import LOGIT_TOL, TOL, delta_error, margin_inputs, normwise, route_of
 from mixture_experts_layer_84_b300 import _lib as L
 from mixture_experts_layer_84_b300 import synth
 from mixture_experts_layer_84_b300 import workloads as W
@@ -30,7 +30,7 @@ def run_layer(w, inp, with_logits=True):
 
 
 def check_routing_and_dispatch(w, bufs, H, sel_bias=None):
-    r = oracle.route(H, w.k, w.score_fn, w.renorm, sel_bias)
+    r = route_of(w, H, sel_bias)
     C = oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.capacity)
     d = oracle.dispatch(r["idx"], w.E, C, w.priority)
     A = int(d["offsets"][-1])
@@ -76,6 +76,10 @@ EDGE += [
                noisy=False, capacity_factor=1.0, n_shared=2, d_shared=40, sel_bias="normal"),
     W.Workload("shared2_bias_bf16", T=413, h=192, E=12, k=3, d_e=136, dtype=W.BF16, score_fn=W.SIGMOID,
                renorm=False, noisy=True, capacity_factor=1.3, n_shared=2, d_shared=200, sel_bias="normal"),
+    # group-limited routing: DS-V3's 8 groups, 4 kept, without a selection bias; softmax with
+    # groups of 16 that straddle the selection lanes' expert chunks, and a capacity limit
+    W.DSV3_SMALL.replace(name="dsv3_small_groups", n_group=8, topk_group=4),
+    W.STRESS_SMALL.replace(name="stress_small_groups", n_group=4, topk_group=2, capacity_factor=1.25),
 ]
 
 
@@ -86,7 +90,8 @@ def test_layer_small(w):
     r, d, A = check_routing_and_dispatch(w, bufs, H, inp.sel_bias)
     ref = oracle.layer_forward(inp, T=w.T, h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn, renorm=w.renorm,
                                capacity_factor=w.capacity_factor, capacity_override=w.capacity,
-                               priority=w.priority, logits=H, sel_bias=inp.sel_bias, shared=inp.shared)
+                               priority=w.priority, logits=H, sel_bias=inp.sel_bias, shared=inp.shared,
+                               n_group=w.n_group, topk_group=w.topk_group)
     tol = TOL[w.dtype]
     assert torch.equal(bufs.X[:A], inp.U[bufs.row_token[:A].long()])
     assert normwise(bufs.act[:A], ref["act"]) <= tol

@@ -164,6 +164,58 @@ def test_route_loss_free_selection_bias(T, E, k, score_fn, renorm):
     assert normwise(gate, want) <= LOGIT_TOL
 
 
+GROUPED = [  # T, E, k, n_group, topk_group, score_fn, renorm, selection bias
+    (300, 256, 8, 8, 4, SG, True, True),     # DS-V3's groups with the loss-free bias (lane = group)
+    (257, 256, 8, 8, 4, SG, True, False),
+    (180, 64, 6, 4, 2, SM, True, False),     # 2 lanes per token, 4 groups of 16
+    (150, 96, 4, 6, 2, SM, True, True),      # 4 lanes of 24 experts, groups of 16 straddle them
+    (100, 12, 4, 3, 2, SM, False, True),     # one lane per token
+    (90, 1024, 16, 32, 8, SG, True, False),  # 32 groups of 32, one per lane
+    (77, 40, 3, 20, 3, SG, False, False),    # groups of 2, r = 1
+    (64, 32, 2, 32, 2, SG, True, False),     # groups of one expert
+    (0, 256, 8, 8, 4, SG, True, False),
+]
+
+
+@pytest.mark.parametrize("T,E,k,n_group,topk_group,score_fn,renorm,bias", GROUPED)
+def test_route_group_limited(T, E, k, n_group, topk_group, score_fn, renorm, bias):
+    """Group-limited routing on the same float32 logits on both sides.  Rows whose group scores
+    and kept-expert keys keep a margin of 1e-4 (far above float32 score rounding) select exactly
+    what the oracle selects; every row uses at most topk_group groups and distinct experts, with
+    gates equal to the scores of what it selected.  The constant rows (all group scores tied)
+    keep the lowest groups and then the lowest ids."""
+    logits = synth.random_logits(T, E, seed=T + E + 5, scale=2.0, tie_fraction=0.0)
+    b = synth.normal((E,), 0.05, seed=E + 1, stream="sel_bias", device="cpu", dtype=torch.float32) if bias else None
+    cfg = L.config(T, 8, E, k, 8, score_fn=score_fn, renorm=renorm, dtype=W.F32, n_group=n_group,
+                   topk_group=topk_group)
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    gate = torch.full((T, k), -7.0, dtype=torch.float32, device="cuda")
+    ws = L.new_workspace(cfg)
+    L.moe_route(cfg, None, None, None, None, None, logits.cuda(), None, idx, gate, ws,
+                sel_bias=None if b is None else b.cuda())
+    assert L.moe_get_device_status(ws) == 0
+    if T == 0:
+        return
+    bb = None if b is None else oracle.f64(b)
+    r = oracle.route(oracle.f64(logits), k, score_fn, renorm, bb, n_group, topk_group)
+    key = r["sel_key"]
+    aff = r["s"] if b is None else key
+    ok = ((oracle.group_margins(aff, n_group, topk_group, k) >= 1e-4)
+          & (oracle.topk_margins(np.where(r["allowed"], key, -np.inf), k) >= 1e-4))
+    assert ok.mean() > 0.5
+    got = idx.cpu().numpy()
+    assert np.array_equal(got[ok], r["idx"][ok])
+    groups = got // (E // n_group)
+    assert all(len(set(g)) <= topk_group for g in groups.tolist())
+    assert all(len(set(row)) == k for row in got.tolist())
+    assert got.min() >= 0 and got.max() < E
+    sel = np.take_along_axis(r["s"], got.astype(np.int64), axis=1)
+    want = sel / sel.sum(axis=1, keepdims=True) if renorm else sel
+    assert normwise(gate, want) <= LOGIT_TOL
+    if T >= 4 and b is None:  # random_logits makes the last two rows constant
+        assert got[-1].tolist() == list(range(k)) == r["idx"][-1].tolist()
+
+
 @pytest.mark.parametrize("E", [8, 256, 1000])
 def test_balance_bias_update(E):
     counts = torch.as_tensor(np.random.default_rng(E).integers(0, 50, size=E), dtype=torch.int32)
