@@ -47,6 +47,10 @@ Sources (page title, section):
          of the K_r/M highest affinities among their experts; the top-k is then
          taken over the experts of the chosen nodes only.  On one GPU the nodes
          become n_group equal, contiguous groups of experts (reading below).
+  [FP8]  same page, 低精度通信: DeepSeek-V3 turns the activations that enter the MoE
+         up-projection into FP8 before the dispatch, so that they feed the
+         up-projection's FP8 forward as they are; the scaling factors are
+         integral powers of 2; the combine stays BF16.
   [BWD]  same page, 专家计算：padding、block-sparse 与 grouped GEMM: the backward of
          the SwiGLU experts is grouped GEMMs too, one group for the input
          gradients and one for the weight gradients.
@@ -66,7 +70,14 @@ Readings where the pages are silent (the same readings the library follows):
     r = k/topk_group highest affinities (the scores s, or s + b with a
     loss-free selection bias); the topk_group best groups are kept, ties to
     the lower group id; the top-k is then taken over the kept groups' experts
-    only (by the usual selection key).  Group selection adds no gradient path.
+    only (by the usual selection key).  Group selection adds no gradient path;
+  * FP8 ([FP8]) is E4M3 (finite, largest 448, round to nearest even).  Every
+    token row of U and every row (output channel) of W_gate and W_up gets one
+    power-of-two scale 2^s, s the smallest integer >= -127 with
+    amax <= 448 * 2^s; codes = E4M3(x * 2^-s).  The up-projection (gate|up)
+    multiplies the dequantised values codes * 2^s exactly; act, the down
+    projection, the shared experts and the combine stay at the layer's
+    precision (bf16).
 
 Every function here is pinned by the `-m "not gpu"` tests (worked examples of
 the pages, closed forms, invariants, brute force and textbook special cases).
@@ -295,6 +306,73 @@ def expert_ffn(X, offsets, W_gate, W_up, W_down, d_e: int):
     return Y, act
 
 
+# --------------------------------------------------------------------------
+# FP8 dispatch and up-projection  [FP8]
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Nearest E4M3 value, ties to even, saturating at +-448.
+
+    E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
+    infinities.  In the binade [2^e, 2^(e+1)), e >= -6, neighbours are
+    2^(e-3) apart; below 2^-6 the subnormals are 2^-9 apart.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, E = np.frexp(a)                      # a = m 2^E, m in [0.5, 1): binade e = E - 1
+    e = np.maximum(E - 1, -6)
+    quantum = np.ldexp(1.0, e - 3)
+    r = np.minimum(np.round(a / quantum) * quantum, E4M3_MAX)  # np.round: half to even
+    return np.copysign(r, x)
+
+
+def e4m3_bits(v) -> np.ndarray:
+    """The 8-bit codes (sign | exponent field << 3 | mantissa) of E4M3 values."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, E = np.frexp(a)
+    e = E - 1
+    normal = a >= 2.0 ** -6
+    field = np.where(normal, e + 7, 0)
+    mant = np.where(normal, (np.ldexp(a, -np.where(normal, e, 0)) - 1.0) * 8.0, a * 2.0 ** 9)
+    sign = np.signbit(v).astype(np.int64) << 7
+    return (sign | (field.astype(np.int64) << 3) | mant.astype(np.int64)).astype(np.uint8)
+
+
+def pow2_scale_exponents(amax) -> np.ndarray:
+    """Per row, the smallest integer s >= -127 with amax <= 448 * 2^s (-127 when amax = 0).
+
+    With amax = m 2^E, m in [0.5, 1), and 448 = 0.875 * 2^9: s = E - 9, plus 1 when m > 0.875.
+    """
+    amax = np.asarray(amax, dtype=np.float64)
+    m, E = np.frexp(amax)
+    s = E - 9 + (m > 0.875).astype(np.int64)
+    return np.where(amax > 0, np.maximum(s, -127), -127).astype(np.int64)
+
+
+def quantize_rows_fp8(A):
+    """Row-wise E4M3 with one power-of-two scale per row: (codes [n, c], s [n]), A ~ codes * 2^s."""
+    A = f64(A)
+    amax = np.max(np.abs(A), axis=1) if A.shape[1] else np.zeros(A.shape[0])
+    s = pow2_scale_exponents(amax)
+    return e4m3_round(np.ldexp(A, -s[:, None])), s
+
+
+def dequantize_rows_fp8(codes, s) -> np.ndarray:
+    return np.ldexp(f64(codes), np.asarray(s, dtype=np.int64)[:, None])
+
+
+def fp8_weights(W) -> np.ndarray:
+    """[E, d, h] weights as the FP8 up-projection sees them: each row quantised and dequantised."""
+    out = np.empty(tuple(W.shape), dtype=np.float64)
+    for e in range(W.shape[0]):
+        out[e] = dequantize_rows_fp8(*quantize_rows_fp8(W[e]))
+    return out
+
+
 def shared_ffn(U, W_gate_sh, W_up_sh, W_down_sh) -> np.ndarray:
     """Y_sh [N_s, T, h]: each shared expert's SwiGLU FFN on every token.  [SHR], [FFN]"""
     U = f64(U)
@@ -390,35 +468,46 @@ def route(H, k: int, score_fn: int, renorm: bool, sel_bias=None, n_group: int = 
 
 def layer_forward(inp, *, T, h, E, k, d_e, score_fn, renorm, capacity_factor,
                   capacity_override=0, priority=CHOICE_MAJOR, logits=None, sel_bias=None, shared=None,
-                  n_group=1, topk_group=1) -> dict:
+                  n_group=1, topk_group=1, fp8=False) -> dict:
     """The full single-GPU MoE layer forward, stage by stage, in float64.
 
     `inp` carries U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down (numpy or
     torch).  If `logits` is given the router GEMM is skipped and those logits
     are used as they are.  `sel_bias` [E] is the loss-free selection bias
     ([LFB]); `shared` = (W_gate_sh, W_up_sh, W_down_sh) adds shared experts
-    ([SHR]); n_group > 1 limits each token to topk_group expert groups ([GRP]).
+    ([SHR]); n_group > 1 limits each token to topk_group expert groups ([GRP]);
+    fp8 runs the dispatch and the up-projection on E4M3 codes ([FP8]): X holds
+    the dequantised token rows, and "U_codes", "U_s" the quantised U.
     """
     H = router_logits(inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps) if logits is None else f64(logits)
     r = route(H, k, score_fn, renorm, sel_bias, n_group, topk_group)
     C = capacity(T, E, k, capacity_factor, capacity_override)
     d = dispatch(r["idx"], E, C, priority)
-    X = permute(inp.U, d["row_token"])
-    Y, act = expert_ffn(X, d["offsets"], inp.W_gate, inp.W_up, inp.W_down, d_e)
+    extra = {}
+    if fp8:
+        codes, s_u = quantize_rows_fp8(inp.U)
+        X = permute(dequantize_rows_fp8(codes, s_u), d["row_token"])
+        Y, act = expert_ffn(X, d["offsets"], fp8_weights(inp.W_gate), fp8_weights(inp.W_up), inp.W_down, d_e)
+        extra = dict(U_codes=codes, U_s=s_u)
+    else:
+        X = permute(inp.U, d["row_token"])
+        Y, act = expert_ffn(X, d["offsets"], inp.W_gate, inp.W_up, inp.W_down, d_e)
     Y_sh = None if shared is None else shared_ffn(inp.U, *shared)
     out = combine(inp.U, Y, d["slot_row"], r["gate"], k, Y_sh)
     st = load_stats(d["counts_routed"], r["s"], T, k, score_fn)
-    return dict(r, **d, X=X, act=act, Y=Y, Y_shared=Y_sh, out=out, z_loss=router_z_loss(r["logits"]), **st)
+    return dict(r, **d, X=X, act=act, Y=Y, Y_shared=Y_sh, out=out, z_loss=router_z_loss(r["logits"]), **st,
+                **extra)
 
 
-def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int, shared=None) -> dict:
+def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int, shared=None, fp8=False) -> dict:
     """out rows (and the Y rows they use) for a sample of tokens.
 
     For full-size checks: X[row] = U[t] for a kept pair, so each needed Y row
     is one expert applied to one token row ([FFN]); out follows [FFN]'s layer
     output.  The sampled rows are grouped by expert so that each expert's
     weights are read (and widened to float64) once.
-    With `shared` the shared experts' outputs ([SHR]) are added too.
+    With `shared` the shared experts' outputs ([SHR]) are added too; with
+    `fp8` the experts see the E4M3 token rows and gate/up weights ([FP8]).
     Returns {"out": [n, h], "Y": {row: [h]}}.
     """
     tokens = [int(t) for t in tokens]
@@ -434,7 +523,12 @@ def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int, shared=None) -> di
     y_of = {}
     for e, pairs in sorted(by_expert.items()):
         x = np.stack([U[t] for t, _ in pairs])
-        y, _ = swiglu(x, inp.W_gate[e], inp.W_up[e], inp.W_down[e])
+        if fp8:
+            x = dequantize_rows_fp8(*quantize_rows_fp8(x))
+            y, _ = swiglu(x, dequantize_rows_fp8(*quantize_rows_fp8(inp.W_gate[e])),
+                          dequantize_rows_fp8(*quantize_rows_fp8(inp.W_up[e])), inp.W_down[e])
+        else:
+            y, _ = swiglu(x, inp.W_gate[e], inp.W_up[e], inp.W_down[e])
         for (t, j), row in zip(pairs, y):
             y_of[(t, j)] = row
     outs, Yrows = [], {}

@@ -535,6 +535,87 @@ def pin_group_limited_bruteforce(O):
         assert all(len(set(g)) <= topk_group for g in groups.tolist())
 
 
+def _e4m3_probe_values():
+    """Every E4M3 grid value, every midpoint between neighbours (ties), points just either side
+    of each midpoint, and log-uniform random values, with both signs."""
+    grid = [0.0] + [k * 2.0 ** -9 for k in range(1, 8)]
+    for e in range(-6, 9):
+        grid += [(1 + m / 8.0) * 2.0 ** e for m in range(8)]
+    grid = np.array(sorted(v for v in grid if v <= 448.0))
+    mids = (grid[1:] + grid[:-1]) / 2
+    rnd = np.exp(_rng(41).uniform(np.log(2.0 ** -12), np.log(448.0), size=4000))
+    v = np.concatenate([grid, mids, mids * (1 + 2.0 ** -20), mids * (1 - 2.0 ** -20), rnd])
+    return grid, np.concatenate([v, -v])
+
+
+def pin_e4m3_rounding_against_torch(O):
+    """E4M3 rounding and bit codes equal torch's float8_e4m3fn cast (round to nearest even) on
+    every grid value, every tie, both sides of every tie and random values."""
+    import torch
+    _, v = _e4m3_probe_values()
+    t = torch.tensor(v, dtype=torch.float64).to(torch.float8_e4m3fn)
+    assert np.array_equal(O.e4m3_round(v), t.to(torch.float64).numpy())
+    assert np.array_equal(O.e4m3_bits(O.e4m3_round(v)), t.view(torch.uint8).numpy())
+
+
+def pin_e4m3_grid(O):
+    """The format's facts: 127 non-negative finite values, largest 448, smallest normal 2^-6,
+    smallest subnormal 2^-9; half the smallest subnormal rounds to zero (tie to even)."""
+    grid, _ = _e4m3_probe_values()
+    dense = np.concatenate([np.linspace(0, 448, 200001), grid])
+    vals = np.unique(O.e4m3_round(dense))
+    assert len(vals) == 127 and vals.max() == 448.0 and vals[1] == 2.0 ** -9
+    assert 2.0 ** -6 in vals and O.e4m3_round(2.0 ** -10) == 0.0 and O.e4m3_round(1.5 * 2.0 ** -10) == 2.0 ** -9
+    assert O.e4m3_round(1000.0) == 448.0
+
+
+def pin_pow2_scale_exponents(O):
+    """The scale 2^s is the smallest power of two with amax <= 448 * 2^s: worked values and a
+    brute-force minimality check."""
+    got = O.pow2_scale_exponents(np.array([448.0, 449.0, 1.0, 0.0, 896.0, 897.0, 3.0, 0.75]))
+    assert got.tolist() == [0, 1, -8, -127, 1, 2, -7, -9]
+    amax = np.exp(_rng(42).uniform(-30, 30, size=2000))
+    s = O.pow2_scale_exponents(amax)
+    assert np.all(amax <= 448.0 * 2.0 ** s.astype(float))
+    assert np.all((amax > 448.0 * 2.0 ** (s - 1.0)) | (s == -127))
+
+
+def pin_fp8_rows_on_grid_and_bounded(O):
+    """Quantised rows: codes are E4M3 values within +-448, the row maximum uses the top binade,
+    and each dequantised entry is within half an E4M3 step (2^-4 relative, or 2^-10 * 2^s in the
+    subnormal range) of the input; fp8_weights applies exactly that to every expert row."""
+    A = _rng(43).normal(size=(30, 200)) * np.exp(_rng(44).uniform(-5, 5, size=(30, 1)))
+    codes, s = O.quantize_rows_fp8(A)
+    assert np.array_equal(O.e4m3_round(codes), codes) and np.abs(codes).max() <= 448.0
+    assert np.all(np.abs(codes).max(axis=1) >= 224.0)
+    deq = O.dequantize_rows_fp8(codes, s)
+    bound = np.maximum(np.abs(A) * 2.0 ** -4, 2.0 ** -10 * 2.0 ** s[:, None].astype(float))
+    assert np.all(np.abs(deq - A) <= bound)
+    W = A.reshape(3, 10, 200)
+    assert np.array_equal(O.fp8_weights(W), deq.reshape(3, 10, 200))
+
+
+def pin_fp8_layer_lossless_on_grid(O):
+    """When every token row and every gate/up weight row is exactly representable after its
+    power-of-two scaling (entries in {0, +-1, +-2, +-3} with a 3 in each row; weights in
+    {+-1/4, +-1/2, +-3/4} with a 3/4 in each row), the FP8 layer equals the unquantised one."""
+    rng = _rng(45)
+    T, h, E, k, d_e = 40, 16, 4, 2, 12
+    U = rng.integers(-3, 4, size=(T, h)).astype(float)
+    U[:, 0] = 3.0
+    def wq(shape):
+        w = rng.choice([-0.75, -0.5, -0.25, 0.25, 0.5, 0.75], size=shape)
+        w[..., 0] = 0.75
+        return w
+    inp = _inputs(U=U, W_r=rng.normal(size=(h, E)) * 0.3, b_r=None, W_noise=None, eps=None,
+                  W_gate=wq((E, d_e, h)), W_up=wq((E, d_e, h)), W_down=rng.normal(size=(E, h, d_e)) * 0.1)
+    kw = dict(T=T, h=h, E=E, k=k, d_e=d_e, score_fn=O.SOFTMAX, renorm=True, capacity_factor=1.0)
+    a, b = O.layer_forward(inp, **kw), O.layer_forward(inp, fp8=True, **kw)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["act"], b["act"])
+    assert np.array_equal(b["U_s"], np.full(T, -7))
+    assert np.array_equal(O.dequantize_rows_fp8(b["U_codes"], b["U_s"]), U)
+
+
 def pin_balance_bias_update(O):
     """e_i = mean(c) - c_i; an overloaded expert's bias drops by u, an underloaded one rises by u,
     one exactly at the mean keeps its bias."""

@@ -198,6 +198,32 @@ def _router_input_backward_no_noise_factor(U, W_r, dH, W_noise=None, eps=None):
     return r
 
 
+def _e4m3_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, E = np.frexp(a)
+    q = np.ldexp(1.0, np.maximum(E - 1, -6) - 3)
+    return np.copysign(np.minimum(np.floor(a / q + 0.5) * q, 448.0), x)
+
+
+def _e4m3_flush_subnormals(x):
+    r = _orig["e4m3_round"](x)
+    return np.where(np.abs(r) < 2.0 ** -6, 0.0 * r, r)
+
+
+def _scale_one_too_small(amax):
+    return _orig["pow2_scale_exponents"](amax) - 1
+
+
+def _fp8_weights_unquantised(W):
+    return np.stack([np.asarray(W[e], dtype=np.float64) for e in range(W.shape[0])])
+
+
+def _quantize_rows_scale_up(A):
+    codes, s = _orig["quantize_rows_fp8"](A)
+    return codes, s + 1
+
+
 MUTANTS = {
     "gates_not_renormalised": ("gates", _gates_no_renorm),
     "ties_to_higher_id": ("topk_select", _topk_ties_high),
@@ -222,6 +248,11 @@ MUTANTS = {
     "loss_free_bias_ignored": ("route", _route_ignores_bias),
     "shared_experts_not_added": ("combine", _combine_ignores_shared),
     "group_mask_ignored": ("topk_select", _topk_ignores_allowed),
+    "e4m3_ties_away_from_zero": ("e4m3_round", _e4m3_ties_away),
+    "e4m3_subnormals_flushed": ("e4m3_round", _e4m3_flush_subnormals),
+    "fp8_scale_one_binade_low": ("pow2_scale_exponents", _scale_one_too_small),
+    "fp8_weights_not_quantised": ("fp8_weights", _fp8_weights_unquantised),
+    "fp8_dequant_with_wrong_scale": ("quantize_rows_fp8", _quantize_rows_scale_up),
     "group_scored_on_best_expert_only": ("group_scores", _group_scores_best_only),
     "groups_strided_not_contiguous": ("group_limited_mask", _group_mask_strided),
     "groups_scored_on_logits": ("route", _route_groups_on_logits),
