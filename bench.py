@@ -149,15 +149,18 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- algorithmic work
 
-def stage_work(w: W.Workload, A: float, n_active: float):
-    """Algorithmic bytes and FLOPs of each stage for one step (A kept pairs, n_active experts with rows)."""
+def stage_work(w: W.Workload, A: float, n_active: float, fp8: bool = False):
+    """Algorithmic bytes and FLOPs of each stage for one step (A kept pairs, n_active experts with rows).
+    fp8: the dispatched rows and the gate/up weights are one byte per element (plus a float32 scale
+    per row)."""
     b = w.elem_bytes
     T, h, E, k, d = w.T, w.h, w.E, w.k, w.d_e
     route_bytes = T * h * b + h * E * b + T * k * 8 + (h * E * b + T * E * 4 if w.noisy else 0)
     route_flops = 2 * T * h * E * (2 if w.noisy else 1)
-    dispatch_bytes = T * h * b + A * h * b + T * k * 12
+    xb, wb = (1, 1) if fp8 else (b, b)
+    dispatch_bytes = T * h * b + A * h * xb + T * k * 12 + (A * 4 if fp8 else 0)
     ffn_flops = 6 * A * h * d
-    ffn_bytes = 3 * h * d * b * n_active + 2 * A * h * b + 2 * A * d * b
+    ffn_bytes = (2 * wb + b) * h * d * n_active + A * h * xb + A * h * b + 2 * A * d * b
     combine_bytes = A * h * b + 2 * T * h * b + T * k * 8 + w.n_shared * T * h * b
     work = {"route": {"bytes": route_bytes, "flops": route_flops},
             "dispatch": {"bytes": dispatch_bytes, "flops": 0},
@@ -403,19 +406,32 @@ def run_b300(args, w: W.Workload):
     n_rot = max(2, min(64, math.ceil(2 * L2_BYTES / max(ubytes, 1))))
     pool = [inp.U] + [synth.normal((w.T, w.h), 1.0, 100 + r, "U", device, w.torch_dtype) for r in range(n_rot - 1)]
     cfg = L.config_of(w)
-    bufs = L.LayerBuffers.allocate(cfg, device=device)
+    fp8 = args.fp8
+    if fp8 and (w.dtype != W.BF16 or w.h % 16):
+        raise SystemExit("bench.py --fp8: needs a bf16 workload with h % 16 == 0")
+    bufs = L.LayerBuffers.allocate(cfg, device=device, with_X=not fp8)
+    w8 = L.FP8Weights.quantize(inp.W_gate, inp.W_up) if fp8 else None  # once, outside every timed region
+    rows8 = L.FP8Rows.allocate(cfg, device=device) if fp8 else None
 
     def stage_calls(U, ev=None):
-        # the stage calls of moe_layer_forward, with events between them
+        # the stage calls of moe_layer_forward (or moe_layer_forward_fp8), with events between them
         L.moe_route(cfg, U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, None, None, bufs.idx, bufs.gate, bufs.ws,
                     sel_bias=inp.sel_bias)
         if ev is not None:
             ev[0].record()
-        L.moe_dispatch(cfg, U, bufs.idx, bufs.counts_routed, bufs.counts_kept, bufs.offsets, bufs.slot_row,
-                       bufs.row_token, bufs.X, bufs.n_dropped, bufs.ws)
+        if fp8:
+            L.moe_dispatch_fp8(cfg, U, bufs.idx, bufs.counts_routed, bufs.counts_kept, bufs.offsets, bufs.slot_row,
+                               bufs.row_token, rows8.X8, rows8.x_scale, bufs.n_dropped, bufs.ws)
+        else:
+            L.moe_dispatch(cfg, U, bufs.idx, bufs.counts_routed, bufs.counts_kept, bufs.offsets, bufs.slot_row,
+                           bufs.row_token, bufs.X, bufs.n_dropped, bufs.ws)
         if ev is not None:
             ev[1].record()
-        L.moe_expert_ffn(cfg, bufs.X, bufs.offsets, inp.W_gate, inp.W_up, inp.W_down, bufs.act, bufs.Y, bufs.ws)
+        if fp8:
+            L.moe_expert_ffn_fp8(cfg, rows8.X8, rows8.x_scale, bufs.offsets, w8, inp.W_down, bufs.act, bufs.Y,
+                                 bufs.ws)
+        else:
+            L.moe_expert_ffn(cfg, bufs.X, bufs.offsets, inp.W_gate, inp.W_up, inp.W_down, bufs.act, bufs.Y, bufs.ws)
         if ev is not None:
             ev[2].record()
         if w.n_shared:
@@ -521,8 +537,12 @@ def run_b300(args, w: W.Workload):
         with torch.cuda.stream(s_comp):
             s_comp.wait_event(ev_in[b])
             s_comp.wait_event(ev_out[b])           # out[b] of two steps back has been read
-            L.moe_layer_forward(cfg, U_dev[b], inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up,
-                                inp.W_down, bset[b], stream=s_comp, sel_bias=inp.sel_bias, shared=inp.shared)
+            if fp8:
+                L.moe_layer_forward_fp8(cfg, U_dev[b], inp.W_r, inp.b_r, inp.W_noise, inp.eps, w8, inp.W_down,
+                                        bset[b], rows8, stream=s_comp, sel_bias=inp.sel_bias, shared=inp.shared)
+            else:
+                L.moe_layer_forward(cfg, U_dev[b], inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up,
+                                    inp.W_down, bset[b], stream=s_comp, sel_bias=inp.sel_bias, shared=inp.shared)
             ev_comp[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])
@@ -548,7 +568,7 @@ def run_b300(args, w: W.Workload):
     # the layer backward (bf16): L = <dO, out> + 0.01 E sum f P + 0.001 L_z, on the forward of
     # the first batch; timed over min(K, 50) steps after 3 warm-up steps (not part of `value`)
     train = None
-    if w.dtype == W.BF16 and not args.no_backward:
+    if w.dtype == W.BF16 and not args.no_backward and not fp8:
         fb = L.LayerBuffers.allocate(cfg, device=device, with_logits=True)
         fwd_args = (cfg, pool[0], inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up, inp.W_down, fb)
         L.moe_layer_forward(*fwd_args, sel_bias=inp.sel_bias, shared=inp.shared)
@@ -601,7 +621,7 @@ def run_b300(args, w: W.Workload):
         stage_ms["combine"].append(e[3].elapsed_time(ends[i]))
     A_mean = sum(A_of[i % n_rot] for i in range(K)) / K
     act_mean = sum(act_of[i % n_rot] for i in range(K)) / K
-    work = stage_work(w, A_mean, act_mean)
+    work = stage_work(w, A_mean, act_mean, fp8)
     peaks, peak_src = measured_peaks()
     stages = {}
     for name, ms in stage_ms.items():
@@ -623,6 +643,13 @@ def run_b300(args, w: W.Workload):
         # float32 CUDA-core FMA peak: 148 SMs x 128 lanes x 2 FLOP x 2.032 GHz
         roof = {"bound": "alu", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12,
                 "peak": 148 * 128 * 2 * 2.032e9 / 1e12, "unit": "TFLOP/s"}
+    elif fp8:
+        # gate|up (4 A h d FLOPs) at twice the bf16 rate (the recipe's nominal fp8 : bf16 ratio) and
+        # down (2 A h d) at the bf16 rate: the peak is the FLOPs over the time both take at peak
+        f1, f2 = 4 * A_mean * w.h * w.d_e, 2 * A_mean * w.h * w.d_e
+        mixed = (f1 + f2) / (f1 / (2 * peaks["bf16_tflops"]) + f2 / peaks["bf16_tflops"]) if f1 + f2 else 1.0
+        roof = {"bound": "tensor", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12, "peak": round(mixed, 1),
+                "unit": "TFLOP/s"}
     elif intensity >= ridge:
         roof = {"bound": "tensor", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
@@ -630,28 +657,35 @@ def run_b300(args, w: W.Workload):
         roof = {"bound": "hbm", "achieved": ffn["bytes"] / (ffn_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    if roof["bound"] == "tensor":
+    if roof["bound"] == "tensor" and not fp8:
         # the same against the bf16 rate measured under the power cap in a seconds-long loop
         roof["peak_sustained"] = peaks["bf16_tflops_sustained"]
         roof["frac_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
     roof["achieved"] = round(roof["achieved"], 2)
-    roof["traffic"] = profile_traffic(w.name)
+    roof["traffic"] = None if fp8 else profile_traffic(w.name)
     roof["kernel"] = "grouped SwiGLU expert GEMM: grouped_gemm_tc gate|up + down, both launches of one step"
     roof["peak_source"] = f"{peak_src}, {'bf16 burst' if roof['bound'] == 'tensor' else roof['bound']}"
+    if fp8:
+        roof["kernel"] = ("grouped SwiGLU expert GEMM: grouped_gemm_tc<true, true> E4M3 gate|up (kind::f8f6f4) + "
+                          "bf16 down, both launches of one step")
+        roof["peak_source"] += ("; E4M3 gate|up at 2x the measured bf16 burst (nominal ratio), combined with "
+                                "bf16 down by their FLOPs")
 
     value = weak_scaling_value(w.T, K, ws_n, max_ms * 1e-3)
     e2e_value = weak_scaling_value(w.T, K, ws_n, max_e2e)
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_n, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(max_ms / K, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == W.BF16 else "f32",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": ("e4m3 dispatch and gate|up, bf16 elsewhere" if fp8 else "bf16") if w.dtype == W.BF16 else "f32",
             "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, device-resident)",
-            "config": workload_config(w, n_rot),
+            "config": dict(workload_config(w, n_rot), **({"fp8": "E4M3 token rows and gate/up weight rows, "
+                                                                  "one power-of-two scale per row"} if fp8 else {})),
             "roofline": roof, "stages": stages,
             "kept_pairs_A": A_mean, "active_experts": act_mean,
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.h * w.elem_bytes,
                     "d2h_bytes_per_step": w.T * w.h * w.elem_bytes + 4,
-                    "how": "moe_layer_forward per step with its U copied in from pinned host memory and out + aux "
+                    "how": f"moe_layer_forward{'_fp8' if fp8 else ''} per step with its U copied in from pinned host memory and out + aux "
                            "copied back; copy-in, layer and copy-out of consecutive steps overlap on three streams"},
             "gpu_launches": launches_per_step(w) * K,
             "launch": "one CUDA graph replay per step (the whole layer)" if graphs else
@@ -659,7 +693,7 @@ def run_b300(args, w: W.Workload):
             "clocks": clk}
     if train:
         line["train_step"] = train
-    if ws_n == 1 and not args.no_cpu_baseline:
+    if ws_n == 1 and not args.no_cpu_baseline and not fp8:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample_tokens)
     print(json.dumps(line), flush=True)
     return 0
@@ -676,6 +710,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the layer backward")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time moe_layer_forward_fp8 (E4M3 dispatch and gate|up GEMM) instead of the bf16 layer")
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

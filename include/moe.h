@@ -358,6 +358,52 @@ typedef struct moe_layer_args {
 moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args* args, void* ws,
                              moe_stream_t stream);
 
+/* ---- FP8 dispatch and up-projection (section 低精度通信) -------------------------------
+ * The activations entering the up-projection travel and multiply as FP8 E4M3 codes with one
+ * power-of-two scale per row; the down projection, the shared experts and the combine stay bf16.
+ * Row rule (all calls below): s = the smallest integer >= -127 with amax(row) <= 448 * 2^s,
+ * scale = 2^s (float32, exact), code = E4M3(x * 2^-s) rounded to nearest even.  bf16 configs
+ * only, with h % 16 == 0 (MOE_ERR_UNSUPPORTED otherwise). */
+
+/* Quantise rows: src [rows, cols] bf16 -> dst [rows, cols] E4M3 bytes, scale [rows] float32.
+ * cols % 8 == 0; src and dst 16- and 8-byte aligned.  For the expert weights: W_gate and W_up
+ * as [E * d_e, h] (one scale per output channel), once, before the layer runs. */
+moe_status moe_quantize_fp8(int64_t rows, int32_t cols, const void* src, uint8_t* dst, float* scale,
+                            moe_stream_t stream);
+
+/* moe_dispatch with FP8 rows: the same routing metadata (bit-exact with moe_dispatch), and
+ *   X8       [T*k, h] E4M3 out         X8[row] = codes of U[row_token[row]]
+ *   x_scale  [T*k] float32 out         the scale of that token row
+ * Each token row is quantised once and copied to its kept slots. */
+moe_status moe_dispatch_fp8(const moe_config* cfg, const void* U, const int32_t* idx,
+                            int32_t* counts_routed, int32_t* counts_kept, int32_t* offsets,
+                            int32_t* slot_row, int32_t* row_token, uint8_t* X8, float* x_scale,
+                            int64_t* n_dropped, void* ws, moe_stream_t stream);
+
+/* moe_expert_ffn with the FP8 up-projection:
+ *   X8, x_scale                        from moe_dispatch_fp8
+ *   W_gate8, W_up8 [E, d_e, h] E4M3    s_gate, s_up [E * d_e] float32: from moe_quantize_fp8
+ *   W_down   [E, h, d_e] bf16          act [T*k, d_e] bf16 out, Y [T*k, h] bf16 out
+ * G = (X8 W_gate8^T) * x_scale[row] * s_gate[col] (and Up alike) on the tensor cores
+ * (kind::f8f6f4, float32 accumulation of exact products), act = SiLU(G) * Up rounded to bf16,
+ * Y = act W_down^T as in moe_expert_ffn. */
+moe_status moe_expert_ffn_fp8(const moe_config* cfg, const uint8_t* X8, const float* x_scale,
+                              const int32_t* offsets, const uint8_t* W_gate8, const uint8_t* W_up8,
+                              const float* s_gate, const float* s_up, const void* W_down, void* act,
+                              void* Y, void* ws, moe_stream_t stream);
+
+/* The FP8 operands of moe_layer_forward_fp8. */
+typedef struct moe_fp8_args {
+  uint8_t* X8; float* x_scale;                    /* [T*k, h], [T*k] outputs of the dispatch */
+  const uint8_t* W_gate8; const uint8_t* W_up8;   /* [E, d_e, h] */
+  const float* s_gate; const float* s_up;         /* [E * d_e] */
+} moe_fp8_args;
+
+/* moe_layer_forward with moe_dispatch_fp8 and moe_expert_ffn_fp8 in place of moe_dispatch and
+ * moe_expert_ffn (args->X, args->W_gate and args->W_up are not used). */
+moe_status moe_layer_forward_fp8(const moe_config* cfg, const moe_layer_args* args,
+                                 const moe_fp8_args* fp8, void* ws, moe_stream_t stream);
+
 /* Gradients and scratch of one layer backward (bf16 configs).  Scratch is caller-owned. */
 typedef struct moe_layer_grads {
   const void* dO;        /* [T, h]   dL/dout */

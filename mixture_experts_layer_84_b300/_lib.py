@@ -26,7 +26,8 @@ EXPORTS = ("moe_version", "moe_status_string", "moe_last_error", "moe_capacity",
            "moe_route", "moe_balance_bias_update", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn",
            "moe_shared_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status", "moe_combine_backward",
            "moe_route_backward", "moe_expert_ffn_backward", "moe_dispatch_backward", "moe_router_input_backward",
-           "moe_layer_backward")
+           "moe_layer_backward", "moe_quantize_fp8", "moe_dispatch_fp8", "moe_expert_ffn_fp8",
+           "moe_layer_forward_fp8")
 
 
 class MoeError(RuntimeError):
@@ -52,6 +53,10 @@ class moe_layer_args(ctypes.Structure):
         "counts_routed", "counts_kept", "offsets", "slot_row", "row_token", "n_dropped", "X", "act", "Y",
         "out", "f", "P", "aux", "z_loss", "sel_bias", "W_gate_shared", "W_up_shared", "W_down_shared",
         "act_shared", "Y_shared")]
+
+
+class moe_fp8_args(ctypes.Structure):
+    _fields_ = [(n, _P) for n in ("X8", "x_scale", "W_gate8", "W_up8", "s_gate", "s_up")]
 
 
 class moe_layer_grads(ctypes.Structure):
@@ -104,6 +109,15 @@ def _load() -> ctypes.CDLL:
     lib.moe_layer_backward.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), ctypes.POINTER(moe_layer_grads), _P, _P]
     lib.moe_layer_forward.restype = S
     lib.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), _P, _P]
+    lib.moe_quantize_fp8.restype = S
+    lib.moe_quantize_fp8.argtypes = [I64, ctypes.c_int32, _P, _P, _P, _P]
+    lib.moe_dispatch_fp8.restype = S
+    lib.moe_dispatch_fp8.argtypes = [cfgp] + [_P] * 10 + [_P, _P]
+    lib.moe_expert_ffn_fp8.restype = S
+    lib.moe_expert_ffn_fp8.argtypes = [cfgp] + [_P] * 10 + [_P, _P]
+    lib.moe_layer_forward_fp8.restype = S
+    lib.moe_layer_forward_fp8.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), ctypes.POINTER(moe_fp8_args), _P,
+                                          _P]
     lib.moe_get_device_status.restype = S
     lib.moe_get_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
     return lib
@@ -328,7 +342,8 @@ class LayerBuffers:
     ws: torch.Tensor
 
     @staticmethod
-    def allocate(cfg: moe_config, device="cuda", with_logits: bool = False) -> "LayerBuffers":
+    def allocate(cfg: moe_config, device="cuda", with_logits: bool = False, with_X: bool = True) -> "LayerBuffers":
+        """with_X=False leaves X empty (the FP8 layer dispatches into FP8Rows instead)."""
         dt = _act_dtype(cfg)
         T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
         i32, f32 = torch.int32, torch.float32
@@ -341,7 +356,8 @@ class LayerBuffers:
             slot_row=torch.empty(T * k, dtype=i32, device=device),
             row_token=torch.empty(T * k, dtype=i32, device=device),
             n_dropped=torch.empty(1, dtype=torch.int64, device=device),
-            X=torch.empty((T * k, h), dtype=dt, device=device), act=torch.empty((T * k, d), dtype=dt, device=device),
+            X=torch.empty((T * k if with_X else 0, h), dtype=dt, device=device),
+            act=torch.empty((T * k, d), dtype=dt, device=device),
             Y=torch.empty((T * k, h), dtype=dt, device=device), out=torch.empty((T, h), dtype=dt, device=device),
             f=torch.empty(E, dtype=f32, device=device), P=torch.empty(E, dtype=f32, device=device),
             aux=torch.empty(1, dtype=f32, device=device), z_loss=torch.empty(1, dtype=f32, device=device),
@@ -379,7 +395,7 @@ def layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: Layer
         slot_row=_ptr(bufs.slot_row, "slot_row", torch.int32, T * k),
         row_token=_ptr(bufs.row_token, "row_token", torch.int32, T * k),
         n_dropped=_ptr(bufs.n_dropped, "n_dropped", torch.int64, 1),
-        X=_ptr(bufs.X, "X", dt, T * k * h), act=_ptr(bufs.act, "act", dt, T * k * d),
+        X=_ptr(bufs.X, "X", dt, T * k * h) if bufs.X.numel() else None, act=_ptr(bufs.act, "act", dt, T * k * d),
         Y=_ptr(bufs.Y, "Y", dt, T * k * h), out=_ptr(bufs.out, "out", dt, T * h),
         f=_ptr(bufs.f, "f", torch.float32, E), P=_ptr(bufs.P, "P", torch.float32, E),
         aux=_ptr(bufs.aux, "aux", torch.float32, 1), z_loss=_ptr(bufs.z_loss, "z_loss", torch.float32, 1),
@@ -389,6 +405,94 @@ def layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: Layer
         act_shared=_ptr(bufs.act_shared, "act_shared", dt, ns * T * ds) if ns else None,
         Y_shared=_ptr(bufs.Y_shared, "Y_shared", dt, ns * T * h) if ns else None)
     return a
+
+
+# ---- FP8 dispatch and up-projection ----------------------------------------------------------
+
+def moe_quantize_fp8(src, dst, scale, stream=None):
+    """src [rows, cols] bf16 -> dst [rows, cols] uint8 E4M3 codes, scale [rows] float32 (powers of two)."""
+    if src.dim() != 2:
+        raise ValueError("src: expected a [rows, cols] tensor")
+    rows, cols = int(src.shape[0]), int(src.shape[1])
+    _check(lib.moe_quantize_fp8(rows, cols, _ptr(src, "src", torch.bfloat16, rows * cols),
+                                _ptr(dst, "dst", torch.uint8, rows * cols), _ptr(scale, "scale", torch.float32, rows),
+                                _stream(stream)))
+
+
+@dataclasses.dataclass
+class FP8Weights:
+    """The gate and up weights as E4M3 codes [E, d_e, h] with one scale per row [E * d_e]."""
+    W_gate8: torch.Tensor
+    W_up8: torch.Tensor
+    s_gate: torch.Tensor
+    s_up: torch.Tensor
+
+    @staticmethod
+    def quantize(W_gate: torch.Tensor, W_up: torch.Tensor, stream=None) -> "FP8Weights":
+        E, d, h = W_gate.shape
+        dev = W_gate.device
+        w = FP8Weights(torch.empty((E, d, h), dtype=torch.uint8, device=dev),
+                       torch.empty((E, d, h), dtype=torch.uint8, device=dev),
+                       torch.empty(E * d, dtype=torch.float32, device=dev),
+                       torch.empty(E * d, dtype=torch.float32, device=dev))
+        moe_quantize_fp8(W_gate.reshape(E * d, h), w.W_gate8, w.s_gate, stream)
+        moe_quantize_fp8(W_up.reshape(E * d, h), w.W_up8, w.s_up, stream)
+        return w
+
+
+@dataclasses.dataclass
+class FP8Rows:
+    """The dispatched token rows as E4M3 codes [T*k, h] with their scales [T*k]."""
+    X8: torch.Tensor
+    x_scale: torch.Tensor
+
+    @staticmethod
+    def allocate(cfg: moe_config, device="cuda") -> "FP8Rows":
+        return FP8Rows(torch.empty((cfg.T * cfg.k, cfg.h), dtype=torch.uint8, device=device),
+                       torch.empty(cfg.T * cfg.k, dtype=torch.float32, device=device))
+
+
+def moe_dispatch_fp8(cfg, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, X8, x_scale, n_dropped,
+                     ws, stream=None):
+    T, E, k, h = cfg.T, cfg.E, cfg.k, cfg.h
+    _check(lib.moe_dispatch_fp8(ctypes.byref(cfg), _ptr(U, "U", torch.bfloat16, T * h),
+                                _ptr(idx, "idx", torch.int32, T * k),
+                                _ptr(counts_routed, "counts_routed", torch.int32, E),
+                                _ptr(counts_kept, "counts_kept", torch.int32, E),
+                                _ptr(offsets, "offsets", torch.int32, E + 1),
+                                _ptr(slot_row, "slot_row", torch.int32, T * k),
+                                _ptr(row_token, "row_token", torch.int32, T * k),
+                                _ptr(X8, "X8", torch.uint8, T * k * h), _ptr(x_scale, "x_scale", torch.float32, T * k),
+                                _ptr(n_dropped, "n_dropped", torch.int64, 1), _ptr(ws, "ws"), _stream(stream)))
+
+
+def moe_expert_ffn_fp8(cfg, X8, x_scale, offsets, w8: FP8Weights, W_down, act, Y, ws, stream=None):
+    T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
+    _check(lib.moe_expert_ffn_fp8(ctypes.byref(cfg), _ptr(X8, "X8", torch.uint8, T * k * h),
+                                  _ptr(x_scale, "x_scale", torch.float32, T * k),
+                                  _ptr(offsets, "offsets", torch.int32, E + 1),
+                                  _ptr(w8.W_gate8, "W_gate8", torch.uint8, E * d * h),
+                                  _ptr(w8.W_up8, "W_up8", torch.uint8, E * d * h),
+                                  _ptr(w8.s_gate, "s_gate", torch.float32, E * d),
+                                  _ptr(w8.s_up, "s_up", torch.float32, E * d),
+                                  _ptr(W_down, "W_down", torch.bfloat16, E * h * d),
+                                  _ptr(act, "act", torch.bfloat16, T * k * d), _ptr(Y, "Y", torch.bfloat16, T * k * h),
+                                  _ptr(ws, "ws"), _stream(stream)))
+
+
+def moe_layer_forward_fp8(cfg, U, W_r, b_r, W_noise, eps, w8: FP8Weights, W_down, bufs: LayerBuffers, rows: FP8Rows,
+                          stream=None, sel_bias=None, shared=None):
+    """The whole layer with the FP8 dispatch and up-projection (bufs.X is not used)."""
+    a = layer_args(cfg, U, W_r, b_r, W_noise, eps, None, None, W_down, bufs, sel_bias, shared)
+    T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
+    f = moe_fp8_args(X8=_ptr(rows.X8, "X8", torch.uint8, T * k * h),
+                     x_scale=_ptr(rows.x_scale, "x_scale", torch.float32, T * k),
+                     W_gate8=_ptr(w8.W_gate8, "W_gate8", torch.uint8, E * d * h),
+                     W_up8=_ptr(w8.W_up8, "W_up8", torch.uint8, E * d * h),
+                     s_gate=_ptr(w8.s_gate, "s_gate", torch.float32, E * d),
+                     s_up=_ptr(w8.s_up, "s_up", torch.float32, E * d))
+    _check(lib.moe_layer_forward_fp8(ctypes.byref(cfg), ctypes.byref(a), ctypes.byref(f), _ptr(bufs.ws, "ws"),
+                                     _stream(stream)))
 
 
 @dataclasses.dataclass

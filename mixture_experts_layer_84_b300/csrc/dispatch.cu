@@ -267,6 +267,7 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
                                                                 offsets, p.C, slot_row, row_token);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (!X) return cudaSuccess;  // routing metadata only (the FP8 dispatch copies the rows itself)
   const int elem = p.bf16 ? 2 : 4;
   const int vpr = p.h * elem / 16;
   const int64_t want = (p.T + 7) / 8;

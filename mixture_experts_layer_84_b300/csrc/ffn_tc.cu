@@ -101,12 +101,18 @@ __device__ __forceinline__ void store_32(bf16* orow, int col0, int n_out, const 
 
 // SWIGLU: out[row, c] = SiLU(A W0^T)[row, c] * (A W1^T)[row, c], c < n_out (= d_e), W0/W1 rows per expert = d_e.
 // plain:  out[row, c] = (A W0^T)[row, c],                         c < n_out (= h),   W0 rows per expert = h.
-template <bool SWIGLU>
+// FP8 (SwiGLU only): A, W0, W1 are E4M3 codes (kind::f8f6f4, 128 K-elements per 128-byte stage row), and
+// each product is scaled back by a_scale[row] * b_scale[weight row] (powers of two) before SiLU * up.
+template <bool SWIGLU, bool FP8 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets, int E, int K,
-                    int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status) {
+                    int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status,
+                    const float* __restrict__ a_scale = nullptr, const float* __restrict__ b0_scale = nullptr,
+                    const float* __restrict__ b1_scale = nullptr) {
+  static_assert(SWIGLU || !FP8, "the FP8 path is the up-projection");
   constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
+  constexpr int BKE = FP8 ? 2 * BK : BK;        // K elements per stage (128 bytes of every row)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = (n_out + TILE_N - 1) / TILE_N;
-  const int KB = (K + BK - 1) / BK;
+  const int KB = (K + BKE - 1) / BKE;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -191,12 +197,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           uint8_t* sa = stages + stage * STAGE_BYTES;
           ptx::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          ptx::tma_load_2d(sa, &tmA, kb * BK, a_row, &full[stage], pol_a);
+          ptx::tma_load_2d(sa, &tmA, kb * BKE, a_row, &full[stage], pol_a);
           if (SWIGLU) {
-            ptx::tma_load_2d(sa + A_BYTES, &tmB0, kb * BK, b_row, &full[stage], pol_b);
-            ptx::tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB1, kb * BK, b_row, &full[stage], pol_b);
+            ptx::tma_load_2d(sa + A_BYTES, &tmB0, kb * BKE, b_row, &full[stage], pol_b);
+            ptx::tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB1, kb * BKE, b_row, &full[stage], pol_b);
           } else {
-            ptx::tma_load_2d(sa + A_BYTES, &tmB0, kb * BK, b_row, &full[stage], pol_b);
+            ptx::tma_load_2d(sa + A_BYTES, &tmB0, kb * BKE, b_row, &full[stage], pol_b);
           }
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+      constexpr uint32_t IDESC = FP8 ? ptx::idesc_e4m3_f32(BM, BN) : ptx::idesc_bf16_f32(BM, BN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -231,10 +237,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_u32(stages + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
+          // 32 bytes of K per MMA: 16 bf16 (kind::f16) or 32 E4M3 (kind::f8f6f4)
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
-            ptx::mma_bf16_ss(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * UK * 2), ptx::sdesc_kmajor_sw128(sb + kk * UK * 2),
-                             IDESC, (kb | kk) != 0 ? 1u : 0u);
+            if (FP8)
+              ptx::mma_f8_ss(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32), ptx::sdesc_kmajor_sw128(sb + kk * 32), IDESC,
+                             (kb | kk) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16_ss(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32), ptx::sdesc_kmajor_sw128(sb + kk * 32),
+                               IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit(&empty[stage]);  // stage is free once these MMAs have read it
           if (++stage == STAGES) {
@@ -269,17 +280,32 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tb = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
       bf16* orow = out + row * n_out;
       if (SWIGLU) {
+        const float xs = (FP8 && row_ok) ? a_scale[row] : 1.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
           uint32_t gv[32], uv[32], packed[16];
           ptx::tmem_ld_32x32b_x32(tb + c, gv);
           ptx::tmem_ld_32x32b_x32(tb + BN / 2 + c, uv);
+          // FP8: lane i holds the scales of output column c + i (shared by every row)
+          float my_sg = 1.f, my_su = 1.f;
+          if (FP8) {
+            const int col = nt * TILE_N + c + lane;
+            const int64_t wrow = static_cast<int64_t>(e) * b_rows_per_expert + col;
+            my_sg = col < n_out ? b0_scale[wrow] : 0.f;
+            my_su = col < n_out ? b1_scale[wrow] : 0.f;
+          }
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a0 = silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i]));
-            const float a1 = silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1]));
-            packed[i] = Vec16<bf16>::pack2(a0, a1);
+            float g0 = __uint_as_float(gv[2 * i]), u0 = __uint_as_float(uv[2 * i]);
+            float g1 = __uint_as_float(gv[2 * i + 1]), u1 = __uint_as_float(uv[2 * i + 1]);
+            if (FP8) {
+              g0 *= xs * __shfl_sync(0xffffffffu, my_sg, 2 * i);
+              u0 *= xs * __shfl_sync(0xffffffffu, my_su, 2 * i);
+              g1 *= xs * __shfl_sync(0xffffffffu, my_sg, 2 * i + 1);
+              u1 *= xs * __shfl_sync(0xffffffffu, my_su, 2 * i + 1);
+            }
+            packed[i] = Vec16<bf16>::pack2(silu_mul(g0, u0), silu_mul(g1, u1));
           }
           if (row_ok) store_32(orow, nt * TILE_N + c, n_out, packed);
         }
@@ -587,17 +613,19 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] read in boxes of box_rows x 64 with the 128-byte swizzle.
-static bool make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// Row-major matrix [rows, cols] of bf16 (or of bytes: E4M3 codes) read in boxes of box_rows x
+// 128 bytes with the 128-byte swizzle.
+static bool make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                      bool bytes = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint64_t strides[1] = {cols * (bytes ? 1 : 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(bytes ? 2 * BK : BK), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(tm, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tc
@@ -691,6 +719,44 @@ cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, 
   const int grid2 = per * static_cast<int>(std::min<int64_t>(units, tiles2));
   cudaError_t e = launch_gemm<true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
                                     static_cast<bf16*>(act), status, s);
+  if (e != cudaSuccess) return e;
+  return launch_gemm<false>(pair, grid2, tmAct, tmD, tmD, offsets, p.E, p.d_e, p.h, p.h, p.Tk, static_cast<bf16*>(Y),
+                            status, s);
+}
+
+// The FP8 up-projection (single-CTA kernel, kind::f8f6f4) followed by the usual bf16 down GEMM.
+cudaError_t launch_ffn_fp8_tc(const Plan& p, const uint8_t* X8, const float* x_scale, const int32_t* offsets,
+                              const uint8_t* W_gate8, const uint8_t* W_up8, const float* s_gate, const float* s_up,
+                              const void* W_down, void* act, void* Y, int32_t* status, cudaStream_t s) {
+  using namespace tc;
+  if (p.Tk == 0) return cudaSuccess;
+  const bool pair = use_pair_tiles(p);
+  const uint32_t a_box = pair ? 128 : BM;
+  const uint32_t down_box = pair ? BN / 2 : BN;
+  CUtensorMap tmX, tmG, tmU, tmAct, tmD;
+  const uint64_t Tk = static_cast<uint64_t>(p.Tk);
+  if (!make_tmap(&tmX, X8, Tk, p.h, BM, true) ||
+      !make_tmap(&tmG, W_gate8, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2, true) ||
+      !make_tmap(&tmU, W_up8, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2, true) ||
+      !make_tmap(&tmAct, act, Tk, p.d_e, a_box) ||
+      !make_tmap(&tmD, W_down, static_cast<uint64_t>(p.E) * p.h, p.d_e, down_box))
+    return cudaErrorNotSupported;
+  const int nsm = current_sm_count();
+  const int64_t mt1 = (p.Tk + BM - 1) / BM + p.E;
+  const int64_t tiles1 = mt1 * ((p.d_e + BN / 2 - 1) / (BN / 2));
+  const int rows_per_tile = pair ? P_BM : BM;
+  const int64_t tiles2 = ((p.Tk + rows_per_tile - 1) / rows_per_tile + p.E) * ((p.h + BN - 1) / BN);
+  if (tiles1 >= (int64_t(1) << 31) || tiles2 >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  const int grid1 = static_cast<int>(std::min<int64_t>(nsm, tiles1));
+  const int per = pair ? 2 : 1;
+  const int grid2 = per * static_cast<int>(std::min<int64_t>(pair ? nsm / 2 : nsm, tiles2));
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  grouped_gemm_tc<true, true><<<grid1, THREADS, SMEM_BYTES, s>>>(tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
+                                                                 static_cast<bf16*>(act), status, x_scale, s_gate,
+                                                                 s_up);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_gemm<false>(pair, grid2, tmAct, tmD, tmD, offsets, p.E, p.d_e, p.h, p.h, p.Tk, static_cast<bf16*>(Y),
                             status, s);

@@ -137,6 +137,12 @@ cudaError_t launch_balance_bias_update(int E, const int32_t* counts_routed, floa
 cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                           const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
                           cudaStream_t s);
+cudaError_t launch_ffn_fp8_tc(const Plan& p, const uint8_t* X8, const float* x_scale, const int32_t* offsets,
+                              const uint8_t* W_gate8, const uint8_t* W_up8, const float* s_gate, const float* s_up,
+                              const void* W_down, void* act, void* Y, int32_t* status, cudaStream_t s);
+cudaError_t launch_quantize_fp8(int64_t rows, int cols, const void* src, uint8_t* dst, float* scale, cudaStream_t s);
+cudaError_t launch_scatter_fp8(const Plan& p, const void* U, const int32_t* slot_row, uint8_t* X8, float* x_scale,
+                               cudaStream_t s);
 cudaError_t launch_ffn_simt_f32(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                                 const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
                                 cudaStream_t s);

@@ -718,6 +718,131 @@ MOE_API moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args
   return MOE_OK;
 }
 
+// ---- FP8 dispatch and up-projection ---------------------------------------------------------
+
+namespace moe {
+
+moe_status check_fp8(const char* fn, const Plan& p) {
+  if (!p.bf16) return fail(MOE_ERR_UNSUPPORTED, "%s: the FP8 path needs a bf16 config", fn);
+  if (p.h % 16 != 0) return fail(MOE_ERR_UNSUPPORTED, "%s: h = %d must be a multiple of 16", fn, p.h);
+  return MOE_OK;
+}
+
+moe_status check_fp8_rows(const char* fn, const Plan& p, const uint8_t* X8, const float* x_scale) {
+  CHECK(check_ptr(fn, "X8", X8, static_cast<size_t>(p.Tk) * p.h, 16));
+  CHECK(check_ptr(fn, "x_scale", x_scale, static_cast<size_t>(p.Tk) * 4, 4));
+  return MOE_OK;
+}
+
+moe_status check_fp8_weights(const char* fn, const Plan& p, const uint8_t* W_gate8, const uint8_t* W_up8,
+                             const float* s_gate, const float* s_up, const void* W_down) {
+  const size_t w = p.Tk > 0 ? static_cast<size_t>(p.E) * p.d_e * p.h : 0;
+  CHECK(check_ptr(fn, "W_gate8", W_gate8, w, 16));
+  CHECK(check_ptr(fn, "W_up8", W_up8, w, 16));
+  CHECK(check_ptr(fn, "s_gate", s_gate, p.Tk > 0 ? static_cast<size_t>(p.E) * p.d_e * 4 : 0, 4));
+  CHECK(check_ptr(fn, "s_up", s_up, p.Tk > 0 ? static_cast<size_t>(p.E) * p.d_e * 4 : 0, 4));
+  CHECK(check_ptr(fn, "W_down", W_down, w * 2, 16));
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+MOE_API moe_status moe_quantize_fp8(int64_t rows, int32_t cols, const void* src, uint8_t* dst, float* scale,
+                                    moe_stream_t stream) {
+  static const char* fn = "moe_quantize_fp8";
+  if (rows < 0 || cols < 1) return moe::fail(MOE_ERR_INVALID_ARG, "%s: rows = %lld, cols = %d", fn,
+                                             static_cast<long long>(rows), cols);
+  if (cols % 8 != 0) return moe::fail(MOE_ERR_UNSUPPORTED, "%s: cols = %d must be a multiple of 8", fn, cols);
+  if (rows >= (int64_t(1) << 40) / cols) return moe::fail(MOE_ERR_UNSUPPORTED, "%s: rows * cols too large", fn);
+  const size_t n = static_cast<size_t>(rows) * cols;
+  CHECK(moe::check_ptr(fn, "src", src, n * 2, 16));
+  CHECK(moe::check_ptr(fn, "dst", dst, n, 8));
+  CHECK(moe::check_ptr(fn, "scale", scale, static_cast<size_t>(rows) * 4, 4));
+  const cudaError_t e = moe::launch_quantize_fp8(rows, cols, src, dst, scale, stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_dispatch_fp8(const moe_config* cfg, const void* U, const int32_t* idx,
+                                    int32_t* counts_routed, int32_t* counts_kept, int32_t* offsets,
+                                    int32_t* slot_row, int32_t* row_token, uint8_t* X8, float* x_scale,
+                                    int64_t* n_dropped, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_dispatch_fp8";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  CHECK(moe::check_fp8(fn, p));
+  // X is replaced by X8: check the rest with U standing in for it
+  CHECK(moe::check_dispatch_args(fn, p, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, U,
+                                 n_dropped, ws));
+  CHECK(moe::check_fp8_rows(fn, p, X8, x_scale));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  cudaError_t e = moe::launch_dispatch(p, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, nullptr,
+                                       n_dropped, w, stream);
+  if (e == cudaSuccess) e = moe::launch_scatter_fp8(p, U, slot_row, X8, x_scale, stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_expert_ffn_fp8(const moe_config* cfg, const uint8_t* X8, const float* x_scale,
+                                      const int32_t* offsets, const uint8_t* W_gate8, const uint8_t* W_up8,
+                                      const float* s_gate, const float* s_up, const void* W_down, void* act, void* Y,
+                                      void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_expert_ffn_fp8";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  CHECK(moe::check_fp8(fn, p));
+  CHECK(moe::check_fp8_rows(fn, p, X8, x_scale));
+  CHECK(moe::check_fp8_weights(fn, p, W_gate8, W_up8, s_gate, s_up, W_down));
+  CHECK(moe::check_ptr(fn, "offsets", offsets, static_cast<size_t>(p.E + 1) * 4, 4));
+  CHECK(moe::check_ptr(fn, "act", act, static_cast<size_t>(p.Tk) * p.d_e * 2, 16));
+  CHECK(moe::check_ptr(fn, "Y", Y, static_cast<size_t>(p.Tk) * p.h * 2, 16));
+  CHECK(moe::check_ptr(fn, "ws", ws, p.ws_total, 256));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const cudaError_t e = moe::launch_ffn_fp8_tc(p, X8, x_scale, offsets, W_gate8, W_up8, s_gate, s_up, W_down, act,
+                                               Y, moe::ws_status(p, w), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_layer_forward_fp8(const moe_config* cfg, const moe_layer_args* a, const moe_fp8_args* f8,
+                                         void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_layer_forward_fp8";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  CHECK(moe::check_fp8(fn, p));
+  if (!a || !f8) return moe::fail(MOE_ERR_INVALID_ARG, "%s: args or fp8 args is NULL", fn);
+  CHECK(moe::check_route_args(fn, p, a->U, a->W_r, a->W_noise, a->eps, nullptr, a->logits_out, a->idx, a->gate, ws));
+  CHECK(moe::check_ptr(fn, "b_r", a->b_r, 0, 4));
+  CHECK(moe::check_dispatch_args(fn, p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row,
+                                 a->row_token, a->U, a->n_dropped, ws));
+  CHECK(moe::check_fp8_rows(fn, p, f8->X8, f8->x_scale));
+  CHECK(moe::check_fp8_weights(fn, p, f8->W_gate8, f8->W_up8, f8->s_gate, f8->s_up, a->W_down));
+  CHECK(moe::check_ptr(fn, "act", a->act, static_cast<size_t>(p.Tk) * p.d_e * 2, 16));
+  CHECK(moe::check_combine_args(fn, p, a->U, a->Y, a->slot_row, a->gate, a->counts_routed, a->out, a->f, a->P,
+                                a->aux, ws));
+  CHECK(moe::check_ptr(fn, "z_loss", a->z_loss, 0, 4));
+  CHECK(moe::check_ptr(fn, "sel_bias", a->sel_bias, 0, 4));
+  CHECK(moe::check_shared_args(fn, p, a->U, a->W_gate_shared, a->W_up_shared, a->W_down_shared, a->act_shared,
+                               a->Y_shared));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  cudaError_t e = moe::launch_route(p, a->U, a->W_r, a->b_r, a->sel_bias, a->W_noise, a->eps, nullptr, a->logits_out,
+                                    a->idx, a->gate, w, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward_fp8/route", e);
+  e = moe::launch_dispatch(p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row, a->row_token,
+                           nullptr, a->n_dropped, w, stream);
+  if (e == cudaSuccess) e = moe::launch_scatter_fp8(p, a->U, a->slot_row, f8->X8, f8->x_scale, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward_fp8/dispatch", e);
+  e = moe::launch_ffn_fp8_tc(p, f8->X8, f8->x_scale, a->offsets, f8->W_gate8, f8->W_up8, f8->s_gate, f8->s_up,
+                             a->W_down, a->act, a->Y, moe::ws_status(p, w), stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward_fp8/expert_ffn", e);
+  if (p.n_shared > 0) {
+    e = moe::launch_shared_ffn(p, a->U, a->W_gate_shared, a->W_up_shared, a->W_down_shared, a->act_shared,
+                               a->Y_shared, w, stream);
+    if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward_fp8/shared_ffn", e);
+  }
+  e = moe::launch_combine(p, a->U, a->Y, p.n_shared > 0 ? a->Y_shared : nullptr, a->slot_row, a->gate,
+                          a->counts_routed, a->out, a->f, a->P, a->aux, a->z_loss, w, stream);
+  if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward_fp8/combine", e);
+  return MOE_OK;
+}
+
 MOE_API moe_status moe_get_device_status(void* ws, moe_stream_t stream, int32_t* code) {
   static const char* fn = "moe_get_device_status";
   if (!ws || !moe::aligned(ws, 256)) return moe::fail(MOE_ERR_INVALID_ARG, "%s: ws is NULL or misaligned", fn);

@@ -118,6 +118,19 @@ def test_group_limited_configs_accepted():
         assert L.lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == L.MOE_OK, kw
 
 
+def test_fp8_entry_points_reject_unsupported_configs_before_any_launch():
+    assert ctypes.sizeof(L.moe_fp8_args) == 6 * 8
+    for cfg, msg in ((L.config(64, 136, 8, 2, 64), "multiple of 16"),
+                     (L.config(64, 128, 8, 2, 64, dtype=W.F32), "bf16")):
+        assert L.lib.moe_dispatch_fp8(ctypes.byref(cfg), *([None] * 12)) == L.MOE_ERR_UNSUPPORTED
+        assert msg in L.lib.moe_last_error().decode()
+        assert L.lib.moe_expert_ffn_fp8(ctypes.byref(cfg), *([None] * 12)) == L.MOE_ERR_UNSUPPORTED
+        assert L.lib.moe_layer_forward_fp8(ctypes.byref(cfg), None, None, None, None) == L.MOE_ERR_UNSUPPORTED
+    assert L.lib.moe_quantize_fp8(4, 12, None, None, None, None) == L.MOE_ERR_UNSUPPORTED
+    assert L.lib.moe_quantize_fp8(4, 16, None, None, None, None) == L.MOE_ERR_INVALID_ARG  # NULL src
+    assert L.lib.moe_quantize_fp8(-1, 16, None, None, None, None) == L.MOE_ERR_INVALID_ARG
+
+
 def test_null_pointers_rejected_before_any_launch():
     cfg = L.config(64, 64, 8, 2, 64, capacity_factor=1.0)
     st = L.lib.moe_route(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, None, None, None)
