@@ -175,7 +175,8 @@ moe_status moe_balance_bias_update(const moe_config* cfg, const int32_t* counts_
  *                                     in slot (priority) order; only the first A rows written
  *   n_dropped [1] int64 out           T*k - A
  * All of it is integer work and bit-exact: the n-th pair (in cfg->priority
- * order) that chose expert e takes slot n and is kept iff n < C. */
+ * order) that chose expert e takes slot n and is kept iff n < C.
+ * X may be NULL: then only the routing metadata is written (for moe_expert_ffn_gather). */
 moe_status moe_dispatch(const moe_config* cfg, const void* U, const int32_t* idx,
                         int32_t* counts_routed, int32_t* counts_kept, int32_t* offsets,
                         int32_t* slot_row, int32_t* row_token, void* X, int64_t* n_dropped,
@@ -233,6 +234,19 @@ moe_status moe_dispatch_noalloc(const moe_config* cfg, const void* U, const int3
 moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const int32_t* offsets,
                           const void* W_gate, const void* W_up, const void* W_down,
                           void* act, void* Y, void* ws, moe_stream_t stream);
+
+/* moe_expert_ffn with the dispatch's row copy fused into the first GEMM (bf16 configs; section
+ * 专家计算：padding、block-sparse 与 grouped GEMM, and the permute of the shapes listing):
+ *   U        [T, h] bf16               token rows
+ *   row_token [T*k] int32              from moe_dispatch: row r of the expert input is U[row_token[r]]
+ *                                      (ids outside [0, T) read row 0 and set MOE_DEV_BAD_ROW)
+ *   offsets, W_gate, W_up, W_down, act, Y   as in moe_expert_ffn
+ * No X is read or written: the first GEMM's producer copies each 128 x 64 A tile straight from
+ * the token rows of U (16-byte cp.async into the swizzled layout of a TMA tile).  act and Y are
+ * bit-identical to moe_expert_ffn on X[r] = U[row_token[r]]. */
+moe_status moe_expert_ffn_gather(const moe_config* cfg, const void* U, const int32_t* row_token,
+                                 const int32_t* offsets, const void* W_gate, const void* W_up,
+                                 const void* W_down, void* act, void* Y, void* ws, moe_stream_t stream);
 
 /* Shared experts (section 细粒度专家与共享专家, the shared-expert isolation of
  * DeepSeekMoE / V3): cfg->n_shared SwiGLU experts that every token passes
@@ -354,7 +368,9 @@ typedef struct moe_layer_args {
 } moe_layer_args;
 
 /* The whole layer: moe_route, moe_dispatch, moe_expert_ffn, (moe_shared_ffn,)
- * moe_combine in order on `stream`, with no host synchronisation in between. */
+ * moe_combine in order on `stream`, with no host synchronisation in between.
+ * args->X == NULL (bf16 configs): the dispatch copies no rows and the expert FFN runs as
+ * moe_expert_ffn_gather, reading the token rows of U directly (the results are identical). */
 moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args* args, void* ws,
                              moe_stream_t stream);
 

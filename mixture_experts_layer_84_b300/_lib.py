@@ -27,7 +27,7 @@ EXPORTS = ("moe_version", "moe_status_string", "moe_last_error", "moe_capacity",
            "moe_shared_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status", "moe_combine_backward",
            "moe_route_backward", "moe_expert_ffn_backward", "moe_dispatch_backward", "moe_router_input_backward",
            "moe_layer_backward", "moe_quantize_fp8", "moe_dispatch_fp8", "moe_expert_ffn_fp8",
-           "moe_layer_forward_fp8")
+           "moe_layer_forward_fp8", "moe_expert_ffn_gather")
 
 
 class MoeError(RuntimeError):
@@ -109,6 +109,8 @@ def _load() -> ctypes.CDLL:
     lib.moe_layer_backward.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), ctypes.POINTER(moe_layer_grads), _P, _P]
     lib.moe_layer_forward.restype = S
     lib.moe_layer_forward.argtypes = [cfgp, ctypes.POINTER(moe_layer_args), _P, _P]
+    lib.moe_expert_ffn_gather.restype = S
+    lib.moe_expert_ffn_gather.argtypes = [cfgp] + [_P] * 8 + [_P, _P]
     lib.moe_quantize_fp8.restype = S
     lib.moe_quantize_fp8.argtypes = [I64, ctypes.c_int32, _P, _P, _P, _P]
     lib.moe_dispatch_fp8.restype = S
@@ -405,6 +407,18 @@ def layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: Layer
         act_shared=_ptr(bufs.act_shared, "act_shared", dt, ns * T * ds) if ns else None,
         Y_shared=_ptr(bufs.Y_shared, "Y_shared", dt, ns * T * h) if ns else None)
     return a
+
+
+def moe_expert_ffn_gather(cfg, U, row_token, offsets, W_gate, W_up, W_down, act, Y, ws, stream=None):
+    """moe_expert_ffn on X[r] = U[row_token[r]] without materialising X (bf16)."""
+    T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
+    bf = torch.bfloat16
+    _check(lib.moe_expert_ffn_gather(ctypes.byref(cfg), _ptr(U, "U", bf, T * h),
+                                     _ptr(row_token, "row_token", torch.int32, T * k),
+                                     _ptr(offsets, "offsets", torch.int32, E + 1),
+                                     _ptr(W_gate, "W_gate", bf, E * d * h), _ptr(W_up, "W_up", bf, E * d * h),
+                                     _ptr(W_down, "W_down", bf, E * h * d), _ptr(act, "act", bf, T * k * d),
+                                     _ptr(Y, "Y", bf, T * k * h), _ptr(ws, "ws"), _stream(stream)))
 
 
 # ---- FP8 dispatch and up-projection ----------------------------------------------------------

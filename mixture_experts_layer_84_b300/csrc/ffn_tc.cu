@@ -99,18 +99,69 @@ __device__ __forceinline__ void store_32(bf16* orow, int col0, int n_out, const 
   }
 }
 
+// ---- gathered A operand (the dispatch's row copy fused into the first GEMM) -------------------
+// Row r of the A operand is row gtok[r] of gsrc ([gsrc_rows, K] bf16).  The producer warp copies
+// it with 16-byte cp.async into the 128-byte-swizzled layout a tiled TMA load writes (16-byte
+// chunk c of tile row r lands at r * 128 + ((c ^ (r & 7)) << 4); stage bases are 1024-byte
+// aligned).  Lane L copies chunk L % 8 of tile rows L / 8 + 4 j, j < 32: each warp-wide copy
+// reads four whole 128-byte row segments.  Copies are waited for GATHER_LAG stages behind the
+// newest, then fenced into the async proxy (the tensor cores read shared memory through it) and
+// announced on the stage's full barrier.
+constexpr int GATHER_LAG = 2;
+static_assert(GATHER_LAG < STAGES, "a stage is announced before its slot is needed again");
+
+struct Gather {
+  const bf16* src;     // [rows, K]
+  const int32_t* tok;  // source row of every A row
+  int64_t rows;        // rows of src
+};
+
+// the source rows of this lane's 32 tile rows (rows past the kept rows, or ids out of range, read row 0)
+__device__ __forceinline__ void gather_tokens(const Gather& g, int64_t first_row, int64_t a_total, int lane,
+                                              int32_t (&tok)[32], int32_t* status) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int64_t r = first_row + (lane >> 3) + 4 * j;
+    int32_t t = 0;
+    if (r < a_total) {
+      t = g.tok[r];
+      if (t < 0 || t >= g.rows) {
+        set_status(status, MOE_DEV_BAD_ROW);
+        t = 0;
+      }
+    }
+    tok[j] = t;
+  }
+}
+
+// one 128-row x 64-column stage of the gathered A operand (columns >= K are zero-filled)
+__device__ __forceinline__ void gather_stage(uint8_t* sa, const bf16* src, int K, const int32_t (&tok)[32], int kb,
+                                             int lane) {
+  const int c = lane & 7;
+  const int col = kb * BK + c * 8;
+  const bool in = col < K;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int r = (lane >> 3) + 4 * j;
+    const bf16* gp = src + static_cast<int64_t>(tok[j]) * K + (in ? col : 0);
+    ptx::cp_async_16(sa + r * 128 + ((c ^ (r & 7)) << 4), gp, in ? 16u : 0u);
+  }
+}
+
 // SWIGLU: out[row, c] = SiLU(A W0^T)[row, c] * (A W1^T)[row, c], c < n_out (= d_e), W0/W1 rows per expert = d_e.
 // plain:  out[row, c] = (A W0^T)[row, c],                         c < n_out (= h),   W0 rows per expert = h.
 // FP8 (SwiGLU only): A, W0, W1 are E4M3 codes (kind::f8f6f4, 128 K-elements per 128-byte stage row), and
 // each product is scaled back by a_scale[row] * b_scale[weight row] (powers of two) before SiLU * up.
-template <bool SWIGLU, bool FP8 = false>
+// GATHER (SwiGLU, bf16): the A operand is gathered from g (the dispatch's row copy fused in).
+template <bool SWIGLU, bool FP8 = false, bool GATHER = false>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets, int E, int K,
                     int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status,
                     const float* __restrict__ a_scale = nullptr, const float* __restrict__ b0_scale = nullptr,
-                    const float* __restrict__ b1_scale = nullptr) {
+                    const float* __restrict__ b1_scale = nullptr, Gather g = Gather{}) {
   static_assert(SWIGLU || !FP8, "the FP8 path is the up-projection");
+  static_assert(!(GATHER && (FP8 || !SWIGLU)), "the gathered A operand is the bf16 up-projection's");
   constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
   constexpr int BKE = FP8 ? 2 * BK : BK;        // K elements per stage (128 bytes of every row)
   extern __shared__ uint8_t smem_raw[];
@@ -151,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int e = 0; e < E; ++e) tab[e + 1] += tab[e];
     if (*bad_flag && blockIdx.x == 0) set_status(status, MOE_DEV_BAD_OFFSETS);
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&full[s], GATHER ? 2 : 1);  // (gather: + the producer warp's A copies)
       ptx::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -176,7 +227,59 @@ __global__ void __launch_bounds__(THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  if (warp == 0) {
+  if (GATHER && warp == 0) {
+    // the whole warp copies A; lane 0 also issues the B loads
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmB0);
+      ptx::prefetch_tmap(&tmB1);
+    }
+    const uint64_t pol_b = ptx::policy_evict_normal();
+    const int64_t a_total = seg_hi(offsets, E - 1, rows_cap);
+    uint32_t it = 0, armed = 0, armed_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      int e, nt, mt;
+      decode_tile(tab, E, NT, tile, &e, &nt, &mt);
+      int32_t tok[32];
+      gather_tokens(g, static_cast<int64_t>(seg_lo(offsets, e)) + mt * BM, a_total, lane, tok, status);
+      const int b_row = e * b_rows_per_expert + nt * TILE_N;
+      for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
+        const bool got = ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = stages + stage * STAGE_BYTES;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&full[stage], B_BYTES);
+          ptx::tma_load_2d(sa + A_BYTES, &tmB0, kb * BK, b_row, &full[stage], pol_b);
+          ptx::tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB1, kb * BK, b_row, &full[stage], pol_b);
+        }
+        gather_stage(sa, g.src, K, tok, kb, lane);
+        ptx::cp_async_commit();
+        armed |= 1u << stage;
+        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+        ++it;
+        if (it > GATHER_LAG) {  // the copies of iteration it - 1 - GATHER_LAG have landed: announce them
+          ptx::cp_async_wait<GATHER_LAG>();
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&full[(it - 1 - GATHER_LAG) % STAGES]);
+        }
+      }
+    }
+    // announce the last stages, then (lane 0) wait until every copy of this CTA has landed
+    ptx::cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      for (uint32_t i = it > GATHER_LAG ? it - GATHER_LAG : 0; i < it; ++i) ptx::mbar_arrive(&full[i % STAGES]);
+      for (int s = 0; s < STAGES; ++s)
+        if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_phase >> s) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     if (lane == 0) {
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB0);
@@ -374,12 +477,15 @@ __device__ __forceinline__ bool wait_cluster_bounded(uint64_t* bar, uint32_t par
   }
 }
 
-template <bool SWIGLU>
+// GATHER (SwiGLU): each CTA gathers its 128 A rows from g; the even CTA's full barrier then also
+// counts one announcement from each CTA's producer warp.
+template <bool SWIGLU, bool GATHER = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     grouped_gemm_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                          const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets, int E, int K,
                          int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out,
-                         int32_t* status) {
+                         int32_t* status, Gather g = Gather{}) {
+  static_assert(SWIGLU || !GATHER, "the gathered A operand is the up-projection's");
   constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -423,7 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int e = 0; e < E; ++e) tab[e + 1] += tab[e];
     if (*bad_flag && blockIdx.x == 0) set_status(status, MOE_DEV_BAD_OFFSETS);
     for (int s = 0; s < P_STAGES; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&full[s], GATHER ? 3 : 1);  // (gather: + both CTAs' A copies)
       ptx::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -449,7 +555,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  if (warp == 0) {
+  if (GATHER && warp == 0) {
+    const CUtensorMap* tmB = even ? &tmB0 : &tmB1;
+    if (lane == 0) ptx::prefetch_tmap(tmB);
+    const uint64_t pol_b = ptx::policy_evict_normal();
+    const int64_t a_total = seg_hi(offsets, E - 1, rows_cap);
+    uint32_t it = 0, armed = 0, armed_phase = 0;
+    bool ok = true;
+    for (int tile = cid; ok && tile < total; tile += ncl) {
+      int e, nt, mt;
+      decode_tile(tab, E, NT, tile, &e, &nt, &mt);
+      int32_t tok[32];
+      gather_tokens(g, static_cast<int64_t>(seg_lo(offsets, e)) + mt * P_BM + static_cast<int>(rank) * 128, a_total,
+                    lane, tok, status);
+      const int b_row = e * b_rows_per_expert + nt * TILE_N;
+      for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t stage = it % P_STAGES, phase = (it / P_STAGES) & 1u;
+        const bool got = ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = stages + stage * P_STAGE_BYTES;
+        if (lane == 0) {
+          const uint32_t full_pair = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
+          if (even) ptx::mbar_arrive_expect_tx(&full[stage], 2 * P_B_BYTES);
+          ptx::tma_load_2d_pair(sa + P_A_BYTES, tmB, kb * BK, b_row, full_pair, pol_b);
+        }
+        gather_stage(sa, g.src, K, tok, kb, lane);
+        ptx::cp_async_commit();
+        armed |= 1u << stage;
+        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+        ++it;
+        if (it > GATHER_LAG) {  // announce the copies of iteration it - 1 - GATHER_LAG to the even CTA
+          ptx::cp_async_wait<GATHER_LAG>();
+          asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+          __syncwarp();
+          if (lane == 0)
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&full[(it - 1 - GATHER_LAG) % P_STAGES]), 0));
+        }
+      }
+    }
+    ptx::cp_async_wait<0>();
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      for (uint32_t i = it > GATHER_LAG ? it - GATHER_LAG : 0; i < it; ++i)
+        ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&full[i % P_STAGES]), 0));
+      if (even) {
+        for (int s = 0; s < P_STAGES; ++s)
+          if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_phase >> s) & 1u);
+      }
+      if (*abort_flag) {
+        // B copies whose completion is counted in the other CTA cannot be awaited here: give them time
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     if (lane == 0) {
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB0);
@@ -643,13 +808,14 @@ static bool use_pair_tiles(const Plan& p) {
   return p.Tk >= static_cast<int64_t>(1024) * p.E;  // mean rows per expert >= 1024
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool GATHER = false>
 static cudaError_t launch_gemm(bool pair, int grid, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                                const int32_t* offsets, int E, int K, int b_rows, int n_out, int64_t rows_cap, bf16* out,
-                               int32_t* status, cudaStream_t s) {
+                               int32_t* status, cudaStream_t s, tc::Gather g = tc::Gather{}) {
   using namespace tc;
   if (pair) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_pair<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = grouped_gemm_tc_pair<SWIGLU, GATHER>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(P_SMEM_BYTES));
     if (e != cudaSuccess) return e;
     // no more clusters than can be resident at once (SMs that cannot be paired stay idle)
@@ -659,18 +825,18 @@ static cudaError_t launch_gemm(bool pair, int grid, const CUtensorMap& a, const 
     lc.dynamicSmemBytes = P_SMEM_BYTES;
     lc.stream = s;
     int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_tc_pair<SWIGLU>, &lc) == cudaSuccess &&
-        max_clusters > 0 && 2 * max_clusters < grid)
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &lc) == cudaSuccess && max_clusters > 0 &&
+        2 * max_clusters < grid)
       grid = 2 * max_clusters;
     (void)cudaGetLastError();
-    grouped_gemm_tc_pair<SWIGLU><<<grid, THREADS, P_SMEM_BYTES, s>>>(a, b0, b1, offsets, E, K, b_rows, n_out, rows_cap,
-                                                                      out, status);
+    kern<<<grid, THREADS, P_SMEM_BYTES, s>>>(a, b0, b1, offsets, E, K, b_rows, n_out, rows_cap, out, status, g);
   } else {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = grouped_gemm_tc<SWIGLU, false, GATHER>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    grouped_gemm_tc<SWIGLU><<<grid, THREADS, SMEM_BYTES, s>>>(a, b0, b1, offsets, E, K, b_rows, n_out, rows_cap, out,
-                                                              status);
+    kern<<<grid, THREADS, SMEM_BYTES, s>>>(a, b0, b1, offsets, E, K, b_rows, n_out, rows_cap, out, status, nullptr,
+                                           nullptr, nullptr, g);
   }
   return cudaGetLastError();
 }
@@ -692,15 +858,16 @@ cudaError_t launch_dense_gemm_tc(const void* A, int64_t rows, int K, const void*
 
 cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                           const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
-                          cudaStream_t s) {
+                          cudaStream_t s, const void* gather_src, const int32_t* gather_rows) {
   using namespace tc;
   if (p.Tk == 0) return cudaSuccess;
   const bool pair = use_pair_tiles(p);
+  const bool gather = gather_rows != nullptr;  // X[row] = gather_src[gather_rows[row]], read by GEMM1 itself
   const uint32_t a_box = pair ? 128 : BM;           // rows of A each CTA stages
   const uint32_t down_box = pair ? BN / 2 : BN;     // rows of W_down each CTA stages
   CUtensorMap tmX, tmG, tmU, tmAct, tmD;
   const uint64_t Tk = static_cast<uint64_t>(p.Tk);
-  if (!make_tmap(&tmX, X, Tk, p.h, a_box) ||
+  if (!make_tmap(&tmX, gather ? gather_src : X, gather ? static_cast<uint64_t>(p.T) : Tk, p.h, a_box) ||
       !make_tmap(&tmG, W_gate, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2) ||
       !make_tmap(&tmU, W_up, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2) ||
       !make_tmap(&tmAct, act, Tk, p.d_e, a_box) ||
@@ -717,8 +884,12 @@ cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, 
   const int per = pair ? 2 : 1;
   const int grid1 = per * static_cast<int>(std::min<int64_t>(units, tiles1));
   const int grid2 = per * static_cast<int>(std::min<int64_t>(units, tiles2));
-  cudaError_t e = launch_gemm<true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
-                                    static_cast<bf16*>(act), status, s);
+  cudaError_t e =
+      gather ? launch_gemm<true, true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
+                                       static_cast<bf16*>(act), status, s,
+                                       Gather{static_cast<const bf16*>(gather_src), gather_rows, p.T})
+             : launch_gemm<true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
+                                 static_cast<bf16*>(act), status, s);
   if (e != cudaSuccess) return e;
   return launch_gemm<false>(pair, grid2, tmAct, tmD, tmD, offsets, p.E, p.d_e, p.h, p.h, p.Tk, static_cast<bf16*>(Y),
                             status, s);

@@ -134,9 +134,11 @@ cudaError_t launch_balance_bias_update(int E, const int32_t* counts_routed, floa
 
 // Grouped bf16 GEMMs on tcgen05 (both FFN halves); returns cudaErrorNotSupported when the
 // tensor maps cannot be built.
+// gather_rows != NULL: X is not read; the first GEMM gathers row r of its A operand from
+// gather_src[gather_rows[r]] ([T, h], the dispatch's row copy fused in).
 cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
                           const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
-                          cudaStream_t s);
+                          cudaStream_t s, const void* gather_src = nullptr, const int32_t* gather_rows = nullptr);
 cudaError_t launch_ffn_fp8_tc(const Plan& p, const uint8_t* X8, const float* x_scale, const int32_t* offsets,
                               const uint8_t* W_gate8, const uint8_t* W_up8, const float* s_gate, const float* s_up,
                               const void* W_down, void* act, void* Y, int32_t* status, cudaStream_t s);

@@ -395,8 +395,10 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const void* U, const int3
   static const char* fn = "moe_dispatch";
   Plan p;
   CHECK(moe::plan_or_fail(fn, cfg, &p));
-  CHECK(moe::check_dispatch_args(fn, p, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, X,
+  // X may be NULL (routing metadata only): U stands in for it in the pointer checks
+  CHECK(moe::check_dispatch_args(fn, p, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, X ? X : U,
                                  n_dropped, ws));
+  CHECK(moe::check_ptr(fn, "X", X, 0, 16));
   const cudaError_t e = moe::launch_dispatch(p, U, idx, counts_routed, counts_kept, offsets, slot_row, row_token, X,
                                              n_dropped, static_cast<uint8_t*>(ws), stream);
   return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
@@ -439,6 +441,22 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const in
   CHECK(moe::check_ffn_args(fn, p, X, offsets, W_gate, W_up, W_down, act, Y, ws));
   const cudaError_t e = moe::launch_expert_ffn(p, X, offsets, W_gate, W_up, W_down, act, Y,
                                                static_cast<uint8_t*>(ws), stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_expert_ffn_gather(const moe_config* cfg, const void* U, const int32_t* row_token,
+                                         const int32_t* offsets, const void* W_gate, const void* W_up,
+                                         const void* W_down, void* act, void* Y, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_expert_ffn_gather";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (!p.bf16) return moe::fail(MOE_ERR_UNSUPPORTED, "%s: the gathered up-projection needs a bf16 config", fn);
+  // U stands in for X in the shared checks; row_token is read for the first A = offsets[E] rows
+  CHECK(moe::check_ffn_args(fn, p, U, offsets, W_gate, W_up, W_down, act, Y, ws));
+  CHECK(moe::check_ptr(fn, "U", U, static_cast<size_t>(p.T) * p.h * 2, 16));
+  CHECK(moe::check_ptr(fn, "row_token", row_token, static_cast<size_t>(p.Tk) * 4, 4));
+  const cudaError_t e = moe::launch_ffn_tc(p, nullptr, offsets, W_gate, W_up, W_down, act, Y,
+                                           moe::ws_status(p, static_cast<uint8_t*>(ws)), stream, U, row_token);
   return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
 }
 
@@ -689,9 +707,14 @@ MOE_API moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args
   if (!a) return moe::fail(MOE_ERR_INVALID_ARG, "%s: args is NULL", fn);
   CHECK(moe::check_route_args(fn, p, a->U, a->W_r, a->W_noise, a->eps, nullptr, a->logits_out, a->idx, a->gate, ws));
   CHECK(moe::check_ptr(fn, "b_r", a->b_r, 0, 4));
+  // X == NULL: the dispatch writes no rows and the first GEMM gathers them from U (bf16)
+  const bool gather = a->X == nullptr;
+  if (gather && !p.bf16)
+    return moe::fail(MOE_ERR_UNSUPPORTED, "%s: X == NULL (gathered up-projection) needs a bf16 config", fn);
+  const void* X = gather ? a->U : a->X;  // U stands in for a missing X in the pointer checks
   CHECK(moe::check_dispatch_args(fn, p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row,
-                                 a->row_token, a->X, a->n_dropped, ws));
-  CHECK(moe::check_ffn_args(fn, p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, ws));
+                                 a->row_token, X, a->n_dropped, ws));
+  CHECK(moe::check_ffn_args(fn, p, X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, ws));
   CHECK(moe::check_combine_args(fn, p, a->U, a->Y, a->slot_row, a->gate, a->counts_routed, a->out, a->f, a->P,
                                 a->aux, ws));
   CHECK(moe::check_ptr(fn, "z_loss", a->z_loss, 0, 4));
@@ -705,7 +728,9 @@ MOE_API moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args
   e = moe::launch_dispatch(p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row, a->row_token,
                            a->X, a->n_dropped, w, stream);
   if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/dispatch", e);
-  e = moe::launch_expert_ffn(p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, w, stream);
+  e = gather ? moe::launch_ffn_tc(p, nullptr, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y,
+                                  moe::ws_status(p, w), stream, a->U, a->row_token)
+             : moe::launch_expert_ffn(p, a->X, a->offsets, a->W_gate, a->W_up, a->W_down, a->act, a->Y, w, stream);
   if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/expert_ffn", e);
   if (p.n_shared > 0) {
     e = moe::launch_shared_ffn(p, a->U, a->W_gate_shared, a->W_up_shared, a->W_down_shared, a->act_shared,
