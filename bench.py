@@ -334,7 +334,7 @@ def ffn_tiles(w: W.Workload) -> str:
     """The grouped-GEMM kernel libmoe picks: 256-row CTA-pair tiles when the mean expert segment is
     at least 1024 rows, else 128-row single-CTA tiles (MOE_FFN_TILES overrides)."""
     env = os.environ.get("MOE_FFN_TILES", "")
-    if env in ("single", "pair"):
+    if env in ("single", "pair", "swab"):
         return env + " (MOE_FFN_TILES)"
     if w.dtype == W.F32:
         return "cuda-core float32"

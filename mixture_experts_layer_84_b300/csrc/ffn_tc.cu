@@ -104,11 +104,10 @@ __device__ __forceinline__ void store_32(bf16* orow, int col0, int n_out, const 
 // it with 16-byte cp.async into the 128-byte-swizzled layout a tiled TMA load writes (16-byte
 // chunk c of tile row r lands at r * 128 + ((c ^ (r & 7)) << 4); stage bases are 1024-byte
 // aligned).  Lane L copies chunk L % 8 of tile rows L / 8 + 4 j, j < 32: each warp-wide copy
-// reads four whole 128-byte row segments.  Copies are waited for GATHER_LAG stages behind the
-// newest, then fenced into the async proxy (the tensor cores read shared memory through it) and
-// announced on the stage's full barrier.
-constexpr int GATHER_LAG = 2;
-static_assert(GATHER_LAG < STAGES, "a stage is announced before its slot is needed again");
+// reads four whole 128-byte row segments.  Copies are waited for (ring size - 1) stages behind
+// the newest, so that every slot but one is in flight, then fenced into the async proxy (the
+// tensor cores read shared memory through it) and announced on the stage's full barrier.
+constexpr int GATHER_LAG = STAGES - 1;  // single-CTA ring; the pair ring uses P_STAGES - 1
 
 struct Gather {
   const bf16* src;     // [rows, K]
@@ -556,6 +555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   if (GATHER && warp == 0) {
+    constexpr int P_GATHER_LAG = P_STAGES - 1;
     const CUtensorMap* tmB = even ? &tmB0 : &tmB1;
     if (lane == 0) ptx::prefetch_tmap(tmB);
     const uint64_t pol_b = ptx::policy_evict_normal();
@@ -587,12 +587,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
         ++it;
-        if (it > GATHER_LAG) {  // announce the copies of iteration it - 1 - GATHER_LAG to the even CTA
-          ptx::cp_async_wait<GATHER_LAG>();
+        if (it > P_GATHER_LAG) {  // announce the copies of iteration it - 1 - P_GATHER_LAG to the even CTA
+          ptx::cp_async_wait<P_GATHER_LAG>();
           asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
           __syncwarp();
           if (lane == 0)
-            ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&full[(it - 1 - GATHER_LAG) % P_STAGES]), 0));
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&full[(it - 1 - P_GATHER_LAG) % P_STAGES]), 0));
         }
       }
     }
@@ -600,7 +600,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
     __syncwarp();
     if (lane == 0) {
-      for (uint32_t i = it > GATHER_LAG ? it - GATHER_LAG : 0; i < it; ++i)
+      for (uint32_t i = it > P_GATHER_LAG ? it - P_GATHER_LAG : 0; i < it; ++i)
         ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&full[i % P_STAGES]), 0));
       if (even) {
         for (int s = 0; s < P_STAGES; ++s)
@@ -761,6 +761,299 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0 && *abort_flag) set_status(status, MOE_DEV_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// Weights as the M operand ("swapped" grouped GEMM on CTA pairs): D^T = W X^T.
+//
+// A 256-row tile of weight rows (128 per CTA) times up to 256 token rows of one
+// expert segment, with the token count N of the last tile of a segment rounded up
+// to 16 only.  Row tiles of 128 or 256 tokens waste up to a whole tile per expert
+// (11% of the MMA work of a 512-row segment split 4+1, 20% with 256-row pairs);
+// with tokens on the N side the waste is under 16 rows per expert, and the CTA
+// pair keeps the stage at 32 KB per CTA.
+//   A (this CTA)  SwiGLU: 64 W_gate rows then the same 64 W_up rows (output
+//                 columns j_base .. j_base + 63, j_base = 128 mt + 64 rank);
+//                 plain: 128 W rows (output columns 256 mt + 128 rank + lane quarter).
+//   B (this CTA)  token rows seg + 256 nt + rank N/2 .. +N/2 (a 128-row box: the
+//                 MMA reads the first N/2 rows of each CTA's B).
+//   TMEM lane i of a CTA = its weight row i, column t = token t of the tile.
+// SwiGLU epilogue: warps of lane quarters 0/1 hold gate, 2/3 the matching up
+// rows.  Per 32-token chunk the two warps of a pair swap halves through shared
+// memory (gate of tokens 16..31 one way, up of tokens 0..15 the other), then each
+// forms SiLU(g) * u for 16 tokens.  Stores: lane = output column, so each warp
+// store writes 32 consecutive columns (64 bytes) of one token row.
+constexpr int S_BN = 256;                                  // tokens per tile at most
+constexpr int S_STAGES = 6;
+constexpr uint32_t S_A_BYTES = 128 * BK * 2;              // 16 KB of weight rows
+constexpr uint32_t S_B_BYTES = 128 * BK * 2;              // 16 KB box of token rows
+constexpr uint32_t S_STAGE_BYTES = S_A_BYTES + S_B_BYTES;
+constexpr uint32_t S_XCH_FLOATS = 2 * 2 * 16 * 32;        // 2 warp pairs x 2 directions x [16][32]
+constexpr size_t S_SMEM_BYTES =
+    1024 + S_STAGES * S_STAGE_BYTES + S_XCH_FLOATS * 4 + P_BAR_BYTES + sizeof(int) * (MAX_E + 1);
+static_assert(S_SMEM_BYTES <= 232448, "shared memory");
+static_assert((2 * S_STAGES + 2 + 2 + 1) * 8 + 12 <= P_BAR_BYTES, "barriers fit P_BAR_BYTES");
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+// AND of `pred` over the `threads` threads of named barrier `id` (every one of them gets it)
+__device__ __forceinline__ bool named_all(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// SWIGLU: out[row, j] = SiLU((X W0^T)[row, j]) * (X W1^T)[row, j], j < n_out (= d_e), W0/W1 rows per expert = d_e.
+// plain:  out[row, m] = (X W0^T)[row, m],                           m < n_out (= h),   W0 rows per expert = h.
+template <bool SWIGLU>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    grouped_gemm_swab(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
+                      const __grid_constant__ CUtensorMap tmX, const int32_t* __restrict__ offsets, int E, int K,
+                      int w_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status) {
+  constexpr int WT = SWIGLU ? 128 : 256;  // output columns per pair tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  float* xch = reinterpret_cast<float*>(smem + S_STAGES * S_STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S_STAGES * S_STAGE_BYTES + S_XCH_FLOATS * 4);
+  uint64_t* empty = full + S_STAGES;
+  uint64_t* tfull = empty + S_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* bad_flag = reinterpret_cast<int*>(tmem_holder + 2);
+  int* tab = reinterpret_cast<int*>(smem + S_STAGES * S_STAGE_BYTES + S_XCH_FLOATS * 4 + P_BAR_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool even = rank == 0;
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int ncl = static_cast<int>(gridDim.x >> 1);
+  const int MT = (n_out + WT - 1) / WT;  // weight tiles per expert
+  const int KB = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    *bad_flag = 0;
+  }
+  __syncthreads();
+  // token tiles per expert; both CTAs of a pair reach the same decisions
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int lo = seg_lo(offsets, e), hi = seg_hi(offsets, e, rows_cap);
+    int m = 0;
+    if (lo < 0 || hi < lo || static_cast<int64_t>(hi) > rows_cap)
+      *bad_flag = 1;
+    else
+      m = (hi - lo + S_BN - 1) / S_BN;
+    tab[e + 1] = m;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tab[0] = 0;
+    for (int e = 0; e < E; ++e) tab[e + 1] += tab[e];
+    if (*bad_flag && blockIdx.x == 0) set_status(status, MOE_DEV_BAD_OFFSETS);
+    for (int s = 0; s < S_STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 8);
+    }
+    ptx::mbar_init(drain, 1);
+    ptx::fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (*bad_flag) return;
+  const int total = tab[E] * MT;
+  if (cid >= total) return;
+  ptx::cluster_sync_all();  // the peer's barriers are initialised before anything arrives on them
+
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmW0);
+      if (SWIGLU) ptx::prefetch_tmap(&tmW1);
+      ptx::prefetch_tmap(&tmX);
+      const uint64_t pol_w = ptx::policy_evict_normal();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < total; tile += ncl) {
+        int e, mt, nt;
+        decode_tile(tab, E, MT, tile, &e, &mt, &nt);
+        const int seg = seg_lo(offsets, e);
+        const int n_e = seg_hi(offsets, e, rows_cap) - seg;
+        const int rem = n_e - nt * S_BN;
+        const int N = rem >= S_BN ? S_BN : (rem + 15) / 16 * 16;
+        const int x_row = seg + nt * S_BN + static_cast<int>(rank) * (N / 2);
+        const int w_row = SWIGLU ? e * w_rows_per_expert + mt * WT + static_cast<int>(rank) * 64
+                                 : e * w_rows_per_expert + mt * WT + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + stage * S_STAGE_BYTES;
+          const uint32_t full_pair = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
+          if (even) ptx::mbar_arrive_expect_tx(&full[stage], 2 * S_STAGE_BYTES);
+          if (SWIGLU) {
+            ptx::tma_load_2d_pair(sa, &tmW0, kb * BK, w_row, full_pair, pol_w);
+            ptx::tma_load_2d_pair(sa + S_A_BYTES / 2, &tmW1, kb * BK, w_row, full_pair, pol_w);
+          } else {
+            ptx::tma_load_2d_pair(sa, &tmW0, kb * BK, w_row, full_pair, pol_w);
+          }
+          ptx::tma_load_2d_pair(sa + S_A_BYTES, &tmX, kb * BK, x_row, full_pair, pol_x);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == S_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (even) {
+        for (int s = 0; s < S_STAGES; ++s)
+          if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_phase >> s) & 1u);
+      }
+      if (*abort_flag) {
+        // copies whose completion is counted in the other CTA cannot be awaited here: give them time
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (even && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cid; ok && tile < total; tile += ncl) {
+        int e, mt, nt;
+        decode_tile(tab, E, MT, tile, &e, &mt, &nt);
+        const int n_e = seg_hi(offsets, e, rows_cap) - seg_lo(offsets, e);
+        const int rem = n_e - nt * S_BN;
+        const int N = rem >= S_BN ? S_BN : (rem + 15) / 16 * 16;
+        const uint32_t idesc = ptx::idesc_bf16_f32(256, N);
+        if (!wait_cluster_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_cluster_bounded(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(stages + stage * S_STAGE_BYTES);
+          const uint32_t sb = sa + S_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UK; ++kk) {
+            ptx::mma_bf16_ss_pair(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32), ptx::sdesc_kmajor_sw128(sb + kk * 32),
+                                  idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair(&empty[stage], 0x3);
+          if (++stage == S_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair(&tfull[acc], 0x3);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      ptx::mma_commit_pair(drain, 0x1);
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    const bool up_half = SWIGLU && q >= 2;
+    const int p = q & 1;     // SwiGLU: warps of quarters p and p + 2 hold gate and up of the same columns
+    float* xg = xch + p * (2 * 16 * 32);  // gate values of tokens 16..31, [16][32]
+    float* xu = xg + 16 * 32;             // up values of tokens 0..15
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = cid; tile < total; tile += ncl) {
+      int e, mt, nt;
+      decode_tile(tab, E, MT, tile, &e, &mt, &nt);
+      const int seg = seg_lo(offsets, e);
+      const int n_e = seg_hi(offsets, e, rows_cap) - seg;
+      const int t_tile = nt * S_BN;
+      const int n_valid = n_e - t_tile < S_BN ? n_e - t_tile : S_BN;
+      const int col = SWIGLU ? mt * WT + static_cast<int>(rank) * 64 + p * 32 + lane
+                             : mt * WT + static_cast<int>(rank) * 128 + q * 32 + lane;
+      const bool col_ok = col < n_out;
+      bf16* obase = out + (static_cast<int64_t>(seg) + t_tile) * n_out + col;
+      // the tcgen05.ld below is warp-collective, and the SwiGLU exchange pairs two warps: both
+      // warps of a pair leave together or not at all
+      const bool ready = wait_cluster_bounded(&tfull[acc], acc_phase, abort_flag);
+      const bool go = SWIGLU ? named_all(1 + p, 64, ready) : __all_sync(0xffffffffu, ready);
+      if (!go) break;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < n_valid; c += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tb + c, v);
+        ptx::tmem_wait_ld();
+        if (SWIGLU) {
+          // swap halves with the partner warp: keep 16 tokens, hand over the other 16
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if (up_half)
+              xu[i * 32 + lane] = __uint_as_float(v[i]);
+            else
+              xg[i * 32 + lane] = __uint_as_float(v[16 + i]);
+          }
+          named_sync(1 + p, 64);
+          const int t0 = c + (up_half ? 16 : 0);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float gv = up_half ? xg[i * 32 + lane] : __uint_as_float(v[i]);
+            const float uv = up_half ? __uint_as_float(v[16 + i]) : xu[i * 32 + lane];
+            if (col_ok && t0 + i < n_valid) obase[static_cast<int64_t>(t0 + i) * n_out] = __float2bfloat16_rn(silu_mul(gv, uv));
+          }
+          named_sync(1 + p, 64);  // both have read the exchange before the next chunk writes it
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col_ok && c + i < n_valid) obase[static_cast<int64_t>(c + i) * n_out] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&tempty[acc]), 0));
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync_all();  // the even CTA's MMAs into this CTA's tensor memory are over
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  if (threadIdx.x == 0 && *abort_flag) set_status(status, MOE_DEV_TIMEOUT);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -806,6 +1099,59 @@ static bool use_pair_tiles(const Plan& p) {
   if (env && strcmp(env, "single") == 0) return false;
   if (env && strcmp(env, "pair") == 0) return true;
   return p.Tk >= static_cast<int64_t>(1024) * p.E;  // mean rows per expert >= 1024
+}
+
+// The swapped-operand pair kernel (weights as M, tokens as N): MOE_FFN_TILES=swab.
+static bool use_swab_tiles(const Plan& p) {
+  const char* env = getenv("MOE_FFN_TILES");
+  (void)p;
+  return env && strcmp(env, "swab") == 0;
+}
+
+template <bool SWIGLU>
+static cudaError_t launch_swab(int64_t tiles, const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& x,
+                               const int32_t* offsets, int E, int K, int w_rows, int n_out, int64_t rows_cap,
+                               bf16* out, int32_t* status, cudaStream_t s) {
+  using namespace tc;
+  auto kern = grouped_gemm_swab<SWIGLU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S_SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  int grid = 2 * static_cast<int>(std::min<int64_t>(current_sm_count() / 2, tiles));
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(grid));
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = S_SMEM_BYTES;
+  lc.stream = s;
+  int max_clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &lc) == cudaSuccess && max_clusters > 0 &&
+      2 * max_clusters < grid)
+    grid = 2 * max_clusters;
+  (void)cudaGetLastError();
+  kern<<<grid, THREADS, S_SMEM_BYTES, s>>>(w0, w1, x, offsets, E, K, w_rows, n_out, rows_cap, out, status);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_ffn_swab(const Plan& p, const void* X, const int32_t* offsets, const void* W_gate,
+                                   const void* W_up, const void* W_down, void* act, void* Y, int32_t* status,
+                                   cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap tmX, tmG, tmU, tmAct, tmD;
+  const uint64_t Tk = static_cast<uint64_t>(p.Tk);
+  if (!make_tmap(&tmX, X, Tk, p.h, 128) ||
+      !make_tmap(&tmG, W_gate, static_cast<uint64_t>(p.E) * p.d_e, p.h, 64) ||
+      !make_tmap(&tmU, W_up, static_cast<uint64_t>(p.E) * p.d_e, p.h, 64) ||
+      !make_tmap(&tmAct, act, Tk, p.d_e, 128) ||
+      !make_tmap(&tmD, W_down, static_cast<uint64_t>(p.E) * p.h, p.d_e, 128))
+    return cudaErrorNotSupported;
+  const int64_t ntiles = (p.Tk + S_BN - 1) / S_BN + p.E;  // token tiles, at most
+  const int64_t tiles1 = ntiles * ((p.d_e + 127) / 128);
+  const int64_t tiles2 = ntiles * ((p.h + 255) / 256);
+  if (tiles1 >= (int64_t(1) << 31) || tiles2 >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  cudaError_t e = launch_swab<true>(tiles1, tmG, tmU, tmX, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
+                                    static_cast<bf16*>(act), status, s);
+  if (e != cudaSuccess) return e;
+  return launch_swab<false>(tiles2, tmD, tmD, tmAct, offsets, p.E, p.d_e, p.h, p.h, p.Tk, static_cast<bf16*>(Y),
+                            status, s);
 }
 
 template <bool SWIGLU, bool GATHER = false>
@@ -861,8 +1207,10 @@ cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, 
                           cudaStream_t s, const void* gather_src, const int32_t* gather_rows) {
   using namespace tc;
   if (p.Tk == 0) return cudaSuccess;
-  const bool pair = use_pair_tiles(p);
   const bool gather = gather_rows != nullptr;  // X[row] = gather_src[gather_rows[row]], read by GEMM1 itself
+  if (!gather && offsets != nullptr && use_swab_tiles(p))
+    return launch_ffn_swab(p, X, offsets, W_gate, W_up, W_down, act, Y, status, s);
+  const bool pair = use_pair_tiles(p);
   const uint32_t a_box = pair ? 128 : BM;           // rows of A each CTA stages
   const uint32_t down_box = pair ? BN / 2 : BN;     // rows of W_down each CTA stages
   CUtensorMap tmX, tmG, tmU, tmAct, tmD;

@@ -30,12 +30,13 @@ def segments(w, seed, zipf):
     return oracle.dispatch(idx, w.E, C, w.priority)
 
 
-@pytest.mark.parametrize("tiles", ["single", "pair"])
+@pytest.mark.parametrize("tiles", ["single", "pair", "swab"])
 @pytest.mark.parametrize("w", W.SMALL + EDGE, ids=lambda w: w.name)
 @pytest.mark.parametrize("zipf", [0.0, 1.2])
 def test_expert_ffn(w, zipf, tiles, monkeypatch):
-    """Both bf16 kernels (128-row tiles on one CTA, 256-row tiles on a CTA pair) against the oracle."""
-    if w.dtype == W.F32 and tiles == "pair":
+    """The three bf16 kernels (128-row tiles on one CTA, 256-row tiles on a CTA pair, and weight
+    rows as M with tokens as N on a CTA pair) against the oracle."""
+    if w.dtype == W.F32 and tiles != "single":
         pytest.skip("float32 runs on the CUDA cores")
     monkeypatch.setenv("MOE_FFN_TILES", tiles)
     inp = synth.generate(w, seed=2, device="cuda")
@@ -64,7 +65,7 @@ def test_expert_ffn(w, zipf, tiles, monkeypatch):
     assert torch.all(Y[A:] == 7.0) and torch.all(act[A:] == 7.0)
 
 
-@pytest.mark.parametrize("dtype,tiles", [(W.BF16, "single"), (W.BF16, "pair"), (W.F32, "single")])
+@pytest.mark.parametrize("dtype,tiles", [(W.BF16, "single"), (W.BF16, "pair"), (W.BF16, "swab"), (W.F32, "single")])
 def test_expert_ffn_rejects_inconsistent_offsets(dtype, tiles, monkeypatch):
     monkeypatch.setenv("MOE_FFN_TILES", tiles)
     w = W.Workload("bad", T=64, h=64, E=4, k=2, d_e=64, dtype=dtype, score_fn=0, renorm=True, noisy=False,

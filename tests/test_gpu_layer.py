@@ -153,3 +153,16 @@ def test_layer_full_size_sampled(w):
     assert delta_error(bufs.out[tt], inp.U[tt], smp["out"], w.dtype) <= tol
     rows = sorted(smp["Y"])
     assert normwise(bufs.Y[torch.as_tensor(rows, device="cuda")], np.stack([smp["Y"][i] for i in rows])) <= tol
+
+
+@pytest.mark.parametrize("w", [W.MIXTRAL, W.DSV3, W.SWITCH, W.STRESS], ids=lambda w: w.name)
+def test_layer_full_size_sampled_swapped_tiles(w, monkeypatch):
+    """The full-size layers again with the expert GEMMs on the weights-as-M pair kernel."""
+    monkeypatch.setenv("MOE_FFN_TILES", "swab")
+    test_layer_full_size_sampled(w)
+
+
+@pytest.mark.parametrize("w", [W.MIXTRAL_SMALL, W.DSV3_SHARED_SMALL, EDGE[-1]], ids=lambda w: w.name)
+def test_layer_small_swapped_tiles(w, monkeypatch):
+    monkeypatch.setenv("MOE_FFN_TILES", "swab")
+    test_layer_small(w)
