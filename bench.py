@@ -332,13 +332,13 @@ def cpu_baseline(w: W.Workload, inp, n_tokens: int = 0, target_s: float = 12.0):
 
 def ffn_tiles(w: W.Workload) -> str:
     """The grouped-GEMM kernel libmoe picks: 256-row CTA-pair tiles when the mean expert segment is
-    at least 1024 rows, else 128-row single-CTA tiles (MOE_FFN_TILES overrides)."""
+    at least 1024 rows, else the weights-as-M pair kernel "swab" (MOE_FFN_TILES overrides)."""
     env = os.environ.get("MOE_FFN_TILES", "")
     if env in ("single", "pair", "swab"):
         return env + " (MOE_FFN_TILES)"
     if w.dtype == W.F32:
         return "cuda-core float32"
-    return "pair" if w.T * w.k >= 1024 * w.E else "single"
+    return "pair" if w.T * w.k >= 1024 * w.E else "swab"
 
 
 def workload_config(w: W.Workload, n_rot: int = 0):
@@ -672,7 +672,9 @@ def run_b300(args, w: W.Workload):
         roof["frac_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
     roof["achieved"] = round(roof["achieved"], 2)
     roof["traffic"] = None if fp8 else profile_traffic(w.name)
-    roof["kernel"] = "grouped SwiGLU expert GEMM: grouped_gemm_tc gate|up + down, both launches of one step"
+    roof["kernel"] = (f"grouped SwiGLU expert GEMM ({ffn_tiles(w)} tiles: "
+                      f"{'grouped_gemm_swab' if ffn_tiles(w).startswith('swab') else 'grouped_gemm_tc'}) "
+                      "gate|up + down, both launches of one step")
     roof["peak_source"] = f"{peak_src}, {'bf16 burst' if roof['bound'] == 'tensor' else roof['bound']}"
     if fp8:
         roof["kernel"] = ("grouped SwiGLU expert GEMM: grouped_gemm_tc<true, true> E4M3 gate|up (kind::f8f6f4) + "

@@ -1089,11 +1089,15 @@ static bool make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t
 }  // namespace tc
 
 // Which kernel runs the two grouped GEMMs.  CTA pairs cut the shared-memory
-// operand traffic per MMA by a third but compute 256-row tiles, so they pay
-// off when the expert segments are long (measured on B300: 0.80 vs 0.67 of
-// the bf16 peak with 6144-row segments, 0.61 vs 0.67 with 512-row ones);
-// shorter segments stay on single-CTA 128-row tiles.  MOE_FFN_TILES=single|pair overrides the
-// choice (for measurement and for testing both kernels).
+// operand traffic per MMA by a third.  With row tiles of 256 tokens they pay off
+// when the expert segments are long (measured on B300: 0.80 vs 0.67 of the bf16
+// peak with 6144-row segments); shorter segments go to the weights-as-M pair
+// kernel, whose token tiles end within 16 rows of each segment (measured:
+// 1100 vs 1017 TFLOP/s with 512-row segments, 82% vs 76% of HBM bandwidth with
+// the 128-row segments of the 256-expert shape).  The single-CTA kernel serves
+// the FP8 and gathered up-projections, one-segment products and the override.
+// MOE_FFN_TILES=single|pair|swab overrides the choice (for measurement and for
+// testing every kernel).
 static bool use_pair_tiles(const Plan& p) {
   const char* env = getenv("MOE_FFN_TILES");
   if (env && strcmp(env, "single") == 0) return false;
@@ -1101,11 +1105,13 @@ static bool use_pair_tiles(const Plan& p) {
   return p.Tk >= static_cast<int64_t>(1024) * p.E;  // mean rows per expert >= 1024
 }
 
-// The swapped-operand pair kernel (weights as M, tokens as N): MOE_FFN_TILES=swab.
+// The swapped-operand pair kernel (weights as M, tokens as N): segments shorter than 1024 rows
+// on average, unless MOE_FFN_TILES names another kernel.
 static bool use_swab_tiles(const Plan& p) {
   const char* env = getenv("MOE_FFN_TILES");
-  (void)p;
-  return env && strcmp(env, "swab") == 0;
+  if (env && (strcmp(env, "single") == 0 || strcmp(env, "pair") == 0)) return false;
+  if (env && strcmp(env, "swab") == 0) return true;
+  return p.Tk < static_cast<int64_t>(1024) * p.E;
 }
 
 template <bool SWIGLU>
