@@ -811,12 +811,18 @@ __device__ __forceinline__ bool named_all(int id, int threads, bool pred) {
 
 // SWIGLU: out[row, j] = SiLU((X W0^T)[row, j]) * (X W1^T)[row, j], j < n_out (= d_e), W0/W1 rows per expert = d_e.
 // plain:  out[row, m] = (X W0^T)[row, m],                           m < n_out (= h),   W0 rows per expert = h.
-template <bool SWIGLU>
+// FP8 (SwiGLU only): X, W0, W1 are E4M3 codes (kind::f8f6f4, 128 K-elements per stage row); each
+// sum is scaled by x_scale[row] * w_scale[weight row] before SiLU * up.
+template <bool SWIGLU, bool FP8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     grouped_gemm_swab(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                       const __grid_constant__ CUtensorMap tmX, const int32_t* __restrict__ offsets, int E, int K,
-                      int w_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status) {
+                      int w_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status,
+                      const float* __restrict__ x_scale = nullptr, const float* __restrict__ w0_scale = nullptr,
+                      const float* __restrict__ w1_scale = nullptr) {
+  static_assert(SWIGLU || !FP8, "the FP8 path is the up-projection");
   constexpr int WT = SWIGLU ? 128 : 256;  // output columns per pair tile
+  constexpr int BKE = FP8 ? 2 * BK : BK;  // K elements per stage (128 bytes of every row)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -837,7 +843,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int cid = static_cast<int>(blockIdx.x >> 1);
   const int ncl = static_cast<int>(gridDim.x >> 1);
   const int MT = (n_out + WT - 1) / WT;  // weight tiles per expert
-  const int KB = (K + BK - 1) / BK;
+  const int KB = (K + BKE - 1) / BKE;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -913,12 +919,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t full_pair = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
           if (even) ptx::mbar_arrive_expect_tx(&full[stage], 2 * S_STAGE_BYTES);
           if (SWIGLU) {
-            ptx::tma_load_2d_pair(sa, &tmW0, kb * BK, w_row, full_pair, pol_w);
-            ptx::tma_load_2d_pair(sa + S_A_BYTES / 2, &tmW1, kb * BK, w_row, full_pair, pol_w);
+            ptx::tma_load_2d_pair(sa, &tmW0, kb * BKE, w_row, full_pair, pol_w);
+            ptx::tma_load_2d_pair(sa + S_A_BYTES / 2, &tmW1, kb * BKE, w_row, full_pair, pol_w);
           } else {
-            ptx::tma_load_2d_pair(sa, &tmW0, kb * BK, w_row, full_pair, pol_w);
+            ptx::tma_load_2d_pair(sa, &tmW0, kb * BKE, w_row, full_pair, pol_w);
           }
-          ptx::tma_load_2d_pair(sa + S_A_BYTES, &tmX, kb * BK, x_row, full_pair, pol_x);
+          ptx::tma_load_2d_pair(sa + S_A_BYTES, &tmX, kb * BKE, x_row, full_pair, pol_x);
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == S_STAGES) {
@@ -949,7 +955,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int n_e = seg_hi(offsets, e, rows_cap) - seg_lo(offsets, e);
         const int rem = n_e - nt * S_BN;
         const int N = rem >= S_BN ? S_BN : (rem + 15) / 16 * 16;
-        const uint32_t idesc = ptx::idesc_bf16_f32(256, N);
+        const uint32_t idesc = FP8 ? ptx::idesc_e4m3_f32(256, N) : ptx::idesc_bf16_f32(256, N);
         if (!wait_cluster_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -964,10 +970,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_u32(stages + stage * S_STAGE_BYTES);
           const uint32_t sb = sa + S_A_BYTES;
+          // 32 bytes of K per MMA: 16 bf16 or 32 E4M3
 #pragma unroll
           for (int kk = 0; kk < BK / UK; ++kk) {
-            ptx::mma_bf16_ss_pair(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32), ptx::sdesc_kmajor_sw128(sb + kk * 32),
+            if (FP8)
+              ptx::mma_f8_ss_pair(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32), ptx::sdesc_kmajor_sw128(sb + kk * 32),
                                   idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16_ss_pair(d_tmem, ptx::sdesc_kmajor_sw128(sa + kk * 32),
+                                    ptx::sdesc_kmajor_sw128(sb + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::mma_commit_pair(&empty[stage], 0x3);
           if (++stage == S_STAGES) {
@@ -1002,6 +1013,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                              : mt * WT + static_cast<int>(rank) * 128 + q * 32 + lane;
       const bool col_ok = col < n_out;
       bf16* obase = out + (static_cast<int64_t>(seg) + t_tile) * n_out + col;
+      // FP8: this lane's weight-row scale (gate rows in quarters 0/1, up rows in 2/3)
+      float w_s = 1.f;
+      if (FP8 && col_ok) w_s = (up_half ? w1_scale : w0_scale)[static_cast<int64_t>(e) * w_rows_per_expert + col];
       // the tcgen05.ld below is warp-collective, and the SwiGLU exchange pairs two warps: both
       // warps of a pair leave together or not at all
       const bool ready = wait_cluster_bounded(&tfull[acc], acc_phase, abort_flag);
@@ -1013,7 +1027,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int c = 0; c < n_valid; c += 32) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(tb + c, v);
+        // FP8: lane i holds the scale of token c + i, shared by every weight row
+        const float my_xs = (FP8 && c + lane < n_valid) ? x_scale[static_cast<int64_t>(seg) + t_tile + c + lane] : 0.f;
         ptx::tmem_wait_ld();
+        if (FP8) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = __float_as_uint(__uint_as_float(v[i]) * (w_s * __shfl_sync(0xffffffffu, my_xs, i)));
+        }
         if (SWIGLU) {
           // swap halves with the partner warp: keep 16 tokens, hand over the other 16
 #pragma unroll
@@ -1114,12 +1135,13 @@ static bool use_swab_tiles(const Plan& p) {
   return p.Tk < static_cast<int64_t>(1024) * p.E;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, bool FP8 = false>
 static cudaError_t launch_swab(int64_t tiles, const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorMap& x,
                                const int32_t* offsets, int E, int K, int w_rows, int n_out, int64_t rows_cap,
-                               bf16* out, int32_t* status, cudaStream_t s) {
+                               bf16* out, int32_t* status, cudaStream_t s, const float* x_scale = nullptr,
+                               const float* w0_scale = nullptr, const float* w1_scale = nullptr) {
   using namespace tc;
-  auto kern = grouped_gemm_swab<SWIGLU>;
+  auto kern = grouped_gemm_swab<SWIGLU, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S_SMEM_BYTES));
   if (e != cudaSuccess) return e;
   int grid = 2 * static_cast<int>(std::min<int64_t>(current_sm_count() / 2, tiles));
@@ -1133,7 +1155,8 @@ static cudaError_t launch_swab(int64_t tiles, const CUtensorMap& w0, const CUten
       2 * max_clusters < grid)
     grid = 2 * max_clusters;
   (void)cudaGetLastError();
-  kern<<<grid, THREADS, S_SMEM_BYTES, s>>>(w0, w1, x, offsets, E, K, w_rows, n_out, rows_cap, out, status);
+  kern<<<grid, THREADS, S_SMEM_BYTES, s>>>(w0, w1, x, offsets, E, K, w_rows, n_out, rows_cap, out, status, x_scale,
+                                           w0_scale, w1_scale);
   return cudaGetLastError();
 }
 
@@ -1275,6 +1298,21 @@ cudaError_t launch_ffn_fp8_tc(const Plan& p, const uint8_t* X8, const float* x_s
   const int grid1 = static_cast<int>(std::min<int64_t>(nsm, tiles1));
   const int per = pair ? 2 : 1;
   const int grid2 = per * static_cast<int>(std::min<int64_t>(pair ? nsm / 2 : nsm, tiles2));
+  if (use_swab_tiles(p)) {
+    // both GEMMs on the weights-as-M pair kernel (64-row gate/up boxes, 128-row token boxes)
+    CUtensorMap sX, sG, sU, sAct, sD;
+    if (!make_tmap(&sX, X8, Tk, p.h, 128, true) ||
+        !make_tmap(&sG, W_gate8, static_cast<uint64_t>(p.E) * p.d_e, p.h, 64, true) ||
+        !make_tmap(&sU, W_up8, static_cast<uint64_t>(p.E) * p.d_e, p.h, 64, true) ||
+        !make_tmap(&sAct, act, Tk, p.d_e, 128) || !make_tmap(&sD, W_down, static_cast<uint64_t>(p.E) * p.h, p.d_e, 128))
+      return cudaErrorNotSupported;
+    const int64_t nt = (p.Tk + S_BN - 1) / S_BN + p.E;
+    cudaError_t e = launch_swab<true, true>(nt * ((p.d_e + 127) / 128), sG, sU, sX, offsets, p.E, p.h, p.d_e, p.d_e,
+                                            p.Tk, static_cast<bf16*>(act), status, s, x_scale, s_gate, s_up);
+    if (e != cudaSuccess) return e;
+    return launch_swab<false>(nt * ((p.h + 255) / 256), sD, sD, sAct, offsets, p.E, p.d_e, p.h, p.h, p.Tk,
+                              static_cast<bf16*>(Y), status, s);
+  }
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;

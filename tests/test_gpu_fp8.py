@@ -85,11 +85,14 @@ FFN = [
 ]
 
 
+@pytest.mark.parametrize("tiles", ["single", "swab"])
 @pytest.mark.parametrize("w", FFN, ids=lambda w: w.name)
 @pytest.mark.parametrize("zipf", [0.0, 1.2])
-def test_expert_ffn_fp8(w, zipf):
+def test_expert_ffn_fp8(w, zipf, tiles, monkeypatch):
     """Weights quantised on the GPU (bit-exact against the oracle), the dispatch's FP8 rows, then
-    act and Y against the oracle's SwiGLU on the dequantised rows and weights."""
+    act and Y against the oracle's SwiGLU on the dequantised rows and weights; the FP8 gate|up
+    GEMM on the single-CTA kernel and on the weights-as-M pair kernel."""
+    monkeypatch.setenv("MOE_FFN_TILES", tiles)
     inp = synth.generate(w, seed=1, device="cuda")
     idx = synth.random_routing(w.T, w.E, w.k, seed=9, zipf_s=zipf).cuda()
     cfg = L.config_of(w)
