@@ -809,6 +809,25 @@ __device__ __forceinline__ bool named_all(int id, int threads, bool pred) {
   return r != 0;
 }
 
+// Token tiling of a segment of n rows: ceil(n / 256) tiles of one size, n / tiles rounded up to 16
+// (at most 256), so that a segment just past a multiple of 256 is not left with a nearly empty
+// tile that still streams a whole K of weights.  (tiles - 1) * size < n always holds, because
+// n > 256 (tiles - 1) and size <= 256.
+__device__ __forceinline__ int swab_tile_rows(int n) {
+  const int tiles = (n + S_BN - 1) / S_BN;
+  if (tiles <= 1) return S_BN;
+  const int rows = ((n + tiles - 1) / tiles + 15) / 16 * 16;
+  return rows < S_BN ? rows : S_BN;
+}
+// First row and MMA width N (rows rounded up to 16) of token tile nt of a segment of n rows.
+__device__ __forceinline__ void swab_tile(int n, int nt, int* t0, int* N) {
+  const int size = swab_tile_rows(n);
+  *t0 = nt * size;
+  const int rem = n - *t0;
+  const int r16 = (rem + 15) / 16 * 16;
+  *N = r16 < size ? r16 : size;
+}
+
 // SWIGLU: out[row, j] = SiLU((X W0^T)[row, j]) * (X W1^T)[row, j], j < n_out (= d_e), W0/W1 rows per expert = d_e.
 // plain:  out[row, m] = (X W0^T)[row, m],                           m < n_out (= h),   W0 rows per expert = h.
 // FP8 (SwiGLU only): X, W0, W1 are E4M3 codes (kind::f8f6f4, 128 K-elements per stage row); each
@@ -905,9 +924,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         decode_tile(tab, E, MT, tile, &e, &mt, &nt);
         const int seg = seg_lo(offsets, e);
         const int n_e = seg_hi(offsets, e, rows_cap) - seg;
-        const int rem = n_e - nt * S_BN;
-        const int N = rem >= S_BN ? S_BN : (rem + 15) / 16 * 16;
-        const int x_row = seg + nt * S_BN + static_cast<int>(rank) * (N / 2);
+        int t0, N;
+        swab_tile(n_e, nt, &t0, &N);
+        const int x_row = seg + t0 + static_cast<int>(rank) * (N / 2);
         const int w_row = SWIGLU ? e * w_rows_per_expert + mt * WT + static_cast<int>(rank) * 64
                                  : e * w_rows_per_expert + mt * WT + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < KB; ++kb) {
@@ -953,8 +972,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         int e, mt, nt;
         decode_tile(tab, E, MT, tile, &e, &mt, &nt);
         const int n_e = seg_hi(offsets, e, rows_cap) - seg_lo(offsets, e);
-        const int rem = n_e - nt * S_BN;
-        const int N = rem >= S_BN ? S_BN : (rem + 15) / 16 * 16;
+        int t0, N;
+        swab_tile(n_e, nt, &t0, &N);
         const uint32_t idesc = FP8 ? ptx::idesc_e4m3_f32(256, N) : ptx::idesc_bf16_f32(256, N);
         if (!wait_cluster_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
@@ -1007,8 +1026,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       decode_tile(tab, E, MT, tile, &e, &mt, &nt);
       const int seg = seg_lo(offsets, e);
       const int n_e = seg_hi(offsets, e, rows_cap) - seg;
-      const int t_tile = nt * S_BN;
-      const int n_valid = n_e - t_tile < S_BN ? n_e - t_tile : S_BN;
+      int t_tile, N;
+      swab_tile(n_e, nt, &t_tile, &N);
+      const int n_valid = n_e - t_tile < N ? n_e - t_tile : N;
       const int col = SWIGLU ? mt * WT + static_cast<int>(rank) * 64 + p * 32 + lane
                              : mt * WT + static_cast<int>(rank) * 128 + q * 32 + lane;
       const bool col_ok = col < n_out;
