@@ -809,23 +809,14 @@ __device__ __forceinline__ bool named_all(int id, int threads, bool pred) {
   return r != 0;
 }
 
-// Token tiling of a segment of n rows: ceil(n / 256) tiles of one size, n / tiles rounded up to 16
-// (at most 256), so that a segment just past a multiple of 256 is not left with a nearly empty
-// tile that still streams a whole K of weights.  (tiles - 1) * size < n always holds, because
-// n > 256 (tiles - 1) and size <= 256.
-__device__ __forceinline__ int swab_tile_rows(int n) {
-  const int tiles = (n + S_BN - 1) / S_BN;
-  if (tiles <= 1) return S_BN;
-  const int rows = ((n + tiles - 1) / tiles + 15) / 16 * 16;
-  return rows < S_BN ? rows : S_BN;
-}
-// First row and MMA width N (rows rounded up to 16) of token tile nt of a segment of n rows.
+// First row and MMA width N of token tile nt of a segment of n rows: 256-row tiles, the last one
+// rounded up to 16 rows.  (Tiles of one balanced size per segment were measured 1-2% slower on the
+// 512-row segments of the Mixtral shape: a short last tile costs only its weight reads, which
+// the segment's full tiles have already brought into L2.)
 __device__ __forceinline__ void swab_tile(int n, int nt, int* t0, int* N) {
-  const int size = swab_tile_rows(n);
-  *t0 = nt * size;
+  *t0 = nt * S_BN;
   const int rem = n - *t0;
-  const int r16 = (rem + 15) / 16 * 16;
-  *N = r16 < size ? r16 : size;
+  *N = rem >= S_BN ? S_BN : (rem + 15) / 16 * 16;
 }
 
 // SWIGLU: out[row, j] = SiLU((X W0^T)[row, j]) * (X W1^T)[row, j], j < n_out (= d_e), W0/W1 rows per expert = d_e.
