@@ -53,6 +53,11 @@ constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + sizeof(i
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 constexpr uint32_t ATOM_BYTES = 64 * 128;  // one MN-major atom column: 64 K-rows of 128 bytes
+// grouped_wgrad stages each epilogue warp's 32 x 32 float32 block (4 KB, 128-byte swizzle) for a
+// TMA store, after the tile table
+constexpr size_t W_STAGING_OFFSET = (STAGES * STAGE_BYTES + BAR_BYTES + sizeof(int) * (MAX_E + 1) + 1023) / 1024 * 1024;
+constexpr size_t W_SMEM_BYTES = 1024 + W_STAGING_OFFSET + 4 * 4096;
+static_assert(W_SMEM_BYTES <= 232448, "shared memory");
 
 enum Mode { DACT = 0, DGU = 1, DX = 2 };
 
@@ -382,10 +387,22 @@ __global__ void __launch_bounds__(THREADS, 1)
 // Weight gradients: out[e][m][n] = sum over the rows r of expert e of A[r][m] B[r][n]
 // (A, B row-major activations, read MN-major), float32 output [E, M, N].  One tile = 128 x 256
 // of one expert; every expert has M/128 x N/256 tiles, an expert with no rows writes zeros.
+// TMA store of a shared block to a 3D tensor at (x, y, z), tracked in this thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, const void* smem_src, int32_t x, int32_t y,
+                                             int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(ptx::smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_wgrad(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const int32_t* __restrict__ offsets, int E, int M, int N, int64_t rows_cap,
-                  float* __restrict__ out, int32_t* status) {
+                  const __grid_constant__ CUtensorMap tmOut, const int32_t* __restrict__ offsets, int E, int M,
+                  int N, int64_t rows_cap, float* __restrict__ out, bool tma_out, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   const Smem m = carve(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -514,35 +531,53 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
+    // Each warp moves its 32 rows x 32 columns of the accumulator through a 4 KB shared block
+    // (128-byte swizzle: row r's 16-byte chunk i at r * 128 + ((i ^ (r & 7)) << 4)) and one TMA
+    // store writes the block as whole 128-byte rows of dW[e]; the [E, M, N] tensor map clips rows
+    // past M and columns past N.  Before a block is refilled, the previous store has read it.
     const int q = warp & 3;
+    uint8_t* blk = reinterpret_cast<uint8_t*>(
+                       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)) +
+                   W_STAGING_OFFSET + q * 4096;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, mt, nt;
       decode(tile, &e, &mt, &nt);
       const bool empty_seg = seg_hi(offsets, e, rows_cap) == seg_lo(offsets, e);
-      const int mrow = mt * BM + q * 32 + lane;
       const bool ready = ptx::mbar_wait_bounded(&m.tfull[acc], acc_phase, m.abort_flag, WAIT_LIMIT_NS);
       if (!__all_sync(0xffffffffu, ready)) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-      float* orow = out + (static_cast<int64_t>(e) * M + mrow) * N;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(tb + c, v);
         ptx::tmem_wait_ld();
         const int col0 = nt * BN + c;
-        if (mrow < M) {
-          if (col0 + 32 <= N && (N & 3) == 0) {
-            float4* d = reinterpret_cast<float4*>(orow + col0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d[i] = empty_seg ? make_float4(0.f, 0.f, 0.f, 0.f)
-                               : make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-          } else {
+        if (col0 >= N) break;  // (warp-uniform)
+        if (!tma_out) {
+          // rows whose length is not a multiple of 4 floats: plain stores
+          const int mrow = mt * BM + q * 32 + lane;
+          if (mrow < M) {
+            float* orow = out + (static_cast<int64_t>(e) * M + mrow) * N;
             for (int i = 0; i < 32 && col0 + i < N; ++i) orow[col0 + i] = empty_seg ? 0.f : __uint_as_float(v[i]);
           }
+          continue;
+        }
+        if (lane == 0) bulk_wait_read0();  // the block's previous store has read it
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 val = empty_seg ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                       : make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          *reinterpret_cast<float4*>(blk + lane * 128 + ((i ^ (lane & 7)) << 4)) = val;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmOut, blk, col0, mt * BM + q * 32, e);
+          bulk_commit();
         }
       }
       ptx::tc_fence_before();
@@ -551,6 +586,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_all();  // every store of this warp has completed
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -603,15 +640,30 @@ static cudaError_t launch_rows(int grid, const CUtensorMap& a0, const CUtensorMa
   return cudaGetLastError();
 }
 
+// float32 [E, M, N] written in boxes of 32 x 32 with the 128-byte swizzle (TMA stores)
+static bool make_tmap_out(CUtensorMap* tm, float* base, int E, int M, int N) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || N % 4 != 0 || reinterpret_cast<uintptr_t>(base) % 16 != 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(E)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 4, static_cast<cuuint64_t>(M) * N * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static cudaError_t launch_wgrad(int nsm, const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int E,
                                 int M, int N, int64_t rows_cap, float* out, int32_t* status, cudaStream_t s) {
+  CUtensorMap tm_out = {};
+  const bool tma_out = make_tmap_out(&tm_out, out, E, M, N);  // false when N % 4 != 0
   cudaError_t e = cudaFuncSetAttribute(grouped_wgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_BYTES));
+                                       static_cast<int>(W_SMEM_BYTES));
   if (e != cudaSuccess) return e;
   const int64_t tiles = static_cast<int64_t>(E) * ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   if (tiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(std::min<int64_t>(nsm, tiles));
-  grouped_wgrad<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, offsets, E, M, N, rows_cap, out, status);
+  grouped_wgrad<<<grid, THREADS, W_SMEM_BYTES, s>>>(a, b, tm_out, offsets, E, M, N, rows_cap, out, tma_out, status);
   return cudaGetLastError();
 }
 

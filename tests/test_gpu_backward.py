@@ -183,3 +183,31 @@ def test_layer_backward(w):
     for n in names:
         refn = ref[n[:-len("_shared")] + "_sh" if n.endswith("_shared") else n]
         assert normwise(getattr(grads, n), refn) <= tol, n
+
+
+@pytest.mark.parametrize("E,noisy", [(6, False), (5, True), (8, False)])
+def test_router_input_backward_narrow_rows(E, noisy):
+    """The router's weight gradients [h, E] with E not a multiple of 4 (rows of E floats take the
+    plain-store epilogue; multiples of 4 the TMA-store one) against the oracle."""
+    import ctypes
+    T, h = 300, 192
+    w = W.Workload("rb", T=T, h=h, E=E, k=2, d_e=64, dtype=W.BF16, score_fn=W.SOFTMAX, renorm=True, noisy=noisy,
+                   capacity_factor=0.0)
+    inp = synth.generate(w, seed=4, device="cuda", experts=False)
+    dH = synth.normal((T, E), 1.0, 3, "logits", "cuda", torch.float32)
+    cfg = L.config_of(w)
+    dU = torch.empty((T, h), dtype=torch.bfloat16, device="cuda")
+    dW_r = torch.full((h, E), 7.0, dtype=torch.float32, device="cuda")
+    dW_n = torch.full((h, E), 7.0, dtype=torch.float32, device="cuda") if noisy else None
+    db = torch.empty(E, dtype=torch.float32, device="cuda")
+    ws = L.new_workspace(cfg)
+    P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    st = L.lib.moe_router_input_backward(ctypes.byref(cfg), P(inp.U), P(inp.W_r), P(inp.W_noise), P(inp.eps), P(dH),
+                                         P(dU), P(dW_r), P(dW_n), P(db), P(ws), None)
+    assert st == L.MOE_OK, L.lib.moe_last_error().decode()
+    assert L.moe_get_device_status(ws) == 0
+    # the library rounds dH (and dN) to bf16 for the tensor-core products
+    ref = oracle.router_input_backward(inp.U, inp.W_r, oracle.f64(dH.bfloat16()), inp.W_noise, inp.eps)
+    assert normwise(dW_r, ref["dW_r"]) <= 2e-2
+    if noisy:
+        assert normwise(dW_n, ref["dW_noise"]) <= 3e-2
