@@ -213,11 +213,15 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
   const int NW = static_cast<int>(blockDim.x) / 32;
   if (blockIdx.x == 0 && threadIdx.x == 0) *ppart_rows = static_cast<int32_t>(gridDim.x);
 
-  // 1. final logits of the tile; rows t0 .. t0 + rows - 1 are contiguous in every input
-  for (int r = warp; r < rows; r += NW) {
-    const int64_t gr = (t0 + r) * E;
-    for (int e = lane; e < E; e += 32) {
-      const int64_t g = gr + e;
+  // 1. final logits of the tile; rows t0 .. t0 + rows - 1 are contiguous in every input, so the
+  // whole block sweeps the tile's rows x E entries in order (coalesced, and every lane busy
+  // even when E is small)
+  const int n_el = rows * E;
+#pragma unroll 2
+  for (int i = threadIdx.x; i < n_el; i += blockDim.x) {
+    const int r = i / E, e = i - r * E;
+    {
+      const int64_t g = t0 * E + i;
       float x;
       if (logits_in) {
         x = logits_in[g];
