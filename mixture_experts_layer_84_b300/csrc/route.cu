@@ -217,9 +217,11 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
   // whole block sweeps the tile's rows x E entries in order (coalesced, and every lane busy
   // even when E is small)
   const int n_el = rows * E;
+  const bool e_pow2 = (E & (E - 1)) == 0;
+  const int e_shift = __ffs(E) - 1;
 #pragma unroll 2
   for (int i = threadIdx.x; i < n_el; i += blockDim.x) {
-    const int r = i / E, e = i - r * E;
+    const int r = e_pow2 ? i >> e_shift : i / E, e = i - r * E;
     {
       const int64_t g = t0 * E + i;
       float x;
