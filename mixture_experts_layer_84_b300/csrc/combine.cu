@@ -22,7 +22,7 @@
 
 namespace moe {
 
-constexpr int COMBINE_UNROLL = 2;  // 4 measured slower with k = 6..8 (register-bound)
+constexpr int COMBINE_UNROLL = 2;  // 4 measured slower with k = 6..8
 
 template <typename T>
 __global__ void __launch_bounds__(256) combine_rows(const uint4* __restrict__ U, const uint4* __restrict__ Y,
