@@ -22,7 +22,10 @@
 // MMA reads them (they hold the next expert's rows).
 // Pipeline, roles and bounded waits follow the forward kernel: warp 0 TMA
 // producer (4 stages), warp 1 tensor-memory owner and MMA issuer (two
-// 128 x 256 float32 accumulators), warps 2-5 epilogue.
+// 128 x 256 float32 accumulators), warps 2-5 epilogue.  The weight gradients'
+// epilogue stages each warp's 32 x 32 float32 block in shared memory and writes
+// it with one TMA store through an [E, M, N] map, so every store leaves as whole
+// 128-byte rows.
 #include <cuda.h>
 
 #include <algorithm>

@@ -8,13 +8,20 @@
 // scoring/renormalisation table), section 负载均衡辅助损失：推导与梯度 (P_i, and
 // the sigmoid form s' = s / sum_j s_j).
 //
-// Two launches.  route_partial_logits streams U once: each block owns BT
-// tokens and one slice of h, stages U and W_r chunks in shared memory with
-// cp.async double buffering and accumulates in float32 registers; small T is
-// split along h so the grid still covers the GPU.  route_select then sums the
-// slices in a fixed order (run-to-run identical), adds bias and noise, and
-// handles one token per warp: scores, k rounds of a warp arg-max, gates and
-// the score sums.
+// Two launches.  The logits come in h-slices: from route_logits_tc (bf16, tensor cores, in
+// route_tc.cu) or from route_partial_logits here (CUDA cores), which streams U once: each block
+// owns BT tokens and one slice of h, stages U and W_r chunks in shared memory with cp.async
+// double buffering and accumulates in float32 registers; small T is split along h so the grid
+// still covers the GPU.  route_select then
+//   1. stages a tile of tokens: the whole block sums each logit's slices in a fixed order
+//      (run-to-run identical) and adds bias and noise;
+//   2. gives each token G lanes (G = E / 32 rounded up to a power of two), each with a chunk of
+//      the experts: maximum and exp-sum by butterflies, then (section 设备受限与节点受限路由,
+//      with groups) the group scores and the kept-group mask, then a running top-k list per
+//      lane on the selection key (the logit, or score + bias with a loss-free selection bias,
+//      section 无辅助损失的负载均衡), merged across the lanes bitonically; gates from the scores;
+//   3. writes the tile's per-expert score sums and LSE^2 sums (section Router z-loss) for
+//      moe_combine's statistics.
 #include <float.h>
 
 #include "common.cuh"
