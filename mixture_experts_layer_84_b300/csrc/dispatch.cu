@@ -22,6 +22,9 @@
 //                    writes slot_row and row_token;
 //   dispatch_scatter one warp per token, 16-byte copies: each U row is read
 //                    once and written to the (up to k) rows it was kept in.
+//                    Skipped when X is NULL: the FP8 dispatch (fp8.cu) copies
+//                    quantised rows instead, and the gathered first GEMM reads
+//                    the rows of U itself.
 #include <algorithm>
 #include <mutex>
 
