@@ -11,8 +11,16 @@ weights alone are larger than L2 on every workload but the tiny one.
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own
 replica (independent batches, no collective on the data path): weak scaling.
 
---impl reference times the plain float64 CPU oracle (oracle/) on the host
-cores on bounded samples of the same workload.
+The default workload is the largest one (stress_bf16: T=65536, h=4096, E=64,
+k=6, d_e=1408).  `value` is the median of --repeats regions of exactly K
+steps, each a CUDA-graph replay of the whole layer.  The stage breakdown is
+device time: each stage is captured as its own graph, and the stage graphs
+are replayed in layer order with events between them.  With one GPU the line
+also carries `per_config`: value, stages and roofline of every other
+workload, measured the same way in the same run.
+
+--impl reference times the plain CPU oracle (oracle/) on the host cores on
+bounded samples of the same workload.
 """
 from __future__ import annotations
 
@@ -397,126 +405,268 @@ def run_reference(args, w: W.Workload):
 
 # ----------------------------------------------------------------------------- B300 arm
 
+STAGES = ("route", "dispatch", "ffn", "shared_ffn", "combine")
+
+
+class LayerRun:
+    """One workload on the device: inputs, rotating token batches, buffers, and CUDA graphs of the
+    whole layer and of each stage (one of each per batch)."""
+
+    def __init__(self, w: W.Workload, device, fp8: bool = False, gather: bool = False):
+        from mixture_experts_layer_84_b300 import _lib as L
+        self.L, self.w, self.device = L, w, device
+        self.inp = inp = synth.generate(w, seed=0, device=device)
+        ubytes = w.T * w.h * w.elem_bytes
+        self.n_rot = max(2, min(64, math.ceil(2 * L2_BYTES / max(ubytes, 1))))
+        self.pool = [inp.U] + [synth.normal((w.T, w.h), 1.0, 100 + r, "U", device, w.torch_dtype)
+                               for r in range(self.n_rot - 1)]
+        self.cfg = L.config_of(w)
+        if fp8 and (w.dtype != W.BF16 or w.h % 16):
+            raise SystemExit("bench.py --fp8: needs a bf16 workload with h % 16 == 0")
+        self.fp8 = fp8
+        self.gather = gather and not fp8 and w.dtype == W.BF16
+        self.bufs = L.LayerBuffers.allocate(self.cfg, device=device, with_X=not (fp8 or self.gather))
+        self.w8 = L.FP8Weights.quantize(inp.W_gate, inp.W_up) if fp8 else None  # once, outside every timed region
+        self.rows8 = L.FP8Rows.allocate(self.cfg, device=device) if fp8 else None
+        self.stages = [s for s in STAGES if s != "shared_ffn" or w.n_shared]
+        self.graphs, self.stage_graphs, self.graph_error = [], [], None
+
+    # the stage calls of moe_layer_forward (or moe_layer_forward_fp8), one function per stage
+    def run_stage(self, name, U):
+        L, w, inp, b, cfg = self.L, self.w, self.inp, self.bufs, self.cfg
+        if name == "route":
+            L.moe_route(cfg, U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, None, None, b.idx, b.gate, b.ws,
+                        sel_bias=inp.sel_bias)
+        elif name == "dispatch":
+            if self.fp8:
+                L.moe_dispatch_fp8(cfg, U, b.idx, b.counts_routed, b.counts_kept, b.offsets, b.slot_row, b.row_token,
+                                   self.rows8.X8, self.rows8.x_scale, b.n_dropped, b.ws)
+            else:  # gather: routing metadata only, the first GEMM reads the token rows itself
+                L.moe_dispatch(cfg, U, b.idx, b.counts_routed, b.counts_kept, b.offsets, b.slot_row, b.row_token,
+                               None if self.gather else b.X, b.n_dropped, b.ws)
+        elif name == "ffn":
+            if self.fp8:
+                L.moe_expert_ffn_fp8(cfg, self.rows8.X8, self.rows8.x_scale, b.offsets, self.w8, inp.W_down, b.act,
+                                     b.Y, b.ws)
+            elif self.gather:
+                L.moe_expert_ffn_gather(cfg, U, b.row_token, b.offsets, inp.W_gate, inp.W_up, inp.W_down, b.act, b.Y,
+                                        b.ws)
+            else:
+                L.moe_expert_ffn(cfg, b.X, b.offsets, inp.W_gate, inp.W_up, inp.W_down, b.act, b.Y, b.ws)
+        elif name == "shared_ffn":
+            L.moe_shared_ffn(cfg, U, inp.W_gate_sh, inp.W_up_sh, inp.W_down_sh, b.act_shared, b.Y_shared, b.ws)
+        elif name == "combine":
+            L.moe_combine(cfg, U, b.Y, b.slot_row, b.gate, b.counts_routed, b.out, b.f, b.P, b.aux, b.ws,
+                          z_loss=b.z_loss, Y_shared=b.Y_shared)
+        else:
+            raise ValueError(name)
+
+    def layer(self, U):
+        for s in self.stages:
+            self.run_stage(s, U)
+
+    def batch_stats(self):
+        """Kept pairs and active experts of each batch (outside any timed region)."""
+        self.A_of, self.act_of = [], []
+        for U in self.pool:
+            self.layer(U)
+            off = self.bufs.offsets.cpu()
+            self.A_of.append(int(off[-1]))
+            self.act_of.append(int(((off[1:] - off[:-1]) > 0).sum()))
+        code = self.L.moe_get_device_status(self.bufs.ws)
+        if code != 0:
+            raise SystemExit(f"bench.py: device status {code} on {self.w.name}")
+
+    def capture(self, enabled: bool = True):
+        """One graph of the whole layer per batch, and one graph per stage per batch."""
+        if not enabled:
+            return
+        dev = self.device
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            self.layer(self.pool[0])  # first calls on this stream outside the capture
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        torch.cuda.synchronize(dev)
+        try:
+            for U in self.pool:
+                g = torch.cuda.CUDAGraph()
+                # relaxed: the library's host-side set-up calls (kernel attributes) are not stream work
+                with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                    self.layer(U)
+                self.graphs.append(g)
+                per = {}
+                for s in self.stages:
+                    gs = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gs, stream=cap, capture_error_mode="relaxed"):
+                        self.run_stage(s, U)
+                    per[s] = gs
+                self.stage_graphs.append(per)
+        except RuntimeError as exc:  # time eager launches instead, and say so
+            self.graphs, self.stage_graphs = [], []
+            self.graph_error = str(exc).splitlines()[0][:200]
+            torch.cuda.synchronize(dev)
+
+    def step(self, i):
+        if self.graphs:
+            self.graphs[i % self.n_rot].replay()
+        else:
+            self.layer(self.pool[i % self.n_rot])
+
+    def stage_step(self, i, ev):
+        """Step i with an event before each stage and after the last (device time of each stage)."""
+        b = i % self.n_rot
+        for j, s in enumerate(self.stages):
+            ev[j].record()
+            if self.stage_graphs:
+                self.stage_graphs[b][s].replay()
+            else:
+                self.run_stage(s, self.pool[b])
+        ev[len(self.stages)].record()
+
+    def time_steps(self, K, warmup):
+        """Milliseconds of exactly K steps (after `warmup` untimed ones), barriers on both sides."""
+        for i in range(warmup):
+            self.step(i)
+        barrier(self.device)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for i in range(K):
+            self.step(i)
+        t1.record()
+        barrier(self.device)
+        return t0.elapsed_time(t1)
+
+    def time_stages(self, K):
+        """Per stage, the median device time over K steps run stage graph by stage graph."""
+        n = len(self.stages)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(K)]
+        for i in range(min(K, 3)):
+            self.stage_step(i, evs[i])  # warm-up of the stage graphs
+        torch.cuda.synchronize(self.device)
+        for i in range(K):
+            self.stage_step(i, evs[i])
+        torch.cuda.synchronize(self.device)
+        return {s: statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                for j, s in enumerate(self.stages)}
+
+    def work(self, K):
+        A_mean = sum(self.A_of[i % self.n_rot] for i in range(K)) / K
+        act_mean = sum(self.act_of[i % self.n_rot] for i in range(K)) / K
+        return A_mean, act_mean, stage_work(self.w, A_mean, act_mean, self.fp8, self.gather)
+
+
+def stage_report(stage_ms, work, peaks):
+    stages = {}
+    for name, m in stage_ms.items():
+        wk = work[name]
+        gbs = wk["bytes"] / (m * 1e-3) / 1e9
+        d = {"ms": round(m, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        if wk["flops"]:
+            tf = wk["flops"] / (m * 1e-3) / 1e12
+            d["TFLOP/s"] = round(tf, 2)
+            d["frac_tensor"] = round(tf / peaks["bf16_tflops"], 4)
+        stages[name] = d
+    return stages
+
+
+def roofline(w: W.Workload, work, ffn_ms, A_mean, peaks, peak_src, fp8=False):
+    """The dominant kernel's roofline: the grouped expert GEMM (both launches of one step)."""
+    ffn = work["ffn"]
+    intensity = ffn["flops"] / max(ffn["bytes"], 1)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if w.dtype == W.F32:
+        # float32 CUDA-core FMA peak: 148 SMs x 128 lanes x 2 FLOP x 2.032 GHz
+        roof = {"bound": "alu", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12,
+                "peak": 148 * 128 * 2 * 2.032e9 / 1e12, "unit": "TFLOP/s"}
+    elif fp8 and intensity >= ridge * 1.5:
+        # gate|up (4 A h d FLOPs) at twice the bf16 rate (the recipe's nominal fp8 : bf16 ratio) and
+        # down (2 A h d) at the bf16 rate: the peak is the FLOPs over the time both take at peak,
+        # 1.5x the bf16 rate, and so is the ridge
+        f1, f2 = 4 * A_mean * w.h * w.d_e, 2 * A_mean * w.h * w.d_e
+        mixed = (f1 + f2) / (f1 / (2 * peaks["bf16_tflops"]) + f2 / peaks["bf16_tflops"]) if f1 + f2 else 1.0
+        roof = {"bound": "tensor", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12, "peak": round(mixed, 1),
+                "unit": "TFLOP/s"}
+    elif intensity >= ridge:
+        roof = {"bound": "tensor", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": ffn["bytes"] / (ffn_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    if roof["bound"] == "tensor" and not fp8:
+        # the same against the bf16 rate measured under the power cap in a seconds-long loop
+        roof["peak_sustained"] = peaks["bf16_tflops_sustained"]
+        roof["frac_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
+    roof["achieved"] = round(roof["achieved"], 2)
+    roof["traffic"] = None if fp8 else profile_traffic(w.name)
+    tiles = ffn_tiles(w)
+    kname = ("ffn_simt_f32" if w.dtype == W.F32 else "grouped_gemm_swab" if tiles.startswith("swab")
+             else "grouped_gemm_tc_pair" if tiles.startswith("pair") else "grouped_gemm_tc")
+    roof["kernel"] = f"grouped SwiGLU expert GEMM ({tiles} tiles: {kname}) gate|up + down, both launches of one step"
+    roof["peak_source"] = f"{peak_src}, {'bf16 burst' if roof['bound'] == 'tensor' else roof['bound']}"
+    roof["timing"] = "median CUDA-event time of the ffn stage graph over the timed steps"
+    if fp8:
+        roof["kernel"] = ("grouped SwiGLU expert GEMM: E4M3 gate|up (kind::f8f6f4) + bf16 down, both launches of "
+                          "one step")
+        if roof["bound"] == "tensor":
+            roof["peak_source"] += ("; E4M3 gate|up at 2x the measured bf16 burst (nominal ratio), combined with "
+                                    "bf16 down by their FLOPs")
+    return roof
+
+
+def measure(run: LayerRun, K: int, warmup: int, repeats: int):
+    """value (median over `repeats` regions of exactly K steps), stage device times, roofline."""
+    run.batch_stats()
+    run.capture()
+    regions = [run.time_steps(K, warmup if r == 0 else 1) for r in range(repeats)]
+    stage_ms = run.time_stages(K)
+    return regions, stage_ms
+
+
+def per_config_entry(w: W.Workload, device, K: int, warmup: int, repeats: int, peaks, peak_src):
+    run = LayerRun(w, device)
+    regions, stage_ms = measure(run, K, warmup, repeats)
+    ms = statistics.median(regions)
+    A_mean, act_mean, work = run.work(K)
+    d = {"workload": w.name, "value": round(w.T * K / (ms * 1e-3), 1), "unit": "tokens/s",
+         "ms_per_step": round(ms / K, 5), "steps": K, "repeats": repeats,
+         "value_range": [round(w.T * K / (max(regions) * 1e-3), 1), round(w.T * K / (min(regions) * 1e-3), 1)],
+         "roofline": roofline(w, work, stage_ms["ffn"], A_mean, peaks, peak_src),
+         "stages": stage_report(stage_ms, work, peaks),
+         "stage_sum_ms": round(sum(stage_ms.values()), 5),
+         "kept_pairs_A": A_mean, "active_experts": act_mean,
+         "launch": "one CUDA graph replay per step" if run.graphs else "eager stage calls",
+         "config": workload_config(w, run.n_rot)}
+    del run
+    torch.cuda.empty_cache()
+    return d
+
+
 def run_b300(args, w: W.Workload):
     ws_n, rank, local = init_dist("nccl")
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    from mixture_experts_layer_84_b300 import _lib as L
+    L = None
+    from mixture_experts_layer_84_b300 import _lib as L  # noqa: F811
 
-    inp = synth.generate(w, seed=0, device=device)
-    ubytes = w.T * w.h * w.elem_bytes
-    n_rot = max(2, min(64, math.ceil(2 * L2_BYTES / max(ubytes, 1))))
-    pool = [inp.U] + [synth.normal((w.T, w.h), 1.0, 100 + r, "U", device, w.torch_dtype) for r in range(n_rot - 1)]
-    cfg = L.config_of(w)
-    fp8 = args.fp8
-    if fp8 and (w.dtype != W.BF16 or w.h % 16):
-        raise SystemExit("bench.py --fp8: needs a bf16 workload with h % 16 == 0")
-    gather = args.gather and not fp8 and w.dtype == W.BF16
-    bufs = L.LayerBuffers.allocate(cfg, device=device, with_X=not (fp8 or gather))
-    w8 = L.FP8Weights.quantize(inp.W_gate, inp.W_up) if fp8 else None  # once, outside every timed region
-    rows8 = L.FP8Rows.allocate(cfg, device=device) if fp8 else None
-
-    def stage_calls(U, ev=None):
-        # the stage calls of moe_layer_forward (or moe_layer_forward_fp8), with events between them
-        L.moe_route(cfg, U, inp.W_r, inp.b_r, inp.W_noise, inp.eps, None, None, bufs.idx, bufs.gate, bufs.ws,
-                    sel_bias=inp.sel_bias)
-        if ev is not None:
-            ev[0].record()
-        if fp8:
-            L.moe_dispatch_fp8(cfg, U, bufs.idx, bufs.counts_routed, bufs.counts_kept, bufs.offsets, bufs.slot_row,
-                               bufs.row_token, rows8.X8, rows8.x_scale, bufs.n_dropped, bufs.ws)
-        else:  # gather: routing metadata only, the first GEMM reads the token rows itself
-            L.moe_dispatch(cfg, U, bufs.idx, bufs.counts_routed, bufs.counts_kept, bufs.offsets, bufs.slot_row,
-                           bufs.row_token, None if gather else bufs.X, bufs.n_dropped, bufs.ws)
-        if ev is not None:
-            ev[1].record()
-        if fp8:
-            L.moe_expert_ffn_fp8(cfg, rows8.X8, rows8.x_scale, bufs.offsets, w8, inp.W_down, bufs.act, bufs.Y,
-                                 bufs.ws)
-        elif gather:
-            L.moe_expert_ffn_gather(cfg, U, bufs.row_token, bufs.offsets, inp.W_gate, inp.W_up, inp.W_down, bufs.act,
-                                    bufs.Y, bufs.ws)
-        else:
-            L.moe_expert_ffn(cfg, bufs.X, bufs.offsets, inp.W_gate, inp.W_up, inp.W_down, bufs.act, bufs.Y, bufs.ws)
-        if ev is not None:
-            ev[2].record()
-        if w.n_shared:
-            L.moe_shared_ffn(cfg, U, inp.W_gate_sh, inp.W_up_sh, inp.W_down_sh, bufs.act_shared, bufs.Y_shared,
-                             bufs.ws)
-        if ev is not None:
-            ev[3].record()
-        L.moe_combine(cfg, U, bufs.Y, bufs.slot_row, bufs.gate, bufs.counts_routed, bufs.out, bufs.f, bufs.P,
-                      bufs.aux, bufs.ws, z_loss=bufs.z_loss, Y_shared=bufs.Y_shared)
-
-    # kept pairs and active experts of each batch (outside any timed region)
-    A_of, act_of = [], []
-    for U in pool:
-        stage_calls(U)
-        off = bufs.offsets.cpu()
-        A_of.append(int(off[-1]))
-        act_of.append(int(((off[1:] - off[:-1]) > 0).sum()))
-    code = L.moe_get_device_status(bufs.ws)
-    if code != 0:
-        raise SystemExit(f"bench.py: device status {code} during warm-up")
-
+    run = LayerRun(w, device, fp8=args.fp8, gather=args.gather)
+    fp8, inp, cfg, bufs, pool, n_rot = run.fp8, run.inp, run.cfg, run.bufs, run.pool, run.n_rot
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    peaks, peak_src = measured_peaks()
+
+    run.batch_stats()
     clocks = ClockSampler(device) if rank == 0 else None
     barrier(device)
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    # one CUDA graph per rotating token batch: the whole moe_layer_forward (the stage calls in
-    # order), replayed as one launch per step
-    graphs, graph_error = [], None
-    if not args.no_graph:
-        cap = torch.cuda.Stream(device)
-        cap.wait_stream(torch.cuda.current_stream(device))
-        with torch.cuda.stream(cap):
-            stage_calls(pool[0])  # first calls on this stream outside the capture
-        torch.cuda.current_stream(device).wait_stream(cap)
-        torch.cuda.synchronize(device)
-        try:
-            for U in pool:
-                g = torch.cuda.CUDAGraph()
-                # relaxed: the library's host-side set-up calls (kernel attributes) are not stream work
-                with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
-                    stage_calls(U)
-                graphs.append(g)
-        except RuntimeError as exc:  # time eager launches instead, and say so
-            graphs, graph_error = [], str(exc).splitlines()[0][:200]
-            torch.cuda.synchronize(device)
-
-    def step(i):
-        if graphs:
-            graphs[i % n_rot].replay()
-        else:
-            stage_calls(pool[i % n_rot])
-
-    # warm-up right before the timed region, so the clocks are at load when timing starts
-    for i in range(args.warmup):
-        step(i)
-    barrier(device)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record()
-    for i in range(K):
-        step(i)
-    t_end.record()
-    barrier(device)
-    total_ms = t_start.elapsed_time(t_end)
-
-    # the stage breakdown: the same steps again, the stage calls issued one by one with events
-    # between them (not part of `value`)
-    for i in range(K):
-        starts[i].record()
-        stage_calls(pool[i % n_rot], evs[i])
-        ends[i].record()
-    torch.cuda.synchronize(device)
+    run.capture(not args.no_graph)
+    # R regions of exactly K steps each (the first after the warm-up); `value` is the median region
+    regions = [run.time_steps(K, args.warmup if r == 0 else 1) for r in range(args.repeats)]
+    stage_ms = run.time_stages(K)
 
     # end to end through the public call: every step copies its tokens in from pinned host memory,
     # runs moe_layer_forward and reads out (and aux) back.  Three streams pipeline the steps: the
@@ -546,8 +696,8 @@ def run_b300(args, w: W.Workload):
             s_comp.wait_event(ev_in[b])
             s_comp.wait_event(ev_out[b])           # out[b] of two steps back has been read
             if fp8:
-                L.moe_layer_forward_fp8(cfg, U_dev[b], inp.W_r, inp.b_r, inp.W_noise, inp.eps, w8, inp.W_down,
-                                        bset[b], rows8, stream=s_comp, sel_bias=inp.sel_bias, shared=inp.shared)
+                L.moe_layer_forward_fp8(cfg, U_dev[b], inp.W_r, inp.b_r, inp.W_noise, inp.eps, run.w8, inp.W_down,
+                                        bset[b], run.rows8, stream=s_comp, sel_bias=inp.sel_bias, shared=inp.shared)
             else:
                 L.moe_layer_forward(cfg, U_dev[b], inp.W_r, inp.b_r, inp.W_noise, inp.eps, inp.W_gate, inp.W_up,
                                     inp.W_down, bset[b], stream=s_comp, sel_bias=inp.sel_bias, shared=inp.shared)
@@ -600,89 +750,27 @@ def run_b300(args, w: W.Workload):
         code = L.moe_get_device_status(fb.ws)
         if code != 0:
             raise SystemExit(f"bench.py: device status {code} after the backward")
-        A0 = A_of[0]
+        A0 = run.A_of[0]
         bwd_flops = 12 * A0 * w.h * w.d_e + 2 * 6 * w.T * w.h * w.E  # experts (2x the forward) + router
         if w.n_shared:
             bwd_flops += 12 * w.T * w.h * w.d_shared * w.n_shared
+        step_ms = statistics.median(regions) / K
         train = {"backward_ms": round(bwd_ms, 4), "steps": KB,
-                 "forward_plus_backward_tokens_per_s": round(w.T / ((total_ms / K + bwd_ms) * 1e-3), 1),
+                 "forward_plus_backward_tokens_per_s": round(w.T / ((step_ms + bwd_ms) * 1e-3), 1),
                  "backward_TFLOP/s": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 2),
                  "what": "moe_layer_backward: combine, gate/aux/z, grouped expert backward (recomputed gate|up), "
                          "router linear, permute; float32 weight gradients"}
         del fb, grads
 
+    total_ms = statistics.median(regions)
     max_ms = max_over_ranks(total_ms, device)
     max_e2e = max_over_ranks(e2e_s, device)
     if rank != 0:
         return 0
 
-    stage_ms = {"route": [], "dispatch": [], "ffn": [], "combine": []}
-    if w.n_shared:
-        stage_ms["shared_ffn"] = []
-    for i in range(K):
-        e = evs[i]
-        stage_ms["route"].append(starts[i].elapsed_time(e[0]))
-        stage_ms["dispatch"].append(e[0].elapsed_time(e[1]))
-        stage_ms["ffn"].append(e[1].elapsed_time(e[2]))
-        if w.n_shared:
-            stage_ms["shared_ffn"].append(e[2].elapsed_time(e[3]))
-        stage_ms["combine"].append(e[3].elapsed_time(ends[i]))
-    A_mean = sum(A_of[i % n_rot] for i in range(K)) / K
-    act_mean = sum(act_of[i % n_rot] for i in range(K)) / K
-    work = stage_work(w, A_mean, act_mean, fp8, gather)
-    peaks, peak_src = measured_peaks()
-    stages = {}
-    for name, ms in stage_ms.items():
-        m = sum(ms) / len(ms)
-        wk = work[name]
-        gbs = wk["bytes"] / (m * 1e-3) / 1e9
-        d = {"ms": round(m, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
-        if wk["flops"]:
-            tf = wk["flops"] / (m * 1e-3) / 1e12
-            d["TFLOP/s"] = round(tf, 2)
-            d["frac_tensor"] = round(tf / peaks["bf16_tflops"], 4)
-        stages[name] = d
-
-    ffn_ms = sum(stage_ms["ffn"]) / K
-    ffn = work["ffn"]
-    intensity = ffn["flops"] / max(ffn["bytes"], 1)
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if w.dtype == W.F32:
-        # float32 CUDA-core FMA peak: 148 SMs x 128 lanes x 2 FLOP x 2.032 GHz
-        roof = {"bound": "alu", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12,
-                "peak": 148 * 128 * 2 * 2.032e9 / 1e12, "unit": "TFLOP/s"}
-    elif fp8 and intensity >= ridge * 1.5:
-        # gate|up (4 A h d FLOPs) at twice the bf16 rate (the recipe's nominal fp8 : bf16 ratio) and
-        # down (2 A h d) at the bf16 rate: the peak is the FLOPs over the time both take at peak,
-        # 1.5x the bf16 rate, and so is the ridge
-        f1, f2 = 4 * A_mean * w.h * w.d_e, 2 * A_mean * w.h * w.d_e
-        mixed = (f1 + f2) / (f1 / (2 * peaks["bf16_tflops"]) + f2 / peaks["bf16_tflops"]) if f1 + f2 else 1.0
-        roof = {"bound": "tensor", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12, "peak": round(mixed, 1),
-                "unit": "TFLOP/s"}
-    elif intensity >= ridge:
-        roof = {"bound": "tensor", "achieved": ffn["flops"] / (ffn_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": ffn["bytes"] / (ffn_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    if roof["bound"] == "tensor" and not fp8:
-        # the same against the bf16 rate measured under the power cap in a seconds-long loop
-        roof["peak_sustained"] = peaks["bf16_tflops_sustained"]
-        roof["frac_sustained"] = round(roof["achieved"] / peaks["bf16_tflops_sustained"], 4)
-    roof["achieved"] = round(roof["achieved"], 2)
-    roof["traffic"] = None if fp8 else profile_traffic(w.name)
-    roof["kernel"] = (f"grouped SwiGLU expert GEMM ({ffn_tiles(w)} tiles: "
-                      f"{'grouped_gemm_swab' if ffn_tiles(w).startswith('swab') else 'grouped_gemm_tc'}) "
-                      "gate|up + down, both launches of one step")
-    roof["peak_source"] = f"{peak_src}, {'bf16 burst' if roof['bound'] == 'tensor' else roof['bound']}"
-    if fp8:
-        roof["kernel"] = ("grouped SwiGLU expert GEMM: grouped_gemm_tc<true, true> E4M3 gate|up (kind::f8f6f4) + "
-                          "bf16 down, both launches of one step")
-        if roof["bound"] == "tensor":
-            roof["peak_source"] += ("; E4M3 gate|up at 2x the measured bf16 burst (nominal ratio), combined with "
-                                    "bf16 down by their FLOPs")
-
+    A_mean, act_mean, work = run.work(K)
+    stages = stage_report(stage_ms, work, peaks)
+    roof = roofline(w, work, stage_ms["ffn"], A_mean, peaks, peak_src, fp8)
     value = weak_scaling_value(w.T, K, ws_n, max_ms * 1e-3)
     e2e_value = weak_scaling_value(w.T, K, ws_n, max_e2e)
     line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_n, "steps": K,
@@ -692,20 +780,31 @@ def run_b300(args, w: W.Workload):
             "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights, device-resident)",
             "config": dict(workload_config(w, n_rot), **({"fp8": "E4M3 token rows and gate/up weight rows, "
                                                                   "one power-of-two scale per row"} if fp8 else {}),
-                           **({"x": "not materialised: the first GEMM gathers U rows"} if gather else {})),
+                           **({"x": "not materialised: the first GEMM gathers U rows"} if run.gather else {})),
+            "repeats": args.repeats,
+            "value_range": [round(weak_scaling_value(w.T, K, ws_n, max(regions) * 1e-3), 1),
+                            round(weak_scaling_value(w.T, K, ws_n, min(regions) * 1e-3), 1)],
             "roofline": roof, "stages": stages,
+            "stage_timing": "device time of each stage's own CUDA graph, replayed in layer order with events between "
+                            "them, median over the K steps",
+            "stage_sum_ms": round(sum(stage_ms.values()), 5),
             "kept_pairs_A": A_mean, "active_experts": act_mean,
             "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.h * w.elem_bytes,
                     "d2h_bytes_per_step": w.T * w.h * w.elem_bytes + 4,
                     "how": f"moe_layer_forward{'_fp8' if fp8 else ''} per step with its U copied in from pinned host memory and out + aux "
                            "copied back; copy-in, layer and copy-out of consecutive steps overlap on three streams"},
-            "gpu_launches": launches_per_step(w, gather) * K,
-            "launch": "one CUDA graph replay per step (the whole layer)" if graphs else
-                      ("eager stage calls" + (f" (graph capture failed: {graph_error})" if graph_error else "")),
+            "gpu_launches": launches_per_step(w, run.gather) * K,
+            "launch": "one CUDA graph replay per step (the whole layer)" if run.graphs else
+                      ("eager stage calls" + (f" (graph capture failed: {run.graph_error})" if run.graph_error else "")),
             "clocks": clk}
     if train:
         line["train_step"] = train
+    del run, bset, U_dev
+    torch.cuda.empty_cache()
+    if ws_n == 1 and not args.no_per_config and not fp8 and not args.gather:
+        line["per_config"] = [per_config_entry(x, device, K, args.warmup, args.repeats, peaks, peak_src)
+                              for x in W.FULL if x.name != w.name]
     if ws_n == 1 and not args.no_cpu_baseline and not fp8:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample_tokens)
     print(json.dumps(line), flush=True)
@@ -715,12 +814,14 @@ def run_b300(args, w: W.Workload):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=W.MIXTRAL.name, choices=sorted(W.BY_NAME))
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--repeats", type=int, default=5, help="timed regions of exactly --steps steps; value = median")
+    ap.add_argument("--workload", default=W.STRESS.name, choices=sorted(W.BY_NAME))
     ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time the named workload only")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the layer backward")
     ap.add_argument("--gather", action="store_true",
@@ -731,6 +832,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("bench.py: --warmup must be >= 3")
+    if args.repeats < 1:
+        raise SystemExit("bench.py: --repeats must be >= 1")
     w = W.BY_NAME[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -208,8 +208,11 @@ moe_status moe_dispatch(const moe_config* cfg, const void* U, const int32_t* idx
  *            streams with no ordering between them) race on the array and give
  *            wrong results: order them on one stream or with events.
  *   First call per device: it looks up the array's device address on the
- *            current device (cudaGetSymbolAddress) and caches it.  Make that
- *            first call before any stream capture begins.
+ *            current device (cudaGetSymbolAddress) and caches it with the id of
+ *            the current context.  Make that first call before any stream
+ *            capture begins.  A call from another context (after
+ *            cudaDeviceReset, or with a context the caller made current) looks
+ *            the address up again; make such a call outside stream capture too.
  *   The current device must be the device that `stream` and every pointer
  *   belong to. */
 #define MOE_NOALLOC_HIST_MAX (1 << 20)

@@ -25,6 +25,8 @@
 //                    Skipped when X is NULL: the FP8 dispatch (fp8.cu) copies
 //                    quantised rows instead, and the gathered first GEMM reads
 //                    the rows of U itself.
+#include <cuda.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -298,21 +300,51 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 int32_t* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};  // unique id of the context the address belongs to
 
-// Device address of g_noalloc_hist on the current device, looked up once per
-// device.  In host code the array's name is only a host-side stand-in, so the
-// kernels get this address, never the name.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (ids are never reused within a process, so
+// a device reset or a switch to another context shows up as a new id); 0 if there is none.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_noalloc_hist in the current context.  In host code the array's name is only
+// a host-side stand-in, so the kernels get this address, never the name.  It is looked up once per
+// device and kept with the id of the context it was found in; a call from another context (after
+// a device reset, or with a context the caller made current) looks it up again.
 cudaError_t noalloc_hist_ptr(int32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_hist);
     if (e != cudaSuccess) return e;
     g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+    g_noalloc_ctx[dev] = current_context_id();  // the lookup made the device's context current
   }
   *out = g_noalloc_ptr[dev];
   return cudaSuccess;

@@ -97,6 +97,12 @@ SMALL = [TINY_FP32, MIXTRAL_SMALL, SWITCH_SMALL, DSV3_SMALL, STRESS_SMALL]
 # Mixtral-shaped with a quarter of d_e: the same kernels and tiles with about
 # 1 GB on the device, for detailed hardware-counter captures.
 MIXTRAL_NARROW = MIXTRAL.replace(name="mixtral_narrow_bf16", d_e=3584)
+# The Switch shape with a quarter of d_e (the same 128 segments of at most 128 tokens, 0.8 GB of
+# expert weights) and the stress shape with 12288 tokens (segments of about 1150 rows, the CTA-pair
+# row tiles, 3.5 GB on the device): small cases of those kernels for hardware-counter captures.
+SWITCH_NARROW = SWITCH.replace(name="switch_narrow_bf16", d_e=1024)
+STRESS_NARROW = STRESS.replace(name="stress_narrow_bf16", T=12288)
+NARROW = [MIXTRAL_NARROW, SWITCH_NARROW, STRESS_NARROW]
 
-BY_NAME = {w.name: w for w in FULL + SMALL + EXTENDED + [MIXTRAL_NARROW, DSV3_SHARED_SMALL]}
+BY_NAME = {w.name: w for w in FULL + SMALL + EXTENDED + NARROW + [DSV3_SHARED_SMALL]}
 

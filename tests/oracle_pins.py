@@ -346,6 +346,29 @@ def pin_sampled_matches_full(O):
         assert np.allclose(y, res["Y"][row], rtol=1e-12, atol=1e-12)
 
 
+def pin_sampled_shared_and_fp8_match_full(O):
+    """sampled_outputs with shared experts, with the FP8 up-projection, and with both, equals
+    layer_forward's out and Y rows, row by row, on a small case with drops (dropped tokens
+    sampled too)."""
+    rng = _rng(12)
+    T, h, E, k, d_e, d_s = 60, 16, 6, 2, 12, 10
+    inp = _small_layer(rng, T, h, E, k, d_e)
+    shared = (rng.normal(size=(2, d_s, h)) * 0.3, rng.normal(size=(2, d_s, h)) * 0.3,
+              rng.normal(size=(2, h, d_s)) * 0.3)
+    for kw in (dict(shared=shared), dict(fp8=True), dict(shared=shared, fp8=True)):
+        res = O.layer_forward(inp, T=T, h=h, E=E, k=k, d_e=d_e, score_fn=0, renorm=True, capacity_factor=0.8,
+                              **kw)
+        assert res["n_dropped"] > 0
+        sr = np.asarray(res["slot_row"]).reshape(T, k)
+        dropped = [int(t) for t in np.nonzero(np.any(sr < 0, axis=1))[0][:3]]
+        toks = sorted(set([0, 9, 31, T - 1] + dropped))
+        smp = O.sampled_outputs(inp, toks, res["idx"], res["gate"], res["slot_row"], k, **kw)
+        assert np.allclose(smp["out"], res["out"][toks], rtol=1e-12, atol=1e-12), kw.keys()
+        assert smp["Y"], kw.keys()
+        for row, y in smp["Y"].items():
+            assert np.allclose(y, res["Y"][row], rtol=1e-12, atol=1e-12), kw.keys()
+
+
 # ---------------------------------------------------------------- statistics
 
 def pin_aux_balance(O):

@@ -208,6 +208,8 @@ def test_router_input_backward_narrow_rows(E, noisy):
     assert L.moe_get_device_status(ws) == 0
     # the library rounds dH (and dN) to bf16 for the tensor-core products
     ref = oracle.router_input_backward(inp.U, inp.W_r, oracle.f64(dH.bfloat16()), inp.W_noise, inp.eps)
-    assert normwise(dW_r, ref["dW_r"]) <= 2e-2
+    err = normwise(dW_r, ref["dW_r"])
+    assert err <= 2e-2, err
     if noisy:
-        assert normwise(dW_n, ref["dW_noise"]) <= 3e-2
+        err = normwise(dW_n, ref["dW_noise"])
+        assert err <= 2e-2, err

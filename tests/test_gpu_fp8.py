@@ -156,8 +156,16 @@ def test_layer_forward_fp8_full_size_sampled():
     bufs, rows = _run_layer_fp8(w, inp)
     r = route_of(w, H, inp.sel_bias)
     assert np.array_equal(bufs.idx.cpu().numpy(), r["idx"])
+    # the drops and slots come from the oracle's own dispatch, checked against the library first
+    C = oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.capacity)
+    d = oracle.dispatch(r["idx"], w.E, C, w.priority)
+    assert np.array_equal(bufs.slot_row.cpu().numpy(), d["slot_row"])
+    assert np.array_equal(bufs.offsets.cpu().numpy(), d["offsets"])
     toks = np.unique(np.concatenate([[0, w.T - 1], np.random.default_rng(0).choice(w.T, size=24, replace=False)]))
-    smp = oracle.sampled_outputs(inp, toks, r["idx"], r["gate"], bufs.slot_row.cpu().numpy(), w.k, fp8=True)
+    dropped = np.nonzero(np.any(d["slot_row"].reshape(w.T, w.k) < 0, axis=1))[0]
+    if dropped.size:
+        toks = np.unique(np.concatenate([toks, dropped[:4]]))
+    smp = oracle.sampled_outputs(inp, toks, r["idx"], r["gate"], d["slot_row"], w.k, fp8=True)
     tt = torch.as_tensor(toks, device="cuda")
     assert normwise(bufs.out[tt], smp["out"]) <= TOL_BF16
     assert delta_error(bufs.out[tt], inp.U[tt], smp["out"], W.BF16) <= TOL_BF16

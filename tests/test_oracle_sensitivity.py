@@ -224,7 +224,22 @@ def _quantize_rows_scale_up(A):
     return codes, s + 1
 
 
+def _sampled_without_shared(inp, tokens, idx, gate, slot_row, k, shared=None, fp8=False):
+    return _orig["sampled_outputs"](inp, tokens, idx, gate, slot_row, k, None, fp8)
+
+
+def _sampled_fp8_weights_unquantised(inp, tokens, idx, gate, slot_row, k, shared=None, fp8=False):
+    if not fp8:
+        return _orig["sampled_outputs"](inp, tokens, idx, gate, slot_row, k, shared, False)
+    # the token rows are quantised, the gate/up weights are not
+    U_q = O.dequantize_rows_fp8(*O.quantize_rows_fp8(np.asarray(inp.U, dtype=np.float64)))
+    sub = type(inp)(**dict(vars(inp), U=U_q))
+    return _orig["sampled_outputs"](sub, tokens, idx, gate, slot_row, k, shared, False)
+
+
 MUTANTS = {
+    "sampled_shared_term_dropped": ("sampled_outputs", _sampled_without_shared),
+    "sampled_fp8_weights_not_quantised": ("sampled_outputs", _sampled_fp8_weights_unquantised),
     "gates_not_renormalised": ("gates", _gates_no_renorm),
     "ties_to_higher_id": ("topk_select", _topk_ties_high),
     "capacity_floor": ("capacity", _capacity_floor),

@@ -72,6 +72,29 @@ def test_noalloc_dispatch_matches_dispatch_on_two_calls_in_a_row():
             assert torch.equal(a, b), f"call {n}: {name} differs from moe_dispatch"
 
 
+@pytest.mark.gpu
+def test_noalloc_dispatch_without_a_status_word():
+    """status = NULL: device-side errors go unreported, the results are still moe_dispatch's."""
+    T, h, E, k = 5000, 128, 16, 2
+    cfg = L.config(T, h, E, k, 8, capacity=400, capacity_factor=0.0, dtype=W.BF16)
+    U = synth.random_rows(T, h, seed=7, stream="X", device="cuda", dtype=torch.bfloat16)
+    idx = synth.random_routing(T, E, k, seed=7, device="cuda", zipf_s=0.8)
+    ref = _buffers(T, E, k, h, torch.bfloat16)
+    ws = L.new_workspace(cfg)
+    L.moe_dispatch(cfg, U, idx, *_args(ref), ws)
+    assert L.moe_get_device_status(ws) == 0
+    got = _buffers(T, E, k, h, torch.bfloat16)
+    L.moe_dispatch_noalloc(cfg, U, idx, *_args(got), None)
+    torch.cuda.synchronize()
+    A = int(ref["offsets"][-1].item())
+    assert int(ref["n_dropped"].item()) > 0
+    for name in OUTPUTS:
+        a, b = got[name], ref[name]
+        if name in ("row_token", "X"):
+            a, b = a[:A], b[:A]
+        assert torch.equal(a, b), f"{name} differs from moe_dispatch"
+
+
 def test_noalloc_dispatch_rejects_sizes_beyond_its_static_scratch():
     # ceil(T*k / 4096) * E = 1025 * 1024 > 2^20 histogram entries: refused on the host, before any
     # CUDA call, so no pointer is needed
