@@ -224,95 +224,50 @@ class _Inp:
         self.__dict__.update(kw)
 
 
-class ExpertsF64:
-    """One kind of expert weight, widened to float64 expert by expert: once and kept (cache=True), or
-    on every use (the oracle's own conversion, for models whose float64 weights would not fit)."""
-
-    def __init__(self, W_all, preload=(), cache=True):
-        self.W = W_all
-        self.use_cache = cache
-        self.cache = {}
-        for e in preload:
-            self[e]
-
-    def __len__(self):
-        return len(self.W)
-
-    def __getitem__(self, e):
-        import oracle
-        e = int(e)
-        if not self.use_cache:
-            return oracle.f64(self.W[e])
-        if e not in self.cache:
-            self.cache[e] = oracle.f64(self.W[e])
-        return self.cache[e]
-
-
-F64_CACHE_BYTES = 24e9  # expert weights are widened once when their float64 copy fits in this
-
-
-def oracle_inputs_host(inp: "synth.LayerInputs", U_host, experts=(), cache=True):
-    """Host copies for the oracle: token rows as given, router weights widened to float64, expert
-    weights widened beforehand (the listed experts) or by the oracle on every use (cache=False,
-    from host bf16 copies made here, outside any timed region)."""
-    import oracle
-    f = oracle.f64
-    Wg, Wu, Wd = (x if cache else x.cpu() for x in (inp.W_gate, inp.W_up, inp.W_down))
-    return _Inp(U=U_host, W_r=f(inp.W_r), b_r=None if inp.b_r is None else f(inp.b_r),
-                W_noise=None if inp.W_noise is None else f(inp.W_noise),
-                eps=None if inp.eps is None else f(inp.eps),
-                W_gate=ExpertsF64(Wg, experts, cache), W_up=ExpertsF64(Wu, experts, cache),
-                W_down=ExpertsF64(Wd, experts, cache),
-                sel_bias=None if inp.sel_bias is None else f(inp.sel_bias),
-                shared=None if inp.shared is None else tuple(f(x) for x in inp.shared))
-
-
-def touched_experts(w: W.Workload, host, tokens):
-    import numpy as np
-    import oracle
-    H = oracle.router_logits(host.U[tokens], host.W_r, host.b_r, host.W_noise,
-                             None if host.eps is None else host.eps[tokens])
-    r = oracle.route(H, w.k, w.score_fn, w.renorm, host.sel_bias, w.n_group, w.topk_group)
-    return sorted(set(np.unique(r["idx"]).tolist()))
+def oracle_inputs_host(inp: "synth.LayerInputs"):
+    """Host copies of the layer's inputs in their own precision (the oracle widens them to double as
+    it reads them).  Made once, outside every timed region."""
+    def host(x):
+        return None if x is None else x.detach().to("cpu").contiguous()
+    return _Inp(U=host(inp.U), W_r=host(inp.W_r), b_r=host(inp.b_r), W_noise=host(inp.W_noise), eps=host(inp.eps),
+                W_gate=host(inp.W_gate), W_up=host(inp.W_up), W_down=host(inp.W_down), sel_bias=host(inp.sel_bias),
+                shared=None if inp.shared is None else tuple(host(x) for x in inp.shared))
 
 
 def oracle_step(w: W.Workload, host, tokens):
-    """The oracle's whole layer forward on a sample of the batch's tokens."""
+    """The oracle's whole layer forward on a sample of the batch's tokens (its capacity from the
+    sample's own size); returns its per-stage seconds."""
     import oracle
-    sub = _Inp(U=host.U[tokens], W_r=host.W_r, b_r=host.b_r, W_noise=host.W_noise,
-               eps=None if host.eps is None else host.eps[tokens],
-               W_gate=host.W_gate, W_up=host.W_up, W_down=host.W_down)
-    return oracle.layer_forward(sub, T=len(tokens), h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn,
-                                renorm=w.renorm, capacity_factor=w.capacity_factor, capacity_override=w.capacity,
-                                priority=w.priority, sel_bias=host.sel_bias, shared=host.shared,
-                                n_group=w.n_group, topk_group=w.topk_group)
+    t = torch.as_tensor(tokens, dtype=torch.int64)
+    sub = _Inp(U=host.U[t], W_r=host.W_r, b_r=host.b_r, W_noise=host.W_noise,
+               eps=None if host.eps is None else host.eps[t], W_gate=host.W_gate, W_up=host.W_up,
+               W_down=host.W_down)
+    r = oracle.layer_forward(sub, T=len(tokens), h=w.h, E=w.E, k=w.k, d_e=w.d_e, score_fn=w.score_fn,
+                             renorm=w.renorm, capacity_factor=w.capacity_factor, capacity_override=w.capacity,
+                             priority=w.priority, sel_bias=host.sel_bias, shared=host.shared, n_group=w.n_group,
+                             topk_group=w.topk_group)
+    return r["seconds"]
 
 
-def blas_threads() -> int:
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
-        if n:
-            return int(max(n))
-    except Exception:
-        pass
-    return os.cpu_count() or 1
+def stage_seconds_report(totals: dict, n_tokens_total: int):
+    whole = sum(totals.values())
+    return {name: {"s": round(s, 4), "share": round(s / whole, 4) if whole > 0 else 0.0,
+                   "us_per_token": round(s / max(1, n_tokens_total) * 1e6, 2)}
+            for name, s in totals.items()}
+
+
+def oracle_cpu_info():
+    import oracle
+    return {"cores": os.cpu_count() or 1, "threads": oracle.threads()}
 
 
 def cpu_baseline(w: W.Workload, inp, n_tokens: int = 0, target_s: float = 12.0):
-    """The oracle as it stands on the host cores, on a bounded sample of the batch: a probe on a
-    few tokens sets the sample size for about `target_s` seconds of CPU work (all T tokens, run
-    again until that time is reached, when the whole batch is faster)."""
+    """The oracle as it stands on the host cores, on a bounded sample of the batch: a probe on a few
+    tokens sets the sample size for about `target_s` seconds of CPU work (all T tokens, run again
+    until that time is reached, when the whole batch is faster)."""
     import numpy as np
-    import oracle
-    sub_inp = synth.LayerInputs(U=inp.U, W_r=inp.W_r, b_r=inp.b_r, W_noise=inp.W_noise, eps=inp.eps,
-                                W_gate=inp.W_gate, W_up=inp.W_up, W_down=inp.W_down, sel_bias=inp.sel_bias,
-                                W_gate_sh=inp.W_gate_sh, W_up_sh=inp.W_up_sh, W_down_sh=inp.W_down_sh)
-    cache = 3 * w.E * w.h * w.d_e * 8 <= F64_CACHE_BYTES
-    host = oracle_inputs_host(sub_inp, oracle.f64(sub_inp.U), cache=cache)
-    # grow the sample 4x at a time until one call takes a quarter of the target (or is the whole
-    # batch), then repeat that call until the target time is reached (30 s at most)
-    oracle_step(w, host, np.arange(min(w.T, 16)))  # untimed: first-call costs (BLAS threads, page faults)
+    host = oracle_inputs_host(inp)
+    oracle_step(w, host, np.arange(min(w.T, 8)))  # untimed: first-call costs (threads, page faults)
     n = min(w.T, 64)
     while True:
         t0 = time.perf_counter()
@@ -322,18 +277,68 @@ def cpu_baseline(w: W.Workload, inp, n_tokens: int = 0, target_s: float = 12.0):
             break
         n = min(w.T, n * 4)
     toks = np.arange(n)
-    reps, t0 = 0, time.perf_counter()
+    reps, totals, t0 = 0, {}, time.perf_counter()
     while True:
-        oracle_step(w, host, toks)
+        sec = oracle_step(w, host, toks)
+        for name, s in sec.items():
+            totals[name] = totals.get(name, 0.0) + s
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= target_s or dt + dt / reps > 30.0:
             break
-    return {"value": n * reps / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"oracle layer forward (float64 numpy) on the first {n} of the batch's {w.T} tokens, "
-                      f"{reps} call(s) in {dt:.1f} s, expert weights widened to float64 "
-                      + ("beforehand" if cache else "by the oracle on every use (their float64 copy is too large)")
-                      + f"; capacity from those {n} tokens"}
+    info = oracle_cpu_info()
+    return {"value": n * reps / dt, "unit": "tokens/s", "cores": info["threads"], "host_cores": info["cores"],
+            "kind": "oracle",
+            "sample": f"C++ oracle layer forward (plain loops, double accumulation, OpenMP over rows, "
+                      f"{info['threads']} threads) on the first {n} of the batch's {w.T} tokens, {reps} call(s) in "
+                      f"{dt:.1f} s; capacity from those {n} tokens",
+            "stages": stage_seconds_report(totals, n * reps)}
+
+
+def run_reference(args, w: W.Workload):
+    import numpy as np
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    host = oracle_inputs_host(synth.generate(w, seed=0, device="cpu"))
+    budget = float(args.reference_budget_s)
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(w.T, size=min(8, w.T), replace=False))
+    oracle_step(w, host, probe)  # untimed: first-call costs
+    t0 = time.perf_counter()
+    oracle_step(w, host, probe)
+    per_call = time.perf_counter() - t0
+    # a call costs a fixed part (each weight row is read once) plus a part per token: size the sample
+    # from two probes so that warm-up + steps fit the budget
+    probe2 = np.sort(rng.choice(w.T, size=min(64, w.T), replace=False))
+    t0 = time.perf_counter()
+    oracle_step(w, host, probe2)
+    per_call2 = time.perf_counter() - t0
+    per_tok = max((per_call2 - per_call) / max(1, len(probe2) - len(probe)), 1e-6)
+    fixed = max(per_call - per_tok * len(probe), 0.0)
+    per_step = budget / max(1, args.steps + args.warmup)
+    n = int(max(1, min(w.T, (per_step - fixed) / per_tok)))
+    for _ in range(args.warmup):
+        oracle_step(w, host, np.sort(rng.choice(w.T, size=n, replace=False)))
+    totals = {}
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for name, s in oracle_step(w, host, np.sort(rng.choice(w.T, size=n, replace=False))).items():
+            totals[name] = totals.get(name, 0.0) + s
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    info = oracle_cpu_info()
+    sample = (f"each step: the C++ oracle layer forward (plain loops, double accumulation, OpenMP over rows, "
+              f"{info['threads']} threads) on {n} tokens drawn from the {w.T}-token batch")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": info["threads"], "host_cores": info["cores"],
+                             "kind": "oracle", "sample": sample, "stages": stage_seconds_report(totals, n * args.steps)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -364,43 +369,6 @@ def workload_config(w: W.Workload, n_rot: int = 0):
         c["l2"] = (f"inputs larger than L2: {n_rot} rotating token batches plus "
                    f"{3 * w.E * w.h * w.d_e * w.elem_bytes / 1e9:.2f} GB of expert weights per step")
     return c
-
-
-def run_reference(args, w: W.Workload):
-    import numpy as np
-    import oracle
-    ws, rank, _ = dist_env()
-    if rank != 0:
-        return 0
-    inp = synth.generate(w, seed=0, device="cpu")
-    cache = 3 * w.E * w.h * w.d_e * 8 <= F64_CACHE_BYTES
-    host = oracle_inputs_host(inp, oracle.f64(inp.U), range(w.E) if cache else (), cache=cache)
-    budget = float(args.reference_budget_s)
-    rng = np.random.default_rng(0)
-    probe = np.sort(rng.choice(w.T, size=min(4, w.T), replace=False))
-    t0 = time.perf_counter()
-    oracle_step(w, host, probe)
-    per_tok = (time.perf_counter() - t0) / len(probe)
-    n = int(max(1, min(w.T, budget / max(1, args.steps + args.warmup) / max(per_tok, 1e-6))))
-    for _ in range(args.warmup):
-        oracle_step(w, host, np.sort(rng.choice(w.T, size=n, replace=False)))
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step(w, host, np.sort(rng.choice(w.T, size=n, replace=False)))
-    dt = time.perf_counter() - t0
-    value = n * args.steps / dt
-    sample = (f"each step: the oracle layer forward (float64 numpy) on {n} tokens drawn from the "
-              f"{w.T}-token batch; expert weights widened to float64 "
-              + ("beforehand" if cache else "by the oracle on every use (inside the timed steps)"))
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-    return 0
 
 
 # ----------------------------------------------------------------------------- B300 arm

@@ -1,98 +1,35 @@
-"""Plain CPU oracle for the single-GPU MoE layer forward.
+"""Plain CPU oracle of the single-GPU MoE layer: the Python face of oracle/moe_oracle.cpp.
 
-TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
-CPU-baseline leg may import or run this module; the library never does.  It
-shares no code with the CUDA path: it is the method's definition written out
-in float64 numpy, step by step, in the order and notation of the pages.
+TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's CPU legs import or run
+this module; the MoE library never does, and the two share no code.  Every step of the method is
+computed in moe_oracle.cpp (plain C++ loops, double accumulation, OpenMP over independent rows);
+this module only marshals arguments: it makes host copies of the inputs in their own float type
+(float64, float32 or bfloat16, widened exactly in C++), allocates the outputs, calls the library
+through ctypes and returns numpy arrays.
 
-Sources (page title, section):
-  [FFN]  "MoE 与专家并行" (hs-black.github.io/posts/scaling-moe), 从稠密 FFN 到 MoE:
-         SwiGLU FFN(u) = W_down (SiLU(W_gate u) ⊙ W_up u);
-         layer output h'_t = u_t + sum_i g_{i,t} FFN_i(u_t), g = 0 off the top-k.
-  [RTR]  same page, 路由器：打分、top-k、加权求和: H = U W_r; score s = softmax or
-         sigmoid of H; top-k set T_t; gates from the selected scores; the
-         noisy top-k logits H_i = (x W_g)_i + N(0,1) * Softplus((x W_noise)_i);
-         the single-GPU shapes listing (permute by expert, grouped FFN,
-         index_add back into token order).
-  [SCR]  same page, softmax 门控还是 sigmoid 门控: the scoring table (softmax
-         then top-k without renormalisation; softmax then renormalise over the
-         selected; top-k then softmax; sigmoid then renormalise) and the
-         identity top-k-then-softmax == softmax-then-renormalise.
-  [CAP]  same page, 专家容量与丢 token: C = ceil(CF * T * k / E); slots are
-         filled in token order, overflow is dropped and takes the residual
-         only; for top-k every token's first choice is placed before any
-         second choice.
-  [AUX]  same page, 负载均衡辅助损失：推导与梯度: f_i = fraction of assignments to
-         expert i, P_i = (1/T) sum_t s_{i,t}, L_aux = alpha * E * sum_i f_i P_i
-         (this oracle reports E * sum f_i P_i, i.e. alpha = 1); for sigmoid
-         scores P_i uses s'_{i,t} = s_{i,t} / sum_j s_{j,t}.
-  [VIO]  same page, 无辅助损失的负载均衡: MaxVio = (max_i Load_i - mean) / mean.
-  [ZL]   same page, Router z-loss 与数值稳定: L_z = (1/T) sum_t (log sum_j e^{H_{t,j}})^2,
-         the mean square of each token's log-sum-exp of its router logits.
-  [SHR]  same page, 细粒度专家与共享专家 (shared expert isolation, the V3 form):
-         h'_t = u_t + sum_{i<=N_s} FFN^(s)_i(u_t) + sum_{i<=N_r} g_{i,t} FFN^(r)_i(u_t);
-         the shared experts take every token and bypass the router.
-  [LFB]  same page, 无辅助损失的负载均衡: a per-expert bias b_i used only to choose
-         the top-k (s_{i,t} + b_i), the gate stays s_{i,t}; after each batch
-         e_i = mean(c) - c_i and b_i <- b_i + u * sign(e_i).
-  [GRD]  same page, 路由器：打分、top-k、加权求和 (how the router learns): with the
-         upstream gradient delta_t = dL/dh'_t, dL/dg_{i,t} = delta_t^T FFN_i(u_t) for
-         the selected experts, then through dg/dH to the logits; section
-         负载均衡辅助损失：推导与梯度 (梯度往哪推): f is a constant, and
-         d(sum_i f_i P_i)/dH_{t,k} = (1/T) s_k (f_k - sum_i f_i s_i) for softmax,
-         (1/T) s'_k (1 - s_k) (f_k - sum_i f_i s'_i) for sigmoid; section Router
-         z-loss: dL_z/dH_{t,k} = (2/T) LSE(H_t) softmax(H_t)_k.
-  [GRP]  same page, 设备受限与节点受限路由 (node-limited routing, the V3 form): a token
-         may use the experts of at most M nodes, the nodes being ranked by the sum
-         of the K_r/M highest affinities among their experts; the top-k is then
-         taken over the experts of the chosen nodes only.  On one GPU the nodes
-         become n_group equal, contiguous groups of experts (reading below).
-  [FP8]  same page, 低精度通信: DeepSeek-V3 turns the activations that enter the MoE
-         up-projection into FP8 before the dispatch, so that they feed the
-         up-projection's FP8 forward as they are; the scaling factors are
-         integral powers of 2; the combine stays BF16.
-  [BWD]  same page, 专家计算：padding、block-sparse 与 grouped GEMM: the backward of
-         the SwiGLU experts is grouped GEMMs too, one group for the input
-         gradients and one for the weight gradients.
+The sources and the readings the oracle follows are listed in the header of moe_oracle.cpp.
+Every function is pinned by the `-m "not gpu"` tests (worked examples of the pages, closed forms,
+invariants, brute force and textbook special cases).
 
-Readings where the pages are silent (the same readings the library follows):
-  * selection is made on the float32 logits (softmax and sigmoid are strictly
-    increasing, so this is the top-k of the scores without exp-rounding ties);
-    ties go to the lower expert id, both for membership and for rank order;
-  * the logits are rounded to float32 before selection and scoring (the
-    library's logits are float32);
-  * "no capacity limit" means C = T (an expert can receive each token once);
-  * f_i counts the router's assignments before drops and is normalised by T*k;
-  * a dropped assignment contributes nothing and the kept gates are not
-    renormalised; rows inside an expert segment are in slot (priority) order;
-  * group-limited routing ([GRP]) on one GPU: group q holds experts
-    [q*E/n_group, (q+1)*E/n_group); a group's score is the sum of its
-    r = k/topk_group highest affinities (the scores s, or s + b with a
-    loss-free selection bias); the topk_group best groups are kept, ties to
-    the lower group id; the top-k is then taken over the kept groups' experts
-    only (by the usual selection key).  Group selection adds no gradient path;
-  * FP8 ([FP8]) is E4M3 (finite, largest 448, round to nearest even).  Every
-    token row of U and every row (output channel) of W_gate and W_up gets one
-    power-of-two scale 2^s, s the smallest integer >= -127 with
-    amax <= 448 * 2^s; codes = E4M3(x * 2^-s).  The up-projection (gate|up)
-    multiplies the dequantised values codes * 2^s exactly; act, the down
-    projection, the shared experts and the combine stay at the layer's
-    precision (bf16).
-
-Every function here is pinned by the `-m "not gpu"` tests (worked examples of
-the pages, closed forms, invariants, brute force and textbook special cases).
+`Oracle(path)` loads one build of the library; the module-level functions are those of the
+default build, oracle/libmoe_oracle.so, compiled from moe_oracle.cpp with g++ when it is missing
+or older than its source.
 """
 from __future__ import annotations
 
-import math
-from fractions import Fraction
+import ctypes
 
 import numpy as np
+
+from .build_oracle import CXXFLAGS, LIB, SRC, build  # noqa: F401
 
 SOFTMAX = 0
 SIGMOID = 1
 CHOICE_MAJOR = 0
 TOKEN_MAJOR = 1
+E4M3_MAX = 448.0
+
+_DT_F64, _DT_F32, _DT_BF16 = 0, 1, 2
 
 
 def f64(a) -> np.ndarray:
@@ -106,650 +43,597 @@ def f64(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
 
 
-# --------------------------------------------------------------------------
-# Router  [RTR]
-# --------------------------------------------------------------------------
-
-def softplus(x: np.ndarray) -> np.ndarray:
-    """Softplus(x) = ln(1 + e^x), written in the overflow-free form."""
-    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
-
-
-def router_logits(U, W_r, b_r=None, W_noise=None, eps=None) -> np.ndarray:
-    """Router logits H = U W_r (+ per-expert bias) (+ noisy-top-k noise), float64.
-
-    [RTR]: H = U W_r with W_r in R^{h x E}; the noisy router adds
-    N(0,1) * Softplus(U W_noise), with the standard-normal draws eps [T, E]
-    passed in.  The bias b_r [E] is an additive per-expert logit offset.
-    """
-    U = f64(U)
-    H = U @ f64(W_r)
-    if b_r is not None:
-        H = H + f64(b_r)[None, :]
-    if W_noise is not None:
-        H = H + f64(eps) * softplus(U @ f64(W_noise))
-    return H
-
-
-def round_f32(H: np.ndarray) -> np.ndarray:
-    """Round to float32 (returned as float64 holding float32 values)."""
-    return np.asarray(H, dtype=np.float32).astype(np.float64)
-
-
-def topk_select(H32: np.ndarray, k: int, allowed=None) -> np.ndarray:
-    """Top-k expert ids per token, highest first, ties to the lower expert id.
-
-    [RTR] step 2 (select the k highest); the stable sort keeps equal values in
-    increasing expert order.  `allowed` [T, E] (group-limited routing) puts
-    every allowed expert ahead of every other one, whatever the values.
-    """
-    key = -np.asarray(H32, dtype=np.float64)
-    if allowed is None:
-        order = np.argsort(key, axis=1, kind="stable")
-    else:
-        order = np.lexsort((key, ~np.asarray(allowed, dtype=bool)), axis=-1)  # lexsort is stable
-    return order[:, :k].astype(np.int32)
-
-
-def group_scores(aff: np.ndarray, n_group: int, r: int) -> np.ndarray:
-    """[T, n_group]: each contiguous expert group's sum of its r highest affinities.  [GRP]"""
-    aff = np.asarray(aff, dtype=np.float64)
-    T, E = aff.shape
-    grouped = -np.sort(-aff.reshape(T, n_group, E // n_group), axis=2)
-    return grouped[:, :, :r].sum(axis=2)
-
-
-def group_limited_mask(aff: np.ndarray, n_group: int, topk_group: int, k: int) -> np.ndarray:
-    """[T, E] bool: the experts of each token's topk_group highest-scoring groups.
-
-    [GRP]: groups ranked by the sum of their k/topk_group highest affinities,
-    ties to the lower group id.
-    """
-    T, E = np.asarray(aff).shape
-    gs = group_scores(aff, n_group, k // topk_group)
-    best = np.argsort(-gs, axis=1, kind="stable")[:, :topk_group]
-    chosen = np.zeros(gs.shape, dtype=bool)
-    np.put_along_axis(chosen, best, True, axis=1)
-    return np.repeat(chosen, E // n_group, axis=1)
-
-
-def scores(H: np.ndarray, score_fn: int) -> np.ndarray:
-    """Affinities s_{i,t}: softmax over the E experts or independent sigmoids.  [RTR] step 1, [SCR]."""
-    H = np.asarray(H, dtype=np.float64)
-    if score_fn == SOFTMAX:
-        z = np.exp(H - H.max(axis=1, keepdims=True))
-        return z / z.sum(axis=1, keepdims=True)
-    if score_fn == SIGMOID:
-        return 1.0 / (1.0 + np.exp(-H))
-    raise ValueError("score_fn")
-
-
-def gates(s: np.ndarray, idx: np.ndarray, renorm: bool) -> np.ndarray:
-    """Gate values of the selected experts, [T, k].
-
-    [SCR]: g_i = s_i / sum_{j in T_t} s_j when renormalised, g_i = s_i otherwise.
-    """
-    sel = np.take_along_axis(s, np.asarray(idx, dtype=np.int64), axis=1)
-    if renorm:
-        return sel / sel.sum(axis=1, keepdims=True)
-    return sel
-
-
-# --------------------------------------------------------------------------
-# Capacity and dispatch  [CAP]
-# --------------------------------------------------------------------------
-
-def capacity(T: int, E: int, k: int, capacity_factor: float, override: int = 0) -> int:
-    """C = ceil(CF * T * k / E), exact on the float32 value of CF; CF <= 0: C = T."""
-    if override > 0:
-        return int(override)
-    if capacity_factor <= 0:
-        return int(T)
-    cf = Fraction(float(np.float32(capacity_factor)))
-    return int(math.ceil(cf * T * k / E))
-
-
-def priority_order(T: int, k: int, priority: int):
-    """The (token, choice) pairs in the order their slots are filled.
-
-    [CAP]: every token's first choice before any second choice (choice-major,
-    tokens in order within a choice); token-major takes a token's choices
-    together.
-    """
-    if priority == CHOICE_MAJOR:
-        j, t = np.meshgrid(np.arange(k), np.arange(T), indexing="ij")
-    elif priority == TOKEN_MAJOR:
-        t, j = np.meshgrid(np.arange(T), np.arange(k), indexing="ij")
-    else:
-        raise ValueError("priority")
-    return t.reshape(-1), j.reshape(-1)
-
-
-def dispatch(idx: np.ndarray, E: int, C: int, priority: int = CHOICE_MAJOR) -> dict:
-    """Capacity-limited assignment of (token, choice) pairs to expert slots.
-
-    [CAP] + the permute of [RTR]'s shapes listing: walking the pairs in
-    priority order, the n-th pair that chose expert e takes slot n of e; it is
-    kept iff n < C.  Kept rows are packed expert by expert (offsets = the
-    exclusive prefix sum of the kept counts) in slot order, so the row of a
-    kept pair is offsets[e] + slot and row_token[row] is its token.
-    Returns counts_routed [E], counts_kept [E], offsets [E+1], slot [T*k]
-    (slot of pair t*k+j), slot_row [T*k] (-1 when dropped), row_token [A],
-    n_dropped.
-    """
-    idx = np.asarray(idx, dtype=np.int64)
-    T, k = idx.shape
-    t_seq, j_seq = priority_order(T, k, priority)
-    e_seq = idx[t_seq, j_seq]
-    counts_routed = np.bincount(e_seq, minlength=E).astype(np.int64)
-    # rank of each pair among the earlier pairs of the same expert (stable sort keeps priority order)
-    grouped = np.argsort(e_seq, kind="stable")
-    first = np.concatenate([[0], np.cumsum(counts_routed)[:-1]])
-    rank = np.empty(T * k, dtype=np.int64)
-    rank[grouped] = np.arange(T * k) - first[e_seq[grouped]]
-    counts_kept = np.minimum(counts_routed, C)
-    offsets = np.concatenate([[0], np.cumsum(counts_kept)]).astype(np.int64)
-    pair = t_seq * k + j_seq
-    slot = np.empty(T * k, dtype=np.int64)
-    slot[pair] = rank
-    kept = rank < C
-    slot_row = np.full(T * k, -1, dtype=np.int64)
-    slot_row[pair[kept]] = offsets[e_seq[kept]] + rank[kept]
-    A = int(offsets[E])
-    row_token = np.full(A, -1, dtype=np.int64)
-    row_token[slot_row[pair[kept]]] = t_seq[kept]
-    return dict(counts_routed=counts_routed, counts_kept=counts_kept, offsets=offsets,
-                slot=slot, slot_row=slot_row, row_token=row_token,
-                n_dropped=int(T * k - A), C=int(C))
-
-
-def permute(U, row_token: np.ndarray) -> np.ndarray:
-    """X = U[row_token]: the expert inputs, contiguous per expert.  [RTR] shapes listing."""
-    return f64(U)[np.asarray(row_token, dtype=np.int64)]
-
-
-# --------------------------------------------------------------------------
-# Experts and combine  [FFN]
-# --------------------------------------------------------------------------
-
-def silu(x: np.ndarray) -> np.ndarray:
-    """SiLU(x) = x * sigmoid(x)."""
-    with np.errstate(over="ignore"):
-        return x / (1.0 + np.exp(-x))
-
-
-def swiglu(x, W_gate_e, W_up_e, W_down_e):
-    """One expert on rows x [n, h]: returns (FFN(x) [n, h], the SiLU(gate)*up activation [n, d_e]).
-
-    [FFN]: FFN(u) = W_down (SiLU(W_gate u) ⊙ W_up u), W_gate, W_up in R^{d_e x h},
-    W_down in R^{h x d_e}.
-    """
-    x = f64(x)
-    a = silu(x @ f64(W_gate_e).T) * (x @ f64(W_up_e).T)
-    return a @ f64(W_down_e).T, a
-
-
-def expert_ffn(X, offsets, W_gate, W_up, W_down, d_e: int):
-    """Y = the grouped FFN over the expert segments of X (rows offsets[e]..offsets[e+1]).
-
-    [RTR] shapes listing (grouped_ffn) with [FFN]'s expert.
-    """
-    X = f64(X)
-    offsets = np.asarray(offsets, dtype=np.int64)
-    E = len(offsets) - 1
-    Y = np.zeros((X.shape[0], X.shape[1]))
-    act = np.zeros((X.shape[0], d_e))
-    for e in range(E):
-        lo, hi = int(offsets[e]), int(offsets[e + 1])
-        if hi > lo:
-            Y[lo:hi], act[lo:hi] = swiglu(X[lo:hi], W_gate[e], W_up[e], W_down[e])
-    return Y, act
-
-
-# --------------------------------------------------------------------------
-# FP8 dispatch and up-projection  [FP8]
-# --------------------------------------------------------------------------
-
-E4M3_MAX = 448.0
-
-
-def e4m3_round(x) -> np.ndarray:
-    """Nearest E4M3 value, ties to even, saturating at +-448.
-
-    E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
-    infinities.  In the binade [2^e, 2^(e+1)), e >= -6, neighbours are
-    2^(e-3) apart; below 2^-6 the subnormals are 2^-9 apart.
-    """
-    x = np.asarray(x, dtype=np.float64)
-    a = np.abs(x)
-    _, E = np.frexp(a)                      # a = m 2^E, m in [0.5, 1): binade e = E - 1
-    e = np.maximum(E - 1, -6)
-    quantum = np.ldexp(1.0, e - 3)
-    r = np.minimum(np.round(a / quantum) * quantum, E4M3_MAX)  # np.round: half to even
-    return np.copysign(r, x)
-
-
-def e4m3_bits(v) -> np.ndarray:
-    """The 8-bit codes (sign | exponent field << 3 | mantissa) of E4M3 values."""
-    v = np.asarray(v, dtype=np.float64)
-    a = np.abs(v)
-    _, E = np.frexp(a)
-    e = E - 1
-    normal = a >= 2.0 ** -6
-    field = np.where(normal, e + 7, 0)
-    mant = np.where(normal, (np.ldexp(a, -np.where(normal, e, 0)) - 1.0) * 8.0, a * 2.0 ** 9)
-    sign = np.signbit(v).astype(np.int64) << 7
-    return (sign | (field.astype(np.int64) << 3) | mant.astype(np.int64)).astype(np.uint8)
-
-
-def pow2_scale_exponents(amax) -> np.ndarray:
-    """Per row, the smallest integer s >= -127 with amax <= 448 * 2^s (-127 when amax = 0).
-
-    With amax = m 2^E, m in [0.5, 1), and 448 = 0.875 * 2^9: s = E - 9, plus 1 when m > 0.875.
-    """
-    amax = np.asarray(amax, dtype=np.float64)
-    m, E = np.frexp(amax)
-    s = E - 9 + (m > 0.875).astype(np.int64)
-    return np.where(amax > 0, np.maximum(s, -127), -127).astype(np.int64)
-
-
-def quantize_rows_fp8(A):
-    """Row-wise E4M3 with one power-of-two scale per row: (codes [n, c], s [n]), A ~ codes * 2^s."""
-    A = f64(A)
-    amax = np.max(np.abs(A), axis=1) if A.shape[1] else np.zeros(A.shape[0])
-    s = pow2_scale_exponents(amax)
-    return e4m3_round(np.ldexp(A, -s[:, None])), s
-
-
-def dequantize_rows_fp8(codes, s) -> np.ndarray:
-    return np.ldexp(f64(codes), np.asarray(s, dtype=np.int64)[:, None])
-
-
-def fp8_weights(W) -> np.ndarray:
-    """[E, d, h] weights as the FP8 up-projection sees them: each row quantised and dequantised."""
-    out = np.empty(tuple(W.shape), dtype=np.float64)
-    for e in range(W.shape[0]):
-        out[e] = dequantize_rows_fp8(*quantize_rows_fp8(W[e]))
-    return out
-
-
-def shared_ffn(U, W_gate_sh, W_up_sh, W_down_sh) -> np.ndarray:
-    """Y_sh [N_s, T, h]: each shared expert's SwiGLU FFN on every token.  [SHR], [FFN]"""
-    U = f64(U)
-    n_s = len(W_gate_sh)
-    Y = np.zeros((n_s,) + U.shape)
-    for i in range(n_s):
-        Y[i], _ = swiglu(U, W_gate_sh[i], W_up_sh[i], W_down_sh[i])
-    return Y
-
-
-def combine(U, Y, slot_row, gate, k: int, Y_shared=None) -> np.ndarray:
-    """out_t = u_t + sum_s Y_shared[s, t] + sum_j g_{j,t} Y[row of (t, j)], kept pairs only, j ascending.
-
-    [FFN] layer output with [RTR]'s index_add back into token order; a dropped
-    pair adds nothing (its token keeps the residual only, [CAP]); [SHR] the
-    shared experts' outputs enter with weight 1.
-    """
-    out = f64(U).copy()
-    if Y_shared is not None:
-        for ys in f64(Y_shared):
-            out += ys
-    T = out.shape[0]
-    sr = np.asarray(slot_row, dtype=np.int64).reshape(T, k)
-    g = f64(gate).reshape(T, k)
-    Y = f64(Y)
-    for j in range(k):
-        m = sr[:, j] >= 0
-        out[m] += g[m, j][:, None] * Y[sr[m, j]]
-    return out
-
-
-# --------------------------------------------------------------------------
-# Load statistics  [AUX], [VIO]
-# --------------------------------------------------------------------------
-
-def load_stats(counts_routed, s: np.ndarray, T: int, k: int, score_fn: int) -> dict:
-    """f_i, P_i, E * sum_i f_i P_i and MaxVio.  [AUX], [VIO]."""
-    counts_routed = np.asarray(counts_routed, dtype=np.float64)
-    E = counts_routed.shape[0]
-    f = counts_routed / (T * k)
-    sp = s / s.sum(axis=1, keepdims=True) if score_fn == SIGMOID else s
-    P = sp.sum(axis=0) / T
-    aux = E * float((f * P).sum())
-    mean = counts_routed.mean()
-    maxvio = float((counts_routed.max() - mean) / mean) if mean > 0 else 0.0
-    return dict(f=f, P=P, aux=aux, maxvio=maxvio)
-
-
-def router_z_loss(H) -> float:
-    """L_z = (1/T) sum_t LSE(H_t)^2 with LSE(x) = log sum_j e^{x_j}.  [ZL]
-
-    The log-sum-exp is taken in the max-shifted form m + log sum_j e^{x_j - m}.
-    """
-    H = np.asarray(H, dtype=np.float64)
-    T = H.shape[0]
-    if T == 0:
-        return 0.0
-    m = H.max(axis=1)
-    lse = m + np.log(np.exp(H - m[:, None]).sum(axis=1))
-    return float((lse ** 2).sum() / T)
-
-
-# --------------------------------------------------------------------------
-# The whole layer
-# --------------------------------------------------------------------------
-
-def balance_bias_update(b, counts_routed, u: float) -> np.ndarray:
-    """One step of the loss-free balancing bias: e_i = mean(c) - c_i, b_i <- b_i + u * sign(e_i).  [LFB]"""
-    c = np.asarray(counts_routed, dtype=np.float64)
-    e = c.mean() - c
-    return f64(b) + u * np.sign(e)
-
-
-def route(H, k: int, score_fn: int, renorm: bool, sel_bias=None, n_group: int = 1, topk_group: int = 1) -> dict:
-    """From logits to (idx, gates, scores): rounding to fp32, selection, scoring, gates.
-
-    Without a selection bias the top-k is taken on the logits (the same order
-    as on the scores).  With one ([LFB]) it is taken on s + b, while the gates
-    still come from s; "sel_key" holds s + b.  With n_group > 1 the top-k is
-    limited to the experts of the topk_group best groups ([GRP]), the groups
-    being scored on the affinities s (s + b with a selection bias); "allowed"
-    holds that [T, E] mask (None without groups).
-    """
-    H32 = round_f32(H)
-    s = scores(H32, score_fn)
-    key = H32 if sel_bias is None else s + f64(sel_bias)[None, :]
-    allowed = None
-    if n_group > 1:
-        allowed = group_limited_mask(s if sel_bias is None else key, n_group, topk_group, k)
-    idx = topk_select(key, k, allowed)
-    return dict(logits=H32, idx=idx, s=s, gate=gates(s, idx, renorm), sel_key=key, allowed=allowed)
-
-
-def layer_forward(inp, *, T, h, E, k, d_e, score_fn, renorm, capacity_factor,
-                  capacity_override=0, priority=CHOICE_MAJOR, logits=None, sel_bias=None, shared=None,
-                  n_group=1, topk_group=1, fp8=False) -> dict:
-    """The full single-GPU MoE layer forward, stage by stage, in float64.
-
-    `inp` carries U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down (numpy or
-    torch).  If `logits` is given the router GEMM is skipped and those logits
-    are used as they are.  `sel_bias` [E] is the loss-free selection bias
-    ([LFB]); `shared` = (W_gate_sh, W_up_sh, W_down_sh) adds shared experts
-    ([SHR]); n_group > 1 limits each token to topk_group expert groups ([GRP]);
-    fp8 runs the dispatch and the up-projection on E4M3 codes ([FP8]): X holds
-    the dequantised token rows, and "U_codes", "U_s" the quantised U.
-    """
-    H = router_logits(inp.U, inp.W_r, inp.b_r, inp.W_noise, inp.eps) if logits is None else f64(logits)
-    r = route(H, k, score_fn, renorm, sel_bias, n_group, topk_group)
-    C = capacity(T, E, k, capacity_factor, capacity_override)
-    d = dispatch(r["idx"], E, C, priority)
-    extra = {}
-    if fp8:
-        codes, s_u = quantize_rows_fp8(inp.U)
-        X = permute(dequantize_rows_fp8(codes, s_u), d["row_token"])
-        Y, act = expert_ffn(X, d["offsets"], fp8_weights(inp.W_gate), fp8_weights(inp.W_up), inp.W_down, d_e)
-        extra = dict(U_codes=codes, U_s=s_u)
-    else:
-        X = permute(inp.U, d["row_token"])
-        Y, act = expert_ffn(X, d["offsets"], inp.W_gate, inp.W_up, inp.W_down, d_e)
-    Y_sh = None if shared is None else shared_ffn(inp.U, *shared)
-    out = combine(inp.U, Y, d["slot_row"], r["gate"], k, Y_sh)
-    st = load_stats(d["counts_routed"], r["s"], T, k, score_fn)
-    return dict(r, **d, X=X, act=act, Y=Y, Y_shared=Y_sh, out=out, z_loss=router_z_loss(r["logits"]), **st,
-                **extra)
-
-
-def sampled_outputs(inp, tokens, idx, gate, slot_row, k: int, shared=None, fp8=False) -> dict:
-    """out rows (and the Y rows they use) for a sample of tokens.
-
-    For full-size checks: X[row] = U[t] for a kept pair, so each needed Y row
-    is one expert applied to one token row ([FFN]); out follows [FFN]'s layer
-    output.  The sampled rows are grouped by expert so that each expert's
-    weights are read (and widened to float64) once.
-    With `shared` the shared experts' outputs ([SHR]) are added too; with
-    `fp8` the experts see the E4M3 token rows and gate/up weights ([FP8]).
-    Returns {"out": [n, h], "Y": {row: [h]}}.
-    """
-    tokens = [int(t) for t in tokens]
-    idx = np.asarray(idx, dtype=np.int64)
-    gate = f64(gate)
-    sr = np.asarray(slot_row, dtype=np.int64).reshape(-1, k)
-    U = {t: f64(inp.U[t]) for t in tokens}
-    by_expert = {}
-    for t in tokens:
-        for j in range(k):
-            if sr[t, j] >= 0:
-                by_expert.setdefault(int(idx[t, j]), []).append((t, j))
-    y_of = {}
-    for e, pairs in sorted(by_expert.items()):
-        x = np.stack([U[t] for t, _ in pairs])
-        if fp8:
-            x = dequantize_rows_fp8(*quantize_rows_fp8(x))
-            y, _ = swiglu(x, dequantize_rows_fp8(*quantize_rows_fp8(inp.W_gate[e])),
-                          dequantize_rows_fp8(*quantize_rows_fp8(inp.W_up[e])), inp.W_down[e])
-        else:
-            y, _ = swiglu(x, inp.W_gate[e], inp.W_up[e], inp.W_down[e])
-        for (t, j), row in zip(pairs, y):
-            y_of[(t, j)] = row
-    outs, Yrows = [], {}
-    sh = {}
-    if shared is not None and tokens:
-        ysh = shared_ffn(np.stack([U[t] for t in tokens]), *shared).sum(axis=0)
-        sh = {t: ysh[i] for i, t in enumerate(tokens)}
-    for t in tokens:
-        acc = U[t].copy()
+# ------------------------------------------------------------------------------ marshalling
+
+class _In:
+    """A host copy of an input in its own float type (float64, float32 or bfloat16; anything else
+    becomes float64), kept alive while the C call runs."""
+
+    def __init__(self, x):
+        self.keep, self.ptr, self.dt = None, None, _DT_F64
+        if x is None:
+            return
+        if hasattr(x, "detach"):
+            import torch
+            t = x.detach()
+            if t.device.type != "cpu":
+                t = t.cpu()
+            t = t.contiguous()
+            if t.dtype == torch.bfloat16:
+                self.dt = _DT_BF16
+            elif t.dtype == torch.float32:
+                self.dt = _DT_F32
+            elif t.dtype != torch.float64:
+                t = t.to(torch.float64)
+            self.keep, self.ptr, self.shape = t, t.data_ptr(), tuple(t.shape)
+            return
+        a = np.ascontiguousarray(x)
+        if a.dtype == np.float32:
+            self.dt = _DT_F32
+        elif a.dtype != np.float64:
+            a = np.ascontiguousarray(a, dtype=np.float64)
+        self.keep, self.ptr, self.shape = a, a.ctypes.data, a.shape
+
+
+def _d(x) -> np.ndarray:
+    return np.ascontiguousarray(f64(x))
+
+
+def _i(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x), dtype=np.int64)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+_P, _I64, _I32, _F64, _F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_float
+_SIGNATURES = {
+    "orc_threads": (_I32, []),
+    "orc_set_threads": (None, [_I32]),
+    "orc_softplus": (None, [_I64, _P, _P]),
+    "orc_round_f32": (None, [_I64, _P, _P]),
+    "orc_router_logits": (None, [_I64, _I32, _I32] + [_P, _I32] * 5 + [_P]),
+    "orc_scores": (None, [_I64, _I32, _P, _I32, _P]),
+    "orc_topk": (None, [_I64, _I32, _P, _I32, _P, _P]),
+    "orc_group_scores": (None, [_I64, _I32, _P, _I32, _I32, _P]),
+    "orc_group_limited_mask": (None, [_I64, _I32, _P, _I32, _I32, _I32, _P]),
+    "orc_gates": (None, [_I64, _I32, _I32, _P, _P, _I32, _P]),
+    "orc_route": (None, [_I64, _I32, _P, _I32, _I32, _I32, _P, _I32, _I32] + [_P] * 6),
+    "orc_capacity": (_I64, [_I64, _I32, _I32, _F32, _I64]),
+    "orc_dispatch": (_I64, [_I64, _I32, _I32, _P, _I64, _I32] + [_P] * 6),
+    "orc_permute": (None, [_I64, _I32, _P, _I32, _P, _P]),
+    "orc_expert_rows": (None, [_I64, _I32, _I32, _P] + [_P, _I32, _I64] * 3 + [_I32, _I32, _P, _P]),
+    "orc_expert_ffn": (None, [_I64, _I32, _I32, _I32, _P, _P] + [_P, _I32] * 3 + [_I32, _P, _P]),
+    "orc_e4m3_round": (None, [_I64, _P, _P]),
+    "orc_e4m3_bits": (None, [_I64, _P, _P]),
+    "orc_pow2_scale_exponents": (None, [_I64, _P, _P]),
+    "orc_quantize_rows_fp8": (None, [_I64, _I64, _P, _I32, _P, _P]),
+    "orc_dequantize_rows_fp8": (None, [_I64, _I64, _P, _P, _P]),
+    "orc_shared_ffn": (None, [_I32, _I64, _I32, _I32] + [_P, _I32] * 4 + [_P]),
+    "orc_combine": (None, [_I64, _I32, _I32, _P, _I32, _P, _P, _P, _I32, _P, _P]),
+    "orc_load_stats": (None, [_I32, _I64, _F64, _P, _P, _I32, _P, _P, _P]),
+    "orc_z_loss": (_F64, [_I64, _I32, _P]),
+    "orc_balance_bias_update": (None, [_I32, _P, _P, _F64, _P]),
+    "orc_topk_margins": (None, [_I64, _I32, _P, _I32, _P]),
+    "orc_group_margins": (None, [_I64, _I32, _P, _I32, _I32, _I32, _P]),
+    "orc_layer_forward": (None, [_I64, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _I64, _I32] + [_P, _I32] * 5 +
+                          [_P] + [_P, _I32] * 3 + [_P, _I32, _I32, _I32, _I32] + [_P, _I32] * 3 + [_I32] +
+                          [_P] * 23),
+    "orc_sampled_combine": (None, [_I64, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P]),
+    "orc_combine_backward": (None, [_I64, _I32, _I32, _I64] + [_P] * 6),
+    "orc_gate_backward": (None, [_I64, _I32, _I32, _P, _P, _P, _I32, _I32, _P]),
+    "orc_aux_loss_grad": (None, [_I64, _I32, _P, _P, _I32, _P]),
+    "orc_z_loss_grad": (None, [_I64, _I32, _P, _P]),
+    "orc_router_backward": (None, [_I64, _I32, _I32, _P, _P, _P, _P, _I32, _I32, _F64, _F64, _P]),
+    "orc_swiglu_backward": (None, [_I64, _I32, _I32, _P] + [_P, _I32, _I64] * 3 + [_P] * 8),
+    "orc_expert_ffn_backward": (None, [_I64, _I32, _I32, _I32, _P, _P] + [_P, _I32] * 3 + [_P] * 8),
+    "orc_dispatch_backward": (None, [_I64, _I32, _I32, _P, _P, _P, _P]),
+    "orc_router_input_backward": (None, [_I64, _I32, _I32, _P, _I32, _P, _I32, _P, _P, _I32, _P, _I32] + [_P] * 4),
+    "orc_layer_backward": (None, [_I64, _I32, _I32, _I32, _I32, _I32, _I32, _F64, _F64] + [_P, _I32] * 7 +
+                           [_I32, _I32] + [_P, _I32] * 3 + [_P] * 4 + [_I64] + [_P] * 22),
+}
+
+STAGES = ("router_logits", "selection", "dispatch", "experts", "shared_experts", "combine", "statistics")
+
+
+# ------------------------------------------------------------------------------ the oracle
+
+class Oracle:
+    """One build of the oracle library, with the method's steps as numpy-returning functions."""
+
+    SOFTMAX, SIGMOID, CHOICE_MAJOR, TOKEN_MAJOR, E4M3_MAX = SOFTMAX, SIGMOID, CHOICE_MAJOR, TOKEN_MAJOR, E4M3_MAX
+    STAGES = STAGES
+
+    def __init__(self, path: str):
+        self.path = path
+        self.lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(self.lib, name)
+            fn.restype, fn.argtypes = res, args
+
+    def threads(self) -> int:
+        """OpenMP threads the oracle's parallel loops use."""
+        return int(self.lib.orc_threads())
+
+    def set_threads(self, n: int) -> None:
+        """Sets the OpenMP thread count of the oracle's parallel loops (results do not depend on it)."""
+        self.lib.orc_set_threads(int(n))
+
+    # ---------------------------------------------------------------- router
+    def softplus(self, x) -> np.ndarray:
+        x = _d(x)
+        out = np.empty_like(x)
+        self.lib.orc_softplus(x.size, _p(x), _p(out))
+        return out
+
+    def router_logits(self, U, W_r, b_r=None, W_noise=None, eps=None) -> np.ndarray:
+        """H = U W_r (+ b_r) (+ eps * Softplus(U W_noise)), float64 [T, E]."""
+        u, w, b, wn, ep = _In(U), _In(W_r), _In(b_r), _In(W_noise), _In(eps)
+        T, h = u.shape
+        E = w.shape[1]
+        H = np.empty((T, E))
+        self.lib.orc_router_logits(T, h, E, u.ptr, u.dt, w.ptr, w.dt, b.ptr, b.dt, wn.ptr, wn.dt, ep.ptr, ep.dt,
+                                   _p(H))
+        return H
+
+    def round_f32(self, H) -> np.ndarray:
+        H = _d(H)
+        out = np.empty_like(H)
+        self.lib.orc_round_f32(H.size, _p(H), _p(out))
+        return out
+
+    def topk_select(self, H32, k: int, allowed=None) -> np.ndarray:
+        key = _d(H32)
+        T, E = key.shape
+        al = None if allowed is None else np.ascontiguousarray(np.asarray(allowed, dtype=bool).astype(np.uint8))
+        idx = np.empty((T, k), dtype=np.int64)
+        self.lib.orc_topk(T, E, _p(key), k, _p(al), _p(idx))
+        return idx.astype(np.int32)
+
+    def group_scores(self, aff, n_group: int, r: int) -> np.ndarray:
+        aff = _d(aff)
+        T, E = aff.shape
+        out = np.empty((T, n_group))
+        self.lib.orc_group_scores(T, E, _p(aff), n_group, r, _p(out))
+        return out
+
+    def group_limited_mask(self, aff, n_group: int, topk_group: int, k: int) -> np.ndarray:
+        aff = _d(aff)
+        T, E = aff.shape
+        out = np.empty((T, E), dtype=np.uint8)
+        self.lib.orc_group_limited_mask(T, E, _p(aff), n_group, topk_group, k, _p(out))
+        return out.astype(bool)
+
+    def scores(self, H, score_fn: int) -> np.ndarray:
+        if score_fn not in (SOFTMAX, SIGMOID):
+            raise ValueError("score_fn")
+        H = _d(H)
+        T, E = H.shape
+        s = np.empty_like(H)
+        self.lib.orc_scores(T, E, _p(H), score_fn, _p(s))
+        return s
+
+    def gates(self, s, idx, renorm: bool) -> np.ndarray:
+        s, idx = _d(s), _i(idx)
+        T, E = s.shape
+        k = idx.shape[1]
+        g = np.empty((T, k))
+        self.lib.orc_gates(T, E, k, _p(s), _p(idx), int(bool(renorm)), _p(g))
+        return g
+
+    def route(self, H, k: int, score_fn: int, renorm: bool, sel_bias=None, n_group: int = 1,
+              topk_group: int = 1) -> dict:
+        """logits (rounded to float32), idx, s, gate, sel_key and (n_group > 1) the allowed mask."""
+        if score_fn not in (SOFTMAX, SIGMOID):
+            raise ValueError("score_fn")
+        H = _d(H)
+        T, E = H.shape
+        sb = None if sel_bias is None else _d(sel_bias)
+        groups = n_group is not None and n_group > 1
+        out = dict(logits=np.empty((T, E)), s=np.empty((T, E)), sel_key=np.empty((T, E)),
+                   allowed=np.empty((T, E), dtype=np.uint8) if groups else None,
+                   idx=np.empty((T, k), dtype=np.int64), gate=np.empty((T, k)))
+        self.lib.orc_route(T, E, _p(H), k, score_fn, int(bool(renorm)), _p(sb), n_group if groups else 1,
+                           topk_group if groups else 1, _p(out["logits"]), _p(out["s"]), _p(out["sel_key"]),
+                           _p(out["allowed"]), _p(out["idx"]), _p(out["gate"]))
+        out["idx"] = out["idx"].astype(np.int32)
+        if groups:
+            out["allowed"] = out["allowed"].astype(bool)
+        return out
+
+    # ---------------------------------------------------------------- capacity and dispatch
+    def capacity(self, T: int, E: int, k: int, capacity_factor: float, override: int = 0) -> int:
+        return int(self.lib.orc_capacity(int(T), int(E), int(k), float(capacity_factor), int(override)))
+
+    def dispatch(self, idx, E: int, C: int, priority: int = CHOICE_MAJOR) -> dict:
+        """counts_routed, counts_kept [E], offsets [E+1], slot, slot_row [T*k] (-1 = dropped),
+        row_token [A], n_dropped, C."""
+        if priority not in (CHOICE_MAJOR, TOKEN_MAJOR):
+            raise ValueError("priority")
+        idx = _i(idx)
+        T, k = idx.shape
+        o = dict(counts_routed=np.empty(E, dtype=np.int64), counts_kept=np.empty(E, dtype=np.int64),
+                 offsets=np.empty(E + 1, dtype=np.int64), slot=np.empty(T * k, dtype=np.int64),
+                 slot_row=np.empty(T * k, dtype=np.int64), row_token=np.full(T * k, -1, dtype=np.int64))
+        dropped = self.lib.orc_dispatch(T, k, E, _p(idx), int(C), priority, _p(o["counts_routed"]),
+                                        _p(o["counts_kept"]), _p(o["offsets"]), _p(o["slot"]), _p(o["slot_row"]),
+                                        _p(o["row_token"]))
+        o["row_token"] = o["row_token"][:int(o["offsets"][E])].copy()
+        o["n_dropped"], o["C"] = int(dropped), int(C)
+        return o
+
+    def permute(self, U, row_token) -> np.ndarray:
+        u, rt = _In(U), _i(row_token)
+        h = u.shape[1]
+        X = np.empty((rt.size, h))
+        self.lib.orc_permute(rt.size, h, u.ptr, u.dt, _p(rt), _p(X))
+        return X
+
+    # ---------------------------------------------------------------- experts
+    def _expert_rows(self, x, Wg_e, Wu_e, Wd_e, fp8_x=False, fp8_w=False):
+        x = _d(x)
+        g, u, d_ = _In(Wg_e), _In(Wu_e), _In(Wd_e)
+        n, h = x.shape
+        d = g.shape[0]
+        y, a = np.empty((n, h)), np.empty((n, d))
+        self.lib.orc_expert_rows(n, h, d, _p(x), g.ptr, g.dt, 0, u.ptr, u.dt, 0, d_.ptr, d_.dt, 0, int(fp8_x),
+                                 int(fp8_w), _p(y), _p(a))
+        return y, a
+
+    def swiglu(self, x, W_gate_e, W_up_e, W_down_e):
+        """One expert on rows x [n, h]: (W_down (SiLU(W_gate x) * W_up x) [n, h], the activation [n, d_e])."""
+        return self._expert_rows(x, W_gate_e, W_up_e, W_down_e)
+
+    def expert_ffn(self, X, offsets, W_gate, W_up, W_down, d_e: int):
+        """(Y, act): the grouped FFN over the expert segments of X."""
+        X, off = _d(X), _i(offsets)
+        g, u, d_ = _In(W_gate), _In(W_up), _In(W_down)
+        A, h = X.shape
+        E = off.size - 1
+        Y, act = np.empty((A, h)), np.empty((A, d_e))
+        self.lib.orc_expert_ffn(A, h, d_e, E, _p(X), _p(off), g.ptr, g.dt, u.ptr, u.dt, d_.ptr, d_.dt, 0, _p(Y),
+                                _p(act))
+        return Y, act
+
+    # ---------------------------------------------------------------- FP8
+    def e4m3_round(self, x):
+        scalar = np.ndim(x) == 0
+        x = _d(x)
+        out = np.empty_like(x)
+        self.lib.orc_e4m3_round(x.size, _p(x), _p(out))
+        return float(out.reshape(-1)[0]) if scalar else out
+
+    def e4m3_bits(self, v) -> np.ndarray:
+        v = _d(v)
+        out = np.empty(v.shape, dtype=np.uint8)
+        self.lib.orc_e4m3_bits(v.size, _p(v), _p(out))
+        return out
+
+    def pow2_scale_exponents(self, amax) -> np.ndarray:
+        a = _d(amax)
+        out = np.empty(a.shape, dtype=np.int64)
+        self.lib.orc_pow2_scale_exponents(a.size, _p(a), _p(out))
+        return out
+
+    def quantize_rows_fp8(self, A):
+        """Row-wise E4M3 with one power-of-two scale per row: (codes [n, c], s [n]), A ~ codes * 2^s."""
+        a = _In(A)
+        n, c = a.shape
+        codes, s = np.empty((n, c)), np.empty(n, dtype=np.int64)
+        self.lib.orc_quantize_rows_fp8(n, c, a.ptr, a.dt, _p(codes), _p(s))
+        return codes, s
+
+    def dequantize_rows_fp8(self, codes, s) -> np.ndarray:
+        codes, s = _d(codes), _i(s)
+        n, c = codes.shape
+        out = np.empty_like(codes)
+        self.lib.orc_dequantize_rows_fp8(n, c, _p(codes), _p(s), _p(out))
+        return out
+
+    def fp8_weights(self, W) -> np.ndarray:
+        """[E, d, h] weights as the FP8 up-projection sees them: each row quantised and dequantised."""
+        shape = tuple(W.shape)
+        flat = W.reshape(-1, shape[-1])
+        return self.dequantize_rows_fp8(*self.quantize_rows_fp8(flat)).reshape(shape)
+
+    # ---------------------------------------------------------------- shared experts, combine, statistics
+    def shared_ffn(self, U, W_gate_sh, W_up_sh, W_down_sh) -> np.ndarray:
+        """Y_sh [N_s, T, h]: each shared expert's SwiGLU FFN on every token."""
+        u, g, up, d_ = _In(U), _In(W_gate_sh), _In(W_up_sh), _In(W_down_sh)
+        T, h = u.shape
+        n_s, d = g.shape[0], g.shape[1]
+        Y = np.empty((n_s, T, h))
+        self.lib.orc_shared_ffn(n_s, T, h, d, u.ptr, u.dt, g.ptr, g.dt, up.ptr, up.dt, d_.ptr, d_.dt, _p(Y))
+        return Y
+
+    def combine(self, U, Y, slot_row, gate, k: int, Y_shared=None) -> np.ndarray:
+        """out_t = u_t + sum_s Y_shared[s, t] + sum_j g_{j,t} Y[row of (t, j)], kept pairs, j ascending."""
+        u, Y, sr, g = _In(U), _d(Y), _i(slot_row), _d(gate)
+        T, h = u.shape
+        ysh = None if Y_shared is None else _d(Y_shared)
+        n_s = 0 if ysh is None else ysh.shape[0]
+        out = np.empty((T, h))
+        self.lib.orc_combine(T, h, k, u.ptr, u.dt, _p(Y), _p(sr), _p(g), n_s, _p(ysh), _p(out))
+        return out
+
+    def load_stats(self, counts_routed, s, T: int, k, score_fn: int) -> dict:
+        """f_i, P_i, E * sum_i f_i P_i and MaxVio."""
+        c, s = _d(counts_routed), _d(s)
+        E = c.size
+        f, P, sc = np.empty(E), np.empty(E), np.empty(2)
+        self.lib.orc_load_stats(E, int(T), float(k), _p(c), _p(s), score_fn, _p(f), _p(P), _p(sc))
+        return dict(f=f, P=P, aux=float(sc[0]), maxvio=float(sc[1]))
+
+    def router_z_loss(self, H) -> float:
+        H = _d(H)
+        if H.ndim == 1:
+            H = H.reshape(1, -1)
+        T, E = H.shape
+        return float(self.lib.orc_z_loss(T, E, _p(H)))
+
+    def balance_bias_update(self, b, counts_routed, u: float) -> np.ndarray:
+        b, c = _d(b), _d(counts_routed)
+        out = np.empty_like(b)
+        self.lib.orc_balance_bias_update(b.size, _p(b), _p(c), float(u), _p(out))
+        return out
+
+    def topk_margins(self, H32, k: int) -> np.ndarray:
+        """Smallest gap between adjacent values among each row's k+1 largest (keeps the tests' routing
+        decisions away from ties)."""
+        H = _d(H32)
+        T, E = H.shape
+        out = np.empty(T)
+        self.lib.orc_topk_margins(T, E, _p(H), k, _p(out))
+        return out
+
+    def group_margins(self, aff, n_group: int, topk_group: int, k: int) -> np.ndarray:
+        """Per token, the gap between the topk_group-th and the next group score (inf when every group
+        is kept)."""
+        a = _d(aff)
+        T, E = a.shape
+        out = np.empty(T)
+        self.lib.orc_group_margins(T, E, _p(a), n_group, topk_group, k, _p(out))
+        return out
+
+    # ---------------------------------------------------------------- the whole layer
+    def layer_forward(self, inp, *, T, h, E, k, d_e, score_fn, renorm, capacity_factor, capacity_override=0,
+                      priority=CHOICE_MAJOR, logits=None, sel_bias=None, shared=None, n_group=1, topk_group=1,
+                      fp8=False) -> dict:
+        """The full single-GPU MoE layer forward, stage by stage.
+
+        `inp` carries U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down (numpy or torch).  `logits`
+        given: the router GEMM is skipped and those logits are used.  `sel_bias` [E]: loss-free
+        selection bias; `shared` = (W_gate_sh, W_up_sh, W_down_sh): shared experts; n_group > 1:
+        group-limited routing; fp8: E4M3 dispatch and up-projection (X holds the dequantised rows,
+        "U_codes", "U_s" the quantised U).  "seconds" holds each stage's wall time (STAGES order).
+        """
+        if score_fn not in (SOFTMAX, SIGMOID) or priority not in (CHOICE_MAJOR, TOKEN_MAJOR):
+            raise ValueError("score_fn / priority")
+        T, h, E, k, d_e = int(T), int(h), int(E), int(k), int(d_e)
+        U, Wr, br = _In(inp.U), _In(inp.W_r), _In(inp.b_r)
+        Wn, ep = _In(inp.W_noise), _In(inp.eps)
+        Wg, Wu, Wd = _In(inp.W_gate), _In(inp.W_up), _In(inp.W_down)
+        H = None if logits is None else _d(logits)
+        sb = None if sel_bias is None else _d(sel_bias)
+        n_s, d_s = 0, 0
+        Sg = Su = Sd = _In(None)
         if shared is not None:
-            acc = acc + sh[t]
-        for j in range(k):
-            if sr[t, j] >= 0:
-                Yrows[int(sr[t, j])] = y_of[(t, j)]
-                acc = acc + gate[t, j] * y_of[(t, j)]
-        outs.append(acc)
-    return dict(out=np.stack(outs) if outs else np.zeros((0, 0)), Y=Yrows)
+            Sg, Su, Sd = (_In(x) for x in shared)
+            n_s, d_s = Sg.shape[0], Sg.shape[1]
+        groups = n_group is not None and n_group > 1
+        Tk = T * k
+        o = dict(logits=np.empty((T, E)), s=np.empty((T, E)), sel_key=np.empty((T, E)),
+                 allowed=np.empty((T, E), dtype=np.uint8) if groups else None,
+                 idx=np.empty((T, k), dtype=np.int64), gate=np.empty((T, k)),
+                 counts_routed=np.empty(E, dtype=np.int64), counts_kept=np.empty(E, dtype=np.int64),
+                 offsets=np.empty(E + 1, dtype=np.int64), slot=np.empty(Tk, dtype=np.int64),
+                 slot_row=np.empty(Tk, dtype=np.int64), row_token=np.full(Tk, -1, dtype=np.int64),
+                 X=np.empty((Tk, h)), act=np.empty((Tk, d_e)), Y=np.empty((Tk, h)),
+                 Y_shared=np.empty((n_s, T, h)) if n_s else None, out=np.empty((T, h)),
+                 f=np.empty(E), P=np.empty(E),
+                 U_codes=np.empty((T, h)) if fp8 else None, U_s=np.empty(T, dtype=np.int64) if fp8 else None)
+        scal, sec = np.empty(5), np.empty(len(STAGES))
+        self.lib.orc_layer_forward(
+            T, h, E, k, d_e, score_fn, int(bool(renorm)), float(capacity_factor), int(capacity_override or 0),
+            priority, U.ptr, U.dt, Wr.ptr, Wr.dt, br.ptr, br.dt, Wn.ptr, Wn.dt, ep.ptr, ep.dt, _p(H), Wg.ptr, Wg.dt,
+            Wu.ptr, Wu.dt, Wd.ptr, Wd.dt, _p(sb), n_group if groups else 1, topk_group if groups else 1, n_s, d_s,
+            Sg.ptr, Sg.dt, Su.ptr, Su.dt, Sd.ptr, Sd.dt, int(bool(fp8)),
+            *(_p(o[n]) for n in ("logits", "s", "sel_key", "allowed", "idx", "gate", "counts_routed", "counts_kept",
+                                 "offsets", "slot", "slot_row", "row_token", "X", "act", "Y", "Y_shared", "out",
+                                 "f", "P", "U_codes", "U_s")),
+            _p(scal), _p(sec))
+        A = int(o["offsets"][E])
+        o["idx"] = o["idx"].astype(np.int32)
+        if groups:
+            o["allowed"] = o["allowed"].astype(bool)
+        for n in ("row_token", "X", "act", "Y"):
+            o[n] = o[n][:A].copy()
+        o.update(C=int(scal[0]), n_dropped=int(scal[1]), aux=float(scal[2]), maxvio=float(scal[3]),
+                 z_loss=float(scal[4]), seconds=dict(zip(STAGES, sec.tolist())))
+        if not fp8:
+            del o["U_codes"], o["U_s"]
+        return o
+
+    def sampled_outputs(self, inp, tokens, idx, gate, slot_row, k: int, shared=None, fp8=False) -> dict:
+        """out rows (and the Y rows they use) for a sample of tokens of a full-size layer.
+
+        Each kept pair's Y row is one expert applied to one token row; the pairs are grouped by
+        expert so that each expert's weights are copied to the host once.  `shared` adds the shared
+        experts; `fp8` gives the experts E4M3 token rows and gate/up weight rows.
+        Returns {"out": [n, h], "Y": {row: [h]}}.
+        """
+        tokens = [int(t) for t in tokens]
+        idx, g, sr = _i(idx), _d(gate), _i(slot_row).reshape(-1, k)
+        n = len(tokens)
+        if n == 0:
+            return dict(out=np.zeros((0, 0)), Y={})
+        if hasattr(inp.U, "detach"):
+            import torch
+            u = _d(inp.U[torch.as_tensor(tokens, device=inp.U.device)])
+        else:
+            u = _d(np.asarray(inp.U)[tokens])
+        h = u.shape[1]
+        y = np.zeros((n, k, h))
+        by_expert = {}
+        for i, t in enumerate(tokens):
+            for j in range(k):
+                if sr[t, j] >= 0:
+                    by_expert.setdefault(int(idx[t, j]), []).append((i, j))
+        for e, pairs in sorted(by_expert.items()):
+            ye, _ = self._expert_rows(u[[i for i, _ in pairs]], inp.W_gate[e], inp.W_up[e], inp.W_down[e],
+                                      fp8_x=fp8, fp8_w=fp8)
+            for (i, j), row in zip(pairs, ye):
+                y[i, j] = row
+        n_s, ysh = 0, None
+        if shared is not None:
+            n_s = len(shared[0])
+            ysh = np.stack([self._expert_rows(u, shared[0][s], shared[1][s], shared[2][s])[0] for s in range(n_s)])
+        sub_sr = np.ascontiguousarray(sr[tokens])
+        sub_g = np.ascontiguousarray(g.reshape(-1, k)[tokens])
+        out = np.empty((n, h))
+        self.lib.orc_sampled_combine(n, h, k, _p(u), _p(y), _p(sub_sr), _p(sub_g), n_s, _p(ysh), _p(out))
+        rows = {int(sub_sr[i, j]): y[i, j] for i in range(n) for j in range(k) if sub_sr[i, j] >= 0}
+        return dict(out=out, Y=rows)
+
+    # ---------------------------------------------------------------- backward
+    def combine_backward(self, dO, Y, slot_row, gate, k: int) -> dict:
+        """d_gate [T, k] = dO_t . Y[row] (0 when dropped), dY [A, h] = g dO_t."""
+        dO, Y, sr, g = _d(dO), _d(Y), _i(slot_row), _d(gate)
+        T, h = dO.shape
+        A = Y.shape[0]
+        d_gate, dY = np.empty((T, k)), np.empty((A, h))
+        self.lib.orc_combine_backward(T, h, k, A, _p(dO), _p(Y), _p(sr), _p(g), _p(d_gate), _p(dY))
+        return dict(d_gate=d_gate, dY=dY)
+
+    def gate_backward(self, H32, idx, d_gate, score_fn: int, renorm: bool) -> np.ndarray:
+        H, idx, dg = _d(H32), _i(idx), _d(d_gate)
+        T, E = H.shape
+        k = idx.shape[1]
+        dg = np.ascontiguousarray(dg.reshape(T, k))
+        dH = np.empty((T, E))
+        self.lib.orc_gate_backward(T, E, k, _p(H), _p(idx), _p(dg), score_fn, int(bool(renorm)), _p(dH))
+        return dH
+
+    def aux_loss_grad(self, H32, f, score_fn: int) -> np.ndarray:
+        H, f = _d(H32), _d(f)
+        T, E = H.shape
+        out = np.empty((T, E))
+        self.lib.orc_aux_loss_grad(T, E, _p(H), _p(f), score_fn, _p(out))
+        return out
+
+    def z_loss_grad(self, H32) -> np.ndarray:
+        H = _d(H32)
+        T, E = H.shape
+        out = np.empty((T, E))
+        self.lib.orc_z_loss_grad(T, E, _p(H), _p(out))
+        return out
+
+    def router_backward(self, H32, idx, d_gate, f, score_fn: int, renorm: bool, w_aux: float = 0.0,
+                        w_z: float = 0.0) -> np.ndarray:
+        """dL/dH for L = (the loss through the gates) + w_aux E sum f P + w_z L_z."""
+        H, idx, dg, f = _d(H32), _i(idx), _d(d_gate), _d(f)
+        T, E = H.shape
+        k = idx.shape[1]
+        dg = np.ascontiguousarray(dg.reshape(T, k))
+        dH = np.empty((T, E))
+        self.lib.orc_router_backward(T, E, k, _p(H), _p(idx), _p(dg), _p(f), score_fn, int(bool(renorm)),
+                                     float(w_aux), float(w_z), _p(dH))
+        return dH
+
+    def swiglu_backward(self, x, W_gate_e, W_up_e, W_down_e, dy) -> dict:
+        x, dy = _d(x), _d(dy)
+        g, u, d_ = _In(W_gate_e), _In(W_up_e), _In(W_down_e)
+        n, h = x.shape
+        d = g.shape[0]
+        o = dict(d_act=np.empty((n, d)), dG=np.empty((n, d)), dUp=np.empty((n, d)), dx=np.empty((n, h)),
+                 dW_gate=np.empty((d, h)), dW_up=np.empty((d, h)), dW_down=np.empty((h, d)))
+        self.lib.orc_swiglu_backward(n, h, d, _p(x), g.ptr, g.dt, 0, u.ptr, u.dt, 0, d_.ptr, d_.dt, 0, _p(dy),
+                                     *(_p(o[m]) for m in ("d_act", "dG", "dUp", "dx", "dW_gate", "dW_up", "dW_down")))
+        return o
+
+    def expert_ffn_backward(self, X, offsets, W_gate, W_up, W_down, dY, d_e: int) -> dict:
+        X, off, dY = _d(X), _i(offsets), _d(dY)
+        g, u, d_ = _In(W_gate), _In(W_up), _In(W_down)
+        A, h = X.shape
+        E = off.size - 1
+        o = dict(d_act=np.empty((A, d_e)), dG=np.empty((A, d_e)), dUp=np.empty((A, d_e)), dX=np.empty((A, h)),
+                 dW_gate=np.empty((E, d_e, h)), dW_up=np.empty((E, d_e, h)), dW_down=np.empty((E, h, d_e)))
+        self.lib.orc_expert_ffn_backward(A, h, d_e, E, _p(X), _p(off), g.ptr, g.dt, u.ptr, u.dt, d_.ptr, d_.dt,
+                                         _p(dY), *(_p(o[m]) for m in ("d_act", "dG", "dUp", "dX", "dW_gate",
+                                                                       "dW_up", "dW_down")))
+        return o
+
+    def dispatch_backward(self, dO, dX, slot_row, k: int) -> np.ndarray:
+        dO, dX, sr = _d(dO), _d(dX), _i(slot_row)
+        T, h = dO.shape
+        dU = np.empty((T, h))
+        self.lib.orc_dispatch_backward(T, h, k, _p(dO), _p(dX), _p(sr), _p(dU))
+        return dU
+
+    def router_input_backward(self, U, W_r, dH, W_noise=None, eps=None) -> dict:
+        u, w, dH = _In(U), _In(W_r), _d(dH)
+        wn, ep = _In(W_noise), _In(eps)
+        T, h = u.shape
+        E = w.shape[1]
+        o = dict(dU=np.empty((T, h)), dW_r=np.empty((h, E)), db_r=np.empty(E),
+                 dW_noise=np.empty((h, E)) if W_noise is not None else None)
+        self.lib.orc_router_input_backward(T, h, E, u.ptr, u.dt, w.ptr, w.dt, _p(dH), wn.ptr, wn.dt, ep.ptr, ep.dt,
+                                           _p(o["dU"]), _p(o["dW_r"]), _p(o["db_r"]), _p(o["dW_noise"]))
+        return o
+
+    def layer_backward(self, inp, fwd: dict, dO, *, k: int, d_e: int, score_fn: int, renorm: bool,
+                       w_aux: float = 0.0, w_z: float = 0.0) -> dict:
+        """Gradients of L = <dO, out> + w_aux E sum_i f_i P_i + w_z L_z through the whole layer, with
+        the routing decisions held fixed.  `fwd` is layer_forward's result."""
+        U, Wr, Wn, ep = _In(inp.U), _In(inp.W_r), _In(inp.W_noise), _In(inp.eps)
+        Wg, Wu, Wd = _In(inp.W_gate), _In(inp.W_up), _In(inp.W_down)
+        shared = getattr(inp, "shared", None)
+        n_s, d_s = 0, 0
+        Sg = Su = Sd = _In(None)
+        if shared is not None:
+            Sg, Su, Sd = (_In(x) for x in shared)
+            n_s, d_s = Sg.shape[0], Sg.shape[1]
+        T, h = U.shape
+        E = Wr.shape[1]
+        logits, idx, sr, g = _d(fwd["logits"]), _i(fwd["idx"]), _i(fwd["slot_row"]), _d(fwd["gate"])
+        X, Y, off, f = _d(fwd["X"]), _d(fwd["Y"]), _i(fwd["offsets"]), _d(fwd["f"])
+        dO = _d(dO)
+        A = X.shape[0]
+        o = dict(dU=np.empty((T, h)), d_gate=np.empty((T, k)), dY=np.empty((A, h)), dH=np.empty((T, E)),
+                 dW_r=np.empty((h, E)), db_r=np.empty(E),
+                 dW_noise=np.empty((h, E)) if inp.W_noise is not None else None,
+                 d_act=np.empty((A, d_e)), dG=np.empty((A, d_e)), dUp=np.empty((A, d_e)), dX=np.empty((A, h)),
+                 dW_gate=np.empty((E, d_e, h)), dW_up=np.empty((E, d_e, h)), dW_down=np.empty((E, h, d_e)),
+                 dW_gate_sh=np.empty((n_s, d_s, h)) if n_s else None, dW_up_sh=np.empty((n_s, d_s, h)) if n_s else None,
+                 dW_down_sh=np.empty((n_s, h, d_s)) if n_s else None)
+        self.lib.orc_layer_backward(
+            T, h, E, k, d_e, score_fn, int(bool(renorm)), float(w_aux), float(w_z), U.ptr, U.dt, Wr.ptr, Wr.dt,
+            Wn.ptr, Wn.dt, ep.ptr, ep.dt, Wg.ptr, Wg.dt, Wu.ptr, Wu.dt, Wd.ptr, Wd.dt, n_s, d_s, Sg.ptr, Sg.dt,
+            Su.ptr, Su.dt, Sd.ptr, Sd.dt, _p(logits), _p(idx), _p(sr), _p(g), A, _p(X), _p(Y), _p(off), _p(f), _p(dO),
+            *(_p(o[m]) for m in ("dU", "d_gate", "dY", "dH", "dW_r", "db_r", "dW_noise", "d_act", "dG", "dUp", "dX",
+                                 "dW_gate", "dW_up", "dW_down", "dW_gate_sh", "dW_up_sh", "dW_down_sh")))
+        if not n_s:
+            del o["dW_gate_sh"], o["dW_up_sh"], o["dW_down_sh"]
+        return o
 
 
-# --------------------------------------------------------------------------
-# Backward of the router side  [GRD]
-# --------------------------------------------------------------------------
+# ------------------------------------------------------------------------------ the default build
 
-def combine_backward(dO, Y, slot_row, gate, k: int) -> dict:
-    """Backward of the combine for the upstream gradient dO [T, h].
+default = Oracle(build())
 
-    out_t = u_t + sum_j g_{t,j} Y[row(t,j)] gives, per kept pair,
-    dL/dg_{t,j} = dO_t . Y[row] ([GRD]) and dL/dY[row] = g_{t,j} dO_t;
-    dropped pairs get d_gate = 0.  Returns d_gate [T, k] and dY [A, h] (rows of Y).
-    """
-    dO, Y, g = f64(dO), f64(Y), f64(gate)
-    T = dO.shape[0]
-    sr = np.asarray(slot_row, dtype=np.int64).reshape(T, k)
-    d_gate = np.zeros((T, k))
-    dY = np.zeros_like(Y)
-    for j in range(k):
-        m = sr[:, j] >= 0
-        rows = sr[m, j]
-        d_gate[m, j] = np.einsum("th,th->t", dO[m], Y[rows])
-        dY[rows] = g.reshape(T, k)[m, j][:, None] * dO[m]
-    return dict(d_gate=d_gate, dY=dY)
+_EXPORTS = ("threads", "set_threads", "softplus", "router_logits", "round_f32", "topk_select", "group_scores",
+            "group_limited_mask", "scores", "gates", "route", "capacity", "dispatch", "permute", "swiglu",
+            "expert_ffn", "e4m3_round", "e4m3_bits", "pow2_scale_exponents", "quantize_rows_fp8",
+            "dequantize_rows_fp8", "fp8_weights", "shared_ffn", "combine", "load_stats", "router_z_loss",
+            "balance_bias_update", "topk_margins", "group_margins", "layer_forward", "sampled_outputs",
+            "combine_backward", "gate_backward", "aux_loss_grad", "z_loss_grad", "router_backward",
+            "swiglu_backward", "expert_ffn_backward", "dispatch_backward", "router_input_backward",
+            "layer_backward")
+for _name in _EXPORTS:
+    globals()[_name] = getattr(default, _name)
 
-
-def gate_backward(H32, idx, d_gate, score_fn: int, renorm: bool) -> np.ndarray:
-    """dL/dH [T, E] from dL/dg through the gate definition ([SCR], [GRD]).
-
-    softmax:  s = softmax(H); g_j = s_{i_j}, or s_{i_j} / sum_m s_{i_m} with renorm;
-    sigmoid:  s = sigmoid(H); the same two forms.  The selection itself is
-    not differentiated (the top-k set is held fixed).
-    """
-    H = np.asarray(H32, dtype=np.float64)
-    T, E = H.shape
-    idx = np.asarray(idx, dtype=np.int64)
-    k = idx.shape[1]
-    s = scores(H, score_fn)
-    sel = np.take_along_axis(s, idx, axis=1)
-    d_gate = f64(d_gate).reshape(T, k)
-    # dL/ds_{i_j} (for the selected experts; the other scores do not enter g)
-    if renorm:
-        S = sel.sum(axis=1, keepdims=True)
-        g = sel / S
-        # g_j = s_j / S: dg_j/ds_m = (delta_jm - g_j) / S
-        ds_sel = (d_gate - (d_gate * g).sum(axis=1, keepdims=True)) / S
-    else:
-        ds_sel = d_gate
-    ds = np.zeros((T, E))
-    np.add.at(ds, (np.repeat(np.arange(T), k), idx.reshape(-1)), ds_sel.reshape(-1))
-    if score_fn == SOFTMAX:
-        # ds_i/dH_k = s_i (delta_ik - s_k)
-        return s * (ds - (ds * s).sum(axis=1, keepdims=True))
-    return ds * s * (1.0 - s)
-
-
-def aux_loss_grad(H32, f, score_fn: int) -> np.ndarray:
-    """d(E * sum_i f_i P_i)/dH [T, E] with f held constant ([AUX], [GRD])."""
-    H = np.asarray(H32, dtype=np.float64)
-    T, E = H.shape
-    f = np.asarray(f, dtype=np.float64)
-    s = scores(H, score_fn)
-    if score_fn == SOFTMAX:
-        return E / T * s * (f[None, :] - (s * f[None, :]).sum(axis=1, keepdims=True))
-    sp = s / s.sum(axis=1, keepdims=True)
-    return E / T * sp * (1.0 - s) * (f[None, :] - (sp * f[None, :]).sum(axis=1, keepdims=True))
-
-
-def z_loss_grad(H32) -> np.ndarray:
-    """dL_z/dH [T, E] = (2/T) LSE(H_t) softmax(H_t) ([ZL])."""
-    H = np.asarray(H32, dtype=np.float64)
-    T = H.shape[0]
-    m = H.max(axis=1, keepdims=True)
-    lse = m + np.log(np.exp(H - m).sum(axis=1, keepdims=True))
-    return 2.0 / T * lse * scores(H, SOFTMAX)
-
-
-def router_backward(H32, idx, d_gate, f, score_fn: int, renorm: bool, w_aux: float = 0.0,
-                    w_z: float = 0.0) -> np.ndarray:
-    """dL/dH for L = (the loss through the gates) + w_aux * E sum f P + w_z * L_z."""
-    dH = gate_backward(H32, idx, d_gate, score_fn, renorm)
-    if w_aux:
-        dH = dH + w_aux * aux_loss_grad(H32, f, score_fn)
-    if w_z:
-        dH = dH + w_z * z_loss_grad(H32)
-    return dH
-
-
-# --------------------------------------------------------------------------
-# Backward of the experts and of the dispatch  [BWD], [FFN]
-# --------------------------------------------------------------------------
-
-def swiglu_backward(x, W_gate_e, W_up_e, W_down_e, dy) -> dict:
-    """Gradients of y = W_down (SiLU(W_gate x) * W_up x) for rows x [n, h] and dL/dy [n, h].
-
-    With G = x W_gate^T, Up = x W_up^T, s = sigmoid(G), a = G s Up:
-      d_act = dy W_down, dW_down = dy^T a,
-      dUp = d_act * G s, dG = d_act * Up * s (1 + G (1 - s)),
-      dx = dG W_gate + dUp W_up, dW_gate = dG^T x, dW_up = dUp^T x.
-    """
-    x, Wg, Wu, Wd, dy = f64(x), f64(W_gate_e), f64(W_up_e), f64(W_down_e), f64(dy)
-    G = x @ Wg.T
-    Up = x @ Wu.T
-    with np.errstate(over="ignore"):
-        sg = 1.0 / (1.0 + np.exp(-G))
-    silu_g = G * sg
-    act = silu_g * Up
-    d_act = dy @ Wd
-    dUp = d_act * silu_g
-    dG = d_act * Up * sg * (1.0 + G * (1.0 - sg))
-    return dict(d_act=d_act, dG=dG, dUp=dUp, dx=dG @ Wg + dUp @ Wu, dW_gate=dG.T @ x, dW_up=dUp.T @ x,
-                dW_down=dy.T @ act)
-
-
-def expert_ffn_backward(X, offsets, W_gate, W_up, W_down, dY, d_e: int) -> dict:
-    """The grouped backward over the expert segments: per row d_act, dG, dUp, dX; per expert
-    dW_gate [E, d_e, h], dW_up [E, d_e, h], dW_down [E, h, d_e] (zero for an expert with no rows)."""
-    X, dY = f64(X), f64(dY)
-    offsets = np.asarray(offsets, dtype=np.int64)
-    E = len(offsets) - 1
-    A, h = X.shape
-    out = dict(d_act=np.zeros((A, d_e)), dG=np.zeros((A, d_e)), dUp=np.zeros((A, d_e)), dX=np.zeros((A, h)),
-               dW_gate=np.zeros((E, d_e, h)), dW_up=np.zeros((E, d_e, h)), dW_down=np.zeros((E, h, d_e)))
-    for e in range(E):
-        lo, hi = int(offsets[e]), int(offsets[e + 1])
-        if hi > lo:
-            b = swiglu_backward(X[lo:hi], W_gate[e], W_up[e], W_down[e], dY[lo:hi])
-            out["d_act"][lo:hi], out["dG"][lo:hi], out["dUp"][lo:hi] = b["d_act"], b["dG"], b["dUp"]
-            out["dX"][lo:hi] = b["dx"]
-            out["dW_gate"][e], out["dW_up"][e], out["dW_down"][e] = b["dW_gate"], b["dW_up"], b["dW_down"]
-    return out
-
-
-def dispatch_backward(dO, dX, slot_row, k: int) -> np.ndarray:
-    """dL/dU from the residual and the permute: dU_t = dO_t + sum_{kept j} dX[row(t, j)] (X = U[perm])."""
-    dU = f64(dO).copy()
-    T = dU.shape[0]
-    sr = np.asarray(slot_row, dtype=np.int64).reshape(T, k)
-    dX = f64(dX)
-    for j in range(k):
-        m = sr[:, j] >= 0
-        dU[m] += dX[sr[m, j]]
-    return dU
-
-
-def router_input_backward(U, W_r, dH, W_noise=None, eps=None) -> dict:
-    """Backward of the router linear H = U W_r + b_r (+ eps * softplus(U W_noise)) ([RTR]).
-
-    dU = dH W_r^T (+ dN W_noise^T), dW_r = U^T dH, db_r = sum_t dH, dW_noise = U^T dN with
-    dN = dH * eps * sigmoid(U W_noise) (softplus' = sigmoid).
-    """
-    U, W_r, dH = f64(U), f64(W_r), f64(dH)
-    out = dict(dU=dH @ W_r.T, dW_r=U.T @ dH, db_r=dH.sum(axis=0), dW_noise=None)
-    if W_noise is not None:
-        with np.errstate(over="ignore"):
-            sg = 1.0 / (1.0 + np.exp(-(U @ f64(W_noise))))
-        dN = dH * f64(eps) * sg
-        out["dU"] = out["dU"] + dN @ f64(W_noise).T
-        out["dW_noise"] = U.T @ dN
-    return out
-
-
-def layer_backward(inp, fwd: dict, dO, *, k: int, d_e: int, score_fn: int, renorm: bool, w_aux: float = 0.0,
-                   w_z: float = 0.0) -> dict:
-    """Gradients of L = <dO, out> + w_aux E sum_i f_i P_i + w_z L_z through the whole layer, with
-    the routing decisions (top-k set, slots, drops) held fixed.  `fwd` is layer_forward's result.
-    [GRD], [BWD], [SHR], [RTR]
-    """
-    cb = combine_backward(dO, fwd["Y"], fwd["slot_row"], fwd["gate"], k)
-    dH = router_backward(fwd["logits"], fwd["idx"], cb["d_gate"], fwd["f"], score_fn, renorm, w_aux, w_z)
-    eb = expert_ffn_backward(fwd["X"], fwd["offsets"], inp.W_gate, inp.W_up, inp.W_down, cb["dY"], d_e)
-    rb = router_input_backward(inp.U, inp.W_r, dH, inp.W_noise, inp.eps)
-    dU = dispatch_backward(dO, eb["dX"], fwd["slot_row"], k) + rb["dU"]
-    out = dict(dU=dU, d_gate=cb["d_gate"], dY=cb["dY"], dH=dH, dW_r=rb["dW_r"], db_r=rb["db_r"],
-               dW_noise=rb["dW_noise"], **{n: eb[n] for n in ("d_act", "dG", "dUp", "dX", "dW_gate", "dW_up",
-                                                              "dW_down")})
-    shared = getattr(inp, "shared", None)
-    if shared is not None:
-        Wg, Wu, Wd = shared
-        sh = [swiglu_backward(inp.U, Wg[i], Wu[i], Wd[i], dO) for i in range(len(Wg))]
-        for b in sh:
-            out["dU"] = out["dU"] + b["dx"]
-        out["dW_gate_sh"] = np.stack([b["dW_gate"] for b in sh])
-        out["dW_up_sh"] = np.stack([b["dW_up"] for b in sh])
-        out["dW_down_sh"] = np.stack([b["dW_down"] for b in sh])
-    return out
-
-
-def group_margins(aff: np.ndarray, n_group: int, topk_group: int, k: int) -> np.ndarray:
-    """Per token, the gap between the topk_group-th and the next group score (inf when every
-    group is kept).  Used by the tests to keep group decisions away from ties."""
-    if topk_group >= n_group:
-        return np.full(np.asarray(aff).shape[0], np.inf)
-    gs = -np.sort(-group_scores(aff, n_group, k // topk_group), axis=1)
-    return gs[:, topk_group - 1] - gs[:, topk_group]
-
-
-def topk_margins(H32: np.ndarray, k: int) -> np.ndarray:
-    """Smallest gap between adjacent values among each row's k+1 largest logits.
-
-    Used by the tests to keep end-to-end routing decisions away from ties:
-    a token whose margin is below the threshold is redrawn.
-    """
-    s = -np.sort(-np.asarray(H32, dtype=np.float64), axis=1)[:, :k + 1]
-    if s.shape[1] < 2:
-        return np.full(s.shape[0], np.inf)
-    return np.min(s[:, :-1] - s[:, 1:], axis=1)
+__all__ = ["Oracle", "build", "f64", "default", "SOFTMAX", "SIGMOID", "CHOICE_MAJOR", "TOKEN_MAJOR", "E4M3_MAX",
+           "STAGES", *_EXPORTS]

@@ -133,6 +133,16 @@ def pin_topk_bruteforce(O):
             assert list(idx[t]) == ref, (E, k, t, H[t], idx[t], ref)
 
 
+def pin_route_selects_on_float32_logits(O):
+    """Routing rounds the logits to float32 first (the library's logits are float32): 1 + 2^-30
+    rounds to 1, so it ties with a logit of 1 and the lower expert id wins; the rounded logits
+    are returned."""
+    H = np.array([[1.0, 1.0 + 2.0 ** -30, 0.5], [0.25, 1.0 + 2.0 ** -22, 1.0]])
+    r = O.route(H, 1, O.SOFTMAX, False)
+    assert r["idx"].tolist() == [[0], [1]]
+    assert r["logits"][0, 1] == 1.0 and r["logits"][1, 1] == 1.0 + 2.0 ** -22
+
+
 def pin_topk_ties(O):
     """Exact ties go to the lower expert id, for membership and for rank order."""
     H = np.array([[1.0, 3.0, 3.0, 2.0, 3.0],
@@ -637,6 +647,22 @@ def pin_fp8_layer_lossless_on_grid(O):
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["act"], b["act"])
     assert np.array_equal(b["U_s"], np.full(T, -7))
     assert np.array_equal(O.dequantize_rows_fp8(b["U_codes"], b["U_s"]), U)
+
+
+def pin_fp8_layer_is_the_composition_of_its_pinned_parts(O):
+    """The FP8 layer on random (off-grid) inputs equals the unquantised path applied to the
+    dequantised token rows (quantize_rows_fp8 / dequantize_rows_fp8) and to fp8_weights of W_gate
+    and W_up, both pinned above against torch's E4M3 cast; and it differs from the unquantised layer."""
+    rng = _rng(46)
+    T, h, E, k, d_e = 40, 16, 4, 2, 12
+    inp = _small_layer(rng, T, h, E, k, d_e)
+    kw = dict(T=T, h=h, E=E, k=k, d_e=d_e, score_fn=O.SOFTMAX, renorm=True, capacity_factor=1.0)
+    q = O.layer_forward(inp, fp8=True, **kw)
+    X = O.dequantize_rows_fp8(*O.quantize_rows_fp8(inp.U))[q["row_token"]]
+    Y, act = O.expert_ffn(X, q["offsets"], O.fp8_weights(inp.W_gate), O.fp8_weights(inp.W_up), inp.W_down, d_e)
+    assert np.array_equal(q["act"], act) and np.array_equal(q["Y"], Y)
+    assert np.array_equal(q["out"], O.combine(inp.U, Y, q["slot_row"], q["gate"], k))
+    assert not np.allclose(q["act"], O.layer_forward(inp, **kw)["act"], rtol=1e-3, atol=0)
 
 
 def pin_balance_bias_update(O):
