@@ -153,6 +153,31 @@ moe_status moe_route(const moe_config* cfg, const void* U, const void* W_r, cons
                      const float* logits_in, float* logits_out, int32_t* idx, float* gate, void* ws,
                      moe_stream_t stream);
 
+/* Bytes of the packed router weights of this config (host only, no CUDA call): 2 * N * h with
+ * N = E (noisy router: 2E) rounded up to a multiple of 16, when the config's router runs on the
+ * tensor cores (bf16 and N <= 256); 0 otherwise (moe_route then reads W_r as it is). */
+moe_status moe_router_pack_size(const moe_config* cfg, size_t* bytes);
+
+/* One-time packing of the router weights for the tensor-core router (section 路由器：打分、
+ * top-k、加权求和: H = U W_r, and the noise projection U W_noise of the noisy router).
+ *   W_r      [h, E] bf16               as for moe_route
+ *   W_noise  [h, E] bf16               noisy router only (cfg->noisy), else ignored
+ *   W_r_packed [N, h] bf16 out         caller-owned, moe_router_pack_size() bytes, 16-byte
+ *                                      aligned: row n < E is column n of W_r, row E + n (noisy)
+ *                                      column n of W_noise, the remaining rows zero
+ * Run it once after the weights change; moe_route_packed and moe_layer_forward (args->W_r_packed)
+ * then skip the per-call packing.  MOE_ERR_UNSUPPORTED when moe_router_pack_size() is 0. */
+moe_status moe_pack_router(const moe_config* cfg, const void* W_r, const void* W_noise, void* W_r_packed,
+                           moe_stream_t stream);
+
+/* moe_route from packed router weights (moe_pack_router): the same results as moe_route with
+ * the weights that were packed, bit for bit.  No stage mode (logits_in).  One kernel: the
+ * router GEMM on the tensor cores with the scores, top-k, gates and the P / z partials in its
+ * epilogue. */
+moe_status moe_route_packed(const moe_config* cfg, const void* U, const void* W_r_packed, const float* b_r,
+                            const float* sel_bias, const float* eps, float* logits_out, int32_t* idx,
+                            float* gate, void* ws, moe_stream_t stream);
+
 /* One step of the loss-free balancing bias (section 无辅助损失的负载均衡):
  *   bias[i] += u * sign(mean(counts_routed) - counts_routed[i]),
  * the sign taken exactly on the integer counts.  counts_routed [E] int32 (e.g. from
@@ -368,6 +393,8 @@ typedef struct moe_layer_args {
   const float* sel_bias;                      /* NULL: no loss-free selection bias */
   const void* W_gate_shared; const void* W_up_shared; const void* W_down_shared;
   void* act_shared; void* Y_shared;           /* used when cfg->n_shared > 0 */
+  const void* W_r_packed;                     /* NULL, or W_r (and W_noise) from moe_pack_router:
+                                               * then the router skips its per-call packing */
 } moe_layer_args;
 
 /* The whole layer: moe_route, moe_dispatch, moe_expert_ffn, (moe_shared_ffn,)

@@ -27,7 +27,8 @@ EXPORTS = ("moe_version", "moe_status_string", "moe_last_error", "moe_capacity",
            "moe_shared_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status", "moe_combine_backward",
            "moe_route_backward", "moe_expert_ffn_backward", "moe_dispatch_backward", "moe_router_input_backward",
            "moe_layer_backward", "moe_quantize_fp8", "moe_dispatch_fp8", "moe_expert_ffn_fp8",
-           "moe_layer_forward_fp8", "moe_expert_ffn_gather")
+           "moe_layer_forward_fp8", "moe_expert_ffn_gather", "moe_router_pack_size", "moe_pack_router",
+           "moe_route_packed")
 
 
 class MoeError(RuntimeError):
@@ -52,7 +53,7 @@ class moe_layer_args(ctypes.Structure):
         "U", "W_r", "b_r", "W_noise", "eps", "W_gate", "W_up", "W_down", "logits_out", "idx", "gate",
         "counts_routed", "counts_kept", "offsets", "slot_row", "row_token", "n_dropped", "X", "act", "Y",
         "out", "f", "P", "aux", "z_loss", "sel_bias", "W_gate_shared", "W_up_shared", "W_down_shared",
-        "act_shared", "Y_shared")]
+        "act_shared", "Y_shared", "W_r_packed")]
 
 
 class moe_fp8_args(ctypes.Structure):
@@ -83,6 +84,12 @@ def _load() -> ctypes.CDLL:
     lib.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(SZ)]
     lib.moe_route.restype = S
     lib.moe_route.argtypes = [cfgp] + [_P] * 10 + [_P, _P]
+    lib.moe_router_pack_size.restype = S
+    lib.moe_router_pack_size.argtypes = [cfgp, ctypes.POINTER(SZ)]
+    lib.moe_pack_router.restype = S
+    lib.moe_pack_router.argtypes = [cfgp, _P, _P, _P, _P]
+    lib.moe_route_packed.restype = S
+    lib.moe_route_packed.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
     lib.moe_balance_bias_update.restype = S
     lib.moe_balance_bias_update.argtypes = [cfgp, _P, ctypes.c_float, _P, _P]
     lib.moe_shared_ffn.restype = S
@@ -241,6 +248,37 @@ def moe_dispatch_noalloc(cfg, U, idx, counts_routed, counts_kept, offsets, slot_
                                     _ptr(status, "status", torch.int32, 1), _stream(stream)))
 
 
+def router_pack_size(cfg: moe_config) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.moe_router_pack_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def moe_pack_router(cfg, W_r, W_noise, stream=None) -> Optional[torch.Tensor]:
+    """The router weights packed once for the tensor-core router ([N, h] bf16), or None when the
+    config's router reads W_r as it is."""
+    n = router_pack_size(cfg)
+    if n == 0:
+        return None
+    dt = _act_dtype(cfg)
+    out = torch.empty(n // 2, dtype=torch.bfloat16, device=W_r.device)
+    _check(lib.moe_pack_router(ctypes.byref(cfg), _ptr(W_r, "W_r", dt, cfg.h * cfg.E),
+                               _ptr(W_noise, "W_noise", dt, cfg.h * cfg.E) if cfg.noisy else None,
+                               _ptr(out, "W_r_packed"), _stream(stream)))
+    return out
+
+
+def moe_route_packed(cfg, U, W_r_packed, b_r, eps, logits_out, idx, gate, ws, stream=None, sel_bias=None):
+    dt = _act_dtype(cfg)
+    T, E, k, h = cfg.T, cfg.E, cfg.k, cfg.h
+    _check(lib.moe_route_packed(ctypes.byref(cfg), _ptr(U, "U", dt, T * h), _ptr(W_r_packed, "W_r_packed"),
+                                _ptr(b_r, "b_r", torch.float32, E), _ptr(sel_bias, "sel_bias", torch.float32, E),
+                                _ptr(eps, "eps", torch.float32, T * E) if cfg.noisy else None,
+                                _ptr(logits_out, "logits_out", torch.float32, T * E),
+                                _ptr(idx, "idx", torch.int32, T * k), _ptr(gate, "gate", torch.float32, T * k),
+                                _ptr(ws, "ws"), _stream(stream)))
+
+
 def moe_balance_bias_update(cfg, counts_routed, u, bias, stream=None):
     """bias += u * sign(mean(counts) - counts), in place on the device."""
     _check(lib.moe_balance_bias_update(ctypes.byref(cfg), _ptr(counts_routed, "counts_routed", torch.int32, cfg.E),
@@ -369,14 +407,15 @@ class LayerBuffers:
 
 
 def moe_layer_forward(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: LayerBuffers, stream=None,
-                      sel_bias=None, shared=None):
-    """The whole layer.  sel_bias: [E] loss-free selection bias; shared: (W_gate_sh, W_up_sh, W_down_sh)."""
-    a = layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs, sel_bias, shared)
+                      sel_bias=None, shared=None, W_r_packed=None):
+    """The whole layer.  sel_bias: [E] loss-free selection bias; shared: (W_gate_sh, W_up_sh, W_down_sh);
+    W_r_packed: the router weights from moe_pack_router (None: packed on each call)."""
+    a = layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs, sel_bias, shared, W_r_packed)
     _check(lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(a), _ptr(bufs.ws, "ws"), _stream(stream)))
 
 
 def layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: LayerBuffers, sel_bias=None,
-               shared=None) -> moe_layer_args:
+               shared=None, W_r_packed=None) -> moe_layer_args:
     """The moe_layer_args of one layer (inputs, weights and every buffer of `bufs`)."""
     dt = _act_dtype(cfg)
     T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
@@ -405,7 +444,8 @@ def layer_args(cfg, U, W_r, b_r, W_noise, eps, W_gate, W_up, W_down, bufs: Layer
         W_gate_shared=_ptr(sg, "W_gate_shared", dt, ns * ds * h), W_up_shared=_ptr(su, "W_up_shared", dt, ns * ds * h),
         W_down_shared=_ptr(sd, "W_down_shared", dt, ns * h * ds),
         act_shared=_ptr(bufs.act_shared, "act_shared", dt, ns * T * ds) if ns else None,
-        Y_shared=_ptr(bufs.Y_shared, "Y_shared", dt, ns * T * h) if ns else None)
+        Y_shared=_ptr(bufs.Y_shared, "Y_shared", dt, ns * T * h) if ns else None,
+        W_r_packed=_ptr(W_r_packed, "W_r_packed"))
     return a
 
 
@@ -495,9 +535,9 @@ def moe_expert_ffn_fp8(cfg, X8, x_scale, offsets, w8: FP8Weights, W_down, act, Y
 
 
 def moe_layer_forward_fp8(cfg, U, W_r, b_r, W_noise, eps, w8: FP8Weights, W_down, bufs: LayerBuffers, rows: FP8Rows,
-                          stream=None, sel_bias=None, shared=None):
+                          stream=None, sel_bias=None, shared=None, W_r_packed=None):
     """The whole layer with the FP8 dispatch and up-projection (bufs.X is not used)."""
-    a = layer_args(cfg, U, W_r, b_r, W_noise, eps, None, None, W_down, bufs, sel_bias, shared)
+    a = layer_args(cfg, U, W_r, b_r, W_noise, eps, None, None, W_down, bufs, sel_bias, shared, W_r_packed)
     T, E, k, h, d = cfg.T, cfg.E, cfg.k, cfg.h, cfg.d_e
     f = moe_fp8_args(X8=_ptr(rows.X8, "X8", torch.uint8, T * k * h),
                      x_scale=_ptr(rows.x_scale, "x_scale", torch.float32, T * k),

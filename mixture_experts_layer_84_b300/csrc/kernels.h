@@ -53,6 +53,10 @@ struct Plan {
   int route_rowblocks = 0; // ceil(T / route_bt)
   int route_splits = 0;    // split of h across blocks (summed in fixed order by the select kernel)
   int route_tc_n = 0;      // > 0: bf16 logits on the tensor cores with this MMA width (E or 2E rounded up to 16)
+  bool route_fused = false;// the fused router (route_tc.cu): logits, scores, top-k and gates in one kernel
+  int rf_tiles = 0;        // its 128-token tiles
+  int rf_cs = 0;           // CTAs per tile (a cluster), each with a slice of h
+  int rf_stages = 0;       // its TMA ring depth
   int sel_threads = 0;     // threads per select block (G lanes per token)
   int sel_tokens = 0;      // tokens per select block
   int sel_blocks = 0;      // ceil(T / sel_tokens): number of P partial rows
@@ -71,9 +75,21 @@ struct Plan {
 // Validates the config and fills `plan`; on failure returns the status and a message.
 moe_status make_plan(const moe_config* cfg, Plan* plan, const char** msg);
 
+// W_r_packed: the router weights from launch_pack_router (NULL: packed into the workspace on each
+// call when the fused router runs).
 cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const float* sel_bias,
                          const void* W_noise, const float* eps, const float* logits_in, float* logits_out,
-                         int32_t* idx, float* gate, uint8_t* ws, cudaStream_t s);
+                         int32_t* idx, float* gate, uint8_t* ws, cudaStream_t s, const void* W_r_packed = nullptr);
+
+// Router weights for the tensor cores: Wt [route_tc_n, h] bf16, K-major (W_r transposed, W_noise
+// transposed below it, zero rows up to route_tc_n).
+cudaError_t launch_pack_router(const Plan& p, const void* W_r, const void* W_noise, void* Wt, cudaStream_t s);
+// The fused router (bf16, route_tc_n > 0) from packed weights Wt.
+cudaError_t launch_route_fused(const Plan& p, const void* U, const void* Wt, const float* b_r, const float* sel_bias,
+                               const float* eps, float* logits_out, int32_t* idx, float* gate, uint8_t* ws,
+                               cudaStream_t s);
+// Dynamic shared memory of one fused-router CTA.
+size_t fused_router_smem(int N, int E, int n_group, int stages);
 
 // Router slice sums U W_r (and U W_noise) on the tensor cores (bf16, p.route_tc_n > 0).
 cudaError_t launch_route_logits_tc(const Plan& p, const void* U, const void* W_r, const void* W_noise, float* part,

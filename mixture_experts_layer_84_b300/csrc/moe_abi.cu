@@ -168,6 +168,17 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 16)));
   }
   q.route_splits = splits;
+  // the fused router: one 128-token tile per cluster of rf_cs CTAs, each CTA a slice of h (at least
+  // two 64-wide K-blocks), clusters of up to 8 while the grid stays within about one wave
+  if (q.route_tc_n > 0) {
+    q.route_fused = true;
+    q.rf_tiles = static_cast<int>((q.T + 127) / 128);
+    const int nkb = (q.h + 63) / 64;
+    int cs = 1;
+    while (cs < 8 && static_cast<int64_t>(q.rf_tiles) * cs * 2 <= 160 && nkb >= cs * 4) cs *= 2;
+    q.rf_cs = cs;
+    q.rf_stages = 4;
+  }
   // selection blocks: 256 threads, fewer (down to a warp) when T is small, so that the
   // blocks still spread over about twice the SMs
   {
@@ -196,7 +207,8 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   q.ws_npart = off;
   if (q.noisy) off += align256(logits_bytes);
   q.ws_ppart = off;
-  off += align256(sizeof(float) * static_cast<size_t>(q.sel_blocks) * (q.E + 1));
+  const int64_t ppart_rows = std::max<int64_t>(q.sel_blocks, static_cast<int64_t>(q.rf_tiles) * q.rf_cs);
+  off += align256(sizeof(float) * static_cast<size_t>(ppart_rows) * (q.E + 1));
   q.ws_hist = off;
   off += align256(sizeof(int32_t) * static_cast<size_t>(q.n_chunks) * q.E);
   q.ws_wt = off;
@@ -373,6 +385,48 @@ MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
   if (!bytes) return moe::fail(MOE_ERR_INVALID_ARG, "moe_workspace_size: bytes is NULL");
   *bytes = p.ws_total;
   return MOE_OK;
+}
+
+MOE_API moe_status moe_router_pack_size(const moe_config* cfg, size_t* bytes) {
+  Plan p;
+  CHECK(moe::plan_or_fail("moe_router_pack_size", cfg, &p));
+  if (!bytes) return moe::fail(MOE_ERR_INVALID_ARG, "moe_router_pack_size: bytes is NULL");
+  *bytes = p.route_tc_n > 0 ? sizeof(uint16_t) * static_cast<size_t>(p.route_tc_n) * p.h : 0;
+  return MOE_OK;
+}
+
+MOE_API moe_status moe_pack_router(const moe_config* cfg, const void* W_r, const void* W_noise, void* W_r_packed,
+                                   moe_stream_t stream) {
+  static const char* fn = "moe_pack_router";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (p.route_tc_n == 0)
+    return moe::fail(MOE_ERR_UNSUPPORTED, "%s: this config's router reads W_r as it is (float32, or > 256 columns)",
+                     fn);
+  const size_t wbytes = sizeof(uint16_t) * static_cast<size_t>(p.h) * p.E;
+  CHECK(moe::check_ptr(fn, "W_r", W_r, wbytes, 2));
+  if (p.noisy) CHECK(moe::check_ptr(fn, "W_noise", W_noise, wbytes, 2));
+  CHECK(moe::check_ptr(fn, "W_r_packed", W_r_packed, sizeof(uint16_t) * static_cast<size_t>(p.route_tc_n) * p.h, 16));
+  const cudaError_t e = moe::launch_pack_router(p, W_r, W_noise, W_r_packed, stream);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
+}
+
+MOE_API moe_status moe_route_packed(const moe_config* cfg, const void* U, const void* W_r_packed, const float* b_r,
+                                    const float* sel_bias, const float* eps, float* logits_out, int32_t* idx,
+                                    float* gate, void* ws, moe_stream_t stream) {
+  static const char* fn = "moe_route_packed";
+  Plan p;
+  CHECK(moe::plan_or_fail(fn, cfg, &p));
+  if (!p.route_fused)
+    return moe::fail(MOE_ERR_UNSUPPORTED, "%s: this config's router does not use packed weights", fn);
+  // W_r and W_noise are replaced by the packed matrix: pass it for both pointer checks
+  CHECK(moe::check_route_args(fn, p, U, W_r_packed, W_r_packed, eps, nullptr, logits_out, idx, gate, ws));
+  CHECK(moe::check_ptr(fn, "W_r_packed", W_r_packed, sizeof(uint16_t) * static_cast<size_t>(p.route_tc_n) * p.h, 16));
+  CHECK(moe::check_ptr(fn, "b_r", b_r, 0, 4));
+  CHECK(moe::check_ptr(fn, "sel_bias", sel_bias, 0, 4));
+  const cudaError_t e = moe::launch_route(p, U, nullptr, b_r, sel_bias, nullptr, eps, nullptr, logits_out, idx, gate,
+                                          static_cast<uint8_t*>(ws), stream, W_r_packed);
+  return e == cudaSuccess ? MOE_OK : moe::cuda_fail(fn, e);
 }
 
 MOE_API moe_status moe_route(const moe_config* cfg, const void* U, const void* W_r, const float* b_r,
@@ -723,7 +777,7 @@ MOE_API moe_status moe_layer_forward(const moe_config* cfg, const moe_layer_args
                                a->Y_shared));
   uint8_t* w = static_cast<uint8_t*>(ws);
   cudaError_t e = moe::launch_route(p, a->U, a->W_r, a->b_r, a->sel_bias, a->W_noise, a->eps, nullptr, a->logits_out,
-                                    a->idx, a->gate, w, stream);
+                                    a->idx, a->gate, w, stream, a->W_r_packed);
   if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward/route", e);
   e = moe::launch_dispatch(p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row, a->row_token,
                            a->X, a->n_dropped, w, stream);
@@ -848,7 +902,7 @@ MOE_API moe_status moe_layer_forward_fp8(const moe_config* cfg, const moe_layer_
                                a->Y_shared));
   uint8_t* w = static_cast<uint8_t*>(ws);
   cudaError_t e = moe::launch_route(p, a->U, a->W_r, a->b_r, a->sel_bias, a->W_noise, a->eps, nullptr, a->logits_out,
-                                    a->idx, a->gate, w, stream);
+                                    a->idx, a->gate, w, stream, a->W_r_packed);
   if (e != cudaSuccess) return moe::cuda_fail("moe_layer_forward_fp8/route", e);
   e = moe::launch_dispatch(p, a->U, a->idx, a->counts_routed, a->counts_kept, a->offsets, a->slot_row, a->row_token,
                            nullptr, a->n_dropped, w, stream);

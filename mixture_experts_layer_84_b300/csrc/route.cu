@@ -27,6 +27,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "select.cuh"
 
 namespace moe {
 
@@ -168,39 +169,15 @@ __global__ void __launch_bounds__(256) route_partial_logits(const T* __restrict_
   }
 }
 
-__device__ __forceinline__ float softplus_f32(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
-
-constexpr int KMAX = 16;
-
-// (value, expert id) order of the selection: larger value first, equal values
-// by the lower expert id.
-__device__ __forceinline__ bool before(float av, int ai, float bv, int bi) {
-  return av > bv || (av == bv && ai < bi);
-}
-
 // Selection over G lanes per token, TB = blockDim.x / G tokens per block.
-//   1. the block stages the tile's final logits in shared memory with
-//      coalesced loads: slice sums added in slice order, + bias, + eps *
-//      softplus(noise slice sums) (or the given logits in stage mode); the
-//      logits also go to logits_out here.  Lane g of a token owns the
-//      expert chunk [g C, (g+1) C), C = ceil(E / G), stored with an odd
-//      stride CS so that the 32 lanes of a warp hit 32 different banks;
-//   2. the G lanes of a token combine their chunks' maxima and exp-sums with
-//      xor shuffles; each lane keeps a running top-KP list of its chunk
-//      (insertion) keyed by the logit, or, given a selection bias (the
-//      loss-free balancing of section 无辅助损失的负载均衡), by score + bias;
-//      the lanes merge their lists (a bitonic merge: the elementwise better
-//      of one list and the other reversed is bitonic and holds the top KP of
-//      both); the gates come from the selected experts' scores; then the
-//      normalised scores are written back;
-//   3. the block adds each expert's column over its tokens in order (the
-//      score sums for P_i), and in column E the tokens' squared log-sum-exp
-//      of the logits (the router z-loss of "MoE 与专家并行", section Router
-//      z-loss 与数值稳定: L_z = (1/T) sum_t LSE(H_t)^2).
-// KP = k rounded up to a power of two (the lists live in registers); ppart
-// rows are E + 1 floats wide.  Scores use the fast exponential (a few ulps;
-// the selection itself compares logits, or score + bias with a margin far
-// above that).
+//   1. the block stages the tile's final logits in shared memory with coalesced loads: slice sums
+//      added in slice order, + bias, + eps * softplus(noise slice sums) (or the given logits in
+//      stage mode); the logits also go to logits_out here;
+//   2. select_tokens (select.cuh): scores, the top-k (logits, or score + bias with a selection
+//      bias; limited to the best groups with n_group > 1), gates, normalised scores, LSE^2;
+//   3. score_column_sums: the block's per-expert score sums and LSE^2 sum in a ppart row (E + 1
+//      floats) for moe_combine's statistics.
+// KP = k rounded up to a power of two (the lists live in registers).
 template <int KP, int G>
 __global__ void __launch_bounds__(SELECT_THREADS) route_select(
     const float* __restrict__ part, const float* __restrict__ npart, int splits, const float* __restrict__ b_r,
@@ -210,14 +187,10 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
     int topk_group) {
   const int TB = static_cast<int>(blockDim.x) / G;
   extern __shared__ float sx[];  // [TB][LD], then zsq[TB], then (groups) gsc[TB][n_group]
-  const int C = (E + G - 1) / G;
-  const int CS = (C & 1) ? C + 2 : C + 1;  // odd
-  const int LD = G * CS;
-  float* zsq = sx + TB * LD;
+  const SelLayout L(E, G);
+  float* zsq = sx + TB * L.LD;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TB;
   const int rows = static_cast<int>(n_tok - t0 < TB ? n_tok - t0 : TB);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NW = static_cast<int>(blockDim.x) / 32;
   if (blockIdx.x == 0 && threadIdx.x == 0) *ppart_rows = static_cast<int32_t>(gridDim.x);
 
   // 1. final logits of the tile; rows t0 .. t0 + rows - 1 are contiguous in every input, so the
@@ -229,230 +202,43 @@ __global__ void __launch_bounds__(SELECT_THREADS) route_select(
 #pragma unroll 2
   for (int i = threadIdx.x; i < n_el; i += blockDim.x) {
     const int r = e_pow2 ? i >> e_shift : i / E, e = i - r * E;
-    {
-      const int64_t g = t0 * E + i;
-      float x;
-      if (logits_in) {
-        x = logits_in[g];
-      } else {
-        // every slice's value is loaded before any is added (one memory latency, not `splits`),
-        // then added in slice order
-        const int64_t stride = n_tok * E;
-        float v[16];
+    const int64_t g = t0 * E + i;
+    float x;
+    if (logits_in) {
+      x = logits_in[g];
+    } else {
+      // every slice's value is loaded before any is added (one memory latency, not `splits`),
+      // then added in slice order
+      const int64_t stride = n_tok * E;
+      float v[16];
 #pragma unroll
-        for (int sp = 0; sp < 16; ++sp) v[sp] = sp < splits ? part[sp * stride + g] : 0.f;
-        x = v[0];
+      for (int sp = 0; sp < 16; ++sp) v[sp] = sp < splits ? part[sp * stride + g] : 0.f;
+      x = v[0];
+#pragma unroll
+      for (int sp = 1; sp < 16; ++sp)
+        if (sp < splits) x += v[sp];
+      if (b_r) x += b_r[e];
+      if (npart) {
+#pragma unroll
+        for (int sp = 0; sp < 16; ++sp) v[sp] = sp < splits ? npart[sp * stride + g] : 0.f;
+        float nz = v[0];
 #pragma unroll
         for (int sp = 1; sp < 16; ++sp)
-          if (sp < splits) x += v[sp];
-        if (b_r) x += b_r[e];
-        if (npart) {
-#pragma unroll
-          for (int sp = 0; sp < 16; ++sp) v[sp] = sp < splits ? npart[sp * stride + g] : 0.f;
-          float nz = v[0];
-#pragma unroll
-          for (int sp = 1; sp < 16; ++sp)
-            if (sp < splits) nz += v[sp];
-          x = fmaf(eps[g], softplus_f32(nz), x);
-        }
+          if (sp < splits) nz += v[sp];
+        x = fmaf(eps[g], softplus_f32(nz), x);
       }
-      if (logits_out) logits_out[g] = x;
-      const int cg = e / C;
-      sx[r * LD + cg * CS + (e - cg * C)] = x;
     }
+    if (logits_out) logits_out[g] = x;
+    sx[L.at(r, e)] = x;
   }
   __syncthreads();
 
-  // 2. G lanes per token: maximum, exp-sum and score denominator, then the top-k
-  const int r = threadIdx.x / G, g = threadIdx.x % G;
-  const bool tok = r < rows;
-  const int e0 = g * C;
-  const int e1 = min(E, e0 + C);
-  float* rowp = sx + r * LD;
-  float* chunk = rowp + g * CS;
-  const bool softmax = score_fn == MOE_SCORE_SOFTMAX;
-  float mx = -INFINITY;
-  if (tok)
-    for (int e = e0; e < e1; ++e) mx = fmaxf(mx, chunk[e - e0]);
-#pragma unroll
-  for (int o = 1; o < G; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum_exp = 0.f, denom = 0.f;
-  if (tok) {
-    for (int e = e0; e < e1; ++e) {
-      const float x = chunk[e - e0];
-      const float ex = __expf(x - mx);
-      sum_exp += ex;
-      denom += softmax ? ex : 1.f / (1.f + __expf(-x));
-    }
-  }
-#pragma unroll
-  for (int o = 1; o < G; o <<= 1) {
-    sum_exp += __shfl_xor_sync(0xffffffffu, sum_exp, o);
-    denom += __shfl_xor_sync(0xffffffffu, denom, o);
-  }
-  // group-limited routing: each group's score is the sum of its r = k / topk_group best
-  // affinities (score, + bias when selecting with one); a lane scores groups g, g + G, ...
-  // reading the token's staged row, then every lane of the token ranks all the groups
-  uint32_t keep = 0xffffffffu;
-  int gsz = E;  // experts per group
-  if (n_group > 1) {
-    gsz = E / n_group;
-    const int r_top = k / topk_group;
-    float* gs = zsq + TB + r * n_group;
-    if (tok) {
-      for (int q = g; q < n_group; q += G) {
-        float best[KP];
-#pragma unroll
-        for (int j = 0; j < KP; ++j) best[j] = -INFINITY;
-        for (int e = q * gsz; e < (q + 1) * gsz; ++e) {
-          const int cg = e / C;
-          const float x = rowp[cg * CS + (e - cg * C)];
-          float a = softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x));
-          if (sel_bias) a += sel_bias[e];
-#pragma unroll
-          for (int j = 0; j < KP; ++j) {
-            if (j < r_top && a > best[j]) {
-              const float t = best[j];
-              best[j] = a;
-              a = t;
-            }
-          }
-        }
-        float sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < KP; ++j)
-          if (j < r_top) sum += best[j];
-        gs[q] = sum;
-      }
-    }
-    __syncwarp();
-    keep = 0;
-    if (tok) {
-      for (int q = 0; q < n_group; ++q) {
-        const float v = gs[q];
-        int rank = 0;
-        for (int q2 = 0; q2 < n_group; ++q2) rank += (gs[q2] > v || (gs[q2] == v && q2 < q)) ? 1 : 0;
-        if (rank < topk_group) keep |= 1u << q;
-      }
-    }
-  }
-  // selection key: the logit, or with a selection bias (loss-free balancing) the score + bias
-  float tv[KP];
-  int ti[KP];
-#pragma unroll
-  for (int j = 0; j < KP; ++j) {
-    tv[j] = -INFINITY;
-    ti[j] = 0x7fffffff;
-  }
-  if (tok) {
-    int grp = e0 / gsz, grp_end = (grp + 1) * gsz;  // the group of expert e, tracked as e advances
-    for (int e = e0; e < e1; ++e) {
-      if (e == grp_end) {
-        ++grp;
-        grp_end += gsz;
-      }
-      if (!((keep >> grp) & 1u)) continue;  // outside the kept groups (never without groups: grp = 0)
-      const float x = chunk[e - e0];
-      const float key =
-          sel_bias ? (softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x))) + sel_bias[e] : x;
-      if (before(key, e, tv[KP - 1], ti[KP - 1])) {
-        float cv = key;
-        int ci = e;
-#pragma unroll
-        for (int j = 0; j < KP; ++j) {
-          if (before(cv, ci, tv[j], ti[j])) {
-            const float tvj = tv[j];
-            const int tij = ti[j];
-            tv[j] = cv;
-            ti[j] = ci;
-            cv = tvj;
-            ci = tij;
-          }
-        }
-      }
-    }
-  }
-  // combine the G lanes' lists (consecutive lanes of one warp)
-#pragma unroll
-  for (int o = 1; o < G; o <<= 1) {
-    float bv[KP];
-    int bi[KP];
-#pragma unroll
-    for (int j = 0; j < KP; ++j) {
-      bv[j] = __shfl_xor_sync(0xffffffffu, tv[KP - 1 - j], o);  // the partner's list, reversed
-      bi[j] = __shfl_xor_sync(0xffffffffu, ti[KP - 1 - j], o);
-    }
-#pragma unroll
-    for (int j = 0; j < KP; ++j) {
-      if (before(bv[j], bi[j], tv[j], ti[j])) {
-        tv[j] = bv[j];
-        ti[j] = bi[j];
-      }
-    }
-#pragma unroll
-    for (int st = KP / 2; st > 0; st >>= 1) {
-#pragma unroll
-      for (int j = 0; j < KP; ++j) {
-        if ((j & st) == 0 && before(tv[j + st], ti[j + st], tv[j], ti[j])) {
-          const float tvj = tv[j];
-          const int tij = ti[j];
-          tv[j] = tv[j + st];
-          ti[j] = ti[j + st];
-          tv[j + st] = tvj;
-          ti[j + st] = tij;
-        }
-      }
-    }
-  }
-  if (tok) {
-    // gates from the scores of the selected experts (their logits are in the staged row)
-    float sel_s[KP], sel_sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < KP; ++j) {
-      sel_s[j] = 0.f;
-      if (j < k) {
-        const int e = ti[j];
-        const int cg = e / C;
-        const float x = rowp[cg * CS + (e - cg * C)];
-        sel_s[j] = softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x));
-        sel_sum += sel_s[j];
-      }
-    }
-    const int64_t t = t0 + r;
-#pragma unroll
-    for (int j = 0; j < KP; ++j) {
-      if (j < k && j % G == g) {
-        idx[t * k + j] = ti[j];
-        gate[t * k + j] = renorm ? sel_s[j] / sel_sum : sel_s[j];
-      }
-    }
-  }
-  // every lane has read what it needs from the row before any lane overwrites its chunk
-  __syncwarp();
-  if (tok) {
-    for (int e = e0; e < e1; ++e) {
-      const float x = chunk[e - e0];
-      chunk[e - e0] = (softmax ? __expf(x - mx) : 1.f / (1.f + __expf(-x))) / denom;
-    }
-    if (g == 0) {
-      const float lse = mx + logf(sum_exp);
-      zsq[r] = lse * lse;
-    }
-  }
+  // 2. G lanes per token: scores, top-k, gates
+  select_tokens<KP, G>(sx, zsq, zsq + TB, rows, t0, E, k, score_fn, renorm, n_group, topk_group, sel_bias, idx, gate);
   __syncthreads();
 
   // 3. the tile's score sums and z-loss sum, tokens in order
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    float acc = 0.f;
-    if (e < E) {
-      const int cg = e / C;
-      const float* col = sx + cg * CS + (e - cg * C);
-      for (int i = 0; i < rows; ++i) acc += col[i * LD];
-    } else {
-      for (int i = 0; i < rows; ++i) acc += zsq[i];
-    }
-    ppart[static_cast<int64_t>(blockIdx.x) * (E + 1) + e] = acc;
-  }
+  score_column_sums(sx, zsq, rows, E, G, ppart + static_cast<int64_t>(blockIdx.x) * (E + 1), false);
 }
 
 namespace {
@@ -529,8 +315,18 @@ cudaError_t launch_select_kp(const Plan& p, const float* part, const float* npar
 
 cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const float* sel_bias,
                          const void* W_noise, const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
-                         uint8_t* ws, cudaStream_t s) {
+                         uint8_t* ws, cudaStream_t s, const void* W_r_packed) {
   if (p.T == 0) return cudaSuccess;
+  if (!logits_in && p.route_fused) {
+    const void* Wt = W_r_packed;
+    if (!Wt) {
+      void* w = ws + p.ws_wt;
+      const cudaError_t e = launch_pack_router(p, W_r, W_noise, w, s);
+      if (e != cudaSuccess) return e;
+      Wt = w;
+    }
+    return launch_route_fused(p, U, Wt, b_r, sel_bias, eps, logits_out, idx, gate, ws, s);
+  }
   float* part = reinterpret_cast<float*>(ws + p.ws_part);
   float* npart = p.noisy ? reinterpret_cast<float*>(ws + p.ws_npart) : nullptr;
   float* ppart = reinterpret_cast<float*>(ws + p.ws_ppart);

@@ -27,6 +27,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "select.cuh"
 
 namespace moe {
 namespace rtc {
@@ -280,6 +281,296 @@ cudaError_t launch_route_logits_tc(const Plan& p, const void* U, const void* W_r
 #undef MOE_RTC_CASE
   }
   return cudaErrorInvalidValue;
+}
+
+
+// ---------------------------------------------------------------------------------------------
+// The fused router: logits on the tensor cores, then scores, top-k, gates and the P / z partials
+// in the epilogue, with no float32 logit round trip through global memory.
+//
+// A cluster of CS CTAs owns one 128-token tile; CTA c of the cluster runs the K-blocks
+// [c nkb / CS, (c+1) nkb / CS) of h through a TMA ring and tcgen05.mma 128 x N x 16 into its
+// tensor memory (N = E, or 2E with the noise columns, rounded up to 16).  Its four epilogue warps
+// copy the float32 accumulator into shared memory.  After a cluster barrier, CTA c takes the rows
+// [c R, (c+1) R), R = 128 / CS, and adds the CS slices of each logit in rank order (run-to-run
+// identical) through distributed shared memory, then the bias and the noise
+// eps * softplus(noise logit).  It stages them for select_tokens (select.cuh) in passes of
+// 256 / G tokens and adds its per-expert score sums and LSE^2 sum into one ppart row.  A second
+// cluster barrier keeps each CTA's shared memory alive until its peers have read it.
+namespace rfu {
+
+using namespace rtc;
+
+constexpr int THREADS = 256;  // warp 0 TMA, warp 1 MMA, warps 4-7 accumulator readout; all 8 select
+constexpr int MAX_STAGES = 8;
+constexpr size_t RF_BAR_BYTES = 256;  // full[8], empty[8], tfull, tensor-memory address, abort flag
+
+struct Geometry {
+  int N, stages, PN, TB, LD, sel_floats;
+  uint32_t stage_bytes;
+  size_t p_bytes, work, smem;
+};
+
+// Shared memory of the fused router: the TMA stages, reused after the main loop for the partial
+// tile P [128][N + 1] and the select staging (sx [TB][LD], zsq [TB], gsc [TB][n_group],
+// colsum [E + 1]), then the barriers.  G = lanes per token of the selection.
+__host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stages, int G) {
+  Geometry g;
+  g.N = N;
+  g.stages = stages;
+  g.stage_bytes = A_BYTES + b_bytes(N);
+  g.PN = N + 1;
+  g.TB = THREADS / G;
+  const int C = (E + G - 1) / G;
+  g.LD = G * ((C & 1) ? C + 2 : C + 1);
+  g.p_bytes = sizeof(float) * 128 * static_cast<size_t>(g.PN);
+  g.sel_floats = g.TB * g.LD + g.TB + g.TB * (n_group > 1 ? n_group : 0) + (E + 1);
+  const size_t ring = static_cast<size_t>(stages) * g.stage_bytes;
+  const size_t tail = g.p_bytes + sizeof(float) * static_cast<size_t>(g.sel_floats);
+  g.work = ((ring > tail ? ring : tail) + 15) / 16 * 16;
+  g.smem = 1024 + g.work + RF_BAR_BYTES;
+  return g;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int KP, int G>
+__global__ void __launch_bounds__(THREADS, 1)
+    route_fused(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW, int64_t T, int h,
+                int E, int N, int stages, int cs, const float* __restrict__ b_r, const float* __restrict__ sel_bias,
+                const float* __restrict__ eps, int noisy, float* __restrict__ logits_out, int32_t* __restrict__ idx,
+                float* __restrict__ gate, float* __restrict__ ppart, int32_t* __restrict__ ppart_rows, int k,
+                int score_fn, int renorm, int n_group, int topk_group, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Geometry geo = geometry(N, E, n_group, stages, G);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + geo.work);
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* tfull = empty + 8;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tfull + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* P = reinterpret_cast<float*>(smem);                       // [128][PN], after the main loop
+  float* sx = reinterpret_cast<float*>(smem + geo.p_bytes);       // select staging
+  float* zsq = sx + geo.TB * geo.LD;
+  float* gsc = zsq + geo.TB;
+  float* colsum = gsc + geo.TB * (n_group > 1 ? n_group : 0);
+
+  const uint32_t tmem_cols = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+  const uint32_t STAGE = geo.stage_bytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(blockIdx.x % cs);
+  const int64_t mt = blockIdx.x / cs;
+  const int nkb = (h + BK - 1) / BK;
+  const int kb_beg = (nkb * rank) / cs, kb_end = (nkb * (rank + 1)) / cs;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < stages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(tfull, 1);
+    ptx::fence_mbarrier_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmU);
+      ptx::prefetch_tmap(&tmW);
+      const uint64_t pol_u = ptx::policy_evict_first();
+      const uint64_t pol_w = ptx::policy_evict_last();
+      uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
+      for (int kb = kb_beg; kb < kb_end; ++kb) {
+        if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS)) break;
+        uint8_t* sa = smem + stage * STAGE;
+        ptx::mbar_arrive_expect_tx(&full[stage], STAGE);
+        ptx::tma_load_2d(sa, &tmU, kb * BK, static_cast<int32_t>(mt * BM), &full[stage], pol_u);
+        ptx::tma_load_2d(sa + A_BYTES, &tmW, kb * BK, 0, &full[stage], pol_w);
+        armed |= 1u << stage;
+        armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == static_cast<uint32_t>(stages)) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      for (int s = 0; s < stages; ++s)
+        if ((armed >> s) & 1u) wait_drain(&full[s], (armed_phase >> s) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t IDESC = ptx::idesc_bf16_f32(BM, N);
+      uint32_t stage = 0, phase = 0;
+      for (int kb = kb_beg; kb < kb_end; ++kb) {
+        if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_LIMIT_NS)) break;
+        ptx::tc_fence_after();
+        const uint32_t sa = ptx::smem_u32(smem + stage * STAGE);
+        const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / UK; ++kk)
+          ptx::mma_bf16_ss(tmem_base, ptx::sdesc_kmajor_sw128(sa + kk * UK * 2),
+                           ptx::sdesc_kmajor_sw128(sb + kk * UK * 2), IDESC, (kb > kb_beg || kk) ? 1u : 0u);
+        ptx::mma_commit(&empty[stage]);
+        if (++stage == static_cast<uint32_t>(stages)) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      ptx::mma_commit(tfull);  // complete (or drained after a timeout): the accumulator may be read
+    }
+    __syncwarp();
+  }
+  // every TMA write has landed and every MMA has read its stage before the stages become P
+  if (warp >= 4) {
+    const int q = warp & 3;
+    const bool ready = wait_drain(tfull, 0);
+    if (__all_sync(0xffffffffu, ready) && !*abort_flag) {
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      float* prow = P + (q * 32 + lane) * geo.PN;
+#pragma unroll 1
+      for (int c = 0; c < N; c += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tb + c, v);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c + i < N) prow[c + i] = __uint_as_float(v[i]);  // N is a multiple of 16, not of 32
+      }
+    } else {
+      *abort_flag = 1;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, tmem_cols);
+  const bool ok = !*abort_flag;
+  ptx::cluster_sync_all();  // every CTA's P is complete
+
+  // rows [rank R, (rank+1) R) of the tile: the CS slices summed in rank order, bias and noise added
+  const int R = BM / cs;
+  const int64_t row0 = mt * BM + static_cast<int64_t>(rank) * R;
+  const int64_t left = T - row0;
+  const int rows_here = left <= 0 ? 0 : left < R ? static_cast<int>(left) : R;
+  const uint32_t p_local = ptx::smem_u32(P);
+  if (ok) {
+    for (int p0 = 0; p0 < rows_here; p0 += geo.TB) {
+      const int rows = min(geo.TB, rows_here - p0);
+      const SelLayout L(E, G);
+      for (int i = threadIdx.x; i < rows * E; i += THREADS) {
+        const int r = i / E, e = i - r * E;
+        const int prow = rank * R + p0 + r;
+        const int64_t t = row0 + p0 + r;
+        float x = 0.f, z = 0.f;
+        for (int c = 0; c < cs; ++c) {
+          const uint32_t base = ptx::mapa_shared(p_local, static_cast<uint32_t>(c)) +
+                                static_cast<uint32_t>(prow * geo.PN + e) * 4u;
+          x += ld_cluster_f32(base);
+          if (noisy) z += ld_cluster_f32(base + static_cast<uint32_t>(E) * 4u);
+        }
+        if (b_r) x += b_r[e];
+        if (noisy) x = fmaf(eps[t * E + e], softplus_f32(z), x);
+        if (logits_out) logits_out[t * E + e] = x;
+        sx[L.at(r, e)] = x;
+      }
+      __syncthreads();
+      select_tokens<KP, G>(sx, zsq, gsc, rows, row0 + p0, E, k, score_fn, renorm, n_group, topk_group, sel_bias,
+                           idx, gate);
+      __syncthreads();
+      score_column_sums(sx, zsq, rows, E, G, colsum, p0 > 0);
+      __syncthreads();
+    }
+    if (rows_here == 0)
+      for (int e = threadIdx.x; e <= E; e += THREADS) colsum[e] = 0.f;
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += THREADS) ppart[static_cast<int64_t>(blockIdx.x) * (E + 1) + e] = colsum[e];
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ppart_rows = static_cast<int32_t>(gridDim.x);
+  if (threadIdx.x == 0 && !ok) set_status(status, MOE_DEV_TIMEOUT);
+  ptx::cluster_sync_all();  // peers have finished reading this CTA's P
+}
+
+template <int KP, int G>
+cudaError_t launch_fused_g(const Plan& p, const CUtensorMap& tmU, const CUtensorMap& tmW, const float* b_r,
+                           const float* sel_bias, const float* eps, float* logits_out, int32_t* idx, float* gate,
+                           float* ppart, int32_t* rows, int32_t* status, cudaStream_t s) {
+  const Geometry geo = geometry(p.route_tc_n, p.E, p.n_group, p.rf_stages, G);
+  auto kern = route_fused<KP, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(geo.smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(p.rf_tiles * p.rf_cs));
+  lc.blockDim = dim3(THREADS);
+  lc.dynamicSmemBytes = geo.smem;
+  lc.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = static_cast<unsigned>(p.rf_cs);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kern, tmU, tmW, p.T, p.h, p.E, p.route_tc_n, p.rf_stages, p.rf_cs, b_r, sel_bias,
+                            eps, p.noisy ? 1 : 0, logits_out, idx, gate, ppart, rows, p.k, p.score_fn, p.renorm,
+                            p.n_group, p.topk_group, status);
+}
+
+template <int KP>
+cudaError_t launch_fused_kp(const Plan& p, const CUtensorMap& tmU, const CUtensorMap& tmW, const float* b_r,
+                            const float* sel_bias, const float* eps, float* logits_out, int32_t* idx, float* gate,
+                            float* ppart, int32_t* rows, int32_t* status, cudaStream_t s) {
+  switch (select_lanes_for(p.E)) {
+#define MOE_RFU_G(gg) \
+  case gg: return launch_fused_g<KP, gg>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
+    MOE_RFU_G(1) MOE_RFU_G(2) MOE_RFU_G(4) MOE_RFU_G(8)
+#undef MOE_RFU_G
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace rfu
+
+size_t fused_router_smem(int N, int E, int n_group, int stages) {
+  return rfu::geometry(N, E, n_group, stages, select_lanes_for(E)).smem;
+}
+
+cudaError_t launch_pack_router(const Plan& p, const void* W_r, const void* W_noise, void* Wt, cudaStream_t s) {
+  const int N = p.route_tc_n;
+  rtc::route_pack_wt<<<dim3((N + 31) / 32, (p.h + 31) / 32), dim3(32, 8), 0, s>>>(
+      static_cast<const bf16*>(W_r), p.noisy ? static_cast<const bf16*>(W_noise) : nullptr, p.h, p.E, N,
+      static_cast<bf16*>(Wt));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_fused(const Plan& p, const void* U, const void* Wt, const float* b_r, const float* sel_bias,
+                               const float* eps, float* logits_out, int32_t* idx, float* gate, uint8_t* ws,
+                               cudaStream_t s) {
+  using namespace rtc;
+  if (p.T == 0) return cudaSuccess;
+  CUtensorMap tmU, tmW;
+  if (!make_tmap(&tmU, U, static_cast<uint64_t>(p.T), p.h, BM) || !make_tmap(&tmW, Wt, p.route_tc_n, p.h, p.route_tc_n))
+    return cudaErrorNotSupported;
+  float* ppart = reinterpret_cast<float*>(ws + p.ws_ppart);
+  int32_t* rows = ws_ppart_rows(p, ws);
+  int32_t* status = ws_status(p, ws);
+  if (p.k <= 2) return rfu::launch_fused_kp<2>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
+  if (p.k <= 4) return rfu::launch_fused_kp<4>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
+  if (p.k <= 8) return rfu::launch_fused_kp<8>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
+  return rfu::launch_fused_kp<16>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
 }
 
 }  // namespace moe

@@ -91,3 +91,27 @@ def margin_inputs(w: W.Workload, seed: int = 0, device="cuda", experts: bool = T
         synth.redraw_rows(inp, torch.as_tensor(bad, dtype=torch.int64), seed, attempt)
         H[bad] = logits_of(w, inp, bad)
     raise RuntimeError(f"could not reach the top-k margin for {w.name}")
+
+
+def check_routing_and_dispatch(w, bufs, H, sel_bias=None):
+    r = route_of(w, H, sel_bias)
+    C = oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.capacity)
+    d = oracle.dispatch(r["idx"], w.E, C, w.priority)
+    A = int(d["offsets"][-1])
+    if bufs.logits is not None:
+        assert normwise(bufs.logits, H) <= LOGIT_TOL
+    assert np.array_equal(bufs.idx.cpu().numpy(), r["idx"])
+    assert normwise(bufs.gate, r["gate"]) <= LOGIT_TOL
+    assert np.array_equal(bufs.counts_routed.cpu().numpy(), d["counts_routed"])
+    assert np.array_equal(bufs.counts_kept.cpu().numpy(), d["counts_kept"])
+    assert np.array_equal(bufs.offsets.cpu().numpy(), d["offsets"])
+    assert np.array_equal(bufs.slot_row.cpu().numpy(), d["slot_row"])
+    assert np.array_equal(bufs.row_token[:A].cpu().numpy(), d["row_token"])
+    assert int(bufs.n_dropped.item()) == d["n_dropped"]
+    st = oracle.load_stats(d["counts_routed"], r["s"], w.T, w.k, w.score_fn)
+    assert normwise(bufs.f, st["f"]) <= 1e-6
+    assert normwise(bufs.P, st["P"]) <= LOGIT_TOL
+    assert abs(float(bufs.aux.item()) - st["aux"]) <= LOGIT_TOL * max(1.0, abs(st["aux"]))
+    zl = oracle.router_z_loss(r["logits"])
+    assert abs(float(bufs.z_loss.item()) - zl) <= LOGIT_TOL * max(1.0, abs(zl))
+    return r, d, A

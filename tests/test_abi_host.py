@@ -45,7 +45,7 @@ def test_version_and_status_strings():
 
 def test_config_struct_layout():
     assert ctypes.sizeof(L.moe_config) == 8 + 4 * 15 + 4  # int64 T, 15 x 32-bit fields, tail padding
-    assert ctypes.sizeof(L.moe_layer_args) == 31 * 8
+    assert ctypes.sizeof(L.moe_layer_args) == 32 * 8
 
 
 @pytest.mark.parametrize("w", W.FULL + W.SMALL, ids=lambda w: w.name)

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import LOGIT_TOL, TOL, delta_error, margin_inputs, normwise, route_of
+from gpu_helpers import TOL, check_routing_and_dispatch, delta_error, margin_inputs, normwise
 from mixture_experts_layer_84_b300 import _lib as L
 from mixture_experts_layer_84_b300 import synth
 from mixture_experts_layer_84_b300 import workloads as W
@@ -27,30 +27,6 @@ def run_layer(w, inp, with_logits=True):
     code = L.moe_get_device_status(bufs.ws)
     assert code == 0, f"device status {code}"
     return cfg, bufs
-
-
-def check_routing_and_dispatch(w, bufs, H, sel_bias=None):
-    r = route_of(w, H, sel_bias)
-    C = oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.capacity)
-    d = oracle.dispatch(r["idx"], w.E, C, w.priority)
-    A = int(d["offsets"][-1])
-    if bufs.logits is not None:
-        assert normwise(bufs.logits, H) <= LOGIT_TOL
-    assert np.array_equal(bufs.idx.cpu().numpy(), r["idx"])
-    assert normwise(bufs.gate, r["gate"]) <= LOGIT_TOL
-    assert np.array_equal(bufs.counts_routed.cpu().numpy(), d["counts_routed"])
-    assert np.array_equal(bufs.counts_kept.cpu().numpy(), d["counts_kept"])
-    assert np.array_equal(bufs.offsets.cpu().numpy(), d["offsets"])
-    assert np.array_equal(bufs.slot_row.cpu().numpy(), d["slot_row"])
-    assert np.array_equal(bufs.row_token[:A].cpu().numpy(), d["row_token"])
-    assert int(bufs.n_dropped.item()) == d["n_dropped"]
-    st = oracle.load_stats(d["counts_routed"], r["s"], w.T, w.k, w.score_fn)
-    assert normwise(bufs.f, st["f"]) <= 1e-6
-    assert normwise(bufs.P, st["P"]) <= LOGIT_TOL
-    assert abs(float(bufs.aux.item()) - st["aux"]) <= LOGIT_TOL * max(1.0, abs(st["aux"]))
-    zl = oracle.router_z_loss(r["logits"])
-    assert abs(float(bufs.z_loss.item()) - zl) <= LOGIT_TOL * max(1.0, abs(zl))
-    return r, d, A
 
 
 EDGE = [
