@@ -189,9 +189,11 @@ def launches_per_step(w: W.Workload, gather: bool = False) -> int:
         return 2  # dispatch scan + statistics
     fused_router = w.dtype == W.BF16 and (2 * w.E if w.noisy else w.E) <= 256
     route = 1 if fused_router else 2       # the fused router (weights packed beforehand), or logits + selection
-    dispatch, ffn, combine = 4, 2, 2       # count, scan, assign, scatter; two GEMMs; rows + statistics
-    if gather:
-        dispatch = 3                       # no scatter: the first GEMM gathers the rows
+    if w.priority == W.PRIORITY_CHOICE_MAJOR:
+        dispatch = 2                       # histograms + scans, then slots + row copy (no copy when gathering)
+    else:
+        dispatch = 3 if gather else 4      # count, scan, assign (, scatter)
+    ffn, combine = 2, 1                    # two GEMMs; rows and statistics
     return route + dispatch + ffn + 2 * w.n_shared + combine
 
 

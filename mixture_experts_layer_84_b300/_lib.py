@@ -89,7 +89,7 @@ def _load() -> ctypes.CDLL:
     lib.moe_pack_router.restype = S
     lib.moe_pack_router.argtypes = [cfgp, _P, _P, _P, _P]
     lib.moe_route_packed.restype = S
-    lib.moe_route_packed.argtypes = [cfgp] + [_P] * 9 + [_P, _P]
+    lib.moe_route_packed.argtypes = [cfgp] + [_P] * 10
     lib.moe_balance_bias_update.restype = S
     lib.moe_balance_bias_update.argtypes = [cfgp, _P, ctypes.c_float, _P, _P]
     lib.moe_shared_ffn.restype = S

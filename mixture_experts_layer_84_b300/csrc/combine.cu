@@ -7,14 +7,13 @@
 // section 负载均衡辅助损失：推导与梯度: f_i, P_i = (1/T) sum_t s_{i,t} and
 // E * sum_i f_i P_i.
 //
-// combine_rows: one warp per token, 16-byte vectors; float32 accumulation of
-// u_t + (shared experts' rows) + g_0 y_0 + g_1 y_1 + ... in choice order,
-// rounded once (section 细粒度专家与共享专家: h'_t = u_t + sum_s FFN_s(u_t) +
-// sum_i g_{i,t} FFN_i(u_t)).
+// combine_stats: one launch.  Warps take (token, row segment) units; each lane issues the loads of
+// u_t, of the shared experts' rows and of the token's kept expert rows before accumulating
+// u_t + (shared experts' rows) + g_0 y_0 + g_1 y_1 + ... in float32, in choice order, rounded once
+// (section 细粒度专家与共享专家: h'_t = u_t + sum_s FFN_s(u_t) + sum_i g_{i,t} FFN_i(u_t)).  The
+// block that finishes last forms f_i, P_i, aux and the z-loss from the router's per-block sums in a
+// fixed order, so they are identical from run to run.
 // balance_bias_update: the loss-free balancing step of section 无辅助损失的负载均衡.
-// load_stats: one block per 32 experts (plus the z-loss column); P_i and L_z
-// sum the router's per-block partials in a fixed order, so they are
-// identical from run to run.
 #include <algorithm>
 
 #include "common.cuh"
@@ -22,18 +21,36 @@
 
 namespace moe {
 
-constexpr int COMBINE_UNROLL = 2;  // 4 measured slower with k = 6..8
+constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_UNROLL = 2;   // 16-byte vectors per lane per row stream in flight
+constexpr int COMBINE_GROUP = 4;    // routed rows whose loads are issued together
 
+// Row combine and statistics in one launch.
+//   Rows: a work unit is one segment of one token's row (segs segments per row, chosen so that
+//   small batches still fill the GPU); a warp takes units in turn, and each lane first issues the
+//   loads of its 16-byte vectors of u_t, of the shared experts' rows and of up to COMBINE_GROUP
+//   kept expert rows, then accumulates in float32 in a fixed order -- u_t, the shared rows in
+//   order, then g_j y_j for j ascending -- and rounds once.
+//   Statistics: the block that finishes last (an atomic count; nobody waits) adds each expert's
+//   column of the router's per-block score sums in block order (P_i, and the z-loss in column E),
+//   forms f_i from the routed counts and aux = E sum_i f_i P_i in expert order, and resets the
+//   count for the next call.  Every result is the same from run to run.
 template <typename T>
-__global__ void __launch_bounds__(256) combine_rows(const uint4* __restrict__ U, const uint4* __restrict__ Y,
-                                                    const uint4* __restrict__ Y_shared, int n_shared,
-                                                    const int32_t* __restrict__ slot_row,
-                                                    const float* __restrict__ gate, uint4* __restrict__ out, int64_t n_tok,
-                                                    int k, int vpr, int64_t rows_cap, int32_t* status) {
+__global__ void __launch_bounds__(COMBINE_THREADS, 2) combine_stats(
+    const uint4* __restrict__ U, const uint4* __restrict__ Y, const uint4* __restrict__ Y_shared, int n_shared,
+    const int32_t* __restrict__ slot_row, const float* __restrict__ gate, uint4* __restrict__ out, int64_t n_tok,
+    int k, int vpr, int segs, int64_t rows_cap, int32_t* status, const float* __restrict__ ppart,
+    const int32_t* __restrict__ ppart_rows, const int32_t* __restrict__ counts_routed, int E, float* __restrict__ f,
+    float* __restrict__ P, float* __restrict__ aux, float* __restrict__ z_loss, int32_t* __restrict__ done_count) {
   constexpr int N = Vec16<T>::N;
   const int lane = threadIdx.x % 32;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tok; t += warps) {
+  const int vps = (vpr + segs - 1) / segs;  // vectors per segment
+  const int64_t units = n_tok * segs;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; u < units; u += warps) {
+    const int64_t t = u / segs;
+    const int seg = static_cast<int>(u - t * segs);
+    const int v_lo = seg * vps, v_hi = min(vpr, v_lo + vps);
     int32_t my_row = -1;
     float my_g = 0.f;
     if (lane < k) {
@@ -44,78 +61,85 @@ __global__ void __launch_bounds__(256) combine_rows(const uint4* __restrict__ U,
         my_row = -1;
       }
     }
-    // warp-uniform trip count: every lane reaches the shuffles below
-    for (int base = 0; base < vpr; base += 32 * COMBINE_UNROLL) {
+    // warp-uniform trip counts: every lane reaches the shuffles
+    for (int base = v_lo; base < v_hi; base += 32 * COMBINE_UNROLL) {
       float acc[COMBINE_UNROLL][N];
+      uint4 uv[COMBINE_UNROLL];
 #pragma unroll
-      for (int u = 0; u < COMBINE_UNROLL; ++u) {
-        const int v = base + lane + 32 * u;
-        if (v < vpr) Vec16<T>::unpack(ldg_stream(U + t * vpr + v), acc[u]);
+      for (int q = 0; q < COMBINE_UNROLL; ++q) {
+        const int v = base + lane + 32 * q;
+        if (v < v_hi) uv[q] = ldg_stream(U + t * vpr + v);
       }
-      // shared experts (every token, weight 1), then the routed experts in choice order
+#pragma unroll
+      for (int q = 0; q < COMBINE_UNROLL; ++q) {
+        const int v = base + lane + 32 * q;
+        if (v < v_hi) Vec16<T>::unpack(uv[q], acc[q]);
+      }
+      // shared experts (every token, weight 1)
       for (int sh = 0; sh < n_shared; ++sh) {
 #pragma unroll
-        for (int u = 0; u < COMBINE_UNROLL; ++u) {
-          const int v = base + lane + 32 * u;
-          if (v < vpr) {
+        for (int q = 0; q < COMBINE_UNROLL; ++q) {
+          const int v = base + lane + 32 * q;
+          if (v < v_hi) {
             float y[N];
             Vec16<T>::unpack(ldg_stream(Y_shared + (static_cast<int64_t>(sh) * n_tok + t) * vpr + v), y);
 #pragma unroll
-            for (int i = 0; i < N; ++i) acc[u][i] += y[i];
+            for (int i = 0; i < N; ++i) acc[q][i] += y[i];
           }
         }
       }
-      for (int j = 0; j < k; ++j) {
-        const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
-        const float g = __shfl_sync(0xffffffffu, my_g, j);
-        if (r < 0) continue;
+      // routed experts in choice order, COMBINE_GROUP rows' loads in flight at once
+      for (int j0 = 0; j0 < k; j0 += COMBINE_GROUP) {
+        int32_t r[COMBINE_GROUP];
+        float g[COMBINE_GROUP];
+        uint4 yv[COMBINE_GROUP][COMBINE_UNROLL];
 #pragma unroll
-        for (int u = 0; u < COMBINE_UNROLL; ++u) {
-          const int v = base + lane + 32 * u;
-          if (v < vpr) {
-            float y[N];
-            Vec16<T>::unpack(ldg_stream(Y + static_cast<int64_t>(r) * vpr + v), y);
+        for (int jj = 0; jj < COMBINE_GROUP; ++jj) {
+          r[jj] = __shfl_sync(0xffffffffu, my_row, (j0 + jj) & 31);
+          g[jj] = __shfl_sync(0xffffffffu, my_g, (j0 + jj) & 31);
+          if (j0 + jj >= k) r[jj] = -1;
 #pragma unroll
-            for (int i = 0; i < N; ++i) acc[u][i] = fmaf(g, y[i], acc[u][i]);
+          for (int q = 0; q < COMBINE_UNROLL; ++q) {
+            const int v = base + lane + 32 * q;
+            if (r[jj] >= 0 && v < v_hi) yv[jj][q] = ldg_stream(Y + static_cast<int64_t>(r[jj]) * vpr + v);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < COMBINE_GROUP; ++jj) {
+          if (r[jj] < 0) continue;
+#pragma unroll
+          for (int q = 0; q < COMBINE_UNROLL; ++q) {
+            const int v = base + lane + 32 * q;
+            if (v < v_hi) {
+              float y[N];
+              Vec16<T>::unpack(yv[jj][q], y);
+#pragma unroll
+              for (int i = 0; i < N; ++i) acc[q][i] = fmaf(g[jj], y[i], acc[q][i]);
+            }
           }
         }
       }
 #pragma unroll
-      for (int u = 0; u < COMBINE_UNROLL; ++u) {
-        const int v = base + lane + 32 * u;
-        if (v < vpr) out[t * vpr + v] = Vec16<T>::pack(acc[u]);
+      for (int q = 0; q < COMBINE_UNROLL; ++q) {
+        const int v = base + lane + 32 * q;
+        if (v < v_hi) out[t * vpr + v] = Vec16<T>::pack(acc[q]);
       }
     }
   }
-}
 
-constexpr int STATS_THREADS = 1024;
-
-// Block b owns experts 32b .. 32b+31 (lane = expert): warp w adds rows w, w+32, ... of the
-// router's per-block score sums, then warp 0 adds the 32 warp sums in order.  The block
-// that finishes last (an atomic count, no waiting) forms aux from f and P in expert order,
-// so every result is the same from run to run.
-__global__ void __launch_bounds__(STATS_THREADS) load_stats(const float* __restrict__ ppart,
-                                                            const int32_t* __restrict__ ppart_rows,
-                                                            const int32_t* __restrict__ counts_routed, int64_t n_tok,
-                                                            int k, int E, float* __restrict__ f,
-                                                            float* __restrict__ P, float* __restrict__ aux,
-                                                            float* __restrict__ z_loss,
-                                                            int32_t* __restrict__ done_count) {
-  __shared__ float part_s[32][33];
+  // statistics, by the last block to finish
   __shared__ int last;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int e = blockIdx.x * 32 + lane;  // column E (the last block) holds the z-loss sums
-  const int n_parts = n_tok > 0 ? *ppart_rows : 0;
-  float s = 0.f;
-  if (e <= E)
-    for (int b = warp; b < n_parts; b += 32) s += ppart[static_cast<int64_t>(b) * (E + 1) + e];
-  part_s[warp][lane] = s;
+  __threadfence();
   __syncthreads();
-  if (warp == 0 && e <= E) {
-    float tot = 0.f;
-    for (int w = 0; w < 32; ++w) tot += part_s[w][lane];
-    const float mean = n_tok > 0 ? tot / static_cast<float>(n_tok) : 0.f;
+  if (threadIdx.x == 0) last = atomicAdd(done_count, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int n_parts = n_tok > 0 ? *ppart_rows : 0;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    float s = 0.f;
+    for (int b = 0; b < n_parts; ++b) s += __ldcg(ppart + static_cast<int64_t>(b) * (E + 1) + e);
+    const float mean = n_tok > 0 ? s / static_cast<float>(n_tok) : 0.f;
     if (e < E) {
       P[e] = mean;
       f[e] = n_tok > 0 ? static_cast<float>(counts_routed[e]) / static_cast<float>(n_tok * k) : 0.f;
@@ -123,18 +147,12 @@ __global__ void __launch_bounds__(STATS_THREADS) load_stats(const float* __restr
       *z_loss = mean;
     }
   }
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    last = atomicAdd(done_count, 1) == static_cast<int>(gridDim.x) - 1;
-    if (last) *done_count = 0;  // ready for the next call
-  }
-  __syncthreads();
-  if (last && threadIdx.x == 0) {
-    __threadfence();
     float a = 0.f;
-    for (int i = 0; i < E; ++i) a += __ldcg(f + i) * __ldcg(P + i);
+    for (int i = 0; i < E; ++i) a += f[i] * P[i];
     *aux = static_cast<float>(E) * a;
+    *done_count = 0;  // ready for the next call
   }
 }
 
@@ -165,26 +183,29 @@ cudaError_t launch_combine(const Plan& p, const void* U, const void* Y, const vo
                            const float* gate, const int32_t* counts_routed, void* out, float* f, float* P, float* aux,
                            float* z_loss, uint8_t* ws, cudaStream_t s) {
   int32_t* status = ws_status(p, ws);
-  if (p.T > 0) {
-    const int vpr = p.h * (p.bf16 ? 2 : 4) / 16;
-    const int64_t want = (p.T + 7) / 8;
-    const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(current_sm_count()) * 8));
-    const int n_sh = Y_shared ? p.n_shared : 0;
-    const uint4* ysh = static_cast<const uint4*>(Y_shared);
-    if (p.bf16)
-      combine_rows<bf16><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh,
-                                                slot_row, gate, static_cast<uint4*>(out), p.T, p.k, vpr, p.Tk, status);
-    else
-      combine_rows<float><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh,
-                                                 slot_row, gate, static_cast<uint4*>(out), p.T, p.k, vpr, p.Tk,
-                                                 status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   const float* ppart = reinterpret_cast<const float*>(ws + p.ws_ppart);
   int32_t* done = reinterpret_cast<int32_t*>(ws + p.ws_status + 128);
-  load_stats<<<(p.E + 1 + 31) / 32, STATS_THREADS, 0, s>>>(ppart, ws_ppart_rows(p, ws), counts_routed, p.T, p.k, p.E,
-                                                           f, P, aux, z_loss, done);
+  const int vpr = p.h * (p.bf16 ? 2 : 4) / 16;
+  // segments per row: enough warps to cover the GPU about 32 deep when T is small, each segment
+  // at least one vector per lane
+  const int sms = current_sm_count();
+  int segs = 1;
+  while (p.T > 0 && p.T * segs < static_cast<int64_t>(sms) * 32 && vpr / (segs * 2) >= 32) segs *= 2;
+  const int64_t units = p.T * segs;
+  const int64_t want = (units + COMBINE_THREADS / 32 - 1) / (COMBINE_THREADS / 32);
+  const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
+  const int n_sh = Y_shared ? p.n_shared : 0;
+  const uint4* ysh = static_cast<const uint4*>(Y_shared);
+  if (p.bf16)
+    combine_stats<bf16><<<blocks, COMBINE_THREADS, 0, s>>>(
+        static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh, slot_row, gate,
+        static_cast<uint4*>(out), p.T, p.k, vpr, segs, p.Tk, status, ppart, ws_ppart_rows(p, ws), counts_routed, p.E,
+        f, P, aux, z_loss, done);
+  else
+    combine_stats<float><<<blocks, COMBINE_THREADS, 0, s>>>(
+        static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh, slot_row, gate,
+        static_cast<uint4*>(out), p.T, p.k, vpr, segs, p.Tk, status, ppart, ws_ppart_rows(p, ws), counts_routed, p.E,
+        f, P, aux, z_loss, done);
   return cudaGetLastError();
 }
 

@@ -36,6 +36,7 @@
 namespace moe {
 
 constexpr int DISPATCH_THREADS = 256;
+constexpr int SCATTER_UNROLL = 4;
 constexpr int DISPATCH_WARPS = DISPATCH_THREADS / 32;
 constexpr int SCAN_THREADS = 1024;
 
@@ -214,8 +215,6 @@ __global__ void __launch_bounds__(DISPATCH_THREADS) dispatch_assign(
   }
 }
 
-constexpr int SCATTER_UNROLL = 4;
-
 // One warp per token (grid-stride): lane l copies 16-byte vectors l, l+32, ...
 __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict__ U, const int32_t* __restrict__ slot_row,
                                                         uint4* __restrict__ X, int64_t T, int k, int vpr) {
@@ -246,11 +245,235 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Choice-major dispatch in two launches.  Pairs are grouped into token chunks of TC tokens; with
+// every token's first choice before any second choice, the slot of pair (t, j) choosing expert e is
+//   sum_{j' < j} cnt[j'][e]  +  sum_{chunks c' < c(t)} h[c'][j][e]  +  #{t' < t in t's chunk : idx[t'][j] = e},
+// cnt[j][e] being the pairs of choice j that chose e over all tokens and h[c][j][e] those of chunk c.
+//   dispatch_hist   per chunk, h[c][j][e]; the block that finishes last (an atomic ticket, nobody
+//                   waits) turns h into exclusive prefixes over chunks plus the choice bases,
+//                   writes the routed and kept counts, the offsets and n_dropped, and resets the
+//                   ticket;
+//   dispatch_place  per chunk and choice: ranks among equal experts inside each warp (match_any)
+//                   on top of the chunk's base and the earlier warps' counts; writes slot_row and
+//                   row_token; then one warp per token reads the token's row of U once and writes
+//                   it to each of its kept rows (skipped when X is NULL).
+constexpr int PLACE_THREADS = 256;
+constexpr int PLACE_WARPS = PLACE_THREADS / 32;
+constexpr int HIST_THREADS = 1024;
+
+__global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __restrict__ idx, int64_t T, int k,
+                                                              int E, int tc, int n_chunks, int64_t C,
+                                                              int32_t* __restrict__ hist, int32_t* __restrict__ ticket,
+                                                              int32_t* __restrict__ counts_routed,
+                                                              int32_t* __restrict__ counts_kept,
+                                                              int32_t* __restrict__ offsets,
+                                                              int64_t* __restrict__ n_dropped, int32_t* status) {
+  extern __shared__ int32_t h_s[];  // [k][E], then (last block) kept[E]
+  const int kE = k * E;
+  for (int i = threadIdx.x; i < kE; i += blockDim.x) h_s[i] = 0;
+  __syncthreads();
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tc;
+  const int64_t t1 = min(t0 + tc, T);
+  bool bad = false;
+  for (int64_t i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+    const int j = static_cast<int>(i % k);
+    const int e = idx[i];
+    if (e >= 0 && e < E)
+      atomicAdd(&h_s[j * E + e], 1);  // integer counts: the order of the adds does not matter
+    else
+      bad = true;
+  }
+  if (bad) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  int32_t* mine = hist + static_cast<int64_t>(blockIdx.x) * kE;
+  for (int i = threadIdx.x; i < kE; i += blockDim.x) mine[i] = h_s[i];
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == n_chunks - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // column (j, e): exclusive prefix over the chunks, loads issued 16 at a time
+  for (int col = threadIdx.x; col < kE; col += blockDim.x) {
+    int32_t run = 0;
+    for (int c0 = 0; c0 < n_chunks; c0 += 16) {
+      int32_t v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] = c0 + q < n_chunks ? __ldcg(hist + static_cast<int64_t>(c0 + q) * kE + col) : 0;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (c0 + q < n_chunks) hist[static_cast<int64_t>(c0 + q) * kE + col] = run;
+        run += v[q];
+      }
+    }
+    h_s[col] = run;  // cnt[j][e]
+  }
+  __syncthreads();
+  int32_t* kept_s = h_s + kE;
+  int32_t* cbase = hist + static_cast<int64_t>(n_chunks) * kE;  // [k][E] choice bases
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = 0;
+    for (int j = 0; j < k; ++j) {
+      cbase[j * E + e] = run;
+      run += h_s[j * E + e];
+    }
+    counts_routed[e] = run;
+    const int32_t kept = static_cast<int32_t>(min(static_cast<int64_t>(run), C));
+    counts_kept[e] = kept;
+    kept_s[e] = kept;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // offsets = exclusive scan of the kept counts (warp 0)
+    const int tid = threadIdx.x;
+    const int per = (E + 31) / 32;
+    const int lo = min(E, tid * per), hi = min(E, lo + per);
+    int32_t s = 0;
+    for (int i = lo; i < hi; ++i) s += kept_s[i];
+    int32_t incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += y;
+    }
+    int32_t run = incl - s;
+    for (int i = lo; i < hi; ++i) {
+      offsets[i] = run;
+      run += kept_s[i];
+    }
+    const int32_t A = __shfl_sync(0xffffffffu, incl, 31);
+    if (tid == 0) {
+      offsets[E] = A;
+      *n_dropped = T * k - A;
+      *ticket = 0;  // ready for the next call
+    }
+  }
+}
+
+__global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
+    const int32_t* __restrict__ idx, int64_t T, int k, int E, int tc, int n_chunks, int64_t C,
+    const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+    int32_t* __restrict__ row_token, const uint4* __restrict__ U, uint4* __restrict__ X, int vpr) {
+  extern __shared__ int32_t sm[];
+  int32_t* wc = sm;                          // [PLACE_WARPS][E]
+  int32_t* rows_s = sm + PLACE_WARPS * E;    // [tc][k]
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int kE = k * E;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tc;
+  const int n = static_cast<int>(min(static_cast<int64_t>(tc), T - t0));
+  const int seg = (tc + PLACE_WARPS - 1) / PLACE_WARPS;  // tokens per warp
+  const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
+  int32_t* my = wc + warp * E;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const int32_t* base = hist + static_cast<int64_t>(blockIdx.x) * kE;
+  const int32_t* cbase = hist + static_cast<int64_t>(n_chunks) * kE;
+  for (int j = 0; j < k; ++j) {
+    for (int i = threadIdx.x; i < PLACE_WARPS * E; i += blockDim.x) wc[i] = 0;
+    __syncthreads();
+    // pass 1: per-warp counts of choice j (w0, w1 are warp-uniform)
+    for (int q = w0; q < w1; q += 32) {
+      const int r = q + lane;
+      int e = -1;
+      if (r < w1) {
+        e = idx[(t0 + r) * k + j];
+        if (e < 0 || e >= E) e = -1;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    // warp bases: choice base + chunk prefix + earlier warps, warps in order
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int32_t run = cbase[j * E + e] + base[j * E + e];
+      for (int w = 0; w < PLACE_WARPS; ++w) {
+        const int32_t v = wc[w * E + e];
+        wc[w * E + e] = run;
+        run += v;
+      }
+    }
+    __syncthreads();
+    // pass 2: slot = warp base + rank among the equal experts of earlier lanes
+    for (int q = w0; q < w1; q += 32) {
+      const int r = q + lane;
+      int e = -1;
+      if (r < w1) {
+        e = idx[(t0 + r) * k + j];
+        if (e < 0 || e >= E) e = -1;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, e);
+      const int32_t slot = e >= 0 ? my[e] + __popc(peers & lt_mask) : -1;
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+      __syncwarp();
+      if (r < w1) {
+        const int64_t t = t0 + r;
+        int32_t row = -1;
+        if (e >= 0 && slot < C) {
+          row = offsets[e] + slot;
+          row_token[row] = static_cast<int32_t>(t);
+        }
+        slot_row[t * k + j] = row;
+        rows_s[r * k + j] = row;
+      }
+    }
+    __syncthreads();
+  }
+  if (!X) return;
+  // the row copy: one warp per token, each U row read once
+  for (int r = warp; r < n; r += PLACE_WARPS) {
+    const int32_t my_row = lane < k ? rows_s[r * k + lane] : -1;
+    const uint4* src = U + (t0 + r) * vpr;
+    for (int b0 = 0; b0 < vpr; b0 += 32 * SCATTER_UNROLL) {
+      uint4 val[SCATTER_UNROLL];
+#pragma unroll
+      for (int u = 0; u < SCATTER_UNROLL; ++u) {
+        const int v = b0 + lane + 32 * u;
+        if (v < vpr) val[u] = ldg_stream(src + v);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int32_t row = __shfl_sync(0xffffffffu, my_row, j);
+        if (row < 0) continue;
+        uint4* dst = X + static_cast<int64_t>(row) * vpr;
+#pragma unroll
+        for (int u = 0; u < SCATTER_UNROLL; ++u) {
+          const int v = b0 + lane + 32 * u;
+          if (v < vpr) dst[v] = val[u];
+        }
+      }
+    }
+  }
+}
+
 cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, int32_t* counts_routed,
                             int32_t* counts_kept, int32_t* offsets, int32_t* slot_row, int32_t* row_token, void* X,
                             int64_t* n_dropped, uint8_t* ws, cudaStream_t s) {
   int32_t* hist = reinterpret_cast<int32_t*>(ws + p.ws_hist);
   int32_t* status = ws_status(p, ws);
+  if (p.priority == MOE_PRIORITY_CHOICE_MAJOR && p.dp_chunks > 0) {
+    int32_t* ticket = reinterpret_cast<int32_t*>(ws + p.ws_status + 192);
+    const size_t hsm = sizeof(int32_t) * (static_cast<size_t>(p.k) * p.E + p.E);
+    if (hsm > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(dispatch_hist, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(hsm));
+      if (e != cudaSuccess) return e;
+    }
+    dispatch_hist<<<p.dp_chunks, HIST_THREADS, hsm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, p.dp_chunks, p.C, hist, ticket,
+                                                          counts_routed, counts_kept, offsets, n_dropped, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t psm = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + static_cast<size_t>(p.dp_tc) * p.k);
+    if (psm > 48 * 1024) {
+      const cudaError_t e = cudaFuncSetAttribute(dispatch_place, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(psm));
+      if (e != cudaSuccess) return e;
+    }
+    dispatch_place<<<p.dp_chunks, PLACE_THREADS, psm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, p.dp_chunks, p.C, hist,
+                                                            offsets, slot_row, row_token, static_cast<const uint4*>(U),
+                                                            static_cast<uint4*>(X), p.h * (p.bf16 ? 2 : 4) / 16);
+    return cudaGetLastError();
+  }
   const size_t hist_smem = sizeof(int32_t) * p.E;
   if (p.n_chunks > 0) {
     dispatch_count<<<p.n_chunks, DISPATCH_THREADS, hist_smem, s>>>(idx, p.T, p.k, p.E, p.priority, p.chunk, hist,

@@ -62,8 +62,10 @@ struct Plan {
   int sel_blocks = 0;      // ceil(T / sel_tokens): number of P partial rows
 
   // dispatch
-  int chunk = 0;           // priority positions per histogram chunk
+  int chunk = 0;           // priority positions per histogram chunk (token-major priority)
   int n_chunks = 0;
+  int dp_tc = 0;           // tokens per chunk of the two-launch choice-major dispatch
+  int dp_chunks = 0;
 
   // workspace byte offsets
   size_t ws_status = 0, ws_part = 0, ws_npart = 0, ws_ppart = 0, ws_hist = 0, ws_wt = 0, ws_total = 0;

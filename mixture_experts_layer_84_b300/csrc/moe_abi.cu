@@ -197,6 +197,13 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     q.chunk = static_cast<int>(std::max<int64_t>(256, std::min<int64_t>(kDispatchChunk, c)));
   }
   q.n_chunks = static_cast<int>((Tk + q.chunk - 1) / q.chunk);
+  // choice-major dispatch: token chunks of 16 .. 256 tokens, about two per SM
+  {
+    int tc = 16;
+    while (tc < 256 && static_cast<int64_t>(tc) * 2 * 148 < q.T) tc *= 2;
+    q.dp_tc = tc;
+    q.dp_chunks = static_cast<int>((q.T + tc - 1) / tc);
+  }
 
   size_t off = 0;
   q.ws_status = off;
@@ -210,7 +217,8 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   const int64_t ppart_rows = std::max<int64_t>(q.sel_blocks, static_cast<int64_t>(q.rf_tiles) * q.rf_cs);
   off += align256(sizeof(float) * static_cast<size_t>(ppart_rows) * (q.E + 1));
   q.ws_hist = off;
-  off += align256(sizeof(int32_t) * static_cast<size_t>(q.n_chunks) * q.E);
+  off += align256(sizeof(int32_t) * std::max(static_cast<size_t>(q.n_chunks) * q.E,
+                                             (static_cast<size_t>(q.dp_chunks) + 1) * q.k * q.E));
   q.ws_wt = off;
   if (q.route_tc_n > 0) off += align256(sizeof(uint16_t) * static_cast<size_t>(q.route_tc_n) * q.h);
   q.rb_np = ((q.noisy ? 2 * q.E : q.E) + 7) / 8 * 8;

@@ -150,3 +150,16 @@ def test_misaligned_pointer_rejected():
     st = L.lib.moe_route(ctypes.byref(cfg), fake, ok, None, None, None, None, None, None, ok, ok, ok, None)
     assert st == L.MOE_ERR_INVALID_ARG
     assert "aligned" in L.lib.moe_last_error().decode()
+
+
+def test_binding_argument_counts_match_the_header():
+    """Every ctypes signature in the binding takes as many arguments as include/*.h declares."""
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", f)).read(), flags=re.S)
+        for m in re.finditer(r"\b(moe_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", src):
+            name, args = m.group(1), m.group(2).strip()
+            n = 0 if args in ("void", "") else len(args.split(","))
+            argtypes = getattr(L.lib, name).argtypes
+            assert argtypes is None and n == 0 or argtypes is not None and len(argtypes) == n, name
