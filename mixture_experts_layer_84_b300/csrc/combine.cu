@@ -24,6 +24,7 @@ namespace moe {
 constexpr int COMBINE_THREADS = 256;
 constexpr int COMBINE_UNROLL = 2;   // 16-byte vectors per lane per row stream in flight
 constexpr int COMBINE_GROUP = 4;    // routed rows whose loads are issued together
+constexpr int STAT_GROUPS = 32;     // first-level slices of the statistics reduction
 
 // Row combine and statistics in one launch.
 //   Rows: a work unit is one segment of one token's row (segs segments per row, chosen so that
@@ -31,8 +32,9 @@ constexpr int COMBINE_GROUP = 4;    // routed rows whose loads are issued togeth
 //   loads of its 16-byte vectors of u_t, of the shared experts' rows and of up to COMBINE_GROUP
 //   kept expert rows, then accumulates in float32 in a fixed order -- u_t, the shared rows in
 //   order, then g_j y_j for j ascending -- and rounds once.
-//   Statistics: the block that finishes last (an atomic count; nobody waits) adds each expert's
-//   column of the router's per-block score sums in block order (P_i, and the z-loss in column E),
+//   Statistics in two levels: the first `groups` blocks each add a slice of the rows of the router's
+//   per-block score sums, every column, in row order; the block that finishes last (an atomic
+//   count; nobody waits) adds those partial rows in group order (P_i, and the z-loss in column E),
 //   forms f_i from the routed counts and aux = E sum_i f_i P_i in expert order, and resets the
 //   count for the next call.  Every result is the same from run to run.
 template <typename T>
@@ -41,8 +43,28 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2) combine_stats(
     const int32_t* __restrict__ slot_row, const float* __restrict__ gate, uint4* __restrict__ out, int64_t n_tok,
     int k, int vpr, int segs, int64_t rows_cap, int32_t* status, const float* __restrict__ ppart,
     const int32_t* __restrict__ ppart_rows, const int32_t* __restrict__ counts_routed, int E, float* __restrict__ f,
-    float* __restrict__ P, float* __restrict__ aux, float* __restrict__ z_loss, int32_t* __restrict__ done_count) {
+    float* __restrict__ P, float* __restrict__ aux, float* __restrict__ z_loss, int32_t* __restrict__ done_count,
+    float* __restrict__ part2, int groups) {
   constexpr int N = Vec16<T>::N;
+  // statistics, first level: block g < groups adds rows [g R, (g+1) R) of the router's per-block
+  // sums, every column, in row order (loads issued eight at a time)
+  if (static_cast<int>(blockIdx.x) < groups && n_tok > 0) {
+    const int n_parts = *ppart_rows;
+    const int R = (n_parts + groups - 1) / groups;
+    const int b0 = min(n_parts, static_cast<int>(blockIdx.x) * R), b1 = min(n_parts, b0 + R);
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+      float s = 0.f;
+      for (int b = b0; b < b1; b += 8) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = b + q < b1 ? ppart[static_cast<int64_t>(b + q) * (E + 1) + e] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (b + q < b1) s += v[q];
+      }
+      part2[static_cast<int64_t>(blockIdx.x) * (E + 1) + e] = s;
+    }
+  }
   const int lane = threadIdx.x % 32;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
   const int vps = (vpr + segs - 1) / segs;  // vectors per segment
@@ -135,10 +157,18 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 2) combine_stats(
   __syncthreads();
   if (!last) return;
   __threadfence();
-  const int n_parts = n_tok > 0 ? *ppart_rows : 0;
+  // second level: the groups' partial sums in group order
+  const int G = n_tok > 0 ? groups : 0;
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     float s = 0.f;
-    for (int b = 0; b < n_parts; ++b) s += __ldcg(ppart + static_cast<int64_t>(b) * (E + 1) + e);
+    for (int b = 0; b < G; b += 8) {
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = b + q < G ? __ldcg(part2 + static_cast<int64_t>(b + q) * (E + 1) + e) : 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (b + q < G) s += v[q];
+    }
     const float mean = n_tok > 0 ? s / static_cast<float>(n_tok) : 0.f;
     if (e < E) {
       P[e] = mean;
@@ -196,16 +226,18 @@ cudaError_t launch_combine(const Plan& p, const void* U, const void* Y, const vo
   const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
   const int n_sh = Y_shared ? p.n_shared : 0;
   const uint4* ysh = static_cast<const uint4*>(Y_shared);
+  float* part2 = reinterpret_cast<float*>(ws + p.ws_stats2);
+  const int groups = std::min(STAT_GROUPS, blocks);
   if (p.bf16)
     combine_stats<bf16><<<blocks, COMBINE_THREADS, 0, s>>>(
         static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh, slot_row, gate,
         static_cast<uint4*>(out), p.T, p.k, vpr, segs, p.Tk, status, ppart, ws_ppart_rows(p, ws), counts_routed, p.E,
-        f, P, aux, z_loss, done);
+        f, P, aux, z_loss, done, part2, groups);
   else
     combine_stats<float><<<blocks, COMBINE_THREADS, 0, s>>>(
         static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh, slot_row, gate,
         static_cast<uint4*>(out), p.T, p.k, vpr, segs, p.Tk, status, ppart, ws_ppart_rows(p, ws), counts_routed, p.E,
-        f, P, aux, z_loss, done);
+        f, P, aux, z_loss, done, part2, groups);
   return cudaGetLastError();
 }
 

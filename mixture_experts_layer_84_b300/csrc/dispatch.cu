@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -246,30 +247,29 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 }
 
 // ---------------------------------------------------------------------------------------------
-// Choice-major dispatch in two launches.  Pairs are grouped into token chunks of TC tokens; with
+// Choice-major dispatch in three launches.  Pairs are grouped into token chunks of TC tokens; with
 // every token's first choice before any second choice, the slot of pair (t, j) choosing expert e is
 //   sum_{j' < j} cnt[j'][e]  +  sum_{chunks c' < c(t)} h[c'][j][e]  +  #{t' < t in t's chunk : idx[t'][j] = e},
 // cnt[j][e] being the pairs of choice j that chose e over all tokens and h[c][j][e] those of chunk c.
-//   dispatch_hist   per chunk, h[c][j][e]; the block that finishes last (an atomic ticket, nobody
-//                   waits) turns h into exclusive prefixes over chunks plus the choice bases,
-//                   writes the routed and kept counts, the offsets and n_dropped, and resets the
-//                   ticket;
+//   dispatch_hist    per chunk, h[c][j][e];
+//   dispatch_colscan one warp per (j, e) column: exclusive prefixes over the chunks and the column
+//                    total; the block that finishes last (an atomic ticket, nobody waits) forms the
+//                    choice bases, the routed and kept counts, the offsets and n_dropped;
 //   dispatch_place  per chunk and choice: ranks among equal experts inside each warp (match_any)
 //                   on top of the chunk's base and the earlier warps' counts; writes slot_row and
-//                   row_token; then one warp per token reads the token's row of U once and writes
-//                   it to each of its kept rows (skipped when X is NULL).
+//                   row_token; then one thread streams the chunk's U rows through shared memory
+//                   with bulk copies, each row read once and written to each of its kept rows
+//                   (skipped when X is NULL).
 constexpr int PLACE_THREADS = 256;
+constexpr uint32_t COPY_RING_BYTES = 96 * 1024;      // row buffers of one dispatch_place block
+constexpr uint64_t COPY_WAIT_LIMIT_NS = 2000000000ull;
 constexpr int PLACE_WARPS = PLACE_THREADS / 32;
 constexpr int HIST_THREADS = 1024;
 
 __global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __restrict__ idx, int64_t T, int k,
-                                                              int E, int tc, int n_chunks, int64_t C,
-                                                              int32_t* __restrict__ hist, int32_t* __restrict__ ticket,
-                                                              int32_t* __restrict__ counts_routed,
-                                                              int32_t* __restrict__ counts_kept,
-                                                              int32_t* __restrict__ offsets,
-                                                              int64_t* __restrict__ n_dropped, int32_t* status) {
-  extern __shared__ int32_t h_s[];  // [k][E], then (last block) kept[E]
+                                                              int E, int tc, int32_t* __restrict__ hist,
+                                                              int32_t* status) {
+  extern __shared__ int32_t h_s[];  // [k][E]
   const int kE = k * E;
   for (int i = threadIdx.x; i < kE; i += blockDim.x) h_s[i] = 0;
   __syncthreads();
@@ -288,36 +288,57 @@ __global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __r
   __syncthreads();
   int32_t* mine = hist + static_cast<int64_t>(blockIdx.x) * kE;
   for (int i = threadIdx.x; i < kE; i += blockDim.x) mine[i] = h_s[i];
+}
+
+// One warp per (choice j, expert e) column of the chunk histograms: lane l adds the chunks
+// [l m, (l+1) m), the warp scans the lane sums, and every chunk's entry becomes the exclusive prefix
+// over the earlier chunks; the column total goes to cnt[j][e].  The block that finishes last (an
+// atomic ticket, nobody waits) forms the choice bases (the pairs of earlier choices per expert),
+// the routed and kept counts, the offsets and n_dropped, and resets the ticket.
+__global__ void __launch_bounds__(256) dispatch_colscan(int32_t* __restrict__ hist, int n_chunks, int k, int E,
+                                                        int64_t C, int64_t Tk, int32_t* __restrict__ ticket,
+                                                        int32_t* __restrict__ counts_routed,
+                                                        int32_t* __restrict__ counts_kept,
+                                                        int32_t* __restrict__ offsets,
+                                                        int64_t* __restrict__ n_dropped) {
+  const int kE = k * E;
+  const int lane = threadIdx.x % 32;
+  const int col = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int32_t* cnt = hist + static_cast<int64_t>(n_chunks + 1) * kE;  // [k][E] column totals
+  if (col < kE) {
+    const int m = (n_chunks + 31) / 32;
+    const int c0 = min(n_chunks, lane * m), c1 = min(n_chunks, c0 + m);
+    int32_t s = 0;
+    for (int c = c0; c < c1; ++c) s += hist[static_cast<int64_t>(c) * kE + col];
+    int32_t incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int32_t run = incl - s;
+    for (int c = c0; c < c1; ++c) {
+      const int64_t o = static_cast<int64_t>(c) * kE + col;
+      const int32_t v = hist[o];
+      hist[o] = run;
+      run += v;
+    }
+    if (lane == 31) cnt[col] = incl;
+  }
   __shared__ int last;
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == n_chunks - 1;
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
   __syncthreads();
   if (!last) return;
   __threadfence();
-  // column (j, e): exclusive prefix over the chunks, loads issued 16 at a time
-  for (int col = threadIdx.x; col < kE; col += blockDim.x) {
-    int32_t run = 0;
-    for (int c0 = 0; c0 < n_chunks; c0 += 16) {
-      int32_t v[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = c0 + q < n_chunks ? __ldcg(hist + static_cast<int64_t>(c0 + q) * kE + col) : 0;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if (c0 + q < n_chunks) hist[static_cast<int64_t>(c0 + q) * kE + col] = run;
-        run += v[q];
-      }
-    }
-    h_s[col] = run;  // cnt[j][e]
-  }
-  __syncthreads();
-  int32_t* kept_s = h_s + kE;
+  __shared__ int32_t kept_s[1024];
   int32_t* cbase = hist + static_cast<int64_t>(n_chunks) * kE;  // [k][E] choice bases
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int32_t run = 0;
     for (int j = 0; j < k; ++j) {
       cbase[j * E + e] = run;
-      run += h_s[j * E + e];
+      run += __ldcg(cnt + j * E + e);
     }
     counts_routed[e] = run;
     const int32_t kept = static_cast<int32_t>(min(static_cast<int64_t>(run), C));
@@ -326,16 +347,15 @@ __global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __r
   }
   __syncthreads();
   if (threadIdx.x < 32) {  // offsets = exclusive scan of the kept counts (warp 0)
-    const int tid = threadIdx.x;
     const int per = (E + 31) / 32;
-    const int lo = min(E, tid * per), hi = min(E, lo + per);
+    const int lo = min(E, lane * per), hi = min(E, lo + per);
     int32_t s = 0;
     for (int i = lo; i < hi; ++i) s += kept_s[i];
     int32_t incl = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (tid >= o) incl += y;
+      if (lane >= o) incl += y;
     }
     int32_t run = incl - s;
     for (int i = lo; i < hi; ++i) {
@@ -343,9 +363,9 @@ __global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __r
       run += kept_s[i];
     }
     const int32_t A = __shfl_sync(0xffffffffu, incl, 31);
-    if (tid == 0) {
+    if (lane == 0) {
       offsets[E] = A;
-      *n_dropped = T * k - A;
+      *n_dropped = Tk - A;
       *ticket = 0;  // ready for the next call
     }
   }
@@ -354,7 +374,8 @@ __global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __r
 __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     const int32_t* __restrict__ idx, int64_t T, int k, int E, int tc, int n_chunks, int64_t C,
     const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
-    int32_t* __restrict__ row_token, const uint4* __restrict__ U, uint4* __restrict__ X, int vpr) {
+    int32_t* __restrict__ row_token, const void* __restrict__ U, void* __restrict__ X, uint32_t row_bytes, int nb,
+    int32_t* status) {
   extern __shared__ int32_t sm[];
   int32_t* wc = sm;                          // [PLACE_WARPS][E]
   int32_t* rows_s = sm + PLACE_WARPS * E;    // [tc][k]
@@ -420,30 +441,62 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     }
     __syncthreads();
   }
-  if (!X) return;
-  // the row copy: one warp per token, each U row read once
-  for (int r = warp; r < n; r += PLACE_WARPS) {
-    const int32_t my_row = lane < k ? rows_s[r * k + lane] : -1;
-    const uint4* src = U + (t0 + r) * vpr;
-    for (int b0 = 0; b0 < vpr; b0 += 32 * SCATTER_UNROLL) {
-      uint4 val[SCATTER_UNROLL];
-#pragma unroll
-      for (int u = 0; u < SCATTER_UNROLL; ++u) {
-        const int v = b0 + lane + 32 * u;
-        if (v < vpr) val[u] = ldg_stream(src + v);
+  if (!X || n == 0) return;
+  // the row copy: one thread streams the chunk's U rows through a ring of NB shared-memory row
+  // buffers (bulk global -> shared loads, NB - 1 in flight) and writes each row to its kept rows
+  // with bulk shared -> global stores; a buffer is reloaded once the stores that read it are done
+  if (threadIdx.x != 0) return;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(rows_s + tc * k) + 127) & ~static_cast<uintptr_t>(127));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(nb) * row_bytes);
+  for (int i = 0; i < nb; ++i) ptx::mbar_init(&bar[i], 1);
+  ptx::fence_mbarrier_init();
+  ptx::fence_proxy_async_smem();
+  const uint8_t* usrc = reinterpret_cast<const uint8_t*>(U) + t0 * row_bytes;
+  int issued = 0;  // loads issued: tokens 0 .. issued - 1
+  auto load = [&](int r) {
+    issued = r + 1;
+    uint64_t* bb = &bar[r % nb];
+    ptx::mbar_arrive_expect_tx(bb, row_bytes);
+    ptx::bulk_load(ring + static_cast<size_t>(r % nb) * row_bytes, usrc + static_cast<int64_t>(r) * row_bytes,
+                   row_bytes, bb);
+  };
+  for (int r = 0; r < min(nb - 1, n); ++r) load(r);
+  bool ok = true;
+  int r = 0;
+  for (; r < n; ++r) {
+    // bounded wait for the load of token r (its buffer's (r / nb)-th use)
+    const uint64_t tw = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(&bar[r % nb], static_cast<uint32_t>((r / nb) & 1))) {
+      if (ptx::globaltimer_ns() - tw > COPY_WAIT_LIMIT_NS) {
+        ok = false;
+        break;
       }
-      for (int j = 0; j < k; ++j) {
-        const int32_t row = __shfl_sync(0xffffffffu, my_row, j);
-        if (row < 0) continue;
-        uint4* dst = X + static_cast<int64_t>(row) * vpr;
-#pragma unroll
-        for (int u = 0; u < SCATTER_UNROLL; ++u) {
-          const int v = b0 + lane + 32 * u;
-          if (v < vpr) dst[v] = val[u];
-        }
+    }
+    if (!ok) break;
+    const uint8_t* src = ring + static_cast<size_t>(r % nb) * row_bytes;
+    for (int j = 0; j < k; ++j) {
+      const int32_t row = rows_s[r * k + j];
+      if (row >= 0) ptx::bulk_store(reinterpret_cast<uint8_t*>(X) + static_cast<int64_t>(row) * row_bytes, src, row_bytes);
+    }
+    ptx::bulk_commit();
+    const int next = r + nb - 1;  // goes into the buffer of token r - 1
+    if (next < n) {
+      if (r >= 1) ptx::bulk_wait_read<1>();  // the stores of token r - 1 have read their buffer
+      load(next);
+    }
+  }
+  if (!ok) {
+    set_status(status, MOE_DEV_TIMEOUT);
+    // loads still in flight land in this block's shared memory: wait for them (bounded) first
+    for (int q = r + 1; q < issued; ++q) {
+      const uint64_t tw = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(&bar[q % nb], static_cast<uint32_t>((q / nb) & 1)) &&
+             ptx::globaltimer_ns() - tw < COPY_WAIT_LIMIT_NS) {
       }
     }
   }
+  ptx::bulk_wait_all();
 }
 
 cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, int32_t* counts_routed,
@@ -453,25 +506,32 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
   int32_t* status = ws_status(p, ws);
   if (p.priority == MOE_PRIORITY_CHOICE_MAJOR && p.dp_chunks > 0) {
     int32_t* ticket = reinterpret_cast<int32_t*>(ws + p.ws_status + 192);
-    const size_t hsm = sizeof(int32_t) * (static_cast<size_t>(p.k) * p.E + p.E);
+    const size_t hsm = sizeof(int32_t) * static_cast<size_t>(p.k) * p.E;
     if (hsm > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(dispatch_hist, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(hsm));
       if (e != cudaSuccess) return e;
     }
-    dispatch_hist<<<p.dp_chunks, HIST_THREADS, hsm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, p.dp_chunks, p.C, hist, ticket,
-                                                          counts_routed, counts_kept, offsets, n_dropped, status);
+    dispatch_hist<<<p.dp_chunks, HIST_THREADS, hsm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, hist, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t psm = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + static_cast<size_t>(p.dp_tc) * p.k);
+    const int cols = p.k * p.E;
+    dispatch_colscan<<<(cols + 7) / 8, 256, 0, s>>>(hist, p.dp_chunks, p.k, p.E, p.C, p.Tk, ticket, counts_routed,
+                                                     counts_kept, offsets, n_dropped);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.h) * (p.bf16 ? 2 : 4);
+    const int nb = X ? static_cast<int>(std::max<uint32_t>(2, std::min<uint32_t>(16, COPY_RING_BYTES / row_bytes))) : 0;
+    const size_t psm = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + static_cast<size_t>(p.dp_tc) * p.k) +
+                       128 + static_cast<size_t>(nb) * row_bytes + 8 * static_cast<size_t>(nb);
     if (psm > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(dispatch_place, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(psm));
       if (e != cudaSuccess) return e;
     }
     dispatch_place<<<p.dp_chunks, PLACE_THREADS, psm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, p.dp_chunks, p.C, hist,
-                                                            offsets, slot_row, row_token, static_cast<const uint4*>(U),
-                                                            static_cast<uint4*>(X), p.h * (p.bf16 ? 2 : 4) / 16);
+                                                            offsets, slot_row, row_token, U, X, row_bytes, nb,
+                                                            status);
     return cudaGetLastError();
   }
   const size_t hist_smem = sizeof(int32_t) * p.E;

@@ -69,6 +69,7 @@ struct Plan {
 
   // workspace byte offsets
   size_t ws_status = 0, ws_part = 0, ws_npart = 0, ws_ppart = 0, ws_hist = 0, ws_wt = 0, ws_total = 0;
+  size_t ws_stats2 = 0;    // first-level partial sums of the statistics [32][E + 1] f32
   // router backward: [dH | dN] bf16 [T, rb_np], [W_r | W_noise] bf16 [h, rb_np], dW float32 [h, rb_np]
   int rb_np = 0;
   size_t ws_rb_dh = 0, ws_rb_w = 0, ws_rb_dw = 0;

@@ -216,9 +216,11 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   q.ws_ppart = off;
   const int64_t ppart_rows = std::max<int64_t>(q.sel_blocks, static_cast<int64_t>(q.rf_tiles) * q.rf_cs);
   off += align256(sizeof(float) * static_cast<size_t>(ppart_rows) * (q.E + 1));
+  q.ws_stats2 = off;
+  off += align256(sizeof(float) * 32 * static_cast<size_t>(q.E + 1));
   q.ws_hist = off;
   off += align256(sizeof(int32_t) * std::max(static_cast<size_t>(q.n_chunks) * q.E,
-                                             (static_cast<size_t>(q.dp_chunks) + 1) * q.k * q.E));
+                                             (static_cast<size_t>(q.dp_chunks) + 2) * q.k * q.E));
   q.ws_wt = off;
   if (q.route_tc_n > 0) off += align256(sizeof(uint16_t) * static_cast<size_t>(q.route_tc_n) * q.h);
   q.rb_np = ((q.noisy ? 2 * q.E : q.E) + 7) / 8 * 8;

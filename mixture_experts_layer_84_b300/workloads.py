@@ -102,7 +102,9 @@ MIXTRAL_NARROW = MIXTRAL.replace(name="mixtral_narrow_bf16", d_e=3584)
 # row tiles, 3.5 GB on the device): small cases of those kernels for hardware-counter captures.
 SWITCH_NARROW = SWITCH.replace(name="switch_narrow_bf16", d_e=1024)
 STRESS_NARROW = STRESS.replace(name="stress_narrow_bf16", T=12288)
-NARROW = [MIXTRAL_NARROW, SWITCH_NARROW, STRESS_NARROW]
+# The 256-expert shape with d_e = 64: the same router, dispatch and combine with 2 GB on the device.
+DSV3_NARROW = DSV3.replace(name="dsv3_narrow_bf16", d_e=64)
+NARROW = [MIXTRAL_NARROW, SWITCH_NARROW, STRESS_NARROW, DSV3_NARROW]
 
 BY_NAME = {w.name: w for w in FULL + SMALL + EXTENDED + NARROW + [DSV3_SHARED_SMALL]}
 
