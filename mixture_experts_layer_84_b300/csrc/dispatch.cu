@@ -308,8 +308,17 @@ __global__ void __launch_bounds__(256) dispatch_colscan(int32_t* __restrict__ hi
   if (col < kE) {
     const int m = (n_chunks + 31) / 32;
     const int c0 = min(n_chunks, lane * m), c1 = min(n_chunks, c0 + m);
+    // up to 8 chunks a lane are loaded at once and kept in registers (one round trip)
+    int32_t vals[8];
     int32_t s = 0;
-    for (int c = c0; c < c1; ++c) s += hist[static_cast<int64_t>(c) * kE + col];
+    if (m <= 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) vals[q] = c0 + q < c1 ? hist[static_cast<int64_t>(c0 + q) * kE + col] : 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) s += vals[q];
+    } else {
+      for (int c = c0; c < c1; ++c) s += hist[static_cast<int64_t>(c) * kE + col];
+    }
     int32_t incl = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -317,11 +326,19 @@ __global__ void __launch_bounds__(256) dispatch_colscan(int32_t* __restrict__ hi
       if (lane >= o) incl += y;
     }
     int32_t run = incl - s;
-    for (int c = c0; c < c1; ++c) {
-      const int64_t o = static_cast<int64_t>(c) * kE + col;
-      const int32_t v = hist[o];
-      hist[o] = run;
-      run += v;
+    if (m <= 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (c0 + q < c1) hist[static_cast<int64_t>(c0 + q) * kE + col] = run;
+        run += vals[q];
+      }
+    } else {
+      for (int c = c0; c < c1; ++c) {
+        const int64_t o = static_cast<int64_t>(c) * kE + col;
+        const int32_t v = hist[o];
+        hist[o] = run;
+        run += v;
+      }
     }
     if (lane == 31) cnt[col] = incl;
   }
@@ -335,10 +352,14 @@ __global__ void __launch_bounds__(256) dispatch_colscan(int32_t* __restrict__ hi
   __shared__ int32_t kept_s[1024];
   int32_t* cbase = hist + static_cast<int64_t>(n_chunks) * kE;  // [k][E] choice bases
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t c[16];  // k <= 16: every choice's total loaded at once
+#pragma unroll
+    for (int j = 0; j < 16; ++j) c[j] = j < k ? __ldcg(cnt + j * E + e) : 0;
     int32_t run = 0;
-    for (int j = 0; j < k; ++j) {
-      cbase[j * E + e] = run;
-      run += __ldcg(cnt + j * E + e);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j < k) cbase[j * E + e] = run;
+      run += c[j];
     }
     counts_routed[e] = run;
     const int32_t kept = static_cast<int32_t>(min(static_cast<int64_t>(run), C));
@@ -375,10 +396,12 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     const int32_t* __restrict__ idx, int64_t T, int k, int E, int tc, int n_chunks, int64_t C,
     const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
     int32_t* __restrict__ row_token, const void* __restrict__ U, void* __restrict__ X, uint32_t row_bytes, int nb,
-    int32_t* status) {
+    int32_t* status, int stage_bases) {
   extern __shared__ int32_t sm[];
   int32_t* wc = sm;                          // [PLACE_WARPS][E]
   int32_t* rows_s = sm + PLACE_WARPS * E;    // [tc][k]
+  int32_t* idx_s = rows_s + tc * k;          // [tc][k]: the chunk's expert ids
+  int32_t* base_s = idx_s + tc * k;          // [k][E]: chunk prefix + choice base (when staged)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int kE = k * E;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tc;
@@ -389,6 +412,11 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int32_t* base = hist + static_cast<int64_t>(blockIdx.x) * kE;
   const int32_t* cbase = hist + static_cast<int64_t>(n_chunks) * kE;
+  // everything the ranking reads, staged with loads that are all in flight together
+  for (int i = threadIdx.x; i < n * k; i += blockDim.x) idx_s[i] = idx[t0 * k + i];
+  if (stage_bases)
+    for (int i = threadIdx.x; i < kE; i += blockDim.x) base_s[i] = base[i] + cbase[i];
+  __syncthreads();
   for (int j = 0; j < k; ++j) {
     for (int i = threadIdx.x; i < PLACE_WARPS * E; i += blockDim.x) wc[i] = 0;
     __syncthreads();
@@ -397,7 +425,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
       const int r = q + lane;
       int e = -1;
       if (r < w1) {
-        e = idx[(t0 + r) * k + j];
+        e = idx_s[r * k + j];
         if (e < 0 || e >= E) e = -1;
       }
       const uint32_t peers = __match_any_sync(0xffffffffu, e);
@@ -407,7 +435,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     __syncthreads();
     // warp bases: choice base + chunk prefix + earlier warps, warps in order
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      int32_t run = cbase[j * E + e] + base[j * E + e];
+      int32_t run = stage_bases ? base_s[j * E + e] : cbase[j * E + e] + base[j * E + e];
       for (int w = 0; w < PLACE_WARPS; ++w) {
         const int32_t v = wc[w * E + e];
         wc[w * E + e] = run;
@@ -420,7 +448,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
       const int r = q + lane;
       int e = -1;
       if (r < w1) {
-        e = idx[(t0 + r) * k + j];
+        e = idx_s[r * k + j];
         if (e < 0 || e >= E) e = -1;
       }
       const uint32_t peers = __match_any_sync(0xffffffffu, e);
@@ -447,7 +475,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   // with bulk shared -> global stores; a buffer is reloaded once the stores that read it are done
   if (threadIdx.x != 0) return;
   uint8_t* ring = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(rows_s + tc * k) + 127) & ~static_cast<uintptr_t>(127));
+      (reinterpret_cast<uintptr_t>(base_s + (stage_bases ? kE : 0)) + 127) & ~static_cast<uintptr_t>(127));
   uint64_t* bar = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(nb) * row_bytes);
   for (int i = 0; i < nb; ++i) ptx::mbar_init(&bar[i], 1);
   ptx::fence_mbarrier_init();
@@ -489,7 +517,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   if (!ok) {
     set_status(status, MOE_DEV_TIMEOUT);
     // loads still in flight land in this block's shared memory: wait for them (bounded) first
-    for (int q = r + 1; q < issued; ++q) {
+    for (int q = r; q < issued; ++q) {
       const uint64_t tw = ptx::globaltimer_ns();
       while (!ptx::mbar_try_wait(&bar[q % nb], static_cast<uint32_t>((q / nb) & 1)) &&
              ptx::globaltimer_ns() - tw < COPY_WAIT_LIMIT_NS) {
@@ -522,7 +550,9 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
     if (e != cudaSuccess) return e;
     const uint32_t row_bytes = static_cast<uint32_t>(p.h) * (p.bf16 ? 2 : 4);
     const int nb = X ? static_cast<int>(std::max<uint32_t>(2, std::min<uint32_t>(16, COPY_RING_BYTES / row_bytes))) : 0;
-    const size_t psm = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + static_cast<size_t>(p.dp_tc) * p.k) +
+    const int stage_bases = p.k * p.E <= 4096 ? 1 : 0;  // the chunk's bases fit 16 KB of shared memory
+    const size_t psm = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + 2 * static_cast<size_t>(p.dp_tc) * p.k +
+                                          (stage_bases ? static_cast<size_t>(p.k) * p.E : 0)) +
                        128 + static_cast<size_t>(nb) * row_bytes + 8 * static_cast<size_t>(nb);
     if (psm > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(dispatch_place, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -531,7 +561,7 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
     }
     dispatch_place<<<p.dp_chunks, PLACE_THREADS, psm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, p.dp_chunks, p.C, hist,
                                                             offsets, slot_row, row_token, U, X, row_bytes, nb,
-                                                            status);
+                                                            status, stage_bases);
     return cudaGetLastError();
   }
   const size_t hist_smem = sizeof(int32_t) * p.E;

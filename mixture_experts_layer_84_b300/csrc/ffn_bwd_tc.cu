@@ -110,8 +110,13 @@ __device__ __forceinline__ void store_32(bf16* orow, int col0, int n_out, const 
 #pragma unroll
     for (int i = 0; i < 4; ++i) d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
   } else {
-    const bf16* src = reinterpret_cast<const bf16*>(packed);
-    for (int i = 0; i < 32 && col0 + i < n_out; ++i) orow[col0 + i] = src[i];
+    // the ragged end of a row: element by element, register indices only (no local copy)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = col0 + 2 * i;
+      if (c < n_out) orow[c] = __ushort_as_bfloat16(static_cast<unsigned short>(packed[i] & 0xffffu));
+      if (c + 1 < n_out) orow[c + 1] = __ushort_as_bfloat16(static_cast<unsigned short>(packed[i] >> 16));
+    }
   }
 }
 

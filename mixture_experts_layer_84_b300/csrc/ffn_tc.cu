@@ -94,8 +94,13 @@ __device__ __forceinline__ void store_32(bf16* orow, int col0, int n_out, const 
 #pragma unroll
     for (int i = 0; i < 4; ++i) d[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
   } else {
-    const bf16* src = reinterpret_cast<const bf16*>(packed);
-    for (int i = 0; i < 32 && col0 + i < n_out; ++i) orow[col0 + i] = src[i];
+    // the ragged end of a row: element by element, register indices only (no local copy)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = col0 + 2 * i;
+      if (c < n_out) orow[c] = __ushort_as_bfloat16(static_cast<unsigned short>(packed[i] & 0xffffu));
+      if (c + 1 < n_out) orow[c + 1] = __ushort_as_bfloat16(static_cast<unsigned short>(packed[i] >> 16));
+    }
   }
 }
 
@@ -457,7 +462,10 @@ constexpr uint32_t P_A_BYTES = 128 * BK * 2;     // 16 KB: this CTA's 128 rows
 constexpr uint32_t P_B_BYTES = 128 * BK * 2;     // 16 KB: this CTA's half of the 256 B rows
 constexpr uint32_t P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr size_t P_BAR_BYTES = 256;           // 17 mbarriers + tmem address + flags
-constexpr size_t P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + P_BAR_BYTES + sizeof(int) * (MAX_E + 1);
+// output staging: one 32-row x 64-column bf16 block (4 KB, 128-byte swizzle) per epilogue warp
+constexpr size_t P_OUT_OFF = (P_STAGES * P_STAGE_BYTES + P_BAR_BYTES + sizeof(int) * (MAX_E + 1) + 1023) / 1024 * 1024;
+constexpr uint32_t P_OUT_BYTES = 32 * 64 * 2;
+constexpr size_t P_SMEM_BYTES = 1024 + P_OUT_OFF + 4 * P_OUT_BYTES;
 static_assert(P_SMEM_BYTES <= 232448, "shared memory");
 static_assert((2 * P_STAGES + 2 + 2 + 1) * 8 + 12 <= P_BAR_BYTES, "barriers fit P_BAR_BYTES");
 
@@ -481,7 +489,8 @@ __device__ __forceinline__ bool wait_cluster_bounded(uint64_t* bar, uint32_t par
 template <bool SWIGLU, bool GATHER = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     grouped_gemm_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                         const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets, int E, int K,
+                         const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
+                         const int32_t* __restrict__ offsets, int E, int K,
                          int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out,
                          int32_t* status, Gather g = Gather{}) {
   static_assert(SWIGLU || !GATHER, "the gathered A operand is the up-projection's");
@@ -704,6 +713,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else {
     const int q = warp & 3;  // tensor-memory lane quarter this warp may read
     const int r_local = static_cast<int>(rank) * 128 + q * 32 + lane;
+    uint8_t* ostage = smem + P_OUT_OFF + q * P_OUT_BYTES;  // 1024-byte aligned
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = cid; tile < total; tile += ncl) {
       int e, nt, mt;
@@ -718,10 +728,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
       bf16* orow = out + row * n_out;
-      if (SWIGLU) {
+      // a warp whose 32 rows all lie inside the segment stages 64-column blocks in shared memory
+      // and stores them with the TMA; a warp that straddles the segment's end stores row by row
+      const bool warp_full = mt * P_BM + static_cast<int>(rank) * 128 + q * 32 + 32 <= n_e;
+      const int row0 = seg + mt * P_BM + static_cast<int>(rank) * 128 + q * 32;
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
-          uint32_t gv[32], uv[32], packed[16];
+      for (int c = 0; c < TILE_N; c += 32) {
+        uint32_t packed[16];
+        if (SWIGLU) {
+          uint32_t gv[32], uv[32];
           ptx::tmem_ld_32x32b_x32(tb + c, gv);
           ptx::tmem_ld_32x32b_x32(tb + BN / 2 + c, uv);
           ptx::tmem_wait_ld();
@@ -731,18 +746,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const float a1 = silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1]));
             packed[i] = Vec16<bf16>::pack2(a0, a1);
           }
-          if (row_ok) store_32(orow, nt * TILE_N + c, n_out, packed);
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32], packed[16];
+        } else {
+          uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(tb + c, v);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             packed[i] = Vec16<bf16>::pack2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        }
+        if (!warp_full) {
           if (row_ok) store_32(orow, nt * TILE_N + c, n_out, packed);
+          continue;
+        }
+        const int half = (c >> 5) & 1;  // which 64 bytes of the block's 128-byte rows
+        if (half == 0) {
+          if (lane == 0) ptx::bulk_wait_read<0>();  // this warp's previous block has been read
+          __syncwarp();
+        }
+        // row `lane`, 16-byte chunks 4 half .. 4 half + 3, at their 128-byte-swizzle positions
+        uint4* srow = reinterpret_cast<uint4*>(ostage + lane * 128);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          srow[(4 * half + i) ^ (lane & 7)] =
+              make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        if (half == 1) {
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmOut, ostage, nt * TILE_N + c - 32, row0);
+            ptx::bulk_commit();
+          }
         }
       }
       ptx::tc_fence_before();
@@ -751,6 +784,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) ptx::bulk_wait_all();  // this warp's stores have completed
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -1200,6 +1235,10 @@ static cudaError_t launch_gemm(bool pair, int grid, const CUtensorMap& a, const 
                                int32_t* status, cudaStream_t s, tc::Gather g = tc::Gather{}) {
   using namespace tc;
   if (pair) {
+    // the pair kernel's epilogue stores 32-row x 64-column blocks of `out` through this map
+    CUtensorMap tmOut;
+    if (!make_tmap(&tmOut, out, static_cast<uint64_t>(rows_cap), static_cast<uint64_t>(n_out), 32))
+      return cudaErrorNotSupported;
     auto kern = grouped_gemm_tc_pair<SWIGLU, GATHER>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(P_SMEM_BYTES));
@@ -1215,7 +1254,7 @@ static cudaError_t launch_gemm(bool pair, int grid, const CUtensorMap& a, const 
         2 * max_clusters < grid)
       grid = 2 * max_clusters;
     (void)cudaGetLastError();
-    kern<<<grid, THREADS, P_SMEM_BYTES, s>>>(a, b0, b1, offsets, E, K, b_rows, n_out, rows_cap, out, status, g);
+    kern<<<grid, THREADS, P_SMEM_BYTES, s>>>(a, b0, b1, tmOut, offsets, E, K, b_rows, n_out, rows_cap, out, status, g);
   } else {
     auto kern = grouped_gemm_tc<SWIGLU, false, GATHER>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -275,6 +275,15 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// 2-D tiled copy shared -> global through a tensor map (elements outside the tensor are not
+// written), tracked in this thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* smem_src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- bulk copies (no tensor map)
 // Global -> shared copy of `bytes` (a multiple of 16; both addresses 16-byte aligned), completion
 // counted as transaction bytes on `bar`.
