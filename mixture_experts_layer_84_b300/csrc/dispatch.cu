@@ -257,11 +257,11 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 //                    choice bases, the routed and kept counts, the offsets and n_dropped;
 //   dispatch_place  per chunk and choice: ranks among equal experts inside each warp (match_any)
 //                   on top of the chunk's base and the earlier warps' counts; writes slot_row and
-//                   row_token; then one thread streams the chunk's U rows through shared memory
-//                   with bulk copies, each row read once and written to each of its kept rows
-//                   (skipped when X is NULL).
+//                   row_token; then the chunk's U rows (contiguous) arrive in shared memory in
+//                   large bulk loads, two buffers deep, and the whole block writes each row to
+//                   its kept rows with coalesced 16-byte stores (skipped when X is NULL).
 constexpr int PLACE_THREADS = 256;
-constexpr uint32_t COPY_RING_BYTES = 96 * 1024;      // row buffers of one dispatch_place block
+constexpr size_t COPY_SMEM_BYTES = 208 * 1024;       // shared memory of one dispatch_place block, at most
 constexpr uint64_t COPY_WAIT_LIMIT_NS = 2000000000ull;
 constexpr int PLACE_WARPS = PLACE_THREADS / 32;
 constexpr int HIST_THREADS = 1024;
@@ -470,61 +470,72 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     __syncthreads();
   }
   if (!X || n == 0) return;
-  // the row copy: one thread streams the chunk's U rows through a ring of NB shared-memory row
-  // buffers (bulk global -> shared loads, NB - 1 in flight) and writes each row to its kept rows
-  // with bulk shared -> global stores; a buffer is reloaded once the stores that read it are done
-  if (threadIdx.x != 0) return;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(
+  // the row copy: the chunk's U rows are contiguous, so they arrive in shared memory in large bulk
+  // loads (two buffers of `sub` rows: the next part loads while this one is written out); all
+  // threads then write each row to its kept rows with coalesced 16-byte stores
+  uint8_t* buf0 = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(base_s + (stage_bases ? kE : 0)) + 127) & ~static_cast<uintptr_t>(127));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(nb) * row_bytes);
-  for (int i = 0; i < nb; ++i) ptx::mbar_init(&bar[i], 1);
-  ptx::fence_mbarrier_init();
-  ptx::fence_proxy_async_smem();
+  const int sub = nb;  // rows per buffer
+  uint8_t* bufs[2] = {buf0, buf0 + static_cast<size_t>(sub) * row_bytes};
+  uint64_t* bar = reinterpret_cast<uint64_t*>(buf0 + 2 * static_cast<size_t>(sub) * row_bytes);
+  __shared__ int abort_s;
+  const int parts = (n + sub - 1) / sub;
   const uint8_t* usrc = reinterpret_cast<const uint8_t*>(U) + t0 * row_bytes;
-  int issued = 0;  // loads issued: tokens 0 .. issued - 1
-  auto load = [&](int r) {
-    issued = r + 1;
-    uint64_t* bb = &bar[r % nb];
-    ptx::mbar_arrive_expect_tx(bb, row_bytes);
-    ptx::bulk_load(ring + static_cast<size_t>(r % nb) * row_bytes, usrc + static_cast<int64_t>(r) * row_bytes,
-                   row_bytes, bb);
-  };
-  for (int r = 0; r < min(nb - 1, n); ++r) load(r);
-  bool ok = true;
-  int r = 0;
-  for (; r < n; ++r) {
-    // bounded wait for the load of token r (its buffer's (r / nb)-th use)
-    const uint64_t tw = ptx::globaltimer_ns();
-    while (!ptx::mbar_try_wait(&bar[r % nb], static_cast<uint32_t>((r / nb) & 1))) {
-      if (ptx::globaltimer_ns() - tw > COPY_WAIT_LIMIT_NS) {
-        ok = false;
-        break;
+  if (threadIdx.x == 0) {
+    abort_s = 0;
+    ptx::mbar_init(&bar[0], 1);
+    ptx::mbar_init(&bar[1], 1);
+    ptx::fence_mbarrier_init();
+    ptx::fence_proxy_async_smem();
+    const uint32_t bytes = static_cast<uint32_t>(min(sub, n)) * row_bytes;
+    ptx::mbar_arrive_expect_tx(&bar[0], bytes);
+    ptx::bulk_load(bufs[0], usrc, bytes, &bar[0]);
+  }
+  const int vpr = static_cast<int>(row_bytes / 16);
+  int pi = 0;
+  for (; pi < parts; ++pi) {
+    if (threadIdx.x == 0) {
+      if (pi + 1 < parts) {  // the other buffer was written out by the whole block before the last barrier
+        ptx::fence_proxy_async_smem();
+        const int r1 = (pi + 1) * sub;
+        const uint32_t bytes = static_cast<uint32_t>(min(sub, n - r1)) * row_bytes;
+        uint64_t* bb = &bar[(pi + 1) & 1];
+        ptx::mbar_arrive_expect_tx(bb, bytes);
+        ptx::bulk_load(bufs[(pi + 1) & 1], usrc + static_cast<int64_t>(r1) * row_bytes, bytes, bb);
+      }
+      const uint64_t tw = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(&bar[pi & 1], static_cast<uint32_t>((pi >> 1) & 1))) {
+        if (ptx::globaltimer_ns() - tw > COPY_WAIT_LIMIT_NS) {
+          abort_s = 1;
+          break;
+        }
       }
     }
-    if (!ok) break;
-    const uint8_t* src = ring + static_cast<size_t>(r % nb) * row_bytes;
-    for (int j = 0; j < k; ++j) {
-      const int32_t row = rows_s[r * k + j];
-      if (row >= 0) ptx::bulk_store(reinterpret_cast<uint8_t*>(X) + static_cast<int64_t>(row) * row_bytes, src, row_bytes);
+    __syncthreads();
+    if (abort_s) break;
+    const int r0 = pi * sub, nr = min(sub, n - r0);
+    const uint4* src = reinterpret_cast<const uint4*>(bufs[pi & 1]);
+    const int per_row = k * vpr;
+    for (int it = threadIdx.x; it < nr * per_row; it += blockDim.x) {
+      const int r = it / per_row;
+      const int rem = it - r * per_row;
+      const int j = rem / vpr, v = rem - j * vpr;
+      const int32_t row = rows_s[(r0 + r) * k + j];
+      if (row >= 0) reinterpret_cast<uint4*>(X)[static_cast<int64_t>(row) * vpr + v] = src[r * vpr + v];
     }
-    ptx::bulk_commit();
-    const int next = r + nb - 1;  // goes into the buffer of token r - 1
-    if (next < n) {
-      if (r >= 1) ptx::bulk_wait_read<1>();  // the stores of token r - 1 have read their buffer
-      load(next);
-    }
+    __syncthreads();
   }
-  if (!ok) {
+  if (abort_s && threadIdx.x == 0) {
     set_status(status, MOE_DEV_TIMEOUT);
-    // loads still in flight land in this block's shared memory: wait for them (bounded) first
-    for (int q = r; q < issued; ++q) {
+    // the loads of the part that timed out and of the next one may still land in this block's shared
+    // memory: wait for them (bounded)
+    for (int q = pi; q < min(pi + 2, parts); ++q) {
       const uint64_t tw = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(&bar[q % nb], static_cast<uint32_t>((q / nb) & 1)) &&
+      while (!ptx::mbar_try_wait(&bar[q & 1], static_cast<uint32_t>((q >> 1) & 1)) &&
              ptx::globaltimer_ns() - tw < COPY_WAIT_LIMIT_NS) {
       }
     }
   }
-  ptx::bulk_wait_all();
 }
 
 cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, int32_t* counts_routed,
@@ -549,11 +560,13 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const uint32_t row_bytes = static_cast<uint32_t>(p.h) * (p.bf16 ? 2 : 4);
-    const int nb = X ? static_cast<int>(std::max<uint32_t>(2, std::min<uint32_t>(16, COPY_RING_BYTES / row_bytes))) : 0;
     const int stage_bases = p.k * p.E <= 4096 ? 1 : 0;  // the chunk's bases fit 16 KB of shared memory
-    const size_t psm = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + 2 * static_cast<size_t>(p.dp_tc) * p.k +
-                                          (stage_bases ? static_cast<size_t>(p.k) * p.E : 0)) +
-                       128 + static_cast<size_t>(nb) * row_bytes + 8 * static_cast<size_t>(nb);
+    const size_t meta = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + 2 * static_cast<size_t>(p.dp_tc) * p.k +
+                                           (stage_bases ? static_cast<size_t>(p.k) * p.E : 0));
+    // two row buffers in what is left of ~208 KB (at least one row each, at most the chunk)
+    const size_t room = meta + 128 + 16 < COPY_SMEM_BYTES ? COPY_SMEM_BYTES - meta - 128 - 16 : 0;
+    const int nb = X ? static_cast<int>(std::max<size_t>(1, std::min<size_t>(p.dp_tc, room / 2 / row_bytes))) : 0;
+    const size_t psm = meta + 128 + 2 * static_cast<size_t>(nb) * row_bytes + 16;
     if (psm > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(dispatch_place, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(psm));
