@@ -290,13 +290,13 @@ cudaError_t launch_route_logits_tc(const Plan& p, const void* U, const void* W_r
 //
 // A cluster of CS CTAs owns one 128-token tile; CTA c of the cluster runs the K-blocks
 // [c nkb / CS, (c+1) nkb / CS) of h through a TMA ring and tcgen05.mma 128 x N x 16 into its
-// tensor memory (N = E, or 2E with the noise columns, rounded up to 16).  Its four epilogue warps
-// copy the float32 accumulator into shared memory.  After a cluster barrier, CTA c takes the rows
-// [c R, (c+1) R), R = 128 / CS, and adds the CS slices of each logit in rank order (run-to-run
-// identical) through distributed shared memory, then the bias and the noise
-// eps * softplus(noise logit).  It stages them for select_tokens (select.cuh) in passes of
-// 256 / G tokens and adds its per-expert score sums and LSE^2 sum into one ppart row.  A second
-// cluster barrier keeps each CTA's shared memory alive until its peers have read it.
+// tensor memory (N = E, or 2E with the noise columns, rounded up to 16).  After a cluster barrier
+// (every CTA is past its main loop), its four epilogue warps push each float32 accumulator row to
+// the cluster CTA that owns the row -- CTA c owns rows [c R, (c+1) R), R = 128 / CS -- with 16-byte
+// remote stores into distributed shared memory.  After a second barrier each CTA adds the CS slices
+// of its logits in rank order (run-to-run identical) from its own shared memory, then the bias
+// and the noise eps * softplus(noise logit), stages them for select_tokens (select.cuh) in passes
+// of 256 / G tokens, and adds its per-expert score sums and LSE^2 sum into one ppart row.
 namespace rfu {
 
 using namespace rtc;
@@ -319,12 +319,12 @@ __host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stag
   g.N = N;
   g.stages = stages;
   g.stage_bytes = A_BYTES + b_bytes(N);
-  g.PN = N + 1;
+  g.PN = N + 4;  // 16-byte rows for the remote vector stores
   g.TB = THREADS / G;
   const int C = (E + G - 1) / G;
   g.LD = G * ((C & 1) ? C + 2 : C + 1);
   g.p_bytes = sizeof(float) * 128 * static_cast<size_t>(g.PN);
-  g.sel_floats = g.TB * g.LD + g.TB + g.TB * (n_group > 1 ? n_group : 0) + (E + 1);
+  g.sel_floats = g.TB * g.LD + g.TB + g.TB * (n_group > 1 ? n_group : 0) + (E + 1) + THREADS;
   const size_t ring = static_cast<size_t>(stages) * g.stage_bytes;
   const size_t tail = g.p_bytes + sizeof(float) * static_cast<size_t>(g.sel_floats);
   g.work = ((ring > tail ? ring : tail) + 15) / 16 * 16;
@@ -332,10 +332,10 @@ __host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stag
   return g;
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+// 16-byte store to a cluster CTA's shared memory (address from mapa).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
 }
 
 template <int KP, int G>
@@ -353,11 +353,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + 8;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tfull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  float* P = reinterpret_cast<float*>(smem);                       // [128][PN], after the main loop
+  float* Q = reinterpret_cast<float*>(smem);                       // [cs][R][PN], after the main loop
   float* sx = reinterpret_cast<float*>(smem + geo.p_bytes);       // select staging
   float* zsq = sx + geo.TB * geo.LD;
   float* gsc = zsq + geo.TB;
   float* colsum = gsc + geo.TB * (n_group > 1 ? n_group : 0);
+  float* colpart = colsum + (E + 1);                               // [THREADS] column-sum partials
 
   const uint32_t tmem_cols = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
   const uint32_t STAGE = geo.stage_bytes;
@@ -433,54 +434,60 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   }
-  // every TMA write has landed and every MMA has read its stage before the stages become P
-  if (warp >= 4) {
+  // the accumulator is complete (or the pipeline gave up); every CTA of the cluster must be past its
+  // main loop before any partial row lands in a peer's shared memory (which held its TMA stages)
+  bool ready = true;
+  if (warp >= 4) ready = __all_sync(0xffffffffu, wait_drain(tfull, 0));
+  if (warp >= 4 && !ready) *abort_flag = 1;
+  __syncthreads();
+  ptx::cluster_sync_all();
+  // partial rows to their owners: tile row i belongs to cluster CTA i / R, which keeps slot
+  // [rank][i % R] of Q [cs][R][PN] for it (16-byte remote stores)
+  const int R = BM / cs;
+  if (warp >= 4 && !*abort_flag) {
     const int q = warp & 3;
-    const bool ready = wait_drain(tfull, 0);
-    if (__all_sync(0xffffffffu, ready) && !*abort_flag) {
-      ptx::tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      float* prow = P + (q * 32 + lane) * geo.PN;
+    const int i = q * 32 + lane;
+    const int owner = i / R, li = i - owner * R;
+    const uint32_t dst = ptx::mapa_shared(ptx::smem_u32(Q + (rank * R + li) * geo.PN), static_cast<uint32_t>(owner));
+    ptx::tc_fence_after();
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < N; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tb + c, v);
-        ptx::tmem_wait_ld();
+    for (int c = 0; c < N; c += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(tb + c, v);
+      ptx::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c + i < N) prow[c + i] = __uint_as_float(v[i]);  // N is a multiple of 16, not of 32
-      }
-    } else {
-      *abort_flag = 1;
+      for (int i4 = 0; i4 < 8; ++i4)
+        if (c + 4 * i4 < N)  // N is a multiple of 16, not of 32
+          st_cluster_v4(dst + static_cast<uint32_t>(c + 4 * i4) * 4u, v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2],
+                        v[4 * i4 + 3]);
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, tmem_cols);
+  ptx::cluster_sync_all();  // every partial row has arrived
   const bool ok = !*abort_flag;
-  ptx::cluster_sync_all();  // every CTA's P is complete
 
-  // rows [rank R, (rank+1) R) of the tile: the CS slices summed in rank order, bias and noise added
-  const int R = BM / cs;
+  // rows [rank R, (rank+1) R) of the tile: the CS slices summed in rank order from local shared
+  // memory, then bias and noise
   const int64_t row0 = mt * BM + static_cast<int64_t>(rank) * R;
   const int64_t left = T - row0;
   const int rows_here = left <= 0 ? 0 : left < R ? static_cast<int>(left) : R;
-  const uint32_t p_local = ptx::smem_u32(P);
   if (ok) {
     for (int p0 = 0; p0 < rows_here; p0 += geo.TB) {
       const int rows = min(geo.TB, rows_here - p0);
       const SelLayout L(E, G);
       for (int i = threadIdx.x; i < rows * E; i += THREADS) {
         const int r = i / E, e = i - r * E;
-        const int prow = rank * R + p0 + r;
-        const int64_t t = row0 + p0 + r;
+        const int li = p0 + r;
+        const int64_t t = row0 + li;
         float x = 0.f, z = 0.f;
         for (int c = 0; c < cs; ++c) {
-          const uint32_t base = ptx::mapa_shared(p_local, static_cast<uint32_t>(c)) +
-                                static_cast<uint32_t>(prow * geo.PN + e) * 4u;
-          x += ld_cluster_f32(base);
-          if (noisy) z += ld_cluster_f32(base + static_cast<uint32_t>(E) * 4u);
+          const float* qr = Q + (c * R + li) * geo.PN;
+          x += qr[e];
+          if (noisy) z += qr[E + e];
         }
         if (b_r) x += b_r[e];
         if (noisy) x = fmaf(eps[t * E + e], softplus_f32(z), x);
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       select_tokens<KP, G>(sx, zsq, gsc, rows, row0 + p0, E, k, score_fn, renorm, n_group, topk_group, sel_bias,
                            idx, gate);
       __syncthreads();
-      score_column_sums(sx, zsq, rows, E, G, colsum, p0 > 0);
+      score_column_sums_split(sx, zsq, rows, E, G, colsum, colpart, p0 > 0);
       __syncthreads();
     }
     if (rows_here == 0)
@@ -501,7 +508,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) *ppart_rows = static_cast<int32_t>(gridDim.x);
   if (threadIdx.x == 0 && !ok) set_status(status, MOE_DEV_TIMEOUT);
-  ptx::cluster_sync_all();  // peers have finished reading this CTA's P
 }
 
 template <int KP, int G>

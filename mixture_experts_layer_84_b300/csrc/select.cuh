@@ -1,6 +1,6 @@
 // Scoring, top-k selection and gates of a tile of tokens whose final router logits are staged in
 // shared memory, and the tile's per-expert score sums for P_i and LSE^2 sum for the z-loss.  Used
-// by the selection kernel (route.cu) and by the fused router (route_fused.cu).
+// by the selection kernel (route.cu) and by the fused router (route_tc.cu).
 //
 // "MoE 与专家并行" (hs-black.github.io/posts/scaling-moe), section 路由器：打分、top-k、加权求和
 // (scores, top-k, gates), section softmax 门控还是 sigmoid 门控 (softmax or sigmoid scores, gates
@@ -244,6 +244,35 @@ __device__ __forceinline__ void score_column_sums(const float* sx, const float* 
     } else {
       for (int i = 0; i < rows; ++i) acc += zsq[i];
     }
+    out[e] = accumulate ? out[e] + acc : acc;
+  }
+}
+
+// score_column_sums with the rows split among all threads: row group q of NG = blockDim.x / (E + 1)
+// groups (at least one) adds rows [q rows / NG, (q+1) rows / NG) of column e into part[q (E + 1) + e];
+// then thread e adds the NG group sums in order.  The block synchronises inside; `part` holds
+// blockDim.x floats.
+__device__ __forceinline__ void score_column_sums_split(const float* sx, const float* zsq, int rows, int E, int G,
+                                                        float* out, float* part, bool accumulate) {
+  const SelLayout L(E, G);
+  const int W = E + 1;
+  const int NG = max(1, static_cast<int>(blockDim.x) / W);
+  for (int t = threadIdx.x; t < NG * W; t += blockDim.x) {
+    const int q = t / W, e = t - q * W;
+    const int i0 = (rows * q) / NG, i1 = (rows * (q + 1)) / NG;
+    float acc = 0.f;
+    if (e < E) {
+      const float* col = sx + L.at(0, e);
+      for (int i = i0; i < i1; ++i) acc += col[i * L.LD];
+    } else {
+      for (int i = i0; i < i1; ++i) acc += zsq[i];
+    }
+    part[t] = acc;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < W; e += blockDim.x) {
+    float acc = 0.f;
+    for (int q = 0; q < NG; ++q) acc += part[q * W + e];
     out[e] = accumulate ? out[e] + acc : acc;
   }
 }
