@@ -190,7 +190,7 @@ def launches_per_step(w: W.Workload, gather: bool = False) -> int:
     fused_router = w.dtype == W.BF16 and (2 * w.E if w.noisy else w.E) <= 256
     route = 1 if fused_router else 2       # the fused router (weights packed beforehand), or logits + selection
     if w.priority == W.PRIORITY_CHOICE_MAJOR:
-        dispatch = 2                       # histograms + scans, then slots + row copy (no copy when gathering)
+        dispatch = 3                       # histograms, column scans, then slots + row copy (no copy when gathering)
     else:
         dispatch = 3 if gather else 4      # count, scan, assign (, scatter)
     ffn, combine = 2, 1                    # two GEMMs; rows and statistics
