@@ -257,11 +257,12 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 //                    choice bases, the routed and kept counts, the offsets and n_dropped;
 //   dispatch_place  per chunk and choice: ranks among equal experts inside each warp (match_any)
 //                   on top of the chunk's base and the earlier warps' counts; writes slot_row and
-//                   row_token; then the chunk's U rows (contiguous) arrive in shared memory in
-//                   large bulk loads, two buffers deep, and the whole block writes each row to
-//                   its kept rows with coalesced 16-byte stores (skipped when X is NULL).
+//                   row_token; meanwhile the chunk's U rows (contiguous) arrive in shared memory
+//                   in large bulk loads, two buffers deep; then each warp writes 512-byte pieces
+//                   of the staged rows to all of their kept rows with coalesced 16-byte stores
+//                   (skipped when X is NULL).
 constexpr int PLACE_THREADS = 256;
-constexpr size_t COPY_SMEM_BYTES = 208 * 1024;       // shared memory of one dispatch_place block, at most
+constexpr size_t COPY_SMEM_BYTES = 100 * 1024;       // shared memory of one dispatch_place block: two fit an SM
 constexpr uint64_t COPY_WAIT_LIMIT_NS = 2000000000ull;
 constexpr int PLACE_WARPS = PLACE_THREADS / 32;
 constexpr int HIST_THREADS = 1024;
@@ -412,6 +413,28 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int32_t* base = hist + static_cast<int64_t>(blockIdx.x) * kE;
   const int32_t* cbase = hist + static_cast<int64_t>(n_chunks) * kE;
+  // the row copy's staging: two buffers of `nb` rows after the ranking's arrays, and their barriers;
+  // the first two parts of the chunk's rows start loading now, under the ranking
+  const bool copy = X != nullptr && n > 0 && nb > 0;
+  const int parts = copy ? (n + nb - 1) / nb : 0;
+  uint8_t* buf0 = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(base_s + (stage_bases ? kE : 0)) + 127) & ~static_cast<uintptr_t>(127));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(buf0 + 2 * static_cast<size_t>(nb) * row_bytes);
+  const uint8_t* usrc = reinterpret_cast<const uint8_t*>(U) + t0 * row_bytes;
+  auto load_part = [&](int q) {  // part q into buffer q & 1 (one thread)
+    const uint32_t bytes = static_cast<uint32_t>(min(nb, n - q * nb)) * row_bytes;
+    uint64_t* bb = &bar[q & 1];
+    ptx::mbar_arrive_expect_tx(bb, bytes);
+    ptx::bulk_load(buf0 + static_cast<size_t>(q & 1) * nb * row_bytes,
+                   usrc + static_cast<int64_t>(q) * nb * row_bytes, bytes, bb);
+  };
+  if (copy && threadIdx.x == 0) {
+    ptx::mbar_init(&bar[0], 1);
+    ptx::mbar_init(&bar[1], 1);
+    ptx::fence_mbarrier_init();
+    ptx::fence_proxy_async_smem();
+    for (int q = 0; q < min(2, parts); ++q) load_part(q);
+  }
   // everything the ranking reads, staged with loads that are all in flight together
   for (int i = threadIdx.x; i < n * k; i += blockDim.x) idx_s[i] = idx[t0 * k + i];
   if (stage_bases)
@@ -469,40 +492,16 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     }
     __syncthreads();
   }
-  if (!X || n == 0) return;
-  // the row copy: the chunk's U rows are contiguous, so they arrive in shared memory in large bulk
-  // loads (two buffers of `sub` rows: the next part loads while this one is written out); all
-  // threads then write each row to its kept rows with coalesced 16-byte stores
-  uint8_t* buf0 = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(base_s + (stage_bases ? kE : 0)) + 127) & ~static_cast<uintptr_t>(127));
-  const int sub = nb;  // rows per buffer
-  uint8_t* bufs[2] = {buf0, buf0 + static_cast<size_t>(sub) * row_bytes};
-  uint64_t* bar = reinterpret_cast<uint64_t*>(buf0 + 2 * static_cast<size_t>(sub) * row_bytes);
+  if (!copy) return;
+  // the row copy: part pi (rows pi nb .. of the chunk) is written out while part pi + 1 loads; each
+  // warp takes 512-byte pieces (row r, 32 16-byte vectors) and stores each to every kept row of r
   __shared__ int abort_s;
-  const int parts = (n + sub - 1) / sub;
-  const uint8_t* usrc = reinterpret_cast<const uint8_t*>(U) + t0 * row_bytes;
-  if (threadIdx.x == 0) {
-    abort_s = 0;
-    ptx::mbar_init(&bar[0], 1);
-    ptx::mbar_init(&bar[1], 1);
-    ptx::fence_mbarrier_init();
-    ptx::fence_proxy_async_smem();
-    const uint32_t bytes = static_cast<uint32_t>(min(sub, n)) * row_bytes;
-    ptx::mbar_arrive_expect_tx(&bar[0], bytes);
-    ptx::bulk_load(bufs[0], usrc, bytes, &bar[0]);
-  }
+  if (threadIdx.x == 0) abort_s = 0;
   const int vpr = static_cast<int>(row_bytes / 16);
+  const int upr = (vpr + 31) / 32;  // 512-byte pieces per row
   int pi = 0;
   for (; pi < parts; ++pi) {
     if (threadIdx.x == 0) {
-      if (pi + 1 < parts) {  // the other buffer was written out by the whole block before the last barrier
-        ptx::fence_proxy_async_smem();
-        const int r1 = (pi + 1) * sub;
-        const uint32_t bytes = static_cast<uint32_t>(min(sub, n - r1)) * row_bytes;
-        uint64_t* bb = &bar[(pi + 1) & 1];
-        ptx::mbar_arrive_expect_tx(bb, bytes);
-        ptx::bulk_load(bufs[(pi + 1) & 1], usrc + static_cast<int64_t>(r1) * row_bytes, bytes, bb);
-      }
       const uint64_t tw = ptx::globaltimer_ns();
       while (!ptx::mbar_try_wait(&bar[pi & 1], static_cast<uint32_t>((pi >> 1) & 1))) {
         if (ptx::globaltimer_ns() - tw > COPY_WAIT_LIMIT_NS) {
@@ -513,22 +512,28 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     }
     __syncthreads();
     if (abort_s) break;
-    const int r0 = pi * sub, nr = min(sub, n - r0);
-    const uint4* src = reinterpret_cast<const uint4*>(bufs[pi & 1]);
-    const int per_row = k * vpr;
-    for (int it = threadIdx.x; it < nr * per_row; it += blockDim.x) {
-      const int r = it / per_row;
-      const int rem = it - r * per_row;
-      const int j = rem / vpr, v = rem - j * vpr;
-      const int32_t row = rows_s[(r0 + r) * k + j];
-      if (row >= 0) reinterpret_cast<uint4*>(X)[static_cast<int64_t>(row) * vpr + v] = src[r * vpr + v];
+    const int r0 = pi * nb, nr = min(nb, n - r0);
+    const uint4* src = reinterpret_cast<const uint4*>(buf0 + static_cast<size_t>(pi & 1) * nb * row_bytes);
+    for (int u = warp; u < nr * upr; u += PLACE_WARPS) {
+      const int r = u / upr;
+      const int v = (u - r * upr) * 32 + lane;
+      const int32_t my_row = lane < k ? rows_s[(r0 + r) * k + lane] : -1;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (v < vpr) val = src[r * vpr + v];
+      for (int j = 0; j < k; ++j) {
+        const int32_t row = __shfl_sync(0xffffffffu, my_row, j);
+        if (row >= 0 && v < vpr) reinterpret_cast<uint4*>(X)[static_cast<int64_t>(row) * vpr + v] = val;
+      }
     }
-    __syncthreads();
+    __syncthreads();  // buffer pi & 1 has been read by every warp
+    if (threadIdx.x == 0 && pi + 2 < parts) {
+      ptx::fence_proxy_async_smem();
+      load_part(pi + 2);
+    }
   }
   if (abort_s && threadIdx.x == 0) {
     set_status(status, MOE_DEV_TIMEOUT);
-    // the loads of the part that timed out and of the next one may still land in this block's shared
-    // memory: wait for them (bounded)
+    // parts pi and pi + 1 may still be loading into this block's shared memory: wait for them (bounded)
     for (int q = pi; q < min(pi + 2, parts); ++q) {
       const uint64_t tw = ptx::globaltimer_ns();
       while (!ptx::mbar_try_wait(&bar[q & 1], static_cast<uint32_t>((q >> 1) & 1)) &&
@@ -563,18 +568,28 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
     const int stage_bases = p.k * p.E <= 4096 ? 1 : 0;  // the chunk's bases fit 16 KB of shared memory
     const size_t meta = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + 2 * static_cast<size_t>(p.dp_tc) * p.k +
                                            (stage_bases ? static_cast<size_t>(p.k) * p.E : 0));
-    // two row buffers in what is left of ~208 KB (at least one row each, at most the chunk)
+    // two row buffers in what is left of COPY_SMEM_BYTES (at most the chunk each); rows too wide for
+    // two buffers in any block are copied by dispatch_scatter after the placement instead
     const size_t room = meta + 128 + 16 < COPY_SMEM_BYTES ? COPY_SMEM_BYTES - meta - 128 - 16 : 0;
-    const int nb = X ? static_cast<int>(std::max<size_t>(1, std::min<size_t>(p.dp_tc, room / 2 / row_bytes))) : 0;
-    const size_t psm = meta + 128 + 2 * static_cast<size_t>(nb) * row_bytes + 16;
+    int nb = X ? static_cast<int>(std::min<size_t>(p.dp_tc, room / 2 / row_bytes)) : 0;
+    if (X && nb == 0 && meta + 128 + 2 * static_cast<size_t>(row_bytes) + 16 <= 200 * 1024) nb = 1;
+    const bool scatter_after = X && nb == 0;
+    const size_t psm = meta + (nb > 0 ? 128 + 2 * static_cast<size_t>(nb) * row_bytes + 16 : 0);
     if (psm > 48 * 1024) {
       const cudaError_t e = cudaFuncSetAttribute(dispatch_place, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(psm));
       if (e != cudaSuccess) return e;
     }
     dispatch_place<<<p.dp_chunks, PLACE_THREADS, psm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, p.dp_chunks, p.C, hist,
-                                                            offsets, slot_row, row_token, U, X, row_bytes, nb,
-                                                            status, stage_bases);
+                                                            offsets, slot_row, row_token, U, nb > 0 ? X : nullptr,
+                                                            row_bytes, nb, status, stage_bases);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !scatter_after) return e;
+    const int vpr = static_cast<int>(row_bytes / 16);
+    const int64_t want = (p.T + 7) / 8;
+    const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(current_sm_count()) * 8));
+    dispatch_scatter<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(U), slot_row, static_cast<uint4*>(X), p.T, p.k,
+                                            vpr);
     return cudaGetLastError();
   }
   const size_t hist_smem = sizeof(int32_t) * p.E;

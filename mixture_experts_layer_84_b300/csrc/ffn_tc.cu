@@ -105,51 +105,32 @@ __device__ __forceinline__ void store_32(bf16* orow, int col0, int n_out, const 
 }
 
 // ---- gathered A operand (the dispatch's row copy fused into the first GEMM) -------------------
-// Row r of the A operand is row gtok[r] of gsrc ([gsrc_rows, K] bf16).  The producer warp copies
-// it with 16-byte cp.async into the 128-byte-swizzled layout a tiled TMA load writes (16-byte
-// chunk c of tile row r lands at r * 128 + ((c ^ (r & 7)) << 4); stage bases are 1024-byte
-// aligned).  Lane L copies chunk L % 8 of tile rows L / 8 + 4 j, j < 32: each warp-wide copy
-// reads four whole 128-byte row segments.  Copies are waited for (ring size - 1) stages behind
-// the newest, so that every slot but one is in flight, then fenced into the async proxy (the
-// tensor cores read shared memory through it) and announced on the stage's full barrier.
-constexpr int GATHER_LAG = STAGES - 1;  // single-CTA ring; the pair ring uses P_STAGES - 1
-
+// Row r of the A operand is row tok[r] of the source ([rows, K] bf16, read through a tensor map
+// whose box is one row of 64 columns).  The producer warp loads a 128-row stage with 32 four-row
+// TMA gathers: lane L brings tile rows 4L..4L+3 into bytes [512 L, 512 L + 512) of the stage.  The
+// 128-byte swizzle follows the shared-memory address, so the stage ends up exactly as one tiled
+// load of 128 consecutive rows would leave it, and the MMA descriptors are unchanged.
 struct Gather {
-  const bf16* src;     // [rows, K]
   const int32_t* tok;  // source row of every A row
-  int64_t rows;        // rows of src
+  int64_t rows;        // rows of the source
 };
 
-// the source rows of this lane's 32 tile rows (rows past the kept rows, or ids out of range, read row 0)
-__device__ __forceinline__ void gather_tokens(const Gather& g, int64_t first_row, int64_t a_total, int lane,
-                                              int32_t (&tok)[32], int32_t* status) {
+// the source rows of A rows first_row .. first_row + 3 (rows past the kept rows, or ids out of
+// range, read row 0; their results are never stored)
+__device__ __forceinline__ int4 gather_rows4(const Gather& g, int64_t first_row, int64_t a_total, int32_t* status) {
+  int32_t t[4];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int64_t r = first_row + (lane >> 3) + 4 * j;
-    int32_t t = 0;
-    if (r < a_total) {
-      t = g.tok[r];
-      if (t < 0 || t >= g.rows) {
+  for (int i = 0; i < 4; ++i) {
+    t[i] = 0;
+    if (first_row + i < a_total) {
+      const int32_t v = g.tok[first_row + i];
+      if (v < 0 || v >= g.rows)
         set_status(status, MOE_DEV_BAD_ROW);
-        t = 0;
-      }
+      else
+        t[i] = v;
     }
-    tok[j] = t;
   }
-}
-
-// one 128-row x 64-column stage of the gathered A operand (columns >= K are zero-filled)
-__device__ __forceinline__ void gather_stage(uint8_t* sa, const bf16* src, int K, const int32_t (&tok)[32], int kb,
-                                             int lane) {
-  const int c = lane & 7;
-  const int col = kb * BK + c * 8;
-  const bool in = col < K;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int r = (lane >> 3) + 4 * j;
-    const bf16* gp = src + static_cast<int64_t>(tok[j]) * K + (in ? col : 0);
-    ptx::cp_async_16(sa + r * 128 + ((c ^ (r & 7)) << 4), gp, in ? 16u : 0u);
-  }
+  return make_int4(t[0], t[1], t[2], t[3]);
 }
 
 // SWIGLU: out[row, c] = SiLU(A W0^T)[row, c] * (A W1^T)[row, c], c < n_out (= d_e), W0/W1 rows per expert = d_e.
@@ -206,7 +187,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int e = 0; e < E; ++e) tab[e + 1] += tab[e];
     if (*bad_flag && blockIdx.x == 0) set_status(status, MOE_DEV_BAD_OFFSETS);
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&full[s], GATHER ? 2 : 1);  // (gather: + the producer warp's A copies)
+      ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -232,23 +213,23 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   if (GATHER && warp == 0) {
-    // the whole warp copies A; lane 0 also issues the B loads
+    // the whole warp loads A (four rows a lane), lane 0 also the B tiles
     if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB0);
       ptx::prefetch_tmap(&tmB1);
     }
+    const uint64_t pol_a = ptx::policy_evict_last();
     const uint64_t pol_b = ptx::policy_evict_normal();
     const int64_t a_total = seg_hi(offsets, E - 1, rows_cap);
-    uint32_t it = 0, armed = 0, armed_phase = 0;
+    uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       int e, nt, mt;
       decode_tile(tab, E, NT, tile, &e, &nt, &mt);
-      int32_t tok[32];
-      gather_tokens(g, static_cast<int64_t>(seg_lo(offsets, e)) + mt * BM, a_total, lane, tok, status);
+      const int4 rows = gather_rows4(g, static_cast<int64_t>(seg_lo(offsets, e)) + mt * BM + 4 * lane, a_total, status);
       const int b_row = e * b_rows_per_expert + nt * TILE_N;
       for (int kb = 0; kb < KB; ++kb) {
-        const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
         const bool got = ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
@@ -256,32 +237,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         uint8_t* sa = stages + stage * STAGE_BYTES;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&full[stage], B_BYTES);
+          ptx::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
           ptx::tma_load_2d(sa + A_BYTES, &tmB0, kb * BK, b_row, &full[stage], pol_b);
           ptx::tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB1, kb * BK, b_row, &full[stage], pol_b);
         }
-        gather_stage(sa, g.src, K, tok, kb, lane);
-        ptx::cp_async_commit();
+        __syncwarp();
+        ptx::tma_gather4(sa + lane * 512, &tmA, kb * BK, rows.x, rows.y, rows.z, rows.w, &full[stage], pol_a);
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-        ++it;
-        if (it > GATHER_LAG) {  // the copies of iteration it - 1 - GATHER_LAG have landed: announce them
-          ptx::cp_async_wait<GATHER_LAG>();
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&full[(it - 1 - GATHER_LAG) % STAGES]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
     }
-    // announce the last stages, then (lane 0) wait until every copy of this CTA has landed
-    ptx::cp_async_wait<0>();
-    ptx::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      for (uint32_t i = it > GATHER_LAG ? it - GATHER_LAG : 0; i < it; ++i) ptx::mbar_arrive(&full[i % STAGES]);
+    // every copy this warp started has landed before the block may exit
+    if (lane == 0)
       for (int s = 0; s < STAGES; ++s)
         if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_phase >> s) & 1u);
-    }
     __syncwarp();
   } else if (warp == 0) {
     if (lane == 0) {
@@ -484,8 +457,7 @@ __device__ __forceinline__ bool wait_cluster_bounded(uint64_t* bar, uint32_t par
   }
 }
 
-// GATHER (SwiGLU): each CTA gathers its 128 A rows from g; the even CTA's full barrier then also
-// counts one announcement from each CTA's producer warp.
+// GATHER (SwiGLU): each CTA gathers its 128 A rows (row ids from g) through tmA, whose box is one row.
 template <bool SWIGLU, bool GATHER = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     grouped_gemm_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -537,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     for (int e = 0; e < E; ++e) tab[e + 1] += tab[e];
     if (*bad_flag && blockIdx.x == 0) set_status(status, MOE_DEV_BAD_OFFSETS);
     for (int s = 0; s < P_STAGES; ++s) {
-      ptx::mbar_init(&full[s], GATHER ? 3 : 1);  // (gather: + both CTAs' A copies)
+      ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -564,59 +536,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   if (GATHER && warp == 0) {
-    constexpr int P_GATHER_LAG = P_STAGES - 1;
+    // the whole warp loads this CTA's A rows (four a lane), lane 0 also its half of the B rows
     const CUtensorMap* tmB = even ? &tmB0 : &tmB1;
-    if (lane == 0) ptx::prefetch_tmap(tmB);
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(tmB);
+    }
+    const uint64_t pol_a = ptx::policy_evict_last();
     const uint64_t pol_b = ptx::policy_evict_normal();
     const int64_t a_total = seg_hi(offsets, E - 1, rows_cap);
-    uint32_t it = 0, armed = 0, armed_phase = 0;
+    uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
     for (int tile = cid; ok && tile < total; tile += ncl) {
       int e, nt, mt;
       decode_tile(tab, E, NT, tile, &e, &nt, &mt);
-      int32_t tok[32];
-      gather_tokens(g, static_cast<int64_t>(seg_lo(offsets, e)) + mt * P_BM + static_cast<int>(rank) * 128, a_total,
-                    lane, tok, status);
+      const int4 rows = gather_rows4(
+          g, static_cast<int64_t>(seg_lo(offsets, e)) + mt * P_BM + static_cast<int>(rank) * 128 + 4 * lane, a_total,
+          status);
       const int b_row = e * b_rows_per_expert + nt * TILE_N;
       for (int kb = 0; kb < KB; ++kb) {
-        const uint32_t stage = it % P_STAGES, phase = (it / P_STAGES) & 1u;
         const bool got = ptx::mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_LIMIT_NS);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         uint8_t* sa = stages + stage * P_STAGE_BYTES;
+        const uint32_t full_pair = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
         if (lane == 0) {
-          const uint32_t full_pair = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
-          if (even) ptx::mbar_arrive_expect_tx(&full[stage], 2 * P_B_BYTES);
+          if (even) ptx::mbar_arrive_expect_tx(&full[stage], 2 * P_STAGE_BYTES);
           ptx::tma_load_2d_pair(sa + P_A_BYTES, tmB, kb * BK, b_row, full_pair, pol_b);
         }
-        gather_stage(sa, g.src, K, tok, kb, lane);
-        ptx::cp_async_commit();
+        __syncwarp();
+        ptx::tma_gather4_pair(sa + lane * 512, &tmA, kb * BK, rows.x, rows.y, rows.z, rows.w, full_pair, pol_a);
         armed |= 1u << stage;
         armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-        ++it;
-        if (it > P_GATHER_LAG) {  // announce the copies of iteration it - 1 - P_GATHER_LAG to the even CTA
-          ptx::cp_async_wait<P_GATHER_LAG>();
-          asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-          __syncwarp();
-          if (lane == 0)
-            ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&full[(it - 1 - P_GATHER_LAG) % P_STAGES]), 0));
+        if (++stage == P_STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
     }
-    ptx::cp_async_wait<0>();
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-    __syncwarp();
     if (lane == 0) {
-      for (uint32_t i = it > P_GATHER_LAG ? it - P_GATHER_LAG : 0; i < it; ++i)
-        ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&full[i % P_STAGES]), 0));
       if (even) {
+        // both CTAs' copies into every stage this CTA armed have landed before the pair may exit
         for (int s = 0; s < P_STAGES; ++s)
           if ((armed >> s) & 1u) mbar_wait_drain(&full[s], (armed_phase >> s) & 1u);
       }
       if (*abort_flag) {
-        // B copies whose completion is counted in the other CTA cannot be awaited here: give them time
+        // copies whose completion is counted in the other CTA cannot be awaited here: give them time
         const uint64_t t0 = ptx::globaltimer_ns();
         while (ptx::globaltimer_ns() - t0 < 1000000ull) {
         }
@@ -1294,7 +1261,8 @@ cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, 
   const uint32_t down_box = pair ? BN / 2 : BN;     // rows of W_down each CTA stages
   CUtensorMap tmX, tmG, tmU, tmAct, tmD;
   const uint64_t Tk = static_cast<uint64_t>(p.Tk);
-  if (!make_tmap(&tmX, gather ? gather_src : X, gather ? static_cast<uint64_t>(p.T) : Tk, p.h, a_box) ||
+  // (gathered: the token rows of the source, one-row boxes for the four-row gathers)
+  if (!make_tmap(&tmX, gather ? gather_src : X, gather ? static_cast<uint64_t>(p.T) : Tk, p.h, gather ? 1 : a_box) ||
       !make_tmap(&tmG, W_gate, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2) ||
       !make_tmap(&tmU, W_up, static_cast<uint64_t>(p.E) * p.d_e, p.h, BN / 2) ||
       !make_tmap(&tmAct, act, Tk, p.d_e, a_box) ||
@@ -1314,7 +1282,7 @@ cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, 
   cudaError_t e =
       gather ? launch_gemm<true, true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
                                        static_cast<bf16*>(act), status, s,
-                                       Gather{static_cast<const bf16*>(gather_src), gather_rows, p.T})
+                                       Gather{gather_rows, p.T})
              : launch_gemm<true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
                                  static_cast<bf16*>(act), status, s);
   if (e != cudaSuccess) return e;

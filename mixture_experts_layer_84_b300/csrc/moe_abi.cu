@@ -178,9 +178,11 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     while (cs < 8 && static_cast<int64_t>(q.rf_tiles) * cs * 2 <= 160 && nkb >= cs * 4) cs *= 2;
     q.rf_cs = cs;
     // ring depth: four stages when the grid takes several waves (two CTAs share an SM, one's
-    // epilogue overlapping the other's loads); up to eight when it fits one wave
+    // epilogue overlapping the other's loads); when it fits one wave, as deep as ~100 KB allows
+    // (up to eight), so that two CTAs still fit an SM: clusters of 8 CTAs that need 8 SMs of one
+    // GPC each do not all fit at once (measured: 28 vs 16 us on the Mixtral router)
     const int stage_kb = 16 + q.route_tc_n * 128 / 1024;
-    q.rf_stages = static_cast<int64_t>(q.rf_tiles) * cs > 148 ? 4 : std::max(4, std::min(8, 192 / stage_kb));
+    q.rf_stages = static_cast<int64_t>(q.rf_tiles) * cs > 148 ? 4 : std::max(4, std::min(8, 100 / stage_kb));
   }
   // selection blocks: 256 threads, fewer (down to a warp) when T is small, so that the
   // blocks still spread over about twice the SMs

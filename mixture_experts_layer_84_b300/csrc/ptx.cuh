@@ -81,6 +81,19 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(cache_policy)
       : "memory");
 }
+// Four rows of a 2-D tensor (rows y0..y3, any order, columns [x, x + box width)) into consecutive
+// box-sized slots of shared memory (tile::gather4; the tensor map's box is one row high).  The
+// 128-byte swizzle is applied on the destination address, so four rows written at a 512-byte
+// offset of a 1024-byte-aligned tile land where rows 4..7 of a tiled load would.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* tm, int32_t x, int32_t y0, int32_t y1,
+                                            int32_t y2, int32_t y3, uint64_t* bar, uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "l"(cache_policy)
+      : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -227,6 +240,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster_addr), "r"(x), "r"(y), "l"(cache_policy)
+      : "memory");
+}
+// tma_gather4 into this CTA's shared memory, counted on a barrier that may sit in the peer CTA.
+__device__ __forceinline__ void tma_gather4_pair(void* smem_dst, const CUtensorMap* tm, int32_t x, int32_t y0,
+                                                 int32_t y1, int32_t y2, int32_t y3, uint32_t bar_cluster_addr,
+                                                 uint64_t cache_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster_addr), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "l"(cache_policy)
       : "memory");
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_holder, uint32_t ncols) {

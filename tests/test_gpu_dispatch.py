@@ -26,6 +26,9 @@ CASES = [
     (1, 1, 1, 1, CM, 0.0, 8),
     (9000, 1024, 16, 50, CM, 1.0, 64),      # largest E and k
     (5000, 7, 3, 1500, TM, 2.0, 200),
+    (4096, 256, 8, 0, CM, 0.5, 7168),       # 256-expert shape at its row width (14 KB rows)
+    (2048, 8, 2, 640, CM, 0.0, 4096),       # Mixtral shape
+    (64, 4, 2, 0, CM, 0.0, 53248),          # 104 KB rows: two do not fit one block, scatter kernel copies
 ]
 
 
