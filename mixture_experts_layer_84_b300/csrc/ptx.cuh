@@ -94,6 +94,10 @@ __device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* t
       "l"(cache_policy)
       : "memory");
 }
+// Fetch the 128-byte line holding p into L2 (a hint; nothing waits for it).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -313,7 +313,8 @@ struct Geometry {
 
 // Shared memory of the fused router: the TMA stages, reused after the main loop for the partial
 // tile P [128][N + 1] and the select staging (sx [TB][LD], zsq [TB], gsc [TB][n_group],
-// colsum [E + 1]), then the barriers.  G = lanes per token of the selection.
+// colsum [E + 1]), then the barriers, then the logit bias and the selection bias [E] each.
+// G = lanes per token of the selection.
 __host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stages, int G) {
   Geometry g;
   g.N = N;
@@ -328,7 +329,7 @@ __host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stag
   const size_t ring = static_cast<size_t>(stages) * g.stage_bytes;
   const size_t tail = g.p_bytes + sizeof(float) * static_cast<size_t>(g.sel_floats);
   g.work = ((ring > tail ? ring : tail) + 15) / 16 * 16;
-  g.smem = 1024 + g.work + RF_BAR_BYTES;
+  g.smem = 1024 + g.work + RF_BAR_BYTES + 2 * sizeof(float) * static_cast<size_t>(E);  // + bias_s, selb_s
   return g;
 }
 
@@ -339,7 +340,7 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
 }
 
 template <int KP, int G>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     route_fused(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW, int64_t T, int h,
                 int E, int N, int stages, int cs, const float* __restrict__ b_r, const float* __restrict__ sel_bias,
                 const float* __restrict__ eps, int noisy, float* __restrict__ logits_out, int32_t* __restrict__ idx,
@@ -359,6 +360,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   float* gsc = zsq + geo.TB;
   float* colsum = gsc + geo.TB * (n_group > 1 ? n_group : 0);
   float* colpart = colsum + (E + 1);                               // [THREADS] column-sum partials
+  float* bias_s = reinterpret_cast<float*>(smem + geo.work + RF_BAR_BYTES);  // b_r (or zeros) [E]
+  float* selb_s = bias_s + E;                                                  // sel_bias [E]
 
   const uint32_t tmem_cols = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
   const uint32_t STAGE = geo.stage_bytes;
@@ -367,6 +370,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int64_t mt = blockIdx.x / cs;
   const int nkb = (h + BK - 1) / BK;
   const int kb_beg = (nkb * rank) / cs, kb_end = (nkb * (rank + 1)) / cs;
+  // the tile rows this CTA selects for: [rank R, (rank+1) R) of the tile
+  const int R = BM / cs;
+  const int64_t row0 = mt * BM + static_cast<int64_t>(rank) * R;
+  const int64_t left = T - row0;
+  const int rows_here = left <= 0 ? 0 : left < R ? static_cast<int>(left) : R;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -433,6 +441,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::mma_commit(tfull);  // complete (or drained after a timeout): the accumulator may be read
     }
     __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    // under the main loop: the biases into shared memory, and this CTA's rows of the noise into L2
+    // (the epilogue reads them with all its loads in flight, but one CTA per SM has few warps)
+    const int i0 = threadIdx.x - 64;
+    for (int e = i0; e < E; e += 64) {
+      bias_s[e] = b_r ? b_r[e] : 0.f;
+      selb_s[e] = sel_bias ? sel_bias[e] : 0.f;
+    }
+    if (noisy && rows_here > 0) {
+      const char* nb = reinterpret_cast<const char*>(eps + row0 * E);
+      const int64_t bytes = static_cast<int64_t>(rows_here) * E * static_cast<int64_t>(sizeof(float));
+      for (int64_t off = static_cast<int64_t>(i0) * 128; off < bytes; off += 64 * 128) ptx::prefetch_l2(nb + off);
+    }
   }
   // the accumulator is complete (or the pipeline gave up); every CTA of the cluster must be past its
   // main loop before any partial row lands in a peer's shared memory (which held its TMA stages)
@@ -443,7 +464,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   ptx::cluster_sync_all();
   // partial rows to their owners: tile row i belongs to cluster CTA i / R, which keeps slot
   // [rank][i % R] of Q [cs][R][PN] for it (16-byte remote stores)
-  const int R = BM / cs;
   if (warp >= 4 && !*abort_flag) {
     const int q = warp & 3;
     const int i = q * 32 + lane;
@@ -471,32 +491,45 @@ __global__ void __launch_bounds__(THREADS, 1)
   const bool ok = !*abort_flag;
 
   // rows [rank R, (rank+1) R) of the tile: the CS slices summed in rank order from local shared
-  // memory, then bias and noise
-  const int64_t row0 = mt * BM + static_cast<int64_t>(rank) * R;
-  const int64_t left = T - row0;
-  const int rows_here = left <= 0 ? 0 : left < R ? static_cast<int>(left) : R;
+  // memory, then bias and noise; the pass's rows x E entries in order, eight a thread at a time
+  // with their noise loads issued together
   if (ok) {
+    constexpr int RB = 8;
     for (int p0 = 0; p0 < rows_here; p0 += geo.TB) {
       const int rows = min(geo.TB, rows_here - p0);
       const SelLayout L(E, G);
-      for (int i = threadIdx.x; i < rows * E; i += THREADS) {
-        const int r = i / E, e = i - r * E;
-        const int li = p0 + r;
-        const int64_t t = row0 + li;
-        float x = 0.f, z = 0.f;
-        for (int c = 0; c < cs; ++c) {
-          const float* qr = Q + (c * R + li) * geo.PN;
-          x += qr[e];
-          if (noisy) z += qr[E + e];
+      const int n_el = rows * E;
+      const float* eps_p = noisy ? eps + (row0 + p0) * E : nullptr;
+      float* lo_p = logits_out ? logits_out + (row0 + p0) * E : nullptr;
+      for (int b = 0; b < n_el; b += RB * THREADS) {
+        float ev[RB];
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+          const int i = b + u * THREADS + static_cast<int>(threadIdx.x);
+          ev[u] = (noisy && i < n_el) ? eps_p[i] : 0.f;
         }
-        if (b_r) x += b_r[e];
-        if (noisy) x = fmaf(eps[t * E + e], softplus_f32(z), x);
-        if (logits_out) logits_out[t * E + e] = x;
-        sx[L.at(r, e)] = x;
+#pragma unroll
+        for (int u = 0; u < RB; ++u) {
+          const int i = b + u * THREADS + static_cast<int>(threadIdx.x);
+          if (i < n_el) {
+            const int r = i / E, e = i - r * E;
+            const int li = p0 + r;
+            float x = 0.f, z = 0.f;
+            for (int c = 0; c < cs; ++c) {
+              const float* qr = Q + (c * R + li) * geo.PN;
+              x += qr[e];
+              if (noisy) z += qr[E + e];
+            }
+            if (b_r) x += bias_s[e];
+            if (noisy) x = fmaf(ev[u], softplus_f32(z), x);
+            if (lo_p) lo_p[i] = x;
+            sx[L.at(r, e)] = x;
+          }
+        }
       }
       __syncthreads();
-      select_tokens<KP, G>(sx, zsq, gsc, rows, row0 + p0, E, k, score_fn, renorm, n_group, topk_group, sel_bias,
-                           idx, gate);
+      select_tokens<KP, G>(sx, zsq, gsc, rows, row0 + p0, E, k, score_fn, renorm, n_group, topk_group,
+                           sel_bias ? selb_s : nullptr, idx, gate);
       __syncthreads();
       score_column_sums_split(sx, zsq, rows, E, G, colsum, colpart, p0 > 0);
       __syncthreads();
