@@ -501,29 +501,60 @@ __global__ void __launch_bounds__(THREADS, 2)
       const int n_el = rows * E;
       const float* eps_p = noisy ? eps + (row0 + p0) * E : nullptr;
       float* lo_p = logits_out ? logits_out + (row0 + p0) * E : nullptr;
-      for (int b = 0; b < n_el; b += RB * THREADS) {
-        float ev[RB];
+      if (THREADS % E == 0) {
+        // every thread keeps one expert e and steps over the rows: no division per entry
+        const int e = static_cast<int>(threadIdx.x) % E, rstep = THREADS / E;
+        const int pos = L.at(0, e);
+        const float be = bias_s[e];
+        for (int r0 = static_cast<int>(threadIdx.x) / E; r0 < rows; r0 += RB * rstep) {
+          float ev[RB];
 #pragma unroll
-        for (int u = 0; u < RB; ++u) {
-          const int i = b + u * THREADS + static_cast<int>(threadIdx.x);
-          ev[u] = (noisy && i < n_el) ? eps_p[i] : 0.f;
-        }
+          for (int u = 0; u < RB; ++u) {
+            const int r = r0 + u * rstep;
+            ev[u] = (noisy && r < rows) ? eps_p[static_cast<int64_t>(r) * E + e] : 0.f;
+          }
 #pragma unroll
-        for (int u = 0; u < RB; ++u) {
-          const int i = b + u * THREADS + static_cast<int>(threadIdx.x);
-          if (i < n_el) {
-            const int r = i / E, e = i - r * E;
-            const int li = p0 + r;
-            float x = 0.f, z = 0.f;
-            for (int c = 0; c < cs; ++c) {
-              const float* qr = Q + (c * R + li) * geo.PN;
-              x += qr[e];
-              if (noisy) z += qr[E + e];
+          for (int u = 0; u < RB; ++u) {
+            const int r = r0 + u * rstep;
+            if (r < rows) {
+              const float* qr = Q + (p0 + r) * geo.PN + e;
+              float x = 0.f, z = 0.f;
+              for (int c = 0; c < cs; ++c) {
+                x += qr[c * R * geo.PN];
+                if (noisy) z += qr[c * R * geo.PN + E];
+              }
+              if (b_r) x += be;
+              if (noisy) x = fmaf(ev[u], softplus_f32(z), x);
+              if (lo_p) lo_p[static_cast<int64_t>(r) * E + e] = x;
+              sx[r * L.LD + pos] = x;
             }
-            if (b_r) x += bias_s[e];
-            if (noisy) x = fmaf(ev[u], softplus_f32(z), x);
-            if (lo_p) lo_p[i] = x;
-            sx[L.at(r, e)] = x;
+          }
+        }
+      } else {
+        for (int b = 0; b < n_el; b += RB * THREADS) {
+          float ev[RB];
+#pragma unroll
+          for (int u = 0; u < RB; ++u) {
+            const int i = b + u * THREADS + static_cast<int>(threadIdx.x);
+            ev[u] = (noisy && i < n_el) ? eps_p[i] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < RB; ++u) {
+            const int i = b + u * THREADS + static_cast<int>(threadIdx.x);
+            if (i < n_el) {
+              const int r = i / E, e = i - r * E;
+              const int li = p0 + r;
+              float x = 0.f, z = 0.f;
+              for (int c = 0; c < cs; ++c) {
+                const float* qr = Q + (c * R + li) * geo.PN;
+                x += qr[e];
+                if (noisy) z += qr[E + e];
+              }
+              if (b_r) x += bias_s[e];
+              if (noisy) x = fmaf(ev[u], softplus_f32(z), x);
+              if (lo_p) lo_p[i] = x;
+              sx[L.at(r, e)] = x;
+            }
           }
         }
       }
