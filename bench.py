@@ -378,6 +378,38 @@ def workload_config(w: W.Workload, n_rot: int = 0):
 STAGES = ("route", "dispatch", "ffn", "shared_ffn", "combine")
 
 
+class _GraphEvents:
+    """CUDA events recorded as nodes of a captured graph (cudaEventRecordExternal), so that the
+    device time between two stages of one graph replay can be read without launch gaps."""
+
+    EXTERNAL = 0x01  # cudaEventRecordExternal
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.rt = ctypes.CDLL("libcudart.so.13")
+        self.rt.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        self.rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.rt.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+
+    def new(self):
+        ev = self.ct.c_void_p()
+        if self.rt.cudaEventCreate(self.ct.byref(ev)) != 0:
+            raise RuntimeError("cudaEventCreate failed")
+        return ev
+
+    def record(self, ev, stream):
+        if self.rt.cudaEventRecordWithFlags(ev, self.ct.c_void_p(stream.cuda_stream), self.EXTERNAL) != 0:
+            raise RuntimeError("cudaEventRecordWithFlags failed")
+
+    def elapsed(self, a, b) -> float:
+        ms = self.ct.c_float()
+        if self.rt.cudaEventElapsedTime(self.ct.byref(ms), a, b) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return ms.value
+
+
 class LayerRun:
     """One workload on the device: inputs, rotating token batches, buffers, and CUDA graphs of the
     whole layer and of each stage (one of each per batch)."""
@@ -400,6 +432,7 @@ class LayerRun:
         self.rows8 = L.FP8Rows.allocate(self.cfg, device=device) if fp8 else None
         self.stages = [s for s in STAGES if s != "shared_ffn" or w.n_shared]
         self.graphs, self.stage_graphs, self.graph_error = [], [], None
+        self.timed_graphs, self.graph_events, self.stage_timing_note = [], None, None
         # the router weights packed once for the tensor-core router (None where it reads W_r as is);
         # timed on its own, outside every timed region
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -489,6 +522,24 @@ class LayerRun:
             self.graphs, self.stage_graphs = [], []
             self.graph_error = str(exc).splitlines()[0][:200]
             torch.cuda.synchronize(dev)
+            return
+        # the whole layer once more per batch, with an event node before each stage and after the last
+        try:
+            ge = _GraphEvents()
+            for U in self.pool:
+                evs = [ge.new() for _ in range(len(self.stages) + 1)]
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+                    for j, s in enumerate(self.stages):
+                        ge.record(evs[j], cap)
+                        self.run_stage(s, U)
+                    ge.record(evs[-1], cap)
+                self.timed_graphs.append((g, evs))
+            self.graph_events = ge
+        except (RuntimeError, OSError, AttributeError) as exc:
+            self.timed_graphs, self.graph_events = [], None
+            self.stage_timing_note = "event nodes unavailable (" + str(exc).splitlines()[0][:120] + ")"
+            torch.cuda.synchronize(dev)
 
     def step(self, i):
         if self.graphs:
@@ -521,8 +572,26 @@ class LayerRun:
         return t0.elapsed_time(t1)
 
     def time_stages(self, K):
-        """Per stage, the median device time over K steps run stage graph by stage graph."""
+        """Per stage, the median device time over K steps: between the event nodes of one whole-layer
+        graph replay where those exist, else between the replays of each stage's own graph."""
         n = len(self.stages)
+        if self.timed_graphs:
+            ge = self.graph_events
+            try:
+                for i in range(min(K, 3)):
+                    self.timed_graphs[i % self.n_rot][0].replay()
+                torch.cuda.synchronize(self.device)
+                per = [[] for _ in range(n)]
+                for i in range(K):
+                    g, evs = self.timed_graphs[i % self.n_rot]
+                    g.replay()
+                    torch.cuda.synchronize(self.device)  # the next replay of this graph re-records its events
+                    for j in range(n):
+                        per[j].append(ge.elapsed(evs[j], evs[j + 1]))
+                return {s: statistics.median(per[j]) for j, s in enumerate(self.stages)}
+            except RuntimeError as exc:
+                self.timed_graphs = []
+                self.stage_timing_note = "event nodes unreadable (" + str(exc).splitlines()[0][:120] + ")"
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(K)]
         for i in range(min(K, 3)):
             self.stage_step(i, evs[i])  # warm-up of the stage graphs
@@ -532,6 +601,14 @@ class LayerRun:
         torch.cuda.synchronize(self.device)
         return {s: statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
                 for j, s in enumerate(self.stages)}
+
+    def stage_timing_desc(self) -> str:
+        if self.timed_graphs:
+            return ("device time between event nodes before each stage of one whole-layer graph replay, median "
+                    "over the K steps (a stage carries the write-back of the dirty L2 lines left by the one before)")
+        what = ("device time of each stage's own CUDA graph, replayed in layer order with events between them, "
+                "median over the K steps")
+        return what + ("; " + self.stage_timing_note if self.stage_timing_note else "")
 
     def work(self, K):
         A_mean = sum(self.A_of[i % self.n_rot] for i in range(K)) / K
@@ -770,8 +847,7 @@ def run_b300(args, w: W.Workload):
             "value_range": [round(weak_scaling_value(w.T, K, ws_n, max(regions) * 1e-3), 1),
                             round(weak_scaling_value(w.T, K, ws_n, min(regions) * 1e-3), 1)],
             "roofline": roof, "stages": stages,
-            "stage_timing": "device time of each stage's own CUDA graph, replayed in layer order with events between "
-                            "them, median over the K steps",
+            "stage_timing": run.stage_timing_desc(),
             "stage_sum_ms": round(sum(stage_ms.values()), 5),
             "kept_pairs_A": A_mean, "active_experts": act_mean,
             "router_pack_ms": None if run.pack_ms is None else round(run.pack_ms, 5),

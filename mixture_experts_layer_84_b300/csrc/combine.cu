@@ -23,21 +23,19 @@ namespace moe {
 
 constexpr int COMBINE_THREADS = 256;
 constexpr int COMBINE_UNROLL = 2;   // 4 measured slower with k = 6..8
-constexpr int COMBINE_JB = 4;       // expert rows whose loads are in flight together
 constexpr int STAT_GROUPS = 32;     // first-level slices of the statistics reduction
 
 // Row combine and statistics in one launch.
 //   Rows: one warp per token (grid-stride), 16-byte vectors; float32 accumulation of u_t, then the
-//   shared experts' rows in order, then g_j y_j for j ascending, rounded once.  The expert rows are
-//   loaded COMBINE_JB choices at a time before they are added, so every lane keeps several loads
-//   in flight.
+//   shared experts' rows in order, then g_j y_j for j ascending, rounded once.  Few registers keep
+//   many warps resident, which is what keeps enough loads in flight.
 //   Statistics in two levels: the first `groups` blocks each add a slice of the rows of the router's
 //   per-block score sums, every column, in row order; the block that finishes last (an atomic
 //   count; nobody waits) adds those partial rows in group order (P_i, and the z-loss in column E),
 //   forms f_i from the routed counts and aux = E sum_i f_i P_i in expert order, and resets the
 //   count for the next call.  Every result is the same from run to run.
 template <typename T>
-__global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_stats(
+__global__ void __launch_bounds__(COMBINE_THREADS) combine_stats(
     const uint4* __restrict__ U, const uint4* __restrict__ Y, const uint4* __restrict__ Y_shared, int n_shared,
     const int32_t* __restrict__ slot_row, const float* __restrict__ gate, uint4* __restrict__ out, int64_t n_tok,
     int k, int vpr, int64_t rows_cap, int32_t* status, const float* __restrict__ ppart,
@@ -99,36 +97,18 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_stats(
           }
         }
       }
-      // the expert rows JB choices at a time: all their loads are issued before any is added, so
-      // that each lane keeps JB x COMBINE_UNROLL loads in flight; then added in choice order
-      for (int j0 = 0; j0 < k; j0 += COMBINE_JB) {
-        int32_t r[COMBINE_JB];
-        float g[COMBINE_JB];
-        uint4 yv[COMBINE_JB][COMBINE_UNROLL];
+      for (int j = 0; j < k; ++j) {
+        const int32_t r = __shfl_sync(0xffffffffu, my_row, j);
+        const float g = __shfl_sync(0xffffffffu, my_g, j);
+        if (r < 0) continue;
 #pragma unroll
-        for (int jj = 0; jj < COMBINE_JB; ++jj) {
-          const int j = j0 + jj;
-          r[jj] = __shfl_sync(0xffffffffu, my_row, j < k ? j : 0);
-          g[jj] = __shfl_sync(0xffffffffu, my_g, j < k ? j : 0);
-          if (j >= k) r[jj] = -1;
+        for (int u = 0; u < COMBINE_UNROLL; ++u) {
+          const int v = base + lane + 32 * u;
+          if (v < vpr) {
+            float y[N];
+            Vec16<T>::unpack(ldg_stream(Y + static_cast<int64_t>(r) * vpr + v), y);
 #pragma unroll
-          for (int u = 0; u < COMBINE_UNROLL; ++u) {
-            const int v = base + lane + 32 * u;
-            if (r[jj] >= 0 && v < vpr) yv[jj][u] = ldg_stream(Y + static_cast<int64_t>(r[jj]) * vpr + v);
-          }
-        }
-#pragma unroll
-        for (int jj = 0; jj < COMBINE_JB; ++jj) {
-          if (r[jj] < 0) continue;
-#pragma unroll
-          for (int u = 0; u < COMBINE_UNROLL; ++u) {
-            const int v = base + lane + 32 * u;
-            if (v < vpr) {
-              float y[N];
-              Vec16<T>::unpack(yv[jj][u], y);
-#pragma unroll
-              for (int i = 0; i < N; ++i) acc[u][i] = fmaf(g[jj], y[i], acc[u][i]);
-            }
+            for (int i = 0; i < N; ++i) acc[u][i] = fmaf(g, y[i], acc[u][i]);
           }
         }
       }

@@ -695,7 +695,7 @@ cudaError_t launch_ffn_backward_tc(const Plan& p, const void* X, const int32_t* 
   using namespace bwd;
   if (p.Tk == 0) return cudaSuccess;
   const uint64_t Tk = static_cast<uint64_t>(p.Tk), E = static_cast<uint64_t>(p.E);
-  CUtensorMap tm_dY, tm_X, tm_dact, tm_dG, tm_dUp, tm_act, tm_Wd, tm_Wg_k, tm_Wu_k, tm_Wg_mn, tm_Wu_mn;
+  CUtensorMap tm_dY, tm_X, tm_dact, tm_dG, tm_dUp, tm_Wd, tm_Wg_k, tm_Wu_k, tm_Wg_mn, tm_Wu_mn;
   CUtensorMap tm_dY_mn, tm_dG_mn, tm_dUp_mn, tm_act_mn, tm_X_mn;
   // row-tiled A operands (K-major boxes of 128 rows) and K-major forward weights (boxes of 128 rows)
   if (!make_tmap(&tm_dY, dY, Tk, p.h, BM) || !make_tmap(&tm_X, X, Tk, p.h, BM) ||

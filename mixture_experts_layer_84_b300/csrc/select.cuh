@@ -23,7 +23,6 @@
 namespace moe {
 
 constexpr int KMAX = 16;
-constexpr int SEL_CMAX = 32;  // experts per lane at most: G = E / 32 rounded up to a power of two
 
 __device__ __forceinline__ float softplus_f32(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
@@ -53,8 +52,7 @@ struct SelLayout {
 // score + bias), the lanes merge their lists bitonically (the elementwise better of one list and
 // the other reversed is bitonic and holds the top KP of both); the gates come from the selected
 // experts' scores.  Then the normalised scores (for P) are written back in place and LSE^2 into
-// zsq[r].  Each lane keeps its chunk (at most SEL_CMAX logits) in registers for the passes that
-// touch every logit.  Every thread of the block must call this (the shuffles span whole warps).  Scores use
+// zsq[r].  Every thread of the block must call this (the shuffles span whole warps).  Scores use
 // the fast exponential (a few ulps; the selection compares logits, or score + bias with a margin
 // far above that).
 template <int KP, int G>
@@ -66,32 +64,23 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
   const bool tok = r < rows;
   const int e0 = g * L.C;
   const int e1 = min(E, e0 + L.C);
-  const int cnt = tok ? max(0, e1 - e0) : 0;  // experts of this lane's chunk (C <= 32)
   float* rowp = sx + r * L.LD;
   float* chunk = rowp + g * L.CS;
   const bool softmax = score_fn == MOE_SCORE_SOFTMAX;
-  // the chunk in registers; maxima, exp-sums and the sigmoid sums in four interleaved partials
-  // (independent chains), combined in a fixed order
-  float xv[SEL_CMAX];
-#pragma unroll
-  for (int j = 0; j < SEL_CMAX; ++j) xv[j] = j < cnt ? chunk[j] : -INFINITY;
-  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int j = 0; j < SEL_CMAX; ++j) m4[j & 3] = fmaxf(m4[j & 3], xv[j]);
-  float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  float mx = -INFINITY;
+  if (tok)
+    for (int e = e0; e < e1; ++e) mx = fmaxf(mx, chunk[e - e0]);
 #pragma unroll
   for (int o = 1; o < G; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float s4[4] = {0.f, 0.f, 0.f, 0.f}, d4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < SEL_CMAX; ++j) {
-    if (j < cnt) {
-      const float ex = __expf(xv[j] - mx);
-      s4[j & 3] += ex;
-      d4[j & 3] += softmax ? ex : 1.f / (1.f + __expf(-xv[j]));
+  float sum_exp = 0.f, denom = 0.f;
+  if (tok) {
+    for (int e = e0; e < e1; ++e) {
+      const float x = chunk[e - e0];
+      const float ex = __expf(x - mx);
+      sum_exp += ex;
+      denom += softmax ? ex : 1.f / (1.f + __expf(-x));
     }
   }
-  float sum_exp = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-  float denom = (d4[0] + d4[1]) + (d4[2] + d4[3]);
 #pragma unroll
   for (int o = 1; o < G; o <<= 1) {
     sum_exp += __shfl_xor_sync(0xffffffffu, sum_exp, o);
@@ -230,9 +219,10 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
   // every lane has read what it needs from the row before any lane overwrites its chunk
   __syncwarp();
   if (tok) {
-#pragma unroll
-    for (int j = 0; j < SEL_CMAX; ++j)
-      if (j < cnt) chunk[j] = (softmax ? __expf(xv[j] - mx) : 1.f / (1.f + __expf(-xv[j]))) / denom;
+    for (int e = e0; e < e1; ++e) {
+      const float x = chunk[e - e0];
+      chunk[e - e0] = (softmax ? __expf(x - mx) : 1.f / (1.f + __expf(-x))) / denom;
+    }
     if (g == 0) {
       const float lse = mx + logf(sum_exp);
       zsq[r] = lse * lse;
