@@ -35,13 +35,13 @@ constexpr int STAT_GROUPS = 32;     // first-level slices of the statistics redu
 //   forms f_i from the routed counts and aux = E sum_i f_i P_i in expert order, and resets the
 //   count for the next call.  Every result is the same from run to run.
 template <typename T>
-__global__ void __launch_bounds__(COMBINE_THREADS) combine_stats(
+__global__ void __launch_bounds__(COMBINE_THREADS, 5) combine_stats(
     const uint4* __restrict__ U, const uint4* __restrict__ Y, const uint4* __restrict__ Y_shared, int n_shared,
     const int32_t* __restrict__ slot_row, const float* __restrict__ gate, uint4* __restrict__ out, int64_t n_tok,
     int k, int vpr, int64_t rows_cap, int32_t* status, const float* __restrict__ ppart,
     const int32_t* __restrict__ ppart_rows, const int32_t* __restrict__ counts_routed, int E, float* __restrict__ f,
     float* __restrict__ P, float* __restrict__ aux, float* __restrict__ z_loss, int32_t* __restrict__ done_count,
-    float* __restrict__ part2, int groups) {
+    float* __restrict__ part2, int groups, int spu) {
   constexpr int N = Vec16<T>::N;
   // statistics, first level: block g < groups adds rows [g R, (g+1) R) of the router's per-block
   // sums, every column, in row order (loads issued eight at a time)
@@ -63,10 +63,27 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_stats(
     }
   }
 
-  // rows
+  // rows: warp tasks of `spu` consecutive 32 x COMBINE_UNROLL-vector pieces of one token row (the
+  // whole row when there are tokens enough for every warp; fewer pieces when there are not, so that
+  // short batches still spread over all warps)
   const int lane = threadIdx.x % 32;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; t < n_tok; t += warps) {
+  const int pieces = (vpr + 32 * COMBINE_UNROLL - 1) / (32 * COMBINE_UNROLL);
+  const int tasks_per_tok = (pieces + spu - 1) / spu;
+  // task = t * tasks_per_tok + q advances by `warps` a step: (t, q) is carried along without division
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  const int64_t dt = warps / tasks_per_tok;
+  const int dq = static_cast<int>(warps - dt * tasks_per_tok);
+  int64_t t = first / tasks_per_tok;
+  int q = static_cast<int>(first - t * tasks_per_tok);
+  for (; t < n_tok; t += dt, q += dq) {
+    if (q >= tasks_per_tok) {
+      q -= tasks_per_tok;
+      ++t;
+      if (t >= n_tok) break;
+    }
+    const int v_lo = q * spu * 32 * COMBINE_UNROLL;
+    const int v_hi = min(vpr, (q + 1) * spu * 32 * COMBINE_UNROLL);
     int32_t my_row = -1;
     float my_g = 0.f;
     if (lane < k) {
@@ -78,18 +95,18 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_stats(
       }
     }
     // warp-uniform trip count: every lane reaches the shuffles below
-    for (int base = 0; base < vpr; base += 32 * COMBINE_UNROLL) {
+    for (int base = v_lo; base < v_hi; base += 32 * COMBINE_UNROLL) {
       float acc[COMBINE_UNROLL][N];
 #pragma unroll
       for (int u = 0; u < COMBINE_UNROLL; ++u) {
         const int v = base + lane + 32 * u;
-        if (v < vpr) Vec16<T>::unpack(ldg_stream(U + t * vpr + v), acc[u]);
+        if (v < v_hi) Vec16<T>::unpack(ldg_stream(U + t * vpr + v), acc[u]);
       }
       for (int sh = 0; sh < n_shared; ++sh) {
 #pragma unroll
         for (int u = 0; u < COMBINE_UNROLL; ++u) {
           const int v = base + lane + 32 * u;
-          if (v < vpr) {
+          if (v < v_hi) {
             float y[N];
             Vec16<T>::unpack(ldg_stream(Y_shared + (static_cast<int64_t>(sh) * n_tok + t) * vpr + v), y);
 #pragma unroll
@@ -104,7 +121,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_stats(
 #pragma unroll
         for (int u = 0; u < COMBINE_UNROLL; ++u) {
           const int v = base + lane + 32 * u;
-          if (v < vpr) {
+          if (v < v_hi) {
             float y[N];
             Vec16<T>::unpack(ldg_stream(Y + static_cast<int64_t>(r) * vpr + v), y);
 #pragma unroll
@@ -115,7 +132,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_stats(
 #pragma unroll
       for (int u = 0; u < COMBINE_UNROLL; ++u) {
         const int v = base + lane + 32 * u;
-        if (v < vpr) out[t * vpr + v] = Vec16<T>::pack(acc[u]);
+        if (v < v_hi) out[t * vpr + v] = Vec16<T>::pack(acc[u]);
       }
     }
   }
@@ -188,21 +205,29 @@ cudaError_t launch_combine(const Plan& p, const void* U, const void* Y, const vo
   int32_t* done = reinterpret_cast<int32_t*>(ws + p.ws_status + 128);
   float* part2 = reinterpret_cast<float*>(ws + p.ws_stats2);
   const int vpr = p.h * (p.bf16 ? 2 : 4) / 16;
-  const int64_t want = (p.T + 7) / 8;
+  // one warp per token, or per piece of a token row when the tokens are few (at most 8 blocks an SM)
+  const int pieces_per_row = (vpr + 32 * COMBINE_UNROLL - 1) / (32 * COMBINE_UNROLL);
+  const int64_t want = (p.T * pieces_per_row + 7) / 8;
   const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(current_sm_count()) * 8)));
   const int n_sh = Y_shared ? p.n_shared : 0;
   const uint4* ysh = static_cast<const uint4*>(Y_shared);
   const int groups = std::min(STAT_GROUPS, blocks);
+  // pieces of a row per warp task: the whole row unless that leaves warps idle
+  const int pieces = (vpr + 32 * COMBINE_UNROLL - 1) / (32 * COMBINE_UNROLL);
+  const int64_t total_warps = static_cast<int64_t>(blocks) * (COMBINE_THREADS / 32);
+  const int64_t want_tasks = total_warps * 2;
+  int spu = pieces;
+  while (spu > 1 && p.T * ((pieces + spu - 1) / spu) < want_tasks) spu = (spu + 1) / 2;
   if (p.bf16)
     combine_stats<bf16><<<blocks, COMBINE_THREADS, 0, s>>>(
         static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh, slot_row, gate,
         static_cast<uint4*>(out), p.T, p.k, vpr, p.Tk, status, ppart, ws_ppart_rows(p, ws), counts_routed, p.E, f, P,
-        aux, z_loss, done, part2, groups);
+        aux, z_loss, done, part2, groups, spu);
   else
     combine_stats<float><<<blocks, COMBINE_THREADS, 0, s>>>(
         static_cast<const uint4*>(U), static_cast<const uint4*>(Y), ysh, n_sh, slot_row, gate,
         static_cast<uint4*>(out), p.T, p.k, vpr, p.Tk, status, ppart, ws_ppart_rows(p, ws), counts_routed, p.E, f, P,
-        aux, z_loss, done, part2, groups);
+        aux, z_loss, done, part2, groups, spu);
   return cudaGetLastError();
 }
 

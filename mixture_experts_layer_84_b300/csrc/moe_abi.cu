@@ -202,9 +202,9 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     q.chunk = static_cast<int>(std::max<int64_t>(256, std::min<int64_t>(kDispatchChunk, c)));
   }
   q.n_chunks = static_cast<int>((Tk + q.chunk - 1) / q.chunk);
-  // choice-major dispatch: token chunks of 16 .. 256 tokens, about two per SM
+  // choice-major dispatch: token chunks of 8 .. 256 tokens, about two per SM
   {
-    int tc = 16;
+    int tc = 8;
     while (tc < 256 && static_cast<int64_t>(tc) * 2 * 148 < q.T) tc *= 2;
     q.dp_tc = tc;
     q.dp_chunks = static_cast<int>((q.T + tc - 1) / tc);

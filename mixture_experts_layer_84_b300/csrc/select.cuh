@@ -31,6 +31,27 @@ __device__ __forceinline__ bool before(float av, int ai, float bv, int bi) {
   return av > bv || (av == bv && ai < bi);
 }
 
+// 1 / (1 + e^-x) with a correctly rounded reciprocal (the same value as the IEEE division).
+__device__ __forceinline__ float sigmoid_f32(float x) { return __frcp_rn(1.f + __expf(-x)); }
+
+// (v, i) into the list (tv, ti), kept in `before` order, the last entry dropping out.  All KP
+// comparisons are made first and every entry then takes its new value independently (the entries
+// from the insertion point on shift down by one), so the dependency chain is a few instructions
+// long instead of KP compare-and-swaps.
+template <int KP>
+__device__ __forceinline__ void insert_sorted(float (&tv)[KP], int (&ti)[KP], float v, int i) {
+  bool gt[KP];
+#pragma unroll
+  for (int j = 0; j < KP; ++j) gt[j] = before(v, i, tv[j], ti[j]);
+#pragma unroll
+  for (int j = KP - 1; j > 0; --j) {
+    tv[j] = gt[j - 1] ? tv[j - 1] : (gt[j] ? v : tv[j]);
+    ti[j] = gt[j - 1] ? ti[j - 1] : (gt[j] ? i : ti[j]);
+  }
+  tv[0] = gt[0] ? v : tv[0];
+  ti[0] = gt[0] ? i : ti[0];
+}
+
 struct SelLayout {
   int C, CS, LD;
   __device__ __forceinline__ SelLayout(int E, int G) {
@@ -78,7 +99,7 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
       const float x = chunk[e - e0];
       const float ex = __expf(x - mx);
       sum_exp += ex;
-      denom += softmax ? ex : 1.f / (1.f + __expf(-x));
+      denom += softmax ? ex : sigmoid_f32(x);
     }
   }
 #pragma unroll
@@ -99,7 +120,7 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
         for (int j = 0; j < KP; ++j) best[j] = -INFINITY;
         for (int e = q * gsz; e < (q + 1) * gsz; ++e) {
           const float x = sx[L.at(r, e)];
-          float a = softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x));
+          float a = softmax ? __expf(x - mx) / denom : sigmoid_f32(x);
           if (sel_bias) a += sel_bias[e];
 #pragma unroll
           for (int j = 0; j < KP; ++j) {
@@ -144,23 +165,8 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
       }
       if (!((keep >> grp) & 1u)) continue;  // outside the kept groups (never without groups: grp = 0)
       const float x = chunk[e - e0];
-      const float key =
-          sel_bias ? (softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x))) + sel_bias[e] : x;
-      if (before(key, e, tv[KP - 1], ti[KP - 1])) {
-        float cv = key;
-        int ci = e;
-#pragma unroll
-        for (int j = 0; j < KP; ++j) {
-          if (before(cv, ci, tv[j], ti[j])) {
-            const float tvj = tv[j];
-            const int tij = ti[j];
-            tv[j] = cv;
-            ti[j] = ci;
-            cv = tvj;
-            ci = tij;
-          }
-        }
-      }
+      const float key = sel_bias ? (softmax ? __expf(x - mx) / denom : sigmoid_f32(x)) + sel_bias[e] : x;
+      if (before(key, e, tv[KP - 1], ti[KP - 1])) insert_sorted<KP>(tv, ti, key, e);
     }
   }
   // combine the G lanes' lists (consecutive lanes of one warp)
@@ -203,7 +209,7 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
       sel_s[j] = 0.f;
       if (j < k) {
         const float x = sx[L.at(r, ti[j])];
-        sel_s[j] = softmax ? __expf(x - mx) / denom : 1.f / (1.f + __expf(-x));
+        sel_s[j] = softmax ? __expf(x - mx) / denom : sigmoid_f32(x);
         sel_sum += sel_s[j];
       }
     }
@@ -221,7 +227,7 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
   if (tok) {
     for (int e = e0; e < e1; ++e) {
       const float x = chunk[e - e0];
-      chunk[e - e0] = (softmax ? __expf(x - mx) : 1.f / (1.f + __expf(-x))) / denom;
+      chunk[e - e0] = (softmax ? __expf(x - mx) : sigmoid_f32(x)) / denom;
     }
     if (g == 0) {
       const float lse = mx + logf(sum_exp);
