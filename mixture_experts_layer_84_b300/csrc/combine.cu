@@ -35,7 +35,7 @@ constexpr int STAT_GROUPS = 32;     // first-level slices of the statistics redu
 //   forms f_i from the routed counts and aux = E sum_i f_i P_i in expert order, and resets the
 //   count for the next call.  Every result is the same from run to run.
 template <typename T>
-__global__ void __launch_bounds__(COMBINE_THREADS, 5) combine_stats(
+__global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_stats(
     const uint4* __restrict__ U, const uint4* __restrict__ Y, const uint4* __restrict__ Y_shared, int n_shared,
     const int32_t* __restrict__ slot_row, const float* __restrict__ gate, uint4* __restrict__ out, int64_t n_tok,
     int k, int vpr, int64_t rows_cap, int32_t* status, const float* __restrict__ ppart,

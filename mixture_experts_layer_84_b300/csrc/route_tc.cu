@@ -313,7 +313,8 @@ struct Geometry {
 
 // Shared memory of the fused router: the TMA stages, reused after the main loop for the partial
 // tile P [128][N + 1] and the select staging (sx [TB][LD], zsq [TB], gsc [TB][n_group],
-// colsum [E + 1]), then the barriers, then the logit bias and the selection bias [E] each.
+// colsum [E + 1]), then the barriers, then the logit bias, the selection bias and each expert's
+// position in a staged row [E] each.
 // G = lanes per token of the selection.
 __host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stages, int G) {
   Geometry g;
@@ -329,7 +330,7 @@ __host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stag
   const size_t ring = static_cast<size_t>(stages) * g.stage_bytes;
   const size_t tail = g.p_bytes + sizeof(float) * static_cast<size_t>(g.sel_floats);
   g.work = ((ring > tail ? ring : tail) + 15) / 16 * 16;
-  g.smem = 1024 + g.work + RF_BAR_BYTES + 2 * sizeof(float) * static_cast<size_t>(E);  // + bias_s, selb_s
+  g.smem = 1024 + g.work + RF_BAR_BYTES + 3 * sizeof(float) * static_cast<size_t>(E);  // + bias_s, selb_s, pos_s
   return g;
 }
 
@@ -362,6 +363,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   float* colpart = colsum + (E + 1);                               // [THREADS] column-sum partials
   float* bias_s = reinterpret_cast<float*>(smem + geo.work + RF_BAR_BYTES);  // b_r (or zeros) [E]
   float* selb_s = bias_s + E;                                                  // sel_bias [E]
+  int* pos_s = reinterpret_cast<int*>(selb_s + E);                             // SelLayout::at(0, e) [E]
 
   const uint32_t tmem_cols = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
   const uint32_t STAGE = geo.stage_bytes;
@@ -445,9 +447,11 @@ __global__ void __launch_bounds__(THREADS, 2)
     // under the main loop: the biases into shared memory, and this CTA's rows of the noise into L2
     // (the epilogue reads them with all its loads in flight, but one CTA per SM has few warps)
     const int i0 = threadIdx.x - 64;
+    const SelLayout L(E, G);
     for (int e = i0; e < E; e += 64) {
       bias_s[e] = b_r ? b_r[e] : 0.f;
       selb_s[e] = sel_bias ? sel_bias[e] : 0.f;
+      pos_s[e] = L.at(0, e);
     }
     if (noisy && rows_here > 0) {
       const char* nb = reinterpret_cast<const char*>(eps + row0 * E);
@@ -491,70 +495,45 @@ __global__ void __launch_bounds__(THREADS, 2)
   const bool ok = !*abort_flag;
 
   // rows [rank R, (rank+1) R) of the tile: the CS slices summed in rank order from local shared
-  // memory, then bias and noise; the pass's rows x E entries in order, eight a thread at a time
-  // with their noise loads issued together
+  // memory, then bias and noise; the pass's rows x E entries in order, RB a thread at a time with
+  // their noise loads issued together.  The loop is kept compact (it runs once per CTA, from a cold
+  // instruction cache): (row, expert) advance by additions, the staged position comes from pos_s.
   if (ok) {
-    constexpr int RB = 8;
+    constexpr int RB = 4;
+    const int dr = THREADS / E, de = THREADS - (THREADS / E) * E;
     for (int p0 = 0; p0 < rows_here; p0 += geo.TB) {
       const int rows = min(geo.TB, rows_here - p0);
-      const SelLayout L(E, G);
       const int n_el = rows * E;
       const float* eps_p = noisy ? eps + (row0 + p0) * E : nullptr;
       float* lo_p = logits_out ? logits_out + (row0 + p0) * E : nullptr;
-      if (THREADS % E == 0) {
-        // every thread keeps one expert e and steps over the rows: no division per entry
-        const int e = static_cast<int>(threadIdx.x) % E, rstep = THREADS / E;
-        const int pos = L.at(0, e);
-        const float be = bias_s[e];
-        for (int r0 = static_cast<int>(threadIdx.x) / E; r0 < rows; r0 += RB * rstep) {
-          float ev[RB];
+      const SelLayout L(E, G);
+      int r = static_cast<int>(threadIdx.x) / E;
+      int e = static_cast<int>(threadIdx.x) - r * E;
+#pragma unroll 1
+      for (int i = threadIdx.x; i < n_el; i += RB * THREADS) {
+        float ev[RB];
 #pragma unroll
-          for (int u = 0; u < RB; ++u) {
-            const int r = r0 + u * rstep;
-            ev[u] = (noisy && r < rows) ? eps_p[static_cast<int64_t>(r) * E + e] : 0.f;
-          }
+        for (int u = 0; u < RB; ++u) ev[u] = (noisy && i + u * THREADS < n_el) ? eps_p[i + u * THREADS] : 0.f;
 #pragma unroll
-          for (int u = 0; u < RB; ++u) {
-            const int r = r0 + u * rstep;
-            if (r < rows) {
-              const float* qr = Q + (p0 + r) * geo.PN + e;
-              float x = 0.f, z = 0.f;
-              for (int c = 0; c < cs; ++c) {
-                x += qr[c * R * geo.PN];
-                if (noisy) z += qr[c * R * geo.PN + E];
-              }
-              if (b_r) x += be;
-              if (noisy) x = fmaf(ev[u], softplus_f32(z), x);
-              if (lo_p) lo_p[static_cast<int64_t>(r) * E + e] = x;
-              sx[r * L.LD + pos] = x;
+        for (int u = 0; u < RB; ++u) {
+          if (i + u * THREADS < n_el) {
+            const float* qr = Q + (p0 + r) * geo.PN + e;
+            float x = 0.f, z = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < cs; ++c) {
+              x += qr[c * R * geo.PN];
+              if (noisy) z += qr[c * R * geo.PN + E];
             }
+            if (b_r) x += bias_s[e];
+            if (noisy) x = fmaf(ev[u], softplus_f32(z), x);
+            if (lo_p) lo_p[i + u * THREADS] = x;
+            sx[r * L.LD + pos_s[e]] = x;
           }
-        }
-      } else {
-        for (int b = 0; b < n_el; b += RB * THREADS) {
-          float ev[RB];
-#pragma unroll
-          for (int u = 0; u < RB; ++u) {
-            const int i = b + u * THREADS + static_cast<int>(threadIdx.x);
-            ev[u] = (noisy && i < n_el) ? eps_p[i] : 0.f;
-          }
-#pragma unroll
-          for (int u = 0; u < RB; ++u) {
-            const int i = b + u * THREADS + static_cast<int>(threadIdx.x);
-            if (i < n_el) {
-              const int r = i / E, e = i - r * E;
-              const int li = p0 + r;
-              float x = 0.f, z = 0.f;
-              for (int c = 0; c < cs; ++c) {
-                const float* qr = Q + (c * R + li) * geo.PN;
-                x += qr[e];
-                if (noisy) z += qr[E + e];
-              }
-              if (b_r) x += bias_s[e];
-              if (noisy) x = fmaf(ev[u], softplus_f32(z), x);
-              if (lo_p) lo_p[i] = x;
-              sx[L.at(r, e)] = x;
-            }
+          r += dr;
+          e += de;
+          if (e >= E) {
+            e -= E;
+            ++r;
           }
         }
       }
