@@ -21,6 +21,10 @@ EDGE = [
                renorm=True, noisy=False, capacity_factor=0.0),
     W.Workload("ffn_tails_f32", T=123, h=72, E=5, k=2, d_e=40, dtype=W.F32, score_fn=W.SOFTMAX, renorm=True,
                noisy=False, capacity_factor=0.0),
+    # segments longer than the weights (~1000 rows against 2 x 72 gate|up and 192 down rows): both
+    # GEMMs take column tiles fastest, with ragged row, column and K tails
+    W.Workload("ffn_long_segments_bf16", T=1500, h=192, E=3, k=2, d_e=72, dtype=W.BF16, score_fn=W.SOFTMAX,
+               renorm=True, noisy=False, capacity_factor=0.0),
 ]
 
 
