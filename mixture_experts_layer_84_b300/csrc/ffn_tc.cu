@@ -229,8 +229,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::prefetch_tmap(&tmB0);
       ptx::prefetch_tmap(&tmB1);
     }
-    const uint64_t pol_a = ptx::policy_evict_last();
-    const uint64_t pol_b = ptx::policy_evict_normal();
+    // the operand that later tiles read again is kept in L2 (A across column tiles, or B across row tiles)
+    const uint64_t pol_a = cols_fastest ? ptx::policy_evict_normal() : ptx::policy_evict_last();
+    const uint64_t pol_b = cols_fastest ? ptx::policy_evict_last() : ptx::policy_evict_normal();
     const int64_t a_total = seg_hi(offsets, E - 1, rows_cap);
     uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
@@ -271,8 +272,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB0);
       if (SWIGLU) ptx::prefetch_tmap(&tmB1);
-      const uint64_t pol_a = ptx::policy_evict_last();
-      const uint64_t pol_b = ptx::policy_evict_normal();
+      // the operand that later tiles read again is kept in L2 (A across column tiles, or B across row tiles)
+      const uint64_t pol_a = cols_fastest ? ptx::policy_evict_normal() : ptx::policy_evict_last();
+      const uint64_t pol_b = cols_fastest ? ptx::policy_evict_last() : ptx::policy_evict_normal();
       uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -552,8 +554,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(tmB);
     }
-    const uint64_t pol_a = ptx::policy_evict_last();
-    const uint64_t pol_b = ptx::policy_evict_normal();
+    // the operand that later tiles read again is kept in L2 (A across column tiles, or B across row tiles)
+    const uint64_t pol_a = cols_fastest ? ptx::policy_evict_normal() : ptx::policy_evict_last();
+    const uint64_t pol_b = cols_fastest ? ptx::policy_evict_last() : ptx::policy_evict_normal();
     const int64_t a_total = seg_hi(offsets, E - 1, rows_cap);
     uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
@@ -606,8 +609,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       ptx::prefetch_tmap(&tmB0);
       if (SWIGLU) ptx::prefetch_tmap(&tmB1);
       const CUtensorMap* tmB = (SWIGLU && !even) ? &tmB1 : &tmB0;
-      const uint64_t pol_a = ptx::policy_evict_last();
-      const uint64_t pol_b = ptx::policy_evict_normal();
+      // the operand that later tiles read again is kept in L2 (A across column tiles, or B across row tiles)
+      const uint64_t pol_a = cols_fastest ? ptx::policy_evict_normal() : ptx::policy_evict_last();
+      const uint64_t pol_b = cols_fastest ? ptx::policy_evict_last() : ptx::policy_evict_normal();
       uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < total; tile += ncl) {
@@ -1293,9 +1297,14 @@ cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, 
   // tile order: the operand re-read per tile of the other is the smaller one of an expert (its mean
   // rows of A against its rows of B, both K wide): on the stress shape the 6144-row segments of X
   // are 50 MB against 23 MB of gate|up weights, and were read from HBM about 2.5 times
+  // (MOE_FFN_ORDER=rows|cols overrides the choice for both GEMMs, for measurement and tests)
   const int64_t a_rows = p.Tk / p.E;
-  const int order1 = a_rows > 2 * static_cast<int64_t>(p.d_e) ? 1 : 0;
-  const int order2 = a_rows > static_cast<int64_t>(p.h) ? 1 : 0;
+  int order1 = a_rows > 2 * static_cast<int64_t>(p.d_e) ? 1 : 0;
+  int order2 = a_rows > static_cast<int64_t>(p.h) ? 1 : 0;
+  if (const char* env = getenv("MOE_FFN_ORDER")) {
+    if (strcmp(env, "rows") == 0) order1 = order2 = 0;
+    if (strcmp(env, "cols") == 0) order1 = order2 = 1;
+  }
   cudaError_t e =
       gather ? launch_gemm<true, true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
                                        static_cast<bf16*>(act), status, s,

@@ -37,12 +37,14 @@ def segments(w, seed, zipf):
 @pytest.mark.parametrize("tiles", ["single", "pair", "swab"])
 @pytest.mark.parametrize("w", W.SMALL + EDGE, ids=lambda w: w.name)
 @pytest.mark.parametrize("zipf", [0.0, 1.2])
-def test_expert_ffn(w, zipf, tiles, monkeypatch):
+def test_expert_ffn(w, zipf, tiles, monkeypatch, order=None):
     """The three bf16 kernels (128-row tiles on one CTA, 256-row tiles on a CTA pair, and weight
     rows as M with tokens as N on a CTA pair) against the oracle."""
     if w.dtype == W.F32 and tiles != "single":
         pytest.skip("float32 runs on the CUDA cores")
     monkeypatch.setenv("MOE_FFN_TILES", tiles)
+    if order:
+        monkeypatch.setenv("MOE_FFN_ORDER", order)
     inp = synth.generate(w, seed=2, device="cuda")
     d = segments(w, seed=9, zipf=zipf)
     A = int(d["offsets"][-1])
@@ -67,6 +69,15 @@ def test_expert_ffn(w, zipf, tiles, monkeypatch):
             assert normwise(Y[lo:hi], Y_ref[lo:hi]) <= tol, e
     # rows >= A are not written
     assert torch.all(Y[A:] == 7.0) and torch.all(act[A:] == 7.0)
+
+
+@pytest.mark.parametrize("order", ["rows", "cols"])
+@pytest.mark.parametrize("tiles", ["single", "pair"])
+@pytest.mark.parametrize("w", [EDGE[0], EDGE[-1]], ids=lambda w: w.name)
+def test_expert_ffn_tile_orders(w, tiles, order, monkeypatch):
+    """Both tile orders (row tiles or column tiles fastest inside an expert) on both row-tiled
+    kernels, with ragged row, column and K tails."""
+    test_expert_ffn(w, 1.2, tiles, monkeypatch, order=order)
 
 
 @pytest.mark.parametrize("dtype,tiles", [(W.BF16, "single"), (W.BF16, "pair"), (W.BF16, "swab"), (W.F32, "single")])
