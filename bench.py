@@ -183,8 +183,8 @@ def stage_work(w: W.Workload, A: float, n_active: float, fp8: bool = False, gath
     return work
 
 
-def launches_per_step(w: W.Workload, gather: bool = False) -> int:
-    """Kernels libmoe launches for one moe_layer_forward of this workload."""
+def launches_per_step(w: W.Workload, gather: bool = False, fp8: bool = False) -> int:
+    """Kernels libmoe launches for one moe_layer_forward (moe_layer_forward_fp8) of this workload."""
     if w.T == 0:
         return 2  # dispatch scan + statistics
     fused_router = w.dtype == W.BF16 and (2 * w.E if w.noisy else w.E) <= 256
@@ -193,6 +193,8 @@ def launches_per_step(w: W.Workload, gather: bool = False) -> int:
         dispatch = 3                       # histograms, column scans, then slots + row copy (no copy when gathering)
     else:
         dispatch = 3 if gather else 4      # count, scan, assign (, scatter)
+    if fp8:
+        dispatch = 3 + 1                   # the metadata only (no bf16 copy), then the E4M3 row copy
     ffn, combine = 2, 1                    # two GEMMs; rows and statistics
     return route + dispatch + ffn + 2 * w.n_shared + combine
 
@@ -856,7 +858,7 @@ def run_b300(args, w: W.Workload):
                     "d2h_bytes_per_step": w.T * w.h * w.elem_bytes + 4,
                     "how": f"moe_layer_forward{'_fp8' if fp8 else ''} per step with its U copied in from pinned host memory and out + aux "
                            "copied back; copy-in, layer and copy-out of consecutive steps overlap on three streams"},
-            "gpu_launches": launches_per_step(w, run.gather) * K,
+            "gpu_launches": launches_per_step(w, run.gather, run.fp8) * K,
             "launch": "one CUDA graph replay per step (the whole layer)" if run.graphs else
                       ("eager stage calls" + (f" (graph capture failed: {run.graph_error})" if run.graph_error else "")),
             "clocks": clk}

@@ -51,6 +51,8 @@ def test_launches_per_step(w, expected):
         tm = w.replace(priority=W.PRIORITY_TOKEN_MAJOR)
         assert bench.launches_per_step(tm) == expected + 1
         assert bench.launches_per_step(tm, gather=True) == expected
+        assert bench.launches_per_step(w, fp8=True) == expected + 1
+        assert bench.launches_per_step(tm, fp8=True) == expected + 1
 
 
 def test_ffn_tiles_rule(monkeypatch):
