@@ -57,6 +57,7 @@ struct Plan {
   int rf_tiles = 0;        // its 128-token tiles
   int rf_cs = 0;           // CTAs per tile (a cluster), each with a slice of h
   int rf_stages = 0;       // its TMA ring depth
+  int rf_threads = 256;    // threads a CTA: 512 when one CTA fills an SM anyway (more warps to select)
   int sel_threads = 0;     // threads per select block (G lanes per token)
   int sel_tokens = 0;      // tokens per select block
   int sel_blocks = 0;      // ceil(T / sel_tokens): number of P partial rows
@@ -92,7 +93,7 @@ cudaError_t launch_route_fused(const Plan& p, const void* U, const void* Wt, con
                                const float* eps, float* logits_out, int32_t* idx, float* gate, uint8_t* ws,
                                cudaStream_t s);
 // Dynamic shared memory of one fused-router CTA.
-size_t fused_router_smem(int N, int E, int n_group, int stages);
+size_t fused_router_smem(int N, int E, int n_group, int stages, int threads);
 
 // Router slice sums U W_r (and U W_noise) on the tensor cores (bf16, p.route_tc_n > 0).
 cudaError_t launch_route_logits_tc(const Plan& p, const void* U, const void* W_r, const void* W_noise, float* part,

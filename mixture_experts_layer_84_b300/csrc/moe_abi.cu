@@ -183,6 +183,9 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     // GPC each do not all fit at once (measured: 28 vs 16 us on the Mixtral router)
     const int stage_kb = 16 + q.route_tc_n * 128 / 1024;
     q.rf_stages = static_cast<int64_t>(q.rf_tiles) * cs > 148 ? 4 : std::max(4, std::min(8, 100 / stage_kb));
+    // one wave whose four-stage ring already fills an SM (N > 96: the 256-expert and the noisy
+    // 128-expert routers): 512 threads, so that the epilogue has 16 warps to hide its latencies
+    q.rf_threads = static_cast<int64_t>(q.rf_tiles) * cs <= 148 && 4 * stage_kb > 113 ? 512 : 256;
   }
   // selection blocks: 256 threads, fewer (down to a warp) when T is small, so that the
   // blocks still spread over about twice the SMs

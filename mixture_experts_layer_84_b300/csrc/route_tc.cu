@@ -301,7 +301,8 @@ namespace rfu {
 
 using namespace rtc;
 
-constexpr int THREADS = 256;  // warp 0 TMA, warp 1 MMA, warps 4-7 accumulator readout; all 8 select
+// NTH = 256 or 512 threads: warp 0 TMA, warp 1 MMA, warps 2-3 stage the biases, warps 4-7 read the
+// accumulator out; every warp reduces and selects
 constexpr int MAX_STAGES = 8;
 constexpr size_t RF_BAR_BYTES = 256;  // full[8], empty[8], tfull, tensor-memory address, abort flag
 
@@ -316,17 +317,17 @@ struct Geometry {
 // colsum [E + 1]), then the barriers, then the logit bias, the selection bias and each expert's
 // position in a staged row [E] each.
 // G = lanes per token of the selection.
-__host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stages, int G) {
+__host__ __device__ inline Geometry geometry(int N, int E, int n_group, int stages, int G, int threads) {
   Geometry g;
   g.N = N;
   g.stages = stages;
   g.stage_bytes = A_BYTES + b_bytes(N);
   g.PN = N + 4;  // 16-byte rows for the remote vector stores
-  g.TB = THREADS / G;
+  g.TB = threads / G;
   const int C = (E + G - 1) / G;
   g.LD = G * ((C & 1) ? C + 2 : C + 1);
   g.p_bytes = sizeof(float) * 128 * static_cast<size_t>(g.PN);
-  g.sel_floats = g.TB * g.LD + g.TB + g.TB * (n_group > 1 ? n_group : 0) + (E + 1) + THREADS;
+  g.sel_floats = g.TB * g.LD + g.TB + g.TB * (n_group > 1 ? n_group : 0) + (E + 1) + threads;
   const size_t ring = static_cast<size_t>(stages) * g.stage_bytes;
   const size_t tail = g.p_bytes + sizeof(float) * static_cast<size_t>(g.sel_floats);
   g.work = ((ring > tail ? ring : tail) + 15) / 16 * 16;
@@ -340,8 +341,8 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                : "memory");
 }
 
-template <int KP, int G>
-__global__ void __launch_bounds__(THREADS, 2)
+template <int KP, int G, int NTH>
+__global__ void __launch_bounds__(NTH, NTH == 512 ? 1 : 2)
     route_fused(const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmW, int64_t T, int h,
                 int E, int N, int stages, int cs, const float* __restrict__ b_r, const float* __restrict__ sel_bias,
                 const float* __restrict__ eps, int noisy, float* __restrict__ logits_out, int32_t* __restrict__ idx,
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                 int score_fn, int renorm, int n_group, int topk_group, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Geometry geo = geometry(N, E, n_group, stages, G);
+  const Geometry geo = geometry(N, E, n_group, stages, G, NTH);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + geo.work);
   uint64_t* empty = full + MAX_STAGES;
   uint64_t* tfull = empty + 8;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   float* zsq = sx + geo.TB * geo.LD;
   float* gsc = zsq + geo.TB;
   float* colsum = gsc + geo.TB * (n_group > 1 ? n_group : 0);
-  float* colpart = colsum + (E + 1);                               // [THREADS] column-sum partials
+  float* colpart = colsum + (E + 1);                               // [NTH] column-sum partials
   float* bias_s = reinterpret_cast<float*>(smem + geo.work + RF_BAR_BYTES);  // b_r (or zeros) [E]
   float* selb_s = bias_s + E;                                                  // sel_bias [E]
   int* pos_s = reinterpret_cast<int*>(selb_s + E);                             // SelLayout::at(0, e) [E]
@@ -461,14 +462,15 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   // the accumulator is complete (or the pipeline gave up); every CTA of the cluster must be past its
   // main loop before any partial row lands in a peer's shared memory (which held its TMA stages)
+  const bool readout = warp >= 4 && warp < 8;
   bool ready = true;
-  if (warp >= 4) ready = __all_sync(0xffffffffu, wait_drain(tfull, 0));
-  if (warp >= 4 && !ready) *abort_flag = 1;
+  if (readout) ready = __all_sync(0xffffffffu, wait_drain(tfull, 0));
+  if (readout && !ready) *abort_flag = 1;
   __syncthreads();
   ptx::cluster_sync_all();
   // partial rows to their owners: tile row i belongs to cluster CTA i / R, which keeps slot
   // [rank][i % R] of Q [cs][R][PN] for it (16-byte remote stores)
-  if (warp >= 4 && !*abort_flag) {
+  if (readout && !*abort_flag) {
     const int q = warp & 3;
     const int i = q * 32 + lane;
     const int owner = i / R, li = i - owner * R;
@@ -500,7 +502,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   // instruction cache): (row, expert) advance by additions, the staged position comes from pos_s.
   if (ok) {
     constexpr int RB = 4;
-    const int dr = THREADS / E, de = THREADS - (THREADS / E) * E;
+    const int dr = NTH / E, de = NTH - (NTH / E) * E;
     for (int p0 = 0; p0 < rows_here; p0 += geo.TB) {
       const int rows = min(geo.TB, rows_here - p0);
       const int n_el = rows * E;
@@ -510,13 +512,13 @@ __global__ void __launch_bounds__(THREADS, 2)
       int r = static_cast<int>(threadIdx.x) / E;
       int e = static_cast<int>(threadIdx.x) - r * E;
 #pragma unroll 1
-      for (int i = threadIdx.x; i < n_el; i += RB * THREADS) {
+      for (int i = threadIdx.x; i < n_el; i += RB * NTH) {
         float ev[RB];
 #pragma unroll
-        for (int u = 0; u < RB; ++u) ev[u] = (noisy && i + u * THREADS < n_el) ? eps_p[i + u * THREADS] : 0.f;
+        for (int u = 0; u < RB; ++u) ev[u] = (noisy && i + u * NTH < n_el) ? eps_p[i + u * NTH] : 0.f;
 #pragma unroll
         for (int u = 0; u < RB; ++u) {
-          if (i + u * THREADS < n_el) {
+          if (i + u * NTH < n_el) {
             const float* qr = Q + (p0 + r) * geo.PN + e;
             float x = 0.f, z = 0.f;
 #pragma unroll 1
@@ -526,7 +528,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             }
             if (b_r) x += bias_s[e];
             if (noisy) x = fmaf(ev[u], softplus_f32(z), x);
-            if (lo_p) lo_p[i + u * THREADS] = x;
+            if (lo_p) lo_p[i + u * NTH] = x;
             sx[r * L.LD + pos_s[e]] = x;
           }
           r += dr;
@@ -545,25 +547,25 @@ __global__ void __launch_bounds__(THREADS, 2)
       __syncthreads();
     }
     if (rows_here == 0)
-      for (int e = threadIdx.x; e <= E; e += THREADS) colsum[e] = 0.f;
+      for (int e = threadIdx.x; e <= E; e += NTH) colsum[e] = 0.f;
     __syncthreads();
-    for (int e = threadIdx.x; e <= E; e += THREADS) ppart[static_cast<int64_t>(blockIdx.x) * (E + 1) + e] = colsum[e];
+    for (int e = threadIdx.x; e <= E; e += NTH) ppart[static_cast<int64_t>(blockIdx.x) * (E + 1) + e] = colsum[e];
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) *ppart_rows = static_cast<int32_t>(gridDim.x);
   if (threadIdx.x == 0 && !ok) set_status(status, MOE_DEV_TIMEOUT);
 }
 
-template <int KP, int G>
+template <int KP, int G, int NTH>
 cudaError_t launch_fused_g(const Plan& p, const CUtensorMap& tmU, const CUtensorMap& tmW, const float* b_r,
                            const float* sel_bias, const float* eps, float* logits_out, int32_t* idx, float* gate,
                            float* ppart, int32_t* rows, int32_t* status, cudaStream_t s) {
-  const Geometry geo = geometry(p.route_tc_n, p.E, p.n_group, p.rf_stages, G);
-  auto kern = route_fused<KP, G>;
+  const Geometry geo = geometry(p.route_tc_n, p.E, p.n_group, p.rf_stages, G, NTH);
+  auto kern = route_fused<KP, G, NTH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(geo.smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(static_cast<unsigned>(p.rf_tiles * p.rf_cs));
-  lc.blockDim = dim3(THREADS);
+  lc.blockDim = dim3(NTH);
   lc.dynamicSmemBytes = geo.smem;
   lc.stream = s;
   cudaLaunchAttribute at[1];
@@ -582,9 +584,19 @@ template <int KP>
 cudaError_t launch_fused_kp(const Plan& p, const CUtensorMap& tmU, const CUtensorMap& tmW, const float* b_r,
                             const float* sel_bias, const float* eps, float* logits_out, int32_t* idx, float* gate,
                             float* ppart, int32_t* rows, int32_t* status, cudaStream_t s) {
+  // 512 threads: twice the lanes per token (half the experts per lane) for the same tokens a pass
+  if (p.rf_threads == 512) {
+    switch (select_lanes_for(p.E)) {
+#define MOE_RFU_G2(gg, g2) \
+  case gg: return launch_fused_g<KP, g2, 512>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
+      MOE_RFU_G2(1, 2) MOE_RFU_G2(2, 4) MOE_RFU_G2(4, 8) MOE_RFU_G2(8, 16)
+#undef MOE_RFU_G2
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (select_lanes_for(p.E)) {
 #define MOE_RFU_G(gg) \
-  case gg: return launch_fused_g<KP, gg>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
+  case gg: return launch_fused_g<KP, gg, 256>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
     MOE_RFU_G(1) MOE_RFU_G(2) MOE_RFU_G(4) MOE_RFU_G(8)
 #undef MOE_RFU_G
   }
@@ -593,8 +605,9 @@ cudaError_t launch_fused_kp(const Plan& p, const CUtensorMap& tmU, const CUtenso
 
 }  // namespace rfu
 
-size_t fused_router_smem(int N, int E, int n_group, int stages) {
-  return rfu::geometry(N, E, n_group, stages, select_lanes_for(E)).smem;
+size_t fused_router_smem(int N, int E, int n_group, int stages, int threads) {
+  const int G = select_lanes_for(E);
+  return rfu::geometry(N, E, n_group, stages, threads == 512 && G < 32 ? 2 * G : G, threads).smem;
 }
 
 cudaError_t launch_pack_router(const Plan& p, const void* W_r, const void* W_noise, void* Wt, cudaStream_t s) {

@@ -1,6 +1,7 @@
 """The fused tensor-core router (bf16, E or 2E <= 256 logit columns) against the oracle, on shapes
-chosen to reach every cluster size (1, 2, 4, 8 CTAs per 128-token tile), ragged last tiles (CTAs of a
-cluster with no rows), h not a multiple of 64, several selection passes per CTA, the noisy router,
+chosen to reach every cluster size (1, 2, 4, 8 CTAs per 128-token tile), both CTA sizes (256 threads,
+and 512 when one CTA fills an SM), ragged last tiles (CTAs of a cluster with no rows), h not a
+multiple of 64, several selection passes per CTA, the noisy router,
 group-limited routing with a selection bias, k = 16; and the router from weights packed once
 (moe_pack_router) against the one that packs them on each call, bit for bit."""
 import numpy as np
@@ -30,6 +31,8 @@ FUSED = [
     _w("cs4_e256_k16", 300, 512, 256, 16, SG),
     _w("e5_narrow", 260, 640, 5, 2, SM, bias="normal"),
     _w("noisy_e128_two_passes", 700, 320, 128, 1, SM, renorm=False, noisy=True, bias="zipf"),
+    # more CTAs than SMs: the 256-thread kernel, 128 rows in two passes of 64 tokens
+    _w("e128_many_tiles_256_threads", 19200, 128, 128, 2, SM),
 ]
 
 
