@@ -462,9 +462,7 @@ __global__ void __launch_bounds__(NTH, NTH == 512 ? 1 : 2)
   }
   // the accumulator is complete (or the pipeline gave up); every CTA of the cluster must be past its
   // main loop before any partial row lands in a peer's shared memory (which held its TMA stages)
-  // accumulator readout: warps 4-7 (each its quadrant of TMEM lanes); with 512 threads warps 8-11
-  // read the same lanes' upper half of the columns
-  const bool readout = warp >= 4 && warp < (NTH == 512 ? 12 : 8);
+  const bool readout = warp >= 4 && warp < 8;
   bool ready = true;
   if (readout) ready = __all_sync(0xffffffffu, wait_drain(tfull, 0));
   if (readout && !ready) *abort_flag = 1;
@@ -479,10 +477,8 @@ __global__ void __launch_bounds__(NTH, NTH == 512 ? 1 : 2)
     const uint32_t dst = ptx::mapa_shared(ptx::smem_u32(Q + (rank * R + li) * geo.PN), static_cast<uint32_t>(owner));
     ptx::tc_fence_after();
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    const int half = NTH == 512 ? (N / 2 + 31) / 32 * 32 : N;
-    const int c_begin = warp >= 8 ? half : 0, c_end = warp < 8 ? half : N;
 #pragma unroll 1
-    for (int c = c_begin; c < c_end; c += 32) {
+    for (int c = 0; c < N; c += 32) {
       uint32_t v[32];
       ptx::tmem_ld_32x32b_x32(tb + c, v);
       ptx::tmem_wait_ld();
