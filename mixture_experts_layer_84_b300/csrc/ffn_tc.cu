@@ -84,6 +84,18 @@ __device__ __forceinline__ void decode_tile(const int* tab, int E, int NT, int t
   }
 }
 
+// L2 hints of the two operands for tile schedule `sched` (bit 0: column tiles fastest; bits 1-2: 0 keeps
+// the operand that later tiles read again (evict_last), 1 gives no hint, 2 also marks the operand
+// read once evict_first)
+__device__ __forceinline__ void l2_policies(int sched, uint64_t* pol_a, uint64_t* pol_b) {
+  const bool cols = sched & 1;
+  const int mode = (sched >> 1) & 3;
+  const uint64_t keep = mode == 0 ? ptx::policy_evict_last() : ptx::policy_evict_normal();
+  const uint64_t once = mode == 2 ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+  *pol_a = cols ? once : keep;
+  *pol_b = cols ? keep : once;
+}
+
 // Wait without regard to the abort flag (drains in-flight work before exit).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -154,7 +166,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets, int E, int K,
                     int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status,
                     const float* __restrict__ a_scale = nullptr, const float* __restrict__ b0_scale = nullptr,
-                    const float* __restrict__ b1_scale = nullptr, Gather g = Gather{}, int cols_fastest = 0) {
+                    const float* __restrict__ b1_scale = nullptr, Gather g = Gather{}, int sched = 0) {
   static_assert(SWIGLU || !FP8, "the FP8 path is the up-projection");
   static_assert(!(GATHER && (FP8 || !SWIGLU)), "the gathered A operand is the bf16 up-projection's");
   constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
@@ -229,15 +241,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::prefetch_tmap(&tmB0);
       ptx::prefetch_tmap(&tmB1);
     }
-    // the operand that later tiles read again is kept in L2 (A across column tiles, or B across row tiles)
-    const uint64_t pol_a = cols_fastest ? ptx::policy_evict_normal() : ptx::policy_evict_last();
-    const uint64_t pol_b = cols_fastest ? ptx::policy_evict_last() : ptx::policy_evict_normal();
+    uint64_t pol_a, pol_b;  // the operand that later tiles read again is kept in L2
+    l2_policies(sched, &pol_a, &pol_b);
     const int64_t a_total = seg_hi(offsets, E - 1, rows_cap);
     uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       int e, nt, mt;
-      decode_tile(tab, E, NT, tile, &e, &nt, &mt, cols_fastest);
+      decode_tile(tab, E, NT, tile, &e, &nt, &mt, sched & 1);
       const int4 rows = gather_rows4(g, static_cast<int64_t>(seg_lo(offsets, e)) + mt * BM + 4 * lane, a_total, status);
       const int b_row = e * b_rows_per_expert + nt * TILE_N;
       for (int kb = 0; kb < KB; ++kb) {
@@ -272,14 +283,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB0);
       if (SWIGLU) ptx::prefetch_tmap(&tmB1);
-      // the operand that later tiles read again is kept in L2 (A across column tiles, or B across row tiles)
-      const uint64_t pol_a = cols_fastest ? ptx::policy_evict_normal() : ptx::policy_evict_last();
-      const uint64_t pol_b = cols_fastest ? ptx::policy_evict_last() : ptx::policy_evict_normal();
+      uint64_t pol_a, pol_b;  // the operand that later tiles read again is kept in L2
+      l2_policies(sched, &pol_a, &pol_b);
       uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
         int e, nt, mt;
-        decode_tile(tab, E, NT, tile, &e, &nt, &mt, cols_fastest);
+        decode_tile(tab, E, NT, tile, &e, &nt, &mt, sched & 1);
         const int a_row = seg_lo(offsets, e) + mt * BM;
         const int b_row = e * b_rows_per_expert + nt * TILE_N;
         for (int kb = 0; kb < KB; ++kb) {
@@ -360,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, nt, mt;
-      decode_tile(tab, E, NT, tile, &e, &nt, &mt, cols_fastest);
+      decode_tile(tab, E, NT, tile, &e, &nt, &mt, sched & 1);
       const int seg = seg_lo(offsets, e);
       const int n_e = seg_hi(offsets, e, rows_cap) - seg;
       const bool row_ok = mt * BM + r_local < n_e;
@@ -476,7 +486,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                          const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
                          const int32_t* __restrict__ offsets, int E, int K,
                          int b_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out,
-                         int32_t* status, Gather g = Gather{}, int cols_fastest = 0) {
+                         int32_t* status, Gather g = Gather{}, int sched = 0) {
   static_assert(SWIGLU || !GATHER, "the gathered A operand is the up-projection's");
   constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
@@ -554,15 +564,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(tmB);
     }
-    // the operand that later tiles read again is kept in L2 (A across column tiles, or B across row tiles)
-    const uint64_t pol_a = cols_fastest ? ptx::policy_evict_normal() : ptx::policy_evict_last();
-    const uint64_t pol_b = cols_fastest ? ptx::policy_evict_last() : ptx::policy_evict_normal();
+    uint64_t pol_a, pol_b;  // the operand that later tiles read again is kept in L2
+    l2_policies(sched, &pol_a, &pol_b);
     const int64_t a_total = seg_hi(offsets, E - 1, rows_cap);
     uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
     bool ok = true;
     for (int tile = cid; ok && tile < total; tile += ncl) {
       int e, nt, mt;
-      decode_tile(tab, E, NT, tile, &e, &nt, &mt, cols_fastest);
+      decode_tile(tab, E, NT, tile, &e, &nt, &mt, sched & 1);
       const int4 rows = gather_rows4(
           g, static_cast<int64_t>(seg_lo(offsets, e)) + mt * P_BM + static_cast<int>(rank) * 128 + 4 * lane, a_total,
           status);
@@ -609,14 +618,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       ptx::prefetch_tmap(&tmB0);
       if (SWIGLU) ptx::prefetch_tmap(&tmB1);
       const CUtensorMap* tmB = (SWIGLU && !even) ? &tmB1 : &tmB0;
-      // the operand that later tiles read again is kept in L2 (A across column tiles, or B across row tiles)
-      const uint64_t pol_a = cols_fastest ? ptx::policy_evict_normal() : ptx::policy_evict_last();
-      const uint64_t pol_b = cols_fastest ? ptx::policy_evict_last() : ptx::policy_evict_normal();
+      uint64_t pol_a, pol_b;  // the operand that later tiles read again is kept in L2
+      l2_policies(sched, &pol_a, &pol_b);
       uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
       for (int tile = cid; ok && tile < total; tile += ncl) {
         int e, nt, mt;
-        decode_tile(tab, E, NT, tile, &e, &nt, &mt, cols_fastest);
+        decode_tile(tab, E, NT, tile, &e, &nt, &mt, sched & 1);
         const int a_row = seg_lo(offsets, e) + mt * P_BM + static_cast<int>(rank) * 128;
         const int b_row = SWIGLU ? e * b_rows_per_expert + nt * TILE_N
                                  : e * b_rows_per_expert + nt * TILE_N + static_cast<int>(rank) * 128;
@@ -698,7 +706,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = cid; tile < total; tile += ncl) {
       int e, nt, mt;
-      decode_tile(tab, E, NT, tile, &e, &nt, &mt, cols_fastest);
+      decode_tile(tab, E, NT, tile, &e, &nt, &mt, sched & 1);
       const int seg = seg_lo(offsets, e);
       const int n_e = seg_hi(offsets, e, rows_cap) - seg;
       const bool row_ok = mt * P_BM + r_local < n_e;
@@ -1213,7 +1221,7 @@ static cudaError_t launch_ffn_swab(const Plan& p, const void* X, const int32_t* 
 template <bool SWIGLU, bool GATHER = false>
 static cudaError_t launch_gemm(bool pair, int grid, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                                const int32_t* offsets, int E, int K, int b_rows, int n_out, int64_t rows_cap, bf16* out,
-                               int32_t* status, cudaStream_t s, tc::Gather g = tc::Gather{}, int cols_fastest = 0) {
+                               int32_t* status, cudaStream_t s, tc::Gather g = tc::Gather{}, int sched = 0) {
   using namespace tc;
   if (pair) {
     // the pair kernel's epilogue stores 32-row x 64-column blocks of `out` through this map
@@ -1236,14 +1244,14 @@ static cudaError_t launch_gemm(bool pair, int grid, const CUtensorMap& a, const 
       grid = 2 * max_clusters;
     (void)cudaGetLastError();
     kern<<<grid, THREADS, P_SMEM_BYTES, s>>>(a, b0, b1, tmOut, offsets, E, K, b_rows, n_out, rows_cap, out, status, g,
-                                             cols_fastest);
+                                             sched);
   } else {
     auto kern = grouped_gemm_tc<SWIGLU, false, GATHER>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
     kern<<<grid, THREADS, SMEM_BYTES, s>>>(a, b0, b1, offsets, E, K, b_rows, n_out, rows_cap, out, status, nullptr,
-                                           nullptr, nullptr, g, cols_fastest);
+                                           nullptr, nullptr, g, sched);
   }
   return cudaGetLastError();
 }
@@ -1305,6 +1313,14 @@ cudaError_t launch_ffn_tc(const Plan& p, const void* X, const int32_t* offsets, 
     if (strcmp(env, "rows") == 0) order1 = order2 = 0;
     if (strcmp(env, "cols") == 0) order1 = order2 = 1;
   }
+  // L2 hints (MOE_FFN_L2=none|first for measurement): bits 1-2 of the tile schedule
+  int l2 = 0;
+  if (const char* env = getenv("MOE_FFN_L2")) {
+    if (strcmp(env, "none") == 0) l2 = 1;
+    if (strcmp(env, "first") == 0) l2 = 2;
+  }
+  order1 |= l2 << 1;
+  order2 |= l2 << 1;
   cudaError_t e =
       gather ? launch_gemm<true, true>(pair, grid1, tmX, tmG, tmU, offsets, p.E, p.h, p.d_e, p.d_e, p.Tk,
                                        static_cast<bf16*>(act), status, s,
