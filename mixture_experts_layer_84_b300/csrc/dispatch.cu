@@ -12,7 +12,9 @@
 // p = j*T + t; token-major: p = t*k + j).  The slot of a pair is the number
 // of earlier pairs with the same expert -- an exclusive prefix count, so it is
 // computed with scans, never with an atomic whose order could leak into the
-// result:
+// result.  Choice-major priority (the default) takes three launches, dispatch_hist,
+// dispatch_colscan and dispatch_place, described where they are defined.  Token-major
+// priority and the workspace-free entry point take these four:
 //   dispatch_count   per chunk of positions, a histogram over experts;
 //   dispatch_scan    one block: per expert, the exclusive prefix over chunks,
 //                    the routed/kept counts, and offsets = exclusive scan of

@@ -65,7 +65,7 @@ struct Plan {
   // dispatch
   int chunk = 0;           // priority positions per histogram chunk (token-major priority)
   int n_chunks = 0;
-  int dp_tc = 0;           // tokens per chunk of the two-launch choice-major dispatch
+  int dp_tc = 0;           // tokens per chunk of the choice-major dispatch (8 .. 256)
   int dp_chunks = 0;
 
   // workspace byte offsets
