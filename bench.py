@@ -190,15 +190,11 @@ def launches_per_step(w: W.Workload, gather: bool = False, fp8: bool = False) ->
     fused_router = w.dtype == W.BF16 and (2 * w.E if w.noisy else w.E) <= 256
     route = 1 if fused_router else 2       # the fused router (weights packed beforehand), or logits + selection
     if w.priority == W.PRIORITY_CHOICE_MAJOR:
-        # histograms, column scans (folded into the histogram launch for k E <= 128 columns), then
-        # slots + row copy (no copy when gathering)
-        dispatch = 2 if w.k * w.E <= 128 else 3
-        meta = dispatch
+        dispatch = 3                       # histograms, column scans, then slots + row copy (no copy when gathering)
     else:
         dispatch = 3 if gather else 4      # count, scan, assign (, scatter)
-        meta = 3
     if fp8:
-        dispatch = meta + 1                # the metadata only (no bf16 copy), then the E4M3 row copy
+        dispatch = 3 + 1                   # the metadata only (no bf16 copy), then the E4M3 row copy
     ffn, combine = 2, 1                    # two GEMMs; rows and statistics
     return route + dispatch + ffn + 2 * w.n_shared + combine
 

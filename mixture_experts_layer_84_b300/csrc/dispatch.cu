@@ -256,8 +256,7 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 //   dispatch_hist    per chunk, h[c][j][e];
 //   dispatch_colscan one warp per (j, e) column: exclusive prefixes over the chunks and the column
 //                    total; the block that finishes last (an atomic ticket, nobody waits) forms the
-//                    choice bases, the routed and kept counts, the offsets and n_dropped.  With
-//                    k E <= 128 columns the last dispatch_hist block does all of this instead;
+//                    choice bases, the routed and kept counts, the offsets and n_dropped;
 //   dispatch_place  per chunk and choice: ranks among equal experts inside each warp (match_any)
 //                   on top of the chunk's base and the earlier warps' counts; writes slot_row and
 //                   row_token; meanwhile the chunk's U rows (contiguous) arrive in shared memory
@@ -270,62 +269,90 @@ constexpr uint64_t COPY_WAIT_LIMIT_NS = 2000000000ull;
 constexpr int PLACE_WARPS = PLACE_THREADS / 32;
 constexpr int HIST_THREADS = 1024;
 
-// One warp scans column col = (choice j, expert e) of the chunk histograms: lane l adds the chunks
-// [l m, (l+1) m), the warp scans the lane sums, every chunk's entry becomes the exclusive prefix over
-// the earlier chunks, and the column total goes to cnt[col].  CG: the histograms were written by
-// other blocks of the same launch (read through L2).
-template <bool CG>
-__device__ __forceinline__ void scan_column(int32_t* __restrict__ hist, int n_chunks, int kE, int col, int lane,
-                                            int32_t* __restrict__ cnt) {
-  const int m = (n_chunks + 31) / 32;
-  const int c0 = min(n_chunks, lane * m), c1 = min(n_chunks, c0 + m);
-  auto load = [&](int64_t o) { return CG ? __ldcg(hist + o) : hist[o]; };
-  // up to 8 chunks a lane are loaded at once and kept in registers (one round trip)
-  int32_t vals[8];
-  int32_t s = 0;
-  if (m <= 8) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) vals[q] = c0 + q < c1 ? load(static_cast<int64_t>(c0 + q) * kE + col) : 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) s += vals[q];
-  } else {
-    for (int c = c0; c < c1; ++c) s += load(static_cast<int64_t>(c) * kE + col);
+__global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __restrict__ idx, int64_t T, int k,
+                                                              int E, int tc, int32_t* __restrict__ hist,
+                                                              int32_t* status) {
+  extern __shared__ int32_t h_s[];  // [k][E]
+  const int kE = k * E;
+  for (int i = threadIdx.x; i < kE; i += blockDim.x) h_s[i] = 0;
+  __syncthreads();
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tc;
+  const int64_t t1 = min(t0 + tc, T);
+  bool bad = false;
+  for (int64_t i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+    const int j = static_cast<int>(i % k);
+    const int e = idx[i];
+    if (e >= 0 && e < E)
+      atomicAdd(&h_s[j * E + e], 1);  // integer counts: the order of the adds does not matter
+    else
+      bad = true;
   }
-  int32_t incl = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  int32_t run = incl - s;
-  if (m <= 8) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (c0 + q < c1) hist[static_cast<int64_t>(c0 + q) * kE + col] = run;
-      run += vals[q];
-    }
-  } else {
-    for (int c = c0; c < c1; ++c) {
-      const int64_t o = static_cast<int64_t>(c) * kE + col;
-      const int32_t v = load(o);
-      hist[o] = run;
-      run += v;
-    }
-  }
-  if (lane == 31) cnt[col] = incl;
+  if (bad) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+  __syncthreads();
+  int32_t* mine = hist + static_cast<int64_t>(blockIdx.x) * kE;
+  for (int i = threadIdx.x; i < kE; i += blockDim.x) mine[i] = h_s[i];
 }
 
-// By one block, once every column total cnt[j][e] is in place: the choice bases (the pairs of
-// earlier choices per expert), the routed and kept counts, offsets = exclusive scan of the kept
-// counts, n_dropped; then the ticket is reset for the next call.
-__device__ void finish_counts(int32_t* __restrict__ hist, int n_chunks, int k, int E, int64_t C, int64_t Tk,
-                              int32_t* __restrict__ counts_routed, int32_t* __restrict__ counts_kept,
-                              int32_t* __restrict__ offsets, int64_t* __restrict__ n_dropped,
-                              int32_t* __restrict__ ticket) {
-  __shared__ int32_t kept_s[1024];
+// One warp per (choice j, expert e) column of the chunk histograms: lane l adds the chunks
+// [l m, (l+1) m), the warp scans the lane sums, and every chunk's entry becomes the exclusive prefix
+// over the earlier chunks; the column total goes to cnt[j][e].  The block that finishes last (an
+// atomic ticket, nobody waits) forms the choice bases (the pairs of earlier choices per expert),
+// the routed and kept counts, the offsets and n_dropped, and resets the ticket.
+__global__ void __launch_bounds__(256) dispatch_colscan(int32_t* __restrict__ hist, int n_chunks, int k, int E,
+                                                        int64_t C, int64_t Tk, int32_t* __restrict__ ticket,
+                                                        int32_t* __restrict__ counts_routed,
+                                                        int32_t* __restrict__ counts_kept,
+                                                        int32_t* __restrict__ offsets,
+                                                        int64_t* __restrict__ n_dropped) {
   const int kE = k * E;
   const int lane = threadIdx.x % 32;
-  const int32_t* cnt = hist + static_cast<int64_t>(n_chunks + 1) * kE;
+  const int col = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  int32_t* cnt = hist + static_cast<int64_t>(n_chunks + 1) * kE;  // [k][E] column totals
+  if (col < kE) {
+    const int m = (n_chunks + 31) / 32;
+    const int c0 = min(n_chunks, lane * m), c1 = min(n_chunks, c0 + m);
+    // up to 8 chunks a lane are loaded at once and kept in registers (one round trip)
+    int32_t vals[8];
+    int32_t s = 0;
+    if (m <= 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) vals[q] = c0 + q < c1 ? hist[static_cast<int64_t>(c0 + q) * kE + col] : 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) s += vals[q];
+    } else {
+      for (int c = c0; c < c1; ++c) s += hist[static_cast<int64_t>(c) * kE + col];
+    }
+    int32_t incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int32_t run = incl - s;
+    if (m <= 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (c0 + q < c1) hist[static_cast<int64_t>(c0 + q) * kE + col] = run;
+        run += vals[q];
+      }
+    } else {
+      for (int c = c0; c < c1; ++c) {
+        const int64_t o = static_cast<int64_t>(c) * kE + col;
+        const int32_t v = hist[o];
+        hist[o] = run;
+        run += v;
+      }
+    }
+    if (lane == 31) cnt[col] = incl;
+  }
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  __shared__ int32_t kept_s[1024];
   int32_t* cbase = hist + static_cast<int64_t>(n_chunks) * kE;  // [k][E] choice bases
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int32_t c[16];  // k <= 16: every choice's total loaded at once
@@ -366,73 +393,6 @@ __device__ void finish_counts(int32_t* __restrict__ hist, int n_chunks, int k, i
       *ticket = 0;  // ready for the next call
     }
   }
-}
-
-// h[c][j][e] of token chunk c (shared-memory counts).  With `fold` (few columns), the block that
-// finishes last (an atomic ticket, nobody waits) also scans every column and finishes the counts,
-// so that dispatch_colscan is not launched.
-__global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __restrict__ idx, int64_t T, int k,
-                                                              int E, int tc, int32_t* __restrict__ hist,
-                                                              int32_t* status, int fold, int n_chunks, int64_t C,
-                                                              int64_t Tk, int32_t* __restrict__ ticket,
-                                                              int32_t* __restrict__ counts_routed,
-                                                              int32_t* __restrict__ counts_kept,
-                                                              int32_t* __restrict__ offsets,
-                                                              int64_t* __restrict__ n_dropped) {
-  extern __shared__ int32_t h_s[];  // [k][E]
-  const int kE = k * E;
-  for (int i = threadIdx.x; i < kE; i += blockDim.x) h_s[i] = 0;
-  __syncthreads();
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tc;
-  const int64_t t1 = min(t0 + tc, T);
-  bool bad = false;
-  for (int64_t i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
-    const int j = static_cast<int>(i % k);
-    const int e = idx[i];
-    if (e >= 0 && e < E)
-      atomicAdd(&h_s[j * E + e], 1);  // integer counts: the order of the adds does not matter
-    else
-      bad = true;
-  }
-  if (bad) set_status(status, MOE_DEV_BAD_EXPERT_ID);
-  __syncthreads();
-  int32_t* mine = hist + static_cast<int64_t>(blockIdx.x) * kE;
-  for (int i = threadIdx.x; i < kE; i += blockDim.x) mine[i] = h_s[i];
-  if (!fold) return;
-  __shared__ int last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  int32_t* cnt = hist + static_cast<int64_t>(n_chunks + 1) * kE;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int col = warp; col < kE; col += blockDim.x / 32) scan_column<true>(hist, n_chunks, kE, col, lane, cnt);
-  __syncthreads();
-  finish_counts(hist, n_chunks, k, E, C, Tk, counts_routed, counts_kept, offsets, n_dropped, ticket);
-}
-
-// One warp per (choice j, expert e) column (scan_column); the block that finishes last (an atomic
-// ticket, nobody waits) finishes the counts (finish_counts).
-__global__ void __launch_bounds__(256) dispatch_colscan(int32_t* __restrict__ hist, int n_chunks, int k, int E,
-                                                        int64_t C, int64_t Tk, int32_t* __restrict__ ticket,
-                                                        int32_t* __restrict__ counts_routed,
-                                                        int32_t* __restrict__ counts_kept,
-                                                        int32_t* __restrict__ offsets,
-                                                        int64_t* __restrict__ n_dropped) {
-  const int kE = k * E;
-  const int col = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  int32_t* cnt = hist + static_cast<int64_t>(n_chunks + 1) * kE;  // [k][E] column totals
-  if (col < kE) scan_column<false>(hist, n_chunks, kE, col, threadIdx.x % 32, cnt);
-  __shared__ int last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  finish_counts(hist, n_chunks, k, E, C, Tk, counts_routed, counts_kept, offsets, n_dropped, ticket);
 }
 
 __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
@@ -598,20 +558,14 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
                                                  static_cast<int>(hsm));
       if (e != cudaSuccess) return e;
     }
-    // up to four columns a warp of one block: the last histogram block scans them (no colscan launch)
-    const int cols = p.k * p.E;
-    const int fold = cols <= 4 * (HIST_THREADS / 32) ? 1 : 0;
-    dispatch_hist<<<p.dp_chunks, HIST_THREADS, hsm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, hist, status, fold,
-                                                         p.dp_chunks, p.C, p.Tk, ticket, counts_routed, counts_kept,
-                                                         offsets, n_dropped);
+    dispatch_hist<<<p.dp_chunks, HIST_THREADS, hsm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, hist, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (!fold) {
-      dispatch_colscan<<<(cols + 7) / 8, 256, 0, s>>>(hist, p.dp_chunks, p.k, p.E, p.C, p.Tk, ticket, counts_routed,
-                                                       counts_kept, offsets, n_dropped);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-    }
+    const int cols = p.k * p.E;
+    dispatch_colscan<<<(cols + 7) / 8, 256, 0, s>>>(hist, p.dp_chunks, p.k, p.E, p.C, p.Tk, ticket, counts_routed,
+                                                     counts_kept, offsets, n_dropped);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const uint32_t row_bytes = static_cast<uint32_t>(p.h) * (p.bf16 ? 2 : 4);
     const int stage_bases = p.k * p.E <= 4096 ? 1 : 0;  // the chunk's bases fit 16 KB of shared memory
     const size_t meta = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + 2 * static_cast<size_t>(p.dp_tc) * p.k +

@@ -38,24 +38,21 @@ def test_stage_work_fp8_and_gather_variants():
     assert g["dispatch"]["bytes"] == w.T * w.k * 12 and g["ffn"] == base["ffn"]
 
 
-@pytest.mark.parametrize("w,expected,folded", [(W.MIXTRAL, 6, True), (W.TINY_FP32, 7, True),
-                                               (W.DSV3_SHARED, 9, False), (W.SWITCH, 6, True),
-                                               (W.STRESS, 7, False), (W.MIXTRAL.replace(name="empty", T=0), 2, True)])
-def test_launches_per_step(w, expected, folded):
+@pytest.mark.parametrize("w,expected", [(W.MIXTRAL, 7), (W.TINY_FP32, 8), (W.DSV3_SHARED, 9),
+                                        (W.SWITCH, 7), (W.MIXTRAL.replace(name="empty", T=0), 2)])
+def test_launches_per_step(w, expected):
     """route (the fused tensor-core router from weights packed beforehand, else logits +
-    selection), dispatch (histograms, column scans unless k E <= 128 folds them into the histogram
-    launch, then slots + row copy), two GEMMs per routed and per shared expert block, combine with
-    statistics; token-major dispatch takes count, scan, assign and scatter; FP8 adds the E4M3 row
-    copy after the metadata."""
+    selection), dispatch (histograms, column scans, then slots + row copy), two GEMMs per routed and
+    per shared expert block, combine with statistics; token-major dispatch takes count, scan,
+    assign and scatter."""
     assert bench.launches_per_step(w) == expected
     if w.T:
-        cm_dispatch = 2 if folded else 3
         assert bench.launches_per_step(w, gather=True) == expected
         tm = w.replace(priority=W.PRIORITY_TOKEN_MAJOR)
-        assert bench.launches_per_step(tm) == expected - cm_dispatch + 4
-        assert bench.launches_per_step(tm, gather=True) == expected - cm_dispatch + 3
+        assert bench.launches_per_step(tm) == expected + 1
+        assert bench.launches_per_step(tm, gather=True) == expected
         assert bench.launches_per_step(w, fp8=True) == expected + 1
-        assert bench.launches_per_step(tm, fp8=True) == expected - cm_dispatch + 3 + 1
+        assert bench.launches_per_step(tm, fp8=True) == expected + 1
 
 
 def test_ffn_tiles_rule(monkeypatch):
