@@ -80,6 +80,13 @@ def test_expert_ffn_tile_orders(w, tiles, order, monkeypatch):
     test_expert_ffn(w, 1.2, tiles, monkeypatch, order=order)
 
 
+@pytest.mark.parametrize("l2", ["none", "first"])
+def test_expert_ffn_l2_hints(l2, monkeypatch):
+    """The L2 hint modes kept for measurement change nothing but the cache policy."""
+    monkeypatch.setenv("MOE_FFN_L2", l2)
+    test_expert_ffn(EDGE[-1], 1.2, "pair", monkeypatch, order="cols")
+
+
 @pytest.mark.parametrize("dtype,tiles", [(W.BF16, "single"), (W.BF16, "pair"), (W.BF16, "swab"), (W.F32, "single")])
 def test_expert_ffn_rejects_inconsistent_offsets(dtype, tiles, monkeypatch):
     monkeypatch.setenv("MOE_FFN_TILES", tiles)
