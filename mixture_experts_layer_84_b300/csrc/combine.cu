@@ -76,32 +76,24 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_stats(
   const int dq = static_cast<int>(warps - dt * tasks_per_tok);
   int64_t t = first / tasks_per_tok;
   int q = static_cast<int>(first - t * tasks_per_tok);
-  // lane j < k holds the row and gate of choice j; the next task's are loaded while this one runs
-  auto fetch = [&](int64_t tt, int32_t& row, float& g) {
-    row = -1;
-    g = 0.f;
-    if (tt < n_tok && lane < k) {
-      row = slot_row[tt * k + lane];
-      g = gate[tt * k + lane];
-    }
-  };
-  int32_t my_row, next_row;
-  float my_g, next_g;
-  fetch(t, my_row, my_g);
-  while (t < n_tok) {
-    int64_t t_next = t + dt;
-    int q_next = q + dq;
-    if (q_next >= tasks_per_tok) {
-      q_next -= tasks_per_tok;
-      ++t_next;
-    }
-    fetch(t_next, next_row, next_g);
-    if (my_row < -1 || my_row >= rows_cap) {
-      set_status(status, MOE_DEV_BAD_ROW);
-      my_row = -1;
+  for (; t < n_tok; t += dt, q += dq) {
+    if (q >= tasks_per_tok) {
+      q -= tasks_per_tok;
+      ++t;
+      if (t >= n_tok) break;
     }
     const int v_lo = q * spu * 32 * COMBINE_UNROLL;
     const int v_hi = min(vpr, (q + 1) * spu * 32 * COMBINE_UNROLL);
+    int32_t my_row = -1;
+    float my_g = 0.f;
+    if (lane < k) {
+      my_row = slot_row[t * k + lane];
+      my_g = gate[t * k + lane];
+      if (my_row < -1 || my_row >= rows_cap) {
+        set_status(status, MOE_DEV_BAD_ROW);
+        my_row = -1;
+      }
+    }
     // warp-uniform trip count: every lane reaches the shuffles below
     for (int base = v_lo; base < v_hi; base += 32 * COMBINE_UNROLL) {
       float acc[COMBINE_UNROLL][N];
@@ -143,10 +135,6 @@ __global__ void __launch_bounds__(COMBINE_THREADS, 4) combine_stats(
         if (v < v_hi) out[t * vpr + v] = Vec16<T>::pack(acc[u]);
       }
     }
-    t = t_next;
-    q = q_next;
-    my_row = next_row;
-    my_g = next_g;
   }
 
   // statistics, by the last block to finish
