@@ -269,9 +269,10 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* X, const int32_t* o
  *   row_token [T*k] int32              from moe_dispatch: row r of the expert input is U[row_token[r]]
  *                                      (ids outside [0, T) read row 0 and set MOE_DEV_BAD_ROW)
  *   offsets, W_gate, W_up, W_down, act, Y   as in moe_expert_ffn
- * No X is read or written: the first GEMM's producer copies each 128 x 64 A tile straight from
- * the token rows of U (16-byte cp.async into the swizzled layout of a TMA tile).  act and Y are
- * bit-identical to moe_expert_ffn on X[r] = U[row_token[r]]. */
+ * No X is read or written: the first GEMM's producer loads each 128 x 64 A tile straight from the
+ * token rows of U (32 four-row TMA gathers into the swizzled layout of a tiled load).  act and Y
+ * are bit-identical to moe_expert_ffn on X[r] = U[row_token[r]].  It is slower than the
+ * materialised X when the first GEMM has many column tiles (each re-reads the gathered rows). */
 moe_status moe_expert_ffn_gather(const moe_config* cfg, const void* U, const int32_t* row_token,
                                  const int32_t* offsets, const void* W_gate, const void* W_up,
                                  const void* W_down, void* act, void* Y, void* ws, moe_stream_t stream);
