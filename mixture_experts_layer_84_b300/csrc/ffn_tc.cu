@@ -9,7 +9,8 @@
 //
 // Kernel (one persistent CTA per SM, 192 threads):
 //   warp 0    TMA producer: 4-stage ring of {X tile 128x64, W tile 256x64}
-//             (bf16, 128-byte swizzle), completion counted on mbarriers;
+//             (bf16, 128-byte swizzle; or X rows by four-row TMA gathers),
+//             completion counted on mbarriers;
 //   warp 1    allocates 512 tensor-memory columns (two 128x256 f32
 //             accumulators) and one lane issues tcgen05.mma 128x256x16,
 //             releasing smem stages and finished accumulators with
@@ -20,9 +21,11 @@
 // Gate|up fusion: a B stage holds 128 rows of W_gate[e] followed by the same
 // 128 rows of W_up[e], so accumulator columns c and 128+c are the gate and up
 // values of output column c; no repacking of the weights is needed.
-// Tile order: expert, then output-column tile, then row tile, so the CTAs that
-// run together share the weight tile (read once from HBM, then from L2), and
-// an expert's rows stay in L2 while its column tiles go by.
+// Tile order: expert by expert; inside an expert either row tiles vary fastest
+// (the CTAs that run together share a weight tile, and the expert's rows are
+// re-read once per column tile) or column tiles do (they share a row tile, and
+// the expert's weights are re-read once per row tile), whichever re-reads the
+// smaller operand; that operand gets the evict_last L2 hint.
 // Every mbarrier wait is bounded (2 s); a wait that gives up makes every role
 // leave its loop, in-flight copies and MMAs are drained (again bounded), the
 // tensor memory is freed and MOE_DEV_TIMEOUT is recorded in the status word.
