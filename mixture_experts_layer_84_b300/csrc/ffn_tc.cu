@@ -467,11 +467,6 @@ constexpr size_t P_SMEM_BYTES = 1024 + P_OUT_OFF + 4 * P_OUT_BYTES;
 static_assert(P_SMEM_BYTES <= 232448, "shared memory");
 static_assert((2 * P_STAGES + 2 + 2 + 1) * 8 + 12 <= P_BAR_BYTES, "barriers fit P_BAR_BYTES");
 
-// 4-byte store to a cluster CTA's shared memory (address from mapa).
-__device__ __forceinline__ void st_cluster_b32(uint32_t addr, int v) {
-  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ bool wait_cluster_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
@@ -822,11 +817,7 @@ constexpr uint32_t S_XCH_FLOATS = 2 * 2 * 16 * 32;        // 2 warp pairs x 2 di
 constexpr size_t S_SMEM_BYTES =
     1024 + S_STAGES * S_STAGE_BYTES + S_XCH_FLOATS * 4 + P_BAR_BYTES + sizeof(int) * (MAX_E + 1);
 static_assert(S_SMEM_BYTES <= 232448, "shared memory");
-constexpr int S_QD = 4;                                   // depth of the tile queue
-static_assert((2 * S_STAGES + 2 + 2 + 1 + 2 * S_QD) * 8 + 12 + 4 * S_QD <= P_BAR_BYTES, "barriers fit P_BAR_BYTES");
-// The tile queue's consumers, all arriving on the even CTA's qempty: the even CTA's MMA issuer and
-// 4 epilogue warps, the odd CTA's producer and 4 epilogue warps.
-constexpr uint32_t S_Q_CONSUMERS = 10;
+static_assert((2 * S_STAGES + 2 + 2 + 1) * 8 + 12 <= P_BAR_BYTES, "barriers fit P_BAR_BYTES");
 
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -864,8 +855,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     grouped_gemm_swab(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                       const __grid_constant__ CUtensorMap tmX, const int32_t* __restrict__ offsets, int E, int K,
                       int w_rows_per_expert, int n_out, int64_t rows_cap, bf16* __restrict__ out, int32_t* status,
-                      int32_t* __restrict__ tile_counter, const float* __restrict__ x_scale = nullptr,
-                      const float* __restrict__ w0_scale = nullptr, const float* __restrict__ w1_scale = nullptr) {
+                      const float* __restrict__ x_scale = nullptr, const float* __restrict__ w0_scale = nullptr,
+                      const float* __restrict__ w1_scale = nullptr) {
   static_assert(SWIGLU || !FP8, "the FP8 path is the up-projection");
   constexpr int WT = SWIGLU ? 128 : 256;  // output columns per pair tile
   constexpr int BKE = FP8 ? 2 * BK : BK;  // K elements per stage (128 bytes of every row)
@@ -878,12 +869,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + S_STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* qfull = drain + 1;       // [S_QD] a tile id is in the queue slot
-  uint64_t* qempty = qfull + S_QD;   // [S_QD] (even CTA) every consumer has read the slot
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(qempty + S_QD);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* bad_flag = reinterpret_cast<int*>(tmem_holder + 2);
-  volatile int* tq = reinterpret_cast<volatile int*>(tmem_holder + 3);  // [S_QD] the tile queue
   int* tab = reinterpret_cast<int*>(smem + S_STAGES * S_STAGE_BYTES + S_XCH_FLOATS * 4 + P_BAR_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -923,10 +911,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       ptx::mbar_init(&tempty[a], 8);
     }
     ptx::mbar_init(drain, 1);
-    for (int s = 0; s < S_QD; ++s) {
-      ptx::mbar_init(&qfull[s], 1);
-      ptx::mbar_init(&qempty[s], S_Q_CONSUMERS);
-    }
     ptx::fence_mbarrier_init();
   }
   __syncthreads();
@@ -953,31 +937,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint64_t pol_x = ptx::policy_evict_last();
       uint32_t stage = 0, phase = 0, armed = 0, armed_phase = 0;
       bool ok = true;
-      for (uint32_t it = 0; ok; ++it) {
-        // the next tile: the even CTA's producer takes it (its cluster's first tile statically, then from
-        // the counter) and publishes it to both CTAs' queues; every other role reads it from its queue
-        const uint32_t slot = it % S_QD, qph = (it / S_QD) & 1u;
-        int tile;
-        if (even) {
-          if (!wait_cluster_bounded(&qempty[slot], qph ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tile = it == 0 ? cid : ncl + atomicAdd(tile_counter, 1);
-          if (tile >= total) tile = -1;
-          tq[slot] = tile;
-          st_cluster_b32(ptx::mapa_shared(ptx::smem_u32(const_cast<int*>(&tq[slot])), 1), tile);
-          ptx::mbar_arrive(&qfull[slot]);
-          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&qfull[slot]), 1));
-        } else {
-          if (!wait_cluster_bounded(&qfull[slot], qph, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tile = tq[slot];
-          ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&qempty[slot]), 0));
-        }
-        if (tile < 0) break;
+      for (int tile = cid; ok && tile < total; tile += ncl) {
         int e, mt, nt;
         decode_tile(tab, E, MT, tile, &e, &mt, &nt);
         const int seg = seg_lo(offsets, e);
@@ -1026,15 +986,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (even && lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (uint32_t it = 0; ok; ++it) {
-        const uint32_t slot = it % S_QD, qph = (it / S_QD) & 1u;
-        if (!wait_cluster_bounded(&qfull[slot], qph, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const int tile = tq[slot];
-        ptx::mbar_arrive(&qempty[slot]);
-        if (tile < 0) break;
+      for (int tile = cid; ok && tile < total; tile += ncl) {
         int e, mt, nt;
         decode_tile(tab, E, MT, tile, &e, &mt, &nt);
         const int n_e = seg_hi(offsets, e, rows_cap) - seg_lo(offsets, e);
@@ -1087,17 +1039,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     float* xg = xch + p * (2 * 16 * 32);  // gate values of tokens 16..31, [16][32]
     float* xu = xg + 16 * 32;             // up values of tokens 0..15
     uint32_t acc = 0, acc_phase = 0;
-    for (uint32_t it = 0;; ++it) {
-      const uint32_t slot = it % S_QD, qph = (it / S_QD) & 1u;
-      const bool got = wait_cluster_bounded(&qfull[slot], qph, abort_flag);
-      const int tile = got ? tq[slot] : -1;
-      __syncwarp();
-      if (got && lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ptx::smem_u32(&qempty[slot]), 0));
-      if (tile < 0) {
-        // a SwiGLU warp pair leaves together: the partner read the same slot (or gives up as well)
-        if (SWIGLU) named_all(1 + p, 64, false);
-        break;
-      }
+    for (int tile = cid; tile < total; tile += ncl) {
       int e, mt, nt;
       decode_tile(tab, E, MT, tile, &e, &mt, &nt);
       const int seg = seg_lo(offsets, e);
@@ -1236,10 +1178,6 @@ static cudaError_t launch_swab(int64_t tiles, const CUtensorMap& w0, const CUten
                                const int32_t* offsets, int E, int K, int w_rows, int n_out, int64_t rows_cap,
                                bf16* out, int32_t* status, cudaStream_t s, const float* x_scale = nullptr,
                                const float* w0_scale = nullptr, const float* w1_scale = nullptr) {
-  // the tile counter (after each cluster's first tile) starts at zero for every launch
-  int32_t* counter = gemm_tile_counter(status);
-  cudaError_t me = cudaMemsetAsync(counter, 0, sizeof(int32_t), s);
-  if (me != cudaSuccess) return me;
   using namespace tc;
   auto kern = grouped_gemm_swab<SWIGLU, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(S_SMEM_BYTES));
@@ -1255,8 +1193,8 @@ static cudaError_t launch_swab(int64_t tiles, const CUtensorMap& w0, const CUten
       2 * max_clusters < grid)
     grid = 2 * max_clusters;
   (void)cudaGetLastError();
-  kern<<<grid, THREADS, S_SMEM_BYTES, s>>>(w0, w1, x, offsets, E, K, w_rows, n_out, rows_cap, out, status, counter,
-                                           x_scale, w0_scale, w1_scale);
+  kern<<<grid, THREADS, S_SMEM_BYTES, s>>>(w0, w1, x, offsets, E, K, w_rows, n_out, rows_cap, out, status, x_scale,
+                                           w0_scale, w1_scale);
   return cudaGetLastError();
 }
 

@@ -170,8 +170,6 @@ cudaError_t launch_ffn_simt_f32(const Plan& p, const void* X, const int32_t* off
                                 cudaStream_t s);
 
 inline int32_t* ws_status(const Plan& p, uint8_t* ws) { return reinterpret_cast<int32_t*>(ws + p.ws_status); }
-// The grouped GEMM's tile counter, 224 bytes into the status area (zeroed before each launch).
-inline int32_t* gemm_tile_counter(int32_t* status) { return status + 56; }
 // Rows of per-block score sums the last router call left in the workspace (read by the statistics).
 inline int32_t* ws_ppart_rows(const Plan& p, uint8_t* ws) {
   return reinterpret_cast<int32_t*>(ws + p.ws_status + 64);
