@@ -58,8 +58,6 @@ struct Plan {
   int rf_cs = 0;           // CTAs per tile (a cluster), each with a slice of h
   int rf_stages = 0;       // its TMA ring depth
   int rf_threads = 256;    // threads a CTA: 512 when one CTA fills an SM anyway (more warps to select)
-  bool route_small = false;  // at most 16 logit columns: the CUDA-core router (route_small) instead
-  int rs_blocks = 0;         // its blocks (16 tokens each)
   int sel_threads = 0;     // threads per select block (G lanes per token)
   int sel_tokens = 0;      // tokens per select block
   int sel_blocks = 0;      // ceil(T / sel_tokens): number of P partial rows
@@ -91,9 +89,6 @@ cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const fl
 // transposed below it, zero rows up to route_tc_n).
 cudaError_t launch_pack_router(const Plan& p, const void* W_r, const void* W_noise, void* Wt, cudaStream_t s);
 // The fused router (bf16, route_tc_n > 0) from packed weights Wt.
-cudaError_t launch_route_small(const Plan& p, const void* U, const void* Wt, const float* b_r, const float* sel_bias,
-                               const float* eps, float* logits_out, int32_t* idx, float* gate, uint8_t* ws,
-                               cudaStream_t s);
 cudaError_t launch_route_fused(const Plan& p, const void* U, const void* Wt, const float* b_r, const float* sel_bias,
                                const float* eps, float* logits_out, int32_t* idx, float* gate, uint8_t* ws,
                                cudaStream_t s);

@@ -186,10 +186,6 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     // one wave whose four-stage ring already fills an SM (N > 96: the 256-expert and the noisy
     // 128-expert routers): 512 threads, so that the epilogue has 16 warps to hide its latencies
     q.rf_threads = static_cast<int64_t>(q.rf_tiles) * cs <= 148 && 4 * stage_kb > 113 ? 512 : 256;
-    // at most 16 logit columns (E <= 16, or E <= 8 noisy): each token is a short dot product per
-    // column, which CUDA cores finish at HBM speed without an MMA tile or a cluster exchange
-    q.route_small = n_cols <= 16;
-    q.rs_blocks = static_cast<int>((q.T + 15) / 16);
   }
   // selection blocks: 256 threads, fewer (down to a warp) when T is small, so that the
   // blocks still spread over about twice the SMs
@@ -226,8 +222,7 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
   q.ws_npart = off;
   if (q.noisy) off += align256(logits_bytes);
   q.ws_ppart = off;
-  const int64_t ppart_rows = std::max<int64_t>(std::max<int64_t>(q.sel_blocks, static_cast<int64_t>(q.rf_tiles) * q.rf_cs),
-                                                q.rs_blocks);
+  const int64_t ppart_rows = std::max<int64_t>(q.sel_blocks, static_cast<int64_t>(q.rf_tiles) * q.rf_cs);
   off += align256(sizeof(float) * static_cast<size_t>(ppart_rows) * (q.E + 1));
   q.ws_stats2 = off;
   off += align256(sizeof(float) * 32 * static_cast<size_t>(q.E + 1));

@@ -313,116 +313,6 @@ cudaError_t launch_select_kp(const Plan& p, const float* part, const float* npar
 
 }  // namespace
 
-// The router for at most 16 logit columns (E <= 16, or E <= 8 with the noise branch), on CUDA
-// cores: 256 threads, each warp two tokens.  Lane l takes the 16-byte vectors l, l + 32, ... of a
-// token's row of U and, for every packed weight row n (W_r^T, then W_noise^T: the layout
-// moe_pack_router writes), adds the 8-element dot products into acc[n]; the warp then adds the
-// lanes' sums (xor shuffles, the same order on every lane).  The two tokens of a warp share each
-// weight vector it loads.  The logits (+ bias, + eps * softplus(noise logits)) are staged for
-// select_tokens with one lane per token, then the block's score sums go to its ppart row.
-// "MoE 与专家并行", section 路由器：打分、top-k、加权求和 (router linear, noisy top-k) and the
-// sections select_tokens cites.
-template <int KP>
-__global__ void __launch_bounds__(256) route_small(
-    const uint4* __restrict__ U, const uint4* __restrict__ Wt, int64_t T, int h, int E, int noisy,
-    const float* __restrict__ b_r, const float* __restrict__ sel_bias, const float* __restrict__ eps,
-    float* __restrict__ logits_out, int32_t* __restrict__ idx, float* __restrict__ gate, float* __restrict__ ppart,
-    int32_t* __restrict__ ppart_rows, int k, int score_fn, int renorm, int n_group, int topk_group) {
-  constexpr int TPB = 16;  // tokens per block: two per warp
-  constexpr int NMAX = 16;
-  __shared__ float sx[TPB * (NMAX + 2)];
-  __shared__ float zsq[TPB];
-  __shared__ float gsc[TPB * MAX_GROUPS];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int nc = noisy ? 2 * E : E;
-  const int vpr = h / 8;  // 16-byte vectors per row
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TPB;
-  const int rows = static_cast<int>(T - t0 < TPB ? T - t0 : TPB);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *ppart_rows = static_cast<int32_t>(gridDim.x);
-  const int ra = 2 * warp, rb = ra + 1;  // this warp's rows of the block
-  const bool has_a = ra < rows, has_b = rb < rows;
-  float acc_a[NMAX], acc_b[NMAX];
-#pragma unroll
-  for (int n = 0; n < NMAX; ++n) acc_a[n] = acc_b[n] = 0.f;
-  const uint4* ua = U + (t0 + ra) * vpr;
-  const uint4* ub = U + (t0 + rb) * vpr;
-#pragma unroll 2
-  for (int v = lane; v < vpr; v += 32) {
-    float xa[8], xb[8];
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    Vec16<bf16>::unpack(has_a ? ldg_stream(ua + v) : zero, xa);
-    Vec16<bf16>::unpack(has_b ? ldg_stream(ub + v) : zero, xb);
-#pragma unroll
-    for (int n = 0; n < NMAX; ++n) {
-      if (n < nc) {
-        float w[8];
-        Vec16<bf16>::unpack(__ldg(Wt + static_cast<int64_t>(n) * vpr + v), w);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc_a[n] = fmaf(xa[i], w[i], acc_a[n]);
-          acc_b[n] = fmaf(xb[i], w[i], acc_b[n]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int n = 0; n < NMAX; ++n) {
-    if (n < nc) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        acc_a[n] += __shfl_xor_sync(0xffffffffu, acc_a[n], o);
-        acc_b[n] += __shfl_xor_sync(0xffffffffu, acc_b[n], o);
-      }
-    }
-  }
-  // lane e < E (first token) and lane 16 + e (second token) finish expert e's logit
-  const SelLayout L(E, 1);
-  const int e = lane & 15;
-  const bool second = lane >= 16;
-  const int r = second ? rb : ra;
-  if (e < E && (second ? has_b : has_a)) {
-    float x = 0.f, z = 0.f;
-#pragma unroll
-    for (int n = 0; n < NMAX; ++n) {  // select registers n = e and n = E + e without local memory
-      const float an = second ? acc_b[n] : acc_a[n];
-      if (n == e) x = an;
-      if (noisy && n == E + e) z = an;
-    }
-    const int64_t t = t0 + r;
-    if (b_r) x += b_r[e];
-    if (noisy) x = fmaf(eps[t * E + e], softplus_f32(z), x);
-    if (logits_out) logits_out[t * E + e] = x;
-    sx[L.at(r, e)] = x;
-  }
-  __syncthreads();
-  select_tokens<KP, 1>(sx, zsq, gsc, rows, t0, E, k, score_fn, renorm, n_group, topk_group, sel_bias, idx, gate);
-  __syncthreads();
-  score_column_sums(sx, zsq, rows, E, 1, ppart + static_cast<int64_t>(blockIdx.x) * (E + 1), false);
-}
-
-cudaError_t launch_route_small(const Plan& p, const void* U, const void* Wt, const float* b_r, const float* sel_bias,
-                               const float* eps, float* logits_out, int32_t* idx, float* gate, uint8_t* ws,
-                               cudaStream_t s) {
-  float* ppart = reinterpret_cast<float*>(ws + p.ws_ppart);
-  int32_t* rows = ws_ppart_rows(p, ws);
-  const uint4* u = static_cast<const uint4*>(U);
-  const uint4* w = static_cast<const uint4*>(Wt);
-#define MOE_RS(KPV)                                                                                           \
-  route_small<KPV><<<p.rs_blocks, 256, 0, s>>>(u, w, p.T, p.h, p.E, p.noisy ? 1 : 0, b_r, sel_bias, eps,        \
-                                               logits_out, idx, gate, ppart, rows, p.k, p.score_fn, p.renorm, \
-                                               p.n_group, p.topk_group)
-  if (p.k <= 2)
-    MOE_RS(2);
-  else if (p.k <= 4)
-    MOE_RS(4);
-  else if (p.k <= 8)
-    MOE_RS(8);
-  else
-    MOE_RS(16);
-#undef MOE_RS
-  return cudaGetLastError();
-}
-
 cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const float* b_r, const float* sel_bias,
                          const void* W_noise, const float* eps, const float* logits_in, float* logits_out, int32_t* idx, float* gate,
                          uint8_t* ws, cudaStream_t s, const void* W_r_packed) {
@@ -435,7 +325,6 @@ cudaError_t launch_route(const Plan& p, const void* U, const void* W_r, const fl
       if (e != cudaSuccess) return e;
       Wt = w;
     }
-    if (p.route_small) return launch_route_small(p, U, Wt, b_r, sel_bias, eps, logits_out, idx, gate, ws, s);
     return launch_route_fused(p, U, Wt, b_r, sel_bias, eps, logits_out, idx, gate, ws, s);
   }
   float* part = reinterpret_cast<float*>(ws + p.ws_part);

@@ -1,6 +1,5 @@
 """The fused tensor-core router (bf16, E or 2E <= 256 logit columns) against the oracle, on shapes
-chosen to reach every cluster size (1, 2, 4, 8 CTAs per 128-token tile), the CUDA-core router for at
-most 16 logit columns, both CTA sizes (256 threads,
+chosen to reach every cluster size (1, 2, 4, 8 CTAs per 128-token tile), both CTA sizes (256 threads,
 and 512 when one CTA fills an SM), ragged last tiles (CTAs of a cluster with no rows), h not a
 multiple of 64, several selection passes per CTA, the noisy router,
 group-limited routing with a selection bias, k = 16; and the router from weights packed once
@@ -25,11 +24,7 @@ def _w(name, T, h, E, k, score, renorm=True, noisy=False, bias="none", **kw):
 
 
 FUSED = [
-    _w("cs8_ragged_tile", 130, 1032, 24, 2, SM),                       # 2 tiles; 2 rows in the last: 7 idle CTAs
-    # at most 16 logit columns: the CUDA-core router (two tokens a warp, a ragged last block)
-    _w("small_e8", 1001, 1032, 8, 2, SM, bias="normal"),
-    _w("small_noisy_e8", 333, 264, 8, 1, SM, renorm=False, noisy=True, bias="zipf"),
-    _w("small_e16_sigmoid_groups", 517, 200, 16, 4, SG, sel_bias="normal", n_group=4, topk_group=2),
+    _w("cs8_ragged_tile", 130, 1032, 8, 2, SM),                        # 2 tiles; 2 rows in the last: 7 idle CTAs
     _w("cs4_noisy", 500, 768, 64, 4, SM, renorm=False, noisy=True, bias="zipf"),
     _w("cs2_sigmoid_groups_bias", 1000, 256, 32, 4, SG, bias="normal", sel_bias="normal", n_group=4, topk_group=2),
     _w("cs1_two_passes", 2000, 192, 128, 3, SM),                       # 128 rows, 64 tokens a pass
