@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <stdlib.h>
+
 #include <algorithm>
 
 #include "kernels.h"
@@ -176,6 +178,11 @@ moe_status make_plan(const moe_config* cfg, Plan* p, const char** msg) {
     const int nkb = (q.h + 63) / 64;
     int cs = 1;
     while (cs < 8 && static_cast<int64_t>(q.rf_tiles) * cs * 2 <= 160 && nkb >= cs * 4) cs *= 2;
+    // (MOE_ROUTE_CS=1|2|4|8 overrides the cluster size, for measurement)
+    if (const char* env = getenv("MOE_ROUTE_CS")) {
+      const int v = atoi(env);
+      if (v == 1 || v == 2 || v == 4 || v == 8) cs = v;
+    }
     q.rf_cs = cs;
     // ring depth: four stages when the grid takes several waves (two CTAs share an SM, one's
     // epilogue overlapping the other's loads); when it fits one wave, as deep as ~100 KB allows
