@@ -419,8 +419,10 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   // the first two parts of the chunk's rows start loading now, under the ranking
   const bool copy = X != nullptr && n > 0 && nb > 0;
   const int parts = copy ? (n + nb - 1) / nb : 0;
-  uint8_t* buf0 = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(base_s + (stage_bases ? kE : 0)) + 127) & ~static_cast<uintptr_t>(127));
+  // (128-byte aligned by an offset from the shared array, not an integer round trip, so that the
+  // compiler keeps the reads of the staged rows in the shared state space)
+  uint8_t* after = reinterpret_cast<uint8_t*>(base_s + (stage_bases ? kE : 0));
+  uint8_t* buf0 = after + ((128u - (ptx::smem_u32(after) & 127u)) & 127u);
   uint64_t* bar = reinterpret_cast<uint64_t*>(buf0 + 2 * static_cast<size_t>(nb) * row_bytes);
   const uint8_t* usrc = reinterpret_cast<const uint8_t*>(U) + t0 * row_bytes;
   auto load_part = [&](int q) {  // part q into buffer q & 1 (one thread)

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr uint32_t STAGE = stage_bytes(N);
   constexpr uint32_t TMEM_COLS = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);  // (shared state space kept)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -349,7 +349,9 @@ __global__ void __launch_bounds__(NTH, NTH == 512 ? 1 : 2)
                 float* __restrict__ gate, float* __restrict__ ppart, int32_t* __restrict__ ppart_rows, int k,
                 int score_fn, int renorm, int n_group, int topk_group, int32_t* status) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // the 1024-byte aligned base as an offset from the shared array itself (not an integer round
+  // trip), so that the compiler keeps every access through it in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   const Geometry geo = geometry(N, E, n_group, stages, G, NTH);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + geo.work);
   uint64_t* empty = full + MAX_STAGES;
