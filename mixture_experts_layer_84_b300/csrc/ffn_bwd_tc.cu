@@ -131,7 +131,7 @@ struct Smem {
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* smem_raw) {
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);  // (shared state space kept)
   Smem m;
   m.stages = smem;
   m.full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -544,9 +544,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // store writes the block as whole 128-byte rows of dW[e]; the [E, M, N] tensor map clips rows
     // past M and columns past N.  Before a block is refilled, the previous store has read it.
     const int q = warp & 3;
-    uint8_t* blk = reinterpret_cast<uint8_t*>(
-                       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)) +
-                   W_STAGING_OFFSET + q * 4096;
+    uint8_t* blk = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u) + W_STAGING_OFFSET + q * 4096;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, mt, nt;

@@ -61,6 +61,14 @@ constexpr size_t BAR_BYTES = 128;             // 13 mbarriers + tmem address + f
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + sizeof(int) * (MAX_E + 1);
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
+// Bytes from the start of the dynamic shared array to its first 1024-byte aligned address (what
+// the 128-byte swizzle and the TMA boxes need).  The aligned base is taken as an offset from the
+// array rather than by rounding the pointer as an integer, so that the compiler can keep every
+// access through it in the shared state space (measured: 0.6-5% faster grouped GEMMs).
+__device__ __forceinline__ uint32_t aligned_1024(const uint8_t* smem_raw) {
+  return (1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u;
+}
+
 // Tile `tile` of the list ordered expert by expert; inside an expert, row tiles vary fastest (the
 // CTAs running together share a B tile, and the A segment is re-read once per column tile), or with
 // cols_fastest the column tiles do (they share an A row tile, and the expert's B is re-read once per
@@ -175,7 +183,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
   constexpr int BKE = FP8 ? 2 * BK : BK;        // K elements per stage (128 bytes of every row)
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + aligned_1024(smem_raw);
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
@@ -493,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   static_assert(SWIGLU || !GATHER, "the gathered A operand is the up-projection's");
   constexpr int TILE_N = SWIGLU ? BN / 2 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + aligned_1024(smem_raw);
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
   uint64_t* empty = full + P_STAGES;
@@ -861,7 +869,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   constexpr int WT = SWIGLU ? 128 : 256;  // output columns per pair tile
   constexpr int BKE = FP8 ? 2 * BK : BK;  // K elements per stage (128 bytes of every row)
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + aligned_1024(smem_raw);
   uint8_t* stages = smem;
   float* xch = reinterpret_cast<float*>(smem + S_STAGES * S_STAGE_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S_STAGES * S_STAGE_BYTES + S_XCH_FLOATS * 4);
