@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(NTH, NTH == 512 ? 1 : 2)
       }
       __syncthreads();
       select_tokens<KP, G>(sx, zsq, gsc, rows, row0 + p0, E, k, score_fn, renorm, n_group, topk_group,
-                           sel_bias ? selb_s : nullptr, idx, gate);
+                           sel_bias ? selb_s : nullptr, idx, gate, pos_s);
       __syncthreads();
       score_column_sums_split(sx, zsq, rows, E, G, colsum, colpart, p0 > 0);
       __syncthreads();

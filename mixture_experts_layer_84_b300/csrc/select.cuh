@@ -77,11 +77,12 @@ struct SelLayout {
 // experts' scores.  Then the normalised scores (for P) are written back in place and LSE^2 into
 // zsq[r].  Every thread of the block must call this (the shuffles span whole warps).  Scores use
 // the fast exponential (a few ulps; the selection compares logits, or score + bias with a margin
-// far above that).
+// far above that), and the normalised scores one reciprocal of the denominator per token.
+// pos (nullable): each expert's position in a staged row, SelLayout::at(0, e), in shared memory.
 template <int KP, int G>
 __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64_t t0, int E, int k, int score_fn,
                               int renorm, int n_group, int topk_group, const float* __restrict__ sel_bias,
-                              int32_t* __restrict__ idx, float* __restrict__ gate) {
+                              int32_t* __restrict__ idx, float* __restrict__ gate, const int* pos = nullptr) {
   const SelLayout L(E, G);
   const int r = threadIdx.x / G, g = threadIdx.x % G;
   const bool tok = r < rows;
@@ -121,7 +122,7 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
 #pragma unroll
         for (int j = 0; j < KP; ++j) best[j] = -INFINITY;
         for (int e = q * gsz; e < (q + 1) * gsz; ++e) {
-          const float x = sx[L.at(r, e)];
+          const float x = sx[pos ? r * L.LD + pos[e] : L.at(r, e)];
           float a = softmax ? __expf(x - mx) / denom : sigmoid_f32(x);
           if (sel_bias) a += sel_bias[e];
 #pragma unroll
@@ -210,7 +211,7 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
     for (int j = 0; j < KP; ++j) {
       sel_s[j] = 0.f;
       if (j < k) {
-        const float x = sx[L.at(r, ti[j])];
+        const float x = sx[pos ? r * L.LD + pos[ti[j]] : L.at(r, ti[j])];
         sel_s[j] = softmax ? __expf(x - mx) / denom : sigmoid_f32(x);
         sel_sum += sel_s[j];
       }
@@ -227,9 +228,10 @@ __device__ void select_tokens(float* sx, float* zsq, float* gsc, int rows, int64
   // every lane has read what it needs from the row before any lane overwrites its chunk
   __syncwarp();
   if (tok) {
+    const float inv = 1.f / denom;
     for (int e = e0; e < e1; ++e) {
       const float x = chunk[e - e0];
-      chunk[e - e0] = (softmax ? __expf(x - mx) : sigmoid_f32(x)) / denom;
+      chunk[e - e0] = (softmax ? __expf(x - mx) : sigmoid_f32(x)) * inv;
     }
     if (g == 0) {
       const float lse = mx + logf(sum_exp);
