@@ -296,7 +296,7 @@ cudaError_t launch_route_logits_tc(const Plan& p, const void* U, const void* W_r
 // remote stores into distributed shared memory.  After a second barrier each CTA adds the CS slices
 // of its logits in rank order (run-to-run identical) from its own shared memory, then the bias
 // and the noise eps * softplus(noise logit), stages them for select_tokens (select.cuh) in passes
-// of 256 / G tokens, and adds its per-expert score sums and LSE^2 sum into one ppart row.
+// of NTH / G tokens, and adds its per-expert score sums and LSE^2 sum into one ppart row.
 namespace rfu {
 
 using namespace rtc;
@@ -586,13 +586,29 @@ template <int KP>
 cudaError_t launch_fused_kp(const Plan& p, const CUtensorMap& tmU, const CUtensorMap& tmW, const float* b_r,
                             const float* sel_bias, const float* eps, float* logits_out, int32_t* idx, float* gate,
                             float* ppart, int32_t* rows, int32_t* status, cudaStream_t s) {
-  // 512 threads: twice the lanes per token (half the experts per lane) for the same tokens a pass
+  // 512 threads: twice the lanes per token (half the experts per lane) when the CTA's rows still
+  // fit one selection pass that way; otherwise the usual lanes, so that the rows take one pass of
+  // 512 / G tokens instead of two (the 128 rows of a one-CTA tile of the 128-expert router),
+  // while that fits shared memory
   if (p.rf_threads == 512) {
-    switch (select_lanes_for(p.E)) {
+    const int G = select_lanes_for(p.E);
+    const int R = 128 / p.rf_cs;
+    const bool wide = R <= 512 / (2 * G) ||
+                      geometry(p.route_tc_n, p.E, p.n_group, p.rf_stages, G, 512).smem > 232448;
+    if (wide) {
+      switch (G) {
 #define MOE_RFU_G2(gg, g2) \
   case gg: return launch_fused_g<KP, g2, 512>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
-      MOE_RFU_G2(1, 2) MOE_RFU_G2(2, 4) MOE_RFU_G2(4, 8) MOE_RFU_G2(8, 16)
+        MOE_RFU_G2(1, 2) MOE_RFU_G2(2, 4) MOE_RFU_G2(4, 8) MOE_RFU_G2(8, 16)
 #undef MOE_RFU_G2
+      }
+    } else {
+      switch (G) {
+#define MOE_RFU_G1(gg) \
+  case gg: return launch_fused_g<KP, gg, 512>(p, tmU, tmW, b_r, sel_bias, eps, logits_out, idx, gate, ppart, rows, status, s);
+        MOE_RFU_G1(1) MOE_RFU_G1(2) MOE_RFU_G1(4) MOE_RFU_G1(8)
+#undef MOE_RFU_G1
+      }
     }
     return cudaErrorInvalidValue;
   }
@@ -607,9 +623,12 @@ cudaError_t launch_fused_kp(const Plan& p, const CUtensorMap& tmU, const CUtenso
 
 }  // namespace rfu
 
-size_t fused_router_smem(int N, int E, int n_group, int stages, int threads) {
+size_t fused_router_smem(int N, int E, int n_group, int stages, int threads, int cs) {
   const int G = select_lanes_for(E);
-  return rfu::geometry(N, E, n_group, stages, threads == 512 && G < 32 ? 2 * G : G, threads).smem;
+  if (threads != 512 || G >= 32) return rfu::geometry(N, E, n_group, stages, G, threads).smem;
+  const size_t narrow = rfu::geometry(N, E, n_group, stages, G, 512).smem;
+  const bool wide = 128 / cs <= 512 / (2 * G) || narrow > 232448;
+  return wide ? rfu::geometry(N, E, n_group, stages, 2 * G, 512).smem : narrow;
 }
 
 cudaError_t launch_pack_router(const Plan& p, const void* W_r, const void* W_noise, void* Wt, cudaStream_t s) {

@@ -27,10 +27,10 @@ FUSED = [
     _w("cs8_ragged_tile", 130, 1032, 8, 2, SM),                        # 2 tiles; 2 rows in the last: 7 idle CTAs
     _w("cs4_noisy", 500, 768, 64, 4, SM, renorm=False, noisy=True, bias="zipf"),
     _w("cs2_sigmoid_groups_bias", 1000, 256, 32, 4, SG, bias="normal", sel_bias="normal", n_group=4, topk_group=2),
-    _w("cs1_two_passes", 2000, 192, 128, 3, SM),                       # 128 rows, 64 tokens a pass
+    _w("cs1_one_pass_512", 2000, 192, 128, 3, SM),                     # 128 rows in one pass (512 threads, 4 lanes)
     _w("cs4_e256_k16", 300, 512, 256, 16, SG),
     _w("e5_narrow", 260, 640, 5, 2, SM, bias="normal"),
-    _w("noisy_e128_two_passes", 700, 320, 128, 1, SM, renorm=False, noisy=True, bias="zipf"),
+    _w("noisy_e128_one_pass", 700, 320, 128, 1, SM, renorm=False, noisy=True, bias="zipf"),
     # more CTAs than SMs: the 256-thread kernel, 128 rows in two passes of 64 tokens
     _w("e128_many_tiles_256_threads", 19200, 128, 128, 2, SM),
 ]
