@@ -92,8 +92,6 @@ cudaError_t launch_pack_router(const Plan& p, const void* W_r, const void* W_noi
 cudaError_t launch_route_fused(const Plan& p, const void* U, const void* Wt, const float* b_r, const float* sel_bias,
                                const float* eps, float* logits_out, int32_t* idx, float* gate, uint8_t* ws,
                                cudaStream_t s);
-// Dynamic shared memory of one fused-router CTA.
-size_t fused_router_smem(int N, int E, int n_group, int stages, int threads, int cs);
 
 // Router slice sums U W_r (and U W_noise) on the tensor cores (bf16, p.route_tc_n > 0).
 cudaError_t launch_route_logits_tc(const Plan& p, const void* U, const void* W_r, const void* W_noise, float* part,

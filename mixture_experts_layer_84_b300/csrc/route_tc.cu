@@ -623,14 +623,6 @@ cudaError_t launch_fused_kp(const Plan& p, const CUtensorMap& tmU, const CUtenso
 
 }  // namespace rfu
 
-size_t fused_router_smem(int N, int E, int n_group, int stages, int threads, int cs) {
-  const int G = select_lanes_for(E);
-  if (threads != 512 || G >= 32) return rfu::geometry(N, E, n_group, stages, G, threads).smem;
-  const size_t narrow = rfu::geometry(N, E, n_group, stages, G, 512).smem;
-  const bool wide = 128 / cs <= 512 / (2 * G) || narrow > 232448;
-  return wide ? rfu::geometry(N, E, n_group, stages, 2 * G, 512).smem : narrow;
-}
-
 cudaError_t launch_pack_router(const Plan& p, const void* W_r, const void* W_noise, void* Wt, cudaStream_t s) {
   const int N = p.route_tc_n;
   rtc::route_pack_wt<<<dim3((N + 31) / 32, (p.h + 31) / 32), dim3(32, 8), 0, s>>>(
