@@ -190,11 +190,18 @@ def launches_per_step(w: W.Workload, gather: bool = False, fp8: bool = False) ->
     fused_router = w.dtype == W.BF16 and (2 * w.E if w.noisy else w.E) <= 256
     route = 1 if fused_router else 2       # the fused router (weights packed beforehand), or logits + selection
     if w.priority == W.PRIORITY_CHOICE_MAJOR:
-        dispatch = 3                       # histograms, column scans, then slots + row copy (no copy when gathering)
+        # histograms, column scans (not when the placement blocks add up histograms of at most 8192
+        # counts themselves), then slots + row copy (no copy when gathering); token chunks of 8 .. 256
+        tc = 8
+        while tc < 256 and tc * 2 * 148 < w.T:
+            tc *= 2
+        meta = 2 if -(-w.T // tc) * w.k * w.E <= 8192 else 3
+        dispatch = meta
     else:
-        dispatch = 3 if gather else 4      # count, scan, assign (, scatter)
+        meta = 3                           # count, scan, assign
+        dispatch = 3 if gather else 4      # (, scatter)
     if fp8:
-        dispatch = 3 + 1                   # the metadata only (no bf16 copy), then the E4M3 row copy
+        dispatch = meta + 1                # the metadata only (no bf16 copy), then the E4M3 row copy
     ffn, combine = 2, 1                    # two GEMMs; rows and statistics
     return route + dispatch + ffn + 2 * w.n_shared + combine
 

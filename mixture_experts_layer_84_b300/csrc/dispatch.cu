@@ -13,7 +13,8 @@
 // of earlier pairs with the same expert -- an exclusive prefix count, so it is
 // computed with scans, never with an atomic whose order could leak into the
 // result.  Choice-major priority (the default) takes three launches, dispatch_hist,
-// dispatch_colscan and dispatch_place, described where they are defined.  Token-major
+// dispatch_colscan and dispatch_place (two when the histograms are small: no column scan),
+// described where they are defined.  Token-major
 // priority and the workspace-free entry point take these four:
 //   dispatch_count   per chunk of positions, a histogram over experts;
 //   dispatch_scan    one block: per expert, the exclusive prefix over chunks,
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 }
 
 // ---------------------------------------------------------------------------------------------
-// Choice-major dispatch in three launches.  Pairs are grouped into token chunks of TC tokens; with
+// Choice-major dispatch in three launches (or two).  Pairs are grouped into token chunks of TC tokens; with
 // every token's first choice before any second choice, the slot of pair (t, j) choosing expert e is
 //   sum_{j' < j} cnt[j'][e]  +  sum_{chunks c' < c(t)} h[c'][j][e]  +  #{t' < t in t's chunk : idx[t'][j] = e},
 // cnt[j][e] being the pairs of choice j that chose e over all tokens and h[c][j][e] those of chunk c.
@@ -263,11 +264,18 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 //                   in large bulk loads, two buffers deep; then each warp writes 512-byte pieces
 //                   of the staged rows to all of their kept rows with coalesced 16-byte stores
 //                   (skipped when X is NULL).
+// When the histograms are small (chunks x k x E <= 8192 counts), there is no column-scan launch:
+// every placement block adds the raw chunk counts itself -- the chunks before its own, and all of
+// them -- forms the choice bases and the offsets in shared memory, and block 0 writes the routed
+// and kept counts, the offsets and n_dropped.  Integer sums: the same values as the scan's.
 constexpr int PLACE_THREADS = 256;
 constexpr size_t COPY_SMEM_BYTES = 100 * 1024;       // shared memory of one dispatch_place block: two fit an SM
 constexpr uint64_t COPY_WAIT_LIMIT_NS = 2000000000ull;
 constexpr int PLACE_WARPS = PLACE_THREADS / 32;
 constexpr int HIST_THREADS = 1024;
+// chunks x k x E counts each placement block adds itself (measured: the 8-expert shape's 4096 take
+// its dispatch from 28.7 to 20.5 us; the 128-expert shape's 32768 gained nothing over the scan)
+constexpr int64_t SELF_SCAN_MAX = 8192;
 
 __global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __restrict__ idx, int64_t T, int k,
                                                               int E, int tc, int32_t* __restrict__ hist,
@@ -395,16 +403,21 @@ __global__ void __launch_bounds__(256) dispatch_colscan(int32_t* __restrict__ hi
   }
 }
 
+// stage_bases: 0 reads the chunk's bases from the scanned histogram, 1 stages them in shared memory,
+// 2 computes them from the raw chunk counts (no column scan; see above).
 __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     const int32_t* __restrict__ idx, int64_t T, int k, int E, int tc, int n_chunks, int64_t C,
-    const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+    const int32_t* __restrict__ hist, int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
     int32_t* __restrict__ row_token, const void* __restrict__ U, void* __restrict__ X, uint32_t row_bytes, int nb,
-    int32_t* status, int stage_bases) {
+    int32_t* status, int stage_bases, int32_t* __restrict__ counts_routed, int32_t* __restrict__ counts_kept,
+    int64_t* __restrict__ n_dropped) {
   extern __shared__ int32_t sm[];
   int32_t* wc = sm;                          // [PLACE_WARPS][E]
   int32_t* rows_s = sm + PLACE_WARPS * E;    // [tc][k]
   int32_t* idx_s = rows_s + tc * k;          // [tc][k]: the chunk's expert ids
   int32_t* base_s = idx_s + tc * k;          // [k][E]: chunk prefix + choice base (when staged)
+  int32_t* tot_s = base_s + k * E;           // self scan: [k][E] column totals
+  int32_t* off_s = tot_s + k * E;            // self scan: [E + 1] offsets
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int kE = k * E;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tc;
@@ -421,7 +434,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   const int parts = copy ? (n + nb - 1) / nb : 0;
   // (128-byte aligned by an offset from the shared array, not an integer round trip, so that the
   // compiler keeps the reads of the staged rows in the shared state space)
-  uint8_t* after = reinterpret_cast<uint8_t*>(base_s + (stage_bases ? kE : 0));
+  uint8_t* after = reinterpret_cast<uint8_t*>(base_s + (stage_bases == 2 ? 2 * kE + E + 1 : stage_bases ? kE : 0));
   uint8_t* buf0 = after + ((128u - (ptx::smem_u32(after) & 127u)) & 127u);
   uint64_t* bar = reinterpret_cast<uint64_t*>(buf0 + 2 * static_cast<size_t>(nb) * row_bytes);
   const uint8_t* usrc = reinterpret_cast<const uint8_t*>(U) + t0 * row_bytes;
@@ -441,8 +454,105 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   }
   // everything the ranking reads, staged with loads that are all in flight together
   for (int i = threadIdx.x; i < n * k; i += blockDim.x) idx_s[i] = idx[t0 * k + i];
-  if (stage_bases)
+  if (stage_bases == 1)
     for (int i = threadIdx.x; i < kE; i += blockDim.x) base_s[i] = base[i] + cbase[i];
+  if (stage_bases == 2) {
+    for (int i = threadIdx.x; i < kE; i += blockDim.x) {
+      base_s[i] = 0;
+      tot_s[i] = 0;
+    }
+    __syncthreads();
+    // columns (j, e): `parts` threads each add every parts-th chunk, before this one and all; four
+    // columns a thread with 16-byte loads when k E allows (the chunk rows are 16-byte aligned then)
+    const int b = static_cast<int>(blockIdx.x);
+    if ((kE & 3) == 0) {
+      const int q4 = kE / 4;
+      const int parts = q4 < PLACE_THREADS ? PLACE_THREADS / q4 : 1;
+      for (int t = threadIdx.x; t < parts * q4; t += blockDim.x) {
+        const int col = (t % q4) * 4, part = t / q4;
+        int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+#pragma unroll 8
+        for (int c = part; c < n_chunks; c += parts) {
+          const int4 v = *reinterpret_cast<const int4*>(hist + static_cast<int64_t>(c) * kE + col);
+          tot.x += v.x;
+          tot.y += v.y;
+          tot.z += v.z;
+          tot.w += v.w;
+          if (c < b) {
+            pre.x += v.x;
+            pre.y += v.y;
+            pre.z += v.z;
+            pre.w += v.w;
+          }
+        }
+        atomicAdd(&base_s[col], pre.x);  // integer counts: the order of the adds does not matter
+        atomicAdd(&base_s[col + 1], pre.y);
+        atomicAdd(&base_s[col + 2], pre.z);
+        atomicAdd(&base_s[col + 3], pre.w);
+        atomicAdd(&tot_s[col], tot.x);
+        atomicAdd(&tot_s[col + 1], tot.y);
+        atomicAdd(&tot_s[col + 2], tot.z);
+        atomicAdd(&tot_s[col + 3], tot.w);
+      }
+    } else {
+      const int parts = kE < PLACE_THREADS ? PLACE_THREADS / kE : 1;
+      for (int t = threadIdx.x; t < parts * kE; t += blockDim.x) {
+        const int col = t % kE, part = t / kE;
+        int32_t pre = 0, tot = 0;
+#pragma unroll 4
+        for (int c = part; c < n_chunks; c += parts) {
+          const int32_t v = hist[static_cast<int64_t>(c) * kE + col];
+          tot += v;
+          pre += c < b ? v : 0;
+        }
+        atomicAdd(&base_s[col], pre);
+        atomicAdd(&tot_s[col], tot);
+      }
+    }
+    __syncthreads();
+    // choice bases (the pairs of earlier choices per expert), routed and kept counts
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int32_t run = 0;
+      for (int j = 0; j < k; ++j) {
+        base_s[j * E + e] += run;
+        run += tot_s[j * E + e];
+      }
+      const int32_t kept = static_cast<int32_t>(min(static_cast<int64_t>(run), C));
+      off_s[e] = kept;
+      if (blockIdx.x == 0) {
+        counts_routed[e] = run;
+        counts_kept[e] = kept;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {  // offsets = exclusive scan of the kept counts
+      const int per = (E + 31) / 32;
+      const int lo = min(E, lane * per), hi = min(E, lo + per);
+      int32_t s = 0;
+      for (int i = lo; i < hi; ++i) s += off_s[i];
+      int32_t incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int32_t run = incl - s;
+      for (int i = lo; i < hi; ++i) {
+        const int32_t v = off_s[i];
+        off_s[i] = run;
+        if (blockIdx.x == 0) offsets[i] = run;
+        run += v;
+      }
+      const int32_t A = __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 0) {
+        off_s[E] = A;
+        if (blockIdx.x == 0) {
+          offsets[E] = A;
+          *n_dropped = T * k - A;
+        }
+      }
+    }
+  }
   __syncthreads();
   for (int j = 0; j < k; ++j) {
     for (int i = threadIdx.x; i < PLACE_WARPS * E; i += blockDim.x) wc[i] = 0;
@@ -487,7 +597,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
         const int64_t t = t0 + r;
         int32_t row = -1;
         if (e >= 0 && slot < C) {
-          row = offsets[e] + slot;
+          row = (stage_bases == 2 ? off_s[e] : offsets[e]) + slot;
           row_token[row] = static_cast<int32_t>(t);
         }
         slot_row[t * k + j] = row;
@@ -564,14 +674,20 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int cols = p.k * p.E;
-    dispatch_colscan<<<(cols + 7) / 8, 256, 0, s>>>(hist, p.dp_chunks, p.k, p.E, p.C, p.Tk, ticket, counts_routed,
-                                                     counts_kept, offsets, n_dropped);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // small histograms: the placement blocks scan them themselves (no column-scan launch)
+    const bool self_scan = static_cast<int64_t>(p.dp_chunks) * cols <= SELF_SCAN_MAX;
+    if (!self_scan) {
+      dispatch_colscan<<<(cols + 7) / 8, 256, 0, s>>>(hist, p.dp_chunks, p.k, p.E, p.C, p.Tk, ticket, counts_routed,
+                                                       counts_kept, offsets, n_dropped);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
     const uint32_t row_bytes = static_cast<uint32_t>(p.h) * (p.bf16 ? 2 : 4);
-    const int stage_bases = p.k * p.E <= 4096 ? 1 : 0;  // the chunk's bases fit 16 KB of shared memory
+    // the chunk's bases in shared memory when they fit 16 KB (self scan: with the totals and offsets)
+    const int stage_bases = self_scan ? 2 : p.k * p.E <= 4096 ? 1 : 0;
+    const size_t staged = stage_bases == 2 ? 2 * static_cast<size_t>(cols) + p.E + 1 : stage_bases ? cols : 0;
     const size_t meta = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + 2 * static_cast<size_t>(p.dp_tc) * p.k +
-                                           (stage_bases ? static_cast<size_t>(p.k) * p.E : 0));
+                                           staged);
     // two row buffers in what is left of COPY_SMEM_BYTES (at most the chunk each); rows too wide for
     // two buffers in any block are copied by dispatch_scatter after the placement instead
     const size_t room = meta + 128 + 16 < COPY_SMEM_BYTES ? COPY_SMEM_BYTES - meta - 128 - 16 : 0;
@@ -586,7 +702,8 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
     }
     dispatch_place<<<p.dp_chunks, PLACE_THREADS, psm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, p.dp_chunks, p.C, hist,
                                                             offsets, slot_row, row_token, U, nb > 0 ? X : nullptr,
-                                                            row_bytes, nb, status, stage_bases);
+                                                            row_bytes, nb, status, stage_bases, counts_routed,
+                                                            counts_kept, n_dropped);
     e = cudaGetLastError();
     if (e != cudaSuccess || !scatter_after) return e;
     const int vpr = static_cast<int>(row_bytes / 16);

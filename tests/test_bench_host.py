@@ -38,21 +38,29 @@ def test_stage_work_fp8_and_gather_variants():
     assert g["dispatch"]["bytes"] == w.T * w.k * 12 and g["ffn"] == base["ffn"]
 
 
-@pytest.mark.parametrize("w,expected", [(W.MIXTRAL, 7), (W.TINY_FP32, 8), (W.DSV3_SHARED, 9),
-                                        (W.SWITCH, 7), (W.MIXTRAL.replace(name="empty", T=0), 2)])
-def test_launches_per_step(w, expected):
+# (workload, choice-major, token-major, token-major gathered, FP8 choice-major, FP8 token-major)
+@pytest.mark.parametrize("w,cm,tm,tm_g,f8,tm_f8", [
+    (W.MIXTRAL, 6, 8, 7, 7, 8),        # 256 chunks x 16 columns: no column-scan launch
+    (W.TINY_FP32, 7, 9, 8, 8, 9),      # two router launches (float32), 32 chunks x 16 columns
+    (W.DSV3_SHARED, 9, 10, 9, 10, 10), # 256 x 2048 columns: the column scan; two shared-expert GEMMs
+    (W.SWITCH, 7, 8, 7, 8, 8),         # 256 x 128 columns: the column scan
+])
+def test_launches_per_step(w, cm, tm, tm_g, f8, tm_f8):
     """route (the fused tensor-core router from weights packed beforehand, else logits +
-    selection), dispatch (histograms, column scans, then slots + row copy), two GEMMs per routed and
-    per shared expert block, combine with statistics; token-major dispatch takes count, scan,
-    assign and scatter."""
-    assert bench.launches_per_step(w) == expected
-    if w.T:
-        assert bench.launches_per_step(w, gather=True) == expected
-        tm = w.replace(priority=W.PRIORITY_TOKEN_MAJOR)
-        assert bench.launches_per_step(tm) == expected + 1
-        assert bench.launches_per_step(tm, gather=True) == expected
-        assert bench.launches_per_step(w, fp8=True) == expected + 1
-        assert bench.launches_per_step(tm, fp8=True) == expected + 1
+    selection), dispatch (histograms, column scans unless the histograms hold at most 8192 counts,
+    then slots + row copy), two GEMMs per routed and per shared expert block, combine with
+    statistics; token-major dispatch takes count, scan, assign and scatter."""
+    t = w.replace(priority=W.PRIORITY_TOKEN_MAJOR)
+    assert bench.launches_per_step(w) == cm
+    assert bench.launches_per_step(w, gather=True) == cm
+    assert bench.launches_per_step(t) == tm
+    assert bench.launches_per_step(t, gather=True) == tm_g
+    assert bench.launches_per_step(w, fp8=True) == f8
+    assert bench.launches_per_step(t, fp8=True) == tm_f8
+
+
+def test_launches_per_step_empty_batch():
+    assert bench.launches_per_step(W.MIXTRAL.replace(name="empty", T=0)) == 2
 
 
 def test_ffn_tiles_rule(monkeypatch):
