@@ -190,12 +190,14 @@ def launches_per_step(w: W.Workload, gather: bool = False, fp8: bool = False) ->
     fused_router = w.dtype == W.BF16 and (2 * w.E if w.noisy else w.E) <= 256
     route = 1 if fused_router else 2       # the fused router (weights packed beforehand), or logits + selection
     if w.priority == W.PRIORITY_CHOICE_MAJOR:
-        # histograms, column scans (not when the placement blocks add up histograms of at most 8192
-        # counts themselves), then slots + row copy (no copy when gathering); token chunks of 8 .. 256
+        # histograms, column scans, then slots + row copy (no copy when gathering); no column scan
+        # when the placement blocks add up histograms of at most 8192 counts themselves, and no
+        # histograms either when they count at most 8192 expert ids themselves (token chunks of
+        # 8 .. 256 tokens)
         tc = 8
         while tc < 256 and tc * 2 * 148 < w.T:
             tc *= 2
-        meta = 2 if -(-w.T // tc) * w.k * w.E <= 8192 else 3
+        meta = 1 if w.T * w.k <= 8192 else 2 if -(-w.T // tc) * w.k * w.E <= 8192 else 3
         dispatch = meta
     else:
         meta = 3                           # count, scan, assign

@@ -13,7 +13,7 @@
 // of earlier pairs with the same expert -- an exclusive prefix count, so it is
 // computed with scans, never with an atomic whose order could leak into the
 // result.  Choice-major priority (the default) takes three launches, dispatch_hist,
-// dispatch_colscan and dispatch_place (two when the histograms are small: no column scan),
+// dispatch_colscan and dispatch_place (two when the histograms are small, one when the batch is),
 // described where they are defined.  Token-major
 // priority and the workspace-free entry point take these four:
 //   dispatch_count   per chunk of positions, a histogram over experts;
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 }
 
 // ---------------------------------------------------------------------------------------------
-// Choice-major dispatch in three launches (or two).  Pairs are grouped into token chunks of TC tokens; with
+// Choice-major dispatch in three launches (two or one for small histograms or batches).  Pairs are grouped into token chunks of TC tokens; with
 // every token's first choice before any second choice, the slot of pair (t, j) choosing expert e is
 //   sum_{j' < j} cnt[j'][e]  +  sum_{chunks c' < c(t)} h[c'][j][e]  +  #{t' < t in t's chunk : idx[t'][j] = e},
 // cnt[j][e] being the pairs of choice j that chose e over all tokens and h[c][j][e] those of chunk c.
@@ -267,7 +267,10 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 // When the histograms are small (chunks x k x E <= 8192 counts), there is no column-scan launch:
 // every placement block adds the raw chunk counts itself -- the chunks before its own, and all of
 // them -- forms the choice bases and the offsets in shared memory, and block 0 writes the routed
-// and kept counts, the offsets and n_dropped.  Integer sums: the same values as the scan's.
+// and kept counts, the offsets and n_dropped.  Integer sums: the same values as the scan's.  When
+// the batch itself is small (T k <= 8192 expert ids) there is no histogram launch either: every
+// placement block counts all the ids (those before its chunk, and all of them), so the dispatch is
+// one launch.
 constexpr int PLACE_THREADS = 256;
 constexpr size_t COPY_SMEM_BYTES = 100 * 1024;       // shared memory of one dispatch_place block: two fit an SM
 constexpr uint64_t COPY_WAIT_LIMIT_NS = 2000000000ull;
@@ -276,6 +279,7 @@ constexpr int HIST_THREADS = 1024;
 // chunks x k x E counts each placement block adds itself (measured: the 8-expert shape's 4096 take
 // its dispatch from 28.7 to 20.5 us; the 128-expert shape's 32768 gained nothing over the scan)
 constexpr int64_t SELF_SCAN_MAX = 8192;
+constexpr int64_t SELF_COUNT_MAX = 8192;  // T k expert ids each placement block counts itself
 
 __global__ void __launch_bounds__(HIST_THREADS) dispatch_hist(const int32_t* __restrict__ idx, int64_t T, int k,
                                                               int E, int tc, int32_t* __restrict__ hist,
@@ -404,7 +408,8 @@ __global__ void __launch_bounds__(256) dispatch_colscan(int32_t* __restrict__ hi
 }
 
 // stage_bases: 0 reads the chunk's bases from the scanned histogram, 1 stages them in shared memory,
-// 2 computes them from the raw chunk counts (no column scan; see above).
+// 2 computes them from the raw chunk counts (no column scan), 3 from the expert ids themselves (no
+// histogram either; see above).
 __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     const int32_t* __restrict__ idx, int64_t T, int k, int E, int tc, int n_chunks, int64_t C,
     const int32_t* __restrict__ hist, int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   const int parts = copy ? (n + nb - 1) / nb : 0;
   // (128-byte aligned by an offset from the shared array, not an integer round trip, so that the
   // compiler keeps the reads of the staged rows in the shared state space)
-  uint8_t* after = reinterpret_cast<uint8_t*>(base_s + (stage_bases == 2 ? 2 * kE + E + 1 : stage_bases ? kE : 0));
+  uint8_t* after = reinterpret_cast<uint8_t*>(base_s + (stage_bases >= 2 ? 2 * kE + E + 1 : stage_bases ? kE : 0));
   uint8_t* buf0 = after + ((128u - (ptx::smem_u32(after) & 127u)) & 127u);
   uint64_t* bar = reinterpret_cast<uint64_t*>(buf0 + 2 * static_cast<size_t>(nb) * row_bytes);
   const uint8_t* usrc = reinterpret_cast<const uint8_t*>(U) + t0 * row_bytes;
@@ -456,7 +461,8 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
   for (int i = threadIdx.x; i < n * k; i += blockDim.x) idx_s[i] = idx[t0 * k + i];
   if (stage_bases == 1)
     for (int i = threadIdx.x; i < kE; i += blockDim.x) base_s[i] = base[i] + cbase[i];
-  if (stage_bases == 2) {
+  // (stage_bases 2 and 3 below)
+  if (stage_bases >= 2) {
     for (int i = threadIdx.x; i < kE; i += blockDim.x) {
       base_s[i] = 0;
       tot_s[i] = 0;
@@ -465,7 +471,22 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
     // columns (j, e): `parts` threads each add every parts-th chunk, before this one and all; four
     // columns a thread with 16-byte loads when k E allows (the chunk rows are 16-byte aligned then)
     const int b = static_cast<int>(blockIdx.x);
-    if ((kE & 3) == 0) {
+    if (stage_bases == 3) {
+      // every expert id of the batch: position p = t k + j lies before the chunk when p < t0 k
+      const int Tk = static_cast<int>(T) * k, p0 = static_cast<int>(t0) * k;
+      bool bad = false;
+      for (int i = threadIdx.x; i < Tk; i += blockDim.x) {
+        const int e = idx[i];
+        if (e < 0 || e >= E) {
+          bad = true;
+          continue;
+        }
+        const int col = (i % k) * E + e;
+        atomicAdd(&tot_s[col], 1);  // integer counts: the order of the adds does not matter
+        if (i < p0) atomicAdd(&base_s[col], 1);
+      }
+      if (bad && b == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+    } else if ((kE & 3) == 0) {
       const int q4 = kE / 4;
       const int parts = q4 < PLACE_THREADS ? PLACE_THREADS / q4 : 1;
       for (int t = threadIdx.x; t < parts * q4; t += blockDim.x) {
@@ -597,7 +618,7 @@ __global__ void __launch_bounds__(PLACE_THREADS) dispatch_place(
         const int64_t t = t0 + r;
         int32_t row = -1;
         if (e >= 0 && slot < C) {
-          row = (stage_bases == 2 ? off_s[e] : offsets[e]) + slot;
+          row = (stage_bases >= 2 ? off_s[e] : offsets[e]) + slot;
           row_token[row] = static_cast<int32_t>(t);
         }
         slot_row[t * k + j] = row;
@@ -670,12 +691,17 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
                                                  static_cast<int>(hsm));
       if (e != cudaSuccess) return e;
     }
-    dispatch_hist<<<p.dp_chunks, HIST_THREADS, hsm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, hist, status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // small batches: the placement blocks count the expert ids themselves (one launch)
+    const bool self_count = p.Tk <= SELF_COUNT_MAX;
+    cudaError_t e = cudaSuccess;
+    if (!self_count) {
+      dispatch_hist<<<p.dp_chunks, HIST_THREADS, hsm, s>>>(idx, p.T, p.k, p.E, p.dp_tc, hist, status);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
     const int cols = p.k * p.E;
     // small histograms: the placement blocks scan them themselves (no column-scan launch)
-    const bool self_scan = static_cast<int64_t>(p.dp_chunks) * cols <= SELF_SCAN_MAX;
+    const bool self_scan = self_count || static_cast<int64_t>(p.dp_chunks) * cols <= SELF_SCAN_MAX;
     if (!self_scan) {
       dispatch_colscan<<<(cols + 7) / 8, 256, 0, s>>>(hist, p.dp_chunks, p.k, p.E, p.C, p.Tk, ticket, counts_routed,
                                                        counts_kept, offsets, n_dropped);
@@ -684,8 +710,8 @@ cudaError_t launch_dispatch(const Plan& p, const void* U, const int32_t* idx, in
     }
     const uint32_t row_bytes = static_cast<uint32_t>(p.h) * (p.bf16 ? 2 : 4);
     // the chunk's bases in shared memory when they fit 16 KB (self scan: with the totals and offsets)
-    const int stage_bases = self_scan ? 2 : p.k * p.E <= 4096 ? 1 : 0;
-    const size_t staged = stage_bases == 2 ? 2 * static_cast<size_t>(cols) + p.E + 1 : stage_bases ? cols : 0;
+    const int stage_bases = self_count ? 3 : self_scan ? 2 : p.k * p.E <= 4096 ? 1 : 0;
+    const size_t staged = stage_bases >= 2 ? 2 * static_cast<size_t>(cols) + p.E + 1 : stage_bases ? cols : 0;
     const size_t meta = sizeof(int32_t) * (static_cast<size_t>(PLACE_WARPS) * p.E + 2 * static_cast<size_t>(p.dp_tc) * p.k +
                                            staged);
     // two row buffers in what is left of COPY_SMEM_BYTES (at most the chunk each); rows too wide for

@@ -40,15 +40,17 @@ def test_stage_work_fp8_and_gather_variants():
 
 # (workload, choice-major, token-major, token-major gathered, FP8 choice-major, FP8 token-major)
 @pytest.mark.parametrize("w,cm,tm,tm_g,f8,tm_f8", [
-    (W.MIXTRAL, 6, 8, 7, 7, 8),        # 256 chunks x 16 columns: no column-scan launch
-    (W.TINY_FP32, 7, 9, 8, 8, 9),      # two router launches (float32), 32 chunks x 16 columns
+    (W.MIXTRAL, 5, 8, 7, 6, 8),        # 4096 ids: one dispatch launch
+    (W.TINY_FP32, 6, 9, 8, 7, 9),      # two router launches (float32), 512 ids
+    (W.MIXTRAL.replace(name="m16k", T=16384), 6, 8, 7, 7, 8),  # 32768 ids, 256 chunks x 16 columns
     (W.DSV3_SHARED, 9, 10, 9, 10, 10), # 256 x 2048 columns: the column scan; two shared-expert GEMMs
     (W.SWITCH, 7, 8, 7, 8, 8),         # 256 x 128 columns: the column scan
 ])
 def test_launches_per_step(w, cm, tm, tm_g, f8, tm_f8):
     """route (the fused tensor-core router from weights packed beforehand, else logits +
-    selection), dispatch (histograms, column scans unless the histograms hold at most 8192 counts,
-    then slots + row copy), two GEMMs per routed and per shared expert block, combine with
+    selection), dispatch (histograms unless the batch holds at most 8192 expert ids, column scans
+    unless the histograms hold at most 8192 counts, then slots + row copy), two GEMMs per routed
+    and per shared expert block, combine with
     statistics; token-major dispatch takes count, scan, assign and scatter."""
     t = w.replace(priority=W.PRIORITY_TOKEN_MAJOR)
     assert bench.launches_per_step(w) == cm

@@ -29,6 +29,10 @@ CASES = [
     (4096, 256, 8, 0, CM, 0.5, 7168),       # 256-expert shape at its row width (14 KB rows)
     (2048, 8, 2, 640, CM, 0.0, 4096),       # Mixtral shape
     (64, 4, 2, 0, CM, 0.0, 53248),          # 104 KB rows: two do not fit one block, scatter kernel copies
+    # more than 8192 ids but small chunk histograms: the placement blocks add the histograms up
+    # themselves (no column scan), with 16-byte loads (k E = 16) and with scalar ones (k E = 10)
+    (16384, 16, 1, 1100, CM, 0.8, 64),
+    (12000, 5, 2, 2500, CM, 0.5, 64),
 ]
 
 
