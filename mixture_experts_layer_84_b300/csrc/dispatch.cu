@@ -250,8 +250,9 @@ __global__ void __launch_bounds__(256) dispatch_scatter(const uint4* __restrict_
 }
 
 // ---------------------------------------------------------------------------------------------
-// Choice-major dispatch in three launches (two or one for small histograms or batches).  Pairs are grouped into token chunks of TC tokens; with
-// every token's first choice before any second choice, the slot of pair (t, j) choosing expert e is
+// Choice-major dispatch in three launches (two or one for small histograms or batches).  Pairs are
+// grouped into token chunks of TC tokens; with every token's first choice before any second
+// choice, the slot of pair (t, j) choosing expert e is
 //   sum_{j' < j} cnt[j'][e]  +  sum_{chunks c' < c(t)} h[c'][j][e]  +  #{t' < t in t's chunk : idx[t'][j] = e},
 // cnt[j][e] being the pairs of choice j that chose e over all tokens and h[c][j][e] those of chunk c.
 //   dispatch_hist    per chunk, h[c][j][e];
